@@ -1,0 +1,131 @@
+"""Batched Soft-DTW on GB300 (sm_103a): a C-ABI CUDA library and its binding.
+
+Low level (same names as the C entry points, torch tensors for pointers):
+    sdtw_workspace_bytes, sdtw_distance, sdtw_forward, sdtw_backward,
+    sdtw_normalized, sdtw_barycenter_step, sdtw_last_device_status
+
+High level, following the usage shown in the SoftDTW-CUDA (PyTorch + Numba)
+README ("Usage", "Fused Mode", "Normalization", "Time Series Barycenters"):
+    SoftDTW(gamma=1.0, fused=False, normalize=False)(x, y) -> (B,) losses, differentiable
+    softdtw_barycenter(sequences, gamma=1.0, max_iter=100, lr=0.1, fused=True) -> (T, D)
+
+PyTorch supplies device memory and streams only; every step of the method runs
+in libsdtw.so's kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from ._lib import (FUSED, OP_BARYCENTER, OP_FWD_BWD, OP_NORMALIZED, UNFUSED, SdtwError, load,
+                   sdtw_backward, sdtw_barycenter_step, sdtw_debug_set_wait, sdtw_distance, sdtw_forward,
+                   sdtw_last_device_status, sdtw_normalized, sdtw_workspace_bytes, workspace)
+
+__all__ = [
+    "SoftDTW", "softdtw_barycenter", "SdtwError", "load", "workspace",
+    "sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
+    "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_debug_set_wait",
+    "UNFUSED", "FUSED", "OP_FWD_BWD", "OP_NORMALIZED", "OP_BARYCENTER",
+]
+
+
+def _prep(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be (B, L, D)")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t.detach().to(torch.float32).contiguous()
+
+
+class _SoftDTWFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, y, gamma, mode):
+        xc, yc = _prep(x, "x"), _prep(y, "y")
+        if xc.shape[0] != yc.shape[0] or xc.shape[2] != yc.shape[2]:
+            raise ValueError("x and y must share batch size and feature dimension")
+        B, N, D = xc.shape
+        M = yc.shape[1]
+        ws = workspace(OP_FWD_BWD, B, N, M, D, mode, xc.device)
+        loss = torch.empty(B, dtype=torch.float32, device=xc.device)
+        sdtw_forward(xc, yc, gamma, mode, loss, ws)
+        ctx.save_for_backward(xc, yc, ws)
+        ctx.gamma, ctx.mode = gamma, mode
+        ctx.dtypes = (x.dtype, y.dtype)
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad):
+        xc, yc, ws = ctx.saved_tensors
+        gx = torch.empty_like(xc) if ctx.needs_input_grad[0] else None
+        gy = torch.empty_like(yc) if ctx.needs_input_grad[1] else None
+        g = grad.detach().to(torch.float32).contiguous()
+        sdtw_backward(xc, yc, ctx.gamma, ctx.mode, g, gx, gy, ws)
+        return (None if gx is None else gx.to(ctx.dtypes[0]),
+                None if gy is None else gy.to(ctx.dtypes[1]), None, None)
+
+
+class _NormalizedFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, y, gamma, mode):
+        xc, yc = _prep(x, "x"), _prep(y, "y")
+        if xc.shape != yc.shape:
+            raise ValueError("normalized Soft-DTW requires x.shape == y.shape")
+        B, N, D = xc.shape
+        loss = torch.empty(B, dtype=torch.float32, device=xc.device)
+        ws = workspace(OP_NORMALIZED, B, N, N, D, mode, xc.device)
+        sdtw_normalized(xc, yc, gamma, mode, loss, None, None, None, ws)
+        ctx.save_for_backward(xc, yc)
+        ctx.gamma, ctx.mode = gamma, mode
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad):
+        xc, yc = ctx.saved_tensors
+        B, N, D = xc.shape
+        ws = workspace(OP_NORMALIZED, B, N, N, D, ctx.mode, xc.device)
+        gx, gy = torch.empty_like(xc), torch.empty_like(yc)
+        loss = torch.empty(B, dtype=torch.float32, device=xc.device)
+        g = grad.detach().to(torch.float32).contiguous()
+        sdtw_normalized(xc, yc, ctx.gamma, ctx.mode, loss, g, gx, gy, ws)
+        return gx, gy, None, None
+
+
+class SoftDTW:
+    """Per-pair Soft-DTW losses (B,), differentiable w.r.t. x and y.
+
+    fused=False stores the (B,N,M) cost tensor; fused=True recomputes it inside
+    the DP kernels. normalize=True gives s(x,y) - (s(x,x) + s(y,y))/2 and needs
+    x.shape == y.shape.
+    """
+
+    def __init__(self, gamma: float = 1.0, dist: str = "sqeuclidean", fused: bool = False,
+                 normalize: bool = False):
+        if dist != "sqeuclidean":
+            raise ValueError("only dist='sqeuclidean' is supported")
+        if not (gamma > 0):
+            raise ValueError("gamma must be > 0")
+        self.gamma = float(gamma)
+        self.mode = FUSED if fused else UNFUSED
+        self.normalize = normalize
+
+    def __call__(self, x: torch.Tensor, y: torch.Tensor) -> torch.Tensor:
+        fn = _NormalizedFn if self.normalize else _SoftDTWFn
+        return fn.apply(x, y, self.gamma, self.mode)
+
+
+def softdtw_barycenter(sequences: torch.Tensor, gamma: float = 1.0, max_iter: int = 100, lr: float = 0.1,
+                       fused: bool = True, init: torch.Tensor | None = None, beta1: float = 0.9,
+                       beta2: float = 0.999, eps: float = 1e-8, return_losses: bool = False):
+    """Soft-DTW barycenter of K sequences (K,T,D) by Adam, initialised to their
+    mean (or `init`). Runs `max_iter` calls of sdtw_barycenter_step."""
+    X = _prep(sequences, "sequences")
+    K, T2, D = X.shape
+    z = (X.mean(dim=0) if init is None else init.detach().to(torch.float32)).contiguous().clone()
+    T = z.shape[0]
+    m = torch.zeros_like(z)
+    v = torch.zeros_like(z)
+    mode = FUSED if fused else UNFUSED
+    ws = workspace(OP_BARYCENTER, K, T, T2, D, mode, X.device)
+    losses = torch.empty(max_iter, dtype=torch.float32, device=X.device)
+    for t in range(1, max_iter + 1):
+        sdtw_barycenter_step(z, m, v, t, X, gamma, lr, beta1, beta2, eps, mode, losses[t - 1:t], ws)
+    return (z, losses) if return_losses else z

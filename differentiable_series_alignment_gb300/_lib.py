@@ -1,0 +1,171 @@
+"""ctypes binding of libsdtw.so: argument marshalling only.
+
+Every function here has the name of the C entry point it wraps and takes torch
+CUDA tensors (fp32, contiguous) in place of device pointers. No arithmetic of
+the method happens in Python: a missing library raises, there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsdtw.so")
+
+UNFUSED, FUSED = 0, 1
+OP_FWD_BWD, OP_NORMALIZED, OP_BARYCENTER = 0, 1, 2
+
+STATUS_NAMES = {
+    0: "SDTW_OK", 1: "SDTW_ERR_ARG", 2: "SDTW_ERR_GAMMA", 3: "SDTW_ERR_EMPTY", 4: "SDTW_ERR_SHAPE",
+    5: "SDTW_ERR_WORKSPACE", 6: "SDTW_ERR_CUDA", 7: "SDTW_ERR_TIMEOUT", 8: "SDTW_ERR_TOO_LARGE",
+}
+
+# Every symbol include/sdtw.h declares.
+EXPORTS = ("sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
+           "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_status_string", "sdtw_debug_set_wait")
+
+
+class SdtwError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({status_string(code)})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libsdtw.so (built in-tree); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with `python -m differentiable_series_alignment_gb300.build`")
+        lib = ctypes.CDLL(path)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.sdtw_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.sdtw_workspace_bytes.restype = sz
+        lib.sdtw_distance.argtypes = [vp, vp, i, i, i, i, vp, vp]
+        lib.sdtw_distance.restype = i
+        lib.sdtw_forward.argtypes = [vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
+        lib.sdtw_forward.restype = i
+        lib.sdtw_backward.argtypes = [vp, vp, i, i, i, i, f, i, vp, vp, vp, vp, sz, vp]
+        lib.sdtw_backward.restype = i
+        lib.sdtw_normalized.argtypes = [vp, vp, i, i, i, f, i, vp, vp, vp, vp, vp, sz, vp]
+        lib.sdtw_normalized.restype = i
+        lib.sdtw_barycenter_step.argtypes = [vp, vp, vp, i, vp, i, i, i, i, f, f, f, f, f, i, vp, vp, sz, vp]
+        lib.sdtw_barycenter_step.restype = i
+        lib.sdtw_last_device_status.argtypes = [vp, vp]
+        lib.sdtw_last_device_status.restype = i
+        lib.sdtw_status_string.argtypes = [i]
+        lib.sdtw_status_string.restype = ctypes.c_char_p
+        lib.sdtw_debug_set_wait.argtypes = [ctypes.c_double, i]
+        lib.sdtw_debug_set_wait.restype = None
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().sdtw_status_string(int(code)).decode()
+    except Exception:
+        return "?"
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _f32(t, name):
+    if t is not None and t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32")
+    return _ptr(t)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise SdtwError(code, where)
+
+
+def _mode(mode) -> int:
+    if isinstance(mode, str):
+        return {"unfused": UNFUSED, "fused": FUSED}[mode]
+    return int(mode)
+
+
+def sdtw_workspace_bytes(op: int, B: int, N: int, M: int, D: int, mode) -> int:
+    return int(load().sdtw_workspace_bytes(int(op), B, N, M, D, _mode(mode)))
+
+
+def workspace(op: int, B: int, N: int, M: int, D: int, mode, device=None) -> torch.Tensor:
+    """A uint8 device tensor of the size sdtw_workspace_bytes asks for (caching allocator: 512-B aligned)."""
+    n = sdtw_workspace_bytes(op, B, N, M, D, mode)
+    if n == 0:
+        raise SdtwError(1, "sdtw_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def sdtw_distance(x, y, C, stream=None):
+    B, N, D = x.shape
+    M = y.shape[1]
+    _check(load().sdtw_distance(_f32(x, "x"), _f32(y, "y"), B, N, M, D, _f32(C, "C"), _stream(stream)),
+           "sdtw_distance")
+
+
+def sdtw_forward(x, y, gamma, mode, loss, ws, stream=None):
+    B, N, D = x.shape
+    M = y.shape[1]
+    _check(load().sdtw_forward(_f32(x, "x"), _f32(y, "y"), B, N, M, D, float(gamma), _mode(mode),
+                               _f32(loss, "loss"), _ptr(ws), ws.numel(), _stream(stream)), "sdtw_forward")
+
+
+def sdtw_backward(x, y, gamma, mode, grad_loss, grad_x, grad_y, ws, stream=None):
+    B, N, D = x.shape
+    M = y.shape[1]
+    _check(load().sdtw_backward(_f32(x, "x"), _f32(y, "y"), B, N, M, D, float(gamma), _mode(mode),
+                                _f32(grad_loss, "grad_loss"), _f32(grad_x, "grad_x"), _f32(grad_y, "grad_y"),
+                                _ptr(ws), ws.numel(), _stream(stream)), "sdtw_backward")
+
+
+def sdtw_normalized(x, y, gamma, mode, loss, grad_loss, grad_x, grad_y, ws, stream=None):
+    B, N, D = x.shape
+    _check(load().sdtw_normalized(_f32(x, "x"), _f32(y, "y"), B, N, D, float(gamma), _mode(mode),
+                                  _f32(loss, "loss"), _f32(grad_loss, "grad_loss"), _f32(grad_x, "grad_x"),
+                                  _f32(grad_y, "grad_y"), _ptr(ws), ws.numel(), _stream(stream)),
+           "sdtw_normalized")
+
+
+def sdtw_barycenter_step(z, m, v, t, X, gamma, lr, beta1, beta2, eps, mode, loss_out, ws, stream=None):
+    T, D = z.shape
+    K, T2, _ = X.shape
+    _check(load().sdtw_barycenter_step(_f32(z, "z"), _f32(m, "m"), _f32(v, "v"), int(t), _f32(X, "X"), K, T, T2,
+                                       D, float(gamma), float(lr), float(beta1), float(beta2), float(eps),
+                                       _mode(mode), _f32(loss_out, "loss_out"), _ptr(ws), ws.numel(),
+                                       _stream(stream)), "sdtw_barycenter_step")
+
+
+def sdtw_last_device_status(ws, stream=None) -> int:
+    return int(load().sdtw_last_device_status(_ptr(ws), _stream(stream)))
+
+
+def sdtw_debug_set_wait(seconds: float, skip_publish: bool = False):
+    load().sdtw_debug_set_wait(float(seconds), 1 if skip_publish else 0)

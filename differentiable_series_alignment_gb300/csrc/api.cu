@@ -1,0 +1,376 @@
+// api.cu -- the C ABI of libsdtw.so: validation, workspace carving, launches.
+//
+// Each entry point validates its arguments on the host (returning before any
+// launch on error), carves the caller's workspace, and enqueues its kernels on
+// the caller's stream. Nothing is allocated here.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "../../include/sdtw.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace sdtw;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+
+unsigned long long g_wait_ns = kDefaultWaitNs;
+int g_skip_publish = 0;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+// Workspace layout. The status word sits at offset 0 for every op.
+struct Layout {
+    size_t status, ctrl_f, ctrl_f_bytes, ctrl_b, ctrl_b_bytes;
+    size_t colsum, rowsum, losses, edge_f, edge_b, vh, e, dsk, gparts, total;
+    int P, N, M, D, NB;
+};
+
+bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
+{
+    if (op < SDTW_OP_FWD_BWD || op > SDTW_OP_BARYCENTER) return false;
+    if (B < 1 || N < 1 || M < 1 || D < 1) return false;
+    if (mode != SDTW_UNFUSED && mode != SDTW_FUSED) return false;
+    const int P = (op == SDTW_OP_NORMALIZED) ? 3 * B : B;
+    if (op == SDTW_OP_NORMALIZED) M = N;
+    const int NB = (N + 31) / 32;
+    const size_t slots = (size_t)skew_slots(N, M) * P;
+    size_t o = 0;
+    L->status = o; o = align_up(o + sizeof(int));
+    L->ctrl_f = o; L->ctrl_f_bytes = sizeof(int) * (1 + (size_t)P + (size_t)P * NB); o = align_up(o + L->ctrl_f_bytes);
+    L->ctrl_b = o; L->ctrl_b_bytes = sizeof(int) * (1 + (size_t)P * NB); o = align_up(o + L->ctrl_b_bytes);
+    L->colsum = o; o = align_up(o + sizeof(double) * (size_t)P * NB);
+    L->rowsum = o; o = align_up(o + sizeof(double) * (size_t)P);
+    L->losses = o; o = align_up(o + sizeof(float) * (size_t)P);
+    L->edge_f = o; o = align_up(o + sizeof(float) * (size_t)P * NB * M);
+    L->edge_b = o; o = align_up(o + sizeof(float2) * (size_t)P * NB * M);
+    L->vh = o; o = align_up(o + sizeof(float2) * slots);
+    L->e = o; o = align_up(o + sizeof(float) * slots);
+    L->dsk = o; if (mode == SDTW_UNFUSED) o = align_up(o + sizeof(float) * slots);
+    L->gparts = o; if (op == SDTW_OP_BARYCENTER) o = align_up(o + sizeof(float) * (size_t)P * N * D);
+    L->total = o;
+    L->P = P; L->N = N; L->M = M; L->D = D; L->NB = NB;
+    return true;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+int env_int(const char* name, int dflt)
+{
+    const char* s = std::getenv(name);
+    if (!s || !*s) return dflt;
+    return std::atoi(s);
+}
+
+// Warps per wavefront CTA: about one 32-row block per SM partition over the
+// whole batch, bounded by the shared memory a fused CTA needs.
+int choose_warps(int P, int NB, int D, bool fused, bool backward, int num_sms)
+{
+    int W = env_int(backward ? "SDTW_WARPS_BWD" : "SDTW_WARPS_FWD", 0);
+    if (W <= 0) {
+        const long long blocks = (long long)P * NB;
+        W = (int)((blocks + num_sms - 1) / num_sms);
+    }
+    if (W > NB) W = NB;
+    if (W > kMaxWarps) W = kMaxWarps;
+    if (W < 1) W = 1;
+    if (fused) {
+        const size_t limit = 220 * 1024;
+        while (W > 1 && wave_smem_fixed(W, false) + (size_t)W * wave_smem_fused_per_warp(D) > limit) --W;
+    }
+    return W;
+}
+
+int num_sms()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        n = v;
+    }
+    return n;
+}
+
+sdtw_status check_common(const void* x, const void* y, int B, int N, int M, int D, float gamma, int mode)
+{
+    if (B < 1 || N < 1 || M < 1 || D < 1) return SDTW_ERR_EMPTY;
+    if (!(gamma > 0.f) || !std::isfinite(gamma)) return SDTW_ERR_GAMMA;
+    if (mode != SDTW_UNFUSED && mode != SDTW_FUSED) return SDTW_ERR_ARG;
+    if (!x || !y) return SDTW_ERR_ARG;
+    if (B > 65535 / 3 || N > (1 << 24) || M > (1 << 24) || D > 400) return SDTW_ERR_TOO_LARGE;
+    if (mode == SDTW_FUSED && wave_smem_fixed(1, false) + wave_smem_fused_per_warp(D) > 220 * 1024)
+        return SDTW_ERR_TOO_LARGE;
+    return SDTW_OK;
+}
+
+sdtw_status check_ws(void* ws, size_t ws_bytes, const Layout& L)
+{
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return SDTW_ERR_WORKSPACE;
+    if (ws_bytes < L.total) return SDTW_ERR_WORKSPACE;
+    return SDTW_OK;
+}
+
+WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamma, bool fused, bool backward)
+{
+    WaveParams q{};
+    q.pr = pr;
+    q.P = L.P; q.N = L.N; q.M = L.M; q.D = L.D; q.NB = L.NB;
+    q.W = choose_warps(L.P, L.NB, L.D, fused && !backward, backward, num_sms());
+    q.S = (L.NB + q.W - 1) / q.W;
+    q.scale = (float)(1.4426950408889634 / (double)gamma);
+    q.unscale = (float)((double)gamma * 0.6931471805599453);
+    q.Dsk = fused ? nullptr : at<float>(ws, L.dsk);
+    q.VH = at<float2>(ws, L.vh);
+    q.E = at<float>(ws, L.e);
+    q.edge_f = at<float>(ws, L.edge_f);
+    q.edge_b = at<float2>(ws, L.edge_b);
+    int* cf = at<int>(ws, L.ctrl_f);
+    q.ticket_f = cf;
+    q.done = cf + 1;
+    q.prog_f = cf + 1 + L.P;
+    int* cb = at<int>(ws, L.ctrl_b);
+    q.ticket_b = cb;
+    q.prog_b = cb + 1;
+    q.colsum = at<double>(ws, L.colsum);
+    q.rowsum = at<double>(ws, L.rowsum);
+    q.loss = at<float>(ws, L.losses);
+    q.status = at<int>(ws, L.status);
+    q.wait_ns = g_wait_ns;
+    q.skip_publish = 0;
+    return q;
+}
+
+#define SDTW_CUDA(call)                                  \
+    do {                                                 \
+        cudaError_t e_ = (call);                         \
+        if (e_ != cudaSuccess) return SDTW_ERR_CUDA;     \
+    } while (0)
+
+// Forward over L.P problems; per-problem losses to `loss_out` (device).
+sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gamma, int mode, float* loss_out,
+                        cudaStream_t st)
+{
+    const bool fused = (mode == SDTW_FUSED);
+    SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.status), 0, sizeof(int), st));
+    SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_f), 0, L.ctrl_f_bytes, st));
+    if (!fused) SDTW_CUDA(launch_dist_skewed(pr, L.P, L.N, L.M, L.D, at<float>(ws, L.dsk), st));
+    WaveParams q = wave_params(pr, L, ws, gamma, fused, false);
+    q.loss = loss_out;
+    q.skip_publish = g_skip_publish;
+    g_skip_publish = 0;
+    SDTW_CUDA(launch_forward(q, fused, st));
+    return SDTW_OK;
+}
+
+sdtw_status run_backward(const Problems& pr, const Layout& L, void* ws, float gamma, int mode, cudaStream_t st)
+{
+    SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_b), 0, L.ctrl_b_bytes, st));
+    WaveParams q = wave_params(pr, L, ws, gamma, mode == SDTW_FUSED, true);
+    SDTW_CUDA(launch_backward(q, st));
+    return SDTW_OK;
+}
+
+// Gradient contractions of the problems of one set (B problems starting at set*B).
+sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void* ws, const float* grad_loss,
+                      float coef, float* out_x, float* out_y, int accumulate, cudaStream_t st)
+{
+    GradParams g{};
+    g.pr = all;
+    g.pr.xs[0] = all.xs[set]; g.pr.ys[0] = all.ys[set];
+    g.pr.xstride[0] = all.xstride[set]; g.pr.ystride[0] = all.ystride[set];
+    g.pr.B = B;
+    g.P = B; g.N = L.N; g.M = L.M; g.D = L.D;
+    g.E = at<float>(ws, L.e) + (size_t)set * B * skew_slots(L.N, L.M);
+    g.grad_loss = grad_loss;
+    g.wmod = B;
+    g.coef = coef;
+    g.omod = B;
+    g.accumulate = accumulate;
+    if (out_x) {
+        g.out = out_x;
+        g.out_stride = (long long)L.N * L.D;
+        SDTW_CUDA(launch_grad_rows(g, st));
+    }
+    if (out_y) {
+        g.out = out_y;
+        g.out_stride = (long long)L.M * L.D;
+        SDTW_CUDA(launch_grad_cols(g, st));
+    }
+    return SDTW_OK;
+}
+
+__global__ void combine_normalized_kernel(const float* l, int B, float* loss)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B) loss[b] = l[b] - 0.5f * (l[B + b] + l[2 * B + b]);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sdtw_workspace_bytes(int op, int B, int N, int M, int D, sdtw_mode mode)
+{
+    Layout L;
+    if (!make_layout(op, B, N, M, D, (int)mode, &L)) return 0;
+    return L.total;
+}
+
+sdtw_status sdtw_distance(const float* x, const float* y, int B, int N, int M, int D, float* C, void* stream)
+{
+    sdtw_status s = check_common(x, y, B, N, M, D, 1.f, SDTW_UNFUSED);
+    if (s != SDTW_OK) return s;
+    if (!C) return SDTW_ERR_ARG;
+    Problems pr{};
+    pr.xs[0] = x; pr.ys[0] = y;
+    pr.xstride[0] = (long long)N * D; pr.ystride[0] = (long long)M * D;
+    pr.B = B;
+    SDTW_CUDA(launch_dist_rowmajor(pr, B, N, M, D, C, static_cast<cudaStream_t>(stream)));
+    return SDTW_OK;
+}
+
+sdtw_status sdtw_forward(const float* x, const float* y, int B, int N, int M, int D, float gamma, sdtw_mode mode,
+                         float* loss, void* ws, size_t ws_bytes, void* stream)
+{
+    sdtw_status s = check_common(x, y, B, N, M, D, gamma, (int)mode);
+    if (s != SDTW_OK) return s;
+    if (!loss) return SDTW_ERR_ARG;
+    Layout L;
+    make_layout(SDTW_OP_FWD_BWD, B, N, M, D, (int)mode, &L);
+    if ((s = check_ws(ws, ws_bytes, L)) != SDTW_OK) return s;
+    Problems pr{};
+    pr.xs[0] = x; pr.ys[0] = y;
+    pr.xstride[0] = (long long)N * D; pr.ystride[0] = (long long)M * D;
+    pr.B = B;
+    return run_forward(pr, L, ws, gamma, (int)mode, loss, static_cast<cudaStream_t>(stream));
+}
+
+sdtw_status sdtw_backward(const float* x, const float* y, int B, int N, int M, int D, float gamma, sdtw_mode mode,
+                          const float* grad_loss, float* grad_x, float* grad_y, void* ws, size_t ws_bytes,
+                          void* stream)
+{
+    sdtw_status s = check_common(x, y, B, N, M, D, gamma, (int)mode);
+    if (s != SDTW_OK) return s;
+    if (!grad_loss) return SDTW_ERR_ARG;
+    Layout L;
+    make_layout(SDTW_OP_FWD_BWD, B, N, M, D, (int)mode, &L);
+    if ((s = check_ws(ws, ws_bytes, L)) != SDTW_OK) return s;
+    Problems pr{};
+    pr.xs[0] = x; pr.ys[0] = y;
+    pr.xstride[0] = (long long)N * D; pr.ystride[0] = (long long)M * D;
+    pr.B = B;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((s = run_backward(pr, L, ws, gamma, (int)mode, st)) != SDTW_OK) return s;
+    if (grad_x || grad_y) return run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, st);
+    return SDTW_OK;
+}
+
+sdtw_status sdtw_normalized(const float* x, const float* y, int B, int N, int D, float gamma, sdtw_mode mode,
+                            float* loss, const float* grad_loss, float* grad_x, float* grad_y, void* ws,
+                            size_t ws_bytes, void* stream)
+{
+    sdtw_status s = check_common(x, y, B, N, N, D, gamma, (int)mode);
+    if (s != SDTW_OK) return s;
+    if (!loss) return SDTW_ERR_ARG;
+    Layout L;
+    make_layout(SDTW_OP_NORMALIZED, B, N, N, D, (int)mode, &L);
+    if ((s = check_ws(ws, ws_bytes, L)) != SDTW_OK) return s;
+    const long long st_ = (long long)N * D;
+    Problems pr{};
+    pr.xs[0] = x; pr.ys[0] = y;   // s(x, y)
+    pr.xs[1] = x; pr.ys[1] = x;   // s(x, x)
+    pr.xs[2] = y; pr.ys[2] = y;   // s(y, y)
+    for (int k = 0; k < 3; ++k) { pr.xstride[k] = st_; pr.ystride[k] = st_; }
+    pr.B = B;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float* l3 = at<float>(ws, L.losses);
+    if ((s = run_forward(pr, L, ws, gamma, (int)mode, l3, st)) != SDTW_OK) return s;
+    combine_normalized_kernel<<<(B + 255) / 256, 256, 0, st>>>(l3, B, loss);
+    SDTW_CUDA(cudaGetLastError());
+    if (!grad_loss || (!grad_x && !grad_y)) return SDTW_OK;
+    if ((s = run_backward(pr, L, ws, gamma, (int)mode, st)) != SDTW_OK) return s;
+    // grad_x = g [gx(x,y) - (gx(x,x) + gy(x,x))/2];  grad_y = g [gy(x,y) - (gx(y,y) + gy(y,y))/2]
+    if ((s = run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, st)) != SDTW_OK) return s;
+    if (grad_x) {
+        if ((s = run_grads(pr, 1, B, L, ws, grad_loss, -0.5f, grad_x, grad_x, 1, st)) != SDTW_OK) return s;
+    }
+    if (grad_y) {
+        if ((s = run_grads(pr, 2, B, L, ws, grad_loss, -0.5f, grad_y, grad_y, 1, st)) != SDTW_OK) return s;
+    }
+    return SDTW_OK;
+}
+
+sdtw_status sdtw_barycenter_step(float* z, float* m, float* v, int t, const float* X, int K, int T, int T2, int D,
+                                 float gamma, float lr, float beta1, float beta2, float eps, sdtw_mode mode,
+                                 float* loss_out, void* ws, size_t ws_bytes, void* stream)
+{
+    sdtw_status s = check_common(z, X, K, T, T2, D, gamma, (int)mode);
+    if (s != SDTW_OK) return s;
+    if (!m || !v || t < 1 || !(lr >= 0.f) || !(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f) ||
+        !(eps >= 0.f))
+        return SDTW_ERR_ARG;
+    Layout L;
+    make_layout(SDTW_OP_BARYCENTER, K, T, T2, D, (int)mode, &L);
+    if ((s = check_ws(ws, ws_bytes, L)) != SDTW_OK) return s;
+    Problems pr{};
+    pr.xs[0] = z; pr.ys[0] = X;
+    pr.xstride[0] = 0;                      // z broadcast against every sequence
+    pr.ystride[0] = (long long)T2 * D;
+    pr.B = K;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float* losses = at<float>(ws, L.losses);
+    if ((s = run_forward(pr, L, ws, gamma, (int)mode, losses, st)) != SDTW_OK) return s;
+    if ((s = run_backward(pr, L, ws, gamma, (int)mode, st)) != SDTW_OK) return s;
+    float* gparts = at<float>(ws, L.gparts);
+    if ((s = run_grads(pr, 0, K, L, ws, nullptr, 1.f / (float)K, gparts, nullptr, 0, st)) != SDTW_OK) return s;
+    const double bc1 = 1.0 - std::pow((double)beta1, (double)t);
+    const double bc2 = 1.0 - std::pow((double)beta2, (double)t);
+    SDTW_CUDA(launch_adam(z, m, v, gparts, K, T * D, lr, beta1, beta2, eps, (float)bc1, (float)bc2, losses, loss_out,
+                          st));
+    return SDTW_OK;
+}
+
+sdtw_status sdtw_last_device_status(void* ws, void* stream)
+{
+    if (!ws) return SDTW_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SDTW_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SDTW_ERR_CUDA;
+    if (h == 0) return SDTW_OK;
+    if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return SDTW_ERR_CUDA;
+    return SDTW_ERR_TIMEOUT;
+}
+
+const char* sdtw_status_string(sdtw_status s)
+{
+    switch (s) {
+        case SDTW_OK: return "ok";
+        case SDTW_ERR_ARG: return "invalid argument";
+        case SDTW_ERR_GAMMA: return "gamma must be finite and > 0";
+        case SDTW_ERR_EMPTY: return "empty input (B, N, M and D must be >= 1)";
+        case SDTW_ERR_SHAPE: return "shape mismatch";
+        case SDTW_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case SDTW_ERR_CUDA: return "CUDA runtime or launch error";
+        case SDTW_ERR_TIMEOUT: return "device-side wait timed out";
+        case SDTW_ERR_TOO_LARGE: return "sizes exceed the library's limits";
+    }
+    return "unknown status";
+}
+
+void sdtw_debug_set_wait(double seconds, int skip_publish)
+{
+    g_wait_ns = (seconds > 0.0) ? (unsigned long long)(seconds * 1e9) : kDefaultWaitNs;
+    g_skip_publish = skip_publish ? 1 : 0;
+}
+
+}  // extern "C"

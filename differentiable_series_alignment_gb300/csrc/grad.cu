@@ -1,0 +1,189 @@
+// grad.cu -- input gradients from the alignment matrix, and the barycenter Adam step.
+//
+// Chain rule through the squared Euclidean cost C[i,j] = |x_i - y_j|^2:
+//   dL/dx_i = g * 2 * sum_j E[i,j] (x_i - y_j) = g * 2 * (rowsum_i(E) x_i - (E y)_i)
+//   dL/dy_j = g * 2 * sum_i E[i,j] (y_j - x_i) = g * 2 * (colsum_j(E) y_j - (E^T x)_j)
+// E arrives in the skewed layout of the wavefront; each CTA un-skews 32x32
+// tiles into shared memory and contracts them with the matching x or y rows.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sdtw {
+
+namespace {
+
+constexpr int kKC = 64;   // k-slice per CTA (16 per warp)
+constexpr int kYS = kKC + 4;
+
+// Un-skew the 32x32 tile (rows of block rb, columns c0..c0+31) into es.
+// ROW_MAJOR: es[r*32 + c]; otherwise es[c*32 + r]. Entries outside the matrix are 0.
+template <bool ROW_MAJOR>
+__device__ __forceinline__ void load_tile(const float* __restrict__ Esk, int N, int M, int p, int rb, int c0,
+                                          float* es)
+{
+    const float* base = Esk + skew_index(N, M, p, rb, 0, 0);
+    for (int idx = threadIdx.x; idx < 63 * 32; idx += blockDim.x) {
+        const int tt = idx >> 5, rr = idx & 31;
+        const int c = tt - rr;
+        if (c < 0 || c >= 32) continue;
+        const bool ok = (c0 + c < M) && (rb * 32 + rr < N);
+        const float v = ok ? base[(long long)(c0 + tt) * 32 + rr] : 0.f;
+        if (ROW_MAJOR) es[rr * 32 + c] = v;
+        else es[c * 32 + rr] = v;
+    }
+}
+
+// grid (NB, P, ceil(D/64)), block 128.
+__global__ void __launch_bounds__(128) grad_rows_kernel(const GradParams g)
+{
+    __shared__ float es[32 * 32];
+    __shared__ __align__(16) float ys[32 * kYS];
+    const int rb = blockIdx.x, p = blockIdx.y, kb = blockIdx.z * kKC;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = g.N, M = g.M, D = g.D;
+    const float* yb = g.pr.y(p);
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    float rs = 0.f;
+    for (int c0 = 0; c0 < M; c0 += 32) {
+        load_tile<false>(g.E, N, M, p, rb, c0, es);
+        for (int idx = threadIdx.x; idx < 32 * kKC; idx += blockDim.x) {
+            const int c = idx / kKC, kk = idx - c * kKC;
+            ys[c * kYS + kk] = (c0 + c < M && kb + kk < D) ? yb[(size_t)(c0 + c) * D + kb + kk] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int c = 0; c < 32; ++c) {
+            const float e = es[c * 32 + lane];
+            rs += e;
+            const float4* yv = reinterpret_cast<const float4*>(ys + c * kYS + warp * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 w = yv[q];
+                acc[4 * q + 0] = fmaf(e, w.x, acc[4 * q + 0]);
+                acc[4 * q + 1] = fmaf(e, w.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(e, w.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(e, w.w, acc[4 * q + 3]);
+            }
+        }
+        __syncthreads();
+    }
+    const int i = rb * 32 + lane;
+    if (i >= N) return;
+    const float w = g.coef * 2.f * (g.grad_loss ? g.grad_loss[p % g.wmod] : 1.f);
+    const float* xi = g.pr.x(p) + (size_t)i * D;
+    float* out = g.out + (long long)(p % g.omod) * g.out_stride + (size_t)i * D;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int kk = kb + warp * 16 + k;
+        if (kk < D) {
+            const float val = w * (rs * xi[kk] - acc[k]);
+            out[kk] = g.accumulate ? out[kk] + val : val;
+        }
+    }
+}
+
+// grid (ceil(M/32), P, ceil(D/64)), block 128.
+__global__ void __launch_bounds__(128) grad_cols_kernel(const GradParams g)
+{
+    __shared__ float es[32 * 32];
+    __shared__ __align__(16) float xs[32 * kYS];
+    const int c0 = blockIdx.x * 32, p = blockIdx.y, kb = blockIdx.z * kKC;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = g.N, M = g.M, D = g.D;
+    const float* xb = g.pr.x(p);
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    float cs = 0.f;
+    const int NB = (N + 31) / 32;
+    for (int rb = 0; rb < NB; ++rb) {
+        load_tile<true>(g.E, N, M, p, rb, c0, es);
+        for (int idx = threadIdx.x; idx < 32 * kKC; idx += blockDim.x) {
+            const int r = idx / kKC, kk = idx - r * kKC;
+            const int i = rb * 32 + r;
+            xs[r * kYS + kk] = (i < N && kb + kk < D) ? xb[(size_t)i * D + kb + kk] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int r = 0; r < 32; ++r) {
+            const float e = es[r * 32 + lane];
+            cs += e;
+            const float4* xv = reinterpret_cast<const float4*>(xs + r * kYS + warp * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 w = xv[q];
+                acc[4 * q + 0] = fmaf(e, w.x, acc[4 * q + 0]);
+                acc[4 * q + 1] = fmaf(e, w.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(e, w.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(e, w.w, acc[4 * q + 3]);
+            }
+        }
+        __syncthreads();
+    }
+    const int j = c0 + lane;
+    if (j >= M) return;
+    const float w = g.coef * 2.f * (g.grad_loss ? g.grad_loss[p % g.wmod] : 1.f);
+    const float* yj = g.pr.y(p) + (size_t)j * D;
+    float* out = g.out + (long long)(p % g.omod) * g.out_stride + (size_t)j * D;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int kk = kb + warp * 16 + k;
+        if (kk < D) {
+            const float val = w * (cs * yj[kk] - acc[k]);
+            out[kk] = g.accumulate ? out[kk] + val : val;
+        }
+    }
+}
+
+// Barycenter: g = sum_k gparts[k] (each part already carries its 1/K), then Adam.
+__global__ void adam_kernel(float* __restrict__ z, float* __restrict__ m, float* __restrict__ v,
+                            const float* __restrict__ gparts, int K, int n, float lr, float b1, float b2,
+                            float eps, float bc1, float bc2, const float* __restrict__ losses,
+                            float* __restrict__ loss_out)
+{
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e == 0 && loss_out) {
+        double s = 0.0;
+        for (int k = 0; k < K; ++k) s += losses[k];
+        *loss_out = (float)(s / K);
+    }
+    if (e >= n) return;
+    float gsum = 0.f;
+    for (int k = 0; k < K; ++k) gsum += gparts[(size_t)k * n + e];
+    const float mm = b1 * m[e] + (1.f - b1) * gsum;
+    const float vv = b2 * v[e] + (1.f - b2) * gsum * gsum;
+    m[e] = mm;
+    v[e] = vv;
+    z[e] -= lr * (mm / bc1) / (sqrtf(vv / bc2) + eps);
+}
+
+}  // namespace
+
+cudaError_t launch_grad_rows(const GradParams& g, cudaStream_t st)
+{
+    dim3 grid((g.N + 31) / 32, g.P, (g.D + kKC - 1) / kKC);
+    grad_rows_kernel<<<grid, 128, 0, st>>>(g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grad_cols(const GradParams& g, cudaStream_t st)
+{
+    dim3 grid((g.M + 31) / 32, g.P, (g.D + kKC - 1) / kKC);
+    grad_cols_kernel<<<grid, 128, 0, st>>>(g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adam(float* z, float* m, float* v, const float* gparts, int K, int n, float lr,
+                        float beta1, float beta2, float eps, float bc1, float bc2, const float* losses,
+                        float* loss_out, cudaStream_t st)
+{
+    const int threads = 256;
+    const int blocks = (n + threads - 1) / threads;
+    adam_kernel<<<blocks > 0 ? blocks : 1, threads, 0, st>>>(z, m, v, gparts, K, n, lr, beta1, beta2, eps, bc1,
+                                                             bc2, losses, loss_out);
+    return cudaGetLastError();
+}
+
+}  // namespace sdtw

@@ -1,0 +1,77 @@
+// kernels.h -- host-side declarations of the library's kernel launchers.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace sdtw {
+
+// Parameters of the two wavefront kernels. All pointers are device pointers
+// into the caller's tensors or the caller's workspace.
+struct WaveParams {
+    Problems pr;
+    int P;            // problems in the batch
+    int N, M, D;
+    int NB;           // 32-row blocks per problem, ceil(N/32)
+    int S;            // strips (CTAs) per problem, ceil(N / (32 W))
+    int W;            // warps per CTA
+    int smem_fixed;   // bytes of dynamic shared memory before the fused buffers
+    float scale;      // log2(e) / gamma
+    float unscale;    // gamma * ln(2)
+    const float* Dsk; // unfused: raw cost, skewed layout; fused: nullptr
+    float2* VH;       // (vl, hu) per cell, skewed layout
+    float* E;         // alignment matrix, skewed layout (backward output)
+    float* edge_f;    // [P][NB][M]  boundary rows between forward strips
+    float2* edge_b;   // [P][NB][M]  boundary messages between backward strips
+    int* prog_f;      // [P][NB]     forward ready counters
+    int* prog_b;      // [P][NB]     backward ready counters
+    int* ticket_f;    // forward strip ticket
+    int* ticket_b;    // backward strip ticket
+    int* done;        // [P]         finished forward strips
+    double* colsum;   // [P][NB]
+    double* rowsum;   // [P]
+    float* loss;      // [P]
+    int* status;      // device status word
+    unsigned long long wait_ns;
+    int skip_publish; // test hook: strip 0 withholds its forward ready counter
+};
+
+size_t wave_smem_fixed(int W, bool backward);
+size_t wave_smem_fused_per_warp(int D);
+cudaError_t launch_forward(WaveParams q, bool fused, cudaStream_t st);
+cudaError_t launch_backward(WaveParams q, cudaStream_t st);
+
+// Unfused cost: raw squared Euclidean distances into the skewed layout.
+cudaError_t launch_dist_skewed(const Problems& pr, int P, int N, int M, int D, float* Dsk,
+                               cudaStream_t st);
+// Cost matrix (P,N,M) row-major.
+cudaError_t launch_dist_rowmajor(const Problems& pr, int P, int N, int M, int D, float* C,
+                                 cudaStream_t st);
+
+// Gradient contractions from the skewed alignment matrix.
+//   row part, for each problem p and row i:
+//     out_x[p][i,:] (+)= coef * w[p] * 2 * (sum_j E[i,j] x_i - sum_j E[i,j] y_j)
+//   column part, for each problem p and column j:
+//     out_y[p][j,:] (+)= coef * w[p] * 2 * (sum_i E[i,j] y_j - sum_i E[i,j] x_i)
+// w[p] = grad_loss[p % wmod] (1 when grad_loss is NULL). out + (p % omod) * stride.
+struct GradParams {
+    Problems pr;
+    int P, N, M, D;
+    const float* E;
+    const float* grad_loss;
+    int wmod;
+    float coef;
+    float* out;
+    long long out_stride;
+    int omod;
+    int accumulate;
+};
+cudaError_t launch_grad_rows(const GradParams& g, cudaStream_t st);
+cudaError_t launch_grad_cols(const GradParams& g, cudaStream_t st);
+
+// Barycenter: grad = (1/K) sum_k gparts[k]; Adam update of z, m, v; mean loss.
+cudaError_t launch_adam(float* z, float* m, float* v, const float* gparts, int K, int n,
+                        float lr, float beta1, float beta2, float eps, float bc1, float bc2,
+                        const float* losses, float* loss_out, cudaStream_t st);
+
+}  // namespace sdtw

@@ -1,0 +1,124 @@
+/*
+ * sdtw.h -- C ABI of the GB300 (sm_103a) batched Soft-DTW library (libsdtw.so).
+ *
+ * The operation is Soft-DTW of Cuturi & Blondel (ICML 2017), the method named
+ * in the "Acknowledgments" of the SoftDTW-CUDA (PyTorch + Numba) README, with
+ * the squared Euclidean cost and the log-space backward of the SoftDTW-CUDA-Torch
+ * paper (abstract, contributions (1)-(3)):
+ *
+ *   C[b,i,j] = sum_k (x[b,i,k] - y[b,j,k])^2
+ *   R[0,0] = 0, R[i,0] = R[0,j] = +inf,
+ *   R[i,j] = C[i,j] + softmin_g(R[i-1,j-1], R[i-1,j], R[i,j-1]),
+ *   softmin_g(a) = -g log sum exp(-a/g),  loss[b] = R[N,M]  (may be negative),
+ *   E = dR[N,M]/dC from the backward recursion done in log space,
+ *   grad_x[b,i] = grad_loss[b] * 2 sum_j E[i,j] (x_i - y_j),
+ *   grad_y[b,j] = grad_loss[b] * 2 sum_i E[i,j] (y_j - x_i).
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are fp32, row-major and contiguous: x (B,N,D), y (B,M,D),
+ *    grad_x like x, grad_y like y, loss and grad_loss (B,).
+ *  - Every tensor pointer and the workspace are DEVICE pointers owned by the
+ *    caller. The library allocates nothing.
+ *  - `ws` is a caller-owned device workspace of at least
+ *    sdtw_workspace_bytes(...) bytes, 256-byte aligned. sdtw_forward leaves in
+ *    it the state that the matching sdtw_backward reads, so the caller keeps it
+ *    unchanged between the two calls (as autograd keeps saved tensors).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream). Argument errors are returned synchronously before any launch.
+ *    A launch failure returns SDTW_ERR_CUDA. A device-side wait that runs out
+ *    of time is reported later by sdtw_last_device_status.
+ *  - No CPU fallback exists: every step runs in this library's CUDA kernels.
+ *  - Inputs containing NaN or inf are not checked; results are then NaN.
+ */
+#ifndef SDTW_H
+#define SDTW_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Distance handling. UNFUSED precomputes the (B,N,M) cost tensor in the
+ * workspace before the DP (README, "Basic (Unfused)"; review page, "proposed
+ * method", fourth bullet). FUSED recomputes the cost inside the DP kernels and
+ * keeps no cost tensor (README, "Fused Mode"; paper abstract, contribution (3)). */
+typedef enum { SDTW_UNFUSED = 0, SDTW_FUSED = 1 } sdtw_mode;
+
+typedef enum {
+    SDTW_OK = 0,
+    SDTW_ERR_ARG = 1,        /* null pointer, bad mode, bad op, bad step number   */
+    SDTW_ERR_GAMMA = 2,      /* gamma not > 0 or not finite                        */
+    SDTW_ERR_EMPTY = 3,      /* B, N, M or D < 1 (empty sequences)                 */
+    SDTW_ERR_SHAPE = 4,      /* shape mismatch (normalized needs equal shapes)     */
+    SDTW_ERR_WORKSPACE = 5,  /* workspace NULL, misaligned or smaller than needed  */
+    SDTW_ERR_CUDA = 6,       /* a CUDA runtime call or a launch failed             */
+    SDTW_ERR_TIMEOUT = 7,    /* a device-side wait ran out of time (device status) */
+    SDTW_ERR_TOO_LARGE = 8   /* sizes overflow the library's 32-bit index limits   */
+} sdtw_status;
+
+/* Operation codes for sdtw_workspace_bytes. */
+#define SDTW_OP_FWD_BWD 0    /* sdtw_forward followed by sdtw_backward           */
+#define SDTW_OP_NORMALIZED 1 /* sdtw_normalized (N == M)                          */
+#define SDTW_OP_BARYCENTER 2 /* sdtw_barycenter_step: B = K sequences, N = T, M = T2 */
+
+/* Bytes of device workspace needed by `op` for these sizes and mode; 0 when the
+ * arguments are invalid. Pure host function, no CUDA call. */
+size_t sdtw_workspace_bytes(int op, int B, int N, int M, int D, sdtw_mode mode);
+
+/* Squared Euclidean cost C (B,N,M), row-major, into `C` (device). The unfused
+ * distance step on its own (README, "Tests": distance correctness). */
+sdtw_status sdtw_distance(const float* x, const float* y, int B, int N, int M, int D,
+                          float* C, void* stream);
+
+/* Forward pass: loss[b] = R_b[N,M] (B,) for every pair (x_b, y_b). Leaves the
+ * DP state for sdtw_backward in `ws`. */
+sdtw_status sdtw_forward(const float* x, const float* y, int B, int N, int M, int D, float gamma,
+                         sdtw_mode mode, float* loss, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward pass for the same (x, y, B, N, M, D, gamma, mode) as the preceding
+ * sdtw_forward on this workspace. grad_loss (B,) is dL/dloss. grad_x and/or
+ * grad_y may be NULL when not wanted; they are overwritten, not accumulated. */
+sdtw_status sdtw_backward(const float* x, const float* y, int B, int N, int M, int D, float gamma,
+                          sdtw_mode mode, const float* grad_loss, float* grad_x, float* grad_y,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Normalized Soft-DTW (README, "Normalization"):
+ *   loss[b] = s(x_b,y_b) - (s(x_b,x_b) + s(y_b,y_b)) / 2,  x and y both (B,N,D).
+ * The three problems run as one batch of 3B. When grad_loss is non-NULL the
+ * input gradients are written too (grad_x/grad_y may be NULL individually). */
+sdtw_status sdtw_normalized(const float* x, const float* y, int B, int N, int D, float gamma,
+                            sdtw_mode mode, float* loss, const float* grad_loss, float* grad_x,
+                            float* grad_y, void* ws, size_t ws_bytes, void* stream);
+
+/* One Adam step of a Soft-DTW barycenter (README, "Time Series Barycenters
+ * (Averaging)"; review page, "proposed method", fifth bullet):
+ *   L(z) = (1/K) sum_k s(z, X_k),  g = dL/dz,
+ *   m <- b1 m + (1-b1) g;  v <- b2 v + (1-b2) g^2;
+ *   z <- z - lr (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps).
+ * z, m, v are (T,D) and updated in place; X is (K,T2,D); t >= 1 is the step
+ * number. loss_out (nullable, one float) receives L at the incoming z. */
+sdtw_status sdtw_barycenter_step(float* z, float* m, float* v, int t, const float* X, int K, int T,
+                                 int T2, int D, float gamma, float lr, float beta1, float beta2,
+                                 float eps, sdtw_mode mode, float* loss_out, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/* Synchronizes `stream`, then reports (and clears) the device status word kept
+ * in `ws`: SDTW_OK, or SDTW_ERR_TIMEOUT when a DP kernel gave up waiting for a
+ * neighbouring tile. */
+sdtw_status sdtw_last_device_status(void* ws, void* stream);
+
+/* Static description of a status code. */
+const char* sdtw_status_string(sdtw_status s);
+
+/* Testing hook. Sets the time limit of every device-side wait (seconds; <= 0
+ * restores the default of 2 s) and, when `skip_publish` is non-zero, makes the
+ * next sdtw_forward withhold the ready flags of the first strip so that waiting
+ * tiles run out of time and the call reports SDTW_ERR_TIMEOUT through
+ * sdtw_last_device_status. No GPU fault is involved. Process-wide. */
+void sdtw_debug_set_wait(double seconds, int skip_publish);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SDTW_H */

@@ -1,0 +1,101 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+sizes workspaces, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from helpers import ROOT, ensure_built
+
+HEADER = os.path.join(ROOT, "include", "sdtw.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdtw_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_built()
+    from differentiable_series_alignment_gb300 import _lib
+    return _lib.load()
+
+
+def test_header_declares_the_documented_entry_points():
+    names = _declared_functions()
+    for n in ("sdtw_workspace_bytes", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
+              "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_status_string", "sdtw_distance"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from differentiable_series_alignment_gb300 import _lib
+    for n in _declared_functions():
+        assert hasattr(lib, n), f"libsdtw.so does not export {n}"
+    assert set(_declared_functions()) == set(_lib.EXPORTS)
+
+
+def test_workspace_sizes(lib):
+    from differentiable_series_alignment_gb300 import _lib as L
+    u = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.UNFUSED)
+    f = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.FUSED)
+    # skewed slots: 16 blocks x (512+31) x 32 per problem
+    slots = 32 * 16 * 543 * 32
+    assert f >= slots * (8 + 4)          # (vl,hu) pairs + alignment matrix
+    assert u >= f + slots * 4            # + the stored cost tensor
+    assert u - f < slots * 4 + 4096
+    n = L.sdtw_workspace_bytes(L.OP_NORMALIZED, 32, 512, 999, 64, L.FUSED)   # M ignored
+    assert n >= 3 * f - 3 * 4096
+    assert L.sdtw_workspace_bytes(L.OP_BARYCENTER, 64, 1024, 1024, 8, L.FUSED) > 0
+    for bad in [(0, 4, 4, 4), (4, 0, 4, 4), (4, 4, 0, 4), (4, 4, 4, 0)]:
+        assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, *bad, L.UNFUSED) == 0
+    assert L.sdtw_workspace_bytes(7, 4, 4, 4, 4, L.UNFUSED) == 0
+    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, 4, 4, 4, 4, 3) == 0
+
+
+def _fwd(lib, x=0x1000, y=0x2000, B=2, N=3, M=4, D=2, gamma=1.0, mode=0, loss=0x3000, ws=0x100000,
+         ws_bytes=1 << 40):
+    vp = ctypes.c_void_p
+    return lib.sdtw_forward(vp(x) if x else None, vp(y) if y else None, B, N, M, D, gamma, mode,
+                            vp(loss) if loss else None, vp(ws) if ws else None, ws_bytes, None)
+
+
+def test_validation_codes_need_no_device(lib):
+    # Every case below must fail in host-side validation, before any CUDA call.
+    assert _fwd(lib, B=0) == 3            # SDTW_ERR_EMPTY
+    assert _fwd(lib, N=0) == 3
+    assert _fwd(lib, M=0) == 3
+    assert _fwd(lib, D=0) == 3
+    assert _fwd(lib, gamma=0.0) == 2      # SDTW_ERR_GAMMA
+    assert _fwd(lib, gamma=-1.0) == 2
+    assert _fwd(lib, gamma=float("inf")) == 2
+    assert _fwd(lib, gamma=float("nan")) == 2
+    assert _fwd(lib, mode=2) == 1         # SDTW_ERR_ARG
+    assert _fwd(lib, x=0) == 1
+    assert _fwd(lib, loss=0) == 1
+    assert _fwd(lib, ws=0) == 5           # SDTW_ERR_WORKSPACE
+    assert _fwd(lib, ws=0x100010) == 5    # misaligned
+    assert _fwd(lib, ws_bytes=16) == 5    # too small
+    assert _fwd(lib, D=100000) == 8       # SDTW_ERR_TOO_LARGE
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert lib.sdtw_status_string(code)
+    assert b"gamma" in lib.sdtw_status_string(2)
+
+
+def test_normalized_and_barycenter_validation(lib):
+    vp = ctypes.c_void_p
+    # gamma invalid
+    assert lib.sdtw_normalized(vp(0x1000), vp(0x2000), 2, 3, 2, 0.0, 0, vp(0x3000), None, None, None,
+                               vp(0x100000), 1 << 40, None) == 2
+    # t = 0 is not a valid Adam step
+    assert lib.sdtw_barycenter_step(vp(0x1000), vp(0x2000), vp(0x3000), 0, vp(0x4000), 4, 8, 8, 2, 1.0, 0.1,
+                                    0.9, 0.999, 1e-8, 1, None, vp(0x100000), 1 << 40, None) == 1
+    # empty sequences
+    assert lib.sdtw_barycenter_step(vp(0x1000), vp(0x2000), vp(0x3000), 1, vp(0x4000), 0, 8, 8, 2, 1.0, 0.1,
+                                    0.9, 0.999, 1e-8, 1, None, vp(0x100000), 1 << 40, None) == 3

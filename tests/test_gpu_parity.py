@@ -1,0 +1,256 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Tolerances: losses rel 1e-4; gradients rel 1e-3 with abs 1e-5, the upstream
+gradient being the 1/B of a batch mean. The CUDA library must be the code that
+runs: every call goes through libsdtw.so.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from differentiable_series_alignment_gb300 import synth
+from helpers import GRAD_ATOL, GRAD_RTOL, LOSS_RTOL, assert_close, ensure_built
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _lib():
+    from differentiable_series_alignment_gb300 import _lib
+    return _lib
+
+
+class warps:
+    """Force the warps-per-CTA choice (and so the strip count) of the wavefront kernels."""
+
+    def __init__(self, fwd, bwd=None):
+        self.fwd, self.bwd = fwd, (fwd if bwd is None else bwd)
+
+    def __enter__(self):
+        self.old = {k: os.environ.get(k) for k in ("SDTW_WARPS_FWD", "SDTW_WARPS_BWD")}
+        if self.fwd:
+            os.environ["SDTW_WARPS_FWD"] = str(self.fwd)
+        if self.bwd:
+            os.environ["SDTW_WARPS_BWD"] = str(self.bwd)
+
+    def __exit__(self, *a):
+        for k, v in self.old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def run_cuda(x, y, gamma, mode, grad_loss=None, want_grads=True):
+    L = _lib()
+    xt = torch.from_numpy(x).cuda()
+    yt = torch.from_numpy(y).cuda()
+    B, N, D = x.shape
+    M = y.shape[1]
+    ws = L.workspace(L.OP_FWD_BWD, B, N, M, D, mode)
+    loss = torch.empty(B, device="cuda")
+    L.sdtw_forward(xt, yt, gamma, mode, loss, ws)
+    out = dict(loss=loss)
+    if want_grads:
+        g = torch.full((B,), 1.0 / B, device="cuda") if grad_loss is None else torch.from_numpy(
+            np.asarray(grad_loss, np.float32)).cuda()
+        gx = torch.empty_like(xt)
+        gy = torch.empty_like(yt)
+        L.sdtw_backward(xt, yt, gamma, mode, g, gx, gy, ws)
+        out.update(gx=gx, gy=gy)
+    assert L.sdtw_last_device_status(ws) == 0
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy().astype(np.float64) for k, v in out.items()}
+
+
+def check_against_oracle(x, y, gamma, mode, grad_loss=None, sample=None, what=""):
+    got = run_cuda(x, y, gamma, mode, grad_loss)
+    B = x.shape[0]
+    gl = np.full(B, 1.0 / B) if grad_loss is None else np.asarray(grad_loss, np.float64)
+    idx = np.arange(B) if sample is None else np.asarray(sample)
+    ol, ogx, ogy = oracle.batch(x[idx], y[idx], gamma, grad_loss=gl[idx])
+    assert_close(got["loss"][idx], ol, LOSS_RTOL, 0.0, f"{what} loss")
+    assert_close(got["gx"][idx], ogx, GRAD_RTOL, GRAD_ATOL, f"{what} grad_x")
+    assert_close(got["gy"][idx], ogy, GRAD_RTOL, GRAD_ATOL, f"{what} grad_y")
+    return got
+
+
+MODES = [("unfused", 0), ("fused", 1)]
+
+
+# --------------------------------------------------------------------------- small config
+
+@pytest.mark.parametrize("mname,mode", MODES)
+def test_small_config(mname, mode):
+    c = synth.CONFIGS[0]
+    x, y = synth.iid_normal_pair(c["B"], c["N"], c["M"], c["D"], 0)
+    check_against_oracle(x, y, 1.0, mode, what=f"small {mname}")
+
+
+@pytest.mark.parametrize("mname,mode", MODES)
+@pytest.mark.parametrize("N,M,D", [(1, 1, 3), (1, 7, 2), (9, 1, 1), (2, 2, 5), (31, 33, 3), (33, 31, 4),
+                                   (64, 65, 7), (100, 37, 16), (37, 100, 1), (129, 130, 9)])
+def test_ragged_shapes(mname, mode, N, M, D):
+    x, y = synth.iid_normal_pair(3, N, M, D, 90, repeat=N * 1000 + M)
+    check_against_oracle(x, y, 0.7, mode, grad_loss=[0.5, -1.25, 2.0], what=f"{N}x{M}x{D} {mname}")
+
+
+@pytest.mark.parametrize("mname,mode", MODES)
+@pytest.mark.parametrize("W", [1, 2, 3, 16])
+def test_strip_decompositions_agree(mname, mode, W):
+    # Many strips (W=1: every 32-row block its own CTA, boundaries through global
+    # memory) down to one strip per problem; all must reproduce the oracle.
+    x, y = synth.iid_normal_pair(2, 200, 150, 6, 91)
+    with warps(W):
+        check_against_oracle(x, y, 1.0, mode, what=f"W={W} {mname}")
+
+
+@pytest.mark.parametrize("gamma", [10.0, 1.0, 0.1, 0.01, 0.001])
+def test_small_gamma_no_nan(gamma):
+    x, y = synth.warped_pair(2, 300, 8, 93)
+    got = check_against_oracle(x, y, gamma, 1, what=f"gamma={gamma}")
+    assert all(np.all(np.isfinite(v)) for v in got.values())
+
+
+def test_fused_equals_unfused():
+    x, y = synth.iid_normal_pair(4, 96, 80, 12, 94)
+    a = run_cuda(x, y, 1.0, 0)
+    b = run_cuda(x, y, 1.0, 1)
+    assert_close(b["loss"], a["loss"], 1e-5, 0.0, "fused vs unfused loss")
+    assert_close(b["gx"], a["gx"], 1e-4, 1e-6, "fused vs unfused grad_x")
+
+
+def test_distance_kernel_matches_definition():
+    L = _lib()
+    x, y = synth.iid_normal_pair(3, 70, 45, 9, 95)
+    C = torch.empty((3, 70, 45), device="cuda")
+    L.sdtw_distance(torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda(), C)
+    x64, y64 = x.astype(np.float64), y.astype(np.float64)
+    ref = ((x64[:, :, None, :] - y64[:, None, :, :]) ** 2).sum(-1)
+    assert_close(C.cpu().numpy(), ref, 1e-5, 1e-5, "distance")
+
+
+# --------------------------------------------------------------------------- headline config
+
+@pytest.mark.parametrize("mname,mode", MODES)
+def test_headline_config(mname, mode):
+    c = synth.CONFIGS[1]
+    x, y = synth.iid_normal_pair(c["B"], c["N"], c["M"], c["D"], 1)
+    check_against_oracle(x, y, 1.0, mode, what=f"headline {mname}")
+
+
+# --------------------------------------------------------------------------- sweep (sampled)
+
+@pytest.mark.parametrize("mname,mode", MODES)
+@pytest.mark.parametrize("L,D", [(128, 128), (1024, 128), (2048, 128), (256, 1), (256, 4), (256, 256)])
+def test_sweep_sampled(mname, mode, L, D):
+    x, y = synth.iid_normal_pair(32, L, L, D, 2, repeat=L * 1000 + D)
+    sample = [0, 31] if L >= 1024 else [0, 7, 31]
+    check_against_oracle(x, y, 1.0, mode, sample=sample, what=f"sweep L={L} D={D} {mname}")
+
+
+# --------------------------------------------------------------------------- normalized
+
+def run_normalized(x, y, gamma, mode, grad_loss):
+    L = _lib()
+    xt, yt = torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda()
+    B, N, D = x.shape
+    ws = L.workspace(L.OP_NORMALIZED, B, N, N, D, mode)
+    loss = torch.empty(B, device="cuda")
+    gx, gy = torch.empty_like(xt), torch.empty_like(yt)
+    g = torch.from_numpy(np.asarray(grad_loss, np.float32)).cuda()
+    L.sdtw_normalized(xt, yt, gamma, mode, loss, g, gx, gy, ws)
+    assert L.sdtw_last_device_status(ws) == 0
+    return loss.cpu().numpy(), gx.cpu().numpy(), gy.cpu().numpy()
+
+
+@pytest.mark.parametrize("mname,mode", MODES)
+@pytest.mark.parametrize("N,D", [(64, 4), (77, 3)])
+def test_normalized(mname, mode, N, D):
+    x, y = synth.iid_normal_pair(4, N, N, D, 96)
+    gl = np.array([0.25, 0.25, -0.5, 1.0])
+    loss, gx, gy = run_normalized(x, y, 0.8, mode, gl)
+    ol, ogx, ogy = oracle.normalized(x, y, 0.8, grad_loss=gl)
+    sxx = oracle.batch(x, x, 0.8)[0]
+    syy = oracle.batch(y, y, 0.8)[0]
+    atol = 1e-4 * np.maximum(1.0, np.maximum(np.abs(sxx), np.abs(syy)))
+    assert np.all(np.abs(loss - ol) <= atol + LOSS_RTOL * np.abs(ol)), (loss, ol)
+    assert_close(gx, ogx, GRAD_RTOL, GRAD_ATOL, "normalized grad_x")
+    assert_close(gy, ogy, GRAD_RTOL, GRAD_ATOL, "normalized grad_y")
+
+
+def test_normalized_of_equal_inputs_is_zero():
+    x, _ = synth.iid_normal_pair(2, 50, 50, 3, 97)
+    loss, gx, gy = run_normalized(x, x.copy(), 1.0, 1, [1.0, 1.0])
+    s = np.abs(oracle.batch(x, x, 1.0)[0])
+    assert np.all(np.abs(loss) <= 1e-4 * np.maximum(1.0, s)), loss
+    gscale = np.abs(oracle.batch(x, x, 1.0, grad_loss=np.ones(2))[1]).max()
+    assert np.abs(gx).max() <= 1e-3 * gscale and np.abs(gy).max() <= 1e-3 * gscale
+
+
+# --------------------------------------------------------------------------- barycenter
+
+@pytest.mark.parametrize("mname,mode", MODES)
+def test_barycenter_steps_match_oracle(mname, mode):
+    L = _lib()
+    X = synth.block_waves(8, 96, 3, 4)
+    z0 = X.astype(np.float64).mean(axis=0).astype(np.float32)
+    Xt = torch.from_numpy(X).cuda()
+    z = torch.from_numpy(z0.copy()).cuda()
+    m = torch.zeros_like(z)
+    v = torch.zeros_like(z)
+    ws = L.workspace(L.OP_BARYCENTER, 8, 96, 96, 3, mode)
+    lo = torch.empty(1, device="cuda")
+    zo, mo, vo = z0.astype(np.float64), np.zeros_like(z0, np.float64), np.zeros_like(z0, np.float64)
+    for t in (1, 2, 3):
+        # oracle step from the CUDA path's current state, so the comparison is per step
+        zc, mc, vc = z.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
+        zo, mo, vo, lref, _ = oracle.barycenter_step(zc, mc, vc, t, X, 1.0, lr=0.1)
+        L.sdtw_barycenter_step(z, m, v, t, Xt, 1.0, 0.1, 0.9, 0.999, 1e-8, mode, lo, ws)
+        assert L.sdtw_last_device_status(ws) == 0
+        assert_close(lo.cpu().numpy(), [lref], LOSS_RTOL, 0.0, f"step {t} loss")
+        assert_close(m.cpu().numpy(), mo, GRAD_RTOL, GRAD_ATOL, f"step {t} first moment")
+        # z moves by ~lr per coordinate; compare the update itself
+        assert_close(z.cpu().numpy() - zc, zo - zc, 2e-3, 1e-6, f"step {t} update")
+
+
+# --------------------------------------------------------------------------- device status
+
+def test_withheld_ready_flag_times_out_and_recovers():
+    L = _lib()
+    x, y = synth.iid_normal_pair(2, 160, 40, 3, 98)
+    xt, yt = torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda()
+    ws = L.workspace(L.OP_FWD_BWD, 2, 160, 40, 3, 1)
+    loss = torch.empty(2, device="cuda")
+    try:
+        with warps(1):
+            L.sdtw_debug_set_wait(0.05, skip_publish=True)
+            L.sdtw_forward(xt, yt, 1.0, 1, loss, ws)
+            assert L.sdtw_last_device_status(ws) == 7   # SDTW_ERR_TIMEOUT
+    finally:
+        L.sdtw_debug_set_wait(0.0, skip_publish=False)
+    # the context is still usable and the next call is correct
+    got = run_cuda(x, y, 1.0, 1)
+    ol, _, _ = oracle.batch(x, y, 1.0)
+    assert_close(got["loss"], ol, LOSS_RTOL, 0.0, "after timeout")
+
+
+def test_validation_errors_raise():
+    L = _lib()
+    x = torch.zeros((2, 5, 3), device="cuda")
+    ws = L.workspace(L.OP_FWD_BWD, 2, 5, 5, 3, 0)
+    loss = torch.empty(2, device="cuda")
+    with pytest.raises(L.SdtwError) as e:
+        L.sdtw_forward(x, x, 0.0, 0, loss, ws)
+    assert e.value.code == 2
+    with pytest.raises(L.SdtwError) as e:
+        L.sdtw_forward(x, x, 1.0, 0, loss, ws[:100])
+    assert e.value.code == 5
