@@ -27,7 +27,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 // Workspace layout. The status word sits at offset 0 for every op.
 struct Layout {
     size_t status, ctrl_f, ctrl_f_bytes, ctrl_b, ctrl_b_bytes;
-    size_t colsum, rowsum, losses, edge_f, edge_b, vh, e, dsk, gparts, total;
+    size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, total;
     int P, N, M, D, NB;
 };
 
@@ -46,6 +46,7 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->ctrl_b = o; L->ctrl_b_bytes = sizeof(int) * (1 + (size_t)P * NB); o = align_up(o + L->ctrl_b_bytes);
     L->colsum = o; o = align_up(o + sizeof(double) * (size_t)P * NB);
     L->rowsum = o; o = align_up(o + sizeof(double) * (size_t)P);
+    L->rowbuf = o; o = align_up(o + sizeof(float) * (size_t)P * M);
     L->losses = o; o = align_up(o + sizeof(float) * (size_t)P);
     L->edge_f = o; o = align_up(o + sizeof(float) * (size_t)P * NB * M);
     L->edge_b = o; o = align_up(o + sizeof(float2) * (size_t)P * NB * M);
@@ -142,6 +143,8 @@ WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamm
     q.prog_b = cb + 1;
     q.colsum = at<double>(ws, L.colsum);
     q.rowsum = at<double>(ws, L.rowsum);
+    q.rowbuf = at<float>(ws, L.rowbuf);
+    q.accurate = env_int("SDTW_ACCURATE", 0);
     q.loss = at<float>(ws, L.losses);
     q.status = at<int>(ws, L.status);
     q.wait_ns = g_wait_ns;

@@ -49,12 +49,17 @@ struct Problems {
     }
 };
 
-// Skewed layout geometry for one problem: NB blocks of (M+31) x 32 slots.
+// Skewed layout geometry for one problem: NB blocks of skew_T(M) x 32 slots,
+// skew_T(M) = M + 31 rounded up to a whole number of wavefront groups (the
+// padding slots hold no cell, so the step loops need no bounds checks).
+__host__ __device__ __forceinline__ int skew_T(int M) {
+    return ((M + 31 + kGroup - 1) / kGroup) * kGroup;
+}
 __host__ __device__ __forceinline__ long long skew_slots(int N, int M) {
-    return (long long)((N + 31) / 32) * (long long)(M + 31) * 32;
+    return (long long)((N + 31) / 32) * (long long)skew_T(M) * 32;
 }
 __host__ __device__ __forceinline__ long long skew_index(int N, int M, int p, int rb, int t, int lane) {
-    return (long long)p * skew_slots(N, M) + ((long long)rb * (M + 31) + t) * 32 + lane;
+    return (long long)p * skew_slots(N, M) + ((long long)rb * skew_T(M) + t) * 32 + lane;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -67,6 +72,72 @@ __device__ __forceinline__ float lg2(float x) {
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// 2^x for x <= 0; 0 for x < -125 (and for x = -inf). Cody & Waite range
+// reduction x = n + f, n = rint(x), f in [-1/2, 1/2], then a degree-7
+// polynomial for 2^f fitted for this library (fit_exp2.py: relative fit error
+// 2.6e-9, mean -4e-10). Its error is dominated by round-to-nearest, so it has
+// no systematic bias, unlike the hardware approximation: the DP recursions add
+// ~N+M of these terms along every path, and a biased exponential would drift
+// the alignment matrix.
+__device__ __forceinline__ float exp2_neg(float x) {
+    const float magic = 12582912.0f;  // 1.5 * 2^23: x + magic rounds x to an integer
+    const float t = x + magic;
+    const float n = t - magic;
+    const float f = x - n;
+    float p = 1.5165811419137754e-05f;
+    p = fmaf(p, f, 0.00015466917830053717f);
+    p = fmaf(p, f, 0.001333407941274345f);
+    p = fmaf(p, f, 0.00961803738027811f);
+    p = fmaf(p, f, 0.055504102259874344f);
+    p = fmaf(p, f, 0.24022650718688965f);
+    p = fmaf(p, f, 0.6931471824645996f);
+    p = fmaf(p, f, 1.0f);
+    const int scale = (__float_as_int(t) - 0x4B400000) << 23;  // n << 23
+    const float r = __int_as_float(__float_as_int(p) + scale);
+    return (x < -125.0f) ? 0.0f : r;
+}
+
+// log2(1 + a + b) for a, b in [0, 1]: the three-term sum of a log-sum-exp whose
+// largest term has been factored out. log2f is the accurate (unbiased) library
+// function.
+__device__ __forceinline__ float log2_1pab(float a, float b) {
+    return log2f((1.0f + a) + b);
+}
+
+// Error-free sum (Knuth's TwoSum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// Squared Euclidean distance accumulator. Terms are summed in fp32 over blocks
+// of kDistBlock components; block sums are added into a (hi, lo) pair with
+// TwoSum, so the result is within about one rounding of the exact sum. A plain
+// sequential fp32 sum over D components is ~5x less accurate, and the
+// gradient reacts to cost errors at that level (the alignment matrix moves by
+// ~1e-4 relative), which the rel 1e-3 gradient tolerance does not absorb where
+// the terms of sum_j E[i,j] (x_i - y_j) cancel.
+constexpr int kDistBlock = 8;
+struct DistAcc {
+    float hi = 0.f, lo = 0.f;
+    __device__ __forceinline__ void add_block(float blk) {
+        float s, e;
+        two_sum(hi, blk, s, e);
+        hi = s;
+        lo += e;
+    }
+    __device__ __forceinline__ float value() const { return hi + lo; }
+};
+
+// Sort three values: lo <= mid <= hi.
+__device__ __forceinline__ void sort3(float a, float b, float c, float& lo, float& mid, float& hi) {
+    const float t1 = fminf(a, b), t2 = fmaxf(a, b);
+    lo = fminf(t1, c);
+    hi = fmaxf(t2, c);
+    mid = fmaxf(t1, fminf(t2, c));
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -42,25 +42,31 @@ __global__ void __launch_bounds__(32 * kDistWarps) dist_skew_kernel(Problems pr,
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int TPW = kDistT / kDistWarps;
-    float acc[TPW];
-#pragma unroll
-    for (int u = 0; u < TPW; ++u) acc[u] = 0.f;
+    DistAcc acc[TPW];
     const int tw = t0 + warp * TPW;
     // lane handles row r0+lane, columns j = t - lane for t in [tw, tw+TPW)
     const int yrow0 = tw - lane - jbase;  // ys row of the first column, in [0, ny)
-    for (int k = 0; k < D; ++k) {
-        const float xv = xs[lane * XS + k];
+    for (int k0 = 0; k0 < D; k0 += kDistBlock) {
+        const int k1 = min(k0 + kDistBlock, D);
+        float blk[TPW];
 #pragma unroll
-        for (int u = 0; u < TPW; ++u) {
-            const float a = xv - ys[(yrow0 + u) * XS + k];
-            acc[u] = fmaf(a, a, acc[u]);
+        for (int u = 0; u < TPW; ++u) blk[u] = 0.f;
+        for (int k = k0; k < k1; ++k) {
+            const float xv = xs[lane * XS + k];
+#pragma unroll
+            for (int u = 0; u < TPW; ++u) {
+                const float a = xv - ys[(yrow0 + u) * XS + k];
+                blk[u] = fmaf(a, a, blk[u]);
+            }
         }
+#pragma unroll
+        for (int u = 0; u < TPW; ++u) acc[u].add_block(blk[u]);
     }
     float* out = Dsk + skew_index(N, M, p, rb, 0, lane);
 #pragma unroll
     for (int u = 0; u < TPW; ++u) {
         const int t = tw + u;
-        if (t < T) out[(long long)t * 32] = acc[u];
+        if (t < T) out[(long long)t * 32] = acc[u].value();
     }
 }
 
@@ -73,12 +79,16 @@ __global__ void dist_rowmajor_kernel(Problems pr, int N, int M, int D, float* __
     if (i >= N || j >= M) return;
     const float* xi = pr.x(p) + (size_t)i * D;
     const float* yj = pr.y(p) + (size_t)j * D;
-    float acc = 0.f;
-    for (int k = 0; k < D; ++k) {
-        const float a = xi[k] - yj[k];
-        acc = fmaf(a, a, acc);
+    DistAcc acc;
+    for (int k0 = 0; k0 < D; k0 += kDistBlock) {
+        float blk = 0.f;
+        for (int k = k0; k < min(k0 + kDistBlock, D); ++k) {
+            const float a = xi[k] - yj[k];
+            blk = fmaf(a, a, blk);
+        }
+        acc.add_block(blk);
     }
-    C[((size_t)p * N + i) * M + j] = acc;
+    C[((size_t)p * N + i) * M + j] = acc.value();
 }
 
 }  // namespace

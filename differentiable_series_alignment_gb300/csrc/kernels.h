@@ -29,15 +29,18 @@ struct WaveParams {
     int* ticket_b;    // backward strip ticket
     int* done;        // [P]         finished forward strips
     double* colsum;   // [P][NB]
-    double* rowsum;   // [P]
+    double* rowsum;   // [P]  (unused)
+    float* rowbuf;    // [P][M]      h of the last row, for the loss
     float* loss;      // [P]
     int* status;      // device status word
     unsigned long long wait_ns;
     int skip_publish; // test hook: strip 0 withholds its forward ready counter
+    int accurate;     // 1: unbiased exp2/log2 in the recursions; 0: MUFU approximations
 };
 
 size_t wave_smem_fixed(int W, bool backward);
 size_t wave_smem_fused_per_warp(int D);
+size_t wave_smem_floor();
 cudaError_t launch_forward(WaveParams q, bool fused, cudaStream_t st);
 cudaError_t launch_backward(WaveParams q, cudaStream_t st);
 

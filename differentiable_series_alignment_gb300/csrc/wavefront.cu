@@ -24,6 +24,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <cstdlib>
+
 namespace sdtw {
 
 namespace {
@@ -36,8 +38,11 @@ __device__ __forceinline__ bool wait_smem(const volatile int* cnt, int target, c
     if (*cnt < target) {
         const unsigned long long t0 = global_ns();
         unsigned it = 0;
+        // Back off while waiting: a spinning warp would take issue slots from
+        // the working warps that share its SM sub-partition.
         while (*cnt < target) {
-            if ((++it & 31u) == 0) {
+            __nanosleep(32);
+            if ((++it & 7u) == 0) {
                 if (ld_volatile_global(q.status) != 0) { ok = false; break; }
                 if (global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); ok = false; break; }
             }
@@ -54,6 +59,7 @@ __device__ __forceinline__ bool wait_global(const int* cnt, int target, const Wa
     if (ld_acquire_gpu(cnt) < target) {
         const unsigned long long t0 = global_ns();
         while (ld_acquire_gpu(cnt) < target) {
+            __nanosleep(64);
             if (ld_volatile_global(q.status) != 0) { ok = false; break; }
             if (global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); ok = false; break; }
         }
@@ -70,10 +76,17 @@ struct FusedSmem {
 }  // namespace
 
 // ---------------------------------------------------------------------------
+// Math variants: ACC selects the unbiased exp2/log2 of common.cuh, otherwise
+// the MUFU approximations.
+// ---------------------------------------------------------------------------
+template <bool ACC> __device__ __forceinline__ float dp_exp2(float x) { return ACC ? exp2_neg(x) : ex2(x); }
+template <bool ACC> __device__ __forceinline__ float dp_log2(float x) { return ACC ? log2f(x) : lg2(x); }
+
+// ---------------------------------------------------------------------------
 // Forward
 // ---------------------------------------------------------------------------
-template <bool FUSED>
-__global__ void __launch_bounds__(kMaxWarps * 32) fwd_kernel(const WaveParams q)
+template <bool FUSED, bool ACC>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams q)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int W = q.W;
@@ -83,6 +96,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) fwd_kernel(const WaveParams q)
     volatile int* cons = prod + W;
     __shared__ int s_tk;
     __shared__ double s_red[kMaxWarps];
+    __shared__ int s_last;
 
     if (threadIdx.x == 0) s_tk = atomicAdd(q.ticket_f, 1);
     if (threadIdx.x < W) { prod[threadIdx.x] = 0; cons[threadIdx.x] = 0; }
@@ -90,17 +104,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32) fwd_kernel(const WaveParams q)
 
     const int tk = s_tk;
     const int p = tk % q.P, strip = tk / q.P;
-    const int N = q.N, M = q.M, T = M + 31;
+    const int N = q.N, M = q.M, T = skew_T(M);
     const int rb = strip * W + warp, r0 = rb * 32, i = r0 + lane;
     const bool active = r0 < N;
     const bool has_top = active && r0 > 0;
     const bool top_global = has_top && warp == 0;
     const bool has_bot = active && (r0 + 32 < N);
     const bool bot_global = has_bot && warp == W - 1;
+    const bool row0_lane = (i == 0);
+    const bool last_lane = (i == N - 1);
     const float scale = q.scale;
+    float* rowbuf = q.rowbuf + (size_t)p * M;
 
-    float c0 = 0.f;              // scaled d(i, 0)
-    float rsum = 0.f, rcmp = 0.f;  // Kahan sum of h over the last row
+    float c0 = 0.f;  // scaled d(i, 0)
 
     FusedSmem fz{};
     int XS = 0;
@@ -132,14 +148,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32) fwd_kernel(const WaveParams q)
         int* prog_out = q.prog_f + (size_t)p * q.NB + strip;
         const int* prog_in = q.prog_f + (size_t)p * q.NB + strip - 1;
         const bool publish_ok = !(q.skip_publish && strip == 0);
+        // Boundary row out of this warp (lane 31): generic pointer into the
+        // shared ring or the global edge buffer.
+        const bool chan_lane = has_bot && lane == 31;
+        float* chan_out = bot_global ? edge_out : ring_out;
+        const int chan_mask = bot_global ? 0x7fffffff : (kRing - 1);
 
         float h_prev = 0.f, v_prev = 0.f;
         float dn[kGroup];
         if (!FUSED) {
 #pragma unroll
-            for (int u = 0; u < kGroup; ++u) dn[u] = (u < T) ? dp[(long long)u * 32] : 0.f;
+            for (int u = 0; u < kGroup; ++u) dn[u] = dp[(long long)u * 32];
         }
-        const int nG = (T + kGroup - 1) / kGroup;
+        const int nG = T / kGroup;
         for (int g = 0; g < nG; ++g) {
             const int s0 = g * kGroup;
             float dc[kGroup];
@@ -148,10 +169,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) fwd_kernel(const WaveParams q)
                 for (int u = 0; u < kGroup; ++u) dc[u] = dn[u];
                 if (g + 1 < nG) {
 #pragma unroll
-                    for (int u = 0; u < kGroup; ++u) {
-                        const int t = s0 + kGroup + u;
-                        dn[u] = (t < T) ? dp[(long long)t * 32] : 0.f;
-                    }
+                    for (int u = 0; u < kGroup; ++u) dn[u] = dp[(long long)(s0 + kGroup + u) * 32];
                 }
             } else if ((s0 & 31) == 0 && s0 < M) {
                 // Raw cost of columns [s0, s0+32) for this warp's 32 rows.
@@ -163,42 +181,47 @@ __global__ void __launch_bounds__(kMaxWarps * 32) fwd_kernel(const WaveParams q)
                     fz.ys[r * XS + k] = (col < M && k < D) ? yb[(size_t)col * D + k] : 0.f;
                 }
                 __syncwarp();
-                float acc[32];
+                for (int half = 0; half < 32; half += 16) {
+                    DistAcc acc[16];
+                    for (int k0 = 0; k0 < D4; k0 += kDistBlock) {
+                        float blk[16];
 #pragma unroll
-                for (int cc = 0; cc < 32; ++cc) acc[cc] = 0.f;
-                for (int k4 = 0; k4 < D4; k4 += 4) {
-                    const float4 xv = *reinterpret_cast<const float4*>(fz.xs + lane * XS + k4);
+                        for (int cc = 0; cc < 16; ++cc) blk[cc] = 0.f;
+                        for (int k4 = k0; k4 < min(k0 + kDistBlock, D4); k4 += 4) {
+                            const float4 xv = *reinterpret_cast<const float4*>(fz.xs + lane * XS + k4);
 #pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) {
-                        const float4 yv = *reinterpret_cast<const float4*>(fz.ys + cc * XS + k4);
-                        float a = xv.x - yv.x;
-                        acc[cc] = fmaf(a, a, acc[cc]);
-                        a = xv.y - yv.y;
-                        acc[cc] = fmaf(a, a, acc[cc]);
-                        a = xv.z - yv.z;
-                        acc[cc] = fmaf(a, a, acc[cc]);
-                        a = xv.w - yv.w;
-                        acc[cc] = fmaf(a, a, acc[cc]);
+                            for (int cc = 0; cc < 16; ++cc) {
+                                const float4 yv = *reinterpret_cast<const float4*>(fz.ys + (half + cc) * XS + k4);
+                                float a = xv.x - yv.x;
+                                blk[cc] = fmaf(a, a, blk[cc]);
+                                a = xv.y - yv.y;
+                                blk[cc] = fmaf(a, a, blk[cc]);
+                                a = xv.z - yv.z;
+                                blk[cc] = fmaf(a, a, blk[cc]);
+                                a = xv.w - yv.w;
+                                blk[cc] = fmaf(a, a, blk[cc]);
+                            }
+                        }
+#pragma unroll
+                        for (int cc = 0; cc < 16; ++cc) acc[cc].add_block(blk[cc]);
                     }
-                }
 #pragma unroll
-                for (int cc = 0; cc < 32; ++cc) fz.dt[((s0 + cc) & 63) * 32 + lane] = acc[cc];
+                    for (int cc = 0; cc < 16; ++cc) fz.dt[((s0 + half + cc) & 63) * 32 + lane] = acc[cc].value();
+                }
                 __syncwarp();
             }
 
             // Upper-neighbour values for lane 0: columns [s0, s0+kGroup).
             float topv = 0.f;
             bool ok = true;
-            if (has_top) {
+            if (has_top && s0 < M) {
                 const int need = min(s0 + kGroup, M);
-                if (s0 < M) {
-                    if (top_global) {
-                        ok = wait_global(prog_in, need, q);
-                        if (ok && lane < kGroup && s0 + lane < M) topv = __ldcg(edge_in + s0 + lane);
-                    } else {
-                        ok = wait_smem(&prod[warp - 1], need, q);
-                        if (ok && lane < kGroup) topv = ring_in[(s0 + lane) & (kRing - 1)];
-                    }
+                if (top_global) {
+                    ok = wait_global(prog_in, need, q);
+                    if (ok && lane < kGroup && s0 + lane < M) topv = __ldcg(edge_in + s0 + lane);
+                } else {
+                    ok = wait_smem(&prod[warp - 1], need, q);
+                    if (ok && lane < kGroup) topv = ring_in[(s0 + lane) & (kRing - 1)];
                 }
             }
             if (ok && has_bot && !bot_global) {
@@ -211,35 +234,27 @@ __global__ void __launch_bounds__(kMaxWarps * 32) fwd_kernel(const WaveParams q)
             for (int u = 0; u < kGroup; ++u) {
                 const int s = s0 + u;
                 const int j = s - lane;
-                float hu = __shfl_up_sync(kFull, h_prev, 1);
+                const float hs = __shfl_up_sync(kFull, h_prev, 1);
                 const float tv = __shfl_sync(kFull, topv, u);
-                if (lane == 0) hu = tv;
+                const float hu = (lane == 0) ? tv : hs;
                 const float vl = v_prev;
-                const float d = FUSED ? fz.dt[(j & 63) * 32 + lane] * scale : dc[u] * scale;
-                const float m = fminf(fminf(0.f, vl), hu);
-                const float S = ex2(m) + ex2(m - vl) + ex2(m - hu);
-                const float tt = d + m - lg2(S);
-                float h = tt - vl, v = tt - hu;
-                float svl = vl, shu = hu;
-                if (i == 0) {
-                    if (j == 0) { h = -kBig; v = -kBig; svl = kBig; shu = kBig; }
-                    else { h = d; v = -kBig; svl = -kBig; shu = kBig; }
-                } else if (j == 0) {
-                    v = d; h = -kBig; svl = kBig; shu = -kBig;
-                }
-                if (j == 0) c0 = d;
-                const bool valid = (i < N) && (j >= 0) && (j < M);
-                if (s < T) vhp[(long long)s * 32] = make_float2(svl, shu);
-                if (has_bot && lane == 31 && valid) {
-                    if (bot_global) edge_out[j] = h;
-                    else ring_out[j & (kRing - 1)] = h;
-                }
-                if (i == N - 1 && valid && j >= 1) {  // Kahan
-                    const float yk = h - rcmp;
-                    const float tk2 = rsum + yk;
-                    rcmp = (tk2 - rsum) - yk;
-                    rsum = tk2;
-                }
+                const float d = (FUSED ? fz.dt[(j & 63) * 32 + lane] : dc[u]) * scale;
+                // t = d + softmin(0, vl, hu) = d + lo - log2(1 + 2^(lo-mid) + 2^(lo-hi))
+                float lo, mid, hi;
+                sort3(0.f, vl, hu, lo, mid, hi);
+                const float lz = dp_log2<ACC>((1.f + dp_exp2<ACC>(lo - mid)) + dp_exp2<ACC>(lo - hi));
+                const float tt = (d + lo) - lz;
+                // first column / first row: a single predecessor (R borders are +inf)
+                const bool col0 = (j == 0);
+                const float h = col0 ? -kBig : (row0_lane ? d : tt - vl);
+                const float v = row0_lane ? -kBig : (col0 ? d : tt - hu);
+                const float svl = col0 ? kBig : (row0_lane ? -kBig : vl);
+                const float shu = row0_lane ? kBig : (col0 ? -kBig : hu);
+                c0 = col0 ? d : c0;
+                vhp[(long long)s * 32] = make_float2(svl, shu);
+                const bool valid = (unsigned)j < (unsigned)M;
+                if (chan_lane && valid) chan_out[j & chan_mask] = h;
+                if (last_lane && valid) rowbuf[j] = h;
                 h_prev = h;
                 v_prev = v;
             }
@@ -258,23 +273,32 @@ __global__ void __launch_bounds__(kMaxWarps * 32) fwd_kernel(const WaveParams q)
         }
     }
 
-    // Loss assembly: R[N,M] = sum_i d(i,0) + sum_{j>=1} h(N-1, j), in scaled units.
+    // Loss: R[N,M] = sum_i d(i,0) + sum_{j>=1} h(N-1, j), scaled units.
     double part = (active && i < N) ? (double)c0 : 0.0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
     if (lane == 0) s_red[warp] = part;
-    if (active && i == N - 1) q.rowsum[p] = (double)rsum - (double)rcmp;
+    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
         double cs = 0.0;
         for (int w = 0; w < W; ++w) cs += s_red[w];
         q.colsum[(size_t)p * q.NB + strip] = cs;
         __threadfence();
-        const int prev = atomicAdd(&q.done[p], 1);
-        if (prev == q.S - 1) {
-            __threadfence();
-            double tot = *reinterpret_cast<volatile double*>(&q.rowsum[p]);
-            for (int k = 0; k < q.S; ++k) tot += *reinterpret_cast<volatile double*>(&q.colsum[(size_t)p * q.NB + k]);
+        s_last = (atomicAdd(&q.done[p], 1) == q.S - 1);
+    }
+    __syncthreads();
+    if (s_last) {  // the last strip of problem p to finish assembles its loss
+        __threadfence();
+        double acc = 0.0;
+        for (int j = 1 + (int)threadIdx.x; j < M; j += blockDim.x) acc += (double)__ldcg(rowbuf + j);
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+        if (lane == 0) s_red[warp] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double tot = 0.0;
+            for (int w = 0; w < W; ++w) tot += s_red[w];
+            for (int k = 0; k < q.S; ++k) tot += __ldcg(&q.colsum[(size_t)p * q.NB + k]);
             q.loss[p] = (float)(tot * (double)q.unscale);
         }
     }
@@ -283,7 +307,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) fwd_kernel(const WaveParams q)
 // ---------------------------------------------------------------------------
 // Backward (log space)
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kMaxWarps * 32) bwd_kernel(const WaveParams q)
+template <bool ACC>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams q)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int W = q.W;
@@ -299,7 +324,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) bwd_kernel(const WaveParams q)
 
     const int tk = s_tk;
     const int p = tk % q.P, strip = q.S - 1 - tk / q.P;
-    const int N = q.N, M = q.M, T = M + 31;
+    const int N = q.N, M = q.M, T = skew_T(M);
+    const int off = T - (M + 31);   // leading padding steps of the reverse walk
     const int rb = strip * W + warp, r0 = rb * 32, i = r0 + lane;
     const bool active = r0 < N;
     if (!active) return;
@@ -307,6 +333,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) bwd_kernel(const WaveParams q)
     const bool below_global = has_below && warp == W - 1;
     const bool has_above = r0 > 0;                     // consumer: the warp (or strip) above
     const bool above_global = has_above && warp == 0;
+    const bool last_lane = (i == N - 1);
 
     const long long sk = skew_index(N, M, p, rb, 0, lane);
     const float2* vhp = q.VH + sk;
@@ -317,80 +344,79 @@ __global__ void __launch_bounds__(kMaxWarps * 32) bwd_kernel(const WaveParams q)
     const float2* edge_in = q.edge_b + ((size_t)p * q.NB + strip + 1) * M;
     int* prog_out = q.prog_b + (size_t)p * q.NB + strip;
     const int* prog_in = q.prog_b + (size_t)p * q.NB + strip + 1;
+    // Messages to the row above (lane 0): generic pointer into ring or edge buffer.
+    // Slot k holds column M-1-k.
+    const bool chan_lane = has_above && lane == 0;
+    float2* chan_out = above_global ? edge_out : ring_out;
+    const int chan_mask = above_global ? 0x7fffffff : (kRing - 1);
 
     float ml = -kBig, su = -kBig, sd = -kBig, rd_hold = -kBig;
     float2 vn[kGroup];
 #pragma unroll
-    for (int u = 0; u < kGroup; ++u) vn[u] = (u < T) ? vhp[(long long)(T - 1 - u) * 32] : make_float2(0.f, 0.f);
-    const int nG = (T + kGroup - 1) / kGroup;
+    for (int u = 0; u < kGroup; ++u) vn[u] = vhp[(long long)(T - 1 - u) * 32];
+    const int nG = T / kGroup;
     for (int g = 0; g < nG; ++g) {
-        const int t0 = g * kGroup;  // first backward step of the group
+        const int t0 = g * kGroup;   // first reverse step of the group
+        const int k0 = t0 - off;     // channel slot read by lane 31 at that step
         float2 vc[kGroup];
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) vc[u] = vn[u];
         if (g + 1 < nG) {
 #pragma unroll
-            for (int u = 0; u < kGroup; ++u) {
-                const int tau = t0 + kGroup + u;
-                vn[u] = (tau < T) ? vhp[(long long)(T - 1 - tau) * 32] : make_float2(0.f, 0.f);
-            }
+            for (int u = 0; u < kGroup; ++u) vn[u] = vhp[(long long)(T - 1 - (t0 + kGroup + u)) * 32];
         }
-        // Messages of the row below for lane 31: slots [t0, t0+kGroup), slot k = column M-1-k.
+        // Messages of the row below for lane 31: slots [k0, k0+kGroup).
         float2 botv = make_float2(-kBig, -kBig);
         bool ok = true;
-        if (has_below && t0 < M) {
-            const int need = min(t0 + kGroup, M);
+        if (has_below && k0 + kGroup > 0 && k0 < M) {
+            const int need = min(k0 + kGroup, M);
             if (below_global) {
                 ok = wait_global(prog_in, need, q);
-                if (ok && lane < kGroup && t0 + lane < M) {
-                    const float2* src = edge_in + t0 + lane;
-                    botv = __ldcg(src);
-                }
+                if (ok && lane < kGroup && k0 + lane >= 0 && k0 + lane < M) botv = __ldcg(edge_in + k0 + lane);
             } else {
                 ok = wait_smem(&prod[warp + 1], need, q);
-                if (ok && lane < kGroup) botv = ring_in[(t0 + lane) & (kRing - 1)];
+                if (ok && lane < kGroup && k0 + lane >= 0) botv = ring_in[(k0 + lane) & (kRing - 1)];
             }
         }
         if (ok && has_above && !above_global) {
-            const int need = t0 + kGroup - 31 - kRing;
+            const int need = k0 + kGroup - 31 - kRing;
             if (need > 0) ok = wait_smem(&cons[warp], need, q);
         }
         if (!ok) break;
 
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
-            const int tau = t0 + u;
-            const int t = T - 1 - tau;
+            const int t = T - 1 - (t0 + u);
             const int j = t - lane;
-            float ru = __shfl_down_sync(kFull, su, 1);
-            float rd = __shfl_down_sync(kFull, sd, 1);
+            const float rs = __shfl_down_sync(kFull, su, 1);
+            const float rds = __shfl_down_sync(kFull, sd, 1);
             const float bx = __shfl_sync(kFull, botv.x, u);
             const float by = __shfl_sync(kFull, botv.y, u);
-            if (lane == 31) { ru = bx; rd = by; }
-            const float a1 = (j < M - 1) ? ml : -kBig;
-            const float a2 = (i < N - 1) ? ru : -kBig;
-            const float a3 = (i < N - 1 && j < M - 1) ? rd_hold : -kBig;
+            const float ru = (lane == 31) ? bx : rs;   // msg_up from (i+1, j)
+            const float rd = (lane == 31) ? by : rds;  // msg_diag from (i+1, j), used next step
+            const float a1 = (j < M - 1) ? ml : -kBig;                    // from (i, j+1)
+            const float a2 = last_lane ? -kBig : ru;                      // from (i+1, j)
+            const float a3 = (last_lane || j >= M - 1) ? -kBig : rd_hold; // from (i+1, j+1)
             rd_hold = rd;
-            const float mx = fmaxf(fmaxf(a1, a2), a3);
-            float lE = mx + lg2(ex2(a1 - mx) + ex2(a2 - mx) + ex2(a3 - mx));
-            if (i == N - 1 && j == M - 1) lE = 0.f;
+            float lo, mid, hi;
+            sort3(a1, a2, a3, lo, mid, hi);
+            float lE = hi + dp_log2<ACC>((1.f + dp_exp2<ACC>(mid - hi)) + dp_exp2<ACC>(lo - hi));
+            lE = (last_lane && j == M - 1) ? 0.f : lE;
+            // log2 normaliser of this cell's own soft-min: the transition
+            // log-probabilities to its diag/left/up predecessors are -Lz, -vl-Lz, -hu-Lz.
             const float2 st = vc[u];
-            const float m = fminf(fminf(0.f, st.x), st.y);
-            const float Lz = lg2(ex2(m) + ex2(m - st.x) + ex2(m - st.y)) - m;
+            float wlo, wmid, whi;
+            sort3(0.f, st.x, st.y, wlo, wmid, whi);
+            const float Lz = dp_log2<ACC>((1.f + dp_exp2<ACC>(wlo - wmid)) + dp_exp2<ACC>(wlo - whi)) - wlo;
             ml = lE + (-st.x - Lz);
             su = lE + (-st.y - Lz);
             sd = lE - Lz;
-            if (t >= 0) ep[(long long)t * 32] = ex2(lE);
-            if (has_above && lane == 0 && j >= 0 && j < M) {
-                const float2 msg = make_float2(su, sd);
-                const int k = M - 1 - j;
-                if (above_global) edge_out[k] = msg;
-                else ring_out[k & (kRing - 1)] = msg;
-            }
+            ep[(long long)t * 32] = ex2(lE);
+            if (chan_lane && (unsigned)j < (unsigned)M) chan_out[(M - 1 - j) & chan_mask] = make_float2(su, sd);
         }
 
         if (has_above && lane == 0) {
-            int cnt = min(max(t0 + kGroup - 31, 0), M);
+            int cnt = min(max(k0 + kGroup - 31, 0), M);
             if (g == nG - 1) cnt = M;
             if (above_global) {
                 st_release_gpu(prog_out, cnt);
@@ -399,7 +425,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) bwd_kernel(const WaveParams q)
                 prod[warp] = cnt;
             }
         }
-        if (has_below && !below_global && lane == 31) cons[warp + 1] = min(t0 + kGroup, M);
+        if (has_below && !below_global && lane == 31) cons[warp + 1] = min(max(k0 + kGroup, 0), M);
     }
 }
 
@@ -420,34 +446,54 @@ size_t wave_smem_fused_per_warp(int D)
     return (size_t)(64 * XS + 64 * 32) * sizeof(float);
 }
 
+// Dynamic shared memory requested by every wavefront CTA, at least. The DP is
+// latency-bound: CTAs must not share an SM, or the warps of the co-resident
+// CTAs split the issue slots and every step slows down. Requesting more than
+// half of an SM's shared memory keeps the block scheduler from packing them.
+size_t wave_smem_floor()
+{
+    static size_t floor_bytes = 0;
+    if (floor_bytes == 0) {
+        int dev = 0, per_sm = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            per_sm <= 0)
+            per_sm = 228 * 1024;
+        const char* env = getenv("SDTW_PACK_CTAS");
+        floor_bytes = (env && *env == '1') ? 1 : (size_t)per_sm / 2 + 1024;
+    }
+    return floor_bytes;
+}
+
 cudaError_t launch_forward(WaveParams q, bool fused, cudaStream_t st)
 {
     const int grid = q.P * q.S;
     q.smem_fixed = (int)wave_smem_fixed(q.W, false);
     size_t smem = q.smem_fixed;
     if (fused) smem += (size_t)q.W * wave_smem_fused_per_warp(q.D);
-    cudaError_t e;
-    if (fused) {
-        e = cudaFuncSetAttribute(fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    smem = max(smem, wave_smem_floor());
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        fwd_kernel<true><<<grid, q.W * 32, smem, st>>>(q);
-    } else {
-        e = cudaFuncSetAttribute(fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        fwd_kernel<false><<<grid, q.W * 32, smem, st>>>(q);
-    }
-    return cudaGetLastError();
+        kern<<<grid, q.W * 32, smem, st>>>(q);
+        return cudaGetLastError();
+    };
+    if (fused) return q.accurate ? go(fwd_kernel<true, true>) : go(fwd_kernel<true, false>);
+    return q.accurate ? go(fwd_kernel<false, true>) : go(fwd_kernel<false, false>);
 }
 
 cudaError_t launch_backward(WaveParams q, cudaStream_t st)
 {
     const int grid = q.P * q.S;
-    const size_t smem = wave_smem_fixed(q.W, true);
-    q.smem_fixed = (int)smem;
-    cudaError_t e = cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    bwd_kernel<<<grid, q.W * 32, smem, st>>>(q);
-    return cudaGetLastError();
+    q.smem_fixed = (int)wave_smem_fixed(q.W, true);
+    const size_t smem = max((size_t)q.smem_fixed, wave_smem_floor());
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, q.W * 32, smem, st>>>(q);
+        return cudaGetLastError();
+    };
+    return q.accurate ? go(bwd_kernel<true>) : go(bwd_kernel<false>);
 }
 
 }  // namespace sdtw
