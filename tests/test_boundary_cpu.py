@@ -42,8 +42,8 @@ def test_workspace_sizes(lib):
     from differentiable_series_alignment_gb300 import _lib as L
     u = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.UNFUSED)
     f = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.FUSED)
-    # skewed slots: 16 blocks x (512+31) x 32 per problem
-    slots = 32 * 16 * 543 * 32
+    # skewed slots: 16 blocks x (512+31 rounded up to a multiple of 16) x 32 per problem
+    slots = 32 * 16 * 544 * 32
     assert f >= slots * (8 + 4)          # (vl,hu) pairs + alignment matrix
     assert u >= f + slots * 4            # + the stored cost tensor
     assert u - f < slots * 4 + 4096
