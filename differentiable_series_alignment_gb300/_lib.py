@@ -25,7 +25,8 @@ STATUS_NAMES = {
 
 # Every symbol include/sdtw.h declares.
 EXPORTS = ("sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
-           "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_status_string", "sdtw_debug_set_wait")
+           "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_status_string", "sdtw_debug_set_wait",
+           "sdtw_forward_noalloc")
 
 
 class SdtwError(RuntimeError):
@@ -64,6 +65,8 @@ def load(path: str = LIB_PATH):
         lib.sdtw_last_device_status.restype = i
         lib.sdtw_status_string.argtypes = [i]
         lib.sdtw_status_string.restype = ctypes.c_char_p
+        lib.sdtw_forward_noalloc.argtypes = [vp, vp, i, i, i, i, f, i, vp, vp]
+        lib.sdtw_forward_noalloc.restype = i
         lib.sdtw_debug_set_wait.argtypes = [ctypes.c_double, i]
         lib.sdtw_debug_set_wait.restype = None
         _lib = lib
@@ -136,6 +139,15 @@ def sdtw_forward(x, y, gamma, mode, loss, ws, stream=None):
     M = y.shape[1]
     _check(load().sdtw_forward(_f32(x, "x"), _f32(y, "y"), B, N, M, D, float(gamma), _mode(mode),
                                _f32(loss, "loss"), _ptr(ws), ws.numel(), _stream(stream)), "sdtw_forward")
+
+
+def sdtw_forward_noalloc(x, y, gamma, mode, loss, stream=None):
+    """Forward pass without a workspace: the library's static scratch is used
+    (callers that cannot allocate; sizes beyond its 64 MiB are rejected)."""
+    B, N, D = x.shape
+    M = y.shape[1]
+    _check(load().sdtw_forward_noalloc(_f32(x, "x"), _f32(y, "y"), B, N, M, D, float(gamma), _mode(mode),
+                                       _f32(loss, "loss"), _stream(stream)), "sdtw_forward_noalloc")
 
 
 def sdtw_backward(x, y, gamma, mode, grad_loss, grad_x, grad_y, ws, stream=None):

@@ -103,6 +103,27 @@ sdtw_status sdtw_barycenter_step(float* z, float* m, float* v, int t, const floa
                                  float eps, sdtw_mode mode, float* loss_out, void* ws,
                                  size_t ws_bytes, void* stream);
 
+/* Forward pass that allocates nothing and takes no workspace. No page of the
+ * method has a counterpart: it exists for callers that cannot allocate device
+ * memory -- a host program with no device allocator of its own (no PyTorch, no
+ * memory pool), or a latency-critical loop that must not call cudaMalloc/
+ * cudaFree, which synchronize the device. The caller passes inputs and
+ * outputs as in sdtw_forward; the scratch comes from one 64 MiB file-scope
+ * device array inside the library, which every GPU that loads the library
+ * holds until the process exits.
+ *  - Sizes whose forward scratch exceeds 64 MiB return SDTW_ERR_TOO_LARGE
+ *    before any launch (for example B=4, N=M=64 fits; B=32, N=M=512 does not).
+ *  - The first call on each device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - All calls share the array and it keeps the last call's contents; the
+ *    control words are cleared at the start of each call. Calls that overlap
+ *    on the GPU (other streams, other host threads) race on it.
+ *  - No state is left for sdtw_backward, and a device-side wait that runs out
+ *    of time is not reported (the loss is then undefined). */
+sdtw_status sdtw_forward_noalloc(const float* x, const float* y, int B, int N, int M, int D,
+                                 float gamma, sdtw_mode mode, float* loss, void* stream);
+
 /* Synchronizes `stream`, then reports (and clears) the device status word kept
  * in `ws`: SDTW_OK, or SDTW_ERR_TIMEOUT when a DP kernel gave up waiting for a
  * neighbouring tile. */
