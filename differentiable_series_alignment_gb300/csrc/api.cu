@@ -42,14 +42,14 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     const size_t slots = (size_t)skew_slots(N, M) * P;
     size_t o = 0;
     L->status = o; o = align_up(o + sizeof(int));
-    L->ctrl_f = o; L->ctrl_f_bytes = sizeof(int) * (1 + (size_t)P + (size_t)P * NB); o = align_up(o + L->ctrl_f_bytes);
-    L->ctrl_b = o; L->ctrl_b_bytes = sizeof(int) * (1 + (size_t)P * NB); o = align_up(o + L->ctrl_b_bytes);
+    L->ctrl_f = o; L->ctrl_f_bytes = sizeof(int) * (1 + (size_t)P); o = align_up(o + L->ctrl_f_bytes);
+    L->ctrl_b = o; L->ctrl_b_bytes = sizeof(int); o = align_up(o + L->ctrl_b_bytes);
     L->colsum = o; o = align_up(o + sizeof(double) * (size_t)P * NB);
     L->rowsum = o; o = align_up(o + sizeof(double) * (size_t)P);
     L->rowbuf = o; o = align_up(o + sizeof(float) * (size_t)P * M);
     L->losses = o; o = align_up(o + sizeof(float) * (size_t)P);
-    L->edge_f = o; o = align_up(o + sizeof(float) * (size_t)P * NB * M);
-    L->edge_b = o; o = align_up(o + sizeof(float2) * (size_t)P * NB * M);
+    L->edge_f = o; o = align_up(o + sizeof(Slot) * (size_t)P * NB * M);
+    L->edge_b = o; o = align_up(o + 2 * sizeof(Slot) * (size_t)P * NB * M);
     L->vh = o; o = align_up(o + sizeof(float2) * slots);
     L->e = o; o = align_up(o + sizeof(float) * slots);
     L->dsk = o; if (mode == SDTW_UNFUSED) o = align_up(o + sizeof(float) * slots);
@@ -132,15 +132,12 @@ WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamm
     q.Dsk = fused ? nullptr : at<float>(ws, L.dsk);
     q.VH = at<float2>(ws, L.vh);
     q.E = at<float>(ws, L.e);
-    q.edge_f = at<float>(ws, L.edge_f);
-    q.edge_b = at<float2>(ws, L.edge_b);
+    q.edge_f = at<Slot>(ws, L.edge_f);
+    q.edge_b = at<Slot>(ws, L.edge_b);
     int* cf = at<int>(ws, L.ctrl_f);
     q.ticket_f = cf;
     q.done = cf + 1;
-    q.prog_f = cf + 1 + L.P;
-    int* cb = at<int>(ws, L.ctrl_b);
-    q.ticket_b = cb;
-    q.prog_b = cb + 1;
+    q.ticket_b = at<int>(ws, L.ctrl_b);
     q.colsum = at<double>(ws, L.colsum);
     q.rowsum = at<double>(ws, L.rowsum);
     q.rowbuf = at<float>(ws, L.rowbuf);
@@ -163,10 +160,12 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
                         cudaStream_t st)
 {
     const bool fused = (mode == SDTW_FUSED);
+    WaveParams q = wave_params(pr, L, ws, gamma, fused, false);
     SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.status), 0, sizeof(int), st));
     SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_f), 0, L.ctrl_f_bytes, st));
+    if (q.S > 1)  // strip boundary slots start untagged
+        SDTW_CUDA(cudaMemsetAsync(q.edge_f, 0, sizeof(Slot) * (size_t)L.P * q.S * L.M, st));
     if (!fused) SDTW_CUDA(launch_dist_skewed(pr, L.P, L.N, L.M, L.D, at<float>(ws, L.dsk), st));
-    WaveParams q = wave_params(pr, L, ws, gamma, fused, false);
     q.loss = loss_out;
     q.skip_publish = g_skip_publish;
     g_skip_publish = 0;
@@ -176,8 +175,9 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
 
 sdtw_status run_backward(const Problems& pr, const Layout& L, void* ws, float gamma, int mode, cudaStream_t st)
 {
-    SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_b), 0, L.ctrl_b_bytes, st));
     WaveParams q = wave_params(pr, L, ws, gamma, mode == SDTW_FUSED, true);
+    SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_b), 0, L.ctrl_b_bytes, st));
+    if (q.S > 1) SDTW_CUDA(cudaMemsetAsync(q.edge_b, 0, 2 * sizeof(Slot) * (size_t)L.P * q.S * L.M, st));
     SDTW_CUDA(launch_backward(q, st));
     return SDTW_OK;
 }

@@ -138,6 +138,23 @@ __device__ __forceinline__ void sort3(float a, float b, float c, float& lo, floa
     mid = fmaxf(t1, fminf(t2, c));
 }
 
+// A channel slot: a value and the tag that validates it (tag = column + 1;
+// 0 = not written yet). Written and read as one 64-bit access, which is
+// single-copy atomic, so a reader that sees the expected tag also sees the
+// value and neither side needs a fence or a separate ready counter.
+struct __align__(8) Slot {
+    float v;
+    unsigned tag;
+};
+__device__ __forceinline__ void slot_store(Slot* p, float v, unsigned tag) {
+    asm volatile("st.volatile.v2.b32 [%0], {%1, %2};" ::"l"(p), "f"(v), "r"(tag) : "memory");
+}
+__device__ __forceinline__ Slot slot_load(const Slot* p) {
+    Slot s;
+    asm volatile("ld.volatile.v2.b32 {%0, %1}, [%2];" : "=f"(s.v), "=r"(s.tag) : "l"(p) : "memory");
+    return s;
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -21,10 +21,8 @@ struct WaveParams {
     const float* Dsk; // unfused: raw cost, skewed layout; fused: nullptr
     float2* VH;       // (vl, hu) per cell, skewed layout
     float* E;         // alignment matrix, skewed layout (backward output)
-    float* edge_f;    // [P][NB][M]  boundary rows between forward strips
-    float2* edge_b;   // [P][NB][M]  boundary messages between backward strips
-    int* prog_f;      // [P][NB]     forward ready counters
-    int* prog_b;      // [P][NB]     backward ready counters
+    Slot* edge_f;     // [P][S][M]     boundary rows between forward strips (tagged)
+    Slot* edge_b;     // [P][S][M][2]  boundary messages between backward strips (tagged)
     int* ticket_f;    // forward strip ticket
     int* ticket_b;    // backward strip ticket
     int* done;        // [P]         finished forward strips

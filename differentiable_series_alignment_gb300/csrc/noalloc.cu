@@ -52,10 +52,10 @@ FwdCarve carve(int B, int N, int M, bool fused)
     FwdCarve c{};
     size_t o = 0;
     c.status = o; o = up256(o + sizeof(int));
-    c.ctrl = o; c.ctrl_bytes = sizeof(int) * (1 + (size_t)B + (size_t)B * NB); o = up256(o + c.ctrl_bytes);
+    c.ctrl = o; c.ctrl_bytes = sizeof(int) * (1 + (size_t)B); o = up256(o + c.ctrl_bytes);
     c.colsum = o; o = up256(o + sizeof(double) * (size_t)B * NB);
     c.rowbuf = o; o = up256(o + sizeof(float) * (size_t)B * M);
-    c.edge = o; o = up256(o + sizeof(float) * (size_t)B * NB * M);
+    c.edge = o; o = up256(o + sizeof(Slot) * (size_t)B * NB * M);
     c.vh = o; o = up256(o + sizeof(float2) * slots);
     c.dsk = o; if (!fused) o = up256(o + sizeof(float) * slots);
     c.total = o;
@@ -132,14 +132,12 @@ extern "C" sdtw_status sdtw_forward_noalloc(const float* x, const float* y, int 
     q.Dsk = fused ? nullptr : reinterpret_cast<const float*>(ws + c.dsk);
     q.VH = reinterpret_cast<float2*>(ws + c.vh);
     q.E = nullptr;
-    q.edge_f = reinterpret_cast<float*>(ws + c.edge);
+    q.edge_f = reinterpret_cast<Slot*>(ws + c.edge);
     q.edge_b = nullptr;
     int* ctrl = reinterpret_cast<int*>(ws + c.ctrl);
     q.ticket_f = ctrl;
     q.done = ctrl + 1;
-    q.prog_f = ctrl + 1 + B;
     q.ticket_b = nullptr;
-    q.prog_b = nullptr;
     q.colsum = reinterpret_cast<double*>(ws + c.colsum);
     q.rowsum = nullptr;
     q.rowbuf = reinterpret_cast<float*>(ws + c.rowbuf);
@@ -149,9 +147,11 @@ extern "C" sdtw_status sdtw_forward_noalloc(const float* x, const float* y, int 
     q.skip_publish = 0;
     q.accurate = 0;
 
-    // The status word and the tickets, counters and ready flags start at zero.
+    // The status word, the ticket, the counters and the strip boundary slots start at zero.
     if (cudaMemsetAsync(ws + c.status, 0, sizeof(int), st) != cudaSuccess) return SDTW_ERR_CUDA;
     if (cudaMemsetAsync(ws + c.ctrl, 0, c.ctrl_bytes, st) != cudaSuccess) return SDTW_ERR_CUDA;
+    if (q.S > 1 && cudaMemsetAsync(ws + c.edge, 0, sizeof(Slot) * (size_t)B * q.S * M, st) != cudaSuccess)
+        return SDTW_ERR_CUDA;
     if (!fused && launch_dist_skewed(pr, B, N, M, D, reinterpret_cast<float*>(ws + c.dsk), st) != cudaSuccess)
         return SDTW_ERR_CUDA;
     if (launch_forward(q, fused, st) != cudaSuccess) return SDTW_ERR_CUDA;

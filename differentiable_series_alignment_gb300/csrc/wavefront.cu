@@ -11,9 +11,10 @@
 //    column M-1 - (s - (31-l)) (backward). The left (right) neighbour stays in
 //    a register, the upper (lower) neighbour arrives by one warp shuffle.
 //  * A CTA owns a strip of W warps = 32W rows. Adjacent warps exchange the
-//    boundary row through a shared-memory ring with producer/consumer counters.
-//  * Strips exchange their boundary row through global memory with
-//    release/acquire ready counters. Strips are handed out by an atomic ticket
+//    boundary row through a shared-memory ring of tagged slots (value and
+//    column tag in one 64-bit word, so no fence or ready counter is needed).
+//  * Strips exchange their boundary row through tagged slots in global memory,
+//    loaded one group ahead of use. Strips are handed out by an atomic ticket
 //    in dependency order, so a CTA only ever waits on a strip already owned by
 //    a running CTA; this holds whatever the grid size and residency.
 //  * Every wait is bounded (global timer); on expiry the kernel sets the
@@ -32,14 +33,12 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-// Bounded wait on a shared-memory counter. Warp-uniform result.
+// Bounded wait on a shared-memory counter (back-pressure of a ring). Warp-uniform result.
 __device__ __forceinline__ bool wait_smem(const volatile int* cnt, int target, const WaveParams& q) {
     bool ok = true;
     if (*cnt < target) {
         const unsigned long long t0 = global_ns();
         unsigned it = 0;
-        // Back off while waiting: a spinning warp would take issue slots from
-        // the working warps that share its SM sub-partition.
         while (*cnt < target) {
             __nanosleep(32);
             if ((++it & 7u) == 0) {
@@ -48,23 +47,33 @@ __device__ __forceinline__ bool wait_smem(const volatile int* cnt, int target, c
             }
         }
     }
-    ok = __shfl_sync(kFull, ok, 0);
-    __threadfence_block();
-    return ok;
+    return __shfl_sync(kFull, ok, 0);
 }
 
-// Bounded wait on a global ready counter (acquire). Warp-uniform result.
-__device__ __forceinline__ bool wait_global(const int* cnt, int target, const WaveParams& q) {
-    bool ok = true;
-    if (ld_acquire_gpu(cnt) < target) {
-        const unsigned long long t0 = global_ns();
-        while (ld_acquire_gpu(cnt) < target) {
-            __nanosleep(64);
-            if (ld_volatile_global(q.status) != 0) { ok = false; break; }
-            if (global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); ok = false; break; }
+// Wait until every lane's slot (or pair of slots) carries its expected tag,
+// reloading the lanes that do not yet. want == 0 marks a lane with nothing to
+// check. Bounded; warp-uniform result.
+template <int NS>
+__device__ __forceinline__ bool validate(Slot (&cur)[NS], const Slot* src, unsigned want, const WaveParams& q) {
+    bool mine = true;
+#pragma unroll
+    for (int k = 0; k < NS; ++k) mine = mine && (want == 0u || cur[k].tag == want);
+    if (__all_sync(kFull, mine)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (!mine) {
+#pragma unroll
+            for (int k = 0; k < NS; ++k) cur[k] = slot_load(src + k);
+            mine = true;
+#pragma unroll
+            for (int k = 0; k < NS; ++k) mine = mine && (cur[k].tag == want);
         }
+        if (__all_sync(kFull, mine)) return true;
+        __nanosleep(20);
+        bool bad = ld_volatile_global(q.status) != 0;
+        if (!bad && global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); bad = true; }
+        if (__any_sync(kFull, bad)) return false;
     }
-    return __shfl_sync(kFull, ok, 0);
 }
 
 struct FusedSmem {
@@ -91,15 +100,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int W = q.W;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float* ring = reinterpret_cast<float*>(smem_raw);                    // [W][kRing]
-    volatile int* prod = reinterpret_cast<volatile int*>(ring + W * kRing);
-    volatile int* cons = prod + W;
+    Slot* ring = reinterpret_cast<Slot*>(smem_raw);                      // [W][kRing], by producer warp
+    volatile int* cons = reinterpret_cast<volatile int*>(ring + W * kRing);  // [W] columns consumed
     __shared__ int s_tk;
     __shared__ double s_red[kMaxWarps];
     __shared__ int s_last;
 
     if (threadIdx.x == 0) s_tk = atomicAdd(q.ticket_f, 1);
-    if (threadIdx.x < W) { prod[threadIdx.x] = 0; cons[threadIdx.x] = 0; }
+    if (threadIdx.x < W) cons[threadIdx.x] = 0;
+    for (int k = threadIdx.x; k < W * kRing; k += blockDim.x) ring[k].tag = 0u;
     __syncthreads();
 
     const int tk = s_tk;
@@ -141,18 +150,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams
         const long long sk = skew_index(N, M, p, rb, 0, lane);
         float2* vhp = q.VH + sk;
         const float* dp = FUSED ? nullptr : q.Dsk + sk;
-        float* ring_out = ring + warp * kRing;
-        const float* ring_in = ring + (warp - 1) * kRing;
-        float* edge_out = q.edge_f + ((size_t)p * q.NB + strip) * M;
-        const float* edge_in = q.edge_f + ((size_t)p * q.NB + strip - 1) * M;
-        int* prog_out = q.prog_f + (size_t)p * q.NB + strip;
-        const int* prog_in = q.prog_f + (size_t)p * q.NB + strip - 1;
-        const bool publish_ok = !(q.skip_publish && strip == 0);
-        // Boundary row out of this warp (lane 31): generic pointer into the
-        // shared ring or the global edge buffer.
-        const bool chan_lane = has_bot && lane == 31;
-        float* chan_out = bot_global ? edge_out : ring_out;
+        Slot* ring_out = ring + warp * kRing;
+        const Slot* ring_in = ring + (warp - 1) * kRing;
+        Slot* edge_out = q.edge_f + ((size_t)p * q.S + strip) * M;
+        const Slot* edge_in = q.edge_f + ((size_t)p * q.S + strip - 1) * M;
+        // Boundary row out of this warp (lane 31), tagged column + 1: into the
+        // shared ring of the next warp or the global edge buffer of the next strip.
+        const bool chan_lane = has_bot && lane == 31 && !(q.skip_publish && strip == 0 && bot_global);
+        Slot* chan_out = bot_global ? edge_out : ring_out;
         const int chan_mask = bot_global ? 0x7fffffff : (kRing - 1);
+        // Upper-boundary values of the first group (global channel: loaded one group ahead).
+        Slot nxt[1];
+        nxt[0].v = 0.f;
+        nxt[0].tag = 0u;
+        if (top_global && lane < kGroup && lane < M) nxt[0] = slot_load(edge_in + lane);
 
         float h_prev = 0.f, v_prev = 0.f;
         float dn[kGroup];
@@ -211,18 +222,25 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams
                 __syncwarp();
             }
 
-            // Upper-neighbour values for lane 0: columns [s0, s0+kGroup).
+            // Upper-neighbour values for lane 0: lane q holds column s0 + q.
             float topv = 0.f;
             bool ok = true;
             if (has_top && s0 < M) {
-                const int need = min(s0 + kGroup, M);
+                const int col = s0 + lane;
+                const unsigned want = (lane < kGroup && col < M) ? (unsigned)(col + 1) : 0u;
+                Slot cur[1];
                 if (top_global) {
-                    ok = wait_global(prog_in, need, q);
-                    if (ok && lane < kGroup && s0 + lane < M) topv = __ldcg(edge_in + s0 + lane);
+                    cur[0] = nxt[0];
+                    ok = validate(cur, edge_in + col, want, q);
+                    const int ncol = col + kGroup;
+                    if (ok && lane < kGroup && ncol < M) nxt[0] = slot_load(edge_in + ncol);
                 } else {
-                    ok = wait_smem(&prod[warp - 1], need, q);
-                    if (ok && lane < kGroup) topv = ring_in[(s0 + lane) & (kRing - 1)];
+                    cur[0].v = 0.f;
+                    cur[0].tag = 0u;
+                    if (want) cur[0] = slot_load(ring_in + (col & (kRing - 1)));
+                    ok = validate(cur, ring_in + (col & (kRing - 1)), want, q);
                 }
+                topv = cur[0].v;
             }
             if (ok && has_bot && !bot_global) {
                 const int need = s0 + kGroup - 31 - kRing;  // ring slots this group overwrites are free
@@ -253,22 +271,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams
                 c0 = col0 ? d : c0;
                 vhp[(long long)s * 32] = make_float2(svl, shu);
                 const bool valid = (unsigned)j < (unsigned)M;
-                if (chan_lane && valid) chan_out[j & chan_mask] = h;
+                if (chan_lane && valid) slot_store(chan_out + (j & chan_mask), h, (unsigned)(j + 1));
                 if (last_lane && valid) rowbuf[j] = h;
                 h_prev = h;
                 v_prev = v;
             }
 
-            if (has_bot && lane == 31) {
-                int cnt = min(max(s0 + kGroup - 31, 0), M);
-                if (g == nG - 1) cnt = M;
-                if (bot_global) {
-                    if (publish_ok) st_release_gpu(prog_out, cnt);
-                } else {
-                    __threadfence_block();
-                    prod[warp] = cnt;
-                }
-            }
             if (has_top && !top_global && lane == 0) cons[warp - 1] = min(s0 + kGroup, M);
         }
     }
@@ -313,13 +321,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int W = q.W;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float2* ring = reinterpret_cast<float2*>(smem_raw);                   // [W][kRing], by producer
-    volatile int* prod = reinterpret_cast<volatile int*>(ring + W * kRing);
-    volatile int* cons = prod + W;
+    Slot* ring = reinterpret_cast<Slot*>(smem_raw);                       // [W][kRing][2], by producer warp
+    volatile int* cons = reinterpret_cast<volatile int*>(ring + 2 * W * kRing);  // [W] slots consumed
     __shared__ int s_tk;
 
     if (threadIdx.x == 0) s_tk = atomicAdd(q.ticket_b, 1);
-    if (threadIdx.x < W) { prod[threadIdx.x] = 0; cons[threadIdx.x] = 0; }
+    if (threadIdx.x < W) cons[threadIdx.x] = 0;
+    for (int k = threadIdx.x; k < 2 * W * kRing; k += blockDim.x) ring[k].tag = 0u;
     __syncthreads();
 
     const int tk = s_tk;
@@ -338,17 +346,23 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
     const long long sk = skew_index(N, M, p, rb, 0, lane);
     const float2* vhp = q.VH + sk;
     float* ep = q.E + sk;
-    float2* ring_out = ring + warp * kRing;
-    const float2* ring_in = ring + (warp + 1) * kRing;
-    float2* edge_out = q.edge_b + ((size_t)p * q.NB + strip) * M;
-    const float2* edge_in = q.edge_b + ((size_t)p * q.NB + strip + 1) * M;
-    int* prog_out = q.prog_b + (size_t)p * q.NB + strip;
-    const int* prog_in = q.prog_b + (size_t)p * q.NB + strip + 1;
-    // Messages to the row above (lane 0): generic pointer into ring or edge buffer.
-    // Slot k holds column M-1-k.
+    Slot* ring_out = ring + 2 * warp * kRing;
+    const Slot* ring_in = ring + 2 * (warp + 1) * kRing;
+    Slot* edge_out = q.edge_b + 2 * ((size_t)p * q.S + strip) * M;
+    const Slot* edge_in = q.edge_b + 2 * ((size_t)p * q.S + strip + 1) * M;
+    // Messages to the row above (lane 0), slot k = column M-1-k, a pair of
+    // tagged slots (msg_up, msg_diag) with tag k + 1: into the shared ring of
+    // the warp above or the global edge buffer of the strip above.
     const bool chan_lane = has_above && lane == 0;
-    float2* chan_out = above_global ? edge_out : ring_out;
+    Slot* chan_out = above_global ? edge_out : ring_out;
     const int chan_mask = above_global ? 0x7fffffff : (kRing - 1);
+    Slot nxt[2];
+    nxt[0].v = nxt[1].v = -kBig;
+    nxt[0].tag = nxt[1].tag = 0u;
+    if (below_global && lane < kGroup) {
+        const int k = lane - off;
+        if (k >= 0 && k < M) { nxt[0] = slot_load(edge_in + 2 * k); nxt[1] = slot_load(edge_in + 2 * k + 1); }
+    }
 
     float ml = -kBig, su = -kBig, sd = -kBig, rd_hold = -kBig;
     float2 vn[kGroup];
@@ -365,18 +379,30 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
 #pragma unroll
             for (int u = 0; u < kGroup; ++u) vn[u] = vhp[(long long)(T - 1 - (t0 + kGroup + u)) * 32];
         }
-        // Messages of the row below for lane 31: slots [k0, k0+kGroup).
+        // Messages of the row below for lane 31: lane q holds slot k0 + q.
         float2 botv = make_float2(-kBig, -kBig);
         bool ok = true;
         if (has_below && k0 + kGroup > 0 && k0 < M) {
-            const int need = min(k0 + kGroup, M);
+            const int k = k0 + lane;
+            const unsigned want = (lane < kGroup && k >= 0 && k < M) ? (unsigned)(k + 1) : 0u;
+            Slot cur[2];
             if (below_global) {
-                ok = wait_global(prog_in, need, q);
-                if (ok && lane < kGroup && k0 + lane >= 0 && k0 + lane < M) botv = __ldcg(edge_in + k0 + lane);
+                cur[0] = nxt[0];
+                cur[1] = nxt[1];
+                ok = validate(cur, edge_in + 2 * k, want, q);
+                const int nk = k + kGroup;
+                if (ok && lane < kGroup && nk >= 0 && nk < M) {
+                    nxt[0] = slot_load(edge_in + 2 * nk);
+                    nxt[1] = slot_load(edge_in + 2 * nk + 1);
+                }
             } else {
-                ok = wait_smem(&prod[warp + 1], need, q);
-                if (ok && lane < kGroup && k0 + lane >= 0) botv = ring_in[(k0 + lane) & (kRing - 1)];
+                const Slot* src = ring_in + 2 * (k & (kRing - 1));
+                cur[0].tag = cur[1].tag = 0u;
+                cur[0].v = cur[1].v = -kBig;
+                if (want) { cur[0] = slot_load(src); cur[1] = slot_load(src + 1); }
+                ok = validate(cur, src, want, q);
             }
+            if (want) botv = make_float2(cur[0].v, cur[1].v);
         }
         if (ok && has_above && !above_global) {
             const int need = k0 + kGroup - 31 - kRing;
@@ -412,19 +438,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
             su = lE + (-st.y - Lz);
             sd = lE - Lz;
             ep[(long long)t * 32] = ex2(lE);
-            if (chan_lane && (unsigned)j < (unsigned)M) chan_out[(M - 1 - j) & chan_mask] = make_float2(su, sd);
-        }
-
-        if (has_above && lane == 0) {
-            int cnt = min(max(k0 + kGroup - 31, 0), M);
-            if (g == nG - 1) cnt = M;
-            if (above_global) {
-                st_release_gpu(prog_out, cnt);
-            } else {
-                __threadfence_block();
-                prod[warp] = cnt;
+            if (chan_lane && (unsigned)j < (unsigned)M) {
+                const int k = M - 1 - j;
+                Slot* dst = chan_out + 2 * (k & chan_mask);
+                slot_store(dst, su, (unsigned)(k + 1));
+                slot_store(dst + 1, sd, (unsigned)(k + 1));
             }
         }
+
         if (has_below && !below_global && lane == 31) cons[warp + 1] = min(max(k0 + kGroup, 0), M);
     }
 }
@@ -434,8 +455,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
 // ---------------------------------------------------------------------------
 size_t wave_smem_fixed(int W, bool backward)
 {
-    const size_t ring = (size_t)W * kRing * (backward ? sizeof(float2) : sizeof(float));
-    const size_t ctr = 2 * (size_t)W * sizeof(int);
+    const size_t ring = (size_t)W * kRing * sizeof(Slot) * (backward ? 2 : 1);
+    const size_t ctr = (size_t)W * sizeof(int);
     return (ring + ctr + 15) & ~(size_t)15;
 }
 
