@@ -198,15 +198,17 @@ sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void
     g.coef = coef;
     g.omod = B;
     g.accumulate = accumulate;
+    const bool simt = env_int("SDTW_GRAD_SIMT", 0) != 0;
+    int* status = at<int>(ws, L.status);
     if (out_x) {
         g.out = out_x;
         g.out_stride = (long long)L.N * L.D;
-        SDTW_CUDA(launch_grad_rows(g, st));
+        SDTW_CUDA(simt ? launch_grad_rows(g, st) : launch_grad_tc(g, false, status, st));
     }
     if (out_y) {
         g.out = out_y;
         g.out_stride = (long long)L.M * L.D;
-        SDTW_CUDA(launch_grad_cols(g, st));
+        SDTW_CUDA(simt ? launch_grad_cols(g, st) : launch_grad_tc(g, true, status, st));
     }
     return SDTW_OK;
 }

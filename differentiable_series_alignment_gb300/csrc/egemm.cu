@@ -1,0 +1,315 @@
+// egemm.cu -- input gradients as tensor-core contractions of the alignment matrix.
+//
+//   grad_x[i,:] = g * 2 * (sum_j E[i,j] x_i - sum_j E[i,j] y_j)    (rows:    E   . [Y | 1])
+//   grad_y[j,:] = g * 2 * (sum_i E[i,j] y_j - sum_i E[i,j] x_i)    (columns: E^T . [X | 1])
+//
+// One CTA computes 128 output rows (tcgen05 M = 128) against all D+1 output
+// columns (the extra column of ones yields the row or column sums of E in the
+// same MMA). The reduction runs over the other sequence in K-tiles of 32. Each
+// tile is loaded from the skewed alignment matrix (or x / y) by the CTA's
+// threads, split into tf32 hi + lo parts (round to nearest) and stored in the
+// 128-byte-swizzled K-major layout; one thread issues the 3xTF32 products
+// hi*hi + lo*hi + hi*lo with tcgen05.mma (fp32 accumulation in tensor memory),
+// committed to an mbarrier. Two smem stages let the loads of tile k+1 overlap
+// the MMAs of tile k. The epilogue reads the accumulators back with tcgen05.ld.
+//
+// Precision: each split product carries ~2^-21 relative error, so E . y keeps
+// ~1e-6 relative accuracy; the gradient is a difference of two such sums that
+// can cancel by ~100x, which leaves it well inside rel 1e-3.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sdtw {
+
+namespace {
+
+constexpr int kBM = 128;       // output rows per CTA (MMA M)
+constexpr int kBK = 32;        // reduction elements per K-tile (128 bytes of fp32 per smem row)
+constexpr int kThreads = 128;  // 4 warps, one per TMEM lane quarter
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Byte offset of element (r, k) in a K-major tile of 32 fp32 per row, 128-byte
+// swizzle: 16-byte chunk index XOR (row mod 8) inside each 8-row, 1 KiB atom.
+__device__ __forceinline__ uint32_t sw128(int r, int k) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k >> 2) ^ r) & 7) << 4) + (k & 3) * 4);
+}
+
+// fp32 -> tf32 hi (round to nearest) and the tf32-rounded remainder.
+__device__ __forceinline__ void split_tf32(float v, float& hi, float& lo) {
+    hi = __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
+    const float r = v - hi;
+    lo = __uint_as_float((__float_as_uint(r) + 0x1000u) & 0xFFFFE000u);
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1 KiB apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;              // leading byte offset (unused with swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;              // descriptor version
+    d |= (uint64_t)2 << 61;              // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: D fp32, A and B tf32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the given phase parity of an mbarrier (all threads).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_test(bar, parity)) {
+        if (global_ns() - t0 > 2000000000ull) {
+            atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(r[q]);
+}
+
+// Stores the split value into the hi and lo tiles of a stage.
+__device__ __forceinline__ void put(unsigned char* hi_tile, unsigned char* lo_tile, int r, int k, float v) {
+    float h, l;
+    split_tf32(v, h, l);
+    const uint32_t o = sw128(r, k);
+    *reinterpret_cast<float*>(hi_tile + o) = h;
+    *reinterpret_cast<float*>(lo_tile + o) = l;
+}
+
+// COLS = false: grad_x rows (A = E rows i, K = j, B = [Y | 1]).
+// COLS = true : grad_y rows (A = E columns j, K = i, B = [X | 1]).
+template <bool COLS>
+__global__ void __launch_bounds__(kThreads, 1) egemm_kernel(const GradParams g, int n_total, int nstages, int* status)
+{
+    extern __shared__ unsigned char smem_dyn[];
+    __shared__ uint64_t s_bar[2];
+    __shared__ uint32_t s_tmem;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int p = blockIdx.y;
+    const int m0 = blockIdx.x * kBM;
+    const int N = g.N, M = g.M, D = g.D;
+    const int rows = COLS ? M : N;     // output rows
+    const int kdim = COLS ? N : M;     // reduction length
+    const float* Ekp = g.E + skew_index(N, M, p, 0, 0, 0);
+    const float* xb = g.pr.x(p);
+    const float* yb = g.pr.y(p);
+    const float* vb = COLS ? xb : yb;  // B operand rows (the other sequence)
+
+    // Stage layout (1 KiB aligned): A hi, A lo (128 x 128 B), B hi, B lo (n_total x 128 B).
+    const uint32_t a_bytes = kBM * 128, b_bytes = (uint32_t)n_total * 128;
+    const uint32_t stage_bytes = 2 * a_bytes + 2 * b_bytes;
+    unsigned char* base =
+        smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+
+    if (tid == 0) {
+        mbar_init(smem_u32(&s_bar[0]), 1);
+        mbar_init(smem_u32(&s_bar[1]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    int ncols = 32;
+    while (ncols < n_total) ncols <<= 1;
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(ncols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = s_tmem;
+
+    const int nK = (kdim + kBK - 1) / kBK;
+    uint32_t phase[2] = {0u, 0u};
+    bool ok = true;
+    for (int kt = 0; kt < nK; ++kt) {
+        const int s = (nstages == 2) ? (kt & 1) : 0;
+        const uint32_t bar = smem_u32(&s_bar[s]);
+        if (kt >= nstages) {  // the MMAs that last read this stage have finished
+            ok = mbar_wait(bar, phase[s], status) && ok;
+            phase[s] ^= 1u;
+        }
+        unsigned char* A_hi = base + s * stage_bytes;
+        unsigned char* A_lo = A_hi + a_bytes;
+        unsigned char* B_hi = A_lo + a_bytes;
+        unsigned char* B_lo = B_hi + b_bytes;
+        const int k0 = kt * kBK;
+
+        // ---- A tile from the skewed alignment matrix (zero outside the matrix)
+        if (!COLS) {
+            // rows i = m0 + 32w + lane (block rb = m0/32 + w), columns j = k0 + c, slot t = j + lane
+            const int rb = (m0 >> 5) + warp;
+            const float* blk = Ekp + (size_t)rb * skew_T(M) * 32;
+            const int i = m0 + 32 * warp + lane;
+            for (int tt = 0; tt < 63; ++tt) {
+                const int c = tt - lane;
+                if (c < 0 || c >= kBK) continue;
+                const int j = k0 + c;
+                const float v = (i < N && j < M && rb * 32 < N) ? blk[(size_t)(k0 + tt) * 32 + lane] : 0.f;
+                put(A_hi, A_lo, 32 * warp + lane, c, v);
+            }
+        } else {
+            // rows j = m0 + r, K index i = k0 + lane (block rb = k0/32), slot t = j + lane
+            const int rb = k0 >> 5;
+            const float* blk = Ekp + (size_t)rb * skew_T(M) * 32;
+            const int i = k0 + lane;
+            for (int tt = warp; tt < kBM + 31; tt += 4) {
+                const int r = tt - lane;
+                if (r < 0 || r >= kBM) continue;
+                const int j = m0 + r;
+                const float v = (i < N && j < M) ? blk[(size_t)(m0 + tt) * 32 + lane] : 0.f;
+                put(A_hi, A_lo, r, lane, v);
+            }
+        }
+        // ---- B tile: row n < D holds the other sequence's coordinate n, row D holds ones
+        for (int idx = tid; idx < n_total * kBK; idx += kThreads) {
+            const int k = idx / n_total, n = idx - k * n_total;
+            const int kk = k0 + k;
+            float v = 0.f;
+            if (kk < kdim) v = (n < D) ? vb[(size_t)kk * D + n] : (n == D ? 1.f : 0.f);
+            put(B_hi, B_lo, n, k, v);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+
+        if (tid == 0) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t ah = smem_u32(A_hi), al = smem_u32(A_lo), bh = smem_u32(B_hi), bl = smem_u32(B_lo);
+            for (int n0 = 0; n0 < n_total; n0 += 256) {
+                const int nn = min(256, n_total - n0);
+                const uint32_t id = idesc_tf32(kBM, nn);
+                const uint32_t d = tmem + (uint32_t)n0;
+                const uint32_t boff = (uint32_t)n0 * 128;  // n0 is a multiple of 8 rows
+#pragma unroll
+                for (int ks = 0; ks < kBK / 8; ++ks) {
+                    const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
+                    const uint32_t first = (kt > 0 || ks > 0) ? 1u : 0u;
+                    mma_tf32(d, sdesc(ah + ko), sdesc(bh + boff + ko), id, first);
+                    mma_tf32(d, sdesc(al + ko), sdesc(bh + boff + ko), id, 1u);
+                    mma_tf32(d, sdesc(ah + ko), sdesc(bl + boff + ko), id, 1u);
+                }
+            }
+            mma_commit(bar);
+        }
+    }
+    // The last commit covers every MMA issued before it.
+    {
+        const int s = (nstages == 2) ? ((nK - 1) & 1) : 0;
+        ok = mbar_wait(smem_u32(&s_bar[s]), phase[s], status) && ok;
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+    // ---- epilogue: warp w holds output rows m0 + 32w + lane in TMEM lanes 32w..32w+31
+    const int row = m0 + 32 * warp + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    float sums[16];
+    tmem_ld16(trow + (uint32_t)(D & ~15), sums);
+    const float sum = sums[D & 15];
+    const float w = g.coef * 2.f * (g.grad_loss ? g.grad_loss[p % g.wmod] : 1.f);
+    const float* own = (COLS ? yb : xb) + (size_t)row * D;
+    float* out = g.out + (long long)(p % g.omod) * g.out_stride + (size_t)row * D;
+    for (int c0 = 0; c0 < D; c0 += 16) {
+        float acc[16];
+        tmem_ld16(trow + (uint32_t)c0, acc);
+        if (ok && row < rows) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int n = c0 + q;
+                if (n < D) {
+                    const float val = w * (sum * own[n] - acc[q]);
+                    out[n] = g.accumulate ? out[n] + val : val;
+                }
+            }
+        }
+    }
+
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+    }
+}
+
+}  // namespace
+
+static int egemm_stages(int D)
+{
+    const int n_total = ((D + 1 + 15) / 16) * 16;
+    const size_t stage = 2 * (size_t)kBM * 128 + 2 * (size_t)n_total * 128;
+    return (1024 + 2 * stage <= 220 * 1024) ? 2 : 1;
+}
+
+size_t egemm_smem_bytes(int D)
+{
+    const int n_total = ((D + 1 + 15) / 16) * 16;
+    const size_t stage = 2 * (size_t)kBM * 128 + 2 * (size_t)n_total * 128;
+    return 1024 + (size_t)egemm_stages(D) * stage;
+}
+
+cudaError_t launch_grad_tc(const GradParams& g, bool cols, int* status, cudaStream_t st)
+{
+    const int n_total = ((g.D + 1 + 15) / 16) * 16;
+    const int stages = egemm_stages(g.D);
+    const size_t smem = egemm_smem_bytes(g.D);
+    const int rows = cols ? g.M : g.N;
+    dim3 grid((rows + kBM - 1) / kBM, g.P);
+    cudaError_t e;
+    if (cols) {
+        e = cudaFuncSetAttribute(egemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        egemm_kernel<true><<<grid, kThreads, smem, st>>>(g, n_total, stages, status);
+    } else {
+        e = cudaFuncSetAttribute(egemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        egemm_kernel<false><<<grid, kThreads, smem, st>>>(g, n_total, stages, status);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace sdtw
