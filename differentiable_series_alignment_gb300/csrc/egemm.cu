@@ -120,35 +120,110 @@ __device__ __forceinline__ void put(unsigned char* hi_tile, unsigned char* lo_ti
     *reinterpret_cast<float*>(lo_tile + o) = l;
 }
 
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// One TMA bulk copy global -> shared (16-byte aligned addresses, size multiple of 16).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Skewed rows of E that one K-tile needs, per row block.
+//   rows (grad_x): for each of the 4 row blocks, slots t in [k0, k0+63)   -> 64 rows copied
+//   cols (grad_y): one row block k0/32, slots t in [m0, m0+159)           -> 160 rows copied
+template <bool COLS>
+struct Raw {
+    static constexpr int kRows = COLS ? 160 : 4 * 64;
+    static constexpr uint32_t kBytes = kRows * 128;
+};
+
+// Issue the copies of K-tile kt into raw buffer (A via bulk copies completed on
+// `bar`, B via 4-byte cp.async in the calling thread's async group).
+template <bool COLS>
+__device__ __forceinline__ void issue_tile(const float* Ekp, const float* vb, int N, int M, int D, int T, int m0,
+                                           int kt, unsigned char* rawA, float* rawB, uint32_t bar, int tid)
+{
+    const int k0 = kt * kBK;
+    const int kdim = COLS ? N : M;
+    if (tid == 0) {
+        uint32_t bytes = 0;
+        const int NB = (N + 31) / 32;
+        if (!COLS) {
+            for (int b = 0; b < 4; ++b) {
+                const int rb = (m0 >> 5) + b;
+                if (rb >= NB) break;
+                const int rows = min(64, T - k0);
+                bytes += rows * 128;
+            }
+        } else {
+            bytes = (uint32_t)min(160, T - m0) * 128;
+        }
+        mbar_expect_tx(bar, bytes);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (!COLS) {
+            for (int b = 0; b < 4; ++b) {
+                const int rb = (m0 >> 5) + b;
+                if (rb >= NB) break;
+                const int rows = min(64, T - k0);
+                bulk_g2s(smem_u32(rawA + b * 64 * 128), Ekp + ((size_t)rb * T + k0) * 32, rows * 128, bar);
+            }
+        } else {
+            const int rb = k0 >> 5;
+            const int rows = min(160, T - m0);
+            bulk_g2s(smem_u32(rawA), Ekp + ((size_t)rb * T + m0) * 32, rows * 128, bar);
+        }
+    }
+    // B rows k0..k0+31 of the other sequence (D floats each, contiguous)
+    const int nrow = min(kBK, kdim - k0);
+    const int nval = nrow * D;
+    const float* src = vb + (size_t)k0 * D;
+    const uint32_t dst = smem_u32(rawB);
+    for (int e = tid; e < nval; e += kThreads) cp_async4(dst + 4u * e, src + e);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 // COLS = false: grad_x rows (A = E rows i, K = j, B = [Y | 1]).
 // COLS = true : grad_y rows (A = E columns j, K = i, B = [X | 1]).
 template <bool COLS>
-__global__ void __launch_bounds__(kThreads, 1) egemm_kernel(const GradParams g, int n_total, int nstages, int* status)
+__global__ void __launch_bounds__(kThreads, 1)
+    egemm_kernel(const GradParams g, int n_total, int tstages, int rstages, int* status)
 {
     extern __shared__ unsigned char smem_dyn[];
-    __shared__ uint64_t s_bar[2];
+    __shared__ uint64_t s_bar[2];   // MMA completion per tile stage
+    __shared__ uint64_t s_raw[2];   // bulk-copy completion per raw buffer
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int p = blockIdx.y;
     const int m0 = blockIdx.x * kBM;
-    const int N = g.N, M = g.M, D = g.D;
+    const int N = g.N, M = g.M, D = g.D, T = skew_T(M);
     const int rows = COLS ? M : N;     // output rows
     const int kdim = COLS ? N : M;     // reduction length
+    const int NB = (N + 31) / 32;
     const float* Ekp = g.E + skew_index(N, M, p, 0, 0, 0);
     const float* xb = g.pr.x(p);
     const float* yb = g.pr.y(p);
     const float* vb = COLS ? xb : yb;  // B operand rows (the other sequence)
 
-    // Stage layout (1 KiB aligned): A hi, A lo (128 x 128 B), B hi, B lo (n_total x 128 B).
+    // Shared memory (1 KiB aligned): tile stages [A hi | A lo | B hi | B lo], then raw buffers [A | B].
     const uint32_t a_bytes = kBM * 128, b_bytes = (uint32_t)n_total * 128;
     const uint32_t stage_bytes = 2 * a_bytes + 2 * b_bytes;
-    unsigned char* base =
-        smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+    const uint32_t rawA_bytes = Raw<COLS>::kBytes, rawB_bytes = ((uint32_t)kBK * D * 4 + 127) & ~127u;
+    unsigned char* base = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+    unsigned char* raw0 = base + tstages * stage_bytes;
 
     if (tid == 0) {
-        mbar_init(smem_u32(&s_bar[0]), 1);
-        mbar_init(smem_u32(&s_bar[1]), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&s_bar[b]), 1);
+            mbar_init(smem_u32(&s_raw[b]), 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     int ncols = 32;
@@ -165,57 +240,67 @@ __global__ void __launch_bounds__(kThreads, 1) egemm_kernel(const GradParams g, 
     const uint32_t tmem = s_tmem;
 
     const int nK = (kdim + kBK - 1) / kBK;
-    uint32_t phase[2] = {0u, 0u};
+    uint32_t mma_phase[2] = {0u, 0u}, raw_phase[2] = {0u, 0u};
     bool ok = true;
+    auto rawA = [&](int r) { return raw0 + r * (rawA_bytes + rawB_bytes); };
+    auto rawB = [&](int r) { return reinterpret_cast<float*>(raw0 + r * (rawA_bytes + rawB_bytes) + rawA_bytes); };
+
+    issue_tile<COLS>(Ekp, vb, N, M, D, T, m0, 0, rawA(0), rawB(0), smem_u32(&s_raw[0]), tid);
     for (int kt = 0; kt < nK; ++kt) {
-        const int s = (nstages == 2) ? (kt & 1) : 0;
-        const uint32_t bar = smem_u32(&s_bar[s]);
-        if (kt >= nstages) {  // the MMAs that last read this stage have finished
-            ok = mbar_wait(bar, phase[s], status) && ok;
-            phase[s] ^= 1u;
+        const int r = (rstages == 2) ? (kt & 1) : 0;
+        const int s = (tstages == 2) ? (kt & 1) : 0;
+        // raw data of tile kt: the bulk copy (mbarrier) and this thread's cp.async group
+        ok = mbar_wait(smem_u32(&s_raw[r]), raw_phase[r], status) && ok;
+        raw_phase[r] ^= 1u;
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
+        if (rstages == 2 && kt + 1 < nK)  // prefetch tile kt+1 into the other raw buffer
+            issue_tile<COLS>(Ekp, vb, N, M, D, T, m0, kt + 1, rawA(r ^ 1), rawB(r ^ 1), smem_u32(&s_raw[r ^ 1]), tid);
+        if (kt >= tstages) {  // the MMAs that last read this tile stage have finished
+            ok = mbar_wait(smem_u32(&s_bar[s]), mma_phase[s], status) && ok;
+            mma_phase[s] ^= 1u;
         }
         unsigned char* A_hi = base + s * stage_bytes;
         unsigned char* A_lo = A_hi + a_bytes;
         unsigned char* B_hi = A_lo + a_bytes;
         unsigned char* B_lo = B_hi + b_bytes;
         const int k0 = kt * kBK;
+        const float* ra = reinterpret_cast<const float*>(rawA(r));
+        const float* rbv = rawB(r);
 
-        // ---- A tile from the skewed alignment matrix (zero outside the matrix)
+        // ---- A tile: un-skew and split (zero outside the matrix)
         if (!COLS) {
-            // rows i = m0 + 32w + lane (block rb = m0/32 + w), columns j = k0 + c, slot t = j + lane
+            // warp w: row block m0/32 + w; lane = row; raw row tt holds slot k0 + tt; column c = tt - lane
             const int rb = (m0 >> 5) + warp;
-            const float* blk = Ekp + (size_t)rb * skew_T(M) * 32;
             const int i = m0 + 32 * warp + lane;
-            for (int tt = 0; tt < 63; ++tt) {
-                const int c = tt - lane;
-                if (c < 0 || c >= kBK) continue;
+            const float* rw = ra + warp * 64 * 32;
+#pragma unroll 8
+            for (int c = 0; c < kBK; ++c) {
                 const int j = k0 + c;
-                const float v = (i < N && j < M && rb * 32 < N) ? blk[(size_t)(k0 + tt) * 32 + lane] : 0.f;
+                const float v = (rb < NB && i < N && j < M) ? rw[(c + lane) * 32 + lane] : 0.f;
                 put(A_hi, A_lo, 32 * warp + lane, c, v);
             }
         } else {
-            // rows j = m0 + r, K index i = k0 + lane (block rb = k0/32), slot t = j + lane
-            const int rb = k0 >> 5;
-            const float* blk = Ekp + (size_t)rb * skew_T(M) * 32;
+            // raw row tt holds slot m0 + tt of block k0/32; lane = K index i - k0; output row r = tt - lane
             const int i = k0 + lane;
-            for (int tt = warp; tt < kBM + 31; tt += 4) {
-                const int r = tt - lane;
-                if (r < 0 || r >= kBM) continue;
-                const int j = m0 + r;
-                const float v = (i < N && j < M) ? blk[(size_t)(m0 + tt) * 32 + lane] : 0.f;
-                put(A_hi, A_lo, r, lane, v);
+#pragma unroll 4
+            for (int rr = warp; rr < kBM; rr += 4) {
+                const int j = m0 + rr;
+                const float v = (i < N && j < M) ? ra[(rr + lane) * 32 + lane] : 0.f;
+                put(A_hi, A_lo, rr, lane, v);
             }
         }
-        // ---- B tile: row n < D holds the other sequence's coordinate n, row D holds ones
+        // ---- B tile: row n < D holds coordinate n of the other sequence, row D holds ones
         for (int idx = tid; idx < n_total * kBK; idx += kThreads) {
             const int k = idx / n_total, n = idx - k * n_total;
-            const int kk = k0 + k;
             float v = 0.f;
-            if (kk < kdim) v = (n < D) ? vb[(size_t)kk * D + n] : (n == D ? 1.f : 0.f);
+            if (k0 + k < kdim) v = (n < D) ? rbv[k * D + n] : (n == D ? 1.f : 0.f);
             put(B_hi, B_lo, n, k, v);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
+        if (rstages == 1 && kt + 1 < nK)  // single raw buffer: refill only after it has been read
+            issue_tile<COLS>(Ekp, vb, N, M, D, T, m0, kt + 1, rawA(0), rawB(0), smem_u32(&s_raw[0]), tid);
 
         if (tid == 0) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -224,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) egemm_kernel(const GradParams g, 
                 const int nn = min(256, n_total - n0);
                 const uint32_t id = idesc_tf32(kBM, nn);
                 const uint32_t d = tmem + (uint32_t)n0;
-                const uint32_t boff = (uint32_t)n0 * 128;  // n0 is a multiple of 8 rows
+                const uint32_t boff = (uint32_t)n0 * 128;
 #pragma unroll
                 for (int ks = 0; ks < kBK / 8; ++ks) {
                     const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
@@ -234,13 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1) egemm_kernel(const GradParams g, 
                     mma_tf32(d, sdesc(ah + ko), sdesc(bl + boff + ko), id, 1u);
                 }
             }
-            mma_commit(bar);
+            mma_commit(smem_u32(&s_bar[s]));
         }
     }
     // The last commit covers every MMA issued before it.
     {
-        const int s = (nstages == 2) ? ((nK - 1) & 1) : 0;
-        ok = mbar_wait(smem_u32(&s_bar[s]), phase[s], status) && ok;
+        const int s = (tstages == 2) ? ((nK - 1) & 1) : 0;
+        ok = mbar_wait(smem_u32(&s_bar[s]), mma_phase[s], status) && ok;
     }
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
@@ -278,36 +363,50 @@ __global__ void __launch_bounds__(kThreads, 1) egemm_kernel(const GradParams g, 
 
 }  // namespace
 
-static int egemm_stages(int D)
+// Shared-memory plan: tile stages (hi/lo of A and B) and raw staging buffers,
+// double-buffered when they fit in 220 KiB (raw buffers first).
+static void egemm_plan(int D, bool cols, int* tstages, int* rstages, size_t* bytes)
 {
     const int n_total = ((D + 1 + 15) / 16) * 16;
     const size_t stage = 2 * (size_t)kBM * 128 + 2 * (size_t)n_total * 128;
-    return (1024 + 2 * stage <= 220 * 1024) ? 2 : 1;
+    const size_t rawA = cols ? Raw<true>::kBytes : Raw<false>::kBytes;
+    const size_t raw = rawA + (((size_t)kBK * D * 4 + 127) & ~(size_t)127);
+    const size_t limit = 220 * 1024;
+    int t = 2, r = 2;
+    auto total = [&](int tt, int rr) { return 1024 + tt * stage + rr * raw; };
+    if (total(t, r) > limit) t = 1;
+    if (total(t, r) > limit) r = 1;
+    *tstages = t;
+    *rstages = r;
+    *bytes = total(t, r);
 }
 
 size_t egemm_smem_bytes(int D)
 {
-    const int n_total = ((D + 1 + 15) / 16) * 16;
-    const size_t stage = 2 * (size_t)kBM * 128 + 2 * (size_t)n_total * 128;
-    return 1024 + (size_t)egemm_stages(D) * stage;
+    int t, r;
+    size_t a, b;
+    egemm_plan(D, false, &t, &r, &a);
+    egemm_plan(D, true, &t, &r, &b);
+    return a > b ? a : b;
 }
 
 cudaError_t launch_grad_tc(const GradParams& g, bool cols, int* status, cudaStream_t st)
 {
     const int n_total = ((g.D + 1 + 15) / 16) * 16;
-    const int stages = egemm_stages(g.D);
-    const size_t smem = egemm_smem_bytes(g.D);
+    int tstages, rstages;
+    size_t smem;
+    egemm_plan(g.D, cols, &tstages, &rstages, &smem);
     const int rows = cols ? g.M : g.N;
     dim3 grid((rows + kBM - 1) / kBM, g.P);
     cudaError_t e;
     if (cols) {
         e = cudaFuncSetAttribute(egemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        egemm_kernel<true><<<grid, kThreads, smem, st>>>(g, n_total, stages, status);
+        egemm_kernel<true><<<grid, kThreads, smem, st>>>(g, n_total, tstages, rstages, status);
     } else {
         e = cudaFuncSetAttribute(egemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        egemm_kernel<false><<<grid, kThreads, smem, st>>>(g, n_total, stages, status);
+        egemm_kernel<false><<<grid, kThreads, smem, st>>>(g, n_total, tstages, rstages, status);
     }
     return cudaGetLastError();
 }
