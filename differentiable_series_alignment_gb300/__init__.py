@@ -16,7 +16,7 @@ from __future__ import annotations
 
 import torch
 
-from ._lib import (FUSED, OP_BARYCENTER, OP_FWD_BWD, OP_NORMALIZED, UNFUSED, SdtwError, load,
+from ._lib import (EXTENDED, FUSED, OP_BARYCENTER, OP_FWD_BWD, OP_NORMALIZED, UNFUSED, SdtwError, auto_precision, load,
                    sdtw_backward, sdtw_barycenter_step, sdtw_debug_set_wait, sdtw_distance, sdtw_forward,
                    sdtw_last_device_status, sdtw_normalized, sdtw_workspace_bytes, workspace)
 
@@ -24,7 +24,7 @@ __all__ = [
     "SoftDTW", "softdtw_barycenter", "SdtwError", "load", "workspace",
     "sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
     "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_debug_set_wait",
-    "UNFUSED", "FUSED", "OP_FWD_BWD", "OP_NORMALIZED", "OP_BARYCENTER",
+    "UNFUSED", "FUSED", "EXTENDED", "OP_FWD_BWD", "OP_NORMALIZED", "OP_BARYCENTER", "auto_precision",
 ]
 
 
@@ -94,22 +94,29 @@ class SoftDTW:
 
     fused=False stores the (B,N,M) cost tensor; fused=True recomputes it inside
     the DP kernels. normalize=True gives s(x,y) - (s(x,x) + s(y,y))/2 and needs
-    x.shape == y.shape.
+    x.shape == y.shape. extended=None picks the double-float forward state for
+    small gamma or long sequences (auto_precision); True/False forces it.
     """
 
     def __init__(self, gamma: float = 1.0, dist: str = "sqeuclidean", fused: bool = False,
-                 normalize: bool = False):
+                 normalize: bool = False, extended: bool | None = None):
         if dist != "sqeuclidean":
             raise ValueError("only dist='sqeuclidean' is supported")
         if not (gamma > 0):
             raise ValueError("gamma must be > 0")
         self.gamma = float(gamma)
-        self.mode = FUSED if fused else UNFUSED
+        self.fused = bool(fused)
         self.normalize = normalize
+        self.extended = extended
 
     def __call__(self, x: torch.Tensor, y: torch.Tensor) -> torch.Tensor:
         fn = _NormalizedFn if self.normalize else _SoftDTWFn
-        return fn.apply(x, y, self.gamma, self.mode)
+        mode = FUSED if self.fused else UNFUSED
+        if self.extended is None:
+            mode |= auto_precision(self.gamma, x.shape[1], y.shape[1])
+        elif self.extended:
+            mode |= EXTENDED
+        return fn.apply(x, y, self.gamma, mode)
 
 
 def softdtw_barycenter(sequences: torch.Tensor, gamma: float = 1.0, max_iter: int = 100, lr: float = 0.1,
@@ -123,7 +130,7 @@ def softdtw_barycenter(sequences: torch.Tensor, gamma: float = 1.0, max_iter: in
     T = z.shape[0]
     m = torch.zeros_like(z)
     v = torch.zeros_like(z)
-    mode = FUSED if fused else UNFUSED
+    mode = (FUSED if fused else UNFUSED) | auto_precision(gamma, T, T2)
     ws = workspace(OP_BARYCENTER, K, T, T2, D, mode, X.device)
     losses = torch.empty(max_iter, dtype=torch.float32, device=X.device)
     for t in range(1, max_iter + 1):

@@ -16,6 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsdtw.so")
 
 UNFUSED, FUSED = 0, 1
+EXTENDED = 2   # precision flag OR-ed into the mode (double-float forward state)
 OP_FWD_BWD, OP_NORMALIZED, OP_BARYCENTER = 0, 1, 2
 
 STATUS_NAMES = {
@@ -111,8 +112,15 @@ def _check(code: int, where: str):
 
 def _mode(mode) -> int:
     if isinstance(mode, str):
-        return {"unfused": UNFUSED, "fused": FUSED}[mode]
+        return {"unfused": UNFUSED, "fused": FUSED, "unfused+extended": UNFUSED | EXTENDED,
+                "fused+extended": FUSED | EXTENDED}[mode]
     return int(mode)
+
+
+def auto_precision(gamma: float, N: int, M: int) -> int:
+    """EXTENDED where fp32 difference-form DP state is not accurate enough for
+    the gradient tolerance: small gamma or long sequences."""
+    return EXTENDED if (gamma < 0.05 or max(N, M) >= 4096) else 0
 
 
 def sdtw_workspace_bytes(op: int, B: int, N: int, M: int, D: int, mode) -> int:

@@ -35,7 +35,8 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
 {
     if (op < SDTW_OP_FWD_BWD || op > SDTW_OP_BARYCENTER) return false;
     if (B < 1 || N < 1 || M < 1 || D < 1) return false;
-    if (mode != SDTW_UNFUSED && mode != SDTW_FUSED) return false;
+    if (mode & ~3) return false;
+    const bool fused = (mode & SDTW_FUSED) != 0, ext = (mode & SDTW_EXTENDED) != 0;
     const int P = (op == SDTW_OP_NORMALIZED) ? 3 * B : B;
     if (op == SDTW_OP_NORMALIZED) M = N;
     const int NB = (N + 31) / 32;
@@ -46,13 +47,13 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->ctrl_b = o; L->ctrl_b_bytes = sizeof(int); o = align_up(o + L->ctrl_b_bytes);
     L->colsum = o; o = align_up(o + sizeof(double) * (size_t)P * NB);
     L->rowsum = o; o = align_up(o + sizeof(double) * (size_t)P);
-    L->rowbuf = o; o = align_up(o + sizeof(float) * (size_t)P * M);
+    L->rowbuf = o; o = align_up(o + sizeof(float2) * (size_t)P * M);
     L->losses = o; o = align_up(o + sizeof(float) * (size_t)P);
-    L->edge_f = o; o = align_up(o + sizeof(Slot) * (size_t)P * NB * M);
+    L->edge_f = o; o = align_up(o + 2 * sizeof(Slot) * (size_t)P * NB * M);
     L->edge_b = o; o = align_up(o + 2 * sizeof(Slot) * (size_t)P * NB * M);
-    L->vh = o; o = align_up(o + sizeof(float2) * slots);
+    L->vh = o; o = align_up(o + (ext ? sizeof(float4) : sizeof(float2)) * slots);
     L->e = o; o = align_up(o + sizeof(float) * slots);
-    L->dsk = o; if (mode == SDTW_UNFUSED) o = align_up(o + sizeof(float) * slots);
+    L->dsk = o; if (!fused) o = align_up(o + (ext ? sizeof(float2) : sizeof(float)) * slots);
     L->gparts = o; if (op == SDTW_OP_BARYCENTER) o = align_up(o + sizeof(float) * (size_t)P * N * D);
     L->total = o;
     L->P = P; L->N = N; L->M = M; L->D = D; L->NB = NB;
@@ -71,7 +72,7 @@ int env_int(const char* name, int dflt)
 
 // Warps per wavefront CTA: about one 32-row block per SM partition over the
 // whole batch, bounded by the shared memory a fused CTA needs.
-int choose_warps(int P, int NB, int D, bool fused, bool backward, int num_sms)
+int choose_warps(int P, int NB, int D, bool fused, bool ext, bool backward, int num_sms)
 {
     int W = env_int(backward ? "SDTW_WARPS_BWD" : "SDTW_WARPS_FWD", 0);
     if (W <= 0) {
@@ -83,7 +84,8 @@ int choose_warps(int P, int NB, int D, bool fused, bool backward, int num_sms)
     if (W < 1) W = 1;
     if (fused) {
         const size_t limit = 220 * 1024;
-        while (W > 1 && wave_smem_fixed(W, false) + (size_t)W * wave_smem_fused_per_warp(D) > limit) --W;
+        const size_t per = ext ? wavex_smem_fused_per_warp(D) : wave_smem_fused_per_warp(D);
+        while (W > 1 && wave_smem_fixed(W, true) + (size_t)W * per > limit) --W;
     }
     return W;
 }
@@ -105,10 +107,12 @@ sdtw_status check_common(const void* x, const void* y, int B, int N, int M, int 
 {
     if (B < 1 || N < 1 || M < 1 || D < 1) return SDTW_ERR_EMPTY;
     if (!(gamma > 0.f) || !std::isfinite(gamma)) return SDTW_ERR_GAMMA;
-    if (mode != SDTW_UNFUSED && mode != SDTW_FUSED) return SDTW_ERR_ARG;
+    if (mode & ~3) return SDTW_ERR_ARG;
     if (!x || !y) return SDTW_ERR_ARG;
     if (B > 65535 / 3 || N > (1 << 24) || M > (1 << 24) || D > 400) return SDTW_ERR_TOO_LARGE;
-    if (mode == SDTW_FUSED && wave_smem_fixed(1, false) + wave_smem_fused_per_warp(D) > 220 * 1024)
+    if ((mode & SDTW_FUSED) &&
+        wave_smem_fixed(1, true) + ((mode & SDTW_EXTENDED) ? wavex_smem_fused_per_warp(D) : wave_smem_fused_per_warp(D)) >
+            220 * 1024)
         return SDTW_ERR_TOO_LARGE;
     return SDTW_OK;
 }
@@ -120,12 +124,12 @@ sdtw_status check_ws(void* ws, size_t ws_bytes, const Layout& L)
     return SDTW_OK;
 }
 
-WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamma, bool fused, bool backward)
+WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamma, bool fused, bool ext, bool backward)
 {
     WaveParams q{};
     q.pr = pr;
     q.P = L.P; q.N = L.N; q.M = L.M; q.D = L.D; q.NB = L.NB;
-    q.W = choose_warps(L.P, L.NB, L.D, fused && !backward, backward, num_sms());
+    q.W = choose_warps(L.P, L.NB, L.D, fused && !backward, ext, backward, num_sms());
     q.S = (L.NB + q.W - 1) / q.W;
     q.scale = (float)(1.4426950408889634 / (double)gamma);
     q.unscale = (float)((double)gamma * 0.6931471805599453);
@@ -142,6 +146,7 @@ WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamm
     q.rowsum = at<double>(ws, L.rowsum);
     q.rowbuf = at<float>(ws, L.rowbuf);
     q.accurate = env_int("SDTW_ACCURATE", 0);
+    q.ext = ext ? 1 : 0;
     q.loss = at<float>(ws, L.losses);
     q.status = at<int>(ws, L.status);
     q.wait_ns = g_wait_ns;
@@ -159,12 +164,20 @@ WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamm
 sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gamma, int mode, float* loss_out,
                         cudaStream_t st)
 {
-    const bool fused = (mode == SDTW_FUSED);
-    WaveParams q = wave_params(pr, L, ws, gamma, fused, false);
+    const bool fused = (mode & SDTW_FUSED) != 0, ext = (mode & SDTW_EXTENDED) != 0;
+    WaveParams q = wave_params(pr, L, ws, gamma, fused, ext, false);
     SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.status), 0, sizeof(int), st));
     SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_f), 0, L.ctrl_f_bytes, st));
     if (q.S > 1)  // strip boundary slots start untagged
-        SDTW_CUDA(cudaMemsetAsync(q.edge_f, 0, sizeof(Slot) * (size_t)L.P * q.S * L.M, st));
+        SDTW_CUDA(cudaMemsetAsync(q.edge_f, 0, (ext ? 2 : 1) * sizeof(Slot) * (size_t)L.P * q.S * L.M, st));
+    if (ext) {
+        if (!fused) SDTW_CUDA(launch_dist_skewed_x(pr, L.P, L.N, L.M, L.D, at<float2>(ws, L.dsk), st));
+        q.loss = loss_out;
+        q.skip_publish = g_skip_publish;
+        g_skip_publish = 0;
+        SDTW_CUDA(launch_forward_x(q, fused, st));
+        return SDTW_OK;
+    }
     if (!fused) SDTW_CUDA(launch_dist_skewed(pr, L.P, L.N, L.M, L.D, at<float>(ws, L.dsk), st));
     q.loss = loss_out;
     q.skip_publish = g_skip_publish;
@@ -175,7 +188,7 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
 
 sdtw_status run_backward(const Problems& pr, const Layout& L, void* ws, float gamma, int mode, cudaStream_t st)
 {
-    WaveParams q = wave_params(pr, L, ws, gamma, mode == SDTW_FUSED, true);
+    WaveParams q = wave_params(pr, L, ws, gamma, (mode & SDTW_FUSED) != 0, (mode & SDTW_EXTENDED) != 0, true);
     SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_b), 0, L.ctrl_b_bytes, st));
     if (q.S > 1) SDTW_CUDA(cudaMemsetAsync(q.edge_b, 0, 2 * sizeof(Slot) * (size_t)L.P * q.S * L.M, st));
     SDTW_CUDA(launch_backward(q, st));
@@ -183,8 +196,11 @@ sdtw_status run_backward(const Problems& pr, const Layout& L, void* ws, float ga
 }
 
 // Gradient contractions of the problems of one set (B problems starting at set*B).
+// Gradients: tensor-core GEMM form (egemm.cu) by default; the difference form
+// (grad.cu, FP32 pipe) in the extended-precision mode, where rows or columns
+// that align to many cells make the GEMM form cancel beyond fp32.
 sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void* ws, const float* grad_loss,
-                      float coef, float* out_x, float* out_y, int accumulate, cudaStream_t st)
+                      float coef, float* out_x, float* out_y, int accumulate, int mode, cudaStream_t st)
 {
     GradParams g{};
     g.pr = all;
@@ -198,7 +214,7 @@ sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void
     g.coef = coef;
     g.omod = B;
     g.accumulate = accumulate;
-    const bool simt = env_int("SDTW_GRAD_SIMT", 0) != 0;
+    const bool simt = (mode & SDTW_EXTENDED) != 0 || env_int("SDTW_GRAD_SIMT", 0) != 0;
     int* status = at<int>(ws, L.status);
     if (out_x) {
         g.out = out_x;
@@ -275,7 +291,7 @@ sdtw_status sdtw_backward(const float* x, const float* y, int B, int N, int M, i
     pr.B = B;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((s = run_backward(pr, L, ws, gamma, (int)mode, st)) != SDTW_OK) return s;
-    if (grad_x || grad_y) return run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, st);
+    if (grad_x || grad_y) return run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, (int)mode, st);
     return SDTW_OK;
 }
 
@@ -304,12 +320,12 @@ sdtw_status sdtw_normalized(const float* x, const float* y, int B, int N, int D,
     if (!grad_loss || (!grad_x && !grad_y)) return SDTW_OK;
     if ((s = run_backward(pr, L, ws, gamma, (int)mode, st)) != SDTW_OK) return s;
     // grad_x = g [gx(x,y) - (gx(x,x) + gy(x,x))/2];  grad_y = g [gy(x,y) - (gx(y,y) + gy(y,y))/2]
-    if ((s = run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, st)) != SDTW_OK) return s;
+    if ((s = run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, (int)mode, st)) != SDTW_OK) return s;
     if (grad_x) {
-        if ((s = run_grads(pr, 1, B, L, ws, grad_loss, -0.5f, grad_x, grad_x, 1, st)) != SDTW_OK) return s;
+        if ((s = run_grads(pr, 1, B, L, ws, grad_loss, -0.5f, grad_x, grad_x, 1, (int)mode, st)) != SDTW_OK) return s;
     }
     if (grad_y) {
-        if ((s = run_grads(pr, 2, B, L, ws, grad_loss, -0.5f, grad_y, grad_y, 1, st)) != SDTW_OK) return s;
+        if ((s = run_grads(pr, 2, B, L, ws, grad_loss, -0.5f, grad_y, grad_y, 1, (int)mode, st)) != SDTW_OK) return s;
     }
     return SDTW_OK;
 }
@@ -336,7 +352,8 @@ sdtw_status sdtw_barycenter_step(float* z, float* m, float* v, int t, const floa
     if ((s = run_forward(pr, L, ws, gamma, (int)mode, losses, st)) != SDTW_OK) return s;
     if ((s = run_backward(pr, L, ws, gamma, (int)mode, st)) != SDTW_OK) return s;
     float* gparts = at<float>(ws, L.gparts);
-    if ((s = run_grads(pr, 0, K, L, ws, nullptr, 1.f / (float)K, gparts, nullptr, 0, st)) != SDTW_OK) return s;
+    if ((s = run_grads(pr, 0, K, L, ws, nullptr, 1.f / (float)K, gparts, nullptr, 0, (int)mode, st)) != SDTW_OK)
+        return s;
     const double bc1 = 1.0 - std::pow((double)beta1, (double)t);
     const double bc2 = 1.0 - std::pow((double)beta2, (double)t);
     SDTW_CUDA(launch_adam(z, m, v, gparts, K, T * D, lr, beta1, beta2, eps, (float)bc1, (float)bc2, losses, loss_out,

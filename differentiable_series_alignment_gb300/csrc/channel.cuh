@@ -1,0 +1,53 @@
+// channel.cuh -- bounded waits on the tagged-slot channels between wavefront warps and strips.
+#pragma once
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sdtw {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Bounded wait on a shared-memory counter (back-pressure of a ring). Warp-uniform result.
+static __device__ __forceinline__ bool wait_smem(const volatile int* cnt, int target, const WaveParams& q) {
+    bool ok = true;
+    if (*cnt < target) {
+        const unsigned long long t0 = global_ns();
+        unsigned it = 0;
+        while (*cnt < target) {
+            __nanosleep(32);
+            if ((++it & 7u) == 0) {
+                if (ld_volatile_global(q.status) != 0) { ok = false; break; }
+                if (global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); ok = false; break; }
+            }
+        }
+    }
+    return __shfl_sync(kFull, ok, 0);
+}
+
+// Wait until every lane's slot (or pair of slots) carries its expected tag,
+// reloading the lanes that do not yet. want == 0 marks a lane with nothing to
+// check. Bounded; warp-uniform result.
+template <int NS>
+static __device__ __forceinline__ bool validate(Slot (&cur)[NS], const Slot* src, unsigned want, const WaveParams& q) {
+    bool mine = true;
+#pragma unroll
+    for (int k = 0; k < NS; ++k) mine = mine && (want == 0u || cur[k].tag == want);
+    if (__all_sync(kFull, mine)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (!mine) {
+#pragma unroll
+            for (int k = 0; k < NS; ++k) cur[k] = slot_load(src + k);
+            mine = true;
+#pragma unroll
+            for (int k = 0; k < NS; ++k) mine = mine && (cur[k].tag == want);
+        }
+        if (__all_sync(kFull, mine)) return true;
+        __nanosleep(20);
+        bool bad = ld_volatile_global(q.status) != 0;
+        if (!bad && global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); bad = true; }
+        if (__any_sync(kFull, bad)) return false;
+    }
+}
+
+}  // namespace sdtw

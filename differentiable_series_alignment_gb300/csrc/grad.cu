@@ -1,8 +1,13 @@
-// grad.cu -- input gradients from the alignment matrix, and the barycenter Adam step.
+// grad.cu -- input gradients from the alignment matrix in difference form, and
+// the barycenter Adam step.
 //
 // Chain rule through the squared Euclidean cost C[i,j] = |x_i - y_j|^2:
-//   dL/dx_i = g * 2 * sum_j E[i,j] (x_i - y_j) = g * 2 * (rowsum_i(E) x_i - (E y)_i)
-//   dL/dy_j = g * 2 * sum_i E[i,j] (y_j - x_i) = g * 2 * (colsum_j(E) y_j - (E^T x)_j)
+//   dL/dx_i = g * 2 * sum_j E[i,j] (x_i - y_j),   dL/dy_j = g * 2 * sum_i E[i,j] (y_j - x_i).
+// These kernels keep the difference form term by term. The GEMM form
+// rowsum_i(E) x_i - (E y)_i (egemm.cu) cancels badly where one row aligns to
+// many columns (stretched warps, rowsum >> 1): at N=M=8192 its fp32 sums miss
+// rel 1e-3 on such rows while the difference form does not. The extended
+// precision path therefore uses these kernels.
 // E arrives in the skewed layout of the wavefront; each CTA un-skews 32x32
 // tiles into shared memory and contracts them with the matching x or y rows.
 #include "common.cuh"
@@ -42,10 +47,17 @@ __global__ void __launch_bounds__(128) grad_rows_kernel(const GradParams g)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = g.N, M = g.M, D = g.D;
     const float* yb = g.pr.y(p);
+    const int i = rb * 32 + lane;
+    float xi[16];
+    const float* xrow = g.pr.x(p) + (size_t)min(i, N - 1) * D;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int kk = kb + warp * 16 + k;
+        xi[k] = (kk < D) ? xrow[kk] : 0.f;
+    }
     float acc[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-    float rs = 0.f;
     for (int c0 = 0; c0 < M; c0 += 32) {
         load_tile<false>(g.E, N, M, p, rb, c0, es);
         for (int idx = threadIdx.x; idx < 32 * kKC; idx += blockDim.x) {
@@ -56,29 +68,26 @@ __global__ void __launch_bounds__(128) grad_rows_kernel(const GradParams g)
 #pragma unroll 4
         for (int c = 0; c < 32; ++c) {
             const float e = es[c * 32 + lane];
-            rs += e;
             const float4* yv = reinterpret_cast<const float4*>(ys + c * kYS + warp * 16);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float4 w = yv[q];
-                acc[4 * q + 0] = fmaf(e, w.x, acc[4 * q + 0]);
-                acc[4 * q + 1] = fmaf(e, w.y, acc[4 * q + 1]);
-                acc[4 * q + 2] = fmaf(e, w.z, acc[4 * q + 2]);
-                acc[4 * q + 3] = fmaf(e, w.w, acc[4 * q + 3]);
+                acc[4 * q + 0] = fmaf(e, xi[4 * q + 0] - w.x, acc[4 * q + 0]);
+                acc[4 * q + 1] = fmaf(e, xi[4 * q + 1] - w.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(e, xi[4 * q + 2] - w.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(e, xi[4 * q + 3] - w.w, acc[4 * q + 3]);
             }
         }
         __syncthreads();
     }
-    const int i = rb * 32 + lane;
     if (i >= N) return;
     const float w = g.coef * 2.f * (g.grad_loss ? g.grad_loss[p % g.wmod] : 1.f);
-    const float* xi = g.pr.x(p) + (size_t)i * D;
     float* out = g.out + (long long)(p % g.omod) * g.out_stride + (size_t)i * D;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
         const int kk = kb + warp * 16 + k;
         if (kk < D) {
-            const float val = w * (rs * xi[kk] - acc[k]);
+            const float val = w * acc[k];
             out[kk] = g.accumulate ? out[kk] + val : val;
         }
     }
@@ -93,10 +102,17 @@ __global__ void __launch_bounds__(128) grad_cols_kernel(const GradParams g)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = g.N, M = g.M, D = g.D;
     const float* xb = g.pr.x(p);
+    const int j = c0 + lane;
+    float yj[16];
+    const float* yrow = g.pr.y(p) + (size_t)min(j, M - 1) * D;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int kk = kb + warp * 16 + k;
+        yj[k] = (kk < D) ? yrow[kk] : 0.f;
+    }
     float acc[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-    float cs = 0.f;
     const int NB = (N + 31) / 32;
     for (int rb = 0; rb < NB; ++rb) {
         load_tile<true>(g.E, N, M, p, rb, c0, es);
@@ -109,29 +125,26 @@ __global__ void __launch_bounds__(128) grad_cols_kernel(const GradParams g)
 #pragma unroll 4
         for (int r = 0; r < 32; ++r) {
             const float e = es[r * 32 + lane];
-            cs += e;
             const float4* xv = reinterpret_cast<const float4*>(xs + r * kYS + warp * 16);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float4 w = xv[q];
-                acc[4 * q + 0] = fmaf(e, w.x, acc[4 * q + 0]);
-                acc[4 * q + 1] = fmaf(e, w.y, acc[4 * q + 1]);
-                acc[4 * q + 2] = fmaf(e, w.z, acc[4 * q + 2]);
-                acc[4 * q + 3] = fmaf(e, w.w, acc[4 * q + 3]);
+                acc[4 * q + 0] = fmaf(e, yj[4 * q + 0] - w.x, acc[4 * q + 0]);
+                acc[4 * q + 1] = fmaf(e, yj[4 * q + 1] - w.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(e, yj[4 * q + 2] - w.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(e, yj[4 * q + 3] - w.w, acc[4 * q + 3]);
             }
         }
         __syncthreads();
     }
-    const int j = c0 + lane;
     if (j >= M) return;
     const float w = g.coef * 2.f * (g.grad_loss ? g.grad_loss[p % g.wmod] : 1.f);
-    const float* yj = g.pr.y(p) + (size_t)j * D;
     float* out = g.out + (long long)(p % g.omod) * g.out_stride + (size_t)j * D;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
         const int kk = kb + warp * 16 + k;
         if (kk < D) {
-            const float val = w * (cs * yj[kk] - acc[k]);
+            const float val = w * acc[k];
             out[kk] = g.accumulate ? out[kk] + val : val;
         }
     }

@@ -19,7 +19,7 @@ struct WaveParams {
     float scale;      // log2(e) / gamma
     float unscale;    // gamma * ln(2)
     const float* Dsk; // unfused: raw cost, skewed layout; fused: nullptr
-    float2* VH;       // (vl, hu) per cell, skewed layout
+    float2* VH;       // (vl, hu) per cell, skewed layout (extended: float4 log2-probabilities)
     float* E;         // alignment matrix, skewed layout (backward output)
     Slot* edge_f;     // [P][S][M]     boundary rows between forward strips (tagged)
     Slot* edge_b;     // [P][S][M][2]  boundary messages between backward strips (tagged)
@@ -34,11 +34,15 @@ struct WaveParams {
     unsigned long long wait_ns;
     int skip_publish; // test hook: strip 0 withholds its forward ready counter
     int accurate;     // 1: unbiased exp2/log2 in the recursions; 0: MUFU approximations
+    int ext;          // 1: extended-precision forward state (wavefront_x.cu)
 };
 
 size_t wave_smem_fixed(int W, bool backward);
 size_t wave_smem_fused_per_warp(int D);
 size_t wave_smem_floor();
+size_t wavex_smem_fused_per_warp(int D);
+cudaError_t launch_forward_x(WaveParams q, bool fused, cudaStream_t st);
+cudaError_t launch_dist_skewed_x(const Problems& pr, int P, int N, int M, int D, float2* Dsk, cudaStream_t st);
 cudaError_t launch_forward(WaveParams q, bool fused, cudaStream_t st);
 cudaError_t launch_backward(WaveParams q, cudaStream_t st);
 

@@ -22,59 +22,16 @@
 //
 // This replaces the per-anti-diagonal kernel launches of the pages' design
 // (review page, "proposed method", first bullet) by one launch per direction.
+#include "channel.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
 #include <cstdlib>
+#include <type_traits>
 
 namespace sdtw {
 
 namespace {
-
-constexpr unsigned kFull = 0xffffffffu;
-
-// Bounded wait on a shared-memory counter (back-pressure of a ring). Warp-uniform result.
-__device__ __forceinline__ bool wait_smem(const volatile int* cnt, int target, const WaveParams& q) {
-    bool ok = true;
-    if (*cnt < target) {
-        const unsigned long long t0 = global_ns();
-        unsigned it = 0;
-        while (*cnt < target) {
-            __nanosleep(32);
-            if ((++it & 7u) == 0) {
-                if (ld_volatile_global(q.status) != 0) { ok = false; break; }
-                if (global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); ok = false; break; }
-            }
-        }
-    }
-    return __shfl_sync(kFull, ok, 0);
-}
-
-// Wait until every lane's slot (or pair of slots) carries its expected tag,
-// reloading the lanes that do not yet. want == 0 marks a lane with nothing to
-// check. Bounded; warp-uniform result.
-template <int NS>
-__device__ __forceinline__ bool validate(Slot (&cur)[NS], const Slot* src, unsigned want, const WaveParams& q) {
-    bool mine = true;
-#pragma unroll
-    for (int k = 0; k < NS; ++k) mine = mine && (want == 0u || cur[k].tag == want);
-    if (__all_sync(kFull, mine)) return true;
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-        if (!mine) {
-#pragma unroll
-            for (int k = 0; k < NS; ++k) cur[k] = slot_load(src + k);
-            mine = true;
-#pragma unroll
-            for (int k = 0; k < NS; ++k) mine = mine && (cur[k].tag == want);
-        }
-        if (__all_sync(kFull, mine)) return true;
-        __nanosleep(20);
-        bool bad = ld_volatile_global(q.status) != 0;
-        if (!bad && global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); bad = true; }
-        if (__any_sync(kFull, bad)) return false;
-    }
-}
 
 struct FusedSmem {
     float* xs;  // [32][XS]  rows of this warp, zero padded
@@ -166,23 +123,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams
         if (top_global && lane < kGroup && lane < M) nxt[0] = slot_load(edge_in + lane);
 
         float h_prev = 0.f, v_prev = 0.f;
-        float dn[kGroup];
+        // raw costs of the next kGroup steps; slot u is refilled with the following
+        // group's value as soon as step u has consumed it
+        float dbuf[kGroup];
         if (!FUSED) {
 #pragma unroll
-            for (int u = 0; u < kGroup; ++u) dn[u] = dp[(long long)u * 32];
+            for (int u = 0; u < kGroup; ++u) dbuf[u] = dp[(long long)u * 32];
         }
         const int nG = T / kGroup;
         for (int g = 0; g < nG; ++g) {
             const int s0 = g * kGroup;
-            float dc[kGroup];
-            if (!FUSED) {
-#pragma unroll
-                for (int u = 0; u < kGroup; ++u) dc[u] = dn[u];
-                if (g + 1 < nG) {
-#pragma unroll
-                    for (int u = 0; u < kGroup; ++u) dn[u] = dp[(long long)(s0 + kGroup + u) * 32];
-                }
-            } else if ((s0 & 31) == 0 && s0 < M) {
+            if (FUSED && (s0 & 31) == 0 && s0 < M) {
                 // Raw cost of columns [s0, s0+32) for this warp's 32 rows.
                 const int D = q.D, D4 = (D + 3) & ~3;
                 __syncwarp();
@@ -256,7 +207,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams
                 const float tv = __shfl_sync(kFull, topv, u);
                 const float hu = (lane == 0) ? tv : hs;
                 const float vl = v_prev;
-                const float d = (FUSED ? fz.dt[(j & 63) * 32 + lane] : dc[u]) * scale;
+                float draw;
+                if (FUSED) {
+                    draw = fz.dt[(j & 63) * 32 + lane];
+                } else {
+                    draw = dbuf[u];
+                    if (g + 1 < nG) dbuf[u] = dp[(long long)(s0 + kGroup + u) * 32];
+                }
+                const float d = draw * scale;
                 // t = d + softmin(0, vl, hu) = d + lo - log2(1 + 2^(lo-mid) + 2^(lo-hi))
                 float lo, mid, hi;
                 sort3(0.f, vl, hu, lo, mid, hi);
@@ -315,7 +273,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams
 // ---------------------------------------------------------------------------
 // Backward (log space)
 // ---------------------------------------------------------------------------
-template <bool ACC>
+// EXT: the extended forward stored the three transition log2-probabilities of
+// each cell (float4: diag, left, up); otherwise the (vl, hu) pair from which
+// they are recomputed.
+template <bool ACC, bool EXT>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams q)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -343,8 +304,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
     const bool above_global = has_above && warp == 0;
     const bool last_lane = (i == N - 1);
 
+    using VT = typename std::conditional<EXT, float4, float2>::type;
     const long long sk = skew_index(N, M, p, rb, 0, lane);
-    const float2* vhp = q.VH + sk;
+    const VT* vhp = reinterpret_cast<const VT*>(q.VH) + sk;
     float* ep = q.E + sk;
     Slot* ring_out = ring + 2 * warp * kRing;
     const Slot* ring_in = ring + 2 * (warp + 1) * kRing;
@@ -365,20 +327,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
     }
 
     float ml = -kBig, su = -kBig, sd = -kBig, rd_hold = -kBig;
-    float2 vn[kGroup];
+    // Per-step state of the next kGroup steps; slot u is refilled with the
+    // following group's value as soon as step u has consumed it.
+    VT buf[kGroup];
 #pragma unroll
-    for (int u = 0; u < kGroup; ++u) vn[u] = vhp[(long long)(T - 1 - u) * 32];
+    for (int u = 0; u < kGroup; ++u) buf[u] = vhp[(long long)(T - 1 - u) * 32];
     const int nG = T / kGroup;
     for (int g = 0; g < nG; ++g) {
         const int t0 = g * kGroup;   // first reverse step of the group
         const int k0 = t0 - off;     // channel slot read by lane 31 at that step
-        float2 vc[kGroup];
-#pragma unroll
-        for (int u = 0; u < kGroup; ++u) vc[u] = vn[u];
-        if (g + 1 < nG) {
-#pragma unroll
-            for (int u = 0; u < kGroup; ++u) vn[u] = vhp[(long long)(T - 1 - (t0 + kGroup + u)) * 32];
-        }
         // Messages of the row below for lane 31: lane q holds slot k0 + q.
         float2 botv = make_float2(-kBig, -kBig);
         bool ok = true;
@@ -428,15 +385,24 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
             sort3(a1, a2, a3, lo, mid, hi);
             float lE = hi + dp_log2<ACC>((1.f + dp_exp2<ACC>(mid - hi)) + dp_exp2<ACC>(lo - hi));
             lE = (last_lane && j == M - 1) ? 0.f : lE;
-            // log2 normaliser of this cell's own soft-min: the transition
-            // log-probabilities to its diag/left/up predecessors are -Lz, -vl-Lz, -hu-Lz.
-            const float2 st = vc[u];
-            float wlo, wmid, whi;
-            sort3(0.f, st.x, st.y, wlo, wmid, whi);
-            const float Lz = dp_log2<ACC>((1.f + dp_exp2<ACC>(wlo - wmid)) + dp_exp2<ACC>(wlo - whi)) - wlo;
-            ml = lE + (-st.x - Lz);
-            su = lE + (-st.y - Lz);
-            sd = lE - Lz;
+            const VT cur = buf[u];
+            if (g + 1 < nG) buf[u] = vhp[(long long)(T - 1 - (t0 + kGroup + u)) * 32];
+            float wl, wu, wd;  // transition log2-probabilities of this cell to its left/up/diag predecessors
+            if (EXT) {
+                const float4 st = reinterpret_cast<const float4&>(cur);
+                wd = st.x; wl = st.y; wu = st.z;
+            } else {
+                // log2 normaliser of this cell's own soft-min: the log-probabilities
+                // to its diag/left/up predecessors are -Lz, -vl-Lz, -hu-Lz.
+                const float2 st = reinterpret_cast<const float2&>(cur);
+                float wlo, wmid, whi;
+                sort3(0.f, st.x, st.y, wlo, wmid, whi);
+                const float Lz = dp_log2<ACC>((1.f + dp_exp2<ACC>(wlo - wmid)) + dp_exp2<ACC>(wlo - whi)) - wlo;
+                wl = -st.x - Lz; wu = -st.y - Lz; wd = -Lz;
+            }
+            ml = lE + wl;
+            su = lE + wu;
+            sd = lE + wd;
             ep[(long long)t * 32] = ex2(lE);
             if (chan_lane && (unsigned)j < (unsigned)M) {
                 const int k = M - 1 - j;
@@ -514,7 +480,8 @@ cudaError_t launch_backward(WaveParams q, cudaStream_t st)
         kern<<<grid, q.W * 32, smem, st>>>(q);
         return cudaGetLastError();
     };
-    return q.accurate ? go(bwd_kernel<true>) : go(bwd_kernel<false>);
+    if (q.ext) return go(bwd_kernel<true, true>);
+    return q.accurate ? go(bwd_kernel<true, false>) : go(bwd_kernel<false, false>);
 }
 
 }  // namespace sdtw

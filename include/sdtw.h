@@ -45,6 +45,17 @@ extern "C" {
  * keeps no cost tensor (README, "Fused Mode"; paper abstract, contribution (3)). */
 typedef enum { SDTW_UNFUSED = 0, SDTW_FUSED = 1 } sdtw_mode;
 
+/* Precision flag, OR-ed into the mode of every entry point except
+ * sdtw_forward_noalloc. Long sequences at small gamma make the gradient react
+ * to cost perturbations below fp32 resolution (at N=M=8192, gamma=0.01 even an
+ * fp64 DP fed correctly rounded fp32 costs misses rel 1e-3). With this flag the
+ * cost and the forward DP state are carried as double-floats (hi + lo fp32
+ * pairs) and the forward stores per-cell transition log-probabilities for the
+ * backward; the workspace grows from 12 to 20 bytes per cell (unfused: 16 to
+ * 28). Without it the DP runs in fp32 difference form, which meets the
+ * tolerances for gamma >= 0.05 and N, M <= 2048 on the tested workloads. */
+#define SDTW_EXTENDED 2
+
 typedef enum {
     SDTW_OK = 0,
     SDTW_ERR_ARG = 1,        /* null pointer, bad mode, bad op, bad step number   */

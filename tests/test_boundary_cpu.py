@@ -53,7 +53,11 @@ def test_workspace_sizes(lib):
     for bad in [(0, 4, 4, 4), (4, 0, 4, 4), (4, 4, 0, 4), (4, 4, 4, 0)]:
         assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, *bad, L.UNFUSED) == 0
     assert L.sdtw_workspace_bytes(7, 4, 4, 4, 4, L.UNFUSED) == 0
-    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, 4, 4, 4, 4, 3) == 0
+    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, 4, 4, 4, 4, 4) == 0
+    # extended precision: 16-byte log-probabilities instead of 8-byte pairs (+8 more unfused)
+    fx = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.FUSED | L.EXTENDED)
+    ux = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.UNFUSED | L.EXTENDED)
+    assert fx - f >= slots * 8 and ux - fx >= slots * 8
 
 
 def _fwd(lib, x=0x1000, y=0x2000, B=2, N=3, M=4, D=2, gamma=1.0, mode=0, loss=0x3000, ws=0x100000,
@@ -73,7 +77,7 @@ def test_validation_codes_need_no_device(lib):
     assert _fwd(lib, gamma=-1.0) == 2
     assert _fwd(lib, gamma=float("inf")) == 2
     assert _fwd(lib, gamma=float("nan")) == 2
-    assert _fwd(lib, mode=2) == 1         # SDTW_ERR_ARG
+    assert _fwd(lib, mode=4) == 1         # SDTW_ERR_ARG
     assert _fwd(lib, x=0) == 1
     assert _fwd(lib, loss=0) == 1
     assert _fwd(lib, ws=0) == 5           # SDTW_ERR_WORKSPACE

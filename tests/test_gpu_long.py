@@ -27,12 +27,14 @@ def test_long_warped_fused(data, gamma, sample):
     from differentiable_series_alignment_gb300 import _lib as Lb
     x, y = data
     xt, yt = torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda()
-    ws = Lb.workspace(Lb.OP_FWD_BWD, B, L, L, D, Lb.FUSED)
+    mode = Lb.FUSED | Lb.auto_precision(gamma, L, L)
+    assert mode & Lb.EXTENDED
+    ws = Lb.workspace(Lb.OP_FWD_BWD, B, L, L, D, mode)
     loss = torch.empty(B, device="cuda")
     gx, gy = torch.empty_like(xt), torch.empty_like(yt)
     g = torch.full((B,), 1.0 / B, device="cuda")
-    Lb.sdtw_forward(xt, yt, gamma, Lb.FUSED, loss, ws)
-    Lb.sdtw_backward(xt, yt, gamma, Lb.FUSED, g, gx, gy, ws)
+    Lb.sdtw_forward(xt, yt, gamma, mode, loss, ws)
+    Lb.sdtw_backward(xt, yt, gamma, mode, g, gx, gy, ws)
     assert Lb.sdtw_last_device_status(ws) == 0
     loss, gx, gy = (t.cpu().numpy().astype(np.float64) for t in (loss, gx, gy))
     del ws
@@ -52,11 +54,12 @@ def test_long_normalized(data):
     xs, ys = np.ascontiguousarray(x[sub]), np.ascontiguousarray(y[sub])
     xt, yt = torch.from_numpy(xs).cuda(), torch.from_numpy(ys).cuda()
     nb = xs.shape[0]
-    ws = Lb.workspace(Lb.OP_NORMALIZED, nb, L, L, D, Lb.FUSED)
+    mode = Lb.FUSED | Lb.EXTENDED
+    ws = Lb.workspace(Lb.OP_NORMALIZED, nb, L, L, D, mode)
     loss = torch.empty(nb, device="cuda")
     gx, gy = torch.empty_like(xt), torch.empty_like(yt)
     g = torch.full((nb,), 1.0 / nb, device="cuda")
-    Lb.sdtw_normalized(xt, yt, gamma, Lb.FUSED, loss, g, gx, gy, ws)
+    Lb.sdtw_normalized(xt, yt, gamma, mode, loss, g, gx, gy, ws)
     assert Lb.sdtw_last_device_status(ws) == 0
     loss, gx, gy = (t.cpu().numpy().astype(np.float64) for t in (loss, gx, gy))
     del ws

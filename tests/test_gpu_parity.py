@@ -115,9 +115,26 @@ def test_strip_decompositions_agree(mname, mode, W):
 
 @pytest.mark.parametrize("gamma", [10.0, 1.0, 0.1, 0.01, 0.001])
 def test_small_gamma_no_nan(gamma):
+    # precision chosen as the high-level API does (double-float state below gamma 0.05)
+    L = _lib()
+    mode = L.FUSED | L.auto_precision(gamma, 300, 300)
     x, y = synth.warped_pair(2, 300, 8, 93)
-    got = check_against_oracle(x, y, gamma, 1, what=f"gamma={gamma}")
+    got = check_against_oracle(x, y, gamma, mode, what=f"gamma={gamma}")
     assert all(np.all(np.isfinite(v)) for v in got.values())
+
+
+@pytest.mark.parametrize("mname,mode", [("unfused+extended", 2), ("fused+extended", 3)])
+@pytest.mark.parametrize("N,M,D", [(1, 1, 3), (1, 7, 2), (9, 1, 1), (31, 33, 3), (100, 37, 16), (129, 130, 9)])
+def test_extended_precision_shapes(mname, mode, N, M, D):
+    x, y = synth.iid_normal_pair(3, N, M, D, 92, repeat=N * 1000 + M)
+    check_against_oracle(x, y, 0.7, mode, grad_loss=[0.5, -1.25, 2.0], what=f"{N}x{M}x{D} {mname}")
+
+
+@pytest.mark.parametrize("W", [1, 3])
+def test_extended_strip_decompositions(W):
+    x, y = synth.iid_normal_pair(2, 200, 150, 6, 91)
+    with warps(W):
+        check_against_oracle(x, y, 0.05, 3, what=f"extended W={W}")
 
 
 def test_fused_equals_unfused():
