@@ -343,13 +343,35 @@ def run_ours(args):
     return 0
 
 
+def run_profile(args):
+    """K untimed steps of the workload (both modes), for wrapping in ncu."""
+    import torch
+    from differentiable_series_alignment_gb300 import _lib as L, synth
+    L.load()
+    x_np, y_np = synth.iid_normal_pair(B, N, M, D, 1)
+    x, y = torch.from_numpy(x_np).cuda(), torch.from_numpy(y_np).cuda()
+    g = torch.full((B,), 1.0 / B, device="cuda")
+    for mode in (L.UNFUSED, L.FUSED):
+        ws = L.workspace(L.OP_FWD_BWD, B, N, M, D, mode)
+        loss, gx, gy = torch.empty(B, device="cuda"), torch.empty_like(x), torch.empty_like(y)
+        for _ in range(args.profile):
+            L.sdtw_forward(x, y, GAMMA, mode, loss, ws)
+            L.sdtw_backward(x, y, GAMMA, mode, g, gx, gy, ws)
+        assert L.sdtw_last_device_status(ws) == 0
+    torch.cuda.synchronize()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--profile", type=int, default=0, help="run this many untimed steps (for ncu) and exit")
     args = ap.parse_args()
+    if args.profile:
+        return run_profile(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
