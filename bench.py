@@ -33,6 +33,9 @@ B, N, M, D, GAMMA = 32, 512, 512, 64, 1.0
 CELLS = B * N * M
 WORKLOAD = "softdtw fwd+bwd B=32 N=M=512 D=64 gamma=1, unfused then fused"
 FALLBACK_HBM_GBS = 6800.0
+# kernels per step: unfused forward (distance, wavefront) + backward (wavefront,
+# two B-image preps, two gradient contractions), fused forward (1) + backward (5)
+LAUNCHES_PER_STEP = 2 + 5 + 1 + 5
 
 
 def log(*a):
@@ -333,7 +336,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": world * 2 * CELLS / (e2e_ms * 1e-3), "unit": "cells/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": K * 9,
+        "gpu_launches": K * LAUNCHES_PER_STEP,
         "clocks": clocks,
         "wall_s_timed": t_wall,
     }

@@ -27,7 +27,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 // Workspace layout. The status word sits at offset 0 for every op.
 struct Layout {
     size_t status, ctrl_f, ctrl_f_bytes, ctrl_b, ctrl_b_bytes;
-    size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, total;
+    size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, bimg, total;
     int P, N, M, D, NB;
 };
 
@@ -55,6 +55,7 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->e = o; o = align_up(o + sizeof(float) * slots);
     L->dsk = o; if (!fused) o = align_up(o + (ext ? sizeof(float2) : sizeof(float)) * slots);
     L->gparts = o; if (op == SDTW_OP_BARYCENTER) o = align_up(o + sizeof(float) * (size_t)P * N * D);
+    L->bimg = o; if (!ext) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, N, M, D));
     L->total = o;
     L->P = P; L->N = N; L->M = M; L->D = D; L->NB = NB;
     return true;
@@ -83,6 +84,7 @@ int choose_warps(int P, int NB, int D, bool fused, bool ext, bool backward, int 
     if (W > kMaxWarps) W = kMaxWarps;
     if (W < 1) W = 1;
     if (fused) {
+        if (W > 8) W = 8;  // fused CTAs are at most 256 threads (register budget of the cost rows)
         const size_t limit = 220 * 1024;
         const size_t per = ext ? wavex_smem_fused_per_warp(D) : wave_smem_fused_per_warp(D);
         while (W > 1 && wave_smem_fixed(W, true) + (size_t)W * per > limit) --W;
@@ -219,12 +221,12 @@ sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void
     if (out_x) {
         g.out = out_x;
         g.out_stride = (long long)L.N * L.D;
-        SDTW_CUDA(simt ? launch_grad_rows(g, st) : launch_grad_tc(g, false, status, st));
+        SDTW_CUDA(simt ? launch_grad_rows(g, st) : launch_grad_tc(g, false, at<float>(ws, L.bimg), status, st));
     }
     if (out_y) {
         g.out = out_y;
         g.out_stride = (long long)L.M * L.D;
-        SDTW_CUDA(simt ? launch_grad_cols(g, st) : launch_grad_tc(g, true, status, st));
+        SDTW_CUDA(simt ? launch_grad_cols(g, st) : launch_grad_tc(g, true, at<float>(ws, L.bimg), status, st));
     }
     return SDTW_OK;
 }

@@ -130,6 +130,99 @@ struct DistAcc {
     __device__ __forceinline__ float value() const { return hi + lo; }
 };
 
+// Packed fp32 pairs (f32x2 instructions: one issue slot for two lanes' worth
+// of arithmetic per thread).
+__device__ __forceinline__ unsigned long long pk2(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(unsigned long long v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// Squared distance of two zero-padded rows of D32 (multiple of 32) floats,
+// 16-byte aligned. Each 32-component group feeds four independent block sums
+// of 8 components (packed fp32 pairs); each block sum enters its own TwoSum
+// (hi, lo) pair, and the four pairs are combined at the end. Four independent
+// chains keep the latency short enough to hide inside a DP step. Shared by the
+// unfused cost kernel and the fused forward, so both see identical costs.
+__device__ __forceinline__ unsigned long long blk8(const float4* x4, const float4* y4) {
+    const float4 xa = x4[0], ya = y4[0], xb = x4[1], yb = y4[1];
+    unsigned long long d = sub2(pk2(xa.x, xa.y), pk2(ya.x, ya.y));
+    unsigned long long b = fma2(d, d, pk2(0.f, 0.f));
+    d = sub2(pk2(xa.z, xa.w), pk2(ya.z, ya.w));
+    b = fma2(d, d, b);
+    d = sub2(pk2(xb.x, xb.y), pk2(yb.x, yb.y));
+    b = fma2(d, d, b);
+    d = sub2(pk2(xb.z, xb.w), pk2(yb.z, yb.w));
+    return fma2(d, d, b);
+}
+__device__ __forceinline__ void fold(DistAcc& a, unsigned long long b) {
+    float e0, e1;
+    upk2(b, e0, e1);
+    a.add_block(e0 + e1);
+}
+__device__ __forceinline__ float dist_rows(const float* __restrict__ xr, const float* __restrict__ yr, int D32) {
+    const float4* x4 = reinterpret_cast<const float4*>(xr);
+    const float4* y4 = reinterpret_cast<const float4*>(yr);
+    DistAcc a0, a1, a2, a3;
+    for (int q = 0; q < (D32 >> 2); q += 8) {
+        fold(a0, blk8(x4 + q, y4 + q));
+        fold(a1, blk8(x4 + q + 2, y4 + q + 2));
+        fold(a2, blk8(x4 + q + 4, y4 + q + 4));
+        fold(a3, blk8(x4 + q + 6, y4 + q + 6));
+    }
+    float s01, e01, s23, e23, s, e;
+    two_sum(a0.hi, a1.hi, s01, e01);
+    two_sum(a2.hi, a3.hi, s23, e23);
+    two_sum(s01, s23, s, e);
+    return s + (e + ((e01 + e23) + ((a0.lo + a1.lo) + (a2.lo + a3.lo))));
+}
+
+// The same arithmetic as dist_rows with one row held in registers (DX = 32 or
+// 64 padded components) and the other row read from shared memory: `r` minus
+// the shared row, in the same block order, so the results are bit-identical.
+template <int DX>
+__device__ __forceinline__ unsigned long long blk8r(const float (&r)[DX], int o, const float4* y4) {
+    const float4 ya = y4[0], yb = y4[1];
+    unsigned long long d = sub2(pk2(r[o], r[o + 1]), pk2(ya.x, ya.y));
+    unsigned long long b = fma2(d, d, pk2(0.f, 0.f));
+    d = sub2(pk2(r[o + 2], r[o + 3]), pk2(ya.z, ya.w));
+    b = fma2(d, d, b);
+    d = sub2(pk2(r[o + 4], r[o + 5]), pk2(yb.x, yb.y));
+    b = fma2(d, d, b);
+    d = sub2(pk2(r[o + 6], r[o + 7]), pk2(yb.z, yb.w));
+    return fma2(d, d, b);
+}
+template <int DX>
+__device__ __forceinline__ float dist_reg(const float (&r)[DX], const float* __restrict__ yr) {
+    const float4* y4 = reinterpret_cast<const float4*>(yr);
+    DistAcc a0, a1, a2, a3;
+#pragma unroll
+    for (int q = 0; q < DX / 4; q += 8) {
+        fold(a0, blk8r(r, 4 * q, y4 + q));
+        fold(a1, blk8r(r, 4 * q + 8, y4 + q + 2));
+        fold(a2, blk8r(r, 4 * q + 16, y4 + q + 4));
+        fold(a3, blk8r(r, 4 * q + 24, y4 + q + 6));
+    }
+    float s01, e01, s23, e23, s, e;
+    two_sum(a0.hi, a1.hi, s01, e01);
+    two_sum(a2.hi, a3.hi, s23, e23);
+    two_sum(s01, s23, s, e);
+    return s + (e + ((e01 + e23) + ((a0.lo + a1.lo) + (a2.lo + a3.lo))));
+}
+
 // Sort three values: lo <= mid <= hi.
 __device__ __forceinline__ void sort3(float a, float b, float c, float& lo, float& mid, float& hi) {
     const float t1 = fminf(a, b), t2 = fmaxf(a, b);

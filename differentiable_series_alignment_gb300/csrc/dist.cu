@@ -13,62 +13,72 @@ namespace sdtw {
 
 namespace {
 
-constexpr int kDistT = 64;      // skewed rows per CTA
-constexpr int kDistWarps = 8;   // each warp covers kDistT / kDistWarps skewed rows
+constexpr int kDistWarps = 8;   // column tiles of 32 per CTA (one per warp), at most
 
-// grid: (ceil((M+31)/kDistT), NB, P), block: 32*kDistWarps.
+// grid: (ceil(M / (32*nw)), NB, P), block 32*nw (nw <= kDistWarps warps).
+// A CTA takes one 32-row block and 32*nw columns. Lane j of warp w holds
+// the y row of column c0 = 32*(blockIdx.x*kDistWarps + w) + j in registers
+// (DX > 0) and walks the 32 x rows, read from shared memory by every lane at
+// once (broadcast); the 32x32 tile then goes through shared memory into the
+// skewed layout. Rows are zero-padded to D32 = roundup(D, 32) components.
+template <int DX>
 __global__ void __launch_bounds__(32 * kDistWarps) dist_skew_kernel(Problems pr, int N, int M, int D,
                                                                    float* __restrict__ Dsk)
 {
-    extern __shared__ float sm[];
-    const int XS = D + 1;
-    float* xs = sm;                     // [32][XS]
-    float* ys = sm + 32 * XS;           // [kDistT + 31][XS], y rows jbase .. jbase + kDistT + 30
-    const int p = blockIdx.z, rb = blockIdx.y, t0 = blockIdx.x * kDistT;
-    const int T = M + 31;
-    const int r0 = rb * 32, jbase = t0 - 31;
+    extern __shared__ __align__(16) float sm[];
+    const int D32 = (D + 31) & ~31, XS = D32 + 4;
+    float* xs = sm;                                  // [32][XS] rows of the block
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float* tile = sm + 32 * XS + warp * 32 * 32;     // [32 rows][32 cols] per warp
+    const int nw = blockDim.x >> 5;
+    float* yw = sm + 32 * XS + nw * 1024 + warp * 32 * XS;  // [32][XS] y rows (DX == 0)
+    const int p = blockIdx.z, rb = blockIdx.y;
+    const int c0 = 32 * (blockIdx.x * nw + warp);
+    const int r0 = rb * 32;
     const float* xb = pr.x(p);
     const float* yb = pr.y(p);
-    for (int e = threadIdx.x; e < 32 * D; e += blockDim.x) {
-        const int r = e / D, k = e - r * D;
-        xs[r * XS + k] = (r0 + r < N) ? xb[(size_t)(r0 + r) * D + k] : 0.f;
+    for (int e = threadIdx.x; e < 32 * D32; e += blockDim.x) {
+        const int r = e / D32, k = e - r * D32;
+        xs[r * XS + k] = (r0 + r < N && k < D) ? xb[(size_t)(r0 + r) * D + k] : 0.f;
     }
-    const int ny = kDistT + 31;
-    for (int e = threadIdx.x; e < ny * D; e += blockDim.x) {
-        const int r = e / D, k = e - r * D;
-        const int j = jbase + r;
-        ys[r * XS + k] = (j >= 0 && j < M) ? yb[(size_t)j * D + k] : 0.f;
+    const int j = c0 + lane;
+    float yr[DX > 0 ? DX : 1];
+    if constexpr (DX > 0) {
+#pragma unroll
+        for (int k = 0; k < DX; ++k) yr[k] = (j < M && k < D) ? yb[(size_t)j * D + k] : 0.f;
+    } else {
+        for (int e = lane; e < 32 * D32; e += 32) {
+            const int r = e / D32, k = e - r * D32;
+            yw[r * XS + k] = (c0 + r < M && k < D) ? yb[(size_t)(c0 + r) * D + k] : 0.f;
+        }
     }
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int TPW = kDistT / kDistWarps;
-    DistAcc acc[TPW];
-    const int tw = t0 + warp * TPW;
-    // lane handles row r0+lane, columns j = t - lane for t in [tw, tw+TPW)
-    const int yrow0 = tw - lane - jbase;  // ys row of the first column, in [0, ny)
-    for (int k0 = 0; k0 < D; k0 += kDistBlock) {
-        const int k1 = min(k0 + kDistBlock, D);
-        float blk[TPW];
-#pragma unroll
-        for (int u = 0; u < TPW; ++u) blk[u] = 0.f;
-        for (int k = k0; k < k1; ++k) {
-            const float xv = xs[lane * XS + k];
-#pragma unroll
-            for (int u = 0; u < TPW; ++u) {
-                const float a = xv - ys[(yrow0 + u) * XS + k];
-                blk[u] = fmaf(a, a, blk[u]);
+    if (c0 < M) {
+        // d(x_i, y_j): the same arithmetic as the fused forward (x minus y)
+        for (int i = 0; i < 32; ++i) {
+            float v;
+            if constexpr (DX > 0) {
+                // dist_reg subtracts the shared row from the register row; (y - x)^2 == (x - y)^2
+                v = dist_reg<DX>(yr, xs + i * XS);
+            } else {
+                v = dist_rows(xs + i * XS, yw + lane * XS, D32);
             }
+            tile[i * 32 + lane] = v;
         }
-#pragma unroll
-        for (int u = 0; u < TPW; ++u) acc[u].add_block(blk[u]);
-    }
-    float* out = Dsk + skew_index(N, M, p, rb, 0, lane);
-#pragma unroll
-    for (int u = 0; u < TPW; ++u) {
-        const int t = tw + u;
-        if (t < T) out[(long long)t * 32] = acc[u].value();
+        __syncwarp();
+        // skewed slot t = col + row: lane = row, t = c0 + to
+        float* out = Dsk + skew_index(N, M, p, rb, 0, lane);
+        for (int to = 0; to < 63; ++to) {
+            const int cc = to - lane;  // column within the tile for this lane's row
+            if (cc >= 0 && cc < 32 && c0 + cc < M && r0 + lane < N)
+                out[(long long)(c0 + to) * 32] = tile[lane * 32 + cc];
+        }
     }
 }
+
+}  // namespace
+
+namespace {
 
 // grid: (ceil(M/32), ceil(N/8), P), block (32, 8).
 __global__ void dist_rowmajor_kernel(Problems pr, int N, int M, int D, float* __restrict__ C)
@@ -95,13 +105,24 @@ __global__ void dist_rowmajor_kernel(Problems pr, int N, int M, int D, float* __
 
 cudaError_t launch_dist_skewed(const Problems& pr, int P, int N, int M, int D, float* Dsk, cudaStream_t st)
 {
-    const int T = M + 31;
-    dim3 grid((T + kDistT - 1) / kDistT, (N + 31) / 32, P);
-    const size_t smem = (size_t)(32 + kDistT + 31) * (D + 1) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(dist_skew_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    dist_skew_kernel<<<grid, 32 * kDistWarps, smem, st>>>(pr, N, M, D, Dsk);
-    return cudaGetLastError();
+    const int D32 = (D + 31) & ~31, XS = D32 + 4;
+    const int dx = (D <= 32) ? 32 : (D <= 64 ? 64 : 0);
+    auto bytes = [&](int nw) {
+        size_t b = (size_t)(32 * XS + nw * 1024) * sizeof(float);
+        if (dx == 0) b += (size_t)nw * 32 * XS * sizeof(float);
+        return b;
+    };
+    int nw = kDistWarps;
+    while (nw > 1 && bytes(nw) > 220 * 1024) --nw;
+    const size_t smem = bytes(nw);
+    dim3 grid((M + 32 * nw - 1) / (32 * nw), (N + 31) / 32, P);
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, 32 * nw, smem, st>>>(pr, N, M, D, Dsk);
+        return cudaGetLastError();
+    };
+    return dx == 32 ? go(dist_skew_kernel<32>) : dx == 64 ? go(dist_skew_kernel<64>) : go(dist_skew_kernel<0>);
 }
 
 cudaError_t launch_dist_rowmajor(const Problems& pr, int P, int N, int M, int D, float* C, cudaStream_t st)

@@ -73,8 +73,10 @@ struct GradParams {
 };
 cudaError_t launch_grad_rows(const GradParams& g, cudaStream_t st);
 // The same contractions on the tensor cores (tcgen05, 3xTF32); cols selects grad_y.
-cudaError_t launch_grad_tc(const GradParams& g, bool cols, int* status, cudaStream_t st);
+// bimg: workspace for the pre-split B operand images (egemm_bimg_bytes).
+cudaError_t launch_grad_tc(const GradParams& g, bool cols, float* bimg, int* status, cudaStream_t st);
 size_t egemm_smem_bytes(int D);
+size_t egemm_bimg_bytes(int P, int N, int M, int D);
 cudaError_t launch_grad_cols(const GradParams& g, cudaStream_t st);
 
 // Barycenter: grad = (1/K) sum_k gparts[k]; Adam update of z, m, v; mean loss.

@@ -112,6 +112,7 @@ extern "C" sdtw_status sdtw_forward_noalloc(const float* x, const float* y, int 
     if (W > kMaxWarps) W = kMaxWarps;
     if (W < 1) W = 1;
     if (fused) {
+        if (W > 8) W = 8;
         while (W > 1 && wave_smem_fixed(W, false) + (size_t)W * wave_smem_fused_per_warp(D) > 220 * 1024) --W;
     }
 

@@ -34,10 +34,46 @@ namespace sdtw {
 namespace {
 
 struct FusedSmem {
-    float* xs;  // [32][XS]  rows of this warp, zero padded
-    float* ys;  // [32][XS]  current 32 columns of y
-    float* dt;  // [64][32]  two tiles of raw cost, slot (col & 63), lane
+    float* xs;  // [32][XS]     rows of this warp, zero padded to D4
+    float* ys;  // [2][32][XS]  y rows of the next two 32-column tiles (cp.async double buffer)
+    float* dt;  // [64][32]     raw cost of two 32-column tiles, slot (col & 63), lane
 };
+
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4f(float* dst, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+
+// Stage y rows [c0, c0+32) of one problem into a [32][XS] tile (zero padded).
+// Asynchronous (cp.async); the caller waits with cp.async.wait_all + __syncwarp.
+__device__ __forceinline__ void stage_y_tile(float* tile, const float* yb, int c0, int M, int D, int D4, int XS,
+                                             int lane)
+{
+    const bool vec = ((D & 3) == 0) && ((reinterpret_cast<uintptr_t>(yb) & 15) == 0);
+    if (vec) {
+        const int per = D4 >> 2;  // float4 per (padded) row
+        for (int e = lane; e < 32 * per; e += 32) {
+            const int r = e / per, q = e - r * per;
+            float* dst = tile + r * XS + 4 * q;
+            if (c0 + r < M && 4 * q < D) cp_async16(dst, yb + (size_t)(c0 + r) * D + 4 * q);
+            else *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    } else {
+        for (int e = lane; e < 32 * D4; e += 32) {
+            const int r = e / D4, k = e - r * D4;
+            float* dst = tile + r * XS + k;
+            if (c0 + r < M && k < D) cp_async4f(dst, yb + (size_t)(c0 + r) * D + k);
+            else *dst = 0.f;
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
 
 }  // namespace
 
@@ -51,8 +87,10 @@ template <bool ACC> __device__ __forceinline__ float dp_log2(float x) { return A
 // ---------------------------------------------------------------------------
 // Forward
 // ---------------------------------------------------------------------------
-template <bool FUSED, bool ACC>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams q)
+// DX (fused only): 32 or 64 keeps the warp's x rows in registers, padded to DX
+// components (D <= DX); 0 reads them from shared memory (D > 64).
+template <bool FUSED, bool ACC, int DX>
+__global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(const WaveParams q)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int W = q.W;
@@ -84,24 +122,47 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams
 
     float c0 = 0.f;  // scaled d(i, 0)
 
+    // Fused: each warp keeps its 32 rows of x, y rows of the next two 32-column
+    // tiles and the raw costs of two tiles. The cost of column s+32 is computed
+    // for all 32 rows during DP step s, one column per step, interleaved with the
+    // latency-bound recursion.
     FusedSmem fz{};
-    int XS = 0;
+    int XS = 0, D4 = 0;
     const float* yb = q.pr.y(p);
     if (FUSED) {
-        const int D = q.D, D4 = (D + 3) & ~3;
+        const int D = q.D;
+        D4 = (D + 31) & ~31;   // rows zero-padded to whole 32-component groups
         XS = D4 + 4;
         float* base = reinterpret_cast<float*>(smem_raw + q.smem_fixed);
-        float* mine = base + (size_t)warp * (64 * XS + 64 * 32);
+        float* mine = base + (size_t)warp * (96 * XS + 64 * 32);
         fz.xs = mine;
         fz.ys = mine + 32 * XS;
-        fz.dt = mine + 64 * XS;
+        fz.dt = mine + 96 * XS;
         const float* xb = q.pr.x(p);
         for (int e = lane; e < 32 * D4; e += 32) {
             const int r = e / D4, k = e - r * D4;
             fz.xs[r * XS + k] = (r0 + r < N && k < D) ? xb[(size_t)(r0 + r) * D + k] : 0.f;
         }
-        __syncwarp();
+        if (active) {
+            stage_y_tile(fz.ys, yb, 0, M, D, D4, XS, lane);             // tile 0 -> buffer 0
+            stage_y_tile(fz.ys + 32 * XS, yb, 32, M, D, D4, XS, lane);  // tile 1 -> buffer 1
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+            __syncwarp();
+        }
     }
+    float xr[DX > 0 ? DX : 1];
+    if constexpr (FUSED && DX > 0) {
+#pragma unroll
+        for (int k = 0; k < DX; ++k) xr[k] = fz.xs[lane * XS + k];
+    }
+    if (FUSED && active) {
+        for (int c = 0; c < 32 && c < M; ++c) {  // costs of tile 0
+            if constexpr (DX > 0) fz.dt[c * 32 + lane] = dist_reg<DX>(xr, fz.ys + c * XS);
+            else fz.dt[c * 32 + lane] = dist_rows(fz.xs + lane * XS, fz.ys + c * XS, D4);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+    if (FUSED) __syncwarp();
 
     if (active) {
         const long long sk = skew_index(N, M, p, rb, 0, lane);
@@ -123,8 +184,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams
         if (top_global && lane < kGroup && lane < M) nxt[0] = slot_load(edge_in + lane);
 
         float h_prev = 0.f, v_prev = 0.f;
-        // raw costs of the next kGroup steps; slot u is refilled with the following
-        // group's value as soon as step u has consumed it
+        // raw costs of the next group of steps (loaded one group ahead)
         float dbuf[kGroup];
         if (!FUSED) {
 #pragma unroll
@@ -133,44 +193,25 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams
         const int nG = T / kGroup;
         for (int g = 0; g < nG; ++g) {
             const int s0 = g * kGroup;
-            if (FUSED && (s0 & 31) == 0 && s0 < M) {
-                // Raw cost of columns [s0, s0+32) for this warp's 32 rows.
-                const int D = q.D, D4 = (D + 3) & ~3;
-                __syncwarp();
-                for (int e = lane; e < 32 * D4; e += 32) {
-                    const int r = e / D4, k = e - r * D4;
-                    const int col = s0 + r;
-                    fz.ys[r * XS + k] = (col < M && k < D) ? yb[(size_t)col * D + k] : 0.f;
+            float dcur[kGroup];
+            if (!FUSED) {  // this group's raw costs; the next group's loads go out now
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u) dcur[u] = dbuf[u];
+                if (g + 1 < nG) {
+#pragma unroll
+                    for (int u = 0; u < kGroup; ++u) dbuf[u] = dp[(long long)(s0 + kGroup + u) * 32];
                 }
+            }
+            if (FUSED && (s0 & 31) == 0) {
+                // New period s0/32: the y rows of tile s0/32 + 1 (costed during this
+                // period) have arrived; the buffer of tile s0/32, whose costs are
+                // complete, is restaged with tile s0/32 + 2. Each lane reads and
+                // writes only its own row's cost slots, so the costs need no barrier.
+                asm volatile("cp.async.wait_all;" ::: "memory");
                 __syncwarp();
-                for (int half = 0; half < 32; half += 16) {
-                    DistAcc acc[16];
-                    for (int k0 = 0; k0 < D4; k0 += kDistBlock) {
-                        float blk[16];
-#pragma unroll
-                        for (int cc = 0; cc < 16; ++cc) blk[cc] = 0.f;
-                        for (int k4 = k0; k4 < min(k0 + kDistBlock, D4); k4 += 4) {
-                            const float4 xv = *reinterpret_cast<const float4*>(fz.xs + lane * XS + k4);
-#pragma unroll
-                            for (int cc = 0; cc < 16; ++cc) {
-                                const float4 yv = *reinterpret_cast<const float4*>(fz.ys + (half + cc) * XS + k4);
-                                float a = xv.x - yv.x;
-                                blk[cc] = fmaf(a, a, blk[cc]);
-                                a = xv.y - yv.y;
-                                blk[cc] = fmaf(a, a, blk[cc]);
-                                a = xv.z - yv.z;
-                                blk[cc] = fmaf(a, a, blk[cc]);
-                                a = xv.w - yv.w;
-                                blk[cc] = fmaf(a, a, blk[cc]);
-                            }
-                        }
-#pragma unroll
-                        for (int cc = 0; cc < 16; ++cc) acc[cc].add_block(blk[cc]);
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < 16; ++cc) fz.dt[((s0 + half + cc) & 63) * 32 + lane] = acc[cc].value();
-                }
-                __syncwarp();
+                const int cnext = s0 + 64;  // first column of tile s0/32 + 2
+                if (cnext < M)
+                    stage_y_tile(fz.ys + ((cnext >> 5) & 1) * 32 * XS, yb, cnext, M, q.D, D4, XS, lane);
             }
 
             // Upper-neighbour values for lane 0: lane q holds column s0 + q.
@@ -210,9 +251,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwd_kernel(const WaveParams
                 float draw;
                 if (FUSED) {
                     draw = fz.dt[(j & 63) * 32 + lane];
+                    // cost of column s+32 (past the last column it is computed from zero rows
+                    // and never read): branch-free, so it interleaves with the DP chain
+                    const int cn = s + 32;
+                    const float* yrow = fz.ys + ((cn >> 5) & 1) * 32 * XS + (cn & 31) * XS;
+                    if constexpr (DX > 0) fz.dt[(cn & 63) * 32 + lane] = dist_reg<DX>(xr, yrow);
+                    else fz.dt[(cn & 63) * 32 + lane] = dist_rows(fz.xs + lane * XS, yrow, D4);
                 } else {
-                    draw = dbuf[u];
-                    if (g + 1 < nG) dbuf[u] = dp[(long long)(s0 + kGroup + u) * 32];
+                    draw = dcur[u];
                 }
                 const float d = draw * scale;
                 // t = d + softmin(0, vl, hu) = d + lo - log2(1 + 2^(lo-mid) + 2^(lo-hi))
@@ -336,6 +382,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
     for (int g = 0; g < nG; ++g) {
         const int t0 = g * kGroup;   // first reverse step of the group
         const int k0 = t0 - off;     // channel slot read by lane 31 at that step
+        VT bcur[EXT ? 1 : kGroup];
+        if (!EXT) {  // this group's state; the next group's loads go out now
+#pragma unroll
+            for (int u = 0; u < kGroup; ++u) bcur[u] = buf[u];
+            if (g + 1 < nG) {
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u) buf[u] = vhp[(long long)(T - 1 - (t0 + kGroup + u)) * 32];
+            }
+        }
         // Messages of the row below for lane 31: lane q holds slot k0 + q.
         float2 botv = make_float2(-kBig, -kBig);
         bool ok = true;
@@ -385,8 +440,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
             sort3(a1, a2, a3, lo, mid, hi);
             float lE = hi + dp_log2<ACC>((1.f + dp_exp2<ACC>(mid - hi)) + dp_exp2<ACC>(lo - hi));
             lE = (last_lane && j == M - 1) ? 0.f : lE;
-            const VT cur = buf[u];
-            if (g + 1 < nG) buf[u] = vhp[(long long)(T - 1 - (t0 + kGroup + u)) * 32];
+            VT cur;
+            if (EXT) {  // single buffer (register budget): refill slot u right after use
+                cur = buf[u];
+                buf[u] = vhp[(long long)(T - 1 - min(t0 + kGroup + u, T - 1)) * 32];
+            } else {
+                cur = bcur[u];
+            }
             float wl, wu, wd;  // transition log2-probabilities of this cell to its left/up/diag predecessors
             if (EXT) {
                 const float4 st = reinterpret_cast<const float4&>(cur);
@@ -428,9 +488,9 @@ size_t wave_smem_fixed(int W, bool backward)
 
 size_t wave_smem_fused_per_warp(int D)
 {
-    const int D4 = (D + 3) & ~3;
+    const int D4 = (D + 31) & ~31;
     const int XS = D4 + 4;
-    return (size_t)(64 * XS + 64 * 32) * sizeof(float);
+    return (size_t)(96 * XS + 64 * 32) * sizeof(float);
 }
 
 // Dynamic shared memory requested by every wavefront CTA, at least. The DP is
@@ -465,8 +525,15 @@ cudaError_t launch_forward(WaveParams q, bool fused, cudaStream_t st)
         kern<<<grid, q.W * 32, smem, st>>>(q);
         return cudaGetLastError();
     };
-    if (fused) return q.accurate ? go(fwd_kernel<true, true>) : go(fwd_kernel<true, false>);
-    return q.accurate ? go(fwd_kernel<false, true>) : go(fwd_kernel<false, false>);
+    if (fused) {
+        const int dx = (q.D <= 32) ? 32 : (q.D <= 64 ? 64 : 0);
+        if (q.accurate)
+            return dx == 32 ? go(fwd_kernel<true, true, 32>) : dx == 64 ? go(fwd_kernel<true, true, 64>)
+                                                                   : go(fwd_kernel<true, true, 0>);
+        return dx == 32 ? go(fwd_kernel<true, false, 32>) : dx == 64 ? go(fwd_kernel<true, false, 64>)
+                                                                : go(fwd_kernel<true, false, 0>);
+    }
+    return q.accurate ? go(fwd_kernel<false, true, 0>) : go(fwd_kernel<false, false, 0>);
 }
 
 cudaError_t launch_backward(WaveParams q, cudaStream_t st)
