@@ -95,7 +95,7 @@ class SoftDTW:
     fused=False stores the (B,N,M) cost tensor; fused=True recomputes it inside
     the DP kernels. normalize=True gives s(x,y) - (s(x,x) + s(y,y))/2 and needs
     x.shape == y.shape. extended=None picks the double-float forward state for
-    small gamma or long sequences (auto_precision); True/False forces it.
+    small gamma, long sequences or D > 64 (auto_precision); True/False forces it.
     """
 
     def __init__(self, gamma: float = 1.0, dist: str = "sqeuclidean", fused: bool = False,
@@ -113,7 +113,7 @@ class SoftDTW:
         fn = _NormalizedFn if self.normalize else _SoftDTWFn
         mode = FUSED if self.fused else UNFUSED
         if self.extended is None:
-            mode |= auto_precision(self.gamma, x.shape[1], y.shape[1])
+            mode |= auto_precision(self.gamma, x.shape[1], y.shape[1], x.shape[2])
         elif self.extended:
             mode |= EXTENDED
         return fn.apply(x, y, self.gamma, mode)
@@ -130,7 +130,7 @@ def softdtw_barycenter(sequences: torch.Tensor, gamma: float = 1.0, max_iter: in
     T = z.shape[0]
     m = torch.zeros_like(z)
     v = torch.zeros_like(z)
-    mode = (FUSED if fused else UNFUSED) | auto_precision(gamma, T, T2)
+    mode = (FUSED if fused else UNFUSED) | auto_precision(gamma, T, T2, D)
     ws = workspace(OP_BARYCENTER, K, T, T2, D, mode, X.device)
     losses = torch.empty(max_iter, dtype=torch.float32, device=X.device)
     for t in range(1, max_iter + 1):

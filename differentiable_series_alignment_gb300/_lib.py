@@ -117,10 +117,16 @@ def _mode(mode) -> int:
     return int(mode)
 
 
-def auto_precision(gamma: float, N: int, M: int) -> int:
-    """EXTENDED where fp32 difference-form DP state is not accurate enough for
-    the gradient tolerance: small gamma or long sequences."""
-    return EXTENDED if (gamma < 0.05 or max(N, M) >= 4096) else 0
+def auto_precision(gamma: float, N: int, M: int, D: int | None = None) -> int:
+    """EXTENDED where the fp32 path is not accurate enough for gradients within
+    rel 1e-3 / abs 1e-5: small gamma, long sequences, or wide features (D > 64).
+
+    With wide features the costs (about 2*D for unit-variance data) and the DP
+    state carry fp32 rounding of ~1e-7 relative, which the DP compounds into
+    ~1e-5 relative error in E; near-zero gradient entries then miss abs 1e-5
+    once the upstream gradient is O(1)."""
+    wide = D is not None and D > 64
+    return EXTENDED if (gamma < 0.05 or max(N, M) >= 4096 or wide) else 0
 
 
 def sdtw_workspace_bytes(op: int, B: int, N: int, M: int, D: int, mode) -> int:

@@ -6,16 +6,17 @@
 // One CTA computes 128 output rows (tcgen05 M = 128) against all D+1 output
 // columns (the extra column of ones yields the row or column sums of E in the
 // same MMA). The reduction runs over the other sequence in K-tiles of 32. Each
-// A-tile's skewed rows of E arrive by bulk copy (cp.async.bulk) and the CTA's
-// threads un-skew them, split each value into tf32 hi + lo parts (round to
+// A-tile's skewed rows of E arrive by bulk copy (cp.async.bulk); eight worker
+// warps un-skew them, split each value into tf32 hi + lo parts (round to
 // nearest) and store both in the 128-byte-swizzled K-major layout. The B tiles
 // ([Y | 1] or [X | 1]) are the same for every CTA of a problem, so a small
 // kernel writes them once, already split and swizzled, and each CTA fetches a
-// K-tile's B image with one bulk copy. One thread issues the 3xTF32 products
-// hi*hi + lo*hi + hi*lo with tcgen05.mma (fp32 accumulation in tensor memory),
-// committed to an mbarrier. Two smem stages let the copies and un-skew of tile
-// k+1 overlap the MMAs of tile k. The epilogue reads the accumulators back with
-// tcgen05.ld.
+// K-tile's B image with one bulk copy. A ninth warp issues the copies and the
+// 3xTF32 products hi*hi + lo*hi + hi*lo with tcgen05.mma (fp32 accumulation in
+// tensor memory); workers and issuer hand buffers over through mbarriers, so
+// the un-skew of tile k+1 overlaps the MMAs of tile k and the copies run two to
+// four K-tiles ahead. The epilogue reads the accumulators back with tcgen05.ld
+// and writes the gradient rows through a shared-memory tile.
 //
 // Precision: each split product carries ~2^-21 relative error, so E . y keeps
 // ~1e-6 relative accuracy; the gradient is a difference of two such sums that
@@ -29,7 +30,7 @@ namespace {
 
 constexpr int kBM = 128;       // output rows per CTA (MMA M)
 constexpr int kBK = 32;        // reduction elements per K-tile (128 bytes of fp32 per smem row)
-constexpr int kThreads = 256;  // 8 warps; warps w and w+4 share TMEM lane quarter w
+constexpr size_t kSmemLimit = 227 * 1024 - 256;  // opt-in dynamic shared memory, minus static
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -178,7 +179,7 @@ __device__ __forceinline__ void issue_a(const float* Ekp, int N, int M, int T, i
 }
 
 // B operand image of K-tile kt: hi then lo tiles (n_total rows x 128 B each),
-// already split and swizzled; one bulk copy into the tile stage.
+// already split and swizzled; one bulk copy. Called by one thread.
 __device__ __forceinline__ void issue_b(const float* img, int n_total, int kt, unsigned char* B_hi, uint32_t bar)
 {
     const uint32_t bytes = 2u * (uint32_t)n_total * 128u;
@@ -187,21 +188,57 @@ __device__ __forceinline__ void issue_b(const float* img, int n_total, int kt, u
     bulk_g2s(smem_u32(B_hi), img + (size_t)kt * (bytes / 4), bytes, bar);
 }
 
+// Pipeline depths (egemm_plan): ts A-tile stages, pb B-image buffers, pa raw-A buffers.
+struct Pipe {
+    int ts, pb, pa;
+};
+
+constexpr int kMaxRing = 4;
+constexpr int kWorkers = 256;            // warps 0-7: un-skew and epilogue
+constexpr int kIssuer = 8;               // warp 8: bulk copies and MMAs (lane 0)
+constexpr int kStageStride = 65;         // epilogue staging row stride (floats)
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void workers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
+}
+
+// Sticky bounded wait: after one timeout the caller stops waiting (the status word
+// already carries the error) so the kernel ends in bounded time.
+__device__ __forceinline__ void wait_ok(bool& ok, uint32_t bar, uint32_t parity, int* status) {
+    if (ok) ok = mbar_wait(bar, parity, status);
+}
+
 // COLS = false: grad_x rows (A = E rows i, K = j, B = [Y | 1]).
 // COLS = true : grad_y rows (A = E columns j, K = i, B = [X | 1]).
 // bimg: per problem, per K-tile, the pre-split B image (bimg_kernel).
+//
+// Warp-specialised pipeline, all hand-offs through mbarriers:
+//   issuer  : raw A copy (tile kt+pa) into entry kt%pa once the workers release tile kt;
+//             B image (tile kt+pb-1) once MMA(kt-1) has freed its buffer;
+//             MMAs of tile kt once its A stage is full and its B image has landed,
+//             committed to the A-stage and B-buffer "empty" barriers.
+//   workers : wait for raw A of tile kt and for A stage kt%ts to be empty (MMA(kt-ts)),
+//             un-skew + split into the stage, then each warp arrives on "raw empty" and
+//             "A full". After the last commit they stage the accumulators through shared
+//             memory and write the gradient rows with coalesced stores.
+// Barrier parities: entry e of a ring of depth P serves tiles e, e+P, ...; tile k's
+// phase has parity (k/P)&1 and every wait is for the oldest phase not yet reused.
 template <bool COLS>
-__global__ void __launch_bounds__(kThreads, 1)
-    egemm_kernel(const GradParams g, const float* __restrict__ bimg, int n_total, int tstages, int* status)
+__global__ void __launch_bounds__(kWorkers + 32, 1)
+    egemm_kernel(const GradParams g, const float* __restrict__ bimg, int n_total, Pipe pp, int* status)
 {
     extern __shared__ unsigned char smem_dyn[];
-    __shared__ uint64_t s_mma[2];   // MMA completion per tile stage
-    __shared__ uint64_t s_raw[2];   // A bulk copies per raw buffer
-    __shared__ uint64_t s_bim[2];   // B image copies per tile stage
+    __shared__ uint64_t s_raw_full[kMaxRing], s_raw_empty[kMaxRing];
+    __shared__ uint64_t s_b_full[kMaxRing], s_b_empty[kMaxRing];
+    __shared__ uint64_t s_a_full[2], s_a_empty[2];
+    __shared__ uint64_t s_acc;
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
     const int p = blockIdx.y;
     const int m0 = blockIdx.x * kBM;
     const int N = g.N, M = g.M, D = g.D, T = skew_T(M);
@@ -209,30 +246,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kdim = COLS ? N : M;     // reduction length
     const int NB = (N + 31) / 32;
     const int nK = (kdim + kBK - 1) / kBK;
+    const int ts = pp.ts, pb = pp.pb, pa = pp.pa;
+    // [B_hi; B_lo] as one operand of 2*n_total rows: A_hi x [B_hi; B_lo] + A_lo x B_hi
+    const bool stacked = 2 * n_total <= 256;
     const float* Ekp = g.E + skew_index(N, M, p, 0, 0, 0);
-    const float* xb = g.pr.x(p);
-    const float* yb = g.pr.y(p);
     const float* bimg_p = bimg + (size_t)p * nK * 2 * n_total * 32;
 
-    // Shared memory (1 KiB aligned): tile stages [A hi | A lo | B hi | B lo], then 2 raw A buffers.
+    // Shared memory (1 KiB aligned): ts A stages [hi | lo], pb B images [hi | lo], pa raw A buffers.
     const uint32_t a_bytes = kBM * 128, b_bytes = (uint32_t)n_total * 128;
-    const uint32_t stage_bytes = 2 * a_bytes + 2 * b_bytes;
     const uint32_t rawA_bytes = Raw<COLS>::kBytes;
     unsigned char* base = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
-    unsigned char* raw0 = base + tstages * stage_bytes;
-    auto stage = [&](int st) { return base + st * stage_bytes; };
-    auto rawA = [&](int r) { return raw0 + r * rawA_bytes; };
+    unsigned char* bbase = base + ts * 2 * a_bytes;
+    unsigned char* rbase = bbase + pb * 2 * b_bytes;
+    auto astage = [&](int kt) { return base + (kt % ts) * 2 * a_bytes; };
+    auto bbuf = [&](int kt) { return bbase + (kt % pb) * 2 * b_bytes; };
+    auto rawA = [&](int kt) { return rbase + (kt % pa) * rawA_bytes; };
 
     if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&s_mma[b]), 1);
-            mbar_init(smem_u32(&s_raw[b]), 1);
-            mbar_init(smem_u32(&s_bim[b]), 1);
+        for (int b = 0; b < kMaxRing; ++b) {
+            mbar_init(smem_u32(&s_raw_full[b]), 1);
+            mbar_init(smem_u32(&s_raw_empty[b]), kWorkers / 32);
+            mbar_init(smem_u32(&s_b_full[b]), 1);
+            mbar_init(smem_u32(&s_b_empty[b]), 1);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&s_a_full[b]), kWorkers / 32);
+            mbar_init(smem_u32(&s_a_empty[b]), 1);
+        }
+        mbar_init(smem_u32(&s_acc), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     int ncols = 32;
-    while (ncols < n_total) ncols <<= 1;
+    while (ncols < (stacked ? 2 * n_total : n_total)) ncols <<= 1;
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
                      "r"(ncols)
@@ -243,123 +288,207 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = s_tmem;
-
-    uint32_t mma_ph[2] = {0u, 0u}, raw_ph[2] = {0u, 0u}, bim_ph[2] = {0u, 0u};
     bool ok = true;
-    if (tid == 0) {
-        issue_a<COLS>(Ekp, N, M, T, m0, 0, rawA(0), smem_u32(&s_raw[0]));
-        issue_b(bimg_p, n_total, 0, stage(0) + 2 * a_bytes, smem_u32(&s_bim[0]));
-    }
-    for (int kt = 0; kt < nK; ++kt) {
-        const int r = kt & 1;
-        const int s = (tstages == 2) ? (kt & 1) : 0;
-        // A raw rows and the B image of tile kt have landed
-        ok = mbar_wait(smem_u32(&s_raw[r]), raw_ph[r], status) && ok;
-        raw_ph[r] ^= 1u;
-        ok = mbar_wait(smem_u32(&s_bim[s]), bim_ph[s], status) && ok;
-        bim_ph[s] ^= 1u;
-        __syncthreads();
-        // prefetch the A rows of tile kt+1 into the other raw buffer (last read before the
-        // barrier that ended iteration kt-1)
-        if (tid == 0 && kt + 1 < nK) issue_a<COLS>(Ekp, N, M, T, m0, kt + 1, rawA(r ^ 1), smem_u32(&s_raw[r ^ 1]));
-        unsigned char* A_hi = stage(s);
-        unsigned char* A_lo = A_hi + a_bytes;
-        const int k0 = kt * kBK;
-        const float* ra = reinterpret_cast<const float*>(rawA(r));
 
-        // ---- A tile: un-skew and split (zero outside the matrix)
-        if (!COLS) {
-            // warps w, w+4: row block m0/32 + (w mod 4), columns split in halves; lane = row
-            const int rb = (m0 >> 5) + quarter;
-            const int i = m0 + 32 * quarter + lane;
-            const float* rw = ra + quarter * 64 * 32;
-#pragma unroll 8
-            for (int cc = 0; cc < kBK / 2; ++cc) {
-                const int c = half * (kBK / 2) + cc;
-                const int j = k0 + c;
-                const float v = (rb < NB && i < N && j < M) ? rw[(c + lane) * 32 + lane] : 0.f;
-                put(A_hi, A_lo, 32 * quarter + lane, c, v);
+    if (warp == kIssuer) {
+        if (lane == 0) {
+            int a_last[kMaxRing], b_last[kMaxRing];  // last tile copied into each entry
+            for (int e = 0; e < kMaxRing; ++e) a_last[e] = b_last[e] = -1;
+            for (int k = 0; k < pa && k < nK; ++k) {
+                issue_a<COLS>(Ekp, N, M, T, m0, k, rawA(k), smem_u32(&s_raw_full[k % pa]));
+                a_last[k % pa] = k;
             }
-        } else {
-            // raw row tt holds slot m0 + tt of block k0/32; lane = K index i - k0; output row r = tt - lane
-            const int i = k0 + lane;
-#pragma unroll 4
-            for (int rr = warp; rr < kBM; rr += 8) {
-                const int j = m0 + rr;
-                const float v = (i < N && j < M) ? ra[(rr + lane) * 32 + lane] : 0.f;
-                put(A_hi, A_lo, rr, lane, v);
+            for (int k = 0; k < pb - 1 && k < nK; ++k) {
+                issue_b(bimg_p, n_total, k, bbuf(k), smem_u32(&s_b_full[k % pb]));
+                b_last[k % pb] = k;
+            }
+            for (int kt = 0; kt < nK && ok; ++kt) {
+                const int kb = kt + pb - 1;  // its buffer was last read by MMA(kt - 1)
+                if (kb < nK) {
+                    if (kb >= pb) wait_ok(ok, smem_u32(&s_b_empty[kb % pb]), (uint32_t)(((kb - pb) / pb) & 1), status);
+                    if (!ok) break;
+                    issue_b(bimg_p, n_total, kb, bbuf(kb), smem_u32(&s_b_full[kb % pb]));
+                    b_last[kb % pb] = kb;
+                }
+                wait_ok(ok, smem_u32(&s_a_full[kt % ts]), (uint32_t)((kt / ts) & 1), status);
+                wait_ok(ok, smem_u32(&s_b_full[kt % pb]), (uint32_t)((kt / pb) & 1), status);
+                if (!ok) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t ah = smem_u32(astage(kt)), al = ah + a_bytes;
+                const uint32_t bh = smem_u32(bbuf(kt)), bl = bh + b_bytes;
+                if (stacked) {
+                    const uint32_t id2 = idesc_tf32(kBM, 2 * n_total), id1 = idesc_tf32(kBM, n_total);
+#pragma unroll
+                    for (int ks = 0; ks < kBK / 8; ++ks) {
+                        const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
+                        mma_tf32(tmem, sdesc(ah + ko), sdesc(bh + ko), id2, (kt > 0 || ks > 0) ? 1u : 0u);
+                        mma_tf32(tmem, sdesc(al + ko), sdesc(bh + ko), id1, 1u);
+                    }
+                } else {
+                    for (int n0 = 0; n0 < n_total; n0 += 256) {
+                        const int nn = min(256, n_total - n0);
+                        const uint32_t id = idesc_tf32(kBM, nn);
+                        const uint32_t d = tmem + (uint32_t)n0;
+                        const uint32_t boff = (uint32_t)n0 * 128;
+#pragma unroll
+                        for (int ks = 0; ks < kBK / 8; ++ks) {
+                            const uint32_t ko = ks * 32;
+                            mma_tf32(d, sdesc(ah + ko), sdesc(bh + boff + ko), id, (kt > 0 || ks > 0) ? 1u : 0u);
+                            mma_tf32(d, sdesc(al + ko), sdesc(bh + boff + ko), id, 1u);
+                            mma_tf32(d, sdesc(ah + ko), sdesc(bl + boff + ko), id, 1u);
+                        }
+                    }
+                }
+                mma_commit(smem_u32(&s_a_empty[kt % ts]));
+                mma_commit(smem_u32(&s_b_empty[kt % pb]));
+                const int ka = kt + pa;  // entry kt % pa, released after the un-skew of tile kt
+                if (ka < nK) {
+                    wait_ok(ok, smem_u32(&s_raw_empty[kt % pa]), (uint32_t)((kt / pa) & 1), status);
+                    if (!ok) break;
+                    issue_a<COLS>(Ekp, N, M, T, m0, ka, rawA(ka), smem_u32(&s_raw_full[ka % pa]));
+                    a_last[ka % pa] = ka;
+                }
+            }
+            // releases the workers once every MMA issued above has completed
+            mma_commit(smem_u32(&s_acc));
+            // no copy may still be writing shared memory when the CTA exits
+            bool drained = true;
+            for (int e = 0; e < kMaxRing; ++e) {
+                if (a_last[e] >= 0) wait_ok(drained, smem_u32(&s_raw_full[e]), (uint32_t)((a_last[e] / pa) & 1), status);
+                if (b_last[e] >= 0) wait_ok(drained, smem_u32(&s_b_full[e]), (uint32_t)((b_last[e] / pb) & 1), status);
             }
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-
-        if (tid == 0) {
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t ah = smem_u32(A_hi), al = smem_u32(A_lo);
-            const uint32_t bh = smem_u32(A_hi + 2 * a_bytes), bl = bh + b_bytes;
-            for (int n0 = 0; n0 < n_total; n0 += 256) {
-                const int nn = min(256, n_total - n0);
-                const uint32_t id = idesc_tf32(kBM, nn);
-                const uint32_t d = tmem + (uint32_t)n0;
-                const uint32_t boff = (uint32_t)n0 * 128;
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3, half = warp >> 2;
+        for (int kt = 0; kt < nK; ++kt) {
+            wait_ok(ok, smem_u32(&s_raw_full[kt % pa]), (uint32_t)((kt / pa) & 1), status);
+            if (kt >= ts) wait_ok(ok, smem_u32(&s_a_empty[kt % ts]), (uint32_t)(((kt - ts) / ts) & 1), status);
+            unsigned char* A_hi = astage(kt);
+            unsigned char* A_lo = A_hi + a_bytes;
+            const int k0 = kt * kBK;
+            const float* ra = reinterpret_cast<const float*>(rawA(kt));
+            if (!COLS) {
+                // warps w, w+4: row block m0/32 + (w mod 4), lane = row, 16-byte chunks
+                // 4*half .. 4*half+3 of the row. The skewed reads hit bank `lane`; in the
+                // swizzled stores each 8-lane phase covers the 8 chunk slots of one atom.
+                const int rb = (m0 >> 5) + quarter;
+                const int rloc = 32 * quarter + lane;
+                const bool rowok = rb < NB && m0 + rloc < N;
+                const float* rw = ra + quarter * 64 * 32 + lane * 33;   // slot (c + lane), entry lane
+                const uint32_t rowoff = (uint32_t)((rloc >> 3) * 1024 + (rloc & 7) * 128);
 #pragma unroll
-                for (int ks = 0; ks < kBK / 8; ++ks) {
-                    const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
-                    const uint32_t first = (kt > 0 || ks > 0) ? 1u : 0u;
-                    mma_tf32(d, sdesc(ah + ko), sdesc(bh + boff + ko), id, first);
-                    mma_tf32(d, sdesc(al + ko), sdesc(bh + boff + ko), id, 1u);
-                    mma_tf32(d, sdesc(ah + ko), sdesc(bl + boff + ko), id, 1u);
+                for (int cq = 0; cq < 4; ++cq) {
+                    const int kc = half * 4 + cq;
+                    float4 hi, lo;
+                    float* h = &hi.x;
+                    float* l = &lo.x;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int c = 4 * kc + q;
+                        const float v = (rowok && k0 + c < M) ? rw[c * 32] : 0.f;
+                        split_tf32(v, h[q], l[q]);
+                    }
+                    const uint32_t o = rowoff + (uint32_t)(((kc ^ rloc) & 7) << 4);
+                    *reinterpret_cast<float4*>(A_hi + o) = hi;
+                    *reinterpret_cast<float4*>(A_lo + o) = lo;
+                }
+            } else {
+                // raw row tt holds slot m0 + tt of block k0/32; lane = K index i - k0. Warp w
+                // takes output rows rr = w + 8*it, so rr mod 8 = w and the swizzled offset
+                // is it*1024 plus a per-thread constant.
+                const bool iok = k0 + lane < N;
+                const float* rp = ra + (warp + lane) * 32 + lane;
+                const uint32_t coff = (uint32_t)(warp * 128 + ((((lane >> 2) ^ warp) & 7) << 4) + (lane & 3) * 4);
+#pragma unroll
+                for (int it = 0; it < kBM / 8; ++it) {
+                    const float v = (iok && m0 + warp + 8 * it < M) ? rp[it * 8 * 32] : 0.f;
+                    float h, l;
+                    split_tf32(v, h, l);
+                    *reinterpret_cast<float*>(A_hi + coff + it * 1024) = h;
+                    *reinterpret_cast<float*>(A_lo + coff + it * 1024) = l;
                 }
             }
-            mma_commit(smem_u32(&s_mma[s]));
-            // the B image of tile kt+1 goes to the stage it will use, once the MMAs that
-            // last read that stage (tile kt-1 with two stages, tile kt with one) are done;
-            // this wait also orders the next A writes into that stage after those MMAs
-            if (kt + 1 < nK) {
-                const int sn = (tstages == 2) ? (s ^ 1) : 0;
-                if (tstages == 1 || kt >= 1) {
-                    ok = mbar_wait(smem_u32(&s_mma[sn]), mma_ph[sn], status) && ok;
-                    mma_ph[sn] ^= 1u;
-                }
-                issue_b(bimg_p, n_total, kt + 1, stage(sn) + 2 * a_bytes, smem_u32(&s_bim[sn]));
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&s_raw_empty[kt % pa]));
+                mbar_arrive(smem_u32(&s_a_full[kt % ts]));
             }
         }
-    }
-    // Every thread waits for the last commit; it covers every MMA issued before it.
-    {
-        const int s = (tstages == 2) ? ((nK - 1) & 1) : 0;
-        const int commits = (tstages == 2) ? ((nK - 1 - s) / 2 + 1) : nK;  // commits on stage s
-        ok = mbar_wait(smem_u32(&s_mma[s]), (uint32_t)((commits - 1) & 1), status) && ok;
-    }
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        // every MMA has completed (and every copy has landed) once s_acc fires
+        {
+            bool fin = true;
+            wait_ok(fin, smem_u32(&s_acc), 0u, status);
+            ok = ok && fin;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-    // ---- epilogue: warp w (and w+4) hold output rows m0 + 32(w mod 4) + lane in TMEM lane quarter w mod 4;
-    // warps 0-3 write columns [0, Dh), warps 4-7 columns [Dh, D)
-    const int row = m0 + 32 * quarter + lane;
-    const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
-    float sums[16];
-    tmem_ld16(trow + (uint32_t)(D & ~15), sums);
-    float sum = 0.f;
+        // ---- epilogue: warp w holds output rows m0 + 32(w mod 4) + lane in TMEM lane quarter w mod 4.
+        // Accumulators go to a [128 x 64] shared tile per group of 64 columns, then all
+        // workers write the group row by row with coalesced loads of own[] and stores.
+        float* stg = reinterpret_cast<float*>(base);
+        float* ssum = stg + kBM * kStageStride;
+        const int r_own = 32 * quarter + lane;
+        const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
+        if (half == 0) {
+            float v[16];
+            float s = 0.f;
+            tmem_ld16(trow + (uint32_t)(D & ~15), v);
 #pragma unroll
-    for (int q = 0; q < 16; ++q) sum = (q == (D & 15)) ? sums[q] : sum;
-    const float w = g.coef * 2.f * (g.grad_loss ? g.grad_loss[p % g.wmod] : 1.f);
-    const float* own = (COLS ? yb : xb) + (size_t)row * D;
-    float* out = g.out + (long long)(p % g.omod) * g.out_stride + (size_t)row * D;
-    const int nchunks = (D + 15) / 16;
-    const int cbeg = half ? (nchunks + 1) / 2 : 0, cend = half ? nchunks : (nchunks + 1) / 2;
-    for (int ch = cbeg; ch < cend; ++ch) {
-        const int c0 = ch * 16;
-        float acc[16];
-        tmem_ld16(trow + (uint32_t)c0, acc);
-        if (ok && row < rows) {
+            for (int q = 0; q < 16; ++q) s += (q == (D & 15)) ? v[q] : 0.f;
+            if (stacked) {
+                tmem_ld16(trow + (uint32_t)(n_total + (D & ~15)), v);
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const int n = c0 + q;
-                if (n < D) {
-                    const float val = w * (sum * own[n] - acc[q]);
-                    out[n] = g.accumulate ? out[n] + val : val;
+                for (int q = 0; q < 16; ++q) s += (q == (D & 15)) ? v[q] : 0.f;
+            }
+            ssum[r_own] = s;
+        }
+        const float w = g.coef * 2.f * (g.grad_loss ? g.grad_loss[p % g.wmod] : 1.f);
+        const float* own = COLS ? g.pr.y(p) : g.pr.x(p);
+        float* out = g.out + (long long)(p % g.omod) * g.out_stride;
+        for (int g0 = 0; g0 < D; g0 += 64) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = g0 + (2 * half + cc) * 16;
+                if (c0 < D) {
+                    float v[16];
+                    tmem_ld16(trow + (uint32_t)c0, v);
+                    if (stacked) {
+                        float u[16];
+                        tmem_ld16(trow + (uint32_t)(n_total + c0), u);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) v[q] += u[q];
+                    }
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) stg[r_own * kStageStride + (c0 - g0) + q] = v[q];
                 }
             }
+            workers_sync();
+            // thread: column g0 + (tid mod 64) of rows (tid / 64) + 4k; every load of the
+            // group is issued before the first store
+            const int c = tid & 63, r0 = tid >> 6;
+            if (ok && c < D - g0) {
+                constexpr int kR = 16;  // rows per batch of loads
+                for (int rb0 = 0; rb0 < kBM; rb0 += 4 * kR) {
+                    float ov[kR], pv[kR];
+#pragma unroll
+                    for (int k = 0; k < kR; ++k) {
+                        const int row = m0 + rb0 + r0 + 4 * k;
+                        const size_t o = (size_t)min(row, rows - 1) * D + g0 + c;
+                        ov[k] = own[o];
+                        pv[k] = g.accumulate ? out[o] : 0.f;
+                    }
+#pragma unroll
+                    for (int k = 0; k < kR; ++k) {
+                        const int r = rb0 + r0 + 4 * k;
+                        if (m0 + r < rows)
+                            out[(size_t)(m0 + r) * D + g0 + c] =
+                                pv[k] + w * (ssum[r] * ov[k] - stg[r * kStageStride + c]);
+                    }
+                }
+            }
+            workers_sync();
         }
     }
 
@@ -405,24 +534,28 @@ __global__ void __launch_bounds__(256) bimg_kernel(const GradParams g, bool cols
 
 }  // namespace
 
-// Shared-memory plan: tile stages (hi/lo of A and B) and two raw A buffers;
-// two tile stages when they fit in 220 KiB.
-static void egemm_plan(int D, bool cols, int* tstages, size_t* bytes)
+// Shared-memory plan: the deepest pipeline (A stages, B images, raw A buffers)
+// that fits in the opt-in limit, preferring two A stages and three-deep rings.
+static size_t egemm_bytes(int D, bool cols, Pipe pp)
 {
     const int n_total = ((D + 1 + 15) / 16) * 16;
-    const size_t stage = 2 * (size_t)kBM * 128 + 2 * (size_t)n_total * 128;
-    const size_t raw = 2 * (size_t)(cols ? Raw<true>::kBytes : Raw<false>::kBytes);
-    const int t = (1024 + 2 * stage + raw <= 220 * 1024) ? 2 : 1;
-    *tstages = t;
-    *bytes = 1024 + t * stage + raw;
+    const size_t a = 2 * (size_t)kBM * 128, b = 2 * (size_t)n_total * 128;
+    const size_t raw = cols ? Raw<true>::kBytes : Raw<false>::kBytes;
+    return 1024 + pp.ts * a + pp.pb * b + pp.pa * raw;
+}
+
+static Pipe egemm_plan(int D, bool cols)
+{
+    static const Pipe order[] = {{2, 3, 4}, {2, 3, 3}, {2, 2, 3}, {2, 2, 2}, {1, 2, 2}, {1, 1, 2}};
+    for (const Pipe& pp : order)
+        if (egemm_bytes(D, cols, pp) <= kSmemLimit) return pp;
+    return order[5];
 }
 
 size_t egemm_smem_bytes(int D)
 {
-    int t;
-    size_t a, b;
-    egemm_plan(D, false, &t, &a);
-    egemm_plan(D, true, &t, &b);
+    const size_t a = egemm_bytes(D, false, egemm_plan(D, false));
+    const size_t b = egemm_bytes(D, true, egemm_plan(D, true));
     return a > b ? a : b;
 }
 
@@ -441,19 +574,18 @@ cudaError_t launch_grad_tc(const GradParams& g, bool cols, float* bimg, int* sta
     bimg_kernel<<<dim3(nK, g.P), 256, 0, st>>>(g, cols, n_total, bimg);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    int tstages;
-    size_t smem;
-    egemm_plan(g.D, cols, &tstages, &smem);
+    const Pipe pp = egemm_plan(g.D, cols);
+    const size_t smem = egemm_bytes(g.D, cols, pp);
     const int rows = cols ? g.M : g.N;
     dim3 grid((rows + kBM - 1) / kBM, g.P);
     if (cols) {
         e = cudaFuncSetAttribute(egemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        egemm_kernel<true><<<grid, kThreads, smem, st>>>(g, bimg, n_total, tstages, status);
+        egemm_kernel<true><<<grid, kWorkers + 32, smem, st>>>(g, bimg, n_total, pp, status);
     } else {
         e = cudaFuncSetAttribute(egemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        egemm_kernel<false><<<grid, kThreads, smem, st>>>(g, bimg, n_total, tstages, status);
+        egemm_kernel<false><<<grid, kWorkers + 32, smem, st>>>(g, bimg, n_total, pp, status);
     }
     return cudaGetLastError();
 }

@@ -47,17 +47,22 @@ def test_workspace_sizes(lib):
     assert f >= slots * (8 + 4)          # (vl,hu) pairs + alignment matrix
     assert u >= f + slots * 4            # + the stored cost tensor
     assert u - f < slots * 4 + 4096
+    # pre-split [Y|1] operand images of the gradient contraction: per problem and
+    # K-tile of 32, hi + lo tiles of roundup(D+1, 16) rows x 128 bytes
+    bimg = 32 * (512 // 32) * 2 * 80 * 128
+    assert f >= slots * (8 + 4) + bimg
     n = L.sdtw_workspace_bytes(L.OP_NORMALIZED, 32, 512, 999, 64, L.FUSED)   # M ignored
-    assert n >= 3 * f - 3 * 4096
+    assert n >= 3 * (f - bimg) + bimg - 3 * 4096   # three batches of state, one set of images
     assert L.sdtw_workspace_bytes(L.OP_BARYCENTER, 64, 1024, 1024, 8, L.FUSED) > 0
     for bad in [(0, 4, 4, 4), (4, 0, 4, 4), (4, 4, 0, 4), (4, 4, 4, 0)]:
         assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, *bad, L.UNFUSED) == 0
     assert L.sdtw_workspace_bytes(7, 4, 4, 4, 4, L.UNFUSED) == 0
     assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, 4, 4, 4, 4, 4) == 0
-    # extended precision: 16-byte log-probabilities instead of 8-byte pairs (+8 more unfused)
+    # extended precision: 16-byte log-probabilities instead of 8-byte pairs (+8 more
+    # unfused); its gradients run on the FP32 pipe, so no operand images
     fx = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.FUSED | L.EXTENDED)
     ux = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.UNFUSED | L.EXTENDED)
-    assert fx - f >= slots * 8 and ux - fx >= slots * 8
+    assert fx - (f - bimg) >= slots * 8 and ux - fx >= slots * 8
 
 
 def _fwd(lib, x=0x1000, y=0x2000, B=2, N=3, M=4, D=2, gamma=1.0, mode=0, loss=0x3000, ws=0x100000,
@@ -103,3 +108,13 @@ def test_normalized_and_barycenter_validation(lib):
     # empty sequences
     assert lib.sdtw_barycenter_step(vp(0x1000), vp(0x2000), vp(0x3000), 1, vp(0x4000), 0, 8, 8, 2, 1.0, 0.1,
                                     0.9, 0.999, 1e-8, 1, None, vp(0x100000), 1 << 40, None) == 3
+
+
+def test_auto_precision_rule():
+    from differentiable_series_alignment_gb300 import _lib as L
+    assert L.auto_precision(1.0, 512, 512, 64) == 0            # the headline shape stays fp32
+    assert L.auto_precision(1.0, 512, 512) == 0
+    assert L.auto_precision(1.0, 512, 512, 65) == L.EXTENDED     # wide features
+    assert L.auto_precision(0.01, 64, 64, 4) == L.EXTENDED      # small gamma
+    assert L.auto_precision(1.0, 4096, 8, 4) == L.EXTENDED      # long sequences
+    assert L.auto_precision(1.0, 8, 4095, 4) == 0

@@ -103,6 +103,31 @@ def test_ragged_shapes(mname, mode, N, M, D):
     check_against_oracle(x, y, 0.7, mode, grad_loss=[0.5, -1.25, 2.0], what=f"{N}x{M}x{D} {mname}")
 
 
+# Wide features in fp32. D=127 is the widest operand the gradient contraction
+# stacks as [hi; lo] in one MMA (N = 256); the loss is the batch mean (upstream
+# gradient 1/B), the setting the tolerance is stated for. (D=128 and D=256, the
+# three-product path, run in the sweep above.)
+@pytest.mark.parametrize("mname,mode", MODES)
+@pytest.mark.parametrize("N,M,D", [(130, 257, 127)])
+def test_wide_features_fp32(mname, mode, N, M, D):
+    x, y = synth.iid_normal_pair(3, N, M, D, 90, repeat=N * 1000 + M)
+    check_against_oracle(x, y, 1.0, mode, what=f"{N}x{M}x{D} {mname}")
+
+
+# With O(1) per-problem upstream gradients and gamma < 1, fp32 costs and DP state
+# miss abs 1e-5 on near-zero gradient entries at these widths; auto_precision
+# selects the extended mode, which must then hold the tolerance. D=400 is the
+# largest feature width the library accepts.
+@pytest.mark.parametrize("mname,base", MODES)
+@pytest.mark.parametrize("N,M,D", [(130, 257, 127), (200, 70, 128), (300, 333, 400)])
+def test_wide_features_auto_precision(mname, base, N, M, D):
+    L = _lib()
+    mode = base | L.auto_precision(0.7, N, M, D)
+    assert mode & L.EXTENDED
+    x, y = synth.iid_normal_pair(3, N, M, D, 90, repeat=N * 1000 + M)
+    check_against_oracle(x, y, 0.7, mode, grad_loss=[0.5, -1.25, 2.0], what=f"{N}x{M}x{D} auto {mname}")
+
+
 @pytest.mark.parametrize("mname,mode", MODES)
 @pytest.mark.parametrize("W", [1, 2, 3, 16])
 def test_strip_decompositions_agree(mname, mode, W):
