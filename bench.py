@@ -34,8 +34,8 @@ CELLS = B * N * M
 WORKLOAD = "softdtw fwd+bwd B=32 N=M=512 D=64 gamma=1, unfused then fused"
 FALLBACK_HBM_GBS = 6800.0
 # kernels per step: unfused forward (distance, wavefront) + backward (wavefront,
-# two B-image preps, two gradient contractions), fused forward (1) + backward (5)
-LAUNCHES_PER_STEP = 2 + 5 + 1 + 5
+# operand-image prep, two gradient contractions), fused forward (1) + backward (4)
+LAUNCHES_PER_STEP = 2 + 4 + 1 + 4
 
 
 def log(*a):

@@ -27,7 +27,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 // Workspace layout. The status word sits at offset 0 for every op.
 struct Layout {
     size_t status, ctrl_f, ctrl_f_bytes, ctrl_b, ctrl_b_bytes;
-    size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, bimg, total;
+    size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, bimg, bimg2, total;
     int P, N, M, D, NB;
 };
 
@@ -55,7 +55,9 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->e = o; o = align_up(o + sizeof(float) * slots);
     L->dsk = o; if (!fused) o = align_up(o + (ext ? sizeof(float2) : sizeof(float)) * slots);
     L->gparts = o; if (op == SDTW_OP_BARYCENTER) o = align_up(o + sizeof(float) * (size_t)P * N * D);
-    L->bimg = o; if (!ext) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, N, M, D));
+    // gradient operand images (one batch of B problems at a time): [Y | 1] and [X | 1]
+    L->bimg = o; if (!ext) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, M, D));
+    L->bimg2 = o; if (!ext) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, N, D));
     L->total = o;
     L->P = P; L->N = N; L->M = M; L->D = D; L->NB = NB;
     return true;
@@ -218,15 +220,18 @@ sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void
     g.accumulate = accumulate;
     const bool simt = (mode & SDTW_EXTENDED) != 0 || env_int("SDTW_GRAD_SIMT", 0) != 0;
     int* status = at<int>(ws, L.status);
+    float* img_rows = at<float>(ws, L.bimg);
+    float* img_cols = at<float>(ws, L.bimg2);
+    if (!simt) SDTW_CUDA(launch_bimg(g, out_x ? img_rows : nullptr, out_y ? img_cols : nullptr, st));
     if (out_x) {
         g.out = out_x;
         g.out_stride = (long long)L.N * L.D;
-        SDTW_CUDA(simt ? launch_grad_rows(g, st) : launch_grad_tc(g, false, at<float>(ws, L.bimg), status, st));
+        SDTW_CUDA(simt ? launch_grad_rows(g, st) : launch_grad_tc(g, false, img_rows, status, st));
     }
     if (out_y) {
         g.out = out_y;
         g.out_stride = (long long)L.M * L.D;
-        SDTW_CUDA(simt ? launch_grad_cols(g, st) : launch_grad_tc(g, true, at<float>(ws, L.bimg), status, st));
+        SDTW_CUDA(simt ? launch_grad_cols(g, st) : launch_grad_tc(g, true, img_cols, status, st));
     }
     return SDTW_OK;
 }

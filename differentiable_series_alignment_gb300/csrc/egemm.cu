@@ -163,7 +163,6 @@ __device__ __forceinline__ void issue_a(const float* Ekp, int N, int M, int T, i
         bytes = (uint32_t)min(160, T - m0) * 128;
     }
     mbar_expect_tx(bar, bytes);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (!COLS) {
         for (int b = 0; b < 4; ++b) {
             const int rb = (m0 >> 5) + b;
@@ -184,7 +183,6 @@ __device__ __forceinline__ void issue_b(const float* img, int n_total, int kt, u
 {
     const uint32_t bytes = 2u * (uint32_t)n_total * 128u;
     mbar_expect_tx(bar, bytes);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     bulk_g2s(smem_u32(B_hi), img + (size_t)kt * (bytes / 4), bytes, bar);
 }
 
@@ -217,10 +215,10 @@ __device__ __forceinline__ void wait_ok(bool& ok, uint32_t bar, uint32_t parity,
 // bimg: per problem, per K-tile, the pre-split B image (bimg_kernel).
 //
 // Warp-specialised pipeline, all hand-offs through mbarriers:
-//   issuer  : raw A copy (tile kt+pa) into entry kt%pa once the workers release tile kt;
-//             B image (tile kt+pb-1) once MMA(kt-1) has freed its buffer;
-//             MMAs of tile kt once its A stage is full and its B image has landed,
-//             committed to the A-stage and B-buffer "empty" barriers.
+//   issuer  : MMAs of tile kt once its A stage is full and its B image has landed,
+//             committed to the A-stage and B-buffer "empty" barriers; then the B image
+//             of tile kt+pb-1 (its buffer freed by MMA(kt-1)) and the raw A rows of
+//             tile kt+pa (entry kt%pa, released by the workers before "A full").
 //   workers : wait for raw A of tile kt and for A stage kt%ts to be empty (MMA(kt-ts)),
 //             un-skew + split into the stage, then each warp arrives on "raw empty" and
 //             "A full". After the last commit they stage the accumulators through shared
@@ -234,7 +232,7 @@ __global__ void __launch_bounds__(kWorkers + 32, 1)
     extern __shared__ unsigned char smem_dyn[];
     __shared__ uint64_t s_raw_full[kMaxRing], s_raw_empty[kMaxRing];
     __shared__ uint64_t s_b_full[kMaxRing], s_b_empty[kMaxRing];
-    __shared__ uint64_t s_a_full[2], s_a_empty[2];
+    __shared__ uint64_t s_a_full[kMaxRing], s_a_empty[kMaxRing];
     __shared__ uint64_t s_acc;
     __shared__ uint32_t s_tmem;
 
@@ -269,7 +267,7 @@ __global__ void __launch_bounds__(kWorkers + 32, 1)
             mbar_init(smem_u32(&s_b_full[b]), 1);
             mbar_init(smem_u32(&s_b_empty[b]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kMaxRing; ++b) {
             mbar_init(smem_u32(&s_a_full[b]), kWorkers / 32);
             mbar_init(smem_u32(&s_a_empty[b]), 1);
         }
@@ -298,24 +296,20 @@ __global__ void __launch_bounds__(kWorkers + 32, 1)
                 issue_a<COLS>(Ekp, N, M, T, m0, k, rawA(k), smem_u32(&s_raw_full[k % pa]));
                 a_last[k % pa] = k;
             }
-            for (int k = 0; k < pb - 1 && k < nK; ++k) {
+            // B image kt + bl is issued after MMA(kt): its buffer last held tile kt + bl - pb,
+            // read by MMA(kt - 1) when pb >= 2 (already complete, no stall)
+            const int bl = pb > 1 ? pb - 1 : 1;
+            for (int k = 0; k < bl && k < nK; ++k) {
                 issue_b(bimg_p, n_total, k, bbuf(k), smem_u32(&s_b_full[k % pb]));
                 b_last[k % pb] = k;
             }
             for (int kt = 0; kt < nK && ok; ++kt) {
-                const int kb = kt + pb - 1;  // its buffer was last read by MMA(kt - 1)
-                if (kb < nK) {
-                    if (kb >= pb) wait_ok(ok, smem_u32(&s_b_empty[kb % pb]), (uint32_t)(((kb - pb) / pb) & 1), status);
-                    if (!ok) break;
-                    issue_b(bimg_p, n_total, kb, bbuf(kb), smem_u32(&s_b_full[kb % pb]));
-                    b_last[kb % pb] = kb;
-                }
                 wait_ok(ok, smem_u32(&s_a_full[kt % ts]), (uint32_t)((kt / ts) & 1), status);
                 wait_ok(ok, smem_u32(&s_b_full[kt % pb]), (uint32_t)((kt / pb) & 1), status);
                 if (!ok) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t ah = smem_u32(astage(kt)), al = ah + a_bytes;
-                const uint32_t bh = smem_u32(bbuf(kt)), bl = bh + b_bytes;
+                const uint32_t bh = smem_u32(bbuf(kt)), bl_ = bh + b_bytes;
                 if (stacked) {
                     const uint32_t id2 = idesc_tf32(kBM, 2 * n_total), id1 = idesc_tf32(kBM, n_total);
 #pragma unroll
@@ -335,13 +329,20 @@ __global__ void __launch_bounds__(kWorkers + 32, 1)
                             const uint32_t ko = ks * 32;
                             mma_tf32(d, sdesc(ah + ko), sdesc(bh + boff + ko), id, (kt > 0 || ks > 0) ? 1u : 0u);
                             mma_tf32(d, sdesc(al + ko), sdesc(bh + boff + ko), id, 1u);
-                            mma_tf32(d, sdesc(ah + ko), sdesc(bl + boff + ko), id, 1u);
+                            mma_tf32(d, sdesc(ah + ko), sdesc(bl_ + boff + ko), id, 1u);
                         }
                     }
                 }
                 mma_commit(smem_u32(&s_a_empty[kt % ts]));
                 mma_commit(smem_u32(&s_b_empty[kt % pb]));
-                const int ka = kt + pa;  // entry kt % pa, released after the un-skew of tile kt
+                const int kb = kt + bl;
+                if (kb < nK) {
+                    if (kb >= pb) wait_ok(ok, smem_u32(&s_b_empty[kb % pb]), (uint32_t)(((kb - pb) / pb) & 1), status);
+                    if (!ok) break;
+                    issue_b(bimg_p, n_total, kb, bbuf(kb), smem_u32(&s_b_full[kb % pb]));
+                    b_last[kb % pb] = kb;
+                }
+                const int ka = kt + pa;  // entry kt % pa, released (before A full) after the un-skew of tile kt
                 if (ka < nK) {
                     wait_ok(ok, smem_u32(&s_raw_empty[kt % pa]), (uint32_t)((kt / pa) & 1), status);
                     if (!ok) break;
@@ -500,35 +501,42 @@ __global__ void __launch_bounds__(kWorkers + 32, 1)
     }
 }
 
-// Pre-split B operand images: for problem p and K-tile kt, rows n < D hold
-// coordinate n of the other sequence's rows kt*32 .. kt*32+31, row D holds ones;
-// written as the hi then lo tf32 tiles in the swizzled smem layout. A 32x32
-// shared tile turns the row-major reads and the K-major writes into full lines.
-// grid (nK, P), block 256.
-__global__ void __launch_bounds__(256) bimg_kernel(const GradParams g, bool cols, int n_total, float* __restrict__ img)
+// Pre-split B operand images, both orientations in one launch (blockIdx.z = 0:
+// [Y | 1] for grad_x, 1: [X | 1] for grad_y): for problem p and K-tile kt, rows
+// n < D hold coordinate n of the other sequence's rows kt*32 .. kt*32+31, row D
+// holds ones; written as the hi then lo tf32 tiles in the swizzled smem layout.
+// The 32 source rows are contiguous: every thread loads its share into a
+// [32 x (n_total+1)] shared tile first, then warps write 128-byte image rows.
+// grid (max K-tiles, P, 2), block 256, dynamic smem 32*(n_total+1)*4; a null
+// image pointer skips that orientation.
+__global__ void __launch_bounds__(256) bimg_kernel(const GradParams g, int n_total, float* __restrict__ img_rows,
+                                                   float* __restrict__ img_cols)
 {
-    __shared__ float t[32][33];
+    extern __shared__ float t[];
+    const bool cols = blockIdx.z == 1;
     const int kt = blockIdx.x, p = blockIdx.y;
     const int D = g.D;
     const int kdim = cols ? g.N : g.M;
     const int nK = (kdim + kBK - 1) / kBK;
-    const float* vb = cols ? g.pr.x(p) : g.pr.y(p);
+    if (kt >= nK) return;
+    const float* src = (cols ? g.pr.x(p) : g.pr.y(p)) + (size_t)kt * kBK * D;
+    float* img = cols ? img_cols : img_rows;
+    if (img == nullptr) return;
     unsigned char* hi = reinterpret_cast<unsigned char*>(img + ((size_t)p * nK + kt) * 2 * n_total * 32);
     unsigned char* lo = hi + (size_t)n_total * 128;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    for (int n0 = 0; n0 < n_total; n0 += 32) {
-        for (int k = ty; k < 32; k += 8) {
-            const int kk = kt * kBK + k, n = n0 + tx;
-            float v = 0.f;
-            if (kk < kdim) v = (n < D) ? vb[(size_t)kk * D + n] : (n == D ? 1.f : 0.f);
-            t[k][tx] = v;
-        }
-        __syncthreads();
-        for (int nn = ty; nn < 32; nn += 8) {
-            const int n = n0 + nn;
-            if (n < n_total) put(hi, lo, n, tx, t[tx][nn]);
-        }
-        __syncthreads();
+    const int ld = n_total + 1;
+    const int here = min(kBK, kdim - kt * kBK);
+#pragma unroll 4
+    for (int idx = threadIdx.x; idx < kBK * n_total; idx += 256) {
+        const int k = idx / n_total, n = idx - k * n_total;
+        float v = 0.f;
+        if (k < here) v = (n < D) ? src[(size_t)k * D + n] : (n == D ? 1.f : 0.f);
+        t[k * ld + n] = v;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < kBK * n_total; idx += 256) {
+        const int n = idx >> 5, k = idx & 31;
+        put(hi, lo, n, k, t[k * ld + n]);
     }
 }
 
@@ -546,10 +554,10 @@ static size_t egemm_bytes(int D, bool cols, Pipe pp)
 
 static Pipe egemm_plan(int D, bool cols)
 {
-    static const Pipe order[] = {{2, 3, 4}, {2, 3, 3}, {2, 2, 3}, {2, 2, 2}, {1, 2, 2}, {1, 1, 2}};
+    static const Pipe order[] = {{3, 3, 3}, {3, 3, 2}, {2, 3, 3}, {2, 2, 3}, {2, 2, 2}, {1, 2, 2}, {1, 1, 2}};
     for (const Pipe& pp : order)
         if (egemm_bytes(D, cols, pp) <= kSmemLimit) return pp;
-    return order[5];
+    return order[6];
 }
 
 size_t egemm_smem_bytes(int D)
@@ -559,21 +567,28 @@ size_t egemm_smem_bytes(int D)
     return a > b ? a : b;
 }
 
-size_t egemm_bimg_bytes(int P, int N, int M, int D)
+size_t egemm_bimg_bytes(int P, int K, int D)
 {
     const int n_total = ((D + 1 + 15) / 16) * 16;
-    const int nK = ((N > M ? N : M) + kBK - 1) / kBK;
+    const int nK = (K + kBK - 1) / kBK;
     return (size_t)P * nK * 2 * n_total * 128;
 }
 
-cudaError_t launch_grad_tc(const GradParams& g, bool cols, float* bimg, int* status, cudaStream_t st)
+cudaError_t launch_bimg(const GradParams& g, float* img_rows, float* img_cols, cudaStream_t st)
 {
     const int n_total = ((g.D + 1 + 15) / 16) * 16;
-    const int kdim = cols ? g.N : g.M;
-    const int nK = (kdim + kBK - 1) / kBK;
-    bimg_kernel<<<dim3(nK, g.P), 256, 0, st>>>(g, cols, n_total, bimg);
-    cudaError_t e = cudaGetLastError();
+    const int nK = ((g.N > g.M ? g.N : g.M) + kBK - 1) / kBK;
+    const size_t smem = sizeof(float) * kBK * (n_total + 1);
+    cudaError_t e = cudaFuncSetAttribute(bimg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    bimg_kernel<<<dim3(nK, g.P, 2), 256, smem, st>>>(g, n_total, img_rows, img_cols);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grad_tc(const GradParams& g, bool cols, const float* bimg, int* status, cudaStream_t st)
+{
+    const int n_total = ((g.D + 1 + 15) / 16) * 16;
+    cudaError_t e;
     const Pipe pp = egemm_plan(g.D, cols);
     const size_t smem = egemm_bytes(g.D, cols, pp);
     const int rows = cols ? g.M : g.N;

@@ -73,10 +73,14 @@ struct GradParams {
 };
 cudaError_t launch_grad_rows(const GradParams& g, cudaStream_t st);
 // The same contractions on the tensor cores (tcgen05, 3xTF32); cols selects grad_y.
-// bimg: workspace for the pre-split B operand images (egemm_bimg_bytes).
-cudaError_t launch_grad_tc(const GradParams& g, bool cols, float* bimg, int* status, cudaStream_t st);
+// Pre-split B operand images: [Y | 1] into img_rows (for grad_x) and [X | 1]
+// into img_cols (for grad_y), one launch; a null pointer skips that image.
+// Each buffer takes egemm_bimg_bytes(P, K, D) with K = M (rows) or N (cols).
+cudaError_t launch_bimg(const GradParams& g, float* img_rows, float* img_cols, cudaStream_t st);
+// bimg: the image for this orientation, written by launch_bimg before.
+cudaError_t launch_grad_tc(const GradParams& g, bool cols, const float* bimg, int* status, cudaStream_t st);
 size_t egemm_smem_bytes(int D);
-size_t egemm_bimg_bytes(int P, int N, int M, int D);
+size_t egemm_bimg_bytes(int P, int K, int D);
 cudaError_t launch_grad_cols(const GradParams& g, cudaStream_t st);
 
 // Barycenter: grad = (1/K) sum_k gparts[k]; Adam update of z, m, v; mean loss.

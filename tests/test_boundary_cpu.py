@@ -47,9 +47,9 @@ def test_workspace_sizes(lib):
     assert f >= slots * (8 + 4)          # (vl,hu) pairs + alignment matrix
     assert u >= f + slots * 4            # + the stored cost tensor
     assert u - f < slots * 4 + 4096
-    # pre-split [Y|1] operand images of the gradient contraction: per problem and
-    # K-tile of 32, hi + lo tiles of roundup(D+1, 16) rows x 128 bytes
-    bimg = 32 * (512 // 32) * 2 * 80 * 128
+    # pre-split [Y|1] and [X|1] operand images of the gradient contraction: per
+    # problem and K-tile of 32, hi + lo tiles of roundup(D+1, 16) rows x 128 bytes
+    bimg = 2 * 32 * (512 // 32) * 2 * 80 * 128
     assert f >= slots * (8 + 4) + bimg
     n = L.sdtw_workspace_bytes(L.OP_NORMALIZED, 32, 512, 999, 64, L.FUSED)   # M ignored
     assert n >= 3 * (f - bimg) + bimg - 3 * 4096   # three batches of state, one set of images
