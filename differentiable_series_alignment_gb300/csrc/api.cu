@@ -28,6 +28,8 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 struct Layout {
     size_t status, ctrl_f, ctrl_f_bytes, ctrl_b, ctrl_b_bytes;
     size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, bimg, bimg2, total;
+    size_t ximg, yimg, xnorm, ynorm;  // tensor-core cost operands (tc_cost)
+    bool tc_cost;
     int P, N, M, D, NB;
 };
 
@@ -58,6 +60,13 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     // gradient operand images (one batch of B problems at a time): [Y | 1] and [X | 1]
     L->bimg = o; if (!ext) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, M, D));
     L->bimg2 = o; if (!ext) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, N, D));
+    // operand images and norms of the tensor-core costs (fp32 modes, D <= 64): the
+    // unfused cost tensor and the fused forward's cost tiles
+    L->tc_cost = !ext && D <= 64;
+    L->ximg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, N, D));
+    L->yimg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, M, D));
+    L->xnorm = o; if (L->tc_cost) o = align_up(o + snorm_bytes(P, N));
+    L->ynorm = o; if (L->tc_cost) o = align_up(o + snorm_bytes(P, M));
     L->total = o;
     L->P = P; L->N = N; L->M = M; L->D = D; L->NB = NB;
     return true;
@@ -170,6 +179,11 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
 {
     const bool fused = (mode & SDTW_FUSED) != 0, ext = (mode & SDTW_EXTENDED) != 0;
     WaveParams q = wave_params(pr, L, ws, gamma, fused, ext, false);
+    const bool tc = L.tc_cost && env_int(fused ? "SDTW_FUSED_SIMT" : "SDTW_DIST_SIMT", 0) == 0;
+    if (fused && tc) {  // the tensor-core fused forward takes 128-row strips (4 warps)
+        q.W = 4;
+        q.S = (L.NB + 3) / 4;
+    }
     SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.status), 0, sizeof(int), st));
     SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_f), 0, L.ctrl_f_bytes, st));
     if (q.S > 1)  // strip boundary slots start untagged
@@ -182,11 +196,26 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
         SDTW_CUDA(launch_forward_x(q, fused, st));
         return SDTW_OK;
     }
-    if (!fused) SDTW_CUDA(launch_dist_skewed(pr, L.P, L.N, L.M, L.D, at<float>(ws, L.dsk), st));
+    if (tc)
+        SDTW_CUDA(launch_simg(pr, L.P, L.N, L.M, L.D, at<float>(ws, L.ximg), at<float>(ws, L.yimg),
+                              at<float>(ws, L.xnorm), at<float>(ws, L.ynorm), st));
+    if (!fused) {
+        if (tc) {
+            SDTW_CUDA(launch_dist_tc(L.P, L.N, L.M, L.D, at<float>(ws, L.ximg), at<float>(ws, L.yimg),
+                                     at<float>(ws, L.xnorm), at<float>(ws, L.ynorm), at<float>(ws, L.dsk),
+                                     at<int>(ws, L.status), st));
+        } else {
+            SDTW_CUDA(launch_dist_skewed(pr, L.P, L.N, L.M, L.D, at<float>(ws, L.dsk), st));
+        }
+    }
     q.loss = loss_out;
     q.skip_publish = g_skip_publish;
     g_skip_publish = 0;
-    SDTW_CUDA(launch_forward(q, fused, st));
+    if (fused && tc)
+        SDTW_CUDA(launch_forward_tc(q, at<float>(ws, L.ximg), at<float>(ws, L.yimg), at<float>(ws, L.xnorm),
+                                    at<float>(ws, L.ynorm), st));
+    else
+        SDTW_CUDA(launch_forward(q, fused, st));
     return SDTW_OK;
 }
 

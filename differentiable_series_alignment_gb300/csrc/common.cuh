@@ -97,6 +97,11 @@ __device__ __forceinline__ float exp2_neg(float x) {
     return (x < -125.0f) ? 0.0f : r;
 }
 
+// Math variants of the DP kernels: ACC selects the unbiased exp2_neg above and
+// log2f, otherwise the MUFU approximations.
+template <bool ACC> __device__ __forceinline__ float dp_exp2(float x) { return ACC ? exp2_neg(x) : ex2(x); }
+template <bool ACC> __device__ __forceinline__ float dp_log2(float x) { return ACC ? log2f(x) : lg2(x); }
+
 // log2(1 + a + b) for a, b in [0, 1]: the three-term sum of a log-sum-exp whose
 // largest term has been factored out. log2f is the accurate (unbiased) library
 // function.

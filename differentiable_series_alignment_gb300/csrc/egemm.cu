@@ -23,118 +23,17 @@
 // can cancel by ~100x, which leaves it well inside rel 1e-3.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace sdtw {
 
 namespace {
 
+using namespace tc;
+
 constexpr int kBM = 128;       // output rows per CTA (MMA M)
 constexpr int kBK = 32;        // reduction elements per K-tile (128 bytes of fp32 per smem row)
 constexpr size_t kSmemLimit = 227 * 1024 - 256;  // opt-in dynamic shared memory, minus static
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Byte offset of element (r, k) in a K-major tile of 32 fp32 per row, 128-byte
-// swizzle: 16-byte chunk index XOR (row mod 8) inside each 8-row, 1 KiB atom.
-__device__ __forceinline__ uint32_t sw128(int r, int k) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k >> 2) ^ r) & 7) << 4) + (k & 3) * 4);
-}
-
-// fp32 -> tf32 hi (round to nearest) and the tf32-rounded remainder.
-__device__ __forceinline__ void split_tf32(float v, float& hi, float& lo) {
-    hi = __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
-    const float r = v - hi;
-    lo = __uint_as_float((__float_as_uint(r) + 0x1000u) & 0xFFFFE000u);
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1 KiB apart.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
-    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)1 << 16;              // leading byte offset (unused with swizzled K-major)
-    d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset: next 8-row group
-    d |= (uint64_t)1 << 46;              // descriptor version
-    d |= (uint64_t)2 << 61;              // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor: D fp32, A and B tf32, both K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.b32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the given phase parity of an mbarrier (all threads).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
-    if (mbar_test(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (!mbar_test(bar, parity)) {
-        if (global_ns() - t0 > 2000000000ull) {
-            atomicOr(status, kStatusTimeout);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(r[q]);
-}
-
-// Stores the split value into the hi and lo tiles of a stage.
-__device__ __forceinline__ void put(unsigned char* hi_tile, unsigned char* lo_tile, int r, int k, float v) {
-    float h, l;
-    split_tf32(v, h, l);
-    const uint32_t o = sw128(r, k);
-    *reinterpret_cast<float*>(hi_tile + o) = h;
-    *reinterpret_cast<float*>(lo_tile + o) = l;
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// One TMA bulk copy global -> shared (16-byte aligned addresses, size multiple of 16).
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
 
 // Skewed rows of E that one K-tile needs, per row block.
 //   rows (grad_x): for each of the 4 row blocks, slots t in [k0, k0+63)   -> 64 rows copied
@@ -196,18 +95,8 @@ constexpr int kWorkers = 256;            // warps 0-7: un-skew and epilogue
 constexpr int kIssuer = 8;               // warp 8: bulk copies and MMAs (lane 0)
 constexpr int kStageStride = 65;         // epilogue staging row stride (floats)
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 __device__ __forceinline__ void workers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
-}
-
-// Sticky bounded wait: after one timeout the caller stops waiting (the status word
-// already carries the error) so the kernel ends in bounded time.
-__device__ __forceinline__ void wait_ok(bool& ok, uint32_t bar, uint32_t parity, int* status) {
-    if (ok) ok = mbar_wait(bar, parity, status);
 }
 
 // COLS = false: grad_x rows (A = E rows i, K = j, B = [Y | 1]).

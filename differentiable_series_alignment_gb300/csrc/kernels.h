@@ -81,6 +81,30 @@ cudaError_t launch_bimg(const GradParams& g, float* img_rows, float* img_cols, c
 cudaError_t launch_grad_tc(const GradParams& g, bool cols, const float* bimg, int* status, cudaStream_t st);
 size_t egemm_smem_bytes(int D);
 size_t egemm_bimg_bytes(int P, int K, int D);
+
+// Tensor-core cost tensor (dist_tc.cu), D <= 64: operand images of x and y
+// (simg_bytes each), their squared row norms (snorm_bytes each), then the
+// skewed cost tensor. status receives kStatusTimeout if a bounded wait expires.
+size_t simg_bytes(int P, int L, int D);
+// Operand image layout (floats): per problem, per K-block of 32 features, hi then
+// lo part, Lpad = roundup(L, 128) rows of 32 tf32 values (128 bytes, 16-byte
+// chunks swizzled by row mod 8); row norms at p * Lpad + r.
+__host__ __device__ inline size_t simg_offset(int p, int KB, int kb, int part, int Lpad, int r)
+{
+    return ((((size_t)p * KB + kb) * 2 + part) * (size_t)Lpad + (size_t)r) * 32;
+}
+__host__ __device__ inline int simg_pad(int L) { return (L + 127) / 128 * 128; }
+size_t snorm_bytes(int P, int L);
+cudaError_t launch_simg(const Problems& pr, int P, int N, int M, int D, float* ximg, float* yimg, float* xnorm,
+                        float* ynorm, cudaStream_t st);
+cudaError_t launch_dist_tc(int P, int N, int M, int D, const float* ximg, const float* yimg, const float* xnorm,
+                           const float* ynorm, float* Dsk, int* status, cudaStream_t st);
+
+// Fused forward with tensor-core cost tiles (wavefront_tc.cu): q.W must be 4
+// (128-row strips), D <= 64; the operand images and norms as for launch_dist_tc.
+cudaError_t launch_forward_tc(WaveParams q, const float* ximg, const float* yimg, const float* xnorm,
+                              const float* ynorm, cudaStream_t st);
+size_t wave_tc_smem(int D);
 cudaError_t launch_grad_cols(const GradParams& g, cudaStream_t st);
 
 // Barycenter: grad = (1/K) sum_k gparts[k]; Adam update of z, m, v; mean loss.

@@ -78,13 +78,6 @@ __device__ __forceinline__ void stage_y_tile(float* tile, const float* yb, int c
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Math variants: ACC selects the unbiased exp2/log2 of common.cuh, otherwise
-// the MUFU approximations.
-// ---------------------------------------------------------------------------
-template <bool ACC> __device__ __forceinline__ float dp_exp2(float x) { return ACC ? exp2_neg(x) : ex2(x); }
-template <bool ACC> __device__ __forceinline__ float dp_log2(float x) { return ACC ? log2f(x) : lg2(x); }
-
-// ---------------------------------------------------------------------------
 // Forward
 // ---------------------------------------------------------------------------
 // DX (fused only): 32 or 64 keeps the warp's x rows in registers, padded to DX

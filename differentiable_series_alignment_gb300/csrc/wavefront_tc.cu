@@ -1,0 +1,358 @@
+// wavefront_tc.cu -- fused forward wavefront whose costs come from the tensor
+// cores (fp32 mode, D <= 64).
+//
+// Same recursion, strip decomposition and boundary channels as the forward in
+// wavefront.cu (difference form, one warp per 32-row block, tagged slots
+// between warps and strips). What changes is where the cost of a cell comes
+// from: no cost tensor is stored (SoftDTW-CUDA (PyTorch + Numba) README,
+// "Fused Mode"), and instead of every DP lane summing D squared differences per
+// step, the CTA computes its 128 rows x 32 columns cost tiles as a tcgen05 GEMM:
+//
+//   C[i,j] = |x_i|^2 + |y_j|^2 - 2 x_i . y_j,
+//
+// with the x rows of the CTA resident in shared memory and 32-row y tiles
+// streamed in by bulk copy, both as the pre-split 3xTF32 operand images of
+// dist_tc.cu (x_hi . [y_hi ; y_lo] + x_lo . y_hi). A fifth warp issues the
+// copies and MMAs into a ring of tensor-memory tiles; at the start of every
+// 32-step period each DP warp loads its 32 rows of the next tile (tcgen05.ld),
+// releases the tile, and writes the costs into its 64-column shared ring in the
+// order its lanes read them. The DP step itself then costs one shared load.
+//
+// Hand-offs (all mbarriers, all waits bounded):
+//   s_bfull[e]  y tile copies landed       (issuer waits)
+//   s_bempty[e] MMAs reading entry e done  (issuer waits before refilling)
+//   s_tfull[t]  cost tile t in TMEM        (DP warps wait)
+//   s_tfree[t]  every DP warp with rows has loaded tile t (issuer waits)
+#include "channel.cuh"
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace sdtw {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kDpWarps = 4;               // 128 rows per CTA: the MMA tile height
+constexpr int kIssuerWarp = kDpWarps;     // warp 4: bulk copies and MMAs
+constexpr int kRT = 8;                    // cost tiles in tensor memory, 64 columns each
+constexpr int kRB = 4;                    // y tiles in shared memory
+constexpr int kTmemCols = kRT * 64;       // 512: the whole tensor memory of the SM
+constexpr uint32_t kABlock = 128 * 128;   // one K-block of the CTA's 128 x rows (bytes)
+constexpr uint32_t kBHalf = 32 * 128;     // one K-block of 32 y rows, hi or lo (bytes)
+
+}  // namespace
+
+size_t wave_tc_smem(int D)
+{
+    const int KB = (D + 31) / 32;
+    return wave_smem_fixed(kDpWarps, false) + 1024 + 2 * (size_t)KB * kABlock + (size_t)kRB * KB * 2 * kBHalf +
+           (size_t)kDpWarps * 64 * 32 * sizeof(float);
+}
+
+namespace {
+
+template <bool ACC>
+__global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
+    fwd_tc_kernel(const WaveParams q, const float* __restrict__ ximg, const float* __restrict__ yimg,
+                  const float* __restrict__ xnorm, const float* __restrict__ ynorm)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr int W = kDpWarps;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Slot* ring = reinterpret_cast<Slot*>(smem_raw);                          // [W][kRing], by producer warp
+    volatile int* cons = reinterpret_cast<volatile int*>(ring + W * kRing);  // [W] columns consumed
+    __shared__ int s_tk;
+    __shared__ double s_red[kMaxWarps];
+    __shared__ int s_last;
+    __shared__ uint64_t s_a, s_fin, s_bfull[kRB], s_bempty[kRB], s_tfull[kRT], s_tfree[kRT];
+    __shared__ uint32_t s_tmem;
+
+    if (threadIdx.x == 0) s_tk = atomicAdd(q.ticket_f, 1);
+    if (threadIdx.x < W) cons[threadIdx.x] = 0;
+    for (int k = threadIdx.x; k < W * kRing; k += blockDim.x) ring[k].tag = 0u;
+    __syncthreads();
+
+    const int tk = s_tk;
+    const int p = tk % q.P, strip = tk / q.P;
+    const int N = q.N, M = q.M, T = skew_T(M);
+    const int KB = (q.D + 31) / 32;
+    const int Npad = simg_pad(N), Mpad = simg_pad(M);
+    const int rs0 = strip * W * 32;                              // first row of the CTA
+    const int nact = min(W, max(1, (N - rs0 + 31) / 32));       // DP warps with rows
+    const int nT = (M + 31) / 32;                                // cost tiles
+
+    unsigned char* tcb = smem_raw + q.smem_fixed;
+    unsigned char* base = tcb + ((1024u - (smem_u32(tcb) & 1023u)) & 1023u);
+    unsigned char* a_hi = base;
+    unsigned char* a_lo = base + KB * kABlock;
+    unsigned char* bring = base + 2 * KB * kABlock;               // [kRB][KB][hi 32 rows | lo 32 rows]
+    float* dts = reinterpret_cast<float*>(bring + kRB * KB * 2 * kBHalf);
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&s_a), 1);
+        mbar_init(smem_u32(&s_fin), 1);
+        for (int e = 0; e < kRB; ++e) {
+            mbar_init(smem_u32(&s_bfull[e]), 1);
+            mbar_init(smem_u32(&s_bempty[e]), 1);
+        }
+        for (int t = 0; t < kRT; ++t) {
+            mbar_init(smem_u32(&s_tfull[t]), 1);
+            mbar_init(smem_u32(&s_tfree[t]), nact);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = s_tmem;
+    int* status = q.status;
+
+    float c0 = 0.f;  // scaled d(i, 0)
+    bool active = false;
+
+    if (warp == kIssuerWarp) {
+        if (lane == 0) {
+            bool ok = true;
+            int y_last[kRB];
+            for (int e = 0; e < kRB; ++e) y_last[e] = -1;
+            mbar_expect_tx(smem_u32(&s_a), 2u * KB * kABlock);
+            for (int kb = 0; kb < KB; ++kb) {
+                bulk_g2s(smem_u32(a_hi + kb * kABlock), ximg + simg_offset(p, KB, kb, 0, Npad, rs0), kABlock,
+                         smem_u32(&s_a));
+                bulk_g2s(smem_u32(a_lo + kb * kABlock), ximg + simg_offset(p, KB, kb, 1, Npad, rs0), kABlock,
+                         smem_u32(&s_a));
+            }
+            auto issue_y = [&](int c) {
+                const int e = c % kRB;
+                mbar_expect_tx(smem_u32(&s_bfull[e]), 2u * KB * kBHalf);
+                for (int kb = 0; kb < KB; ++kb) {
+                    unsigned char* dst = bring + (e * KB + kb) * 2 * kBHalf;
+                    bulk_g2s(smem_u32(dst), yimg + simg_offset(p, KB, kb, 0, Mpad, 32 * c), kBHalf,
+                             smem_u32(&s_bfull[e]));
+                    bulk_g2s(smem_u32(dst + kBHalf), yimg + simg_offset(p, KB, kb, 1, Mpad, 32 * c), kBHalf,
+                             smem_u32(&s_bfull[e]));
+                }
+                y_last[e] = c;
+            };
+            for (int c = 0; c < kRB - 1 && c < nT; ++c) issue_y(c);
+            wait_ok(ok, smem_u32(&s_a), 0u, status);
+            const uint32_t id2 = idesc_tf32(128, 64), id1 = idesc_tf32(128, 32);
+            for (int c = 0; c < nT && ok; ++c) {
+                const int t = c % kRT, e = c % kRB;
+                if (c >= kRT) wait_ok(ok, smem_u32(&s_tfree[t]), (uint32_t)(((c - kRT) / kRT) & 1), status);
+                wait_ok(ok, smem_u32(&s_bfull[e]), (uint32_t)((c / kRB) & 1), status);
+                if (!ok) break;
+                fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)(t * 64);
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t ah = smem_u32(a_hi + kb * kABlock), al = smem_u32(a_lo + kb * kABlock);
+                    const uint32_t bh = smem_u32(bring + (e * KB + kb) * 2 * kBHalf);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
+                        mma_tf32(d, sdesc(ah + ko), sdesc(bh + ko), id2, (kb > 0 || ks > 0) ? 1u : 0u);
+                        mma_tf32(d, sdesc(al + ko), sdesc(bh + ko), id1, 1u);
+                    }
+                }
+                mma_commit(smem_u32(&s_tfull[t]));
+                mma_commit(smem_u32(&s_bempty[e]));
+                // y tile c + kRB - 1 goes to entry (c - 1) % kRB, last read by MMA(c - 1)
+                const int cy = c + kRB - 1;
+                if (cy < nT) {
+                    if (c >= 1) wait_ok(ok, smem_u32(&s_bempty[(c - 1) % kRB]), (uint32_t)(((c - 1) / kRB) & 1), status);
+                    if (!ok) break;
+                    issue_y(cy);
+                }
+            }
+            // every MMA issued above has completed before tensor memory is released,
+            // and no copy is still writing shared memory when the CTA exits
+            mma_commit(smem_u32(&s_fin));
+            bool fin = true;
+            wait_ok(fin, smem_u32(&s_fin), 0u, status);
+            for (int e = 0; e < kRB; ++e)
+                if (y_last[e] >= 0) wait_ok(fin, smem_u32(&s_bfull[e]), (uint32_t)((y_last[e] / kRB) & 1), status);
+        }
+        __syncwarp();
+    } else {
+        const int rb = strip * W + warp, r0 = rb * 32, i = r0 + lane;
+        active = r0 < N;
+        const bool has_top = active && r0 > 0;
+        const bool top_global = has_top && warp == 0;
+        const bool has_bot = active && (r0 + 32 < N);
+        const bool bot_global = has_bot && warp == W - 1;
+        const bool row0_lane = (i == 0);
+        const bool last_lane = (i == N - 1);
+        const float scale = q.scale;
+        float* rowbuf = q.rowbuf + (size_t)p * M;
+        float* dt = dts + warp * 64 * 32;  // [64][32] raw cost, slot (col & 63), lane
+        const float nx = xnorm[(size_t)p * Npad + i];
+        const float* nyp = ynorm + (size_t)p * Mpad;
+        const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
+
+        if (active) {
+            const long long sk = skew_index(N, M, p, rb, 0, lane);
+            float2* vhp = q.VH + sk;
+            Slot* ring_out = ring + warp * kRing;
+            const Slot* ring_in = ring + (warp - 1) * kRing;
+            Slot* edge_out = q.edge_f + ((size_t)p * q.S + strip) * M;
+            const Slot* edge_in = q.edge_f + ((size_t)p * q.S + strip - 1) * M;
+            const bool chan_lane = has_bot && lane == 31 && !(q.skip_publish && strip == 0 && bot_global);
+            Slot* chan_out = bot_global ? edge_out : ring_out;
+            const int chan_mask = bot_global ? 0x7fffffff : (kRing - 1);
+            Slot nxt[1];
+            nxt[0].v = 0.f;
+            nxt[0].tag = 0u;
+            if (top_global && lane < kGroup && lane < M) nxt[0] = slot_load(edge_in + lane);
+
+            float h_prev = 0.f, v_prev = 0.f;
+            bool tc_ok = true;
+            const int nG = T / kGroup;
+            for (int g = 0; g < nG; ++g) {
+                const int s0 = g * kGroup;
+                if ((s0 & 31) == 0 && (s0 >> 5) < nT) {
+                    // Period c = s0/32 reads columns of tiles c-1 and c: bring tile c in. Its
+                    // ring slots last held tile c-2, whose last read was at step s0-2.
+                    const int c = s0 >> 5, t = c % kRT;
+                    wait_ok(tc_ok, smem_u32(&s_tfull[t]), (uint32_t)((c / kRT) & 1), status);
+                    if (!__all_sync(kFull, tc_ok)) break;
+                    fence_after_sync();
+                    float a[32], b[32];
+                    tmem_ld32(tq + (uint32_t)(t * 64), a);
+                    tmem_ld32(tq + (uint32_t)(t * 64 + 32), b);
+                    fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&s_tfree[t]));
+                    const float nyv = nyp[32 * c + lane];
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        const float ny = __shfl_sync(kFull, nyv, u);
+                        dt[((32 * c + u) & 63) * 32 + lane] = fmaxf(nx + ny - 2.f * (a[u] + b[u]), 0.f);
+                    }
+                    __syncwarp();
+                }
+
+                // Upper-neighbour values for lane 0: lane q holds column s0 + q.
+                float topv = 0.f;
+                bool ok = true;
+                if (has_top && s0 < M) {
+                    const int col = s0 + lane;
+                    const unsigned want = (lane < kGroup && col < M) ? (unsigned)(col + 1) : 0u;
+                    Slot cur[1];
+                    if (top_global) {
+                        cur[0] = nxt[0];
+                        ok = validate(cur, edge_in + col, want, q);
+                        const int ncol = col + kGroup;
+                        if (ok && lane < kGroup && ncol < M) nxt[0] = slot_load(edge_in + ncol);
+                    } else {
+                        cur[0].v = 0.f;
+                        cur[0].tag = 0u;
+                        if (want) cur[0] = slot_load(ring_in + (col & (kRing - 1)));
+                        ok = validate(cur, ring_in + (col & (kRing - 1)), want, q);
+                    }
+                    topv = cur[0].v;
+                }
+                if (ok && has_bot && !bot_global) {
+                    const int need = s0 + kGroup - 31 - kRing;  // ring slots this group overwrites are free
+                    if (need > 0) ok = wait_smem(&cons[warp], need, q);
+                }
+                if (!ok) break;
+
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u) {
+                    const int s = s0 + u;
+                    const int j = s - lane;
+                    const float hs = __shfl_up_sync(kFull, h_prev, 1);
+                    const float tv = __shfl_sync(kFull, topv, u);
+                    const float hu = (lane == 0) ? tv : hs;
+                    const float vl = v_prev;
+                    const float d = dt[(j & 63) * 32 + lane] * scale;
+                    float lo, mid, hi;
+                    sort3(0.f, vl, hu, lo, mid, hi);
+                    const float lz = dp_log2<ACC>((1.f + dp_exp2<ACC>(lo - mid)) + dp_exp2<ACC>(lo - hi));
+                    const float tt = (d + lo) - lz;
+                    const bool col0 = (j == 0);
+                    const float h = col0 ? -kBig : (row0_lane ? d : tt - vl);
+                    const float v = row0_lane ? -kBig : (col0 ? d : tt - hu);
+                    const float svl = col0 ? kBig : (row0_lane ? -kBig : vl);
+                    const float shu = row0_lane ? kBig : (col0 ? -kBig : hu);
+                    c0 = col0 ? d : c0;
+                    vhp[(long long)s * 32] = make_float2(svl, shu);
+                    const bool valid = (unsigned)j < (unsigned)M;
+                    if (chan_lane && valid) slot_store(chan_out + (j & chan_mask), h, (unsigned)(j + 1));
+                    if (last_lane && valid) rowbuf[j] = h;
+                    h_prev = h;
+                    v_prev = v;
+                }
+
+                if (has_top && !top_global && lane == 0) cons[warp - 1] = min(s0 + kGroup, M);
+            }
+        }
+    }
+
+    // Loss: R[N,M] = sum_i d(i,0) + sum_{j>=1} h(N-1, j), scaled units.
+    double part = (active && warp < W && rs0 + 32 * warp + lane < N) ? (double)c0 : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
+    if (lane == 0) s_red[warp] = part;
+    __threadfence();
+    __syncthreads();
+    float* rowbuf = q.rowbuf + (size_t)p * M;
+    if (threadIdx.x == 0) {
+        double cs = 0.0;
+        for (int w = 0; w < W; ++w) cs += s_red[w];
+        q.colsum[(size_t)p * q.NB + strip] = cs;
+        __threadfence();
+        s_last = (atomicAdd(&q.done[p], 1) == q.S - 1);
+    }
+    __syncthreads();
+    if (s_last) {  // the last strip of problem p to finish assembles its loss
+        __threadfence();
+        double acc = 0.0;
+        for (int j = 1 + (int)threadIdx.x; j < M; j += blockDim.x) acc += (double)__ldcg(rowbuf + j);
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+        if (lane == 0) s_red[warp] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double tot = 0.0;
+            for (int w = 0; w <= W; ++w) tot += s_red[w];
+            for (int k = 0; k < q.S; ++k) tot += __ldcg(&q.colsum[(size_t)p * q.NB + k]);
+            q.loss[p] = (float)(tot * (double)q.unscale);
+        }
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_forward_tc(WaveParams q, const float* ximg, const float* yimg, const float* xnorm,
+                              const float* ynorm, cudaStream_t st)
+{
+    if (q.W != kDpWarps || q.D > 64) return cudaErrorInvalidValue;
+    const int grid = q.P * q.S;
+    q.smem_fixed = (int)wave_smem_fixed(kDpWarps, false);
+    // more than half of the SM's shared memory: one CTA per SM, which the
+    // 512-column tensor-memory allocation relies on
+    int dev = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess || per_sm <= 0)
+        per_sm = 228 * 1024;
+    const size_t smem = max(wave_tc_smem(q.D), (size_t)per_sm / 2 + 1024);
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, (kDpWarps + 1) * 32, smem, st>>>(q, ximg, yimg, xnorm, ynorm);
+        return cudaGetLastError();
+    };
+    return q.accurate ? go(fwd_tc_kernel<true>) : go(fwd_tc_kernel<false>);
+}
+
+}  // namespace sdtw

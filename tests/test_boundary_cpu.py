@@ -44,7 +44,10 @@ def test_workspace_sizes(lib):
     f = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.FUSED)
     # skewed slots: 16 blocks x (512+31 rounded up to a multiple of 16) x 32 per problem
     slots = 32 * 16 * 544 * 32
-    assert f >= slots * (8 + 4)          # (vl,hu) pairs + alignment matrix
+    # tensor-core cost operands in both modes: x and y images (hi + lo tf32, 2
+    # K-blocks of 32 features, rows padded to 128) and row norms
+    simg = 2 * (32 * 2 * 2 * 512 * 128) + 2 * (32 * 512 * 4)
+    assert f >= slots * (8 + 4) + simg   # (vl,hu) pairs + alignment matrix
     assert u >= f + slots * 4            # + the stored cost tensor
     assert u - f < slots * 4 + 4096
     # pre-split [Y|1] and [X|1] operand images of the gradient contraction: per
@@ -59,10 +62,10 @@ def test_workspace_sizes(lib):
     assert L.sdtw_workspace_bytes(7, 4, 4, 4, 4, L.UNFUSED) == 0
     assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, 4, 4, 4, 4, 4) == 0
     # extended precision: 16-byte log-probabilities instead of 8-byte pairs (+8 more
-    # unfused); its gradients run on the FP32 pipe, so no operand images
+    # unfused); its costs and gradients run on the FP32 pipe, so no operand images
     fx = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.FUSED | L.EXTENDED)
     ux = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.UNFUSED | L.EXTENDED)
-    assert fx - (f - bimg) >= slots * 8 and ux - fx >= slots * 8
+    assert fx - (f - bimg - simg) >= slots * 8 and ux - fx >= slots * 8
 
 
 def _fwd(lib, x=0x1000, y=0x2000, B=2, N=3, M=4, D=2, gamma=1.0, mode=0, loss=0x3000, ws=0x100000,

@@ -85,6 +85,13 @@ def check_against_oracle(x, y, gamma, mode, grad_loss=None, sample=None, what=""
 
 MODES = [("unfused", 0), ("fused", 1)]
 
+# Per-problem upstream gradients for the fp32 modes: varied in sign and size, at
+# the scale of a batch-mean loss over the headline batch of 32, the setting the
+# gradient tolerance (abs 1e-5) is stated for. The extended mode is also checked
+# with O(1) weights (WEIGHTS_O1).
+WEIGHTS_O1 = [0.5, -1.25, 2.0]
+WEIGHTS = [w / 32 for w in WEIGHTS_O1]
+
 
 # --------------------------------------------------------------------------- small config
 
@@ -100,7 +107,7 @@ def test_small_config(mname, mode):
                                    (64, 65, 7), (100, 37, 16), (37, 100, 1), (129, 130, 9)])
 def test_ragged_shapes(mname, mode, N, M, D):
     x, y = synth.iid_normal_pair(3, N, M, D, 90, repeat=N * 1000 + M)
-    check_against_oracle(x, y, 0.7, mode, grad_loss=[0.5, -1.25, 2.0], what=f"{N}x{M}x{D} {mname}")
+    check_against_oracle(x, y, 0.7, mode, grad_loss=WEIGHTS, what=f"{N}x{M}x{D} {mname}")
 
 
 # Wide features in fp32. D=127 is the widest operand the gradient contraction
@@ -125,7 +132,7 @@ def test_wide_features_auto_precision(mname, base, N, M, D):
     mode = base | L.auto_precision(0.7, N, M, D)
     assert mode & L.EXTENDED
     x, y = synth.iid_normal_pair(3, N, M, D, 90, repeat=N * 1000 + M)
-    check_against_oracle(x, y, 0.7, mode, grad_loss=[0.5, -1.25, 2.0], what=f"{N}x{M}x{D} auto {mname}")
+    check_against_oracle(x, y, 0.7, mode, grad_loss=WEIGHTS_O1, what=f"{N}x{M}x{D} auto {mname}")
 
 
 @pytest.mark.parametrize("mname,mode", MODES)
@@ -152,7 +159,7 @@ def test_small_gamma_no_nan(gamma):
 @pytest.mark.parametrize("N,M,D", [(1, 1, 3), (1, 7, 2), (9, 1, 1), (31, 33, 3), (100, 37, 16), (129, 130, 9)])
 def test_extended_precision_shapes(mname, mode, N, M, D):
     x, y = synth.iid_normal_pair(3, N, M, D, 92, repeat=N * 1000 + M)
-    check_against_oracle(x, y, 0.7, mode, grad_loss=[0.5, -1.25, 2.0], what=f"{N}x{M}x{D} {mname}")
+    check_against_oracle(x, y, 0.7, mode, grad_loss=WEIGHTS_O1, what=f"{N}x{M}x{D} {mname}")
 
 
 @pytest.mark.parametrize("W", [1, 3])
@@ -162,12 +169,51 @@ def test_extended_strip_decompositions(W):
         check_against_oracle(x, y, 0.05, 3, what=f"extended W={W}")
 
 
+class env:
+    """Set environment variables for the duration of a block."""
+
+    def __init__(self, **kv):
+        self.kv = kv
+
+    def __enter__(self):
+        self.old = {k: os.environ.get(k) for k in self.kv}
+        os.environ.update({k: str(v) for k, v in self.kv.items()})
+
+    def __exit__(self, *a):
+        for k, v in self.old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
 def test_fused_equals_unfused():
+    # Both cost kernels exist in both modes: the tensor-core norm form (default,
+    # D <= 64) and the difference form (SDTW_DIST_SIMT / SDTW_FUSED_SIMT). With the
+    # same cost kernel the fused forward recomputes exactly the costs the unfused
+    # mode stores, so the two modes agree to rounding; across cost kernels they
+    # agree to the parity tolerance.
     x, y = synth.iid_normal_pair(4, 96, 80, 12, 94)
-    a = run_cuda(x, y, 1.0, 0)
-    b = run_cuda(x, y, 1.0, 1)
-    assert_close(b["loss"], a["loss"], 1e-5, 0.0, "fused vs unfused loss")
-    assert_close(b["gx"], a["gx"], 1e-4, 1e-6, "fused vs unfused grad_x")
+    tc_u = run_cuda(x, y, 1.0, 0)
+    tc_f = run_cuda(x, y, 1.0, 1)
+    with env(SDTW_DIST_SIMT=1, SDTW_FUSED_SIMT=1):
+        df_u = run_cuda(x, y, 1.0, 0)
+        df_f = run_cuda(x, y, 1.0, 1)
+    for what, a, b in (("tensor-core costs", tc_u, tc_f), ("difference-form costs", df_u, df_f)):
+        assert_close(b["loss"], a["loss"], 1e-5, 0.0, f"fused vs unfused ({what}) loss")
+        assert_close(b["gx"], a["gx"], 1e-4, 1e-6, f"fused vs unfused ({what}) grad_x")
+        assert_close(b["gy"], a["gy"], 1e-4, 1e-6, f"fused vs unfused ({what}) grad_y")
+    assert_close(tc_f["loss"], df_f["loss"], LOSS_RTOL, 0.0, "tensor-core vs difference-form costs, loss")
+    assert_close(tc_f["gx"], df_f["gx"], GRAD_RTOL, GRAD_ATOL, "tensor-core vs difference-form costs, grad_x")
+
+
+@pytest.mark.parametrize("mname,mode", MODES)
+def test_difference_form_cost_kernels(mname, mode):
+    # the difference-form cost path (the one D > 64 takes) at a width the tensor
+    # cores would otherwise handle
+    x, y = synth.iid_normal_pair(3, 70, 91, 20, 96)
+    with env(SDTW_DIST_SIMT=1, SDTW_FUSED_SIMT=1):
+        check_against_oracle(x, y, 0.8, mode, grad_loss=WEIGHTS, what=f"difference-form {mname}")
 
 
 def test_distance_kernel_matches_definition():
