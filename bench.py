@@ -33,9 +33,14 @@ B, N, M, D, GAMMA = 32, 512, 512, 64, 1.0
 CELLS = B * N * M
 WORKLOAD = "softdtw fwd+bwd B=32 N=M=512 D=64 gamma=1, unfused then fused"
 FALLBACK_HBM_GBS = 6800.0
-# kernels per step: unfused forward (distance, wavefront) + backward (wavefront,
-# operand-image prep, two gradient contractions), fused forward (1) + backward (4)
-LAUNCHES_PER_STEP = 2 + 4 + 1 + 4
+# DRAM bytes (read + write) of one bwd_kernel launch at this workload, from one
+# `ncu --set full` capture of it: 71.55 MB read + 8.17 MB written. Set to None
+# whenever the kernel changes until it is captured again.
+BWD_DRAM_BYTES = 79.72e6
+# kernels per step: unfused forward (operand images, cost tensor, wavefront) + backward
+# (wavefront, gradient operand images, two gradient contractions), fused forward
+# (operand images, wavefront with tensor-core costs) + backward (4)
+LAUNCHES_PER_STEP = 3 + 4 + 2 + 4
 
 
 def log(*a):
@@ -280,16 +285,18 @@ def run_ours(args):
         per_mode[name]["workspace_MB"] = ws.numel() / 2**20
         del ws, loss, gx_, gy_
 
-    # ---- roofline of the dominant kernel: the backward wavefront (fused mode, no gradient kernels)
+    # ---- roofline of the dominant kernel: the backward wavefront (38% of the kernel time of a step in
+    # the launch list), timed alone through sdtw_backward without input gradients (fused workspace)
     hbm, src = measured_peaks()
     bw_ms = per_mode["fused"]["bwd_wavefront_ms"]
     slots = B * ((N + 31) // 32) * (M + 31) * 32
-    bytes_bwd = CELLS * (8 + 4)  # (vl,hu) read + E write per cell
+    bytes_bwd = CELLS * (8 + 4)  # (v_left, h_up) pair read + E written, per cell
     achieved = bytes_bwd / (bw_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": None, "kernel": "bwd_kernel (log-space backward wavefront)",
+                "traffic": BWD_DRAM_BYTES, "kernel": "bwd_kernel (log-space backward wavefront)",
                 "peak_source": src, "algorithmic_bytes_per_launch": bytes_bwd, "skewed_slots": slots,
-                "launch_ms": bw_ms}
+                "launch_ms": bw_ms,
+                "note": "latency-bound: N+M-1 dependent DP steps; traffic from one ncu capture of this kernel"}
 
     # ---- end to end through the public API, host buffers, both modes
     xh = torch.from_numpy(x_np).pin_memory()
