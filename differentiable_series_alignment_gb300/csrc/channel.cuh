@@ -7,17 +7,22 @@ namespace sdtw {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// The waits below spin on the value itself and look at the global status word and
+// the clock only every kPollEvery retries: a global load per retry would put an
+// L2 round trip between the producer's store and the consumer noticing it.
+constexpr unsigned kPollEvery = 32;
+
 // Bounded wait on a shared-memory counter (back-pressure of a ring). Warp-uniform result.
 static __device__ __forceinline__ bool wait_smem(const volatile int* cnt, int target, const WaveParams& q) {
     bool ok = true;
     if (*cnt < target) {
-        const unsigned long long t0 = global_ns();
-        unsigned it = 0;
-        while (*cnt < target) {
-            __nanosleep(32);
-            if ((++it & 7u) == 0) {
+        unsigned long long t0 = 0;
+        for (unsigned it = 1; *cnt < target; ++it) {
+            if ((it % kPollEvery) == 0) {
+                if (t0 == 0) t0 = global_ns();
                 if (ld_volatile_global(q.status) != 0) { ok = false; break; }
                 if (global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); ok = false; break; }
+                __nanosleep(32);
             }
         }
     }
@@ -33,8 +38,8 @@ static __device__ __forceinline__ bool validate(Slot (&cur)[NS], const Slot* src
 #pragma unroll
     for (int k = 0; k < NS; ++k) mine = mine && (want == 0u || cur[k].tag == want);
     if (__all_sync(kFull, mine)) return true;
-    const unsigned long long t0 = global_ns();
-    for (;;) {
+    unsigned long long t0 = 0;
+    for (unsigned it = 1;; ++it) {
         if (!mine) {
 #pragma unroll
             for (int k = 0; k < NS; ++k) cur[k] = slot_load(src + k);
@@ -43,10 +48,13 @@ static __device__ __forceinline__ bool validate(Slot (&cur)[NS], const Slot* src
             for (int k = 0; k < NS; ++k) mine = mine && (cur[k].tag == want);
         }
         if (__all_sync(kFull, mine)) return true;
-        __nanosleep(20);
-        bool bad = ld_volatile_global(q.status) != 0;
-        if (!bad && global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); bad = true; }
-        if (__any_sync(kFull, bad)) return false;
+        if ((it % kPollEvery) == 0) {
+            if (t0 == 0) t0 = global_ns();
+            bool bad = ld_volatile_global(q.status) != 0;
+            if (!bad && global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); bad = true; }
+            if (__any_sync(kFull, bad)) return false;
+            __nanosleep(20);
+        }
     }
 }
 

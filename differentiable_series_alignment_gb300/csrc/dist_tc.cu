@@ -40,7 +40,8 @@ constexpr uint32_t kBlockBytes = kTile * 128;  // one K-block of 128 rows (32 tf
 constexpr int kStg = 63 * 32;                // per-warp skew staging (floats)
 
 // grid (Lpad/32, P, 2): z = 0 writes the x image, z = 1 the y image. block 256.
-// Rows past the sequence end are zero (image and norm).
+// Rows past the sequence end are zero (image and norm). KB <= 2: every thread
+// issues all of its loads (at most 8) before the first shared store.
 __global__ void __launch_bounds__(256) simg_kernel(Problems pr, int N, int M, int D, int KB, float* __restrict__ ximg,
                                                    float* __restrict__ yimg, float* __restrict__ xnorm,
                                                    float* __restrict__ ynorm)
@@ -55,25 +56,43 @@ __global__ void __launch_bounds__(256) simg_kernel(Problems pr, int N, int M, in
     float* img = isy ? yimg : ximg;
     float* nrm = isy ? ynorm : xnorm;
     const int D32 = 32 * KB, ld = D32 + 1;
-    for (int idx = threadIdx.x; idx < 32 * D32; idx += blockDim.x) {
+    const int n = 32 * D32 / 256;  // values per thread: 4 or 8
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int idx = threadIdx.x + 256 * u;
         const int r = idx / D32, k = idx - r * D32;
-        t[r * ld + k] = (r0 + r < L && k < D) ? src[(size_t)(r0 + r) * D + k] : 0.f;
+        v[u] = (u < n && r0 + r < L && k < D) ? src[(size_t)(r0 + r) * D + k] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int idx = threadIdx.x + 256 * u;
+        const int r = idx / D32, k = idx - r * D32;
+        if (u < n) t[r * ld + k] = v[u];
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-        // compensated fp32: each square split exactly (fma), partial sums by TwoSum
-        const int r = threadIdx.x;
+    {
+        // squared norm of row tid/8: eight threads take every eighth feature (exact
+        // squares by fma, TwoSum partial sums), then pairwise TwoSum across the eight
+        const int r = threadIdx.x >> 3, part = threadIdx.x & 7;
         float s = 0.f, c = 0.f;
-        for (int k = 0; k < D; ++k) {
-            const float v = t[r * ld + k];
-            const float sq = v * v;
-            const float e = fmaf(v, v, -sq);
+        for (int k = part; k < D; k += 8) {
+            const float x = t[r * ld + k];
+            const float sq = x * x;
             float sn, err;
             two_sum(s, sq, sn, err);
             s = sn;
-            c += err + e;
+            c += err + fmaf(x, x, -sq);
         }
-        nrm[(size_t)p * Lpad + r0 + r] = s + c;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const float so = __shfl_xor_sync(0xffffffffu, s, o), co = __shfl_xor_sync(0xffffffffu, c, o);
+            float sn, err;
+            two_sum(s, so, sn, err);
+            s = sn;
+            c += co + err;
+        }
+        if (part == 0) nrm[(size_t)p * Lpad + r0 + r] = s + c;
     }
     // a warp writes one 128-byte image row (32 features of one row) per pass
     for (int idx = threadIdx.x; idx < 32 * D32; idx += blockDim.x) {

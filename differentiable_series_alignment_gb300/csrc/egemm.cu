@@ -11,9 +11,9 @@
 // nearest) and store both in the 128-byte-swizzled K-major layout. The B tiles
 // ([Y | 1] or [X | 1]) are the same for every CTA of a problem, so a small
 // kernel writes them once, already split and swizzled, and each CTA fetches a
-// K-tile's B image with one bulk copy. A ninth warp issues the copies and the
-// 3xTF32 products hi*hi + lo*hi + hi*lo with tcgen05.mma (fp32 accumulation in
-// tensor memory); workers and issuer hand buffers over through mbarriers, so
+// K-tile's B image with one bulk copy. One warp issues the 3xTF32 products
+// hi*hi + lo*hi + hi*lo with tcgen05.mma (fp32 accumulation in tensor memory)
+// and two more issue the bulk copies; all hand buffers over through mbarriers, so
 // the un-skew of tile k+1 overlaps the MMAs of tile k and the copies run two to
 // four K-tiles ahead. The epilogue reads the accumulators back with tcgen05.ld
 // and writes the gradient rows through a shared-memory tile.
@@ -92,7 +92,10 @@ struct Pipe {
 
 constexpr int kMaxRing = 4;
 constexpr int kWorkers = 256;            // warps 0-7: un-skew and epilogue
-constexpr int kIssuer = 8;               // warp 8: bulk copies and MMAs (lane 0)
+constexpr int kMmaWarp = 8;              // warp 8: tcgen05.mma issue (lane 0)
+constexpr int kCopyAWarp = 9;            // warp 9: bulk copies of the skewed E rows (lane 0)
+constexpr int kCopyBWarp = 10;           // warp 10: bulk copies of the B images (lane 0)
+constexpr int kThreadsTotal = kWorkers + 3 * 32;
 constexpr int kStageStride = 65;         // epilogue staging row stride (floats)
 
 __device__ __forceinline__ void workers_sync() {
@@ -104,18 +107,18 @@ __device__ __forceinline__ void workers_sync() {
 // bimg: per problem, per K-tile, the pre-split B image (bimg_kernel).
 //
 // Warp-specialised pipeline, all hand-offs through mbarriers:
-//   issuer  : MMAs of tile kt once its A stage is full and its B image has landed,
-//             committed to the A-stage and B-buffer "empty" barriers; then the B image
-//             of tile kt+pb-1 (its buffer freed by MMA(kt-1)) and the raw A rows of
-//             tile kt+pa (entry kt%pa, released by the workers before "A full").
-//   workers : wait for raw A of tile kt and for A stage kt%ts to be empty (MMA(kt-ts)),
+//   MMA warp   : MMAs of tile kt once its A stage is full and its B image has landed,
+//                committed to the A-stage and B-buffer "empty" barriers.
+//   copy warps : raw E rows of tile k once the workers released entry k % pa; the B
+//                image of tile k once MMA(k - pb) has freed buffer k % pb.
+//   workers    : wait for raw A of tile kt and for A stage kt%ts to be empty (MMA(kt-ts)),
 //             un-skew + split into the stage, then each warp arrives on "raw empty" and
 //             "A full". After the last commit they stage the accumulators through shared
 //             memory and write the gradient rows with coalesced stores.
 // Barrier parities: entry e of a ring of depth P serves tiles e, e+P, ...; tile k's
 // phase has parity (k/P)&1 and every wait is for the oldest phase not yet reused.
 template <bool COLS>
-__global__ void __launch_bounds__(kWorkers + 32, 1)
+__global__ void __launch_bounds__(kThreadsTotal, 1)
     egemm_kernel(const GradParams g, const float* __restrict__ bimg, int n_total, Pipe pp, int* status)
 {
     extern __shared__ unsigned char smem_dyn[];
@@ -177,21 +180,8 @@ __global__ void __launch_bounds__(kWorkers + 32, 1)
     const uint32_t tmem = s_tmem;
     bool ok = true;
 
-    if (warp == kIssuer) {
+    if (warp == kMmaWarp) {
         if (lane == 0) {
-            int a_last[kMaxRing], b_last[kMaxRing];  // last tile copied into each entry
-            for (int e = 0; e < kMaxRing; ++e) a_last[e] = b_last[e] = -1;
-            for (int k = 0; k < pa && k < nK; ++k) {
-                issue_a<COLS>(Ekp, N, M, T, m0, k, rawA(k), smem_u32(&s_raw_full[k % pa]));
-                a_last[k % pa] = k;
-            }
-            // B image kt + bl is issued after MMA(kt): its buffer last held tile kt + bl - pb,
-            // read by MMA(kt - 1) when pb >= 2 (already complete, no stall)
-            const int bl = pb > 1 ? pb - 1 : 1;
-            for (int k = 0; k < bl && k < nK; ++k) {
-                issue_b(bimg_p, n_total, k, bbuf(k), smem_u32(&s_b_full[k % pb]));
-                b_last[k % pb] = k;
-            }
             for (int kt = 0; kt < nK && ok; ++kt) {
                 wait_ok(ok, smem_u32(&s_a_full[kt % ts]), (uint32_t)((kt / ts) & 1), status);
                 wait_ok(ok, smem_u32(&s_b_full[kt % pb]), (uint32_t)((kt / pb) & 1), status);
@@ -224,29 +214,41 @@ __global__ void __launch_bounds__(kWorkers + 32, 1)
                 }
                 mma_commit(smem_u32(&s_a_empty[kt % ts]));
                 mma_commit(smem_u32(&s_b_empty[kt % pb]));
-                const int kb = kt + bl;
-                if (kb < nK) {
-                    if (kb >= pb) wait_ok(ok, smem_u32(&s_b_empty[kb % pb]), (uint32_t)(((kb - pb) / pb) & 1), status);
-                    if (!ok) break;
-                    issue_b(bimg_p, n_total, kb, bbuf(kb), smem_u32(&s_b_full[kb % pb]));
-                    b_last[kb % pb] = kb;
-                }
-                const int ka = kt + pa;  // entry kt % pa, released (before A full) after the un-skew of tile kt
-                if (ka < nK) {
-                    wait_ok(ok, smem_u32(&s_raw_empty[kt % pa]), (uint32_t)((kt / pa) & 1), status);
-                    if (!ok) break;
-                    issue_a<COLS>(Ekp, N, M, T, m0, ka, rawA(ka), smem_u32(&s_raw_full[ka % pa]));
-                    a_last[ka % pa] = ka;
-                }
             }
             // releases the workers once every MMA issued above has completed
             mma_commit(smem_u32(&s_acc));
-            // no copy may still be writing shared memory when the CTA exits
-            bool drained = true;
-            for (int e = 0; e < kMaxRing; ++e) {
-                if (a_last[e] >= 0) wait_ok(drained, smem_u32(&s_raw_full[e]), (uint32_t)((a_last[e] / pa) & 1), status);
-                if (b_last[e] >= 0) wait_ok(drained, smem_u32(&s_b_full[e]), (uint32_t)((b_last[e] / pb) & 1), status);
+        }
+        __syncwarp();
+    } else if (warp == kCopyAWarp) {
+        // raw E rows of tile k into entry k % pa, once the workers released tile k - pa
+        if (lane == 0) {
+            int last[kMaxRing];
+            for (int e = 0; e < kMaxRing; ++e) last[e] = -1;
+            for (int k = 0; k < nK && ok; ++k) {
+                if (k >= pa) wait_ok(ok, smem_u32(&s_raw_empty[k % pa]), (uint32_t)(((k - pa) / pa) & 1), status);
+                if (!ok) break;
+                issue_a<COLS>(Ekp, N, M, T, m0, k, rawA(k), smem_u32(&s_raw_full[k % pa]));
+                last[k % pa] = k;
             }
+            bool drained = true;  // no copy may still be writing shared memory when the CTA exits
+            for (int e = 0; e < kMaxRing; ++e)
+                if (last[e] >= 0) wait_ok(drained, smem_u32(&s_raw_full[e]), (uint32_t)((last[e] / pa) & 1), status);
+        }
+        __syncwarp();
+    } else if (warp == kCopyBWarp) {
+        // B image of tile k into buffer k % pb, once MMA(k - pb) has read it
+        if (lane == 0) {
+            int last[kMaxRing];
+            for (int e = 0; e < kMaxRing; ++e) last[e] = -1;
+            for (int k = 0; k < nK && ok; ++k) {
+                if (k >= pb) wait_ok(ok, smem_u32(&s_b_empty[k % pb]), (uint32_t)(((k - pb) / pb) & 1), status);
+                if (!ok) break;
+                issue_b(bimg_p, n_total, k, bbuf(k), smem_u32(&s_b_full[k % pb]));
+                last[k % pb] = k;
+            }
+            bool drained = true;
+            for (int e = 0; e < kMaxRing; ++e)
+                if (last[e] >= 0) wait_ok(drained, smem_u32(&s_b_full[e]), (uint32_t)((last[e] / pb) & 1), status);
         }
         __syncwarp();
     } else {
@@ -415,12 +417,23 @@ __global__ void __launch_bounds__(256) bimg_kernel(const GradParams g, int n_tot
     unsigned char* lo = hi + (size_t)n_total * 128;
     const int ld = n_total + 1;
     const int here = min(kBK, kdim - kt * kBK);
-#pragma unroll 4
-    for (int idx = threadIdx.x; idx < kBK * n_total; idx += 256) {
-        const int k = idx / n_total, n = idx - k * n_total;
-        float v = 0.f;
-        if (k < here) v = (n < D) ? src[(size_t)k * D + n] : (n == D ? 1.f : 0.f);
-        t[k * ld + n] = v;
+    // loads in batches of 16 per thread, all issued before their shared stores
+    for (int base = 0; base < kBK * n_total; base += 256 * 16) {
+        float v[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int idx = base + threadIdx.x + 256 * u;
+            const int k = idx / n_total, n = idx - k * n_total;
+            float x = 0.f;
+            if (idx < kBK * n_total && k < here) x = (n < D) ? src[(size_t)k * D + n] : (n == D ? 1.f : 0.f);
+            v[u] = x;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int idx = base + threadIdx.x + 256 * u;
+            const int k = idx / n_total, n = idx - k * n_total;
+            if (idx < kBK * n_total) t[k * ld + n] = v[u];
+        }
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < kBK * n_total; idx += 256) {
@@ -485,11 +498,11 @@ cudaError_t launch_grad_tc(const GradParams& g, bool cols, const float* bimg, in
     if (cols) {
         e = cudaFuncSetAttribute(egemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        egemm_kernel<true><<<grid, kWorkers + 32, smem, st>>>(g, bimg, n_total, pp, status);
+        egemm_kernel<true><<<grid, kThreadsTotal, smem, st>>>(g, bimg, n_total, pp, status);
     } else {
         e = cudaFuncSetAttribute(egemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        egemm_kernel<false><<<grid, kWorkers + 32, smem, st>>>(g, bimg, n_total, pp, status);
+        egemm_kernel<false><<<grid, kThreadsTotal, smem, st>>>(g, bimg, n_total, pp, status);
     }
     return cudaGetLastError();
 }
