@@ -56,12 +56,29 @@ def dist_env():
 
 # --------------------------------------------------------------------------- reference arm
 
+def time_max_over_ranks(total_ms, device=None):
+    """The slowest rank's timed total (ms): every rank gets the max, so the job's
+    throughput is the units all ranks processed over the longest time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(total_ms)
+    t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, steps, cells_per_step, total_ms):
+    """Whole-job cells/s: every rank runs `steps` steps of its own batch (weak scaling)."""
+    return world * steps * cells_per_step / (total_ms * 1e-3)
+
+
 def run_reference(args):
+    ws, rank, _ = dist_env()
+    if ws > 1 and rank != 0:  # rank 0 alone times the oracle; the others exit without work
+        return 0
     import oracle
     from differentiable_series_alignment_gb300 import synth
-    ws, rank, _ = dist_env()
-    if ws > 1 and rank != 0:
-        return 0
     x, y = synth.iid_normal_pair(B, N, M, D, 1)
     cores = oracle.threads_used(0)
     sample = max(1, min(cores, B))  # problems per step: one per host core, run in parallel
@@ -234,15 +251,11 @@ def run_ours(args):
         dist.barrier()
     clocks = clk.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = float(np.sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = time_max_over_ranks(float(np.sum(step_ms)), dev)
     for mode in (L.UNFUSED, L.FUSED):
         assert L.sdtw_last_device_status(bufs[mode]["ws"]) == 0
     cells_per_step = 2 * CELLS
-    value = world * K * cells_per_step / (total_ms * 1e-3)
+    value = job_value(world, K, cells_per_step, total_ms)
 
     # ---- per mode, per kernel (events on the launching stream), L2 flushed between iterations
     def timed(fn, iters):

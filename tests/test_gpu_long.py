@@ -71,3 +71,34 @@ def test_long_normalized(data):
     assert np.all(np.abs(loss - ol) <= atol + LOSS_RTOL * np.abs(ol)), (loss, ol)
     assert_close(gx, ogx, GRAD_RTOL, GRAD_ATOL, "long normalized grad_x")
     assert_close(gy, ogy, GRAD_RTOL, GRAD_ATOL, "long normalized grad_y")
+
+
+def test_barycenter_full_size():
+    """The barycenter workload at full size: K=64 block-wave sequences of length
+    1024, D=8, gamma=1, lr=0.1, fused mode, initialised to the mean. Two steps are
+    checked against the oracle from the CUDA path's own state; the remaining 98 of
+    the 100 steps run on the GPU, with finite losses that end below the first."""
+    from differentiable_series_alignment_gb300 import _lib as Lb
+    K, T, D = 64, 1024, 8
+    X = synth.block_waves(K, T, D, 4)
+    mode = Lb.FUSED | Lb.auto_precision(1.0, T, T, D)
+    z0 = X.astype(np.float64).mean(axis=0).astype(np.float32)
+    Xt = torch.from_numpy(X).cuda()
+    z = torch.from_numpy(z0.copy()).cuda()
+    m, v = torch.zeros_like(z), torch.zeros_like(z)
+    ws = Lb.workspace(Lb.OP_BARYCENTER, K, T, T, D, mode)
+    losses = torch.empty(100, device="cuda")
+    for t in (1, 2):
+        zc, mc, vc = z.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
+        zo, mo, vo, lref, _ = oracle.barycenter_step(zc, mc, vc, t, X, 1.0, lr=0.1)
+        Lb.sdtw_barycenter_step(z, m, v, t, Xt, 1.0, 0.1, 0.9, 0.999, 1e-8, mode, losses[t - 1:t], ws)
+        assert Lb.sdtw_last_device_status(ws) == 0
+        assert_close(losses[t - 1:t].cpu().numpy(), [lref], LOSS_RTOL, 0.0, f"full-size barycenter step {t} loss")
+        assert_close(m.cpu().numpy(), mo, GRAD_RTOL, GRAD_ATOL, f"full-size barycenter step {t} first moment")
+        assert_close(z.cpu().numpy() - zc, zo - zc, 2e-3, 1e-6, f"full-size barycenter step {t} update")
+    for t in range(3, 101):
+        Lb.sdtw_barycenter_step(z, m, v, t, Xt, 1.0, 0.1, 0.9, 0.999, 1e-8, mode, losses[t - 1:t], ws)
+    assert Lb.sdtw_last_device_status(ws) == 0
+    lo = losses.cpu().numpy()
+    assert np.all(np.isfinite(lo)) and np.all(np.isfinite(z.cpu().numpy()))
+    assert lo[-1] < lo[0]
