@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/sdtw.h"
 #include "common.cuh"
@@ -232,8 +233,7 @@ sdtw_status run_backward(const Problems& pr, const Layout& L, void* ws, float ga
 // Gradients: tensor-core GEMM form (egemm.cu) by default; the difference form
 // (grad.cu, FP32 pipe) in the extended-precision mode, where rows or columns
 // that align to many cells make the GEMM form cancel beyond fp32.
-sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void* ws, const float* grad_loss,
-                      float coef, float* out_x, float* out_y, int accumulate, int mode, cudaStream_t st)
+GradParams grad_params(const Problems& all, int set, int B, const Layout& L, void* ws)
 {
     GradParams g{};
     g.pr = all;
@@ -242,6 +242,30 @@ sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void
     g.pr.B = B;
     g.P = B; g.N = L.N; g.M = L.M; g.D = L.D;
     g.E = at<float>(ws, L.e) + (size_t)set * B * skew_slots(L.N, L.M);
+    return g;
+}
+
+// A second stream per device for work that can overlap the caller's stream
+// (created once, non-blocking; ordered against the caller's stream by events).
+cudaStream_t side_stream()
+{
+    static std::mutex mu;
+    static cudaStream_t streams[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+        streams[dev] = nullptr;
+    return streams[dev];
+}
+
+// images_ready: when not null, the operand images were already launched on
+// another stream; the contractions wait on this event instead of building them.
+sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void* ws, const float* grad_loss,
+                      float coef, float* out_x, float* out_y, int accumulate, int mode, cudaStream_t st,
+                      cudaEvent_t images_ready = nullptr)
+{
+    GradParams g = grad_params(all, set, B, L, ws);
     g.grad_loss = grad_loss;
     g.wmod = B;
     g.coef = coef;
@@ -251,7 +275,8 @@ sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void
     int* status = at<int>(ws, L.status);
     float* img_rows = at<float>(ws, L.bimg);
     float* img_cols = at<float>(ws, L.bimg2);
-    if (!simt) SDTW_CUDA(launch_bimg(g, out_x ? img_rows : nullptr, out_y ? img_cols : nullptr, st));
+    if (!simt && images_ready) SDTW_CUDA(cudaStreamWaitEvent(st, images_ready, 0));
+    else if (!simt) SDTW_CUDA(launch_bimg(g, out_x ? img_rows : nullptr, out_y ? img_cols : nullptr, st));
     if (out_x) {
         g.out = out_x;
         g.out_stride = (long long)L.N * L.D;
@@ -326,9 +351,33 @@ sdtw_status sdtw_backward(const float* x, const float* y, int B, int N, int M, i
     pr.xstride[0] = (long long)N * D; pr.ystride[0] = (long long)M * D;
     pr.B = B;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if ((s = run_backward(pr, L, ws, gamma, (int)mode, st)) != SDTW_OK) return s;
-    if (grad_x || grad_y) return run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, (int)mode, st);
-    return SDTW_OK;
+    // The gradient operand images depend on x and y only: they are built on a side
+    // stream while the backward wavefront runs (it leaves most of each SM idle).
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    const bool tc_grads = (grad_x || grad_y) && !(mode & SDTW_EXTENDED) && env_int("SDTW_GRAD_SIMT", 0) == 0;
+    if (tc_grads && (side = side_stream()) != nullptr &&
+        cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
+        cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess) {
+        GradParams g = grad_params(pr, 0, B, L, ws);
+        bool launched = cudaEventRecord(fork, st) == cudaSuccess && cudaStreamWaitEvent(side, fork, 0) == cudaSuccess &&
+                        launch_bimg(g, grad_x ? at<float>(ws, L.bimg) : nullptr,
+                                    grad_y ? at<float>(ws, L.bimg2) : nullptr, side) == cudaSuccess &&
+                        cudaEventRecord(join, side) == cudaSuccess;
+        cudaEventDestroy(fork);  // released once complete
+        if (!launched) {
+            cudaEventDestroy(join);
+            return SDTW_ERR_CUDA;
+        }
+    }
+    s = run_backward(pr, L, ws, gamma, (int)mode, st);
+    if (s == SDTW_OK && (grad_x || grad_y))
+        s = run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, (int)mode, st, join);
+    if (join) {
+        if (s != SDTW_OK) cudaStreamWaitEvent(st, join, 0);  // keep the side work ordered before later calls
+        cudaEventDestroy(join);
+    }
+    return s;
 }
 
 sdtw_status sdtw_normalized(const float* x, const float* y, int B, int N, int D, float gamma, sdtw_mode mode,

@@ -12,13 +12,14 @@
 // hi + lo parts (round to nearest), stored in the 128-byte-swizzled K-major
 // layout that tcgen05.mma reads, in K-blocks of 32 features, together with the
 // squared norm of the row (compensated fp32: exact squares, TwoSum partial
-// sums). A cost CTA (dist_tc_kernel) bulk-copies the 128 x-rows and 128 y-rows of its tile into
-// shared memory and one thread issues the 3xTF32 products
-//   x_hi . [y_hi ; y_lo]  (N = 256)   and   x_lo . y_hi  (N = 128)
-// per 8-wide K step into tensor memory. Eight warps read the accumulators back,
-// form the cost, clamp it at 0 and write the skewed layout of the wavefront
-// through a per-warp shared staging tile, so every global store is a 128-byte
-// slot row.
+// sums). A cost CTA (dist_tc_kernel) keeps the 128 x rows of its block in shared
+// memory and streams the y rows in tiles of 64 by bulk copy; one thread issues
+// the 3xTF32 products
+//   x_hi . [y_hi ; y_lo]  (N = 128)   and   x_lo . y_hi  (N = 64)
+// per 8-wide K step into one of two tensor-memory slots, while eight warps drain
+// the other slot: they read the accumulators back, form the cost, clamp it at 0
+// and write the skewed layout of the wavefront through a per-warp shared staging
+// tile, so every global store is a 128-byte slot row.
 //
 // Precision: the dot carries ~2^-21 of sum_k |x_k y_k|, and the final fp32
 // combination a few ulps of C; at D <= 64 that keeps the gradient of the
@@ -34,10 +35,13 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTile = 128;                   // rows and columns per cost CTA
-constexpr int kTcThreads = 256;              // 8 warps
-constexpr uint32_t kBlockBytes = kTile * 128;  // one K-block of 128 rows (32 tf32 each)
-constexpr int kStg = 63 * 32;                // per-warp skew staging (floats)
+constexpr int kTile = 128;                     // x rows per cost CTA (the MMA height)
+constexpr int kColTile = 64;                   // y columns per cost tile
+constexpr int kTcWarps = 8;                    // epilogue warps; warp 8 copies and issues the MMAs
+constexpr int kTcThreads = (kTcWarps + 1) * 32;
+constexpr uint32_t kBlockBytes = kTile * 128;  // one K-block of 128 x rows (32 tf32 each)
+constexpr uint32_t kYHalf = kColTile * 128;    // one K-block of 64 y rows, hi or lo
+constexpr int kStg = 63 * 32;                  // per-warp skew staging (floats)
 
 // grid (Lpad/32, P, 2): z = 0 writes the x image, z = 1 the y image. block 256.
 // Rows past the sequence end are zero (image and norm). KB <= 2: every thread
@@ -105,7 +109,13 @@ __global__ void __launch_bounds__(256) simg_kernel(Problems pr, int N, int M, in
     }
 }
 
-// grid (ceil(M/128), ceil(N/128), P), block 256. One 128 x 128 cost tile.
+// grid (ceil(N/128), P), block 288: one CTA per 128-row block of x and problem,
+// walking the y columns in tiles of 64. Warp 8 (lane 0) copies the x rows once
+// and each y tile into a two-entry ring, and issues every tile's MMAs into one of
+// two tensor-memory slots; warps 0-7 drain a slot (epilogue) while the next
+// tile's MMAs run. Hand-offs (all bounded mbarrier waits):
+//   s_bfull[e]  y tile in entry e      s_bempty[e] its MMAs are done
+//   s_tfull[t]  costs in TMEM slot t   s_tfree[t]  the 8 epilogue warps read slot t
 template <int KB>
 __global__ void __launch_bounds__(kTcThreads, 1)
     dist_tc_kernel(int N, int M, const float* __restrict__ ximg, const float* __restrict__ yimg,
@@ -113,25 +123,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    int* status)
 {
     extern __shared__ unsigned char smem_dyn[];
-    __shared__ uint64_t s_load, s_mma;
+    __shared__ uint64_t s_a, s_done, s_bfull[2], s_bempty[2], s_tfull[2], s_tfree[2];
     __shared__ uint32_t s_tmem;
-    __shared__ float s_ny[kTile];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int p = blockIdx.z, r0 = blockIdx.y * kTile, c0 = blockIdx.x * kTile;
+    const int p = blockIdx.y, r0 = blockIdx.x * kTile;
     const int Npad = (N + kTile - 1) / kTile * kTile, Mpad = (M + kTile - 1) / kTile * kTile;
     const int NB = (N + 31) / 32;
+    const int nC = (M + kColTile - 1) / kColTile;
 
-    // shared memory (1 KiB aligned): A_hi[KB], A_lo[KB], B[KB] = [y_hi ; y_lo], staging
+    // shared memory (1 KiB aligned): A_hi[KB], A_lo[KB], 2 y entries of KB x [hi 64 rows | lo 64 rows], staging
     unsigned char* base = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
     unsigned char* a_hi = base;
     unsigned char* a_lo = base + KB * kBlockBytes;
-    unsigned char* bst = base + 2 * KB * kBlockBytes;
-    float* stg = reinterpret_cast<float*>(bst + 2 * KB * kBlockBytes) + warp * kStg;
+    unsigned char* yring = base + 2 * KB * kBlockBytes;
+    auto yent = [&](int e, int kb) { return yring + (e * KB + kb) * 2 * kYHalf; };
+    float* stg = reinterpret_cast<float*>(yring + 2 * KB * 2 * kYHalf) + warp * kStg;
 
     if (tid == 0) {
-        mbar_init(smem_u32(&s_load), 1);
-        mbar_init(smem_u32(&s_mma), 1);
+        mbar_init(smem_u32(&s_a), 1);
+        mbar_init(smem_u32(&s_done), 1);
+        for (int e = 0; e < 2; ++e) {
+            mbar_init(smem_u32(&s_bfull[e]), 1);
+            mbar_init(smem_u32(&s_bempty[e]), 1);
+            mbar_init(smem_u32(&s_tfull[e]), 1);
+            mbar_init(smem_u32(&s_tfree[e]), kTcWarps);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tmem_alloc(&s_tmem, 256);
@@ -139,77 +156,101 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = s_tmem;
-
     bool ok = true;
-    if (tid == 0) {
-        mbar_expect_tx(smem_u32(&s_load), 4u * KB * kBlockBytes);
-        for (int kb = 0; kb < KB; ++kb) {
-            bulk_g2s(smem_u32(a_hi + kb * kBlockBytes), ximg + simg_offset(p, KB, kb, 0, Npad, r0), kBlockBytes,
-                     smem_u32(&s_load));
-            bulk_g2s(smem_u32(a_lo + kb * kBlockBytes), ximg + simg_offset(p, KB, kb, 1, Npad, r0), kBlockBytes,
-                     smem_u32(&s_load));
-            bulk_g2s(smem_u32(bst + kb * 2 * kBlockBytes), yimg + simg_offset(p, KB, kb, 0, Mpad, c0), kBlockBytes,
-                     smem_u32(&s_load));
-            bulk_g2s(smem_u32(bst + kb * 2 * kBlockBytes + kBlockBytes), yimg + simg_offset(p, KB, kb, 1, Mpad, c0),
-                     kBlockBytes, smem_u32(&s_load));
-        }
-    }
-    if (tid < kTile) s_ny[tid] = ynorm[(size_t)p * Mpad + c0 + tid];
-    if (tid == 0) {
-        wait_ok(ok, smem_u32(&s_load), 0u, status);
-        if (!ok) {
-            // no copy may still be writing shared memory when the CTA exits
-            bool drained = true;
-            wait_ok(drained, smem_u32(&s_load), 0u, status);
-        }
-        fence_after_sync();
-        const uint32_t id2 = idesc_tf32(kTile, 2 * kTile), id1 = idesc_tf32(kTile, kTile);
-#pragma unroll
-        for (int kb = 0; kb < KB; ++kb) {
-            const uint32_t ah = smem_u32(a_hi + kb * kBlockBytes), al = smem_u32(a_lo + kb * kBlockBytes);
-            const uint32_t bh = smem_u32(bst + kb * 2 * kBlockBytes);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
-                mma_tf32(tmem, sdesc(ah + ko), sdesc(bh + ko), id2, (kb > 0 || ks > 0) ? 1u : 0u);
-                mma_tf32(tmem, sdesc(al + ko), sdesc(bh + ko), id1, 1u);
-            }
-        }
-        mma_commit(smem_u32(&s_mma));
-    }
-    __syncthreads();  // s_ny
-    wait_ok(ok, smem_u32(&s_mma), 0u, status);
-    fence_after_sync();
 
-    // ---- epilogue: warp w reads rows 32(w mod 4) + lane (its TMEM lane quarter) and
-    // columns [64 (w / 4), 64 (w / 4) + 64) in two chunks of 32
-    const int q = warp & 3, half = warp >> 2;
-    const int rb = (r0 >> 5) + q;
-    const int row = r0 + 32 * q + lane;
-    const float nx = xnorm[(size_t)p * Npad + row];
-    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
-    float* out = (rb < NB) ? Dsk + skew_index(N, M, p, rb, 0, lane) : nullptr;
-    const bool skip = out == nullptr || !__all_sync(0xffffffffu, ok);  // warp-uniform
-#pragma unroll 1
-    for (int cc = 0; cc < 2; ++cc) {
-        const int ch = 2 * half + cc;
-        float a[32], b[32];
-        tmem_ld32(trow + (uint32_t)(32 * ch), a);
-        tmem_ld32(trow + (uint32_t)(kTile + 32 * ch), b);
-        if (skip) continue;
+    if (warp == kTcWarps) {
+        if (lane == 0) {
+            mbar_expect_tx(smem_u32(&s_a), 2u * KB * kBlockBytes);
+            for (int kb = 0; kb < KB; ++kb) {
+                bulk_g2s(smem_u32(a_hi + kb * kBlockBytes), ximg + simg_offset(p, KB, kb, 0, Npad, r0), kBlockBytes,
+                         smem_u32(&s_a));
+                bulk_g2s(smem_u32(a_lo + kb * kBlockBytes), ximg + simg_offset(p, KB, kb, 1, Npad, r0), kBlockBytes,
+                         smem_u32(&s_a));
+            }
+            int y_last[2] = {-1, -1};
+            auto issue_y = [&](int c) {
+                const int e = c & 1;
+                mbar_expect_tx(smem_u32(&s_bfull[e]), 2u * KB * kYHalf);
+                for (int kb = 0; kb < KB; ++kb) {
+                    bulk_g2s(smem_u32(yent(e, kb)), yimg + simg_offset(p, KB, kb, 0, Mpad, c * kColTile), kYHalf,
+                             smem_u32(&s_bfull[e]));
+                    bulk_g2s(smem_u32(yent(e, kb) + kYHalf), yimg + simg_offset(p, KB, kb, 1, Mpad, c * kColTile),
+                             kYHalf, smem_u32(&s_bfull[e]));
+                }
+                y_last[e] = c;
+            };
+            for (int c = 0; c < 2 && c < nC; ++c) issue_y(c);
+            wait_ok(ok, smem_u32(&s_a), 0u, status);
+            const uint32_t id2 = idesc_tf32(kTile, 2 * kColTile), id1 = idesc_tf32(kTile, kColTile);
+            for (int c = 0; c < nC && ok; ++c) {
+                const int e = c & 1, t = c & 1;
+                wait_ok(ok, smem_u32(&s_bfull[e]), (uint32_t)((c >> 1) & 1), status);
+                if (c >= 2) wait_ok(ok, smem_u32(&s_tfree[t]), (uint32_t)(((c - 2) >> 1) & 1), status);
+                if (!ok) break;
+                fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)(t * 2 * kColTile);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float c = fmaxf(nx + s_ny[32 * ch + j] - 2.f * (a[j] + b[j]), 0.f);
-            stg[(j + lane) * 32 + lane] = c;
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t ah = smem_u32(a_hi + kb * kBlockBytes), al = smem_u32(a_lo + kb * kBlockBytes);
+                    const uint32_t bh = smem_u32(yent(e, kb));
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
+                        mma_tf32(d, sdesc(ah + ko), sdesc(bh + ko), id2, (kb > 0 || ks > 0) ? 1u : 0u);
+                        mma_tf32(d, sdesc(al + ko), sdesc(bh + ko), id1, 1u);
+                    }
+                }
+                mma_commit(smem_u32(&s_tfull[t]));
+                mma_commit(smem_u32(&s_bempty[e]));
+                if (c + 2 < nC) {  // entry e takes tile c + 2 once MMA(c) has read it
+                    wait_ok(ok, smem_u32(&s_bempty[e]), (uint32_t)((c >> 1) & 1), status);
+                    if (!ok) break;
+                    issue_y(c + 2);
+                }
+            }
+            // no MMA may still be running, and no copy still writing shared memory, at exit
+            mma_commit(smem_u32(&s_done));
+            bool fin = true;
+            wait_ok(fin, smem_u32(&s_done), 0u, status);
+            for (int e = 0; e < 2; ++e)
+                if (y_last[e] >= 0) wait_ok(fin, smem_u32(&s_bfull[e]), (uint32_t)((y_last[e] >> 1) & 1), status);
         }
         __syncwarp();
-        // skewed slot c0 + 32 ch + t holds column (t - lane) of this chunk for this lane's row
-        const int cb = c0 + 32 * ch;
-        for (int t = 0; t < 63; ++t) {
-            const int j = t - lane;
-            if (j >= 0 && j < 32 && cb + j < M && row < N) out[(long long)(cb + t) * 32] = stg[t * 32 + lane];
+    } else {
+        // warp w: TMEM lane quarter w mod 4 (rows r0 + 32(w mod 4) + lane), 32-column half w / 4 of each tile
+        const int q = warp & 3, half = warp >> 2;
+        const int rb = (r0 >> 5) + q;
+        const int row = r0 + 32 * q + lane;
+        const float nx = xnorm[(size_t)p * Npad + row];
+        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+        float* out = (rb < NB) ? Dsk + skew_index(N, M, p, rb, 0, lane) : nullptr;
+        for (int c = 0; c < nC; ++c) {
+            const int t = c & 1;
+            wait_ok(ok, smem_u32(&s_tfull[t]), (uint32_t)((c >> 1) & 1), status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            fence_after_sync();
+            float a[32], b[32];
+            tmem_ld32(trow + (uint32_t)(t * 2 * kColTile + 32 * half), a);
+            tmem_ld32(trow + (uint32_t)(t * 2 * kColTile + kColTile + 32 * half), b);
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s_tfree[t]));
+            const int cb = c * kColTile + 32 * half;  // first column of this warp's chunk
+            if (out == nullptr || cb >= M) continue;  // warp-uniform
+            const float nyv = ynorm[(size_t)p * Mpad + cb + lane];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float ny = __shfl_sync(0xffffffffu, nyv, j);
+                stg[(j + lane) * 32 + lane] = fmaxf(nx + ny - 2.f * (a[j] + b[j]), 0.f);
+            }
+            __syncwarp();
+            // skewed slot cb + tt holds column (tt - lane) of this chunk for this lane's row
+            for (int tt = 0; tt < 63; ++tt) {
+                const int j = tt - lane;
+                if (j >= 0 && j < 32 && cb + j < M && row < N) out[(long long)(cb + tt) * 32] = stg[tt * 32 + lane];
+            }
+            __syncwarp();
         }
-        __syncwarp();
     }
 
     fence_before_sync();
@@ -250,8 +291,9 @@ cudaError_t launch_dist_tc(int P, int N, int M, int D, const float* ximg, const 
 {
     const int KB = (D + 31) / 32;
     if (KB < 1 || KB > 2) return cudaErrorInvalidValue;
-    const size_t smem = 1024 + 4 * (size_t)KB * kBlockBytes + 8 * kStg * sizeof(float);
-    dim3 grid((M + kTile - 1) / kTile, (N + kTile - 1) / kTile, P);
+    const size_t smem = 1024 + 2 * (size_t)KB * kBlockBytes + 2 * (size_t)KB * 2 * kYHalf +
+                        (size_t)kTcWarps * kStg * sizeof(float);
+    dim3 grid((N + kTile - 1) / kTile, P);
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
