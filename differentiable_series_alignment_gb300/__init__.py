@@ -7,6 +7,7 @@ Low level (same names as the C entry points, torch tensors for pointers):
 High level, following the usage shown in the SoftDTW-CUDA (PyTorch + Numba)
 README ("Usage", "Fused Mode", "Normalization", "Time Series Barycenters"):
     SoftDTW(gamma=1.0, fused=False, normalize=False)(x, y) -> (B,) losses, differentiable
+    soft_dtw_cost(C, gamma=1.0) -> (B,) losses of a given (B,N,M) cost, differentiable in C
     softdtw_barycenter(sequences, gamma=1.0, max_iter=100, lr=0.1, fused=True) -> (T, D)
 
 PyTorch supplies device memory and streams only; every step of the method runs
@@ -16,15 +17,17 @@ from __future__ import annotations
 
 import torch
 
-from ._lib import (EXTENDED, FUSED, OP_BARYCENTER, OP_FWD_BWD, OP_NORMALIZED, UNFUSED, SdtwError, auto_precision, load,
-                   sdtw_backward, sdtw_barycenter_step, sdtw_debug_set_wait, sdtw_distance, sdtw_forward,
-                   sdtw_last_device_status, sdtw_normalized, sdtw_workspace_bytes, workspace)
+from ._lib import (EXTENDED, FUSED, OP_BARYCENTER, OP_COST, OP_FWD_BWD, OP_NORMALIZED, UNFUSED, SdtwError,
+                   auto_precision, load, sdtw_backward, sdtw_backward_cost, sdtw_barycenter_step, sdtw_debug_set_wait,
+                   sdtw_distance, sdtw_forward, sdtw_forward_cost, sdtw_last_device_status, sdtw_normalized,
+                   sdtw_workspace_bytes, workspace)
 
 __all__ = [
-    "SoftDTW", "softdtw_barycenter", "SdtwError", "load", "workspace",
+    "SoftDTW", "soft_dtw_cost", "softdtw_barycenter", "SdtwError", "load", "workspace",
     "sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
-    "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_debug_set_wait",
-    "UNFUSED", "FUSED", "EXTENDED", "OP_FWD_BWD", "OP_NORMALIZED", "OP_BARYCENTER", "auto_precision",
+    "sdtw_barycenter_step", "sdtw_forward_cost", "sdtw_backward_cost", "sdtw_last_device_status",
+    "sdtw_debug_set_wait", "UNFUSED", "FUSED", "EXTENDED", "OP_FWD_BWD", "OP_NORMALIZED", "OP_BARYCENTER",
+    "OP_COST", "auto_precision",
 ]
 
 
@@ -87,6 +90,42 @@ class _NormalizedFn(torch.autograd.Function):
         g = grad.detach().to(torch.float32).contiguous()
         sdtw_normalized(xc, yc, ctx.gamma, ctx.mode, loss, g, gx, gy, ws)
         return gx, gy, None, None
+
+
+class _CostFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, C, gamma, mode):
+        Cc = C.detach().to(torch.float32).contiguous()
+        if Cc.dim() != 3 or not Cc.is_cuda:
+            raise ValueError("C must be a (B, N, M) CUDA tensor")
+        B, N, M = Cc.shape
+        ws = workspace(OP_COST, B, N, M, 1, mode, Cc.device)
+        loss = torch.empty(B, dtype=torch.float32, device=Cc.device)
+        sdtw_forward_cost(Cc, gamma, mode, loss, ws)
+        ctx.save_for_backward(Cc, ws)
+        ctx.gamma, ctx.mode, ctx.dtype = gamma, mode, C.dtype
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad):
+        Cc, ws = ctx.saved_tensors
+        gC = torch.empty_like(Cc)
+        sdtw_backward_cost(Cc, ctx.gamma, ctx.mode, grad.detach().to(torch.float32).contiguous(), gC, ws)
+        return gC.to(ctx.dtype), None, None
+
+
+def soft_dtw_cost(C: torch.Tensor, gamma: float = 1.0, extended: bool | None = None) -> torch.Tensor:
+    """Soft-DTW losses (B,) of a caller-supplied cost tensor C (B,N,M), for any
+    discrepancy; differentiable in C (dL/dC = grad_loss * alignment matrix).
+    extended=None picks the double-float DP state for small gamma or long
+    sequences; True/False forces it."""
+    if not (gamma > 0):
+        raise ValueError("gamma must be > 0")
+    if extended is None:
+        mode = auto_precision(gamma, C.shape[1], C.shape[2])
+    else:
+        mode = EXTENDED if extended else 0
+    return _CostFn.apply(C, float(gamma), mode)
 
 
 class SoftDTW:

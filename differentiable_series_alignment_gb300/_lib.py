@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libsdtw.so")
 
 UNFUSED, FUSED = 0, 1
 EXTENDED = 2   # precision flag OR-ed into the mode (double-float forward state)
-OP_FWD_BWD, OP_NORMALIZED, OP_BARYCENTER = 0, 1, 2
+OP_FWD_BWD, OP_NORMALIZED, OP_BARYCENTER, OP_COST = 0, 1, 2, 3
 
 STATUS_NAMES = {
     0: "SDTW_OK", 1: "SDTW_ERR_ARG", 2: "SDTW_ERR_GAMMA", 3: "SDTW_ERR_EMPTY", 4: "SDTW_ERR_SHAPE",
@@ -27,7 +27,7 @@ STATUS_NAMES = {
 # Every symbol include/sdtw.h declares.
 EXPORTS = ("sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
            "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_status_string", "sdtw_debug_set_wait",
-           "sdtw_forward_noalloc")
+           "sdtw_forward_noalloc", "sdtw_forward_cost", "sdtw_backward_cost")
 
 
 class SdtwError(RuntimeError):
@@ -68,6 +68,10 @@ def load(path: str = LIB_PATH):
         lib.sdtw_status_string.restype = ctypes.c_char_p
         lib.sdtw_forward_noalloc.argtypes = [vp, vp, i, i, i, i, f, i, vp, vp]
         lib.sdtw_forward_noalloc.restype = i
+        lib.sdtw_forward_cost.argtypes = [vp, i, i, i, f, i, vp, vp, sz, vp]
+        lib.sdtw_forward_cost.restype = i
+        lib.sdtw_backward_cost.argtypes = [vp, i, i, i, f, i, vp, vp, vp, sz, vp]
+        lib.sdtw_backward_cost.restype = i
         lib.sdtw_debug_set_wait.argtypes = [ctypes.c_double, i]
         lib.sdtw_debug_set_wait.restype = None
         _lib = lib
@@ -170,6 +174,19 @@ def sdtw_backward(x, y, gamma, mode, grad_loss, grad_x, grad_y, ws, stream=None)
     _check(load().sdtw_backward(_f32(x, "x"), _f32(y, "y"), B, N, M, D, float(gamma), _mode(mode),
                                 _f32(grad_loss, "grad_loss"), _f32(grad_x, "grad_x"), _f32(grad_y, "grad_y"),
                                 _ptr(ws), ws.numel(), _stream(stream)), "sdtw_backward")
+
+
+def sdtw_forward_cost(C, gamma, mode, loss, ws, stream=None):
+    B, N, M = C.shape
+    _check(load().sdtw_forward_cost(_f32(C, "C"), B, N, M, float(gamma), _mode(mode), _f32(loss, "loss"), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "sdtw_forward_cost")
+
+
+def sdtw_backward_cost(C, gamma, mode, grad_loss, grad_C, ws, stream=None):
+    B, N, M = C.shape
+    _check(load().sdtw_backward_cost(_f32(C, "C"), B, N, M, float(gamma), _mode(mode),
+                                     _f32(grad_loss, "grad_loss"), _f32(grad_C, "grad_C"), _ptr(ws), ws.numel(),
+                                     _stream(stream)), "sdtw_backward_cost")
 
 
 def sdtw_normalized(x, y, gamma, mode, loss, grad_loss, grad_x, grad_y, ws, stream=None):

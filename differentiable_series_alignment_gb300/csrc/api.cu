@@ -36,10 +36,12 @@ struct Layout {
 
 bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
 {
-    if (op < SDTW_OP_FWD_BWD || op > SDTW_OP_BARYCENTER) return false;
+    if (op < SDTW_OP_FWD_BWD || op > SDTW_OP_COST) return false;
+    if (op == SDTW_OP_COST) D = 1;  // no features: the cost is given
     if (B < 1 || N < 1 || M < 1 || D < 1) return false;
     if (mode & ~3) return false;
     const bool fused = (mode & SDTW_FUSED) != 0, ext = (mode & SDTW_EXTENDED) != 0;
+    if (op == SDTW_OP_COST && fused) return false;
     const int P = (op == SDTW_OP_NORMALIZED) ? 3 * B : B;
     if (op == SDTW_OP_NORMALIZED) M = N;
     const int NB = (N + 31) / 32;
@@ -59,11 +61,12 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->dsk = o; if (!fused) o = align_up(o + (ext ? sizeof(float2) : sizeof(float)) * slots);
     L->gparts = o; if (op == SDTW_OP_BARYCENTER) o = align_up(o + sizeof(float) * (size_t)P * N * D);
     // gradient operand images (one batch of B problems at a time): [Y | 1] and [X | 1]
-    L->bimg = o; if (!ext) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, M, D));
-    L->bimg2 = o; if (!ext) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, N, D));
+    const bool xy = op != SDTW_OP_COST;  // the path has x and y (and input gradients)
+    L->bimg = o; if (!ext && xy) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, M, D));
+    L->bimg2 = o; if (!ext && xy) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, N, D));
     // operand images and norms of the tensor-core costs (fp32 modes, D <= 64): the
     // unfused cost tensor and the fused forward's cost tiles
-    L->tc_cost = !ext && D <= 64;
+    L->tc_cost = !ext && D <= 64 && xy;
     L->ximg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, N, D));
     L->yimg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, M, D));
     L->xnorm = o; if (L->tc_cost) o = align_up(o + snorm_bytes(P, N));
@@ -175,8 +178,9 @@ WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamm
     } while (0)
 
 // Forward over L.P problems; per-problem losses to `loss_out` (device).
+// cost: when not null, the caller's (P,N,M) cost tensor replaces the distance step.
 sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gamma, int mode, float* loss_out,
-                        cudaStream_t st)
+                        cudaStream_t st, const float* cost = nullptr)
 {
     const bool fused = (mode & SDTW_FUSED) != 0, ext = (mode & SDTW_EXTENDED) != 0;
     WaveParams q = wave_params(pr, L, ws, gamma, fused, ext, false);
@@ -190,7 +194,8 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
     if (q.S > 1)  // strip boundary slots start untagged
         SDTW_CUDA(cudaMemsetAsync(q.edge_f, 0, (ext ? 2 : 1) * sizeof(Slot) * (size_t)L.P * q.S * L.M, st));
     if (ext) {
-        if (!fused) SDTW_CUDA(launch_dist_skewed_x(pr, L.P, L.N, L.M, L.D, at<float2>(ws, L.dsk), st));
+        if (cost) SDTW_CUDA(launch_skew_cost(cost, L.P, L.N, L.M, true, at<float>(ws, L.dsk), st));
+        else if (!fused) SDTW_CUDA(launch_dist_skewed_x(pr, L.P, L.N, L.M, L.D, at<float2>(ws, L.dsk), st));
         q.loss = loss_out;
         q.skip_publish = g_skip_publish;
         g_skip_publish = 0;
@@ -200,7 +205,9 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
     if (tc)
         SDTW_CUDA(launch_simg(pr, L.P, L.N, L.M, L.D, at<float>(ws, L.ximg), at<float>(ws, L.yimg),
                               at<float>(ws, L.xnorm), at<float>(ws, L.ynorm), st));
-    if (!fused) {
+    if (cost) {
+        SDTW_CUDA(launch_skew_cost(cost, L.P, L.N, L.M, false, at<float>(ws, L.dsk), st));
+    } else if (!fused) {
         if (tc) {
             SDTW_CUDA(launch_dist_tc(L.P, L.N, L.M, L.D, at<float>(ws, L.ximg), at<float>(ws, L.yimg),
                                      at<float>(ws, L.xnorm), at<float>(ws, L.ynorm), at<float>(ws, L.dsk),
@@ -294,6 +301,16 @@ __global__ void combine_normalized_kernel(const float* l, int B, float* loss)
 {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < B) loss[b] = l[b] - 0.5f * (l[B + b] + l[2 * B + b]);
+}
+
+sdtw_status check_cost(const float* C, int B, int N, int M, float gamma, int mode)
+{
+    if (B < 1 || N < 1 || M < 1) return SDTW_ERR_EMPTY;
+    if (!(gamma > 0.f) || !std::isfinite(gamma)) return SDTW_ERR_GAMMA;
+    if ((mode & ~3) || (mode & SDTW_FUSED)) return SDTW_ERR_ARG;
+    if (!C) return SDTW_ERR_ARG;
+    if (B > 65535 / 3 || N > (1 << 24) || M > (1 << 24)) return SDTW_ERR_TOO_LARGE;
+    return SDTW_OK;
 }
 
 }  // namespace
@@ -443,6 +460,37 @@ sdtw_status sdtw_barycenter_step(float* z, float* m, float* v, int t, const floa
     const double bc2 = 1.0 - std::pow((double)beta2, (double)t);
     SDTW_CUDA(launch_adam(z, m, v, gparts, K, T * D, lr, beta1, beta2, eps, (float)bc1, (float)bc2, losses, loss_out,
                           st));
+    return SDTW_OK;
+}
+
+sdtw_status sdtw_forward_cost(const float* C, int B, int N, int M, float gamma, sdtw_mode mode, float* loss,
+                              void* ws, size_t ws_bytes, void* stream)
+{
+    sdtw_status s = check_cost(C, B, N, M, gamma, (int)mode);
+    if (s != SDTW_OK) return s;
+    if (!loss) return SDTW_ERR_ARG;
+    Layout L;
+    make_layout(SDTW_OP_COST, B, N, M, 1, (int)mode, &L);
+    if ((s = check_ws(ws, ws_bytes, L)) != SDTW_OK) return s;
+    Problems pr{};
+    pr.B = B;
+    return run_forward(pr, L, ws, gamma, (int)mode, loss, static_cast<cudaStream_t>(stream), C);
+}
+
+sdtw_status sdtw_backward_cost(const float* C, int B, int N, int M, float gamma, sdtw_mode mode,
+                               const float* grad_loss, float* grad_C, void* ws, size_t ws_bytes, void* stream)
+{
+    sdtw_status s = check_cost(C, B, N, M, gamma, (int)mode);
+    if (s != SDTW_OK) return s;
+    if (!grad_loss || !grad_C) return SDTW_ERR_ARG;
+    Layout L;
+    make_layout(SDTW_OP_COST, B, N, M, 1, (int)mode, &L);
+    if ((s = check_ws(ws, ws_bytes, L)) != SDTW_OK) return s;
+    Problems pr{};
+    pr.B = B;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((s = run_backward(pr, L, ws, gamma, (int)mode, st)) != SDTW_OK) return s;
+    SDTW_CUDA(launch_unskew_grad(at<float>(ws, L.e), B, N, M, grad_loss, grad_C, st));
     return SDTW_OK;
 }
 

@@ -105,6 +105,12 @@ cudaError_t launch_dist_tc(int P, int N, int M, int D, const float* ximg, const 
 cudaError_t launch_forward_tc(WaveParams q, const float* ximg, const float* yimg, const float* xnorm,
                               const float* ynorm, cudaStream_t st);
 size_t wave_tc_smem(int D);
+
+// Caller-supplied costs (cost.cu): C (P,N,M) row-major into the skewed cost slots
+// (float, or (c, 0) pairs when ext), and grad_C = grad_loss[p] * E back out.
+cudaError_t launch_skew_cost(const float* C, int P, int N, int M, bool ext, float* Dsk, cudaStream_t st);
+cudaError_t launch_unskew_grad(const float* E, int P, int N, int M, const float* grad_loss, float* gC,
+                               cudaStream_t st);
 cudaError_t launch_grad_cols(const GradParams& g, cudaStream_t st);
 
 // Barycenter: grad = (1/K) sum_k gparts[k]; Adam update of z, m, v; mean loss.

@@ -72,6 +72,7 @@ typedef enum {
 #define SDTW_OP_FWD_BWD 0    /* sdtw_forward followed by sdtw_backward           */
 #define SDTW_OP_NORMALIZED 1 /* sdtw_normalized (N == M)                          */
 #define SDTW_OP_BARYCENTER 2 /* sdtw_barycenter_step: B = K sequences, N = T, M = T2 */
+#define SDTW_OP_COST 3       /* sdtw_forward_cost followed by sdtw_backward_cost; D is ignored */
 
 /* Bytes of device workspace needed by `op` for these sizes and mode; 0 when the
  * arguments are invalid. Pure host function, no CUDA call. */
@@ -134,6 +135,23 @@ sdtw_status sdtw_barycenter_step(float* z, float* m, float* v, int t, const floa
  *    of time is not reported (the loss is then undefined). */
 sdtw_status sdtw_forward_noalloc(const float* x, const float* y, int B, int N, int M, int D,
                                  float gamma, sdtw_mode mode, float* loss, void* stream);
+
+/* Soft-DTW on a caller-supplied cost tensor C (B,N,M), row-major: any
+ * discrepancy, not only the squared Euclidean one (the SoftDTW README's `dist=`
+ * argument, "Usage"; Soft-DTW paper, section 2). loss[b] = R_b[N,M] with
+ * R[i,j] = C[b,i,j] + softmin_g(R[i-1,j-1], R[i-1,j], R[i,j-1]).
+ * mode: SDTW_UNFUSED, optionally OR-ed with SDTW_EXTENDED; SDTW_FUSED is
+ * SDTW_ERR_ARG (there is no cost to fuse). Workspace: op SDTW_OP_COST. Leaves the
+ * DP state for sdtw_backward_cost in `ws`. */
+sdtw_status sdtw_forward_cost(const float* C, int B, int N, int M, float gamma, sdtw_mode mode,
+                              float* loss, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward pass of sdtw_forward_cost on the same workspace and arguments:
+ * grad_C[b,i,j] = grad_loss[b] * E_b[i,j] = dL/dC[b,i,j] (B,N,M), row-major,
+ * overwritten. */
+sdtw_status sdtw_backward_cost(const float* C, int B, int N, int M, float gamma, sdtw_mode mode,
+                               const float* grad_loss, float* grad_C, void* ws, size_t ws_bytes,
+                               void* stream);
 
 /* Synchronizes `stream`, then reports (and clears) the device status word kept
  * in `ws`: SDTW_OK, or SDTW_ERR_TIMEOUT when a DP kernel gave up waiting for a

@@ -121,3 +121,26 @@ def test_auto_precision_rule():
     assert L.auto_precision(0.01, 64, 64, 4) == L.EXTENDED      # small gamma
     assert L.auto_precision(1.0, 4096, 8, 4) == L.EXTENDED      # long sequences
     assert L.auto_precision(1.0, 8, 4095, 4) == 0
+
+
+def test_given_cost_entry_points_validate_on_the_host(lib):
+    from differentiable_series_alignment_gb300 import _lib as L
+    # workspace: the DP state of an unfused problem without x/y operand images
+    w = L.sdtw_workspace_bytes(L.OP_COST, 4, 100, 37, 0, L.UNFUSED)
+    slots = 4 * 4 * 80 * 32    # 4 problems x 4 row blocks x T = 37 + 31 rounded up to 16 x 32 lanes
+    assert w >= slots * (8 + 4 + 4)   # (v_left, h_up) pairs, alignment matrix, cost
+    assert L.sdtw_workspace_bytes(L.OP_COST, 4, 100, 37, 7, L.UNFUSED) == w      # D is ignored
+    assert L.sdtw_workspace_bytes(L.OP_COST, 4, 100, 37, 1, L.FUSED) == 0        # nothing to fuse
+    assert L.sdtw_workspace_bytes(L.OP_COST, 4, 100, 37, 1, L.EXTENDED) > w
+    vp = ctypes.c_void_p
+    f = lib.sdtw_forward_cost
+    f.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, vp, vp,
+                  ctypes.c_size_t, vp]
+    f.restype = ctypes.c_int
+    ok = dict(C=vp(0x1000), B=2, N=3, M=4, g=1.0, mode=0, loss=vp(0x2000), ws=vp(0x100000), n=1 << 40)
+    call = lambda **kw: f(*[dict(ok, **kw)[k] for k in ("C", "B", "N", "M", "g", "mode", "loss", "ws", "n")], None)
+    assert call(B=0) == 3 and call(M=0) == 3          # SDTW_ERR_EMPTY
+    assert call(g=0.0) == 2 and call(g=float("nan")) == 2
+    assert call(mode=L.FUSED) == 1 and call(mode=4) == 1
+    assert call(C=None) == 1 and call(loss=None) == 1
+    assert call(ws=None) == 5 and call(ws=vp(0x100001)) == 5 and call(n=16) == 5

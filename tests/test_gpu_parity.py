@@ -310,6 +310,59 @@ def test_barycenter_steps_match_oracle(mname, mode):
         assert_close(z.cpu().numpy() - zc, zo - zc, 2e-3, 1e-6, f"step {t} update")
 
 
+# --------------------------------------------------------------------------- caller-supplied costs
+
+def _cost_batch(kind, B, N, M, seed):
+    g = np.random.default_rng(seed)
+    if kind == "l1":      # |x - y| summed over 3 features: a non-Euclidean, non-negative cost
+        x = g.standard_normal((B, N, 3))
+        y = g.standard_normal((B, M, 3))
+        return np.abs(x[:, :, None, :] - y[:, None, :, :]).sum(-1).astype(np.float32)
+    return (2.0 * g.standard_normal((B, N, M))).astype(np.float32)   # signed costs
+
+
+@pytest.mark.parametrize("mname,mode,weights", [("fp32", 0, WEIGHTS), ("extended", 2, WEIGHTS_O1)])
+@pytest.mark.parametrize("kind", ["l1", "signed"])
+@pytest.mark.parametrize("N,M", [(1, 1), (1, 9), (7, 1), (33, 31), (100, 37), (129, 130)])
+def test_given_cost_matches_oracle(mname, mode, weights, kind, N, M):
+    L = _lib()
+    B, gamma = 3, 0.8
+    C = _cost_batch(kind, B, N, M, N * 1000 + M)
+    Ct = torch.from_numpy(C).cuda()
+    ws = L.workspace(L.OP_COST, B, N, M, 1, mode)
+    loss = torch.empty(B, device="cuda")
+    gC = torch.empty_like(Ct)
+    g = torch.tensor(weights, dtype=torch.float32, device="cuda")
+    L.sdtw_forward_cost(Ct, gamma, mode, loss, ws)
+    L.sdtw_backward_cost(Ct, gamma, mode, g, gC, ws)
+    assert L.sdtw_last_device_status(ws) == 0
+    ol, ogC = [], []
+    for b in range(B):
+        R = oracle.forward_from_cost(C[b], gamma)
+        ol.append(R[N, M])
+        ogC.append(weights[b] * oracle.backward_from_cost(C[b], R, gamma))
+    assert_close(loss.cpu().numpy(), np.array(ol), LOSS_RTOL, 1e-6, f"cost {kind} {N}x{M} {mname} loss")
+    assert_close(gC.cpu().numpy(), np.stack(ogC), GRAD_RTOL, GRAD_ATOL, f"cost {kind} {N}x{M} {mname} grad_C")
+
+
+def test_given_squared_euclidean_cost_reproduces_softdtw():
+    # the cost path fed the squared Euclidean cost equals the x/y path, values and
+    # (through the chain rule dC/dx) gradients, via the autograd wrappers
+    from differentiable_series_alignment_gb300 import SoftDTW, soft_dtw_cost
+    x, y = synth.iid_normal_pair(4, 70, 61, 5, 97)
+    xt = torch.from_numpy(x).cuda().requires_grad_(True)
+    yt = torch.from_numpy(y).cuda().requires_grad_(True)
+    a = SoftDTW(gamma=0.9)(xt, yt)
+    a.mean().backward()
+    gxa = xt.grad.detach().clone()
+    xt.grad = None
+    C = ((xt[:, :, None, :] - yt[:, None, :, :]) ** 2).sum(-1)   # test-side cost, plain torch
+    b = soft_dtw_cost(C, gamma=0.9)
+    b.mean().backward()
+    assert_close(b.detach().cpu().numpy(), a.detach().cpu().numpy(), LOSS_RTOL, 0.0, "cost vs x/y loss")
+    assert_close(xt.grad.cpu().numpy(), gxa.cpu().numpy(), GRAD_RTOL, GRAD_ATOL, "cost vs x/y grad_x")
+
+
 # --------------------------------------------------------------------------- device status
 
 def test_withheld_ready_flag_times_out_and_recovers():
