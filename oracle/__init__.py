@@ -51,7 +51,7 @@ def _load():
             lib.oracle_batch.restype = i
             lib.oracle_normalized.argtypes = [_dp, _dp, i, i, i, d, _dp, _dp, _dp, _dp, i]
             lib.oracle_normalized.restype = i
-            lib.oracle_barycenter_step.argtypes = [_dp, _dp, _dp, i, _dp, i, i, i, i, d, d, d, d,
+            lib.oracle_barycenter_step.argtypes = [_dp, _dp, _dp, i, _dp, i, i, i, i, d, d, d, d, d,
                                                    d, _dp, _dp, i]
             lib.oracle_barycenter_step.restype = i
             lib.oracle_forward.argtypes = [_dp, i, i, d, _dp]
@@ -149,8 +149,11 @@ def normalized(x, y, gamma, grad_loss=None, nthreads=0):
     return loss, gx, gy
 
 
-def barycenter_step(z, m, v, t, X, gamma, lr=0.1, beta1=0.9, beta2=0.999, eps=1e-8, nthreads=0):
-    """One Adam step; returns (z, m, v, loss_at_incoming_z, grad) as new arrays."""
+def barycenter_step(z, m, v, t, X, gamma, lr=0.1, beta1=0.9, beta2=0.999, eps=1e-8, nthreads=0,
+                    max_grad_norm=0.0):
+    """One Adam step; returns (z, m, v, loss_at_incoming_z, grad) as new arrays.
+    max_grad_norm > 0 clips the gradient by its global L2 norm before Adam; the
+    returned grad is the unclipped one."""
     z, m, v, X = _f64(z).copy(), _f64(m).copy(), _f64(v).copy(), _f64(X)
     T, D = z.shape
     K, T2, _ = X.shape
@@ -158,7 +161,8 @@ def barycenter_step(z, m, v, t, X, gamma, lr=0.1, beta1=0.9, beta2=0.999, eps=1e
     grad = np.empty_like(z)
     rc = _load().oracle_barycenter_step(_ptr(z), _ptr(m), _ptr(v), int(t), _ptr(X), K, T, T2, D,
                                         float(gamma), float(lr), float(beta1), float(beta2),
-                                        float(eps), ctypes.byref(loss), _ptr(grad), int(nthreads))
+                                        float(eps), float(max_grad_norm), ctypes.byref(loss), _ptr(grad),
+                                        int(nthreads))
     if rc != 0:
         raise ValueError("oracle_barycenter_step: bad argument or allocation failure")
     return z, m, v, loss.value, grad

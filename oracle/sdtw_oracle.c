@@ -255,9 +255,13 @@ int oracle_normalized(const double* x, const double* y, int B, int N, int D, dou
 /* One Adam step of the barycenter z (T,D) against X (K,T2,D). z, m, v updated
  * in place; t is the 1-based step number. loss_out (nullable) receives the
  * objective at the incoming z. grad_out (nullable, (T,D)) receives its gradient. */
+/* One Adam step of the barycenter. max_grad_norm > 0 clips the gradient by its
+ * global L2 norm first (SoftDTW README, "Time Series Barycenters": gradient
+ * clipping; scale min(1, max_grad_norm / ||g||)); grad_out receives the raw,
+ * unclipped gradient. */
 int oracle_barycenter_step(double* z, double* m, double* v, int t, const double* X, int K,
                            int T, int T2, int D, double gamma, double lr, double b1, double b2,
-                           double eps, double* loss_out, double* grad_out, int nthreads)
+                           double eps, double max_grad_norm, double* loss_out, double* grad_out, int nthreads)
 {
     if (K < 1 || T < 1 || T2 < 1 || D < 1 || t < 1) return -1;
     const size_t n = (size_t)T * D;
@@ -276,10 +280,18 @@ int oracle_barycenter_step(double* z, double* m, double* v, int t, const double*
         for (int k = 0; k < K; ++k) L += ls[k];
         if (loss_out) *loss_out = L / K;
         const double c1 = 1.0 - pow(b1, t), c2 = 1.0 - pow(b2, t);
+        double nrm2 = 0.0;
         for (size_t q = 0; q < n; ++q) {
             double g = 0.0;
             for (int k = 0; k < K; ++k) g += gz[(size_t)k * n + q];
-            if (grad_out) grad_out[q] = g;
+            gz[q] = g;  /* part 0 now holds the summed gradient */
+            nrm2 += g * g;
+        }
+        const double nrm = sqrt(nrm2);
+        const double scale = (max_grad_norm > 0.0 && nrm > max_grad_norm) ? max_grad_norm / nrm : 1.0;
+        for (size_t q = 0; q < n; ++q) {
+            const double g = gz[q] * scale;
+            if (grad_out) grad_out[q] = gz[q];
             m[q] = b1 * m[q] + (1.0 - b1) * g;
             v[q] = b2 * v[q] + (1.0 - b2) * g * g;
             z[q] -= lr * (m[q] / c1) / (sqrt(v[q] / c2) + eps);

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
+from differentiable_series_alignment_gb300 import synth
 
 RNG = np.random.default_rng(1234)
 
@@ -381,3 +382,24 @@ def test_batch_equals_single_per_problem():
         assert loss[b] == s["loss"]
         np.testing.assert_array_equal(gx[b], s["gx"])
         np.testing.assert_array_equal(gy[b], s["gy"])
+
+
+def test_barycenter_gradient_clipping_pins():
+    """Clipping by the global L2 norm: a bound at or above ||g|| changes nothing,
+    and below it the first step's moments carry exactly the clipped norm
+    (m = (1-b1) g c/||g||, v = (1-b2) (g c/||g||)^2), while the first Adam step
+    itself is scale-free."""
+    X = synth.block_waves(4, 24, 2, 4)
+    z = X.astype(np.float64).mean(axis=0)
+    zero = np.zeros_like(z)
+    z1, m1, v1, l1, g = oracle.barycenter_step(z, zero, zero, 1, X, 1.0)
+    nrm = float(np.linalg.norm(g))
+    assert nrm > 0
+    za, ma, va, la, ga = oracle.barycenter_step(z, zero, zero, 1, X, 1.0, max_grad_norm=nrm * 1.0001)
+    assert np.array_equal(za, z1) and np.array_equal(ma, m1) and np.array_equal(va, v1) and la == l1
+    c = 0.25 * nrm
+    zc, mc, vc, lc, gc = oracle.barycenter_step(z, zero, zero, 1, X, 1.0, max_grad_norm=c)
+    assert np.array_equal(gc, g)                                  # the raw gradient is returned
+    assert np.linalg.norm(mc) == pytest.approx(0.1 * c, rel=1e-12)
+    assert vc.sum() == pytest.approx(0.001 * c * c, rel=1e-12)
+    np.testing.assert_allclose(zc, z1, rtol=0, atol=1e-6)         # step 1 moves lr*sign(g) either way
