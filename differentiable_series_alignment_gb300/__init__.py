@@ -15,17 +15,21 @@ in libsdtw.so's kernels.
 """
 from __future__ import annotations
 
+import math
+
 import torch
 
 from ._lib import (EXTENDED, FUSED, OP_BARYCENTER, OP_COST, OP_FWD_BWD, OP_NORMALIZED, UNFUSED, SdtwError,
-                   auto_precision, load, sdtw_backward, sdtw_backward_cost, sdtw_barycenter_step, sdtw_debug_set_wait,
+                   auto_precision, load, sdtw_backward, sdtw_backward_cost, sdtw_barycenter_step,
+                   sdtw_barycenter_step_clipped, sdtw_debug_set_wait,
                    sdtw_distance, sdtw_forward, sdtw_forward_cost, sdtw_last_device_status, sdtw_normalized,
                    sdtw_workspace_bytes, workspace)
 
 __all__ = [
     "SoftDTW", "soft_dtw_cost", "softdtw_barycenter", "SdtwError", "load", "workspace",
     "sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
-    "sdtw_barycenter_step", "sdtw_forward_cost", "sdtw_backward_cost", "sdtw_last_device_status",
+    "sdtw_barycenter_step", "sdtw_barycenter_step_clipped", "sdtw_forward_cost", "sdtw_backward_cost",
+    "sdtw_last_device_status", "cosine_lr",
     "sdtw_debug_set_wait", "UNFUSED", "FUSED", "EXTENDED", "OP_FWD_BWD", "OP_NORMALIZED", "OP_BARYCENTER",
     "OP_COST", "auto_precision",
 ]
@@ -158,20 +162,53 @@ class SoftDTW:
         return fn.apply(x, y, self.gamma, mode)
 
 
+def cosine_lr(t: int, max_iter: int, lr: float, lr_min: float = 0.0) -> float:
+    """Learning rate of step t (1-based) under cosine annealing from lr at t = 1
+    to lr_min after max_iter steps, without restarts."""
+    return lr_min + 0.5 * (lr - lr_min) * (1.0 + math.cos(math.pi * (t - 1) / max_iter))
+
+
 def softdtw_barycenter(sequences: torch.Tensor, gamma: float = 1.0, max_iter: int = 100, lr: float = 0.1,
                        fused: bool = True, init: torch.Tensor | None = None, beta1: float = 0.9,
-                       beta2: float = 0.999, eps: float = 1e-8, return_losses: bool = False):
+                       beta2: float = 0.999, eps: float = 1e-8, return_losses: bool = False,
+                       lr_schedule: str | None = None, lr_min: float = 0.0, max_grad_norm: float | None = None,
+                       early_stopping: bool = False, tol: float = 1e-4, patience: int = 10, check_every: int = 10):
     """Soft-DTW barycenter of K sequences (K,T,D) by Adam, initialised to their
-    mean (or `init`). Runs `max_iter` calls of sdtw_barycenter_step."""
+    mean (or `init`), one sdtw_barycenter_step per iteration (README, "Time Series
+    Barycenters"). Optional, as the README lists them (their parameters are not
+    given there): lr_schedule="cosine" anneals the rate to lr_min over max_iter
+    steps; max_grad_norm clips the gradient by its global L2 norm; early_stopping
+    stops once the loss has not improved by more than tol * |best| for `patience`
+    steps (losses are read back every `check_every` steps). Returns z, or
+    (z, losses of the steps run) with return_losses."""
     X = _prep(sequences, "sequences")
     K, T2, D = X.shape
     z = (X.mean(dim=0) if init is None else init.detach().to(torch.float32)).contiguous().clone()
     T = z.shape[0]
     m = torch.zeros_like(z)
     v = torch.zeros_like(z)
+    if lr_schedule not in (None, "cosine"):
+        raise ValueError("lr_schedule must be None or 'cosine'")
     mode = (FUSED if fused else UNFUSED) | auto_precision(gamma, T, T2, D)
     ws = workspace(OP_BARYCENTER, K, T, T2, D, mode, X.device)
     losses = torch.empty(max_iter, dtype=torch.float32, device=X.device)
+    clip = float(max_grad_norm) if max_grad_norm else 0.0
+    best, stale, ran = math.inf, 0, 0
     for t in range(1, max_iter + 1):
-        sdtw_barycenter_step(z, m, v, t, X, gamma, lr, beta1, beta2, eps, mode, losses[t - 1:t], ws)
+        lr_t = cosine_lr(t, max_iter, lr, lr_min) if lr_schedule == "cosine" else lr
+        if clip > 0.0:
+            sdtw_barycenter_step_clipped(z, m, v, t, X, gamma, lr_t, beta1, beta2, eps, clip, mode,
+                                         losses[t - 1:t], ws)
+        else:
+            sdtw_barycenter_step(z, m, v, t, X, gamma, lr_t, beta1, beta2, eps, mode, losses[t - 1:t], ws)
+        ran = t
+        if early_stopping and (t % check_every == 0 or t == max_iter):
+            for lv in losses[t - (t - 1) % check_every - 1:t].tolist():
+                if lv < best - tol * abs(best) or best == math.inf:
+                    best, stale = min(best, lv), 0
+                else:
+                    stale += 1
+            if stale >= patience:
+                break
+    losses = losses[:ran]
     return (z, losses) if return_losses else z

@@ -27,7 +27,7 @@ STATUS_NAMES = {
 # Every symbol include/sdtw.h declares.
 EXPORTS = ("sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
            "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_status_string", "sdtw_debug_set_wait",
-           "sdtw_forward_noalloc", "sdtw_forward_cost", "sdtw_backward_cost")
+           "sdtw_forward_noalloc", "sdtw_forward_cost", "sdtw_backward_cost", "sdtw_barycenter_step_clipped")
 
 
 class SdtwError(RuntimeError):
@@ -68,6 +68,9 @@ def load(path: str = LIB_PATH):
         lib.sdtw_status_string.restype = ctypes.c_char_p
         lib.sdtw_forward_noalloc.argtypes = [vp, vp, i, i, i, i, f, i, vp, vp]
         lib.sdtw_forward_noalloc.restype = i
+        lib.sdtw_barycenter_step_clipped.argtypes = [vp, vp, vp, i, vp, i, i, i, i, f, f, f, f, f, f, i, vp, vp,
+                                                     sz, vp]
+        lib.sdtw_barycenter_step_clipped.restype = i
         lib.sdtw_forward_cost.argtypes = [vp, i, i, i, f, i, vp, vp, sz, vp]
         lib.sdtw_forward_cost.restype = i
         lib.sdtw_backward_cost.argtypes = [vp, i, i, i, f, i, vp, vp, vp, sz, vp]
@@ -174,6 +177,17 @@ def sdtw_backward(x, y, gamma, mode, grad_loss, grad_x, grad_y, ws, stream=None)
     _check(load().sdtw_backward(_f32(x, "x"), _f32(y, "y"), B, N, M, D, float(gamma), _mode(mode),
                                 _f32(grad_loss, "grad_loss"), _f32(grad_x, "grad_x"), _f32(grad_y, "grad_y"),
                                 _ptr(ws), ws.numel(), _stream(stream)), "sdtw_backward")
+
+
+def sdtw_barycenter_step_clipped(z, m, v, t, X, gamma, lr, beta1, beta2, eps, max_grad_norm, mode, loss_out, ws,
+                                 stream=None):
+    T, D = z.shape
+    K, T2, _ = X.shape
+    _check(load().sdtw_barycenter_step_clipped(_f32(z, "z"), _f32(m, "m"), _f32(v, "v"), int(t), _f32(X, "X"), K, T,
+                                               T2, D, float(gamma), float(lr), float(beta1), float(beta2), float(eps),
+                                               float(max_grad_norm), _mode(mode), _f32(loss_out, "loss_out"),
+                                               _ptr(ws), ws.numel(), _stream(stream)),
+           "sdtw_barycenter_step_clipped")
 
 
 def sdtw_forward_cost(C, gamma, mode, loss, ws, stream=None):

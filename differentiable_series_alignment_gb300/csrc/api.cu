@@ -28,7 +28,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 // Workspace layout. The status word sits at offset 0 for every op.
 struct Layout {
     size_t status, ctrl_f, ctrl_f_bytes, ctrl_b, ctrl_b_bytes;
-    size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, bimg, bimg2, total;
+    size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, gnorm, bimg, bimg2, total;
     size_t ximg, yimg, xnorm, ynorm;  // tensor-core cost operands (tc_cost)
     bool tc_cost;
     int P, N, M, D, NB;
@@ -60,6 +60,7 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->e = o; o = align_up(o + sizeof(float) * slots);
     L->dsk = o; if (!fused) o = align_up(o + (ext ? sizeof(float2) : sizeof(float)) * slots);
     L->gparts = o; if (op == SDTW_OP_BARYCENTER) o = align_up(o + sizeof(float) * (size_t)P * N * D);
+    L->gnorm = o; if (op == SDTW_OP_BARYCENTER) o = align_up(o + sizeof(float) * (((size_t)N * D + 255) / 256));
     // gradient operand images (one batch of B problems at a time): [Y | 1] and [X | 1]
     const bool xy = op != SDTW_OP_COST;  // the path has x and y (and input gradients)
     L->bimg = o; if (!ext && xy) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, M, D));
@@ -436,10 +437,19 @@ sdtw_status sdtw_barycenter_step(float* z, float* m, float* v, int t, const floa
                                  float gamma, float lr, float beta1, float beta2, float eps, sdtw_mode mode,
                                  float* loss_out, void* ws, size_t ws_bytes, void* stream)
 {
+    return sdtw_barycenter_step_clipped(z, m, v, t, X, K, T, T2, D, gamma, lr, beta1, beta2, eps, 0.f, mode,
+                                        loss_out, ws, ws_bytes, stream);
+}
+
+sdtw_status sdtw_barycenter_step_clipped(float* z, float* m, float* v, int t, const float* X, int K, int T, int T2,
+                                         int D, float gamma, float lr, float beta1, float beta2, float eps,
+                                         float max_grad_norm, sdtw_mode mode, float* loss_out, void* ws,
+                                         size_t ws_bytes, void* stream)
+{
     sdtw_status s = check_common(z, X, K, T, T2, D, gamma, (int)mode);
     if (s != SDTW_OK) return s;
     if (!m || !v || t < 1 || !(lr >= 0.f) || !(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f) ||
-        !(eps >= 0.f))
+        !(eps >= 0.f) || !(max_grad_norm >= 0.f))
         return SDTW_ERR_ARG;
     Layout L;
     make_layout(SDTW_OP_BARYCENTER, K, T, T2, D, (int)mode, &L);
@@ -458,8 +468,12 @@ sdtw_status sdtw_barycenter_step(float* z, float* m, float* v, int t, const floa
         return s;
     const double bc1 = 1.0 - std::pow((double)beta1, (double)t);
     const double bc2 = 1.0 - std::pow((double)beta2, (double)t);
-    SDTW_CUDA(launch_adam(z, m, v, gparts, K, T * D, lr, beta1, beta2, eps, (float)bc1, (float)bc2, losses, loss_out,
-                          st));
+    if (max_grad_norm > 0.f)
+        SDTW_CUDA(launch_adam_clipped(z, m, v, gparts, K, T * D, lr, beta1, beta2, eps, (float)bc1, (float)bc2,
+                                      max_grad_norm, at<float>(ws, L.gnorm), losses, loss_out, st));
+    else
+        SDTW_CUDA(launch_adam(z, m, v, gparts, K, T * D, lr, beta1, beta2, eps, (float)bc1, (float)bc2, losses,
+                              loss_out, st));
     return SDTW_OK;
 }
 

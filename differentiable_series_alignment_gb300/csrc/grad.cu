@@ -172,7 +172,74 @@ __global__ void adam_kernel(float* __restrict__ z, float* __restrict__ m, float*
     z[e] -= lr * (mm / bc1) / (sqrtf(vv / bc2) + eps);
 }
 
+// Gradient clipping (by global L2 norm) for the barycenter step, in two launches:
+// gsum_kernel sums the K parts of each element into part 0 (k order as in
+// adam_kernel) and writes one partial sum of squares per block (fixed tree order);
+// adam_clip_kernel adds the partials in block order, scales the gradient by
+// min(1, max_norm / ||g||) and applies Adam. grid ceil(n/256), block 256.
+__global__ void __launch_bounds__(256) gsum_kernel(float* __restrict__ gparts, int K, int n,
+                                                   float* __restrict__ partials)
+{
+    __shared__ float red[256];
+    const int e = blockIdx.x * 256 + threadIdx.x;
+    float g = 0.f;
+    if (e < n) {
+        for (int k = 0; k < K; ++k) g += gparts[(size_t)k * n + e];
+        gparts[e] = g;
+    }
+    red[threadIdx.x] = g * g;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) partials[blockIdx.x] = red[0];
+}
+
+__global__ void __launch_bounds__(256) adam_clip_kernel(float* __restrict__ z, float* __restrict__ m,
+                                                        float* __restrict__ v, const float* __restrict__ g, int n,
+                                                        float lr, float b1, float b2, float eps, float bc1, float bc2,
+                                                        const float* __restrict__ partials, int nparts,
+                                                        float max_norm, int K, const float* __restrict__ losses,
+                                                        float* __restrict__ loss_out)
+{
+    __shared__ float s_scale;
+    if (threadIdx.x == 0) {
+        double s2 = 0.0;
+        for (int b = 0; b < nparts; ++b) s2 += partials[b];
+        const float nrm = (float)sqrt(s2);
+        s_scale = (max_norm > 0.f && nrm > max_norm) ? max_norm / nrm : 1.f;
+        if (blockIdx.x == 0 && loss_out) {
+            double l = 0.0;
+            for (int k = 0; k < K; ++k) l += losses[k];
+            *loss_out = (float)(l / K);
+        }
+    }
+    __syncthreads();
+    const int e = blockIdx.x * 256 + threadIdx.x;
+    if (e >= n) return;
+    const float gg = g[e] * s_scale;
+    const float mm = b1 * m[e] + (1.f - b1) * gg;
+    const float vv = b2 * v[e] + (1.f - b2) * gg * gg;
+    m[e] = mm;
+    v[e] = vv;
+    z[e] -= lr * (mm / bc1) / (sqrtf(vv / bc2) + eps);
+}
+
 }  // namespace
+
+cudaError_t launch_adam_clipped(float* z, float* m, float* v, float* gparts, int K, int n, float lr, float beta1,
+                                float beta2, float eps, float bc1, float bc2, float max_norm, float* partials,
+                                const float* losses, float* loss_out, cudaStream_t st)
+{
+    const int blocks = (n + 255) / 256;
+    gsum_kernel<<<blocks, 256, 0, st>>>(gparts, K, n, partials);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    adam_clip_kernel<<<blocks, 256, 0, st>>>(z, m, v, gparts, n, lr, beta1, beta2, eps, bc1, bc2, partials, blocks,
+                                             max_norm, K, losses, loss_out);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_grad_rows(const GradParams& g, cudaStream_t st)
 {

@@ -108,6 +108,12 @@ size_t wave_tc_smem(int D);
 
 // Caller-supplied costs (cost.cu): C (P,N,M) row-major into the skewed cost slots
 // (float, or (c, 0) pairs when ext), and grad_C = grad_loss[p] * E back out.
+// Barycenter Adam step with the gradient clipped by its global L2 norm
+// (max_norm > 0); partials: ceil(n/256) floats of scratch.
+cudaError_t launch_adam_clipped(float* z, float* m, float* v, float* gparts, int K, int n, float lr, float beta1,
+                                float beta2, float eps, float bc1, float bc2, float max_norm, float* partials,
+                                const float* losses, float* loss_out, cudaStream_t st);
+
 cudaError_t launch_skew_cost(const float* C, int P, int N, int M, bool ext, float* Dsk, cudaStream_t st);
 cudaError_t launch_unskew_grad(const float* E, int P, int N, int M, const float* grad_loss, float* gC,
                                cudaStream_t st);

@@ -115,6 +115,16 @@ sdtw_status sdtw_barycenter_step(float* z, float* m, float* v, int t, const floa
                                  float eps, sdtw_mode mode, float* loss_out, void* ws,
                                  size_t ws_bytes, void* stream);
 
+/* sdtw_barycenter_step with the gradient clipped by its global L2 norm first
+ * (README, "Time Series Barycenters": gradient clipping for stability; the page
+ * gives no rule, the one adopted is g <- g * min(1, max_grad_norm / ||g||)).
+ * max_grad_norm = 0 is the unclipped step; negative or NaN is SDTW_ERR_ARG.
+ * Same workspace (SDTW_OP_BARYCENTER). */
+sdtw_status sdtw_barycenter_step_clipped(float* z, float* m, float* v, int t, const float* X, int K, int T,
+                                         int T2, int D, float gamma, float lr, float beta1, float beta2,
+                                         float eps, float max_grad_norm, sdtw_mode mode, float* loss_out,
+                                         void* ws, size_t ws_bytes, void* stream);
+
 /* Forward pass that allocates nothing and takes no workspace. No page of the
  * method has a counterpart: it exists for callers that cannot allocate device
  * memory -- a host program with no device allocator of its own (no PyTorch, no

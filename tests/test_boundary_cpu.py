@@ -144,3 +144,11 @@ def test_given_cost_entry_points_validate_on_the_host(lib):
     assert call(mode=L.FUSED) == 1 and call(mode=4) == 1
     assert call(C=None) == 1 and call(loss=None) == 1
     assert call(ws=None) == 5 and call(ws=vp(0x100001)) == 5 and call(n=16) == 5
+
+
+def test_cosine_schedule_values():
+    from differentiable_series_alignment_gb300 import cosine_lr
+    assert cosine_lr(1, 100, 0.1) == 0.1                                      # starts at lr
+    assert cosine_lr(51, 100, 0.1, 0.0) == pytest.approx(0.05)                # halfway: the mean
+    assert cosine_lr(101, 100, 0.1, 0.01) == pytest.approx(0.01)              # ends at lr_min
+    assert all(cosine_lr(t, 100, 0.1) >= cosine_lr(t + 1, 100, 0.1) for t in range(1, 100))

@@ -363,6 +363,44 @@ def test_given_squared_euclidean_cost_reproduces_softdtw():
     assert_close(xt.grad.cpu().numpy(), gxa.cpu().numpy(), GRAD_RTOL, GRAD_ATOL, "cost vs x/y grad_x")
 
 
+@pytest.mark.parametrize("mname,mode", MODES)
+def test_clipped_barycenter_steps_match_oracle(mname, mode):
+    # a bound well below ||g|| so the clipping acts on every step
+    L = _lib()
+    X = synth.block_waves(8, 96, 3, 5)
+    z0 = X.astype(np.float64).mean(axis=0).astype(np.float32)
+    Xt = torch.from_numpy(X).cuda()
+    z = torch.from_numpy(z0.copy()).cuda()
+    m, v = torch.zeros_like(z), torch.zeros_like(z)
+    ws = L.workspace(L.OP_BARYCENTER, 8, 96, 96, 3, mode)
+    lo = torch.empty(1, device="cuda")
+    _, _, _, _, g0 = oracle.barycenter_step(z0, np.zeros_like(z0), np.zeros_like(z0), 1, X, 1.0)
+    clip = 0.3 * float(np.linalg.norm(g0))
+    for t in (1, 2, 3):
+        zc, mc, vc = z.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
+        zo, mo, vo, lref, _ = oracle.barycenter_step(zc, mc, vc, t, X, 1.0, lr=0.1, max_grad_norm=clip)
+        L.sdtw_barycenter_step_clipped(z, m, v, t, Xt, 1.0, 0.1, 0.9, 0.999, 1e-8, clip, mode, lo, ws)
+        assert L.sdtw_last_device_status(ws) == 0
+        assert_close(lo.cpu().numpy(), [lref], LOSS_RTOL, 0.0, f"clipped step {t} loss")
+        assert_close(m.cpu().numpy(), mo, GRAD_RTOL, GRAD_ATOL, f"clipped step {t} first moment")
+        assert_close(v.cpu().numpy(), vo, 2e-3, 1e-9, f"clipped step {t} second moment")
+        assert_close(z.cpu().numpy() - zc, zo - zc, 2e-3, 1e-6, f"clipped step {t} update")
+
+
+def test_barycenter_driver_schedule_clipping_and_early_stopping():
+    from differentiable_series_alignment_gb300 import softdtw_barycenter
+    X = torch.from_numpy(synth.block_waves(16, 128, 2, 6)).cuda()
+    z, lo = softdtw_barycenter(X, gamma=1.0, max_iter=400, lr=0.1, lr_schedule="cosine", lr_min=0.001,
+                               max_grad_norm=1.0, early_stopping=True, tol=1e-3, patience=20, check_every=10,
+                               return_losses=True)
+    lo = lo.cpu().numpy()
+    assert np.all(np.isfinite(lo)) and torch.isfinite(z).all()
+    assert len(lo) < 400            # converged and stopped early
+    assert lo[-1] < lo[0]
+    z2, lo2 = softdtw_barycenter(X, gamma=1.0, max_iter=30, lr=0.1, return_losses=True)
+    assert len(lo2) == 30
+
+
 # --------------------------------------------------------------------------- device status
 
 def test_withheld_ready_flag_times_out_and_recovers():
