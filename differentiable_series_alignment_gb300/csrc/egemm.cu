@@ -269,6 +269,14 @@ __global__ void __launch_bounds__(kThreadsTotal, 1)
                 const bool rowok = rb < NB && m0 + rloc < N;
                 const float* rw = ra + quarter * 64 * 32 + lane * 33;   // slot (c + lane), entry lane
                 const uint32_t rowoff = (uint32_t)((rloc >> 3) * 1024 + (rloc & 7) * 128);
+                // all 16 values first: the stage stores could alias the raw buffer for the
+                // compiler, which would otherwise chain every load behind the previous store
+                float vals[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int c = 4 * (half * 4 + (u >> 2)) + (u & 3);
+                    vals[u] = (rowok && k0 + c < M) ? rw[c * 32] : 0.f;
+                }
 #pragma unroll
                 for (int cq = 0; cq < 4; ++cq) {
                     const int kc = half * 4 + cq;
@@ -276,11 +284,7 @@ __global__ void __launch_bounds__(kThreadsTotal, 1)
                     float* h = &hi.x;
                     float* l = &lo.x;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int c = 4 * kc + q;
-                        const float v = (rowok && k0 + c < M) ? rw[c * 32] : 0.f;
-                        split_tf32(v, h[q], l[q]);
-                    }
+                    for (int q = 0; q < 4; ++q) split_tf32(vals[4 * cq + q], h[q], l[q]);
                     const uint32_t o = rowoff + (uint32_t)(((kc ^ rloc) & 7) << 4);
                     *reinterpret_cast<float4*>(A_hi + o) = hi;
                     *reinterpret_cast<float4*>(A_lo + o) = lo;
@@ -292,11 +296,13 @@ __global__ void __launch_bounds__(kThreadsTotal, 1)
                 const bool iok = k0 + lane < N;
                 const float* rp = ra + (warp + lane) * 32 + lane;
                 const uint32_t coff = (uint32_t)(warp * 128 + ((((lane >> 2) ^ warp) & 7) << 4) + (lane & 3) * 4);
+                float vals[kBM / 8];
+#pragma unroll
+                for (int it = 0; it < kBM / 8; ++it) vals[it] = (iok && m0 + warp + 8 * it < M) ? rp[it * 8 * 32] : 0.f;
 #pragma unroll
                 for (int it = 0; it < kBM / 8; ++it) {
-                    const float v = (iok && m0 + warp + 8 * it < M) ? rp[it * 8 * 32] : 0.f;
                     float h, l;
-                    split_tf32(v, h, l);
+                    split_tf32(vals[it], h, l);
                     *reinterpret_cast<float*>(A_hi + coff + it * 1024) = h;
                     *reinterpret_cast<float*>(A_lo + coff + it * 1024) = l;
                 }
