@@ -21,7 +21,7 @@ import torch
 
 from ._lib import (EXTENDED, FUSED, OP_BARYCENTER, OP_COST, OP_FWD_BWD, OP_NORMALIZED, UNFUSED, SdtwError,
                    auto_precision, load, sdtw_backward, sdtw_backward_cost, sdtw_barycenter_step,
-                   sdtw_barycenter_step_clipped, sdtw_debug_set_wait,
+                   sdtw_backward_varlen, sdtw_barycenter_step_clipped, sdtw_debug_set_wait, sdtw_forward_varlen,
                    sdtw_distance, sdtw_forward, sdtw_forward_cost, sdtw_last_device_status, sdtw_normalized,
                    sdtw_workspace_bytes, workspace)
 
@@ -29,7 +29,7 @@ __all__ = [
     "SoftDTW", "soft_dtw_cost", "softdtw_barycenter", "SdtwError", "load", "workspace",
     "sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
     "sdtw_barycenter_step", "sdtw_barycenter_step_clipped", "sdtw_forward_cost", "sdtw_backward_cost",
-    "sdtw_last_device_status", "cosine_lr",
+    "sdtw_last_device_status", "cosine_lr", "sdtw_forward_varlen", "sdtw_backward_varlen",
     "sdtw_debug_set_wait", "UNFUSED", "FUSED", "EXTENDED", "OP_FWD_BWD", "OP_NORMALIZED", "OP_BARYCENTER",
     "OP_COST", "auto_precision",
 ]
@@ -68,6 +68,37 @@ class _SoftDTWFn(torch.autograd.Function):
         sdtw_backward(xc, yc, ctx.gamma, ctx.mode, g, gx, gy, ws)
         return (None if gx is None else gx.to(ctx.dtypes[0]),
                 None if gy is None else gy.to(ctx.dtypes[1]), None, None)
+
+
+class _SoftDTWVarlenFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, y, x_lengths, y_lengths, gamma, mode):
+        xc, yc = _prep(x, "x"), _prep(y, "y")
+        if xc.shape[0] != yc.shape[0] or xc.shape[2] != yc.shape[2]:
+            raise ValueError("x and y must share batch size and feature dimension")
+        lx = None if x_lengths is None else x_lengths.to(device=xc.device, dtype=torch.int32).contiguous()
+        ly = None if y_lengths is None else y_lengths.to(device=xc.device, dtype=torch.int32).contiguous()
+        B, N, D = xc.shape
+        M = yc.shape[1]
+        ws = workspace(OP_FWD_BWD, B, N, M, D, mode, xc.device)
+        loss = torch.empty(B, dtype=torch.float32, device=xc.device)
+        sdtw_forward_varlen(xc, yc, lx, ly, gamma, mode, loss, ws)
+        ctx.save_for_backward(xc, yc, ws)
+        ctx.lens = (lx, ly)
+        ctx.gamma, ctx.mode = gamma, mode
+        ctx.dtypes = (x.dtype, y.dtype)
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad):
+        xc, yc, ws = ctx.saved_tensors
+        lx, ly = ctx.lens
+        gx = torch.empty_like(xc) if ctx.needs_input_grad[0] else None
+        gy = torch.empty_like(yc) if ctx.needs_input_grad[1] else None
+        sdtw_backward_varlen(xc, yc, lx, ly, ctx.gamma, ctx.mode, grad.detach().to(torch.float32).contiguous(), gx,
+                             gy, ws)
+        return (None if gx is None else gx.to(ctx.dtypes[0]),
+                None if gy is None else gy.to(ctx.dtypes[1]), None, None, None, None)
 
 
 class _NormalizedFn(torch.autograd.Function):
@@ -152,13 +183,21 @@ class SoftDTW:
         self.normalize = normalize
         self.extended = extended
 
-    def __call__(self, x: torch.Tensor, y: torch.Tensor) -> torch.Tensor:
-        fn = _NormalizedFn if self.normalize else _SoftDTWFn
+    def __call__(self, x: torch.Tensor, y: torch.Tensor, x_lengths: torch.Tensor | None = None,
+                 y_lengths: torch.Tensor | None = None) -> torch.Tensor:
+        """x_lengths / y_lengths (B,) integer tensors make (x, y) a padded batch: pair b
+        aligns x[b, :x_lengths[b]] with y[b, :y_lengths[b]]; padded rows get zero
+        gradient and must be finite."""
         mode = FUSED if self.fused else UNFUSED
         if self.extended is None:
             mode |= auto_precision(self.gamma, x.shape[1], y.shape[1], x.shape[2])
         elif self.extended:
             mode |= EXTENDED
+        if x_lengths is not None or y_lengths is not None:
+            if self.normalize:
+                raise ValueError("normalize=True takes equal-length sequences")
+            return _SoftDTWVarlenFn.apply(x, y, x_lengths, y_lengths, self.gamma, mode)
+        fn = _NormalizedFn if self.normalize else _SoftDTWFn
         return fn.apply(x, y, self.gamma, mode)
 
 

@@ -27,7 +27,8 @@ STATUS_NAMES = {
 # Every symbol include/sdtw.h declares.
 EXPORTS = ("sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
            "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_status_string", "sdtw_debug_set_wait",
-           "sdtw_forward_noalloc", "sdtw_forward_cost", "sdtw_backward_cost", "sdtw_barycenter_step_clipped")
+           "sdtw_forward_noalloc", "sdtw_forward_cost", "sdtw_backward_cost", "sdtw_barycenter_step_clipped",
+           "sdtw_forward_varlen", "sdtw_backward_varlen")
 
 
 class SdtwError(RuntimeError):
@@ -68,6 +69,10 @@ def load(path: str = LIB_PATH):
         lib.sdtw_status_string.restype = ctypes.c_char_p
         lib.sdtw_forward_noalloc.argtypes = [vp, vp, i, i, i, i, f, i, vp, vp]
         lib.sdtw_forward_noalloc.restype = i
+        lib.sdtw_forward_varlen.argtypes = [vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
+        lib.sdtw_forward_varlen.restype = i
+        lib.sdtw_backward_varlen.argtypes = [vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, vp, vp, sz, vp]
+        lib.sdtw_backward_varlen.restype = i
         lib.sdtw_barycenter_step_clipped.argtypes = [vp, vp, vp, i, vp, i, i, i, i, f, f, f, f, f, f, i, vp, vp,
                                                      sz, vp]
         lib.sdtw_barycenter_step_clipped.restype = i
@@ -177,6 +182,32 @@ def sdtw_backward(x, y, gamma, mode, grad_loss, grad_x, grad_y, ws, stream=None)
     _check(load().sdtw_backward(_f32(x, "x"), _f32(y, "y"), B, N, M, D, float(gamma), _mode(mode),
                                 _f32(grad_loss, "grad_loss"), _f32(grad_x, "grad_x"), _f32(grad_y, "grad_y"),
                                 _ptr(ws), ws.numel(), _stream(stream)), "sdtw_backward")
+
+
+def _i32(t, name):
+    if t is None:
+        return None
+    if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def sdtw_forward_varlen(x, y, x_lengths, y_lengths, gamma, mode, loss, ws, stream=None):
+    B, N, D = x.shape
+    M = y.shape[1]
+    _check(load().sdtw_forward_varlen(_f32(x, "x"), _f32(y, "y"), _i32(x_lengths, "x_lengths"),
+                                      _i32(y_lengths, "y_lengths"), B, N, M, D, float(gamma), _mode(mode),
+                                      _f32(loss, "loss"), _ptr(ws), ws.numel(), _stream(stream)),
+           "sdtw_forward_varlen")
+
+
+def sdtw_backward_varlen(x, y, x_lengths, y_lengths, gamma, mode, grad_loss, grad_x, grad_y, ws, stream=None):
+    B, N, D = x.shape
+    M = y.shape[1]
+    _check(load().sdtw_backward_varlen(_f32(x, "x"), _f32(y, "y"), _i32(x_lengths, "x_lengths"),
+                                       _i32(y_lengths, "y_lengths"), B, N, M, D, float(gamma), _mode(mode),
+                                       _f32(grad_loss, "grad_loss"), _f32(grad_x, "grad_x"), _f32(grad_y, "grad_y"),
+                                       _ptr(ws), ws.numel(), _stream(stream)), "sdtw_backward_varlen")
 
 
 def sdtw_barycenter_step_clipped(z, m, v, t, X, gamma, lr, beta1, beta2, eps, max_grad_norm, mode, loss_out, ws,

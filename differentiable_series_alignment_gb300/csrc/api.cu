@@ -180,11 +180,15 @@ WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamm
 
 // Forward over L.P problems; per-problem losses to `loss_out` (device).
 // cost: when not null, the caller's (P,N,M) cost tensor replaces the distance step.
+// lens_n / lens_m: per-problem lengths (device), or null for full N x M problems.
 sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gamma, int mode, float* loss_out,
-                        cudaStream_t st, const float* cost = nullptr)
+                        cudaStream_t st, const float* cost = nullptr, const int* lens_n = nullptr,
+                        const int* lens_m = nullptr)
 {
     const bool fused = (mode & SDTW_FUSED) != 0, ext = (mode & SDTW_EXTENDED) != 0;
     WaveParams q = wave_params(pr, L, ws, gamma, fused, ext, false);
+    q.lens_n = lens_n;
+    q.lens_m = lens_m;
     const bool tc = L.tc_cost && env_int(fused ? "SDTW_FUSED_SIMT" : "SDTW_DIST_SIMT", 0) == 0;
     if (fused && tc) {  // the tensor-core fused forward takes 128-row strips (4 warps)
         q.W = 4;
@@ -228,9 +232,12 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
     return SDTW_OK;
 }
 
-sdtw_status run_backward(const Problems& pr, const Layout& L, void* ws, float gamma, int mode, cudaStream_t st)
+sdtw_status run_backward(const Problems& pr, const Layout& L, void* ws, float gamma, int mode, cudaStream_t st,
+                         const int* lens_n = nullptr, const int* lens_m = nullptr)
 {
     WaveParams q = wave_params(pr, L, ws, gamma, (mode & SDTW_FUSED) != 0, (mode & SDTW_EXTENDED) != 0, true);
+    q.lens_n = lens_n;
+    q.lens_m = lens_m;
     SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_b), 0, L.ctrl_b_bytes, st));
     if (q.S > 1) SDTW_CUDA(cudaMemsetAsync(q.edge_b, 0, 2 * sizeof(Slot) * (size_t)L.P * q.S * L.M, st));
     SDTW_CUDA(launch_backward(q, st));
@@ -341,6 +348,13 @@ sdtw_status sdtw_distance(const float* x, const float* y, int B, int N, int M, i
 sdtw_status sdtw_forward(const float* x, const float* y, int B, int N, int M, int D, float gamma, sdtw_mode mode,
                          float* loss, void* ws, size_t ws_bytes, void* stream)
 {
+    return sdtw_forward_varlen(x, y, nullptr, nullptr, B, N, M, D, gamma, mode, loss, ws, ws_bytes, stream);
+}
+
+sdtw_status sdtw_forward_varlen(const float* x, const float* y, const int* x_lengths, const int* y_lengths, int B,
+                                int N, int M, int D, float gamma, sdtw_mode mode, float* loss, void* ws,
+                                size_t ws_bytes, void* stream)
+{
     sdtw_status s = check_common(x, y, B, N, M, D, gamma, (int)mode);
     if (s != SDTW_OK) return s;
     if (!loss) return SDTW_ERR_ARG;
@@ -351,12 +365,21 @@ sdtw_status sdtw_forward(const float* x, const float* y, int B, int N, int M, in
     pr.xs[0] = x; pr.ys[0] = y;
     pr.xstride[0] = (long long)N * D; pr.ystride[0] = (long long)M * D;
     pr.B = B;
-    return run_forward(pr, L, ws, gamma, (int)mode, loss, static_cast<cudaStream_t>(stream));
+    return run_forward(pr, L, ws, gamma, (int)mode, loss, static_cast<cudaStream_t>(stream), nullptr, x_lengths,
+                       y_lengths);
 }
 
 sdtw_status sdtw_backward(const float* x, const float* y, int B, int N, int M, int D, float gamma, sdtw_mode mode,
                           const float* grad_loss, float* grad_x, float* grad_y, void* ws, size_t ws_bytes,
                           void* stream)
+{
+    return sdtw_backward_varlen(x, y, nullptr, nullptr, B, N, M, D, gamma, mode, grad_loss, grad_x, grad_y, ws,
+                                ws_bytes, stream);
+}
+
+sdtw_status sdtw_backward_varlen(const float* x, const float* y, const int* x_lengths, const int* y_lengths, int B,
+                                 int N, int M, int D, float gamma, sdtw_mode mode, const float* grad_loss,
+                                 float* grad_x, float* grad_y, void* ws, size_t ws_bytes, void* stream)
 {
     sdtw_status s = check_common(x, y, B, N, M, D, gamma, (int)mode);
     if (s != SDTW_OK) return s;
@@ -388,7 +411,7 @@ sdtw_status sdtw_backward(const float* x, const float* y, int B, int N, int M, i
             return SDTW_ERR_CUDA;
         }
     }
-    s = run_backward(pr, L, ws, gamma, (int)mode, st);
+    s = run_backward(pr, L, ws, gamma, (int)mode, st, x_lengths, y_lengths);
     if (s == SDTW_OK && (grad_x || grad_y))
         s = run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, (int)mode, st, join);
     if (join) {

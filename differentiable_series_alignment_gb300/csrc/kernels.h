@@ -35,6 +35,8 @@ struct WaveParams {
     int skip_publish; // test hook: strip 0 withholds its forward ready counter
     int accurate;     // 1: unbiased exp2/log2 in the recursions; 0: MUFU approximations
     int ext;          // 1: extended-precision forward state (wavefront_x.cu)
+    const int* lens_n; // per-problem lengths of x and y (device, P each), or null: every
+    const int* lens_m; // problem spans N x M. A problem aligns its leading N_b x M_b block.
 };
 
 size_t wave_smem_fixed(int W, bool backward);

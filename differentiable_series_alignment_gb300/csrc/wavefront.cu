@@ -108,8 +108,11 @@ __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(co
     const bool top_global = has_top && warp == 0;
     const bool has_bot = active && (r0 + 32 < N);
     const bool bot_global = has_bot && warp == W - 1;
+    // this problem's own lengths (a padded batch): it aligns rows < Nb, columns < Mb
+    const int Nb = q.lens_n ? min(max(q.lens_n[p], 1), N) : N;
+    const int Mb = q.lens_m ? min(max(q.lens_m[p], 1), M) : M;
     const bool row0_lane = (i == 0);
-    const bool last_lane = (i == N - 1);
+    const bool last_lane = (i == Nb - 1);
     const float scale = q.scale;
     float* rowbuf = q.rowbuf + (size_t)p * M;
 
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(co
                 vhp[(long long)s * 32] = make_float2(svl, shu);
                 const bool valid = (unsigned)j < (unsigned)M;
                 if (chan_lane && valid) slot_store(chan_out + (j & chan_mask), h, (unsigned)(j + 1));
-                if (last_lane && valid) rowbuf[j] = h;
+                if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = h;
                 h_prev = h;
                 v_prev = v;
             }
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(co
     }
 
     // Loss: R[N,M] = sum_i d(i,0) + sum_{j>=1} h(N-1, j), scaled units.
-    double part = (active && i < N) ? (double)c0 : 0.0;
+    double part = (active && i < Nb) ? (double)c0 : 0.0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
     if (lane == 0) s_red[warp] = part;
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(co
     if (s_last) {  // the last strip of problem p to finish assembles its loss
         __threadfence();
         double acc = 0.0;
-        for (int j = 1 + (int)threadIdx.x; j < M; j += blockDim.x) acc += (double)__ldcg(rowbuf + j);
+        for (int j = 1 + (int)threadIdx.x; j < Mb; j += blockDim.x) acc += (double)__ldcg(rowbuf + j);
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
         if (lane == 0) s_red[warp] = acc;
         __syncthreads();
@@ -341,7 +344,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
     const bool below_global = has_below && warp == W - 1;
     const bool has_above = r0 > 0;                     // consumer: the warp (or strip) above
     const bool above_global = has_above && warp == 0;
-    const bool last_lane = (i == N - 1);
+    // this problem's own lengths (a padded batch): it aligns rows < Nb, columns < Mb
+    const int Nb = q.lens_n ? min(max(q.lens_n[p], 1), N) : N;
+    const int Mb = q.lens_m ? min(max(q.lens_m[p], 1), M) : M;
+    const bool last_lane = (i == Nb - 1);
+    const bool row_in = i < Nb;
 
     using VT = typename std::conditional<EXT, float4, float2>::type;
     const long long sk = skew_index(N, M, p, rb, 0, lane);
@@ -425,14 +432,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
             const float by = __shfl_sync(kFull, botv.y, u);
             const float ru = (lane == 31) ? bx : rs;   // msg_up from (i+1, j)
             const float rd = (lane == 31) ? by : rds;  // msg_diag from (i+1, j), used next step
-            const float a1 = (j < M - 1) ? ml : -kBig;                    // from (i, j+1)
-            const float a2 = last_lane ? -kBig : ru;                      // from (i+1, j)
-            const float a3 = (last_lane || j >= M - 1) ? -kBig : rd_hold; // from (i+1, j+1)
+            const float a1 = (j < Mb - 1) ? ml : -kBig;                    // from (i, j+1)
+            const float a2 = last_lane ? -kBig : ru;                       // from (i+1, j)
+            const float a3 = (last_lane || j >= Mb - 1) ? -kBig : rd_hold; // from (i+1, j+1)
             rd_hold = rd;
             float lo, mid, hi;
             sort3(a1, a2, a3, lo, mid, hi);
             float lE = hi + dp_log2<ACC>((1.f + dp_exp2<ACC>(mid - hi)) + dp_exp2<ACC>(lo - hi));
-            lE = (last_lane && j == M - 1) ? 0.f : lE;
+            lE = (last_lane && j == Mb - 1) ? 0.f : lE;
             VT cur;
             if (EXT) {  // single buffer (register budget): refill slot u right after use
                 cur = buf[u];
@@ -456,7 +463,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
             ml = lE + wl;
             su = lE + wu;
             sd = lE + wd;
-            ep[(long long)t * 32] = ex2(lE);
+            // cells outside this problem's own N_b x M_b block carry no alignment
+            ep[(long long)t * 32] = (row_in && (unsigned)j < (unsigned)Mb) ? ex2(lE) : 0.f;
             if (chan_lane && (unsigned)j < (unsigned)M) {
                 const int k = M - 1 - j;
                 Slot* dst = chan_out + 2 * (k & chan_mask);

@@ -184,7 +184,10 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
         const bool has_bot = active && (r0 + 32 < N);
         const bool bot_global = has_bot && warp == W - 1;
         const bool row0_lane = (i == 0);
-        const bool last_lane = (i == N - 1);
+        // this problem's own lengths (a padded batch): it aligns rows < Nb, columns < Mb
+        const int Nb = q.lens_n ? min(max(q.lens_n[p], 1), N) : N;
+        const int Mb = q.lens_m ? min(max(q.lens_m[p], 1), M) : M;
+        const bool last_lane = (i == Nb - 1);
         const float scale = q.scale;
         float* rowbuf = q.rowbuf + (size_t)p * M;
         float* dt = dts + warp * 64 * 32;  // [64][32] raw cost, slot (col & 63), lane
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                     vhp[(long long)s * 32] = make_float2(svl, shu);
                     const bool valid = (unsigned)j < (unsigned)M;
                     if (chan_lane && valid) slot_store(chan_out + (j & chan_mask), h, (unsigned)(j + 1));
-                    if (last_lane && valid) rowbuf[j] = h;
+                    if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = h;
                     h_prev = h;
                     v_prev = v;
                 }
@@ -293,7 +296,9 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     }
 
     // Loss: R[N,M] = sum_i d(i,0) + sum_{j>=1} h(N-1, j), scaled units.
-    double part = (active && warp < W && rs0 + 32 * warp + lane < N) ? (double)c0 : 0.0;
+    const int Nb = q.lens_n ? min(max(q.lens_n[p], 1), N) : N;
+    const int Mb = q.lens_m ? min(max(q.lens_m[p], 1), M) : M;
+    double part = (active && warp < W && rs0 + 32 * warp + lane < Nb) ? (double)c0 : 0.0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
     if (lane == 0) s_red[warp] = part;
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     if (s_last) {  // the last strip of problem p to finish assembles its loss
         __threadfence();
         double acc = 0.0;
-        for (int j = 1 + (int)threadIdx.x; j < M; j += blockDim.x) acc += (double)__ldcg(rowbuf + j);
+        for (int j = 1 + (int)threadIdx.x; j < Mb; j += blockDim.x) acc += (double)__ldcg(rowbuf + j);
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
         if (lane == 0) s_red[warp] = acc;
         __syncthreads();

@@ -151,7 +151,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
     const bool has_bot = active && (r0 + 32 < N);
     const bool bot_global = has_bot && warp == W - 1;
     const bool row0_lane = (i == 0);
-    const bool last_lane = (i == N - 1);
+    // this problem's own lengths (a padded batch): it aligns rows < Nb, columns < Mb
+    const int Nb = q.lens_n ? min(max(q.lens_n[p], 1), N) : N;
+    const int Mb = q.lens_m ? min(max(q.lens_m[p], 1), M) : M;
+    const bool last_lane = (i == Nb - 1);
     const float scale = q.scale;
     float2* rowbuf = reinterpret_cast<float2*>(q.rowbuf) + (size_t)p * M;
     const dd zero = mk(0.f, 0.f), nbig = mk(-kBig, 0.f);
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
                     slot_store(dst, h.hi, (unsigned)(j + 1));
                     slot_store(dst + 1, h.lo, (unsigned)(j + 1));
                 }
-                if (last_lane && valid) rowbuf[j] = make_float2(h.hi, h.lo);
+                if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = make_float2(h.hi, h.lo);
                 h_prev = h;
                 v_prev = v;
             }
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
     }
 
     // Loss: R[N,M] = sum_i d(i,0) + sum_{j>=1} h(N-1, j), scaled units, in fp64.
-    double part = (active && i < N) ? (double)c0.hi + (double)c0.lo : 0.0;
+    double part = (active && i < Nb) ? (double)c0.hi + (double)c0.lo : 0.0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
     if (lane == 0) s_red[warp] = part;
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
     if (s_last) {
         __threadfence();
         double acc = 0.0;
-        for (int j = 1 + (int)threadIdx.x; j < M; j += blockDim.x) {
+        for (int j = 1 + (int)threadIdx.x; j < Mb; j += blockDim.x) {
             const float2 hv = __ldcg(rowbuf + j);
             acc += (double)hv.x + (double)hv.y;
         }

@@ -95,6 +95,23 @@ sdtw_status sdtw_backward(const float* x, const float* y, int B, int N, int M, i
                           sdtw_mode mode, const float* grad_loss, float* grad_x, float* grad_y,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* sdtw_forward / sdtw_backward on a padded batch of unequal lengths (SoftDTW
+ * README: sequences of any length; the pages show no padded-batch interface, the
+ * one adopted is this). x_lengths and y_lengths are DEVICE int arrays (B,):
+ * problem b aligns x_b[0, N_b) with y_b[0, M_b), N_b = x_lengths[b], M_b =
+ * y_lengths[b], so loss[b] = R_b[N_b, M_b]; lengths are clamped to [1, N] and
+ * [1, M] on the device (they are not read on the host). Gradients of padded
+ * rows are 0; the padding of x and y must be finite (zeros are fine). Either
+ * array may be NULL (full length). The workspace is that of sdtw_forward for
+ * the padded sizes, and the backward must get the same lengths. */
+sdtw_status sdtw_forward_varlen(const float* x, const float* y, const int* x_lengths, const int* y_lengths,
+                                int B, int N, int M, int D, float gamma, sdtw_mode mode, float* loss,
+                                void* ws, size_t ws_bytes, void* stream);
+sdtw_status sdtw_backward_varlen(const float* x, const float* y, const int* x_lengths,
+                                 const int* y_lengths, int B, int N, int M, int D, float gamma,
+                                 sdtw_mode mode, const float* grad_loss, float* grad_x, float* grad_y,
+                                 void* ws, size_t ws_bytes, void* stream);
+
 /* Normalized Soft-DTW (README, "Normalization"):
  *   loss[b] = s(x_b,y_b) - (s(x_b,x_b) + s(y_b,y_b)) / 2,  x and y both (B,N,D).
  * The three problems run as one batch of 3B. When grad_loss is non-NULL the

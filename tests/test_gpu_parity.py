@@ -310,6 +310,51 @@ def test_barycenter_steps_match_oracle(mname, mode):
         assert_close(z.cpu().numpy() - zc, zo - zc, 2e-3, 1e-6, f"step {t} update")
 
 
+# --------------------------------------------------------------------------- padded batches
+
+@pytest.mark.parametrize("mname,mode,weights", [("unfused", 0, WEIGHTS + [0.25 / 32]),
+                                                ("fused", 1, WEIGHTS + [0.25 / 32]),
+                                                ("unfused+extended", 2, WEIGHTS_O1 + [0.25]),
+                                                ("fused+extended", 3, WEIGHTS_O1 + [0.25])])
+def test_padded_batch_matches_oracle(mname, mode, weights):
+    L = _lib()
+    B, N, M, D, gamma = 4, 100, 90, 6, 0.9
+    lx, ly = [100, 37, 1, 64], [90, 90, 5, 33]
+    x, y = synth.iid_normal_pair(B, N, M, D, 99)
+    for b in range(B):               # zero padding beyond each pair's lengths
+        x[b, lx[b]:] = 0.0
+        y[b, ly[b]:] = 0.0
+    xt, yt = torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda()
+    lxt = torch.tensor(lx, dtype=torch.int32, device="cuda")
+    lyt = torch.tensor(ly, dtype=torch.int32, device="cuda")
+    ws = L.workspace(L.OP_FWD_BWD, B, N, M, D, mode)
+    loss = torch.empty(B, device="cuda")
+    gx, gy = torch.empty_like(xt), torch.empty_like(yt)
+    g = torch.tensor(weights, dtype=torch.float32, device="cuda")
+    L.sdtw_forward_varlen(xt, yt, lxt, lyt, gamma, mode, loss, ws)
+    L.sdtw_backward_varlen(xt, yt, lxt, lyt, gamma, mode, g, gx, gy, ws)
+    assert L.sdtw_last_device_status(ws) == 0
+    loss, gx, gy = loss.cpu().numpy(), gx.cpu().numpy(), gy.cpu().numpy()
+    for b in range(B):
+        o = oracle.single(x[b, :lx[b]], y[b, :ly[b]], gamma, g=weights[b])
+        assert_close(loss[b:b + 1], [o["loss"]], LOSS_RTOL, 1e-6, f"padded {mname} pair {b} loss")
+        assert_close(gx[b, :lx[b]], o["gx"], GRAD_RTOL, GRAD_ATOL, f"padded {mname} pair {b} grad_x")
+        assert_close(gy[b, :ly[b]], o["gy"], GRAD_RTOL, GRAD_ATOL, f"padded {mname} pair {b} grad_y")
+        assert not np.any(gx[b, lx[b]:]) and not np.any(gy[b, ly[b]:])   # padding gets zero gradient
+
+
+def test_padded_batch_autograd_and_full_lengths():
+    from differentiable_series_alignment_gb300 import SoftDTW
+    x, y = synth.iid_normal_pair(3, 50, 41, 4, 100)
+    xt = torch.from_numpy(x).cuda().requires_grad_(True)
+    yt = torch.from_numpy(y).cuda()
+    full = SoftDTW(gamma=1.0)(xt, yt)
+    lens = SoftDTW(gamma=1.0)(xt, yt, torch.tensor([50, 50, 50]), torch.tensor([41, 41, 41]))
+    assert_close(lens.detach().cpu().numpy(), full.detach().cpu().numpy(), 1e-6, 0.0, "full lengths")
+    lens.sum().backward()
+    assert torch.isfinite(xt.grad).all()
+
+
 # --------------------------------------------------------------------------- caller-supplied costs
 
 def _cost_batch(kind, B, N, M, seed):
