@@ -98,14 +98,20 @@ __global__ void __launch_bounds__(256) simg_kernel(Problems pr, int N, int M, in
         }
         if (part == 0) nrm[(size_t)p * Lpad + r0 + r] = s + c;
     }
-    // a warp writes one 128-byte image row (32 features of one row) per pass
-    for (int idx = threadIdx.x; idx < 32 * D32; idx += blockDim.x) {
-        const int k = idx & 31, r = (idx >> 5) & 31, kb = idx >> 10;
-        float h, l;
-        split_tf32(t[r * ld + kb * 32 + k], h, l);
-        const uint32_t o = (uint32_t)((((k >> 2) ^ (r & 7)) << 4) + (k & 3) * 4) / 4;
-        img[simg_offset(p, KB, kb, 0, Lpad, r0 + r) + o] = h;
-        img[simg_offset(p, KB, kb, 1, Lpad, r0 + r) + o] = l;
+    // one 16-byte chunk (4 features) per thread and pass: eight threads write one
+    // 128-byte image row (its chunks permuted by the swizzle), a warp four rows
+    const size_t part = (size_t)Lpad * 32;   // floats between the hi and lo images of a K-block
+    for (int idx = threadIdx.x; idx < 32 * D32 / 4; idx += blockDim.x) {
+        const int c8 = idx & 7, r = (idx >> 3) & 31, kb = idx >> 8;
+        const float* src4 = t + r * ld + kb * 32 + 4 * c8;
+        float4 hi, lo;
+        split_tf32(src4[0], hi.x, lo.x);
+        split_tf32(src4[1], hi.y, lo.y);
+        split_tf32(src4[2], hi.z, lo.z);
+        split_tf32(src4[3], hi.w, lo.w);
+        float* row = img + simg_offset(p, KB, kb, 0, Lpad, r0 + r) + 4 * (c8 ^ (r & 7));
+        *reinterpret_cast<float4*>(row) = hi;
+        *reinterpret_cast<float4*>(row + part) = lo;
     }
 }
 
