@@ -41,6 +41,8 @@ BWD_DRAM_BYTES = 79.55e6
 # (wavefront, gradient operand images, two gradient contractions), fused forward
 # (operand images, wavefront with tensor-core costs) + backward (4)
 LAUNCHES_PER_STEP = 3 + 4 + 2 + 4
+# chunks of the batch in the end-to-end (host buffer) step
+E2E_CHUNKS = 2
 
 
 def log(*a):
@@ -195,7 +197,7 @@ def cpu_baseline():
 def run_ours(args):
     import torch
     import torch.distributed as dist
-    from differentiable_series_alignment_gb300 import SoftDTW, _lib as L, synth
+    from differentiable_series_alignment_gb300 import _lib as L, synth
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -311,22 +313,21 @@ def run_ours(args):
                 "launch_ms": bw_ms,
                 "note": "latency-bound: N+M-1 dependent DP steps; traffic from one ncu capture of this kernel"}
 
-    # ---- end to end through the public API, host buffers, both modes
+    # ---- end to end through the C ABI with HOST buffers, both modes: every step copies the
+    # batch in from pinned host memory and the losses and gradients back out
+    # (sdtw_value_and_grad_host: the batch runs as E2E_CHUNKS chunks on side streams, so the
+    # copies of one chunk overlap the kernels of the others)
     xh = torch.from_numpy(x_np).pin_memory()
     yh = torch.from_numpy(y_np).pin_memory()
-    outs = {m_: (torch.empty(B).pin_memory(), torch.empty_like(xh).pin_memory(), torch.empty_like(yh).pin_memory())
-            for m_ in (False, True)}
+    glh = torch.full((B,), 1.0 / B).pin_memory()
+    hbuf = {m_: (torch.empty(B).pin_memory(), torch.empty_like(xh).pin_memory(), torch.empty_like(yh).pin_memory(),
+                 L.host_workspace(B, N, M, D, m_, E2E_CHUNKS, device=dev))
+            for m_ in (L.UNFUSED, L.FUSED)}
 
     def e2e_step():
-        for fused in (False, True):
-            xd = xh.to(dev, non_blocking=True).requires_grad_(True)
-            yd = yh.to(dev, non_blocking=True).requires_grad_(True)
-            loss = SoftDTW(gamma=GAMMA, fused=fused)(xd, yd)
-            loss.mean().backward()
-            lo, gxo, gyo = outs[fused]
-            lo.copy_(loss.detach(), non_blocking=True)
-            gxo.copy_(xd.grad, non_blocking=True)
-            gyo.copy_(yd.grad, non_blocking=True)
+        for mode in (L.UNFUSED, L.FUSED):
+            lo, gxo, gyo, wsh = hbuf[mode]
+            L.sdtw_value_and_grad_host(xh, yh, glh, GAMMA, mode, lo, gxo, gyo, E2E_CHUNKS, wsh, stream)
 
     for _ in range(3):
         e2e_step()
@@ -339,7 +340,9 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / ke
-    h2d = 2 * (xh.numel() + yh.numel()) * 4
+    for mode in (L.UNFUSED, L.FUSED):
+        assert L.sdtw_last_device_status(hbuf[mode][3], stream) == 0
+    h2d = 2 * (xh.numel() + yh.numel() + B) * 4
     d2h = 2 * (B + xh.numel() + yh.numel()) * 4
 
     if rank != 0:

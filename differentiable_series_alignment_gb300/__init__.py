@@ -7,6 +7,7 @@ Low level (same names as the C entry points, torch tensors for pointers):
 High level, following the usage shown in the SoftDTW-CUDA (PyTorch + Numba)
 README ("Usage", "Fused Mode", "Normalization", "Time Series Barycenters"):
     SoftDTW(gamma=1.0, fused=False, normalize=False)(x, y) -> (B,) losses, differentiable
+    value_and_grad_host(x, y, gamma=1.0, fused=False) -> (loss, grad_x, grad_y) of a host batch
     soft_dtw_cost(C, gamma=1.0) -> (B,) losses of a given (B,N,M) cost, differentiable in C
     softdtw_barycenter(sequences, gamma=1.0, max_iter=100, lr=0.1, fused=True) -> (T, D)
 
@@ -23,7 +24,8 @@ from ._lib import (EXTENDED, FUSED, OP_BARYCENTER, OP_COST, OP_FWD_BWD, OP_NORMA
                    auto_precision, load, sdtw_backward, sdtw_backward_cost, sdtw_barycenter_step,
                    sdtw_backward_varlen, sdtw_barycenter_step_clipped, sdtw_debug_set_wait, sdtw_forward_varlen,
                    sdtw_distance, sdtw_forward, sdtw_forward_cost, sdtw_last_device_status, sdtw_normalized,
-                   sdtw_workspace_bytes, workspace)
+                   sdtw_workspace_bytes, workspace, host_workspace, sdtw_host_workspace_bytes,
+                   sdtw_value_and_grad_host)
 
 __all__ = [
     "SoftDTW", "soft_dtw_cost", "softdtw_barycenter", "SdtwError", "load", "workspace",
@@ -31,7 +33,8 @@ __all__ = [
     "sdtw_barycenter_step", "sdtw_barycenter_step_clipped", "sdtw_forward_cost", "sdtw_backward_cost",
     "sdtw_last_device_status", "cosine_lr", "sdtw_forward_varlen", "sdtw_backward_varlen",
     "sdtw_debug_set_wait", "UNFUSED", "FUSED", "EXTENDED", "OP_FWD_BWD", "OP_NORMALIZED", "OP_BARYCENTER",
-    "OP_COST", "auto_precision",
+    "OP_COST", "auto_precision", "value_and_grad_host", "host_workspace", "sdtw_host_workspace_bytes",
+    "sdtw_value_and_grad_host",
 ]
 
 
@@ -199,6 +202,41 @@ class SoftDTW:
             return _SoftDTWVarlenFn.apply(x, y, x_lengths, y_lengths, self.gamma, mode)
         fn = _NormalizedFn if self.normalize else _SoftDTWFn
         return fn.apply(x, y, self.gamma, mode)
+
+
+def value_and_grad_host(x: torch.Tensor, y: torch.Tensor, gamma: float = 1.0, fused: bool = False,
+                        grad_loss: torch.Tensor | None = None, chunks: int = 2, extended: bool | None = None,
+                        device=None):
+    """Losses (B,) and input gradients of a batch held in host memory, in one call
+    that overlaps the host<->device copies of one chunk of the batch with the
+    kernels of the others. x (B,N,D), y (B,M,D) are float32 CPU tensors (pinned
+    for overlap); grad_loss (B,) defaults to ones. Returns pinned CPU tensors
+    (loss, grad_x, grad_y), complete when this function returns."""
+    if not (gamma > 0):
+        raise ValueError("gamma must be > 0")
+    if x.dim() != 3 or y.dim() != 3 or x.shape[0] != y.shape[0] or x.shape[2] != y.shape[2]:
+        raise ValueError("x must be (B,N,D) and y (B,M,D)")
+    B, N, D = x.shape
+    M = y.shape[1]
+    mode = FUSED if fused else UNFUSED
+    if extended is None:
+        mode |= auto_precision(gamma, N, M, D)
+    elif extended:
+        mode |= EXTENDED
+    pin = torch.cuda.is_available()
+    xh = x.detach().to(torch.float32).contiguous()
+    yh = y.detach().to(torch.float32).contiguous()
+    gl = torch.ones(B) if grad_loss is None else grad_loss.detach().to(torch.float32).contiguous()
+    loss = torch.empty(B, pin_memory=pin)
+    gx = torch.empty((B, N, D), pin_memory=pin)
+    gy = torch.empty((B, M, D), pin_memory=pin)
+    ws = host_workspace(B, N, M, D, mode, chunks, device=device)
+    stream = torch.cuda.current_stream(ws.device)
+    sdtw_value_and_grad_host(xh, yh, gl, gamma, mode, loss, gx, gy, chunks, ws, stream)
+    code = sdtw_last_device_status(ws, stream)
+    if code != 0:
+        raise SdtwError(code, "value_and_grad_host")
+    return loss, gx, gy
 
 
 def cosine_lr(t: int, max_iter: int, lr: float, lr_min: float = 0.0) -> float:

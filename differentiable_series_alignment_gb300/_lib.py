@@ -28,7 +28,7 @@ STATUS_NAMES = {
 EXPORTS = ("sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
            "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_status_string", "sdtw_debug_set_wait",
            "sdtw_forward_noalloc", "sdtw_forward_cost", "sdtw_backward_cost", "sdtw_barycenter_step_clipped",
-           "sdtw_forward_varlen", "sdtw_backward_varlen")
+           "sdtw_forward_varlen", "sdtw_backward_varlen", "sdtw_host_workspace_bytes", "sdtw_value_and_grad_host")
 
 
 class SdtwError(RuntimeError):
@@ -80,6 +80,10 @@ def load(path: str = LIB_PATH):
         lib.sdtw_forward_cost.restype = i
         lib.sdtw_backward_cost.argtypes = [vp, i, i, i, f, i, vp, vp, vp, sz, vp]
         lib.sdtw_backward_cost.restype = i
+        lib.sdtw_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.sdtw_host_workspace_bytes.restype = sz
+        lib.sdtw_value_and_grad_host.argtypes = [vp, vp, vp, i, i, i, i, f, i, vp, vp, vp, i, vp, sz, vp]
+        lib.sdtw_value_and_grad_host.restype = i
         lib.sdtw_debug_set_wait.argtypes = [ctypes.c_double, i]
         lib.sdtw_debug_set_wait.restype = None
         _lib = lib
@@ -151,6 +155,36 @@ def workspace(op: int, B: int, N: int, M: int, D: int, mode, device=None) -> tor
     if n == 0:
         raise SdtwError(1, "sdtw_workspace_bytes")
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _host_f32(t, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 CPU tensor (page-locked for overlap)")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def sdtw_host_workspace_bytes(B: int, N: int, M: int, D: int, mode, chunks: int = 0) -> int:
+    return int(load().sdtw_host_workspace_bytes(B, N, M, D, _mode(mode), int(chunks)))
+
+
+def host_workspace(B: int, N: int, M: int, D: int, mode, chunks: int = 0, device=None) -> torch.Tensor:
+    """Device workspace of sdtw_value_and_grad_host (uint8, caching allocator: 512-B aligned)."""
+    n = sdtw_host_workspace_bytes(B, N, M, D, mode, chunks)
+    if n == 0:
+        raise SdtwError(1, "sdtw_host_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def sdtw_value_and_grad_host(x, y, grad_loss, gamma, mode, loss, grad_x, grad_y, chunks, ws, stream=None):
+    """x, y, grad_loss, loss, grad_x, grad_y: CPU tensors; ws: device workspace. Asynchronous on `stream`."""
+    B, N, D = x.shape
+    M = y.shape[1]
+    _check(load().sdtw_value_and_grad_host(_host_f32(x, "x"), _host_f32(y, "y"), _host_f32(grad_loss, "grad_loss"),
+                                           B, N, M, D, float(gamma), _mode(mode), _host_f32(loss, "loss"),
+                                           _host_f32(grad_x, "grad_x"), _host_f32(grad_y, "grad_y"), int(chunks),
+                                           _ptr(ws), ws.numel(), _stream(stream)), "sdtw_value_and_grad_host")
 
 
 def sdtw_distance(x, y, C, stream=None):

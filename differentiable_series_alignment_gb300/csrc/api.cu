@@ -121,6 +121,11 @@ int num_sms()
     return n;
 }
 
+// SMs the batch being launched may count on: the whole device, or its share
+// while the chunks of a host-buffer call run side by side on several streams.
+thread_local int t_sm_share = 0;
+int sm_budget() { return t_sm_share > 0 ? t_sm_share : num_sms(); }
+
 sdtw_status check_common(const void* x, const void* y, int B, int N, int M, int D, float gamma, int mode)
 {
     if (B < 1 || N < 1 || M < 1 || D < 1) return SDTW_ERR_EMPTY;
@@ -147,7 +152,7 @@ WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamm
     WaveParams q{};
     q.pr = pr;
     q.P = L.P; q.N = L.N; q.M = L.M; q.D = L.D; q.NB = L.NB;
-    q.W = choose_warps(L.P, L.NB, L.D, fused && !backward, ext, backward, num_sms());
+    q.W = choose_warps(L.P, L.NB, L.D, fused && !backward, ext, backward, sm_budget());
     q.S = (L.NB + q.W - 1) / q.W;
     q.scale = (float)(1.4426950408889634 / (double)gamma);
     q.unscale = (float)((double)gamma * 0.6931471805599453);
@@ -272,6 +277,71 @@ cudaStream_t side_stream()
     if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
         streams[dev] = nullptr;
     return streams[dev];
+}
+
+// Streams on which the chunks of a host-buffer call run side by side (created
+// once per device, non-blocking; ordered against the caller's stream by events).
+constexpr int kMaxChunks = 8;
+bool chunk_streams(cudaStream_t (&out)[kMaxChunks])
+{
+    static std::mutex mu;
+    static cudaStream_t streams[64][kMaxChunks] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int c = 0; c < kMaxChunks; ++c) {
+        if (!streams[dev][c] && cudaStreamCreateWithFlags(&streams[dev][c], cudaStreamNonBlocking) != cudaSuccess) {
+            streams[dev][c] = nullptr;
+            return false;
+        }
+        out[c] = streams[dev][c];
+    }
+    return true;
+}
+
+int host_chunks(int B, int chunks)
+{
+    if (chunks <= 0) chunks = 2;
+    if (chunks > kMaxChunks) chunks = kMaxChunks;
+    return chunks < B ? chunks : B;
+}
+
+// Device workspace of sdtw_value_and_grad_host: the aggregated status word at
+// offset 0, device copies of the inputs and outputs, then one forward/backward
+// workspace per chunk (sized for the largest chunk).
+struct HostLayout {
+    size_t x, y, gx, gy, gl, loss, ws0, ws_stride, total;
+    int chunks;
+};
+
+bool make_host_layout(int B, int N, int M, int D, int mode, int chunks, HostLayout* H)
+{
+    if (B < 1 || N < 1 || M < 1 || D < 1) return false;
+    H->chunks = host_chunks(B, chunks);
+    const int bmax = (B + H->chunks - 1) / H->chunks;
+    Layout L;
+    if (!make_layout(SDTW_OP_FWD_BWD, bmax, N, M, D, mode, &L)) return false;
+    size_t o = align_up(sizeof(int));
+    H->x = o; o = align_up(o + sizeof(float) * (size_t)B * N * D);
+    H->y = o; o = align_up(o + sizeof(float) * (size_t)B * M * D);
+    H->gx = o; o = align_up(o + sizeof(float) * (size_t)B * N * D);
+    H->gy = o; o = align_up(o + sizeof(float) * (size_t)B * M * D);
+    H->gl = o; o = align_up(o + sizeof(float) * (size_t)B);
+    H->loss = o; o = align_up(o + sizeof(float) * (size_t)B);
+    H->ws0 = o;
+    H->ws_stride = align_up(L.total);
+    H->total = o + (size_t)H->chunks * H->ws_stride;
+    return true;
+}
+
+// status[0] = OR of the status words of the chunk workspaces.
+__global__ void gather_status_kernel(int* status, const char* ws0, size_t stride, int chunks)
+{
+    if (threadIdx.x == 0) {
+        int v = 0;
+        for (int c = 0; c < chunks; ++c) v |= *reinterpret_cast<const int*>(ws0 + (size_t)c * stride);
+        *status = v;
+    }
 }
 
 // images_ready: when not null, the operand images were already launched on
@@ -528,6 +598,84 @@ sdtw_status sdtw_backward_cost(const float* C, int B, int N, int M, float gamma,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((s = run_backward(pr, L, ws, gamma, (int)mode, st)) != SDTW_OK) return s;
     SDTW_CUDA(launch_unskew_grad(at<float>(ws, L.e), B, N, M, grad_loss, grad_C, st));
+    return SDTW_OK;
+}
+
+size_t sdtw_host_workspace_bytes(int B, int N, int M, int D, sdtw_mode mode, int chunks)
+{
+    HostLayout H;
+    if (!make_host_layout(B, N, M, D, (int)mode, chunks, &H)) return 0;
+    return H.total;
+}
+
+sdtw_status sdtw_value_and_grad_host(const float* x, const float* y, const float* grad_loss, int B, int N, int M,
+                                     int D, float gamma, sdtw_mode mode, float* loss, float* grad_x, float* grad_y,
+                                     int chunks, void* ws, size_t ws_bytes, void* stream)
+{
+    sdtw_status s = check_common(x, y, B, N, M, D, gamma, (int)mode);
+    if (s != SDTW_OK) return s;
+    const bool grads = grad_x || grad_y;
+    if (!loss || (grads && !grad_loss)) return SDTW_ERR_ARG;
+    HostLayout H;
+    if (!make_host_layout(B, N, M, D, (int)mode, chunks, &H)) return SDTW_ERR_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 || ws_bytes < H.total) return SDTW_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t cs[kMaxChunks];
+    if (!chunk_streams(cs)) return SDTW_ERR_CUDA;
+    cudaEvent_t fork = nullptr;
+    SDTW_CUDA(cudaEventCreateWithFlags(&fork, cudaEventDisableTiming));
+    if (cudaEventRecord(fork, st) != cudaSuccess) {
+        cudaEventDestroy(fork);
+        return SDTW_ERR_CUDA;
+    }
+    const int prev_share = t_sm_share;
+    t_sm_share = num_sms() / H.chunks > 0 ? num_sms() / H.chunks : 1;
+    const size_t xr = (size_t)N * D, yr = (size_t)M * D;  // floats per problem
+    const auto h2d = cudaMemcpyHostToDevice;
+    const auto d2h = cudaMemcpyDeviceToHost;
+    for (int c = 0; c < H.chunks && s == SDTW_OK; ++c) {
+        const int b0 = (int)((long long)c * B / H.chunks), b1 = (int)((long long)(c + 1) * B / H.chunks);
+        const int Bc = b1 - b0;
+        cudaStream_t sc = cs[c];
+        float* xd = at<float>(ws, H.x) + b0 * xr;
+        float* yd = at<float>(ws, H.y) + b0 * yr;
+        float* gxd = grad_x ? at<float>(ws, H.gx) + b0 * xr : nullptr;
+        float* gyd = grad_y ? at<float>(ws, H.gy) + b0 * yr : nullptr;
+        float* gld = at<float>(ws, H.gl) + b0;
+        float* lossd = at<float>(ws, H.loss) + b0;
+        void* wsc = at<char>(ws, H.ws0 + (size_t)c * H.ws_stride);
+        // inputs of this chunk in, its forward and backward, its outputs out: the copies
+        // of one chunk overlap the kernels of the others
+        bool ok = cudaStreamWaitEvent(sc, fork, 0) == cudaSuccess &&
+                  cudaMemcpyAsync(xd, x + b0 * xr, sizeof(float) * Bc * xr, h2d, sc) == cudaSuccess &&
+                  cudaMemcpyAsync(yd, y + b0 * yr, sizeof(float) * Bc * yr, h2d, sc) == cudaSuccess &&
+                  (!grads || cudaMemcpyAsync(gld, grad_loss + b0, sizeof(float) * Bc, h2d, sc) == cudaSuccess);
+        if (!ok) s = SDTW_ERR_CUDA;
+        if (s == SDTW_OK) s = sdtw_forward(xd, yd, Bc, N, M, D, gamma, mode, lossd, wsc, H.ws_stride, sc);
+        if (s == SDTW_OK && grads)
+            s = sdtw_backward(xd, yd, Bc, N, M, D, gamma, mode, gld, gxd, gyd, wsc, H.ws_stride, sc);
+        if (s == SDTW_OK) {
+            ok = cudaMemcpyAsync(loss + b0, lossd, sizeof(float) * Bc, d2h, sc) == cudaSuccess &&
+                 (!grad_x || cudaMemcpyAsync(grad_x + b0 * xr, gxd, sizeof(float) * Bc * xr, d2h, sc) == cudaSuccess) &&
+                 (!grad_y || cudaMemcpyAsync(grad_y + b0 * yr, gyd, sizeof(float) * Bc * yr, d2h, sc) == cudaSuccess);
+            if (!ok) s = SDTW_ERR_CUDA;
+        }
+        // join, whatever happened, so that later work on the caller's stream stays ordered
+        cudaEvent_t join = nullptr;
+        if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+            s = SDTW_ERR_CUDA;
+            break;
+        }
+        if ((cudaEventRecord(join, sc) != cudaSuccess || cudaStreamWaitEvent(st, join, 0) != cudaSuccess) &&
+            s == SDTW_OK)
+            s = SDTW_ERR_CUDA;
+        cudaEventDestroy(join);  // released once complete
+    }
+    t_sm_share = prev_share;
+    cudaEventDestroy(fork);
+    if (s != SDTW_OK) return s;
+    gather_status_kernel<<<1, 32, 0, st>>>(at<int>(ws, 0), at<char>(ws, H.ws0), H.ws_stride, H.chunks);
+    SDTW_CUDA(cudaGetLastError());
     return SDTW_OK;
 }
 

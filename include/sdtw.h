@@ -18,7 +18,8 @@
  *  - Tensors are fp32, row-major and contiguous: x (B,N,D), y (B,M,D),
  *    grad_x like x, grad_y like y, loss and grad_loss (B,).
  *  - Every tensor pointer and the workspace are DEVICE pointers owned by the
- *    caller. The library allocates nothing.
+ *    caller, except the tensors of sdtw_value_and_grad_host, which are HOST
+ *    pointers. The library allocates no memory.
  *  - `ws` is a caller-owned device workspace of at least
  *    sdtw_workspace_bytes(...) bytes, 256-byte aligned. sdtw_forward leaves in
  *    it the state that the matching sdtw_backward reads, so the caller keeps it
@@ -179,6 +180,35 @@ sdtw_status sdtw_forward_cost(const float* C, int B, int N, int M, float gamma, 
 sdtw_status sdtw_backward_cost(const float* C, int B, int N, int M, float gamma, sdtw_mode mode,
                                const float* grad_loss, float* grad_C, void* ws, size_t ws_bytes,
                                void* stream);
+
+/* Bytes of device workspace needed by sdtw_value_and_grad_host; 0 when the
+ * arguments are invalid. Pure host function, no CUDA call. */
+size_t sdtw_host_workspace_bytes(int B, int N, int M, int D, sdtw_mode mode, int chunks);
+
+/* Loss and input gradients of a batch that lives in HOST memory: the training
+ * step of the SoftDTW README's "Usage" (loss of a batch, then its backward) with
+ * the host<->device copies included. x (B,N,D), y (B,M,D) and grad_loss (B,)
+ * are read from host memory; loss (B,), grad_x (B,N,D) and grad_y (B,M,D) are
+ * written to host memory (grad_x / grad_y may be NULL; grad_loss may be NULL
+ * only when both are). Use page-locked host memory (cudaHostAlloc): pageable
+ * buffers give the same results without overlap.
+ * The batch is cut into `chunks` groups of problems (<= 0: 2; at most 8 and at
+ * most B), each run on a stream of its own that copies its inputs in, runs
+ * sdtw_forward and sdtw_backward and copies its outputs out, so the copies of one
+ * chunk overlap the kernels of the others; each chunk's wavefronts are sized
+ * for its share of the SMs. The wavefronts of a small batch are latency-bound
+ * (each chunk takes about as long as the whole batch), so there more chunks
+ * only delay the last one; large batches gain from more. The call is asynchronous on `stream` like every
+ * other: the host outputs are complete once the stream reaches this point, and
+ * the host inputs must stay unchanged until then.
+ * `ws` (device, 256-byte aligned) holds at least sdtw_host_workspace_bytes(B, N,
+ * M, D, mode, chunks) bytes; its status word (offset 0) gathers the chunks'
+ * device status, so sdtw_last_device_status(ws, stream) reports a timed-out
+ * wait of any chunk. */
+sdtw_status sdtw_value_and_grad_host(const float* x, const float* y, const float* grad_loss, int B, int N,
+                                     int M, int D, float gamma, sdtw_mode mode, float* loss,
+                                     float* grad_x, float* grad_y, int chunks, void* ws,
+                                     size_t ws_bytes, void* stream);
 
 /* Synchronizes `stream`, then reports (and clears) the device status word kept
  * in `ws`: SDTW_OK, or SDTW_ERR_TIMEOUT when a DP kernel gave up waiting for a

@@ -152,3 +152,34 @@ def test_cosine_schedule_values():
     assert cosine_lr(51, 100, 0.1, 0.0) == pytest.approx(0.05)                # halfway: the mean
     assert cosine_lr(101, 100, 0.1, 0.01) == pytest.approx(0.01)              # ends at lr_min
     assert all(cosine_lr(t, 100, 0.1) >= cosine_lr(t + 1, 100, 0.1) for t in range(1, 100))
+
+
+def test_host_batch_workspace_and_validation(lib):
+    from differentiable_series_alignment_gb300 import _lib as L
+    B, N, M, D = 32, 512, 512, 64
+    io = 4 * (2 * B * N * D + 2 * B * M * D + 2 * B)      # x, y, grad_x, grad_y, grad_loss, loss
+    for mode in (L.UNFUSED, L.FUSED):
+        w4 = L.sdtw_host_workspace_bytes(B, N, M, D, mode, 4)
+        per_chunk = L.sdtw_workspace_bytes(L.OP_FWD_BWD, B // 4, N, M, D, mode)
+        assert w4 >= io + 4 * per_chunk
+        assert w4 < io + 4 * per_chunk + 16 * 4096
+        assert L.sdtw_host_workspace_bytes(B, N, M, D, mode, 0) == L.sdtw_host_workspace_bytes(B, N, M, D, mode, 2)
+        assert L.sdtw_host_workspace_bytes(B, N, M, D, mode, 99) == L.sdtw_host_workspace_bytes(B, N, M, D, mode, 8)
+        # chunks never exceed the batch; uneven chunks are sized for the largest
+        assert L.sdtw_host_workspace_bytes(3, N, M, D, mode, 8) == L.sdtw_host_workspace_bytes(3, N, M, D, mode, 3)
+        w5 = L.sdtw_host_workspace_bytes(5, N, M, D, mode, 2)
+        assert w5 >= 2 * L.sdtw_workspace_bytes(L.OP_FWD_BWD, 3, N, M, D, mode)
+    assert L.sdtw_host_workspace_bytes(0, N, M, D, L.UNFUSED, 4) == 0
+    assert L.sdtw_host_workspace_bytes(B, N, M, 0, L.UNFUSED, 4) == 0
+    vp = ctypes.c_void_p
+    ok = dict(x=vp(0x1000), y=vp(0x2000), g=vp(0x3000), B=2, N=3, M=4, D=2, gamma=1.0, mode=0, loss=vp(0x4000),
+              gx=vp(0x5000), gy=vp(0x6000), chunks=2, ws=vp(0x100000), n=1 << 40)
+    keys = ("x", "y", "g", "B", "N", "M", "D", "gamma", "mode", "loss", "gx", "gy", "chunks", "ws", "n")
+    call = lambda **kw: lib.sdtw_value_and_grad_host(*[dict(ok, **kw)[k] for k in keys], None)
+    # every case fails in host-side validation, before any CUDA call
+    assert call(B=0) == 3 and call(D=0) == 3             # SDTW_ERR_EMPTY
+    assert call(gamma=0.0) == 2                          # SDTW_ERR_GAMMA
+    assert call(x=None) == 1 and call(loss=None) == 1    # SDTW_ERR_ARG
+    assert call(g=None) == 1                             # gradients asked for without grad_loss
+    assert call(mode=4) == 1
+    assert call(ws=None) == 5 and call(ws=vp(0x100008)) == 5 and call(n=64) == 5   # SDTW_ERR_WORKSPACE

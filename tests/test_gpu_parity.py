@@ -448,6 +448,51 @@ def test_barycenter_driver_schedule_clipping_and_early_stopping():
 
 # --------------------------------------------------------------------------- device status
 
+@pytest.mark.parametrize("mname,mode", MODES)
+@pytest.mark.parametrize("B,chunks", [(5, 3), (1, 4), (7, 8)])
+def test_host_batch_matches_oracle_and_device_path(mname, mode, B, chunks):
+    """Host buffers in, host buffers out, the batch cut into uneven chunks on side
+    streams: the same losses and gradients as the oracle and the device-buffer path."""
+    L = _lib()
+    N, M, D, gamma = 100, 77, 8, 0.8
+    x, y = synth.iid_normal_pair(B, N, M, D, 77, repeat=B * 10 + chunks)
+    w = (np.arange(B) % 3 - 1.0 + 0.5) / 32           # mixed-sign batch-scale weights
+    xh, yh = torch.from_numpy(x).pin_memory(), torch.from_numpy(y).pin_memory()
+    gl = torch.from_numpy(w.astype(np.float32)).pin_memory()
+    loss = torch.full((B,), float("nan")).pin_memory()
+    gx, gy = torch.full_like(xh, float("nan")).pin_memory(), torch.full_like(yh, float("nan")).pin_memory()
+    ws = L.host_workspace(B, N, M, D, mode, chunks)
+    L.sdtw_value_and_grad_host(xh, yh, gl, gamma, mode, loss, gx, gy, chunks, ws)
+    assert L.sdtw_last_device_status(ws) == 0
+    ol, ogx, ogy = oracle.batch(x, y, gamma, grad_loss=w)
+    assert_close(loss.numpy(), ol, LOSS_RTOL, 0.0, f"host batch {mname} loss")
+    assert_close(gx.numpy(), ogx, GRAD_RTOL, GRAD_ATOL, f"host batch {mname} grad_x")
+    assert_close(gy.numpy(), ogy, GRAD_RTOL, GRAD_ATOL, f"host batch {mname} grad_y")
+    dev = run_cuda(x, y, gamma, mode, grad_loss=w)
+    assert_close(loss.numpy(), dev["loss"], 1e-6, 0.0, f"host batch {mname} loss vs device path")
+    assert np.array_equal(gx.numpy(), dev["gx"].astype(np.float32))
+    assert np.array_equal(gy.numpy(), dev["gy"].astype(np.float32))
+
+
+def test_host_batch_high_level_function_and_loss_only():
+    from differentiable_series_alignment_gb300 import value_and_grad_host
+    L = _lib()
+    B, N, M, D = 6, 64, 48, 5
+    x, y = synth.iid_normal_pair(B, N, M, D, 78)
+    loss, gx, gy = value_and_grad_host(torch.from_numpy(x), torch.from_numpy(y), gamma=1.0, fused=True,
+                                       grad_loss=torch.full((B,), 1.0 / B), chunks=4)
+    ol, ogx, ogy = oracle.batch(x, y, 1.0, grad_loss=np.full(B, 1.0 / B))
+    assert_close(loss.numpy(), ol, LOSS_RTOL, 0.0, "value_and_grad_host loss")
+    assert_close(gx.numpy(), ogx, GRAD_RTOL, GRAD_ATOL, "value_and_grad_host grad_x")
+    assert_close(gy.numpy(), ogy, GRAD_RTOL, GRAD_ATOL, "value_and_grad_host grad_y")
+    # loss only: no gradients asked for, grad_loss may be absent
+    ws = L.host_workspace(B, N, M, D, L.UNFUSED, 2)
+    lo = torch.empty(B).pin_memory()
+    L.sdtw_value_and_grad_host(torch.from_numpy(x), torch.from_numpy(y), None, 1.0, L.UNFUSED, lo, None, None, 2, ws)
+    assert L.sdtw_last_device_status(ws) == 0
+    assert_close(lo.numpy(), ol, LOSS_RTOL, 0.0, "host batch loss only")
+
+
 def test_withheld_ready_flag_times_out_and_recovers():
     L = _lib()
     x, y = synth.iid_normal_pair(2, 160, 40, 3, 98)
