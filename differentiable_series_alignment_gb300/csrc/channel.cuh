@@ -12,12 +12,15 @@ constexpr unsigned kFull = 0xffffffffu;
 // L2 round trip between the producer's store and the consumer noticing it.
 constexpr unsigned kPollEvery = 32;
 
-// Bounded wait on a shared-memory counter (back-pressure of a ring). Warp-uniform result.
-static __device__ __forceinline__ bool wait_smem(const volatile int* cnt, int target, const WaveParams& q) {
+// Bounded wait on a shared-memory counter (back-pressure of a ring). `seen` gets
+// the count observed, so the caller can skip the next checks while its target
+// stays at or below it. Warp-uniform result.
+static __device__ __forceinline__ bool wait_smem(const volatile int* cnt, int target, const WaveParams& q, int& seen) {
     bool ok = true;
-    if (*cnt < target) {
+    int c = *cnt;
+    if (c < target) {
         unsigned long long t0 = 0;
-        for (unsigned it = 1; *cnt < target; ++it) {
+        for (unsigned it = 1; (c = *cnt) < target; ++it) {
             if ((it % kPollEvery) == 0) {
                 if (t0 == 0) t0 = global_ns();
                 if (ld_volatile_global(q.status) != 0) { ok = false; break; }
@@ -26,6 +29,7 @@ static __device__ __forceinline__ bool wait_smem(const volatile int* cnt, int ta
             }
         }
     }
+    seen = __shfl_sync(kFull, c, 0);
     return __shfl_sync(kFull, ok, 0);
 }
 

@@ -244,8 +244,11 @@ struct __align__(8) Slot {
     float v;
     unsigned tag;
 };
+// A slot publishes one value and nothing else, so its store needs no ordering
+// against other memory operations of the producer (no "memory" clobber): the
+// consumer reads only the slot itself and accepts it once the tag matches.
 __device__ __forceinline__ void slot_store(Slot* p, float v, unsigned tag) {
-    asm volatile("st.volatile.v2.b32 [%0], {%1, %2};" ::"l"(p), "f"(v), "r"(tag) : "memory");
+    asm volatile("st.volatile.v2.b32 [%0], {%1, %2};" ::"l"(p), "f"(v), "r"(tag));
 }
 __device__ __forceinline__ Slot slot_load(const Slot* p) {
     Slot s;

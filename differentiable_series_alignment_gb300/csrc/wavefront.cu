@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(co
 #pragma unroll
             for (int u = 0; u < kGroup; ++u) dbuf[u] = dp[(long long)u * 32];
         }
+        int cons_seen = 0;  // last count read from the next warp's consumption counter
         const int nG = T / kGroup;
         for (int g = 0; g < nG; ++g) {
             const int s0 = g * kGroup;
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(co
             }
             if (ok && has_bot && !bot_global) {
                 const int need = s0 + kGroup - 31 - kRing;  // ring slots this group overwrites are free
-                if (need > 0) ok = wait_smem(&cons[warp], need, q);
+                if (need > cons_seen) ok = wait_smem(&cons[warp], need, q, cons_seen);
             }
             if (!ok) break;
 
@@ -318,8 +319,11 @@ __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(co
 // EXT: the extended forward stored the three transition log2-probabilities of
 // each cell (float4: diag, left, up); otherwise the (vl, hu) pair from which
 // they are recomputed.
-template <bool ACC, bool EXT>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams q)
+// MAXT: the block size the kernel is compiled for. Strips of at most 8 warps take
+// the 256-thread build, whose register budget holds the prefetched state of a
+// whole group without spilling.
+template <bool ACC, bool EXT, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1) bwd_kernel(const WaveParams q)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int W = q.W;
@@ -378,6 +382,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
     VT buf[kGroup];
 #pragma unroll
     for (int u = 0; u < kGroup; ++u) buf[u] = vhp[(long long)(T - 1 - u) * 32];
+    int cons_seen = 0;  // last count read from the next warp's consumption counter
     const int nG = T / kGroup;
     for (int g = 0; g < nG; ++g) {
         const int t0 = g * kGroup;   // first reverse step of the group
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) bwd_kernel(const WaveParams
         }
         if (ok && has_above && !above_global) {
             const int need = k0 + kGroup - 31 - kRing;
-            if (need > 0) ok = wait_smem(&cons[warp], need, q);
+            if (need > cons_seen) ok = wait_smem(&cons[warp], need, q, cons_seen);
         }
         if (!ok) break;
 
@@ -548,8 +553,12 @@ cudaError_t launch_backward(WaveParams q, cudaStream_t st)
         kern<<<grid, q.W * 32, smem, st>>>(q);
         return cudaGetLastError();
     };
-    if (q.ext) return go(bwd_kernel<true, true>);
-    return q.accurate ? go(bwd_kernel<true, false>) : go(bwd_kernel<false, false>);
+    if (q.W <= 8) {
+        if (q.ext) return go(bwd_kernel<true, true, 256>);
+        return q.accurate ? go(bwd_kernel<true, false, 256>) : go(bwd_kernel<false, false, 256>);
+    }
+    if (q.ext) return go(bwd_kernel<true, true, kMaxWarps * 32>);
+    return q.accurate ? go(bwd_kernel<true, false, kMaxWarps * 32>) : go(bwd_kernel<false, false, kMaxWarps * 32>);
 }
 
 }  // namespace sdtw

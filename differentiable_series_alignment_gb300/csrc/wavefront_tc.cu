@@ -212,6 +212,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
 
             float h_prev = 0.f, v_prev = 0.f;
             bool tc_ok = true;
+            int cons_seen = 0;  // last count read from the next warp's consumption counter
             const int nG = T / kGroup;
             for (int g = 0; g < nG; ++g) {
                 const int s0 = g * kGroup;
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                 }
                 if (ok && has_bot && !bot_global) {
                     const int need = s0 + kGroup - 31 - kRing;  // ring slots this group overwrites are free
-                    if (need > 0) ok = wait_smem(&cons[warp], need, q);
+                    if (need > cons_seen) ok = wait_smem(&cons[warp], need, q, cons_seen);
                 }
                 if (!ok) break;
 

@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
         }
 
         dd h_prev = zero, v_prev = zero;
+        int cons_seen = 0;  // last count read from the next warp's consumption counter
         const int nG = T / kGroup;
         for (int g = 0; g < nG; ++g) {
             const int s0 = g * kGroup;
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
             }
             if (ok && has_bot && !bot_global) {
                 const int need = s0 + kGroup - 31 - kRing;
-                if (need > 0) ok = wait_smem(&cons[warp], need, q);
+                if (need > cons_seen) ok = wait_smem(&cons[warp], need, q, cons_seen);
             }
             if (!ok) break;
 
