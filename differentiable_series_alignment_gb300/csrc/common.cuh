@@ -250,6 +250,13 @@ struct __align__(8) Slot {
 __device__ __forceinline__ void slot_store(Slot* p, float v, unsigned tag) {
     asm volatile("st.volatile.v2.b32 [%0], {%1, %2};" ::"l"(p), "f"(v), "r"(tag));
 }
+// slot_store under a per-lane predicate, as one predicated instruction: a branch
+// around the store would diverge (one lane publishes) in every DP step.
+__device__ __forceinline__ void slot_store_if(bool pred, Slot* p, float v, unsigned tag) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t@q st.volatile.v2.b32 [%0], {%1, %2};\n\t}"
+        ::"l"(p), "f"(v), "r"(tag), "r"((unsigned)pred));
+}
 __device__ __forceinline__ Slot slot_load(const Slot* p) {
     Slot s;
     asm volatile("ld.volatile.v2.b32 {%0, %1}, [%2];" : "=f"(s.v), "=r"(s.tag) : "l"(p) : "memory");

@@ -265,14 +265,17 @@ __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(co
                 const float tt = (d + lo) - lz;
                 // first column / first row: a single predecessor (R borders are +inf)
                 const bool col0 = (j == 0);
-                const float h = col0 ? -kBig : (row0_lane ? d : tt - vl);
-                const float v = row0_lane ? -kBig : (col0 ? d : tt - hu);
+                // border values picked off the dependency chain: one select follows tt
+                const bool border = col0 || row0_lane;
+                const float hb = col0 ? -kBig : d, vb = row0_lane ? -kBig : d;
+                const float h = border ? hb : tt - vl;
+                const float v = border ? vb : tt - hu;
                 const float svl = col0 ? kBig : (row0_lane ? -kBig : vl);
                 const float shu = row0_lane ? kBig : (col0 ? -kBig : hu);
                 c0 = col0 ? d : c0;
                 vhp[(long long)s * 32] = make_float2(svl, shu);
                 const bool valid = (unsigned)j < (unsigned)M;
-                if (chan_lane && valid) slot_store(chan_out + (j & chan_mask), h, (unsigned)(j + 1));
+                slot_store_if(chan_lane && valid, chan_out + (j & chan_mask), h, (unsigned)(j + 1));
                 if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = h;
                 h_prev = h;
                 v_prev = v;
@@ -435,10 +438,12 @@ __global__ void __launch_bounds__(MAXT, 1) bwd_kernel(const WaveParams q)
             const float rds = __shfl_down_sync(kFull, sd, 1);
             const float bx = __shfl_sync(kFull, botv.x, u);
             const float by = __shfl_sync(kFull, botv.y, u);
-            const float ru = (lane == 31) ? bx : rs;   // msg_up from (i+1, j)
             const float rd = (lane == 31) ? by : rds;  // msg_diag from (i+1, j), used next step
             const float a1 = (j < Mb - 1) ? ml : -kBig;                    // from (i, j+1)
-            const float a2 = last_lane ? -kBig : ru;                       // from (i+1, j)
+            // from (i+1, j): msg_up of the row below (lane 31: from the next warp), none
+            // past the last row; one select follows the shuffle
+            const bool a2k = last_lane || lane == 31;
+            const float a2 = a2k ? (last_lane ? -kBig : bx) : rs;
             const float a3 = (last_lane || j >= Mb - 1) ? -kBig : rd_hold; // from (i+1, j+1)
             rd_hold = rd;
             float lo, mid, hi;
@@ -470,11 +475,12 @@ __global__ void __launch_bounds__(MAXT, 1) bwd_kernel(const WaveParams q)
             sd = lE + wd;
             // cells outside this problem's own N_b x M_b block carry no alignment
             ep[(long long)t * 32] = (row_in && (unsigned)j < (unsigned)Mb) ? ex2(lE) : 0.f;
-            if (chan_lane && (unsigned)j < (unsigned)M) {
+            {
+                const bool pub = chan_lane && (unsigned)j < (unsigned)M;
                 const int k = M - 1 - j;
                 Slot* dst = chan_out + 2 * (k & chan_mask);
-                slot_store(dst, su, (unsigned)(k + 1));
-                slot_store(dst + 1, sd, (unsigned)(k + 1));
+                slot_store_if(pub, dst, su, (unsigned)(k + 1));
+                slot_store_if(pub, dst + 1, sd, (unsigned)(k + 1));
             }
         }
 

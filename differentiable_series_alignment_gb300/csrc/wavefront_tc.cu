@@ -278,14 +278,17 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                     const float lz = dp_log2<ACC>((1.f + dp_exp2<ACC>(lo - mid)) + dp_exp2<ACC>(lo - hi));
                     const float tt = (d + lo) - lz;
                     const bool col0 = (j == 0);
-                    const float h = col0 ? -kBig : (row0_lane ? d : tt - vl);
-                    const float v = row0_lane ? -kBig : (col0 ? d : tt - hu);
+                    // border values picked off the dependency chain: one select follows tt
+                    const bool border = col0 || row0_lane;
+                    const float hb = col0 ? -kBig : d, vb = row0_lane ? -kBig : d;
+                    const float h = border ? hb : tt - vl;
+                    const float v = border ? vb : tt - hu;
                     const float svl = col0 ? kBig : (row0_lane ? -kBig : vl);
                     const float shu = row0_lane ? kBig : (col0 ? -kBig : hu);
                     c0 = col0 ? d : c0;
                     vhp[(long long)s * 32] = make_float2(svl, shu);
                     const bool valid = (unsigned)j < (unsigned)M;
-                    if (chan_lane && valid) slot_store(chan_out + (j & chan_mask), h, (unsigned)(j + 1));
+                    slot_store_if(chan_lane && valid, chan_out + (j & chan_mask), h, (unsigned)(j + 1));
                     if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = h;
                     h_prev = h;
                     v_prev = v;
