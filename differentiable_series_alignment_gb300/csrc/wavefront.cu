@@ -180,24 +180,36 @@ __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(co
         if (top_global && lane < kGroup && lane < M) nxt[0] = slot_load(edge_in + lane);
 
         float h_prev = 0.f, v_prev = 0.f;
-        // raw costs of the next group of steps (loaded one group ahead)
-        float dbuf[kGroup];
-        if (!FUSED) {
+        // Raw costs: a group's 16 skewed slot rows of this warp are one contiguous 2 KB
+        // block; it is copied one group ahead into a per-warp double buffer in shared
+        // memory with cp.async (no register scoreboard stays pending across the DP
+        // steps), then read into registers at the start of its group.
+        float* dsm = FUSED ? nullptr : reinterpret_cast<float*>(smem_raw + q.smem_fixed) + warp * 2 * kGroup * 32;
+        const float* dwarp = FUSED ? nullptr : dp - lane;
+        auto stage_costs = [&](int g) {  // group g -> buffer g & 1, 64 bytes per lane
+            float* dst = dsm + (g & 1) * kGroup * 32 + lane * 16;
+            const float* src = dwarp + (long long)g * kGroup * 32 + lane * 16;
 #pragma unroll
-            for (int u = 0; u < kGroup; ++u) dbuf[u] = dp[(long long)u * 32];
-        }
+            for (int c = 0; c < 4; ++c) cp_async16(dst + 4 * c, src + 4 * c);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        if (!FUSED) stage_costs(0);
         int cons_seen = 0;  // last count read from the next warp's consumption counter
         const int nG = T / kGroup;
         for (int g = 0; g < nG; ++g) {
             const int s0 = g * kGroup;
             float dcur[kGroup];
-            if (!FUSED) {  // this group's raw costs; the next group's loads go out now
-#pragma unroll
-                for (int u = 0; u < kGroup; ++u) dcur[u] = dbuf[u];
+            if (!FUSED) {  // the next group's copy goes out, then this group's costs are read
                 if (g + 1 < nG) {
-#pragma unroll
-                    for (int u = 0; u < kGroup; ++u) dbuf[u] = dp[(long long)(s0 + kGroup + u) * 32];
+                    stage_costs(g + 1);
+                    asm volatile("cp.async.wait_group 1;" ::: "memory");
+                } else {
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");
                 }
+                __syncwarp();
+                const float* cur = dsm + (g & 1) * kGroup * 32 + lane;
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u) dcur[u] = cur[u * 32];
             }
             if (FUSED && (s0 & 31) == 0) {
                 // New period s0/32: the y rows of tile s0/32 + 1 (costed during this
@@ -530,6 +542,7 @@ cudaError_t launch_forward(WaveParams q, bool fused, cudaStream_t st)
     q.smem_fixed = (int)wave_smem_fixed(q.W, false);
     size_t smem = q.smem_fixed;
     if (fused) smem += (size_t)q.W * wave_smem_fused_per_warp(q.D);
+    else smem += (size_t)q.W * 2 * kGroup * 32 * sizeof(float);  // staged raw costs
     smem = max(smem, wave_smem_floor());
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
