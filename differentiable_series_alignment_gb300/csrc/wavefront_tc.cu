@@ -48,10 +48,16 @@ size_t wave_tc_smem(int D)
 {
     const int KB = (D + 31) / 32;
     return wave_smem_fixed(kDpWarps, false) + 1024 + 2 * (size_t)KB * kABlock + (size_t)kRB * KB * 2 * kBHalf +
-           (size_t)kDpWarps * 64 * 32 * sizeof(float);
+           (size_t)kDpWarps * (64 + 2) * 32 * sizeof(float);
 }
 
 namespace {
+
+// 4-byte asynchronous global -> shared copy (completion: cp.async.wait_group).
+__device__ __forceinline__ void cp_async4(float* dst, const float* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
 
 template <bool ACC>
 __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
@@ -89,6 +95,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     unsigned char* a_lo = base + KB * kABlock;
     unsigned char* bring = base + 2 * KB * kABlock;               // [kRB][KB][hi 32 rows | lo 32 rows]
     float* dts = reinterpret_cast<float*>(bring + kRB * KB * 2 * kBHalf);
+    float* nys = dts + W * 64 * 32;                                // [W][2][32] y norms of the next tiles
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&s_a), 1);
@@ -193,7 +200,14 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
         float* dt = dts + warp * 64 * 32;  // [64][32] raw cost, slot (col & 63), lane
         const float nx = xnorm[(size_t)p * Npad + i];
         const float* nyp = ynorm + (size_t)p * Mpad;
+        // the 32 y norms of a cost tile reach shared memory one period ahead (cp.async),
+        // so no global load is waited for at the start of a period
+        float* nyw = nys + warp * 2 * 32;
         const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
+        if (active) {
+            cp_async4(nyw + lane, nyp + lane);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
 
         if (active) {
             const long long sk = skew_index(N, M, p, rb, 0, lane);
@@ -229,7 +243,13 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                     fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&s_tfree[t]));
-                    const float nyv = nyp[32 * c + lane];
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                    __syncwarp();
+                    const float nyv = nyw[(c & 1) * 32 + lane];
+                    if (c + 1 < nT) {  // its buffer was last read in period c - 1
+                        cp_async4(nyw + ((c + 1) & 1) * 32 + lane, nyp + 32 * (c + 1) + lane);
+                        asm volatile("cp.async.commit_group;" ::: "memory");
+                    }
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const float ny = __shfl_sync(kFull, nyv, u);
@@ -296,6 +316,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
 
                 if (has_top && !top_global && lane == 0) cons[warp - 1] = min(s0 + kGroup, M);
             }
+            asm volatile("cp.async.wait_all;" ::: "memory");  // none in flight past an early exit
         }
     }
 
