@@ -5,7 +5,8 @@ baseline may import this package. The CUDA library never calls it and shares no
 code with it. The arithmetic lives in ``sdtw_oracle.c`` (plain C, double
 precision); this module compiles it with gcc on first use and wraps it with
 ctypes. Inputs are converted to float64 exactly (float32 -> float64 is exact),
-so the oracle sees the very values the CUDA path sees.
+so the oracle sees the very values the CUDA path sees. ``normalized_unequal``
+composes three ``batch`` calls in Python (its definition, term by term).
 """
 from __future__ import annotations
 
@@ -147,6 +148,26 @@ def normalized(x, y, gamma, grad_loss=None, nthreads=0):
     if rc != 0:
         raise ValueError("oracle_normalized: bad argument or allocation failure")
     return loss, gx, gy
+
+
+def normalized_unequal(x, y, gamma, grad_loss=None, nthreads=0):
+    """Normalized Soft-DTW of pairs whose sequences differ in length, x (B,N,D) and
+    y (B,M,D): the definition of the SoftDTW README's "Normalization" section,
+    s(x,y) - (s(x,x) + s(y,y))/2, applied unchanged to N != M, with the three
+    terms from `batch`:
+        grad_x = g [gx(x,y) - (gx(x,x) + gy(x,x))/2]
+        grad_y = g [gy(x,y) - (gx(y,y) + gy(y,y))/2]
+    (x sits in both slots of s(x,x), so both of its gradients count)."""
+    x, y = _f64(x), _f64(y)
+    if x.ndim != 3 or y.ndim != 3 or x.shape[0] != y.shape[0] or x.shape[2] != y.shape[2]:
+        raise ValueError("x must be (B,N,D) and y (B,M,D)")
+    lxy, gxy_x, gxy_y = batch(x, y, gamma, grad_loss=grad_loss, nthreads=nthreads)
+    lxx, gxx_x, gxx_y = batch(x, x, gamma, grad_loss=grad_loss, nthreads=nthreads)
+    lyy, gyy_x, gyy_y = batch(y, y, gamma, grad_loss=grad_loss, nthreads=nthreads)
+    loss = lxy - 0.5 * (lxx + lyy)
+    if grad_loss is None:
+        return loss, None, None
+    return loss, gxy_x - 0.5 * (gxx_x + gxx_y), gxy_y - 0.5 * (gyy_x + gyy_y)
 
 
 def barycenter_step(z, m, v, t, X, gamma, lr=0.1, beta1=0.9, beta2=0.999, eps=1e-8, nthreads=0,

@@ -323,6 +323,63 @@ def test_normalized_matches_three_separate_values():
         assert loss[b] == pytest.approx(expect, rel=1e-10, abs=1e-10)
 
 
+def test_unequal_normalized_reduces_to_the_equal_length_oracle():
+    # at N == M the composed definition must agree with the C oracle's own normalized
+    g = np.random.default_rng(40)
+    x = g.standard_normal((3, 9, 2))
+    y = g.standard_normal((3, 9, 2))
+    w = np.array([0.5, -1.0, 2.0])
+    l1, gx1, gy1 = oracle.normalized(x, y, 0.8, grad_loss=w)
+    l2, gx2, gy2 = oracle.normalized_unequal(x, y, 0.8, grad_loss=w)
+    np.testing.assert_allclose(l2, l1, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(gx2, gx1, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(gy2, gy1, rtol=1e-10, atol=1e-12)
+
+
+def test_unequal_normalized_values_by_brute_force():
+    g = np.random.default_rng(41)
+    x = g.standard_normal((2, 6, 3))
+    y = g.standard_normal((2, 4, 3))
+    loss, _, _ = oracle.normalized_unequal(x, y, 0.6)
+    for b in range(2):
+        s = lambda a, c: _brute(_cost(a, c), 0.6)[0]
+        expect = s(x[b], y[b]) - 0.5 * (s(x[b], x[b]) + s(y[b], y[b]))
+        assert loss[b] == pytest.approx(expect, rel=1e-10, abs=1e-10)
+
+
+def test_unequal_normalized_is_symmetric_with_gradients_swapped():
+    g = np.random.default_rng(42)
+    x = g.standard_normal((2, 7, 2))
+    y = g.standard_normal((2, 4, 2))
+    w = np.array([1.0, -0.5])
+    l1, gx1, gy1 = oracle.normalized_unequal(x, y, 0.9, grad_loss=w)
+    l2, gx2, gy2 = oracle.normalized_unequal(y, x, 0.9, grad_loss=w)
+    np.testing.assert_allclose(l2, l1, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(gx2, gy1, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(gy2, gx1, rtol=1e-10, atol=1e-12)
+
+
+def test_unequal_normalized_gradient_matches_central_differences():
+    g = np.random.default_rng(43)
+    x = g.standard_normal((1, 5, 2))
+    y = g.standard_normal((1, 3, 2))
+    gamma = 0.7
+    _, gx, gy = oracle.normalized_unequal(x, y, gamma, grad_loss=[1.0])
+    h = 1e-6
+
+    def f(a, b):
+        return oracle.normalized_unequal(a, b, gamma)[0][0]
+
+    for arr, grad, first in ((x, gx, True), (y, gy, False)):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            p, m = arr.copy(), arr.copy()
+            p[idx] += h
+            m[idx] -= h
+            fd[idx] = ((f(p, y) - f(m, y)) if first else (f(x, p) - f(x, m))) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-8)
+
+
 # --------------------------------------------------------------------------- barycenter step
 
 def test_adam_first_step_moves_each_coordinate_by_lr_against_the_gradient():
