@@ -20,7 +20,8 @@ import math
 
 import torch
 
-from ._lib import (EXTENDED, FUSED, OP_BARYCENTER, OP_COST, OP_FWD_BWD, OP_NORMALIZED, UNFUSED, SdtwError,
+from ._lib import (EXTENDED, FUSED, OP_BARYCENTER, OP_COST, OP_FWD_BWD, OP_NORMALIZED, OP_NORMALIZED_UNEQUAL,
+                   UNFUSED, SdtwError, sdtw_normalized_unequal,
                    auto_precision, load, sdtw_backward, sdtw_backward_cost, sdtw_barycenter_step,
                    sdtw_backward_varlen, sdtw_barycenter_step_clipped, sdtw_debug_set_wait, sdtw_forward_varlen,
                    sdtw_distance, sdtw_forward, sdtw_forward_cost, sdtw_last_device_status, sdtw_normalized,
@@ -34,7 +35,7 @@ __all__ = [
     "sdtw_last_device_status", "cosine_lr", "sdtw_forward_varlen", "sdtw_backward_varlen",
     "sdtw_debug_set_wait", "UNFUSED", "FUSED", "EXTENDED", "OP_FWD_BWD", "OP_NORMALIZED", "OP_BARYCENTER",
     "OP_COST", "auto_precision", "value_and_grad_host", "host_workspace", "sdtw_host_workspace_bytes",
-    "sdtw_value_and_grad_host",
+    "sdtw_value_and_grad_host", "sdtw_normalized_unequal", "OP_NORMALIZED_UNEQUAL",
 ]
 
 
@@ -104,16 +105,27 @@ class _SoftDTWVarlenFn(torch.autograd.Function):
                 None if gy is None else gy.to(ctx.dtypes[1]), None, None, None, None)
 
 
+def _normalized_call(xc, yc, gamma, mode, loss, g, gx, gy):
+    """Equal lengths: one batch of 3B (sdtw_normalized); unequal: three batches of
+    their own shapes (sdtw_normalized_unequal)."""
+    B, N, D = xc.shape
+    M = yc.shape[1]
+    if N == M:
+        ws = workspace(OP_NORMALIZED, B, N, N, D, mode, xc.device)
+        sdtw_normalized(xc, yc, gamma, mode, loss, g, gx, gy, ws)
+    else:
+        ws = workspace(OP_NORMALIZED_UNEQUAL, B, N, M, D, mode, xc.device)
+        sdtw_normalized_unequal(xc, yc, gamma, mode, loss, g, gx, gy, ws)
+
+
 class _NormalizedFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, x, y, gamma, mode):
         xc, yc = _prep(x, "x"), _prep(y, "y")
-        if xc.shape != yc.shape:
-            raise ValueError("normalized Soft-DTW requires x.shape == y.shape")
-        B, N, D = xc.shape
-        loss = torch.empty(B, dtype=torch.float32, device=xc.device)
-        ws = workspace(OP_NORMALIZED, B, N, N, D, mode, xc.device)
-        sdtw_normalized(xc, yc, gamma, mode, loss, None, None, None, ws)
+        if xc.shape[0] != yc.shape[0] or xc.shape[2] != yc.shape[2]:
+            raise ValueError("normalized Soft-DTW needs x (B,N,D) and y (B,M,D)")
+        loss = torch.empty(xc.shape[0], dtype=torch.float32, device=xc.device)
+        _normalized_call(xc, yc, gamma, mode, loss, None, None, None)
         ctx.save_for_backward(xc, yc)
         ctx.gamma, ctx.mode = gamma, mode
         return loss
@@ -121,12 +133,10 @@ class _NormalizedFn(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad):
         xc, yc = ctx.saved_tensors
-        B, N, D = xc.shape
-        ws = workspace(OP_NORMALIZED, B, N, N, D, ctx.mode, xc.device)
         gx, gy = torch.empty_like(xc), torch.empty_like(yc)
-        loss = torch.empty(B, dtype=torch.float32, device=xc.device)
+        loss = torch.empty(xc.shape[0], dtype=torch.float32, device=xc.device)
         g = grad.detach().to(torch.float32).contiguous()
-        sdtw_normalized(xc, yc, ctx.gamma, ctx.mode, loss, g, gx, gy, ws)
+        _normalized_call(xc, yc, ctx.gamma, ctx.mode, loss, g, gx, gy)
         return gx, gy, None, None
 
 
@@ -170,8 +180,8 @@ class SoftDTW:
     """Per-pair Soft-DTW losses (B,), differentiable w.r.t. x and y.
 
     fused=False stores the (B,N,M) cost tensor; fused=True recomputes it inside
-    the DP kernels. normalize=True gives s(x,y) - (s(x,x) + s(y,y))/2 and needs
-    x.shape == y.shape. extended=None picks the double-float forward state for
+    the DP kernels. normalize=True gives s(x,y) - (s(x,x) + s(y,y))/2; x and y may
+    differ in length. extended=None picks the double-float forward state for
     small gamma, long sequences or D > 64 (auto_precision); True/False forces it.
     """
 
@@ -198,7 +208,7 @@ class SoftDTW:
             mode |= EXTENDED
         if x_lengths is not None or y_lengths is not None:
             if self.normalize:
-                raise ValueError("normalize=True takes equal-length sequences")
+                raise ValueError("normalize=True takes whole sequences, not a padded batch (x and y may differ in length)")
             return _SoftDTWVarlenFn.apply(x, y, x_lengths, y_lengths, self.gamma, mode)
         fn = _NormalizedFn if self.normalize else _SoftDTWFn
         return fn.apply(x, y, self.gamma, mode)

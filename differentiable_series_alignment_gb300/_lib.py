@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libsdtw.so")
 
 UNFUSED, FUSED = 0, 1
 EXTENDED = 2   # precision flag OR-ed into the mode (double-float forward state)
-OP_FWD_BWD, OP_NORMALIZED, OP_BARYCENTER, OP_COST = 0, 1, 2, 3
+OP_FWD_BWD, OP_NORMALIZED, OP_BARYCENTER, OP_COST, OP_NORMALIZED_UNEQUAL = 0, 1, 2, 3, 4
 
 STATUS_NAMES = {
     0: "SDTW_OK", 1: "SDTW_ERR_ARG", 2: "SDTW_ERR_GAMMA", 3: "SDTW_ERR_EMPTY", 4: "SDTW_ERR_SHAPE",
@@ -28,7 +28,8 @@ STATUS_NAMES = {
 EXPORTS = ("sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backward", "sdtw_normalized",
            "sdtw_barycenter_step", "sdtw_last_device_status", "sdtw_status_string", "sdtw_debug_set_wait",
            "sdtw_forward_noalloc", "sdtw_forward_cost", "sdtw_backward_cost", "sdtw_barycenter_step_clipped",
-           "sdtw_forward_varlen", "sdtw_backward_varlen", "sdtw_host_workspace_bytes", "sdtw_value_and_grad_host")
+           "sdtw_forward_varlen", "sdtw_backward_varlen", "sdtw_host_workspace_bytes", "sdtw_value_and_grad_host",
+           "sdtw_normalized_unequal")
 
 
 class SdtwError(RuntimeError):
@@ -61,6 +62,8 @@ def load(path: str = LIB_PATH):
         lib.sdtw_backward.restype = i
         lib.sdtw_normalized.argtypes = [vp, vp, i, i, i, f, i, vp, vp, vp, vp, vp, sz, vp]
         lib.sdtw_normalized.restype = i
+        lib.sdtw_normalized_unequal.argtypes = [vp, vp, i, i, i, i, f, i, vp, vp, vp, vp, vp, sz, vp]
+        lib.sdtw_normalized_unequal.restype = i
         lib.sdtw_barycenter_step.argtypes = [vp, vp, vp, i, vp, i, i, i, i, f, f, f, f, f, i, vp, vp, sz, vp]
         lib.sdtw_barycenter_step.restype = i
         lib.sdtw_last_device_status.argtypes = [vp, vp]
@@ -274,6 +277,15 @@ def sdtw_normalized(x, y, gamma, mode, loss, grad_loss, grad_x, grad_y, ws, stre
                                   _f32(loss, "loss"), _f32(grad_loss, "grad_loss"), _f32(grad_x, "grad_x"),
                                   _f32(grad_y, "grad_y"), _ptr(ws), ws.numel(), _stream(stream)),
            "sdtw_normalized")
+
+
+def sdtw_normalized_unequal(x, y, gamma, mode, loss, grad_loss, grad_x, grad_y, ws, stream=None):
+    B, N, D = x.shape
+    M = y.shape[1]
+    _check(load().sdtw_normalized_unequal(_f32(x, "x"), _f32(y, "y"), B, N, M, D, float(gamma), _mode(mode),
+                                          _f32(loss, "loss"), _f32(grad_loss, "grad_loss"), _f32(grad_x, "grad_x"),
+                                          _f32(grad_y, "grad_y"), _ptr(ws), ws.numel(), _stream(stream)),
+           "sdtw_normalized_unequal")
 
 
 def sdtw_barycenter_step(z, m, v, t, X, gamma, lr, beta1, beta2, eps, mode, loss_out, ws, stream=None):

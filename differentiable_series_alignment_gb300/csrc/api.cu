@@ -344,6 +344,38 @@ __global__ void gather_status_kernel(int* status, const char* ws0, size_t stride
     }
 }
 
+// Workspace of sdtw_normalized_unequal: the forward/backward workspaces of the
+// three batches s(x,y) (N x M), s(x,x) (N x N) and s(y,y) (M x M), in that order;
+// the first one's status word (offset 0) receives the OR of all three at the end.
+struct Norm3Layout {
+    Layout L[3];
+    size_t off[3], total;
+};
+
+bool make_norm3_layout(int B, int N, int M, int D, int mode, Norm3Layout* H)
+{
+    const int n[3] = {N, N, M}, m[3] = {M, N, M};
+    size_t o = 0;
+    for (int k = 0; k < 3; ++k) {
+        if (!make_layout(SDTW_OP_FWD_BWD, B, n[k], m[k], D, mode, &H->L[k])) return false;
+        H->off[k] = o;
+        o = align_up(o + H->L[k].total);
+    }
+    H->total = o;
+    return true;
+}
+
+__global__ void gather3_status_kernel(int* out, const int* s1, const int* s2)
+{
+    if (threadIdx.x == 0) *out = *out | *s1 | *s2;
+}
+
+__global__ void combine3_normalized_kernel(const float* lxy, const float* lxx, const float* lyy, int B, float* loss)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B) loss[b] = lxy[b] - 0.5f * (lxx[b] + lyy[b]);
+}
+
 // images_ready: when not null, the operand images were already launched on
 // another stream; the contractions wait on this event instead of building them.
 sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void* ws, const float* grad_loss,
@@ -397,6 +429,10 @@ extern "C" {
 
 size_t sdtw_workspace_bytes(int op, int B, int N, int M, int D, sdtw_mode mode)
 {
+    if (op == SDTW_OP_NORMALIZED_UNEQUAL) {
+        Norm3Layout H;
+        return make_norm3_layout(B, N, M, D, (int)mode, &H) ? H.total : 0;
+    }
     Layout L;
     if (!make_layout(op, B, N, M, D, (int)mode, &L)) return 0;
     return L.total;
@@ -598,6 +634,79 @@ sdtw_status sdtw_backward_cost(const float* C, int B, int N, int M, float gamma,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((s = run_backward(pr, L, ws, gamma, (int)mode, st)) != SDTW_OK) return s;
     SDTW_CUDA(launch_unskew_grad(at<float>(ws, L.e), B, N, M, grad_loss, grad_C, st));
+    return SDTW_OK;
+}
+
+sdtw_status sdtw_normalized_unequal(const float* x, const float* y, int B, int N, int M, int D, float gamma,
+                                    sdtw_mode mode, float* loss, const float* grad_loss, float* grad_x,
+                                    float* grad_y, void* ws, size_t ws_bytes, void* stream)
+{
+    sdtw_status s = check_common(x, y, B, N, M, D, gamma, (int)mode);
+    if (s != SDTW_OK) return s;
+    if (!loss) return SDTW_ERR_ARG;
+    Norm3Layout H;
+    if (!make_norm3_layout(B, N, M, D, (int)mode, &H)) return SDTW_ERR_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 || ws_bytes < H.total) return SDTW_ERR_WORKSPACE;
+    const bool grads = grad_loss && (grad_x || grad_y);
+    Problems pr[3] = {};
+    const float* xs[3] = {x, x, y};
+    const float* ys[3] = {y, x, y};
+    const long long xst[3] = {(long long)N * D, (long long)N * D, (long long)M * D};
+    const long long yst[3] = {(long long)M * D, (long long)N * D, (long long)M * D};
+    void* wsk[3];
+    for (int k = 0; k < 3; ++k) {
+        pr[k].xs[0] = xs[k]; pr[k].ys[0] = ys[k];
+        pr[k].xstride[0] = xst[k]; pr[k].ystride[0] = yst[k];
+        pr[k].B = B;
+        wsk[k] = at<char>(ws, H.off[k]);
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t cs[kMaxChunks];
+    if (!chunk_streams(cs)) return SDTW_ERR_CUDA;
+    // The three wavefront pairs are independent and latency-bound: they run side by
+    // side on three streams, each sized for a third of the SMs.
+    cudaEvent_t fork = nullptr;
+    SDTW_CUDA(cudaEventCreateWithFlags(&fork, cudaEventDisableTiming));
+    if (cudaEventRecord(fork, st) != cudaSuccess) {
+        cudaEventDestroy(fork);
+        return SDTW_ERR_CUDA;
+    }
+    const int prev_share = t_sm_share;
+    t_sm_share = num_sms() / 3 > 0 ? num_sms() / 3 : 1;
+    for (int k = 0; k < 3; ++k) {
+        if (s == SDTW_OK && cudaStreamWaitEvent(cs[k], fork, 0) != cudaSuccess) s = SDTW_ERR_CUDA;
+        if (s == SDTW_OK)
+            s = run_forward(pr[k], H.L[k], wsk[k], gamma, (int)mode, at<float>(wsk[k], H.L[k].losses), cs[k]);
+        if (s == SDTW_OK && grads) s = run_backward(pr[k], H.L[k], wsk[k], gamma, (int)mode, cs[k]);
+        cudaEvent_t join = nullptr;  // joined whatever happened, so later work stays ordered
+        if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+            if (s == SDTW_OK) s = SDTW_ERR_CUDA;
+            continue;
+        }
+        if ((cudaEventRecord(join, cs[k]) != cudaSuccess || cudaStreamWaitEvent(st, join, 0) != cudaSuccess) &&
+            s == SDTW_OK)
+            s = SDTW_ERR_CUDA;
+        cudaEventDestroy(join);
+    }
+    t_sm_share = prev_share;
+    cudaEventDestroy(fork);
+    if (s != SDTW_OK) return s;
+    combine3_normalized_kernel<<<(B + 255) / 256, 256, 0, st>>>(at<float>(wsk[0], H.L[0].losses),
+                                                                at<float>(wsk[1], H.L[1].losses),
+                                                                at<float>(wsk[2], H.L[2].losses), B, loss);
+    SDTW_CUDA(cudaGetLastError());
+    if (grads) {
+        // grad_x = g [gx(x,y) - (gx(x,x) + gy(x,x))/2];  grad_y = g [gy(x,y) - (gx(y,y) + gy(y,y))/2]
+        s = run_grads(pr[0], 0, B, H.L[0], wsk[0], grad_loss, 1.f, grad_x, grad_y, 0, (int)mode, st);
+        if (s == SDTW_OK && grad_x)
+            s = run_grads(pr[1], 0, B, H.L[1], wsk[1], grad_loss, -0.5f, grad_x, grad_x, 1, (int)mode, st);
+        if (s == SDTW_OK && grad_y)
+            s = run_grads(pr[2], 0, B, H.L[2], wsk[2], grad_loss, -0.5f, grad_y, grad_y, 1, (int)mode, st);
+        if (s != SDTW_OK) return s;
+    }
+    gather3_status_kernel<<<1, 32, 0, st>>>(at<int>(wsk[0], H.L[0].status), at<int>(wsk[1], H.L[1].status),
+                                            at<int>(wsk[2], H.L[2].status));
+    SDTW_CUDA(cudaGetLastError());
     return SDTW_OK;
 }
 

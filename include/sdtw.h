@@ -74,6 +74,7 @@ typedef enum {
 #define SDTW_OP_NORMALIZED 1 /* sdtw_normalized (N == M)                          */
 #define SDTW_OP_BARYCENTER 2 /* sdtw_barycenter_step: B = K sequences, N = T, M = T2 */
 #define SDTW_OP_COST 3       /* sdtw_forward_cost followed by sdtw_backward_cost; D is ignored */
+#define SDTW_OP_NORMALIZED_UNEQUAL 4 /* sdtw_normalized_unequal: x (B,N,D), y (B,M,D)     */
 
 /* Bytes of device workspace needed by `op` for these sizes and mode; 0 when the
  * arguments are invalid. Pure host function, no CUDA call. */
@@ -120,6 +121,21 @@ sdtw_status sdtw_backward_varlen(const float* x, const float* y, const int* x_le
 sdtw_status sdtw_normalized(const float* x, const float* y, int B, int N, int D, float gamma,
                             sdtw_mode mode, float* loss, const float* grad_loss, float* grad_x,
                             float* grad_y, void* ws, size_t ws_bytes, void* stream);
+
+/* Normalized Soft-DTW of sequences of different lengths, x (B,N,D) and y (B,M,D):
+ * the README's "Normalization" definition, loss[b] = s(x_b,y_b) - (s(x_b,x_b) +
+ * s(y_b,y_b)) / 2, applied unchanged to N != M (the README's own interface takes
+ * equal shapes only; this entry lifts that restriction). The three terms are three
+ * batches of different shapes (N x M, N x N, M x M) whose wavefronts run side by
+ * side on internal streams ordered against `stream`; N == M gives the same values
+ * as sdtw_normalized. Arguments as for sdtw_normalized: when grad_loss is non-NULL
+ * the input gradients are written (grad_x (B,N,D) and grad_y (B,M,D), either may
+ * be NULL). Workspace: sdtw_workspace_bytes(SDTW_OP_NORMALIZED_UNEQUAL, B, N, M, D,
+ * mode); its status word gathers the three batches' device status. */
+sdtw_status sdtw_normalized_unequal(const float* x, const float* y, int B, int N, int M, int D,
+                                    float gamma, sdtw_mode mode, float* loss, const float* grad_loss,
+                                    float* grad_x, float* grad_y, void* ws, size_t ws_bytes,
+                                    void* stream);
 
 /* One Adam step of a Soft-DTW barycenter (README, "Time Series Barycenters
  * (Averaging)"; review page, "proposed method", fifth bullet):

@@ -183,3 +183,24 @@ def test_host_batch_workspace_and_validation(lib):
     assert call(g=None) == 1                             # gradients asked for without grad_loss
     assert call(mode=4) == 1
     assert call(ws=None) == 5 and call(ws=vp(0x100008)) == 5 and call(n=64) == 5   # SDTW_ERR_WORKSPACE
+
+
+def test_unequal_normalized_workspace_and_validation(lib):
+    from differentiable_series_alignment_gb300 import _lib as L
+    B, N, M, D = 4, 100, 37, 8
+    for mode in (L.UNFUSED, L.FUSED, L.FUSED | L.EXTENDED):
+        w = L.sdtw_workspace_bytes(L.OP_NORMALIZED_UNEQUAL, B, N, M, D, mode)
+        parts = [L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, n, m, D, mode) for n, m in ((N, M), (N, N), (M, M))]
+        assert sum(parts) <= w <= sum(parts) + 3 * 256
+    assert L.sdtw_workspace_bytes(L.OP_NORMALIZED_UNEQUAL, 0, N, M, D, L.UNFUSED) == 0
+    assert L.sdtw_workspace_bytes(L.OP_NORMALIZED_UNEQUAL, B, N, 0, D, L.UNFUSED) == 0
+    vp = ctypes.c_void_p
+    ok = dict(x=vp(0x1000), y=vp(0x2000), B=2, N=5, M=3, D=2, g=1.0, mode=0, loss=vp(0x3000), gl=None, gx=None,
+              gy=None, ws=vp(0x100000), n=1 << 40)
+    keys = ("x", "y", "B", "N", "M", "D", "g", "mode", "loss", "gl", "gx", "gy", "ws", "n")
+    call = lambda **kw: lib.sdtw_normalized_unequal(*[dict(ok, **kw)[k] for k in keys], None)
+    # every case fails in host-side validation, before any CUDA call
+    assert call(M=0) == 3 and call(B=0) == 3              # SDTW_ERR_EMPTY
+    assert call(g=0.0) == 2                                # SDTW_ERR_GAMMA
+    assert call(y=None) == 1 and call(loss=None) == 1 and call(mode=8) == 1
+    assert call(ws=None) == 5 and call(ws=vp(0x100004)) == 5 and call(n=100) == 5

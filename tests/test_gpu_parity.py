@@ -284,6 +284,61 @@ def test_normalized_of_equal_inputs_is_zero():
     assert np.abs(gx).max() <= 1e-3 * gscale and np.abs(gy).max() <= 1e-3 * gscale
 
 
+def run_normalized_unequal(x, y, gamma, mode, gl):
+    L = _lib()
+    xt, yt = torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda()
+    B, N, D = x.shape
+    M = y.shape[1]
+    ws = L.workspace(L.OP_NORMALIZED_UNEQUAL, B, N, M, D, mode)
+    loss = torch.empty(B, device="cuda")
+    g = torch.tensor(np.asarray(gl, np.float32), device="cuda")
+    gx, gy = torch.empty_like(xt), torch.empty_like(yt)
+    L.sdtw_normalized_unequal(xt, yt, gamma, mode, loss, g, gx, gy, ws)
+    assert L.sdtw_last_device_status(ws) == 0
+    return loss.cpu().numpy().astype(np.float64), gx.cpu().numpy(), gy.cpu().numpy()
+
+
+@pytest.mark.parametrize("mname,mode", MODES + [("unfused+extended", 2), ("fused+extended", 3)])
+@pytest.mark.parametrize("N,M,D", [(100, 37, 8), (33, 130, 3), (1, 9, 2)])
+def test_unequal_normalized_matches_oracle(mname, mode, N, M, D):
+    x, y = synth.iid_normal_pair(3, N, M, D, 98, repeat=N * 1000 + M)
+    gl = np.array(WEIGHTS)
+    loss, gx, gy = run_normalized_unequal(x, y, 0.8, mode, gl)
+    ol, ogx, ogy = oracle.normalized_unequal(x, y, 0.8, grad_loss=gl)
+    sxx = oracle.batch(x, x, 0.8)[0]
+    syy = oracle.batch(y, y, 0.8)[0]
+    atol = 1e-4 * np.maximum(1.0, np.maximum(np.abs(sxx), np.abs(syy)))
+    assert np.all(np.abs(loss - ol) <= atol + LOSS_RTOL * np.abs(ol)), (loss, ol)
+    assert_close(gx, ogx, GRAD_RTOL, GRAD_ATOL, f"unequal normalized {mname} grad_x")
+    assert_close(gy, ogy, GRAD_RTOL, GRAD_ATOL, f"unequal normalized {mname} grad_y")
+
+
+@pytest.mark.parametrize("mname,mode", MODES)
+def test_unequal_normalized_at_equal_lengths_agrees_with_the_batched_entry(mname, mode):
+    x, y = synth.iid_normal_pair(4, 64, 64, 5, 99)
+    gl = [0.25, -0.5, 1.0, 0.125]
+    a = run_normalized(x, y, 0.9, mode, gl)
+    b = run_normalized_unequal(x, y, 0.9, mode, gl)
+    scale = np.abs(oracle.batch(x, x, 0.9)[0]).max()
+    assert np.abs(a[0] - b[0]).max() <= 1e-5 * max(1.0, scale)
+    for u, v in zip(a[1:], b[1:]):
+        assert np.abs(u - v).max() <= 1e-5 * max(1e-3, np.abs(u).max())
+
+
+def test_unequal_normalized_through_autograd():
+    from differentiable_series_alignment_gb300 import SoftDTW
+    x, y = synth.iid_normal_pair(2, 40, 70, 4, 100)
+    xt = torch.from_numpy(x).cuda().requires_grad_(True)
+    yt = torch.from_numpy(y).cuda().requires_grad_(True)
+    loss = SoftDTW(gamma=1.0, normalize=True, fused=True)(xt, yt)
+    (loss * torch.tensor([0.5, -1.0], device="cuda")).sum().backward()
+    ol, ogx, ogy = oracle.normalized_unequal(x, y, 1.0, grad_loss=[0.5, -1.0])
+    s = np.maximum(np.abs(oracle.batch(x, x, 1.0)[0]), np.abs(oracle.batch(y, y, 1.0)[0]))
+    assert np.all(np.abs(loss.detach().cpu().numpy() - ol) <= 1e-4 * np.maximum(1.0, s) + LOSS_RTOL * np.abs(ol))
+    assert_close(xt.grad.cpu().numpy(), ogx, GRAD_RTOL, 32 * GRAD_ATOL, "autograd unequal normalized grad_x")
+    assert_close(yt.grad.cpu().numpy(), ogy, GRAD_RTOL, 32 * GRAD_ATOL, "autograd unequal normalized grad_y")
+
+
 # --------------------------------------------------------------------------- barycenter
 
 @pytest.mark.parametrize("mname,mode", MODES)
