@@ -20,7 +20,7 @@ import math
 
 import torch
 
-from ._lib import (EXTENDED, FUSED, OP_BARYCENTER, OP_COST, OP_FWD_BWD, OP_NORMALIZED, OP_NORMALIZED_UNEQUAL,
+from ._lib import (CHECKPOINT, EXTENDED, FUSED, OP_BARYCENTER, OP_COST, OP_FWD_BWD, OP_NORMALIZED, OP_NORMALIZED_UNEQUAL,
                    UNFUSED, SdtwError, sdtw_normalized_unequal,
                    auto_precision, load, sdtw_backward, sdtw_backward_cost, sdtw_barycenter_step,
                    sdtw_backward_varlen, sdtw_barycenter_step_clipped, sdtw_debug_set_wait, sdtw_forward_varlen,
@@ -35,7 +35,7 @@ __all__ = [
     "sdtw_last_device_status", "cosine_lr", "sdtw_forward_varlen", "sdtw_backward_varlen",
     "sdtw_debug_set_wait", "UNFUSED", "FUSED", "EXTENDED", "OP_FWD_BWD", "OP_NORMALIZED", "OP_BARYCENTER",
     "OP_COST", "auto_precision", "value_and_grad_host", "host_workspace", "sdtw_host_workspace_bytes",
-    "sdtw_value_and_grad_host", "sdtw_normalized_unequal", "OP_NORMALIZED_UNEQUAL",
+    "sdtw_value_and_grad_host", "sdtw_normalized_unequal", "OP_NORMALIZED_UNEQUAL", "CHECKPOINT",
 ]
 
 
@@ -183,18 +183,25 @@ class SoftDTW:
     the DP kernels. normalize=True gives s(x,y) - (s(x,x) + s(y,y))/2; x and y may
     differ in length. extended=None picks the double-float forward state for
     small gamma, long sequences or D > 64 (auto_precision); True/False forces it.
+    checkpoint=True (fused, fp32, D <= 64, not normalized) keeps no per-cell forward
+    state: the backward recomputes it band by band (128 rows) from the boundary rows
+    the forward kept; the workspace holds one band, and the backward's time grows
+    with the number of bands.
     """
 
     def __init__(self, gamma: float = 1.0, dist: str = "sqeuclidean", fused: bool = False,
-                 normalize: bool = False, extended: bool | None = None):
+                 normalize: bool = False, extended: bool | None = None, checkpoint: bool = False):
         if dist != "sqeuclidean":
             raise ValueError("only dist='sqeuclidean' is supported")
         if not (gamma > 0):
             raise ValueError("gamma must be > 0")
+        if checkpoint and (not fused or normalize or extended):
+            raise ValueError("checkpoint=True needs fused=True, normalize=False and the fp32 state")
         self.gamma = float(gamma)
         self.fused = bool(fused)
         self.normalize = normalize
         self.extended = extended
+        self.checkpoint = bool(checkpoint)
 
     def __call__(self, x: torch.Tensor, y: torch.Tensor, x_lengths: torch.Tensor | None = None,
                  y_lengths: torch.Tensor | None = None) -> torch.Tensor:
@@ -202,7 +209,9 @@ class SoftDTW:
         aligns x[b, :x_lengths[b]] with y[b, :y_lengths[b]]; padded rows get zero
         gradient and must be finite."""
         mode = FUSED if self.fused else UNFUSED
-        if self.extended is None:
+        if self.checkpoint:
+            mode |= CHECKPOINT
+        elif self.extended is None:
             mode |= auto_precision(self.gamma, x.shape[1], y.shape[1], x.shape[2])
         elif self.extended:
             mode |= EXTENDED

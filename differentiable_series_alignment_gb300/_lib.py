@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libsdtw.so")
 
 UNFUSED, FUSED = 0, 1
 EXTENDED = 2   # precision flag OR-ed into the mode (double-float forward state)
+CHECKPOINT = 4  # with FUSED: no per-cell forward state kept, bands recomputed in the backward
 OP_FWD_BWD, OP_NORMALIZED, OP_BARYCENTER, OP_COST, OP_NORMALIZED_UNEQUAL = 0, 1, 2, 3, 4
 
 STATUS_NAMES = {
@@ -132,7 +133,7 @@ def _check(code: int, where: str):
 def _mode(mode) -> int:
     if isinstance(mode, str):
         return {"unfused": UNFUSED, "fused": FUSED, "unfused+extended": UNFUSED | EXTENDED,
-                "fused+extended": FUSED | EXTENDED}[mode]
+                "fused+extended": FUSED | EXTENDED, "fused+checkpoint": FUSED | CHECKPOINT}[mode]
     return int(mode)
 
 

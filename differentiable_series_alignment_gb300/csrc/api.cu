@@ -31,21 +31,34 @@ struct Layout {
     size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, gnorm, bimg, bimg2, total;
     size_t ximg, yimg, xnorm, ynorm;  // tensor-core cost operands (tc_cost)
     bool tc_cost;
+    bool ckpt;   // checkpointed fused mode: VH / E / the [X | 1] image hold one band
     int P, N, M, D, NB;
 };
+
+// Checkpointed fused mode: bands of kBandBlocks 32-row blocks (the fused forward's
+// 128-row strips). The forward keeps only each band's outgoing boundary row; the
+// backward recomputes one band at a time.
+constexpr int kBandBlocks = 4;
 
 bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
 {
     if (op < SDTW_OP_FWD_BWD || op > SDTW_OP_COST) return false;
     if (op == SDTW_OP_COST) D = 1;  // no features: the cost is given
     if (B < 1 || N < 1 || M < 1 || D < 1) return false;
-    if (mode & ~3) return false;
+    if (mode & ~7) return false;
     const bool fused = (mode & SDTW_FUSED) != 0, ext = (mode & SDTW_EXTENDED) != 0;
+    const bool ckpt = (mode & SDTW_CHECKPOINT) != 0;
     if (op == SDTW_OP_COST && fused) return false;
+    // checkpointing recomputes bands with the tensor-core fused forward (fp32, D <= 64)
+    if (ckpt && (op != SDTW_OP_FWD_BWD || !fused || ext || D > 64)) return false;
     const int P = (op == SDTW_OP_NORMALIZED) ? 3 * B : B;
     if (op == SDTW_OP_NORMALIZED) M = N;
     const int NB = (N + 31) / 32;
+    const int SB = (NB + kBandBlocks - 1) / kBandBlocks;   // bands (checkpointed mode)
     const size_t slots = (size_t)skew_slots(N, M) * P;
+    // per-cell state and E: every cell, or one band of every problem
+    const size_t vslots = ckpt ? (size_t)P * (NB < kBandBlocks ? NB : kBandBlocks) * skew_T(M) * 32 : slots;
+    const size_t edge_rows = ckpt ? (size_t)SB : (size_t)NB;   // boundary rows kept per problem
     size_t o = 0;
     L->status = o; o = align_up(o + sizeof(int));
     L->ctrl_f = o; L->ctrl_f_bytes = sizeof(int) * (1 + (size_t)P); o = align_up(o + L->ctrl_f_bytes);
@@ -54,17 +67,18 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->rowsum = o; o = align_up(o + sizeof(double) * (size_t)P);
     L->rowbuf = o; o = align_up(o + sizeof(float2) * (size_t)P * M);
     L->losses = o; o = align_up(o + sizeof(float) * (size_t)P);
-    L->edge_f = o; o = align_up(o + 2 * sizeof(Slot) * (size_t)P * NB * M);
-    L->edge_b = o; o = align_up(o + 2 * sizeof(Slot) * (size_t)P * NB * M);
-    L->vh = o; o = align_up(o + (ext ? sizeof(float4) : sizeof(float2)) * slots);
-    L->e = o; o = align_up(o + sizeof(float) * slots);
+    L->edge_f = o; o = align_up(o + 2 * sizeof(Slot) * (size_t)P * edge_rows * M);
+    L->edge_b = o; o = align_up(o + 2 * sizeof(Slot) * (size_t)P * edge_rows * M);
+    L->vh = o; o = align_up(o + (ext ? sizeof(float4) : sizeof(float2)) * vslots);
+    L->e = o; o = align_up(o + sizeof(float) * vslots);
     L->dsk = o; if (!fused) o = align_up(o + (ext ? sizeof(float2) : sizeof(float)) * slots);
     L->gparts = o; if (op == SDTW_OP_BARYCENTER) o = align_up(o + sizeof(float) * (size_t)P * N * D);
     L->gnorm = o; if (op == SDTW_OP_BARYCENTER) o = align_up(o + sizeof(float) * (((size_t)N * D + 255) / 256));
     // gradient operand images (one batch of B problems at a time): [Y | 1] and [X | 1]
     const bool xy = op != SDTW_OP_COST;  // the path has x and y (and input gradients)
     L->bimg = o; if (!ext && xy) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, M, D));
-    L->bimg2 = o; if (!ext && xy) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, N, D));
+    L->bimg2 = o;
+    if (!ext && xy) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, ckpt ? (N < 32 * kBandBlocks ? N : 32 * kBandBlocks) : N, D));
     // operand images and norms of the tensor-core costs (fp32 modes, D <= 64): the
     // unfused cost tensor and the fused forward's cost tiles
     L->tc_cost = !ext && D <= 64 && xy;
@@ -74,6 +88,7 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->ynorm = o; if (L->tc_cost) o = align_up(o + snorm_bytes(P, M));
     L->total = o;
     L->P = P; L->N = N; L->M = M; L->D = D; L->NB = NB;
+    L->ckpt = ckpt;
     return true;
 }
 
@@ -126,11 +141,17 @@ int num_sms()
 thread_local int t_sm_share = 0;
 int sm_budget() { return t_sm_share > 0 ? t_sm_share : num_sms(); }
 
-sdtw_status check_common(const void* x, const void* y, int B, int N, int M, int D, float gamma, int mode)
+// allow_ckpt: the entry point takes SDTW_CHECKPOINT (sdtw_forward / sdtw_backward and
+// their padded-batch forms), which needs the tensor-core fused forward.
+sdtw_status check_common(const void* x, const void* y, int B, int N, int M, int D, float gamma, int mode,
+                         bool allow_ckpt = false)
 {
     if (B < 1 || N < 1 || M < 1 || D < 1) return SDTW_ERR_EMPTY;
     if (!(gamma > 0.f) || !std::isfinite(gamma)) return SDTW_ERR_GAMMA;
-    if (mode & ~3) return SDTW_ERR_ARG;
+    if (mode & ~(allow_ckpt ? 7 : 3)) return SDTW_ERR_ARG;
+    if ((mode & SDTW_CHECKPOINT) && (!(mode & SDTW_FUSED) || (mode & SDTW_EXTENDED) || D > 64 ||
+                                     env_int("SDTW_FUSED_SIMT", 0) != 0))
+        return SDTW_ERR_ARG;
     if (!x || !y) return SDTW_ERR_ARG;
     if (B > 65535 / 3 || N > (1 << 24) || M > (1 << 24) || D > 400) return SDTW_ERR_TOO_LARGE;
     if ((mode & SDTW_FUSED) &&
@@ -229,11 +250,80 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
     q.loss = loss_out;
     q.skip_publish = g_skip_publish;
     g_skip_publish = 0;
+    if (L.ckpt) q.VH = nullptr;  // only the strips' boundary rows are kept (edge_f)
     if (fused && tc)
         SDTW_CUDA(launch_forward_tc(q, at<float>(ws, L.ximg), at<float>(ws, L.yimg), at<float>(ws, L.xnorm),
                                     at<float>(ws, L.ynorm), st));
     else
         SDTW_CUDA(launch_forward(q, fused, st));
+    return SDTW_OK;
+}
+
+// Checkpointed backward with gradients: for each band of kBandBlocks row blocks, from
+// the last band up, recompute the band's forward state from the boundary row the
+// forward kept above it, run the band's backward wavefront (its lower boundary
+// messages come from the band below, run just before), then the band's share of the
+// gradient contractions: its rows of grad_x, and its rows' terms of grad_y, which
+// accumulate over the bands.
+sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, float gamma, int mode,
+                              const float* grad_loss, float* grad_x, float* grad_y, cudaStream_t st,
+                              const int* lens_n, const int* lens_m)
+{
+    const int SB = (L.NB + kBandBlocks - 1) / kBandBlocks;
+    int* status = at<int>(ws, L.status);
+    WaveParams qb0 = wave_params(pr, L, ws, gamma, true, false, true);
+    if (SB > 1) SDTW_CUDA(cudaMemsetAsync(qb0.edge_b, 0, 2 * sizeof(Slot) * (size_t)L.P * SB * L.M, st));
+    GradParams g{};
+    g.pr = pr;
+    g.P = L.P; g.M = L.M; g.D = L.D;
+    g.E = at<float>(ws, L.e);
+    g.grad_loss = grad_loss;
+    g.wmod = L.P;
+    g.omod = L.P;
+    g.coef = 1.f;
+    float* img_rows = at<float>(ws, L.bimg);
+    float* img_cols = at<float>(ws, L.bimg2);
+    if (grad_x) {  // [Y | 1] does not depend on the band
+        g.N = L.N;
+        SDTW_CUDA(launch_bimg(g, img_rows, nullptr, st));
+    }
+    for (int k = SB - 1; k >= 0; --k) {
+        const int rb0 = k * kBandBlocks;
+        const int nb = L.NB - rb0 < kBandBlocks ? L.NB - rb0 : kBandBlocks;
+        const int row0 = 32 * rb0;
+        const int nrows = L.N - row0 < 32 * kBandBlocks ? L.N - row0 : 32 * kBandBlocks;
+        // 1. the band's forward state, from the kept boundary row above it
+        WaveParams qf = wave_params(pr, L, ws, gamma, true, false, false);
+        qf.W = kBandBlocks; qf.S = 1; qf.strip0 = k; qf.S_all = SB;
+        qf.vh_rb0 = rb0; qf.vh_nb = nb; qf.no_loss = 1;
+        qf.lens_n = lens_n; qf.lens_m = lens_m;
+        SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_f), 0, L.ctrl_f_bytes, st));
+        SDTW_CUDA(launch_forward_tc(qf, at<float>(ws, L.ximg), at<float>(ws, L.yimg), at<float>(ws, L.xnorm),
+                                    at<float>(ws, L.ynorm), st));
+        // 2. the band's backward wavefront
+        WaveParams qb = wave_params(pr, L, ws, gamma, true, false, true);
+        qb.W = kBandBlocks; qb.S = 1; qb.strip0 = k; qb.S_all = SB;
+        qb.vh_rb0 = rb0; qb.vh_nb = nb;
+        qb.lens_n = lens_n; qb.lens_m = lens_m;
+        SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_b), 0, L.ctrl_b_bytes, st));
+        SDTW_CUDA(launch_backward(qb, st));
+        // 3. the band's gradient terms: E of the band is a problem of nrows x M
+        g.pr.xs[0] = pr.xs[0] + (size_t)row0 * L.D;
+        g.N = nrows;
+        if (grad_x) {
+            g.out = grad_x + (size_t)row0 * L.D;
+            g.out_stride = (long long)L.N * L.D;
+            g.accumulate = 0;
+            SDTW_CUDA(launch_grad_tc(g, false, img_rows, status, st));
+        }
+        if (grad_y) {
+            SDTW_CUDA(launch_bimg(g, nullptr, img_cols, st));
+            g.out = grad_y;
+            g.out_stride = (long long)L.M * L.D;
+            g.accumulate = k < SB - 1;
+            SDTW_CUDA(launch_grad_tc(g, true, img_cols, status, st));
+        }
+    }
     return SDTW_OK;
 }
 
@@ -461,7 +551,7 @@ sdtw_status sdtw_forward_varlen(const float* x, const float* y, const int* x_len
                                 int N, int M, int D, float gamma, sdtw_mode mode, float* loss, void* ws,
                                 size_t ws_bytes, void* stream)
 {
-    sdtw_status s = check_common(x, y, B, N, M, D, gamma, (int)mode);
+    sdtw_status s = check_common(x, y, B, N, M, D, gamma, (int)mode, true);
     if (s != SDTW_OK) return s;
     if (!loss) return SDTW_ERR_ARG;
     Layout L;
@@ -487,7 +577,7 @@ sdtw_status sdtw_backward_varlen(const float* x, const float* y, const int* x_le
                                  int N, int M, int D, float gamma, sdtw_mode mode, const float* grad_loss,
                                  float* grad_x, float* grad_y, void* ws, size_t ws_bytes, void* stream)
 {
-    sdtw_status s = check_common(x, y, B, N, M, D, gamma, (int)mode);
+    sdtw_status s = check_common(x, y, B, N, M, D, gamma, (int)mode, true);
     if (s != SDTW_OK) return s;
     if (!grad_loss) return SDTW_ERR_ARG;
     Layout L;
@@ -498,6 +588,10 @@ sdtw_status sdtw_backward_varlen(const float* x, const float* y, const int* x_le
     pr.xstride[0] = (long long)N * D; pr.ystride[0] = (long long)M * D;
     pr.B = B;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (L.ckpt) {
+        if (env_int("SDTW_GRAD_SIMT", 0) != 0) return SDTW_ERR_ARG;
+        return run_backward_ckpt(pr, L, ws, gamma, (int)mode, grad_loss, grad_x, grad_y, st, x_lengths, y_lengths);
+    }
     // The gradient operand images depend on x and y only: they are built on a side
     // stream while the backward wavefront runs (it leaves most of each SM idle).
     cudaStream_t side = nullptr;

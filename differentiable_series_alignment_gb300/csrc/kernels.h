@@ -37,7 +37,23 @@ struct WaveParams {
     int ext;          // 1: extended-precision forward state (wavefront_x.cu)
     const int* lens_n; // per-problem lengths of x and y (device, P each), or null: every
     const int* lens_m; // problem spans N x M. A problem aligns its leading N_b x M_b block.
+    // Band launches of the checkpointed backward: this launch covers strips
+    // [strip0, strip0 + S) of S_all strips per problem, and VH / E hold only row
+    // blocks [vh_rb0, vh_rb0 + vh_nb) of every problem. Zeros: the whole problem.
+    int strip0, S_all, vh_rb0, vh_nb;
+    int no_loss;       // 1: a recompute of stored boundary rows; no loss is assembled
 };
+
+// Strips per problem for the boundary-row buffers.
+__host__ __device__ inline int strips_all(const WaveParams& q) { return q.S_all > 0 ? q.S_all : q.S; }
+
+// Index of (problem p, row block rb, step 0, lane) in the VH / E buffers: the skewed
+// layout restricted to the launch's band of row blocks.
+__host__ __device__ inline long long band_index(const WaveParams& q, int p, int rb, int lane, int T)
+{
+    const int nb = q.vh_nb > 0 ? q.vh_nb : q.NB;
+    return ((long long)p * nb + (rb - q.vh_rb0)) * T * 32 + lane;
+}
 
 size_t wave_smem_fixed(int W, bool backward);
 size_t wave_smem_fused_per_warp(int D);

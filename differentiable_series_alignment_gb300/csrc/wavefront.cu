@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(MAXT, 1) bwd_kernel(const WaveParams q)
     __syncthreads();
 
     const int tk = s_tk;
-    const int p = tk % q.P, strip = q.S - 1 - tk / q.P;
+    const int p = tk % q.P, strip = q.strip0 + q.S - 1 - tk / q.P;
     const int N = q.N, M = q.M, T = skew_T(M);
     const int off = T - (M + 31);   // leading padding steps of the reverse walk
     const int rb = strip * W + warp, r0 = rb * 32, i = r0 + lane;
@@ -370,13 +370,14 @@ __global__ void __launch_bounds__(MAXT, 1) bwd_kernel(const WaveParams q)
     const bool row_in = i < Nb;
 
     using VT = typename std::conditional<EXT, float4, float2>::type;
-    const long long sk = skew_index(N, M, p, rb, 0, lane);
+    const long long sk = band_index(q, p, rb, lane, T);
     const VT* vhp = reinterpret_cast<const VT*>(q.VH) + sk;
     float* ep = q.E + sk;
     Slot* ring_out = ring + 2 * warp * kRing;
     const Slot* ring_in = ring + 2 * (warp + 1) * kRing;
-    Slot* edge_out = q.edge_b + 2 * ((size_t)p * q.S + strip) * M;
-    const Slot* edge_in = q.edge_b + 2 * ((size_t)p * q.S + strip + 1) * M;
+    const int S_all = strips_all(q);
+    Slot* edge_out = q.edge_b + 2 * ((size_t)p * S_all + strip) * M;
+    const Slot* edge_in = q.edge_b + 2 * ((size_t)p * S_all + strip + 1) * M;
     // Messages to the row above (lane 0), slot k = column M-1-k, a pair of
     // tagged slots (msg_up, msg_diag) with tag k + 1: into the shared ring of
     // the warp above or the global edge buffer of the strip above.

@@ -81,7 +81,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     __syncthreads();
 
     const int tk = s_tk;
-    const int p = tk % q.P, strip = tk / q.P;
+    const int p = tk % q.P, strip = q.strip0 + tk / q.P;
     const int N = q.N, M = q.M, T = skew_T(M);
     const int KB = (q.D + 31) / 32;
     const int Npad = simg_pad(N), Mpad = simg_pad(M);
@@ -210,12 +210,14 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
         }
 
         if (active) {
-            const long long sk = skew_index(N, M, p, rb, 0, lane);
-            float2* vhp = q.VH + sk;
+            // the state for the backward (none in a checkpointed forward, which keeps only
+            // the strips' boundary rows)
+            const bool store_vh = q.VH != nullptr;
+            float2* vhp = store_vh ? q.VH + band_index(q, p, rb, lane, T) : nullptr;
             Slot* ring_out = ring + warp * kRing;
             const Slot* ring_in = ring + (warp - 1) * kRing;
-            Slot* edge_out = q.edge_f + ((size_t)p * q.S + strip) * M;
-            const Slot* edge_in = q.edge_f + ((size_t)p * q.S + strip - 1) * M;
+            Slot* edge_out = q.edge_f + ((size_t)p * strips_all(q) + strip) * M;
+            const Slot* edge_in = q.edge_f + ((size_t)p * strips_all(q) + strip - 1) * M;
             const bool chan_lane = has_bot && lane == 31 && !(q.skip_publish && strip == 0 && bot_global);
             Slot* chan_out = bot_global ? edge_out : ring_out;
             const int chan_mask = bot_global ? 0x7fffffff : (kRing - 1);
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                     const float svl = col0 ? kBig : (row0_lane ? -kBig : vl);
                     const float shu = row0_lane ? kBig : (col0 ? -kBig : hu);
                     c0 = col0 ? d : c0;
-                    vhp[(long long)s * 32] = make_float2(svl, shu);
+                    if (store_vh) vhp[(long long)s * 32] = make_float2(svl, shu);
                     const bool valid = (unsigned)j < (unsigned)M;
                     slot_store_if(chan_lane && valid, chan_out + (j & chan_mask), h, (unsigned)(j + 1));
                     if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = h;
@@ -320,7 +322,8 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
         }
     }
 
-    // Loss: R[N,M] = sum_i d(i,0) + sum_{j>=1} h(N-1, j), scaled units.
+    // Loss: R[N,M] = sum_i d(i,0) + sum_{j>=1} h(N-1, j), scaled units (not in a recompute).
+    if (!q.no_loss) {
     const int Nb = q.lens_n ? min(max(q.lens_n[p], 1), N) : N;
     const int Mb = q.lens_m ? min(max(q.lens_m[p], 1), M) : M;
     double part = (active && warp < W && rs0 + 32 * warp + lane < Nb) ? (double)c0 : 0.0;
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
         for (int w = 0; w < W; ++w) cs += s_red[w];
         q.colsum[(size_t)p * q.NB + strip] = cs;
         __threadfence();
-        s_last = (atomicAdd(&q.done[p], 1) == q.S - 1);
+        s_last = (atomicAdd(&q.done[p], 1) == strips_all(q) - 1);
     }
     __syncthreads();
     if (s_last) {  // the last strip of problem p to finish assembles its loss
@@ -348,9 +351,10 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
         if (threadIdx.x == 0) {
             double tot = 0.0;
             for (int w = 0; w <= W; ++w) tot += s_red[w];
-            for (int k = 0; k < q.S; ++k) tot += __ldcg(&q.colsum[(size_t)p * q.NB + k]);
+            for (int k = 0; k < strips_all(q); ++k) tot += __ldcg(&q.colsum[(size_t)p * q.NB + k]);
             q.loss[p] = (float)(tot * (double)q.unscale);
         }
+    }
     }
 
     fence_before_sync();

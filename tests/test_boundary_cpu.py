@@ -204,3 +204,29 @@ def test_unequal_normalized_workspace_and_validation(lib):
     assert call(g=0.0) == 2                                # SDTW_ERR_GAMMA
     assert call(y=None) == 1 and call(loss=None) == 1 and call(mode=8) == 1
     assert call(ws=None) == 5 and call(ws=vp(0x100004)) == 5 and call(n=100) == 5
+
+
+def test_checkpoint_workspace_and_validation(lib):
+    from differentiable_series_alignment_gb300 import _lib as L
+    B, N, M, D = 32, 512, 512, 64
+    full = L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, D, L.FUSED)
+    ck = L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, D, L.FUSED | L.CHECKPOINT)
+    T = 544
+    band = B * 4 * T * 32                       # cells of one 128-row band of every problem
+    assert ck > band * 12                       # (v_left, h_up) pairs and E of one band
+    assert full - ck >= (B * 16 * T * 32 - band) * 12   # the other bands' state and E are gone
+    assert ck < full / 2
+    # only the fp32 tensor-core fused path checkpoints
+    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, D, L.UNFUSED | L.CHECKPOINT) == 0
+    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, D, L.FUSED | L.EXTENDED | L.CHECKPOINT) == 0
+    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, 65, L.FUSED | L.CHECKPOINT) == 0
+    assert L.sdtw_workspace_bytes(L.OP_NORMALIZED, B, N, N, D, L.FUSED | L.CHECKPOINT) == 0
+    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, 2, 3, 4, 2, 8) == 0
+    # host-side validation, before any CUDA call
+    assert _fwd(lib, mode=L.FUSED | L.CHECKPOINT, ws_bytes=16) == 5     # accepted flag, small workspace
+    assert _fwd(lib, mode=L.UNFUSED | L.CHECKPOINT) == 1
+    assert _fwd(lib, mode=L.FUSED | L.EXTENDED | L.CHECKPOINT) == 1
+    assert _fwd(lib, mode=L.FUSED | L.CHECKPOINT, D=65) == 1
+    vp = ctypes.c_void_p
+    assert lib.sdtw_normalized(vp(0x1000), vp(0x2000), 2, 3, 2, 1.0, L.FUSED | L.CHECKPOINT, vp(0x3000), None,
+                               None, None, vp(0x100000), 1 << 40, None) == 1

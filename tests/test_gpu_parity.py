@@ -339,6 +339,55 @@ def test_unequal_normalized_through_autograd():
     assert_close(yt.grad.cpu().numpy(), ogy, GRAD_RTOL, 32 * GRAD_ATOL, "autograd unequal normalized grad_y")
 
 
+CKPT = 1 | 4   # SDTW_FUSED | SDTW_CHECKPOINT
+
+
+@pytest.mark.parametrize("N,M,D", [(64, 70, 8), (128, 33, 16), (129, 100, 5), (300, 77, 64), (512, 512, 64)])
+def test_checkpointed_fused_matches_oracle(N, M, D):
+    x, y = synth.iid_normal_pair(3, N, M, D, 101, repeat=N * 1000 + M)
+    check_against_oracle(x, y, 0.9, CKPT, grad_loss=WEIGHTS, what=f"checkpoint {N}x{M}x{D}")
+
+
+@pytest.mark.parametrize("N,M", [(300, 77), (257, 130)])
+def test_checkpointed_fused_agrees_with_stored_state(N, M):
+    """The recomputed bands repeat the forward's arithmetic exactly, so losses and
+    grad_x equal those of the stored-state fused mode bit for bit; grad_y sums the
+    bands' terms in another order."""
+    x, y = synth.iid_normal_pair(4, N, M, 12, 102, repeat=N)
+    w = [0.03, -0.02, 0.05, 0.01]
+    a = run_cuda(x, y, 1.1, 1, grad_loss=w)
+    b = run_cuda(x, y, 1.1, CKPT, grad_loss=w)
+    assert np.array_equal(a["loss"], b["loss"])
+    assert np.array_equal(a["gx"], b["gx"])
+    assert_close(b["gy"], a["gy"], 1e-5, 1e-8, "checkpoint grad_y vs stored state")
+
+
+def test_checkpointed_padded_batch_and_autograd():
+    from differentiable_series_alignment_gb300 import SoftDTW
+    L = _lib()
+    B, N, M, D, gamma = 3, 200, 150, 6, 0.8
+    lx, ly = [200, 131, 7], [150, 90, 150]
+    x, y = synth.iid_normal_pair(B, N, M, D, 103)
+    for b in range(B):
+        x[b, lx[b]:] = 0.0
+        y[b, ly[b]:] = 0.0
+    xt = torch.from_numpy(x).cuda().requires_grad_(True)
+    yt = torch.from_numpy(y).cuda().requires_grad_(True)
+    lxt = torch.tensor(lx, dtype=torch.int32, device="cuda")
+    lyt = torch.tensor(ly, dtype=torch.int32, device="cuda")
+    loss = SoftDTW(gamma=gamma, fused=True, checkpoint=True)(xt, yt, lxt, lyt)
+    w = torch.tensor(WEIGHTS, device="cuda")
+    (loss * w).sum().backward()
+    loss = loss.detach().cpu().numpy()
+    gx, gy = xt.grad.cpu().numpy(), yt.grad.cpu().numpy()
+    for b in range(B):
+        o = oracle.single(x[b, :lx[b]], y[b, :ly[b]], gamma, g=WEIGHTS[b])
+        assert_close(loss[b:b + 1], [o["loss"]], LOSS_RTOL, 1e-6, f"checkpoint padded pair {b} loss")
+        assert_close(gx[b, :lx[b]], o["gx"], GRAD_RTOL, GRAD_ATOL, f"checkpoint padded pair {b} grad_x")
+        assert_close(gy[b, :ly[b]], o["gy"], GRAD_RTOL, GRAD_ATOL, f"checkpoint padded pair {b} grad_y")
+        assert not np.any(gx[b, lx[b]:]) and not np.any(gy[b, ly[b]:])
+
+
 # --------------------------------------------------------------------------- barycenter
 
 @pytest.mark.parametrize("mname,mode", MODES)
