@@ -59,7 +59,9 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
-template <bool ACC>
+// STORE: the per-cell state for the backward is written (false in a checkpointed
+// forward, which keeps only the strips' boundary rows).
+template <bool ACC, bool STORE>
 __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     fwd_tc_kernel(const WaveParams q, const float* __restrict__ ximg, const float* __restrict__ yimg,
                   const float* __restrict__ xnorm, const float* __restrict__ ynorm)
@@ -210,10 +212,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
         }
 
         if (active) {
-            // the state for the backward (none in a checkpointed forward, which keeps only
-            // the strips' boundary rows)
-            const bool store_vh = q.VH != nullptr;
-            float2* vhp = store_vh ? q.VH + band_index(q, p, rb, lane, T) : nullptr;
+            float2* vhp = STORE ? q.VH + band_index(q, p, rb, lane, T) : nullptr;
             Slot* ring_out = ring + warp * kRing;
             const Slot* ring_in = ring + (warp - 1) * kRing;
             Slot* edge_out = q.edge_f + ((size_t)p * strips_all(q) + strip) * M;
@@ -308,7 +307,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                     const float svl = col0 ? kBig : (row0_lane ? -kBig : vl);
                     const float shu = row0_lane ? kBig : (col0 ? -kBig : hu);
                     c0 = col0 ? d : c0;
-                    if (store_vh) vhp[(long long)s * 32] = make_float2(svl, shu);
+                    if constexpr (STORE) vhp[(long long)s * 32] = make_float2(svl, shu);
                     const bool valid = (unsigned)j < (unsigned)M;
                     slot_store_if(chan_lane && valid, chan_out + (j & chan_mask), h, (unsigned)(j + 1));
                     if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = h;
@@ -386,7 +385,8 @@ cudaError_t launch_forward_tc(WaveParams q, const float* ximg, const float* yimg
         kern<<<grid, (kDpWarps + 1) * 32, smem, st>>>(q, ximg, yimg, xnorm, ynorm);
         return cudaGetLastError();
     };
-    return q.accurate ? go(fwd_tc_kernel<true>) : go(fwd_tc_kernel<false>);
+    if (q.VH == nullptr) return q.accurate ? go(fwd_tc_kernel<true, false>) : go(fwd_tc_kernel<false, false>);
+    return q.accurate ? go(fwd_tc_kernel<true, true>) : go(fwd_tc_kernel<false, true>);
 }
 
 }  // namespace sdtw
