@@ -282,8 +282,21 @@ def run_ours(args):
                           "cells_per_s": CELLS / (fb_ms * 1e-3)}
         assert L.sdtw_last_device_status(b["ws"]) == 0
 
+    # the checkpointed fused mode (no per-cell forward state; bands recomputed in the
+    # backward): reported beside the two modes of the step, not part of it
+    ck = L.FUSED | L.CHECKPOINT
+    bufs[ck] = {"ws": L.workspace(L.OP_FWD_BWD, B, N, M, D, ck, dev), "loss": torch.empty(B, device=dev),
+                "gx": torch.empty_like(x), "gy": torch.empty_like(y)}
+    b = bufs[ck]
+    ck_iters = max(10, min(50, K))
+    f_ms = timed(lambda: L.sdtw_forward(x, y, GAMMA, ck, b["loss"], b["ws"]), ck_iters)
+    fb_ms = timed(lambda: (L.sdtw_forward(x, y, GAMMA, ck, b["loss"], b["ws"]),
+                           L.sdtw_backward(x, y, GAMMA, ck, g, b["gx"], b["gy"], b["ws"])), ck_iters)
+    per_mode["fused_checkpoint"] = {"fwd_ms": f_ms, "fwd_bwd_ms": fb_ms, "cells_per_s": CELLS / (fb_ms * 1e-3)}
+    assert L.sdtw_last_device_status(b["ws"]) == 0
+
     # peak memory of one fwd+bwd per mode, inputs and gradient buffers resident
-    for mode, name in ((L.UNFUSED, "unfused"), (L.FUSED, "fused")):
+    for mode, name in ((L.UNFUSED, "unfused"), (L.FUSED, "fused"), (ck, "fused_checkpoint")):
         del bufs[mode]
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
