@@ -36,7 +36,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one bwd_kernel launch at this workload, from one
 # `ncu --set full` capture of it: 71.55 MB read + 8.00 MB written. Set to None
 # whenever the kernel changes until it is captured again.
-BWD_DRAM_BYTES = 79.10e6
+BWD_DRAM_BYTES = 76.41e6
 # kernels per step: unfused forward (operand images, cost tensor, wavefront) + backward
 # (wavefront, gradient operand images, two gradient contractions), fused forward
 # (operand images, wavefront with tensor-core costs) + backward (4)
