@@ -15,7 +15,7 @@ Workload shapes follow the pages:
   * block-wave sequences for the barycenter of Figure 2.
 No public dataset is named on the pages; these recipes stand in for data.
 
-Seed convention: seed = config_index * 1000 + repeat.
+Seed convention: seed = seed_base * 1000 + repeat.
 """
 from __future__ import annotations
 
@@ -26,18 +26,18 @@ __all__ = [
     "iid_normal_pair",
     "warped_pair",
     "block_waves",
-    "CONFIGS",
+    "WORKLOADS",
 ]
 
 
-def rng_for(config_index: int, repeat: int = 0) -> np.random.Generator:
-    """PCG64 generator seeded by ``config_index * 1000 + repeat``."""
-    return np.random.Generator(np.random.PCG64(config_index * 1000 + repeat))
+def rng_for(seed_base: int, repeat: int = 0) -> np.random.Generator:
+    """PCG64 generator seeded by ``seed_base * 1000 + repeat``."""
+    return np.random.Generator(np.random.PCG64(seed_base * 1000 + repeat))
 
 
-def iid_normal_pair(B: int, N: int, M: int, D: int, config_index: int, repeat: int = 0):
+def iid_normal_pair(B: int, N: int, M: int, D: int, seed_base: int, repeat: int = 0):
     """x (B,N,D) and y (B,M,D), entries iid N(0,1), as float32."""
-    g = rng_for(config_index, repeat)
+    g = rng_for(seed_base, repeat)
     x = g.standard_normal((B, N, D)).astype(np.float32)
     y = g.standard_normal((B, M, D)).astype(np.float32)
     return x, y
@@ -59,12 +59,12 @@ def _random_monotone_warp(g: np.random.Generator, L: int, segments: int = 8) -> 
     return np.interp(np.arange(L, dtype=np.float64), knots_t, knots_v)
 
 
-def warped_pair(B: int, L: int, D: int, config_index: int, repeat: int = 0,
+def warped_pair(B: int, L: int, D: int, seed_base: int, repeat: int = 0,
                 noise: float = 0.1, segments: int = 8):
     """x ~ N(0,1) of shape (B,L,D); y[b,j] = x[b] linearly interpolated at
     phi_b(j) plus N(0, noise^2), with phi_b a random monotone piecewise-linear
     warp (one per batch element)."""
-    g = rng_for(config_index, repeat)
+    g = rng_for(seed_base, repeat)
     x = g.standard_normal((B, L, D))
     y = np.empty_like(x)
     for b in range(B):
@@ -77,13 +77,13 @@ def warped_pair(B: int, L: int, D: int, config_index: int, repeat: int = 0,
     return x.astype(np.float32), y.astype(np.float32)
 
 
-def block_waves(K: int, T: int, D: int, config_index: int, repeat: int = 0,
+def block_waves(K: int, T: int, D: int, seed_base: int, repeat: int = 0,
                 pmin: float = 64.0, pmax: float = 256.0, noise: float = 0.1):
     """K sequences (K,T,D): each channel is a +-1 square wave
     s(t) = +1 if floor(2 (t + phase) / P) is even else -1, with period
     P ~ U[pmin, pmax] and phase ~ U[0, P) drawn per sequence and channel,
     plus N(0, noise^2)."""
-    g = rng_for(config_index, repeat)
+    g = rng_for(seed_base, repeat)
     P = g.uniform(pmin, pmax, size=(K, 1, D))
     phase = g.uniform(0.0, 1.0, size=(K, 1, D)) * P
     t = np.arange(T, dtype=np.float64)[None, :, None]
@@ -92,16 +92,13 @@ def block_waves(K: int, T: int, D: int, config_index: int, repeat: int = 0,
     return s.astype(np.float32)
 
 
-# The five workloads (index = seed base). Sizes only; gamma and mode per entry.
-CONFIGS = {
-    0: dict(name="small B=4 N=M=64 D=4", B=4, N=64, M=64, D=4, gammas=(1.0,), modes=("unfused",)),
-    1: dict(name="headline B=32 N=M=512 D=64", B=32, N=512, M=512, D=64, gammas=(1.0,),
-            modes=("unfused", "fused")),
-    2: dict(name="sweep B=32 (L at D=128; D at L=256)", B=32,
-            L_sweep=(128, 256, 512, 1024, 2048), D_at_L=128,
-            D_sweep=(1, 4, 16, 64, 128, 256), L_at_D=256, gammas=(1.0,), modes=("unfused", "fused")),
-    3: dict(name="long warped B=8 N=M=8192 D=128", B=8, N=8192, M=8192, D=128,
-            gammas=(1.0, 0.1, 0.01), modes=("fused",)),
-    4: dict(name="barycenter K=64 T=1024 D=8", K=64, T=1024, D=8, steps=100, lr=0.1,
-            gammas=(1.0,), modes=("fused",)),
+# The five workloads by name, each with the seed base its inputs are drawn with.
+# Sizes only; gamma and mode per entry.
+WORKLOADS = {
+    "small": dict(seed=0, B=4, N=64, M=64, D=4, gammas=(1.0,), modes=("unfused",)),
+    "headline": dict(seed=1, B=32, N=512, M=512, D=64, gammas=(1.0,), modes=("unfused", "fused")),
+    "sweep": dict(seed=2, B=32, L_sweep=(128, 256, 512, 1024, 2048), D_at_L=128,
+                  D_sweep=(1, 4, 16, 64, 128, 256), L_at_D=256, gammas=(1.0,), modes=("unfused", "fused")),
+    "long_warped": dict(seed=3, B=8, N=8192, M=8192, D=128, gammas=(1.0, 0.1, 0.01), modes=("fused",)),
+    "barycenter": dict(seed=4, K=64, T=1024, D=8, steps=100, lr=0.1, gammas=(1.0,), modes=("fused",)),
 }

@@ -97,8 +97,8 @@ WEIGHTS = [w / 32 for w in WEIGHTS_O1]
 
 @pytest.mark.parametrize("mname,mode", MODES)
 def test_small_config(mname, mode):
-    c = synth.CONFIGS[0]
-    x, y = synth.iid_normal_pair(c["B"], c["N"], c["M"], c["D"], 0)
+    c = synth.WORKLOADS["small"]
+    x, y = synth.iid_normal_pair(c["B"], c["N"], c["M"], c["D"], c["seed"])
     check_against_oracle(x, y, 1.0, mode, what=f"small {mname}")
 
 
@@ -230,8 +230,8 @@ def test_distance_kernel_matches_definition():
 
 @pytest.mark.parametrize("mname,mode", MODES)
 def test_headline_config(mname, mode):
-    c = synth.CONFIGS[1]
-    x, y = synth.iid_normal_pair(c["B"], c["N"], c["M"], c["D"], 1)
+    c = synth.WORKLOADS["headline"]
+    x, y = synth.iid_normal_pair(c["B"], c["N"], c["M"], c["D"], c["seed"])
     check_against_oracle(x, y, 1.0, mode, what=f"headline {mname}")
 
 
