@@ -326,6 +326,27 @@ def run_ours(args):
                 "launch_ms": bw_ms,
                 "note": "latency-bound: N+M-1 dependent DP steps; traffic from one ncu capture of this kernel"}
 
+    # ---- the same kernel against its latency floor. One 32-row strip over a long row
+    # has no neighbour to wait for, so its time per step is the free-running step of
+    # the backward recursion; a pass over one N x M problem takes at least N+M-1 of
+    # them. Timed through the library like the rest (one warp, fused workspace).
+    Lc = 8192
+    x1_np, y1_np = synth.iid_normal_pair(1, 32, Lc, D, 5)
+    x1, y1 = torch.from_numpy(x1_np).to(dev), torch.from_numpy(y1_np).to(dev)
+    ws1 = L.workspace(L.OP_FWD_BWD, 1, 32, Lc, D, L.FUSED, dev)
+    loss1, g1 = torch.empty(1, device=dev), torch.ones(1, device=dev)
+    L.sdtw_forward(x1, y1, GAMMA, L.FUSED, loss1, ws1)
+    strip_ms = timed(lambda: L.sdtw_backward(x1, y1, GAMMA, L.FUSED, g1, None, None, ws1), 20)
+    assert L.sdtw_last_device_status(ws1) == 0
+    steps1 = ((Lc + 31 + 15) // 16) * 16          # skewed steps of one strip
+    step_ns = strip_ms * 1e6 / steps1
+    floor_ms = (N + M - 1) * step_ns * 1e-6
+    roofline["latency"] = {"chain_steps": N + M - 1, "free_step_ns": step_ns, "floor_ms": floor_ms,
+                           "frac": floor_ms / bw_ms,
+                           "note": "free-running step measured on one 32 x 8192 strip (whole launch / its "
+                                   "8224 steps); frac = floor_ms / launch_ms"}
+    del ws1
+
     # ---- end to end through the C ABI with HOST buffers, both modes: every step copies the
     # batch in from pinned host memory and the losses and gradients back out
     # (sdtw_value_and_grad_host: the batch runs as E2E_CHUNKS chunks on side streams, so the
