@@ -188,8 +188,19 @@ def cpu_baseline():
         dt = time.perf_counter() - t0
         if dt > 8.0 or reps >= 20:
             break
+    # the same on one core: two problems of the batch, repeated for about a second
+    t1 = time.perf_counter()
+    reps1 = 0
+    while True:
+        oracle.batch(x[:2], y[:2], GAMMA, grad_loss=gl[:2], nthreads=1)
+        reps1 += 1
+        dt1 = time.perf_counter() - t1
+        if dt1 > 1.0:
+            break
     return {"value": reps * CELLS / dt, "unit": "cells/s", "cores": cores, "kind": "oracle",
-            "sample": f"{reps} x the full batch B=32 N=M=512 D=64, fwd+bwd with gradients, fp64, {dt:.1f} s"}
+            "sample": f"{reps} x the full batch B=32 N=M=512 D=64, fwd+bwd with gradients, fp64, {dt:.1f} s",
+            "single_core": {"value": reps1 * 2 * N * M / dt1, "unit": "cells/s", "cores": 1,
+                            "sample": f"{reps1} x 2 problems of the batch, {dt1:.1f} s"}}
 
 
 # --------------------------------------------------------------------------- our arm
