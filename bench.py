@@ -33,10 +33,26 @@ B, N, M, D, GAMMA = 32, 512, 512, 64, 1.0
 CELLS = B * N * M
 WORKLOAD = "softdtw fwd+bwd B=32 N=M=512 D=64 gamma=1, unfused then fused"
 FALLBACK_HBM_GBS = 6800.0
-# DRAM bytes (read + write) of one bwd_kernel launch at this workload, from one
-# `ncu --set full` capture of it: 71.55 MB read + 8.00 MB written. Set to None
-# whenever the kernel changes until it is captured again.
-BWD_DRAM_BYTES = 76.41e6
+# Per-cell accounting of the method for the roofline (one forward + backward):
+#   HBM bytes: unfused 28 (cost written, then read by the forward and by the
+#   backward; R written and read; E written and read once for both contractions),
+#   fused 8 (R written and read; costs recomputed on chip). The double-float state
+#   counts R and the stored cost at 8 bytes: unfused 48, fused 16. Inputs read
+#   and gradients written once come on top.
+#   SFU operations: forward 2 ex2 + 1 lg2 (the three-term soft-min), backward
+#   2 ex2 + 1 lg2 (the log-sum-exp of the three messages) + 1 ex2 (E itself).
+ALG_BYTES = {("unfused", False): 28, ("fused", False): 8, ("unfused", True): 48, ("fused", True): 16}
+FWD_EX2, FWD_LG2, BWD_EX2, BWD_LG2 = 2, 1, 3, 1
+# SFU issue rate per SM and clock on this part: ex2 32, lg2 16 (a one-instruction
+# microbenchmark with 8 independent chains per thread measured 31.7 and 15.9).
+EX2_PER_SM_CLK, LG2_PER_SM_CLK = 32, 16
+FALLBACK_SM_MHZ = 2070.0
+# DRAM bytes (read + write) of one bwd_kernel launch of this workload's fused step
+# from one ncu capture (`dram__bytes_read.sum + dram__bytes_write.sum`), with the
+# SHA-256 of the sources that build the kernel at the time of the capture; the
+# bench reports it only while those sources are unchanged (else null).
+BWD_TRAFFIC = {"sha256": None, "bytes": None}
+BWD_SOURCES = ("wavefront.cu", "common.cuh", "channel.cuh", "kernels.h")
 # kernels per step: unfused forward (operand images, cost tensor, wavefront) + backward
 # (wavefront, gradient operand images, two gradient contractions), fused forward
 # (operand images, wavefront with tensor-core costs) + backward (4)
@@ -174,6 +190,50 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def sm_clock_mhz():
+    """Maximum SM clock: MEASURED_PEAKS.json's, else the part's nominal maximum."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        v = float(json.load(open(p)).get("sm_max_mhz") or 0)
+        if v > 0:
+            return v
+    except Exception:
+        pass
+    return FALLBACK_SM_MHZ
+
+
+def sfu_rates(num_sms):
+    """(ex2/s, lg2/s) at the maximum SM clock."""
+    hz = sm_clock_mhz() * 1e6
+    return num_sms * EX2_PER_SM_CLK * hz, num_sms * LG2_PER_SM_CLK * hz
+
+
+def sources_sha256(names):
+    import hashlib
+    h = hashlib.sha256()
+    for n_ in names:
+        with open(os.path.join(ROOT, "differentiable_series_alignment_gb300", "csrc", n_), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def roofline_bound(cells, hbm_bytes, ex2, lg2, hbm_gbs, rates):
+    """The roofline time of `cells` DP cells moving `hbm_bytes` and issuing ex2/lg2
+    per cell: the slower of HBM at its measured peak and the SFU at its issue rate."""
+    t_hbm = hbm_bytes / (hbm_gbs * 1e9)
+    t_sfu = cells * (ex2 / rates[0] + lg2 / rates[1])
+    return {"hbm_us": t_hbm * 1e6, "sfu_us": t_sfu * 1e6, "bound": "hbm" if t_hbm >= t_sfu else "sfu",
+            "bound_us": max(t_hbm, t_sfu) * 1e6}
+
+
+def step_roofline(cells, io_bytes, mode_name, ext, hbm_gbs, rates, ms):
+    """Roofline fraction of one forward + backward (both directions of the DP)."""
+    r = roofline_bound(cells, cells * ALG_BYTES[(mode_name, ext)] + io_bytes, FWD_EX2 + BWD_EX2,
+                       FWD_LG2 + BWD_LG2, hbm_gbs, rates)
+    r["frac"] = r["bound_us"] / (ms * 1e3)
+    return r
+
+
 def cpu_baseline():
     import oracle
     from differentiable_series_alignment_gb300 import synth
@@ -201,6 +261,129 @@ def cpu_baseline():
             "sample": f"{reps} x the full batch B=32 N=M=512 D=64, fwd+bwd with gradients, fp64, {dt:.1f} s",
             "single_core": {"value": reps1 * 2 * N * M / dt1, "unit": "cells/s", "cores": 1,
                             "sample": f"{reps1} x 2 problems of the batch, {dt1:.1f} s"}}
+
+
+# --------------------------------------------------------------------------- the other workloads
+
+def measure_per_config(L, synth, dev, flush, stream, hbm, rates, step_ns):
+    """DP cells/s, peak device memory above the resident inputs and gradient buffers,
+    and the roofline fraction (slower of HBM at the method's bytes and the SFU at its
+    ex2/lg2 count, over the measured forward + backward) of every workload beside the
+    headline: the small one, the length and width sweep in both modes, the long
+    time-warped pairs at three gammas plus their normalized form, and 100 barycenter
+    steps (with and without early stopping). The precision mode is the one the
+    high-level API picks for the workload's batch-mean loss."""
+    import torch
+    from differentiable_series_alignment_gb300 import softdtw_barycenter
+
+    def median_ms(fn, reps, warm=1):
+        for _ in range(warm):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for k in range(reps):
+            flush.fill_(k & 0xff)
+            ev[k][0].record(stream)
+            fn()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) for a, b in ev]))
+
+    def point(x, y, gamma, mode, reps, normalized=False):
+        B_, N_, D_ = x.shape
+        M_ = y.shape[1]
+        gx, gy = torch.empty_like(x), torch.empty_like(y)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+        base = torch.cuda.memory_allocated(dev)
+        op = L.OP_NORMALIZED if normalized else L.OP_FWD_BWD
+        ws = L.workspace(op, B_, N_, M_, D_, mode, dev)
+        loss = torch.empty(B_, device=dev)
+        g = torch.full((B_,), 1.0 / B_, device=dev)
+        if normalized:
+            def fb():
+                L.sdtw_normalized(x, y, gamma, mode, loss, g, gx, gy, ws)
+        else:
+            def fb():
+                L.sdtw_forward(x, y, gamma, mode, loss, ws)
+                L.sdtw_backward(x, y, gamma, mode, g, gx, gy, ws)
+        ms = median_ms(fb, reps)
+        assert L.sdtw_last_device_status(ws) == 0
+        assert bool(torch.isfinite(loss).all()) and bool(torch.isfinite(gx).all())
+        peak = (torch.cuda.max_memory_allocated(dev) - base) / 2**20
+        cells = (3 if normalized else 1) * B_ * N_ * M_
+        name = "fused" if mode & L.FUSED else "unfused"
+        ext = bool(mode & L.EXTENDED)
+        r = step_roofline(cells, 2 * B_ * (N_ + M_) * D_ * 4, name, ext, hbm, rates, ms)
+        floor = 2 * (N_ + M_ - 1) * step_ns * 1e-6
+        out = {"mode": name + ("+extended" if ext else ""), "ms": ms, "cells": cells,
+               "cells_per_s": cells / (ms * 1e-3), "peak_MB_above_inputs": peak,
+               "workspace_MB": ws.numel() / 2**20, "roofline_frac": r["frac"], "roofline": r,
+               "latency_floor_ms": floor, "latency_frac": floor / ms}
+        del ws, loss, gx, gy
+        return out
+
+    res = {}
+    t0 = time.perf_counter()
+    c = synth.WORKLOADS["small"]
+    x, y = (torch.from_numpy(a).to(dev) for a in synth.iid_normal_pair(c["B"], c["N"], c["M"], c["D"], c["seed"]))
+    prec = L.auto_precision(1.0, c["N"], c["M"], c["D"], c["B"])
+    res["small"] = [dict(point(x, y, 1.0, m | prec, 20), B=c["B"], N=c["N"], M=c["M"], D=c["D"], gamma=1.0)
+                    for m in (L.UNFUSED, L.FUSED)]
+
+    c = synth.WORKLOADS["sweep"]
+    pts = [(Ls, c["D_at_L"]) for Ls in c["L_sweep"]] + [(c["L_at_D"], Ds) for Ds in c["D_sweep"]]
+    res["sweep"] = []
+    for Ls, Ds in pts:
+        x, y = (torch.from_numpy(a).to(dev)
+                for a in synth.iid_normal_pair(32, Ls, Ls, Ds, c["seed"], repeat=Ls * 1000 + Ds))
+        prec = L.auto_precision(1.0, Ls, Ls, Ds, 32)
+        for m in (L.UNFUSED, L.FUSED):
+            res["sweep"].append(dict(point(x, y, 1.0, m | prec, 5 if Ls <= 512 else 3), B=32, L=Ls, D=Ds, gamma=1.0))
+        del x, y
+
+    c = synth.WORKLOADS["long_warped"]
+    xn, yn = synth.warped_pair(c["B"], c["N"], c["D"], c["seed"])
+    x, y = torch.from_numpy(xn).to(dev), torch.from_numpy(yn).to(dev)
+    res["long_warped"] = []
+    for gamma in c["gammas"]:
+        m = L.FUSED | L.auto_precision(gamma, c["N"], c["M"], c["D"], c["B"])
+        res["long_warped"].append(dict(point(x, y, gamma, m, 2), B=c["B"], N=c["N"], D=c["D"], gamma=gamma))
+        res["long_warped"].append(dict(point(x, y, gamma, m, 2, normalized=True), B=c["B"], N=c["N"], D=c["D"],
+                                       gamma=gamma, variant="normalized"))
+    del x, y
+
+    c = synth.WORKLOADS["barycenter"]
+    X = torch.from_numpy(synth.block_waves(c["K"], c["T"], c["D"], c["seed"])).to(dev)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    softdtw_barycenter(X, gamma=1.0, max_iter=3, lr=c["lr"], fused=True)          # warm-up
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    z, lo = softdtw_barycenter(X, gamma=1.0, max_iter=c["steps"], lr=c["lr"], fused=True, return_losses=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    peak = (torch.cuda.max_memory_allocated(dev) - base) / 2**20
+    cells = c["steps"] * c["K"] * c["T"] * c["T"]
+    r = step_roofline(cells, c["steps"] * 2 * c["K"] * 2 * c["T"] * c["D"] * 4, "fused", False, hbm, rates, ms)
+    lo = lo.cpu().numpy()
+    _, lo_es = softdtw_barycenter(X, gamma=1.0, max_iter=c["steps"], lr=c["lr"], fused=True, early_stopping=True,
+                                  return_losses=True)
+    lo_es = lo_es.cpu().numpy()
+    res["barycenter"] = {"K": c["K"], "T": c["T"], "D": c["D"], "steps": c["steps"], "lr": c["lr"], "gamma": 1.0,
+                         "mode": "fused", "ms": ms, "ms_per_step": ms / c["steps"], "cells": cells,
+                         "cells_per_s": cells / (ms * 1e-3), "peak_MB_above_inputs": peak,
+                         "roofline_frac": r["frac"], "roofline": r, "loss_first": float(lo[0]),
+                         "loss_last": float(lo[-1]),
+                         "early_stopping": {"iterations": int(len(lo_es)), "of": c["steps"],
+                                            "saved_frac": 1.0 - len(lo_es) / c["steps"],
+                                            "loss_last": float(lo_es[-1]),
+                                            "rule": "tol=1e-4 relative improvement, patience=10, checked every 10"}}
+    res["wall_s"] = time.perf_counter() - t0
+    return res
 
 
 # --------------------------------------------------------------------------- our arm
@@ -324,18 +507,37 @@ def run_ours(args):
         per_mode[name]["workspace_MB"] = ws.numel() / 2**20
         del ws, loss, gx_, gy_
 
-    # ---- roofline of the dominant kernel: the backward wavefront (38% of the kernel time of a step in
-    # the launch list), timed alone through sdtw_backward without input gradients (fused workspace)
+    # ---- roofline of the dominant kernel: the backward wavefront (the largest share of a
+    # step's kernel time in the launch list), timed alone through sdtw_backward without input
+    # gradients (fused workspace). Its roofline is the slower of two bounds per launch:
+    # HBM at the method's bytes for the fused backward (R read once, 4 B per cell; E stays
+    # on chip) and the SFU at the method's 3 ex2 + 1 lg2 per cell.
     hbm, src = measured_peaks()
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rates = sfu_rates(num_sms)
     bw_ms = per_mode["fused"]["bwd_wavefront_ms"]
-    slots = B * ((N + 31) // 32) * (M + 31) * 32
-    bytes_bwd = CELLS * (8 + 4)  # (v_left, h_up) pair read + E written, per cell
-    achieved = bytes_bwd / (bw_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": BWD_DRAM_BYTES, "kernel": "bwd_kernel (log-space backward wavefront)",
-                "peak_source": src, "algorithmic_bytes_per_launch": bytes_bwd, "skewed_slots": slots,
-                "launch_ms": bw_ms,
-                "note": "latency-bound: N+M-1 dependent DP steps; traffic from one ncu capture of this kernel"}
+    bytes_bwd = CELLS * 4
+    rb = roofline_bound(CELLS, bytes_bwd, BWD_EX2, BWD_LG2, hbm, rates)
+    if rb["bound"] == "hbm":
+        achieved, peak, unit = bytes_bwd / (bw_ms * 1e-3) / 1e9, hbm, "GB/s"
+    else:
+        achieved = CELLS * (BWD_EX2 + BWD_LG2) / (bw_ms * 1e-3) / 1e12
+        peak = CELLS * (BWD_EX2 + BWD_LG2) / (rb["sfu_us"] * 1e-6) / 1e12
+        unit = "Tops/s (ex2 + lg2)"
+    sha = sources_sha256(BWD_SOURCES)
+    traffic = BWD_TRAFFIC["bytes"] if BWD_TRAFFIC["sha256"] == sha else None
+    impl_bytes = CELLS * (8 + 4)   # what this kernel moves: the stored (v_left, h_up) pair, E written
+    roofline = {"bound": rb["bound"], "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": rb["bound_us"] / (bw_ms * 1e3), "traffic": traffic,
+                "kernel": "bwd_kernel (log-space backward wavefront, fused step)",
+                "peak_source": f"HBM {src} ({hbm:.0f} GB/s); SFU ex2 {rates[0]:.3g}/s, lg2 {rates[1]:.3g}/s "
+                               f"({EX2_PER_SM_CLK} and {LG2_PER_SM_CLK} per SM and clock at "
+                               f"{sm_clock_mhz():.0f} MHz x {num_sms} SMs)",
+                "algorithmic_bytes_per_launch": bytes_bwd, "sfu_ops_per_cell": {"ex2": BWD_EX2, "lg2": BWD_LG2},
+                "hbm_us": rb["hbm_us"], "sfu_us": rb["sfu_us"], "launch_ms": bw_ms,
+                "implementation_bytes_per_launch": impl_bytes,
+                "traffic_over_algorithmic": (traffic / bytes_bwd) if traffic else None,
+                "traffic_sources_sha256": sha}
 
     # ---- the same kernel against its latency floor. One 32-row strip over a long row
     # has no neighbour to wait for, so its time per step is the free-running step of
@@ -357,6 +559,17 @@ def run_ours(args):
                            "note": "free-running step measured on one 32 x 8192 strip (whole launch / its "
                                    "8224 steps); frac = floor_ms / launch_ms"}
     del ws1
+
+    # the whole step per mode against the same two bounds (both directions, inputs and
+    # gradients moved once)
+    io = 2 * B * (N + M) * D * 4
+    for name in ("unfused", "fused"):
+        per_mode[name]["roofline"] = step_roofline(CELLS, io, name, False, hbm, rates, per_mode[name]["fwd_bwd_ms"])
+        per_mode[name]["latency_floor_ms"] = 2 * floor_ms
+
+    per_config = None
+    if args.per_config:
+        per_config = measure_per_config(L, synth, dev, flush, stream, hbm, rates, step_ns)
 
     # ---- end to end through the C ABI with HOST buffers, both modes: every step copies the
     # batch in from pinned host memory and the losses and gradients back out
@@ -401,6 +614,7 @@ def run_ours(args):
                    "cells_per_step": cells_per_step, "l2": "flushed between timed steps (256 MiB write)"},
         "per_mode": per_mode,
         "roofline": roofline,
+        "per_config": per_config,
         "cpu_baseline": cpu,
         "e2e": {"value": world * 2 * CELLS / (e2e_ms * 1e-3), "unit": "cells/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -440,6 +654,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--profile", type=int, default=0, help="run this many untimed steps (for ncu) and exit")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip the throughput / peak-memory / roofline figures of the other workloads")
     args = ap.parse_args()
     if args.profile:
         return run_profile(args)

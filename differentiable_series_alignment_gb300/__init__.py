@@ -21,7 +21,8 @@ import math
 import torch
 
 from ._lib import (CHECKPOINT, EXTENDED, FUSED, OP_BARYCENTER, OP_COST, OP_FWD_BWD, OP_NORMALIZED, OP_NORMALIZED_UNEQUAL,
-                   UNFUSED, SdtwError, sdtw_normalized_unequal,
+                   UNFUSED, SdtwError, sdtw_normalized_unequal, sdtw_normalized_backward,
+                   sdtw_normalized_unequal_backward, sdtw_debug_set_options,
                    auto_precision, load, sdtw_backward, sdtw_backward_cost, sdtw_barycenter_step,
                    sdtw_backward_varlen, sdtw_barycenter_step_clipped, sdtw_debug_set_wait, sdtw_forward_varlen,
                    sdtw_distance, sdtw_forward, sdtw_forward_cost, sdtw_last_device_status, sdtw_normalized,
@@ -36,6 +37,7 @@ __all__ = [
     "sdtw_debug_set_wait", "UNFUSED", "FUSED", "EXTENDED", "OP_FWD_BWD", "OP_NORMALIZED", "OP_BARYCENTER",
     "OP_COST", "auto_precision", "value_and_grad_host", "host_workspace", "sdtw_host_workspace_bytes",
     "sdtw_value_and_grad_host", "sdtw_normalized_unequal", "OP_NORMALIZED_UNEQUAL", "CHECKPOINT",
+    "sdtw_normalized_backward", "sdtw_normalized_unequal_backward", "sdtw_debug_set_options",
 ]
 
 
@@ -105,17 +107,14 @@ class _SoftDTWVarlenFn(torch.autograd.Function):
                 None if gy is None else gy.to(ctx.dtypes[1]), None, None, None, None)
 
 
-def _normalized_call(xc, yc, gamma, mode, loss, g, gx, gy):
-    """Equal lengths: one batch of 3B (sdtw_normalized); unequal: three batches of
-    their own shapes (sdtw_normalized_unequal)."""
+def _normalized_ws(xc, yc, mode):
+    """Workspace of the normalized entry for these shapes: one batch of 3B
+    (sdtw_normalized) at equal lengths, three batches of their own shapes
+    (sdtw_normalized_unequal) otherwise."""
     B, N, D = xc.shape
     M = yc.shape[1]
-    if N == M:
-        ws = workspace(OP_NORMALIZED, B, N, N, D, mode, xc.device)
-        sdtw_normalized(xc, yc, gamma, mode, loss, g, gx, gy, ws)
-    else:
-        ws = workspace(OP_NORMALIZED_UNEQUAL, B, N, M, D, mode, xc.device)
-        sdtw_normalized_unequal(xc, yc, gamma, mode, loss, g, gx, gy, ws)
+    op = OP_NORMALIZED if N == M else OP_NORMALIZED_UNEQUAL
+    return workspace(op, B, N, M, D, mode, xc.device)
 
 
 class _NormalizedFn(torch.autograd.Function):
@@ -125,19 +124,30 @@ class _NormalizedFn(torch.autograd.Function):
         if xc.shape[0] != yc.shape[0] or xc.shape[2] != yc.shape[2]:
             raise ValueError("normalized Soft-DTW needs x (B,N,D) and y (B,M,D)")
         loss = torch.empty(xc.shape[0], dtype=torch.float32, device=xc.device)
-        _normalized_call(xc, yc, gamma, mode, loss, None, None, None)
-        ctx.save_for_backward(xc, yc)
+        ws = _normalized_ws(xc, yc, mode)
+        if xc.shape[1] == yc.shape[1]:
+            sdtw_normalized(xc, yc, gamma, mode, loss, None, None, None, ws)
+        else:
+            sdtw_normalized_unequal(xc, yc, gamma, mode, loss, None, None, None, ws)
+        # the workspace holds the forward state of the three problems: the backward
+        # runs from it without repeating the forward
+        ctx.save_for_backward(xc, yc, ws)
         ctx.gamma, ctx.mode = gamma, mode
+        ctx.dtypes = (x.dtype, y.dtype)
         return loss
 
     @staticmethod
     def backward(ctx, grad):
-        xc, yc = ctx.saved_tensors
-        gx, gy = torch.empty_like(xc), torch.empty_like(yc)
-        loss = torch.empty(xc.shape[0], dtype=torch.float32, device=xc.device)
+        xc, yc, ws = ctx.saved_tensors
+        gx = torch.empty_like(xc) if ctx.needs_input_grad[0] else None
+        gy = torch.empty_like(yc) if ctx.needs_input_grad[1] else None
         g = grad.detach().to(torch.float32).contiguous()
-        _normalized_call(xc, yc, ctx.gamma, ctx.mode, loss, g, gx, gy)
-        return gx, gy, None, None
+        if xc.shape[1] == yc.shape[1]:
+            sdtw_normalized_backward(xc, yc, ctx.gamma, ctx.mode, g, gx, gy, ws)
+        else:
+            sdtw_normalized_unequal_backward(xc, yc, ctx.gamma, ctx.mode, g, gx, gy, ws)
+        return (None if gx is None else gx.to(ctx.dtypes[0]),
+                None if gy is None else gy.to(ctx.dtypes[1]), None, None)
 
 
 class _CostFn(torch.autograd.Function):
@@ -181,8 +191,11 @@ class SoftDTW:
 
     fused=False stores the (B,N,M) cost tensor; fused=True recomputes it inside
     the DP kernels. normalize=True gives s(x,y) - (s(x,x) + s(y,y))/2; x and y may
-    differ in length. extended=None picks the double-float forward state for
-    small gamma, long sequences or D > 64 (auto_precision); True/False forces it.
+    differ in length. extended=None picks the double-float forward state unless
+    the fp32 state is accurate enough for a batch-mean loss over these B pairs
+    (auto_precision: small gamma, long sequences, D > 256, or D > 4 with B < 32
+    select it); pass extended=True when the losses are summed rather than
+    averaged. True/False forces it.
     checkpoint=True (fused, fp32, D <= 64, not normalized) keeps no per-cell forward
     state: the backward recomputes it band by band (128 rows) from the boundary rows
     the forward kept; the workspace holds one band, and the backward's time grows
@@ -212,7 +225,7 @@ class SoftDTW:
         if self.checkpoint:
             mode |= CHECKPOINT
         elif self.extended is None:
-            mode |= auto_precision(self.gamma, x.shape[1], y.shape[1], x.shape[2])
+            mode |= auto_precision(self.gamma, x.shape[1], y.shape[1], x.shape[2], x.shape[0])
         elif self.extended:
             mode |= EXTENDED
         if x_lengths is not None or y_lengths is not None:
@@ -238,14 +251,17 @@ def value_and_grad_host(x: torch.Tensor, y: torch.Tensor, gamma: float = 1.0, fu
     B, N, D = x.shape
     M = y.shape[1]
     mode = FUSED if fused else UNFUSED
+    gl = torch.ones(B) if grad_loss is None else grad_loss.detach().to(torch.float32).contiguous()
     if extended is None:
-        mode |= auto_precision(gamma, N, M, D)
+        # the upstream weights are known here: the batch rule of auto_precision takes
+        # the batch size whose mean would give the largest of them
+        wmax = float(gl.abs().max()) if B > 0 else 1.0
+        mode |= auto_precision(gamma, N, M, D, int(math.ceil(1.0 / wmax - 1e-6)) if wmax > 0 else B)
     elif extended:
         mode |= EXTENDED
     pin = torch.cuda.is_available()
     xh = x.detach().to(torch.float32).contiguous()
     yh = y.detach().to(torch.float32).contiguous()
-    gl = torch.ones(B) if grad_loss is None else grad_loss.detach().to(torch.float32).contiguous()
     loss = torch.empty(B, pin_memory=pin)
     gx = torch.empty((B, N, D), pin_memory=pin)
     gy = torch.empty((B, M, D), pin_memory=pin)
@@ -285,7 +301,7 @@ def softdtw_barycenter(sequences: torch.Tensor, gamma: float = 1.0, max_iter: in
     v = torch.zeros_like(z)
     if lr_schedule not in (None, "cosine"):
         raise ValueError("lr_schedule must be None or 'cosine'")
-    mode = (FUSED if fused else UNFUSED) | auto_precision(gamma, T, T2, D)
+    mode = (FUSED if fused else UNFUSED) | auto_precision(gamma, T, T2, D, K)   # the loss is the mean over K
     ws = workspace(OP_BARYCENTER, K, T, T2, D, mode, X.device)
     losses = torch.empty(max_iter, dtype=torch.float32, device=X.device)
     clip = float(max_grad_norm) if max_grad_norm else 0.0

@@ -23,6 +23,14 @@ constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 unsigned long long g_wait_ns = kDefaultWaitNs;
 int g_skip_publish = 0;
 
+// Kernel choices forced by sdtw_debug_set_options (testing only; zeros: the
+// library's own choices).
+struct DebugOptions {
+    int warps_fwd, warps_bwd;   // warps per wavefront CTA (> 0: forced)
+    int dist_simt, fused_simt;  // difference-form cost kernels in the fp32 modes
+};
+DebugOptions g_dbg{};
+
 size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 // Workspace layout. The status word sits at offset 0 for every op.
@@ -49,8 +57,8 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     const bool fused = (mode & SDTW_FUSED) != 0, ext = (mode & SDTW_EXTENDED) != 0;
     const bool ckpt = (mode & SDTW_CHECKPOINT) != 0;
     if (op == SDTW_OP_COST && fused) return false;
-    // checkpointing recomputes bands with the tensor-core fused forward (fp32, D <= 64)
-    if (ckpt && (op != SDTW_OP_FWD_BWD || !fused || ext || D > 64)) return false;
+    // checkpointing recomputes bands with the tensor-core fused forward (fp32, D <= 256)
+    if (ckpt && (op != SDTW_OP_FWD_BWD || !fused || ext || D > 32 * kMaxTcKBlocks)) return false;
     const int P = (op == SDTW_OP_NORMALIZED) ? 3 * B : B;
     if (op == SDTW_OP_NORMALIZED) M = N;
     const int NB = (N + 31) / 32;
@@ -79,9 +87,9 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->bimg = o; if (!ext && xy) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, M, D));
     L->bimg2 = o;
     if (!ext && xy) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, ckpt ? (N < 32 * kBandBlocks ? N : 32 * kBandBlocks) : N, D));
-    // operand images and norms of the tensor-core costs (fp32 modes, D <= 64): the
+    // operand images and norms of the tensor-core costs (fp32 modes, D <= 256): the
     // unfused cost tensor and the fused forward's cost tiles
-    L->tc_cost = !ext && D <= 64 && xy;
+    L->tc_cost = !ext && D <= 32 * kMaxTcKBlocks && xy;
     L->ximg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, N, D));
     L->yimg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, M, D));
     L->xnorm = o; if (L->tc_cost) o = align_up(o + snorm_bytes(P, N));
@@ -95,18 +103,11 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
 template <typename T>
 T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
 
-int env_int(const char* name, int dflt)
-{
-    const char* s = std::getenv(name);
-    if (!s || !*s) return dflt;
-    return std::atoi(s);
-}
-
 // Warps per wavefront CTA: about one 32-row block per SM partition over the
 // whole batch, bounded by the shared memory a fused CTA needs.
 int choose_warps(int P, int NB, int D, bool fused, bool ext, bool backward, int num_sms)
 {
-    int W = env_int(backward ? "SDTW_WARPS_BWD" : "SDTW_WARPS_FWD", 0);
+    int W = backward ? g_dbg.warps_bwd : g_dbg.warps_fwd;
     if (W <= 0) {
         const long long blocks = (long long)P * NB;
         W = (int)((blocks + num_sms - 1) / num_sms);
@@ -149,8 +150,8 @@ sdtw_status check_common(const void* x, const void* y, int B, int N, int M, int 
     if (B < 1 || N < 1 || M < 1 || D < 1) return SDTW_ERR_EMPTY;
     if (!(gamma > 0.f) || !std::isfinite(gamma)) return SDTW_ERR_GAMMA;
     if (mode & ~(allow_ckpt ? 7 : 3)) return SDTW_ERR_ARG;
-    if ((mode & SDTW_CHECKPOINT) && (!(mode & SDTW_FUSED) || (mode & SDTW_EXTENDED) || D > 64 ||
-                                     env_int("SDTW_FUSED_SIMT", 0) != 0))
+    if ((mode & SDTW_CHECKPOINT) &&
+        (!(mode & SDTW_FUSED) || (mode & SDTW_EXTENDED) || D > 32 * kMaxTcKBlocks || g_dbg.fused_simt))
         return SDTW_ERR_ARG;
     if (!x || !y) return SDTW_ERR_ARG;
     if (B > 65535 / 3 || N > (1 << 24) || M > (1 << 24) || D > 400) return SDTW_ERR_TOO_LARGE;
@@ -189,7 +190,6 @@ WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamm
     q.colsum = at<double>(ws, L.colsum);
     q.rowsum = at<double>(ws, L.rowsum);
     q.rowbuf = at<float>(ws, L.rowbuf);
-    q.accurate = env_int("SDTW_ACCURATE", 0);
     q.ext = ext ? 1 : 0;
     q.loss = at<float>(ws, L.losses);
     q.status = at<int>(ws, L.status);
@@ -215,7 +215,7 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
     WaveParams q = wave_params(pr, L, ws, gamma, fused, ext, false);
     q.lens_n = lens_n;
     q.lens_m = lens_m;
-    const bool tc = L.tc_cost && env_int(fused ? "SDTW_FUSED_SIMT" : "SDTW_DIST_SIMT", 0) == 0;
+    const bool tc = L.tc_cost && !(fused ? g_dbg.fused_simt : g_dbg.dist_simt);
     if (fused && tc) {  // the tensor-core fused forward takes 128-row strips (4 warps)
         q.W = 4;
         q.S = (L.NB + 3) / 4;
@@ -228,8 +228,7 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
         if (cost) SDTW_CUDA(launch_skew_cost(cost, L.P, L.N, L.M, true, at<float>(ws, L.dsk), st));
         else if (!fused) SDTW_CUDA(launch_dist_skewed_x(pr, L.P, L.N, L.M, L.D, at<float2>(ws, L.dsk), st));
         q.loss = loss_out;
-        q.skip_publish = g_skip_publish;
-        g_skip_publish = 0;
+        q.skip_publish = debug_take_skip_publish();
         SDTW_CUDA(launch_forward_x(q, fused, st));
         return SDTW_OK;
     }
@@ -248,8 +247,7 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
         }
     }
     q.loss = loss_out;
-    q.skip_publish = g_skip_publish;
-    g_skip_publish = 0;
+    q.skip_publish = debug_take_skip_publish();
     if (L.ckpt) q.VH = nullptr;  // only the strips' boundary rows are kept (edge_f)
     if (fused && tc)
         SDTW_CUDA(launch_forward_tc(q, at<float>(ws, L.ximg), at<float>(ws, L.yimg), at<float>(ws, L.xnorm),
@@ -369,6 +367,22 @@ cudaStream_t side_stream()
     return streams[dev];
 }
 
+// Events that order side-stream work against the caller's stream. Each call site
+// has its own slots, created once per host thread and device and reused: a slot
+// is recorded and then waited on before the same thread records it again, and
+// cudaStreamWaitEvent takes the record current at the time of the call. (The
+// host-batch entry calls sdtw_backward inside its chunks, hence separate slots.)
+enum EventSlot { kEvBwdFork, kEvBwdJoin, kEvHostFork, kEvHostJoin, kEvNormFork, kEvNormJoin, kEvSlots };
+cudaEvent_t cached_event(EventSlot slot)
+{
+    thread_local cudaEvent_t ev[64][kEvSlots] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    cudaEvent_t& e = ev[dev][slot];
+    if (!e && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) e = nullptr;
+    return e;
+}
+
 // Streams on which the chunks of a host-buffer call run side by side (created
 // once per device, non-blocking; ordered against the caller's stream by events).
 constexpr int kMaxChunks = 8;
@@ -478,7 +492,7 @@ sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void
     g.coef = coef;
     g.omod = B;
     g.accumulate = accumulate;
-    const bool simt = (mode & SDTW_EXTENDED) != 0 || env_int("SDTW_GRAD_SIMT", 0) != 0;
+    const bool simt = (mode & SDTW_EXTENDED) != 0;
     int* status = at<int>(ws, L.status);
     float* img_rows = at<float>(ws, L.bimg);
     float* img_cols = at<float>(ws, L.bimg2);
@@ -495,6 +509,13 @@ sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void
         SDTW_CUDA(simt ? launch_grad_cols(g, st) : launch_grad_tc(g, true, img_cols, status, st));
     }
     return SDTW_OK;
+}
+
+// out[i] = exp2_neg(x[i]): the library's own exp2 of the double-float path, for its test.
+__global__ void exp2_neg_kernel(const float* x, float* out, int n)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] = exp2_neg(x[i]);
 }
 
 __global__ void combine_normalized_kernel(const float* l, int B, float* loss)
@@ -514,6 +535,16 @@ sdtw_status check_cost(const float* C, int B, int N, int M, float gamma, int mod
 }
 
 }  // namespace
+
+namespace sdtw {
+unsigned long long debug_wait_ns() { return g_wait_ns; }
+int debug_take_skip_publish()
+{
+    const int v = g_skip_publish;
+    g_skip_publish = 0;
+    return v;
+}
+}  // namespace sdtw
 
 extern "C" {
 
@@ -589,47 +620,48 @@ sdtw_status sdtw_backward_varlen(const float* x, const float* y, const int* x_le
     pr.B = B;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (L.ckpt) {
-        if (env_int("SDTW_GRAD_SIMT", 0) != 0) return SDTW_ERR_ARG;
         return run_backward_ckpt(pr, L, ws, gamma, (int)mode, grad_loss, grad_x, grad_y, st, x_lengths, y_lengths);
     }
     // The gradient operand images depend on x and y only: they are built on a side
     // stream while the backward wavefront runs (it leaves most of each SM idle).
     cudaStream_t side = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
-    const bool tc_grads = (grad_x || grad_y) && !(mode & SDTW_EXTENDED) && env_int("SDTW_GRAD_SIMT", 0) == 0;
-    if (tc_grads && (side = side_stream()) != nullptr &&
-        cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
-        cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess) {
+    const bool tc_grads = (grad_x || grad_y) && !(mode & SDTW_EXTENDED);
+    if (tc_grads && (side = side_stream()) != nullptr && (fork = cached_event(kEvBwdFork)) != nullptr &&
+        (join = cached_event(kEvBwdJoin)) != nullptr) {
         GradParams g = grad_params(pr, 0, B, L, ws);
         bool launched = cudaEventRecord(fork, st) == cudaSuccess && cudaStreamWaitEvent(side, fork, 0) == cudaSuccess &&
                         launch_bimg(g, grad_x ? at<float>(ws, L.bimg) : nullptr,
                                     grad_y ? at<float>(ws, L.bimg2) : nullptr, side) == cudaSuccess &&
                         cudaEventRecord(join, side) == cudaSuccess;
-        cudaEventDestroy(fork);  // released once complete
-        if (!launched) {
-            cudaEventDestroy(join);
-            return SDTW_ERR_CUDA;
-        }
+        if (!launched) return SDTW_ERR_CUDA;
+    } else {
+        join = nullptr;
     }
     s = run_backward(pr, L, ws, gamma, (int)mode, st, x_lengths, y_lengths);
     if (s == SDTW_OK && (grad_x || grad_y))
         s = run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, (int)mode, st, join);
-    if (join) {
-        if (s != SDTW_OK) cudaStreamWaitEvent(st, join, 0);  // keep the side work ordered before later calls
-        cudaEventDestroy(join);
-    }
+    if (join && s != SDTW_OK) cudaStreamWaitEvent(st, join, 0);  // keep the side work ordered before later calls
     return s;
 }
 
-sdtw_status sdtw_normalized(const float* x, const float* y, int B, int N, int D, float gamma, sdtw_mode mode,
-                            float* loss, const float* grad_loss, float* grad_x, float* grad_y, void* ws,
-                            size_t ws_bytes, void* stream)
+}  // extern "C"
+
+namespace {
+
+// Normalized Soft-DTW of equal lengths over one batch of 3B problems. fwd: the
+// forward and the combined losses; bwd: the backward wavefronts and the ordered
+// gradient launches, reading the state the forward left in `ws`.
+sdtw_status normalized_impl(const float* x, const float* y, int B, int N, int D, float gamma, int mode, float* loss,
+                            const float* grad_loss, float* grad_x, float* grad_y, void* ws, size_t ws_bytes,
+                            cudaStream_t st, bool fwd, bool bwd)
 {
-    sdtw_status s = check_common(x, y, B, N, N, D, gamma, (int)mode);
+    sdtw_status s = check_common(x, y, B, N, N, D, gamma, mode);
     if (s != SDTW_OK) return s;
-    if (!loss) return SDTW_ERR_ARG;
+    if (fwd && !loss) return SDTW_ERR_ARG;
+    if (!fwd && !grad_loss) return SDTW_ERR_ARG;
     Layout L;
-    make_layout(SDTW_OP_NORMALIZED, B, N, N, D, (int)mode, &L);
+    make_layout(SDTW_OP_NORMALIZED, B, N, N, D, mode, &L);
     if ((s = check_ws(ws, ws_bytes, L)) != SDTW_OK) return s;
     const long long st_ = (long long)N * D;
     Problems pr{};
@@ -638,22 +670,111 @@ sdtw_status sdtw_normalized(const float* x, const float* y, int B, int N, int D,
     pr.xs[2] = y; pr.ys[2] = y;   // s(y, y)
     for (int k = 0; k < 3; ++k) { pr.xstride[k] = st_; pr.ystride[k] = st_; }
     pr.B = B;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    float* l3 = at<float>(ws, L.losses);
-    if ((s = run_forward(pr, L, ws, gamma, (int)mode, l3, st)) != SDTW_OK) return s;
-    combine_normalized_kernel<<<(B + 255) / 256, 256, 0, st>>>(l3, B, loss);
-    SDTW_CUDA(cudaGetLastError());
-    if (!grad_loss || (!grad_x && !grad_y)) return SDTW_OK;
-    if ((s = run_backward(pr, L, ws, gamma, (int)mode, st)) != SDTW_OK) return s;
+    if (fwd) {
+        float* l3 = at<float>(ws, L.losses);
+        if ((s = run_forward(pr, L, ws, gamma, mode, l3, st)) != SDTW_OK) return s;
+        combine_normalized_kernel<<<(B + 255) / 256, 256, 0, st>>>(l3, B, loss);
+        SDTW_CUDA(cudaGetLastError());
+    }
+    if (!bwd || !grad_loss || (!grad_x && !grad_y)) return SDTW_OK;
+    if ((s = run_backward(pr, L, ws, gamma, mode, st)) != SDTW_OK) return s;
     // grad_x = g [gx(x,y) - (gx(x,x) + gy(x,x))/2];  grad_y = g [gy(x,y) - (gx(y,y) + gy(y,y))/2]
-    if ((s = run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, (int)mode, st)) != SDTW_OK) return s;
+    if ((s = run_grads(pr, 0, B, L, ws, grad_loss, 1.f, grad_x, grad_y, 0, mode, st)) != SDTW_OK) return s;
     if (grad_x) {
-        if ((s = run_grads(pr, 1, B, L, ws, grad_loss, -0.5f, grad_x, grad_x, 1, (int)mode, st)) != SDTW_OK) return s;
+        if ((s = run_grads(pr, 1, B, L, ws, grad_loss, -0.5f, grad_x, grad_x, 1, mode, st)) != SDTW_OK) return s;
     }
     if (grad_y) {
-        if ((s = run_grads(pr, 2, B, L, ws, grad_loss, -0.5f, grad_y, grad_y, 1, (int)mode, st)) != SDTW_OK) return s;
+        if ((s = run_grads(pr, 2, B, L, ws, grad_loss, -0.5f, grad_y, grad_y, 1, mode, st)) != SDTW_OK) return s;
     }
     return SDTW_OK;
+}
+
+// Normalized Soft-DTW of unequal lengths: three batches (N x M, N x N, M x M) on
+// three streams. fwd / bwd as for normalized_impl.
+sdtw_status normalized_unequal_impl(const float* x, const float* y, int B, int N, int M, int D, float gamma, int mode,
+                                    float* loss, const float* grad_loss, float* grad_x, float* grad_y, void* ws,
+                                    size_t ws_bytes, cudaStream_t st, bool fwd, bool bwd)
+{
+    sdtw_status s = check_common(x, y, B, N, M, D, gamma, mode);
+    if (s != SDTW_OK) return s;
+    if (fwd && !loss) return SDTW_ERR_ARG;
+    if (!fwd && !grad_loss) return SDTW_ERR_ARG;
+    Norm3Layout H;
+    if (!make_norm3_layout(B, N, M, D, mode, &H)) return SDTW_ERR_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 || ws_bytes < H.total) return SDTW_ERR_WORKSPACE;
+    const bool grads = bwd && grad_loss && (grad_x || grad_y);
+    if (!fwd && !grads) return SDTW_OK;
+    Problems pr[3] = {};
+    const float* xs[3] = {x, x, y};
+    const float* ys[3] = {y, x, y};
+    const long long xst[3] = {(long long)N * D, (long long)N * D, (long long)M * D};
+    const long long yst[3] = {(long long)M * D, (long long)N * D, (long long)M * D};
+    void* wsk[3];
+    for (int k = 0; k < 3; ++k) {
+        pr[k].xs[0] = xs[k]; pr[k].ys[0] = ys[k];
+        pr[k].xstride[0] = xst[k]; pr[k].ystride[0] = yst[k];
+        pr[k].B = B;
+        wsk[k] = at<char>(ws, H.off[k]);
+    }
+    cudaStream_t cs[kMaxChunks];
+    if (!chunk_streams(cs)) return SDTW_ERR_CUDA;
+    // The three wavefront pairs are independent and latency-bound: they run side by
+    // side on three streams, each sized for a third of the SMs.
+    cudaEvent_t fork = cached_event(kEvNormFork), join = cached_event(kEvNormJoin);
+    if (!fork || !join || cudaEventRecord(fork, st) != cudaSuccess) return SDTW_ERR_CUDA;
+    const int prev_share = t_sm_share;
+    t_sm_share = num_sms() / 3 > 0 ? num_sms() / 3 : 1;
+    for (int k = 0; k < 3; ++k) {
+        if (s == SDTW_OK && cudaStreamWaitEvent(cs[k], fork, 0) != cudaSuccess) s = SDTW_ERR_CUDA;
+        if (s == SDTW_OK && fwd)
+            s = run_forward(pr[k], H.L[k], wsk[k], gamma, mode, at<float>(wsk[k], H.L[k].losses), cs[k]);
+        if (s == SDTW_OK && grads) s = run_backward(pr[k], H.L[k], wsk[k], gamma, mode, cs[k]);
+        // joined whatever happened, so later work stays ordered
+        if ((cudaEventRecord(join, cs[k]) != cudaSuccess || cudaStreamWaitEvent(st, join, 0) != cudaSuccess) &&
+            s == SDTW_OK)
+            s = SDTW_ERR_CUDA;
+    }
+    t_sm_share = prev_share;
+    if (s != SDTW_OK) return s;
+    if (fwd) {
+        combine3_normalized_kernel<<<(B + 255) / 256, 256, 0, st>>>(at<float>(wsk[0], H.L[0].losses),
+                                                                    at<float>(wsk[1], H.L[1].losses),
+                                                                    at<float>(wsk[2], H.L[2].losses), B, loss);
+        SDTW_CUDA(cudaGetLastError());
+    }
+    if (grads) {
+        // grad_x = g [gx(x,y) - (gx(x,x) + gy(x,x))/2];  grad_y = g [gy(x,y) - (gx(y,y) + gy(y,y))/2]
+        s = run_grads(pr[0], 0, B, H.L[0], wsk[0], grad_loss, 1.f, grad_x, grad_y, 0, mode, st);
+        if (s == SDTW_OK && grad_x)
+            s = run_grads(pr[1], 0, B, H.L[1], wsk[1], grad_loss, -0.5f, grad_x, grad_x, 1, mode, st);
+        if (s == SDTW_OK && grad_y)
+            s = run_grads(pr[2], 0, B, H.L[2], wsk[2], grad_loss, -0.5f, grad_y, grad_y, 1, mode, st);
+        if (s != SDTW_OK) return s;
+    }
+    gather3_status_kernel<<<1, 32, 0, st>>>(at<int>(wsk[0], H.L[0].status), at<int>(wsk[1], H.L[1].status),
+                                            at<int>(wsk[2], H.L[2].status));
+    SDTW_CUDA(cudaGetLastError());
+    return SDTW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sdtw_status sdtw_normalized(const float* x, const float* y, int B, int N, int D, float gamma, sdtw_mode mode,
+                            float* loss, const float* grad_loss, float* grad_x, float* grad_y, void* ws,
+                            size_t ws_bytes, void* stream)
+{
+    return normalized_impl(x, y, B, N, D, gamma, (int)mode, loss, grad_loss, grad_x, grad_y, ws, ws_bytes,
+                           static_cast<cudaStream_t>(stream), true, true);
+}
+
+sdtw_status sdtw_normalized_backward(const float* x, const float* y, int B, int N, int D, float gamma,
+                                     sdtw_mode mode, const float* grad_loss, float* grad_x, float* grad_y, void* ws,
+                                     size_t ws_bytes, void* stream)
+{
+    return normalized_impl(x, y, B, N, D, gamma, (int)mode, nullptr, grad_loss, grad_x, grad_y, ws, ws_bytes,
+                           static_cast<cudaStream_t>(stream), false, true);
 }
 
 sdtw_status sdtw_barycenter_step(float* z, float* m, float* v, int t, const float* X, int K, int T, int T2, int D,
@@ -735,73 +856,16 @@ sdtw_status sdtw_normalized_unequal(const float* x, const float* y, int B, int N
                                     sdtw_mode mode, float* loss, const float* grad_loss, float* grad_x,
                                     float* grad_y, void* ws, size_t ws_bytes, void* stream)
 {
-    sdtw_status s = check_common(x, y, B, N, M, D, gamma, (int)mode);
-    if (s != SDTW_OK) return s;
-    if (!loss) return SDTW_ERR_ARG;
-    Norm3Layout H;
-    if (!make_norm3_layout(B, N, M, D, (int)mode, &H)) return SDTW_ERR_ARG;
-    if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 || ws_bytes < H.total) return SDTW_ERR_WORKSPACE;
-    const bool grads = grad_loss && (grad_x || grad_y);
-    Problems pr[3] = {};
-    const float* xs[3] = {x, x, y};
-    const float* ys[3] = {y, x, y};
-    const long long xst[3] = {(long long)N * D, (long long)N * D, (long long)M * D};
-    const long long yst[3] = {(long long)M * D, (long long)N * D, (long long)M * D};
-    void* wsk[3];
-    for (int k = 0; k < 3; ++k) {
-        pr[k].xs[0] = xs[k]; pr[k].ys[0] = ys[k];
-        pr[k].xstride[0] = xst[k]; pr[k].ystride[0] = yst[k];
-        pr[k].B = B;
-        wsk[k] = at<char>(ws, H.off[k]);
-    }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaStream_t cs[kMaxChunks];
-    if (!chunk_streams(cs)) return SDTW_ERR_CUDA;
-    // The three wavefront pairs are independent and latency-bound: they run side by
-    // side on three streams, each sized for a third of the SMs.
-    cudaEvent_t fork = nullptr;
-    SDTW_CUDA(cudaEventCreateWithFlags(&fork, cudaEventDisableTiming));
-    if (cudaEventRecord(fork, st) != cudaSuccess) {
-        cudaEventDestroy(fork);
-        return SDTW_ERR_CUDA;
-    }
-    const int prev_share = t_sm_share;
-    t_sm_share = num_sms() / 3 > 0 ? num_sms() / 3 : 1;
-    for (int k = 0; k < 3; ++k) {
-        if (s == SDTW_OK && cudaStreamWaitEvent(cs[k], fork, 0) != cudaSuccess) s = SDTW_ERR_CUDA;
-        if (s == SDTW_OK)
-            s = run_forward(pr[k], H.L[k], wsk[k], gamma, (int)mode, at<float>(wsk[k], H.L[k].losses), cs[k]);
-        if (s == SDTW_OK && grads) s = run_backward(pr[k], H.L[k], wsk[k], gamma, (int)mode, cs[k]);
-        cudaEvent_t join = nullptr;  // joined whatever happened, so later work stays ordered
-        if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
-            if (s == SDTW_OK) s = SDTW_ERR_CUDA;
-            continue;
-        }
-        if ((cudaEventRecord(join, cs[k]) != cudaSuccess || cudaStreamWaitEvent(st, join, 0) != cudaSuccess) &&
-            s == SDTW_OK)
-            s = SDTW_ERR_CUDA;
-        cudaEventDestroy(join);
-    }
-    t_sm_share = prev_share;
-    cudaEventDestroy(fork);
-    if (s != SDTW_OK) return s;
-    combine3_normalized_kernel<<<(B + 255) / 256, 256, 0, st>>>(at<float>(wsk[0], H.L[0].losses),
-                                                                at<float>(wsk[1], H.L[1].losses),
-                                                                at<float>(wsk[2], H.L[2].losses), B, loss);
-    SDTW_CUDA(cudaGetLastError());
-    if (grads) {
-        // grad_x = g [gx(x,y) - (gx(x,x) + gy(x,x))/2];  grad_y = g [gy(x,y) - (gx(y,y) + gy(y,y))/2]
-        s = run_grads(pr[0], 0, B, H.L[0], wsk[0], grad_loss, 1.f, grad_x, grad_y, 0, (int)mode, st);
-        if (s == SDTW_OK && grad_x)
-            s = run_grads(pr[1], 0, B, H.L[1], wsk[1], grad_loss, -0.5f, grad_x, grad_x, 1, (int)mode, st);
-        if (s == SDTW_OK && grad_y)
-            s = run_grads(pr[2], 0, B, H.L[2], wsk[2], grad_loss, -0.5f, grad_y, grad_y, 1, (int)mode, st);
-        if (s != SDTW_OK) return s;
-    }
-    gather3_status_kernel<<<1, 32, 0, st>>>(at<int>(wsk[0], H.L[0].status), at<int>(wsk[1], H.L[1].status),
-                                            at<int>(wsk[2], H.L[2].status));
-    SDTW_CUDA(cudaGetLastError());
-    return SDTW_OK;
+    return normalized_unequal_impl(x, y, B, N, M, D, gamma, (int)mode, loss, grad_loss, grad_x, grad_y, ws, ws_bytes,
+                                   static_cast<cudaStream_t>(stream), true, true);
+}
+
+sdtw_status sdtw_normalized_unequal_backward(const float* x, const float* y, int B, int N, int M, int D,
+                                             float gamma, sdtw_mode mode, const float* grad_loss, float* grad_x,
+                                             float* grad_y, void* ws, size_t ws_bytes, void* stream)
+{
+    return normalized_unequal_impl(x, y, B, N, M, D, gamma, (int)mode, nullptr, grad_loss, grad_x, grad_y, ws,
+                                   ws_bytes, static_cast<cudaStream_t>(stream), false, true);
 }
 
 size_t sdtw_host_workspace_bytes(int B, int N, int M, int D, sdtw_mode mode, int chunks)
@@ -825,12 +889,8 @@ sdtw_status sdtw_value_and_grad_host(const float* x, const float* y, const float
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaStream_t cs[kMaxChunks];
     if (!chunk_streams(cs)) return SDTW_ERR_CUDA;
-    cudaEvent_t fork = nullptr;
-    SDTW_CUDA(cudaEventCreateWithFlags(&fork, cudaEventDisableTiming));
-    if (cudaEventRecord(fork, st) != cudaSuccess) {
-        cudaEventDestroy(fork);
-        return SDTW_ERR_CUDA;
-    }
+    cudaEvent_t fork = cached_event(kEvHostFork), join = cached_event(kEvHostJoin);
+    if (!fork || !join || cudaEventRecord(fork, st) != cudaSuccess) return SDTW_ERR_CUDA;
     const int prev_share = t_sm_share;
     t_sm_share = num_sms() / H.chunks > 0 ? num_sms() / H.chunks : 1;
     const size_t xr = (size_t)N * D, yr = (size_t)M * D;  // floats per problem
@@ -864,18 +924,11 @@ sdtw_status sdtw_value_and_grad_host(const float* x, const float* y, const float
             if (!ok) s = SDTW_ERR_CUDA;
         }
         // join, whatever happened, so that later work on the caller's stream stays ordered
-        cudaEvent_t join = nullptr;
-        if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
-            s = SDTW_ERR_CUDA;
-            break;
-        }
         if ((cudaEventRecord(join, sc) != cudaSuccess || cudaStreamWaitEvent(st, join, 0) != cudaSuccess) &&
             s == SDTW_OK)
             s = SDTW_ERR_CUDA;
-        cudaEventDestroy(join);  // released once complete
     }
     t_sm_share = prev_share;
-    cudaEventDestroy(fork);
     if (s != SDTW_OK) return s;
     gather_status_kernel<<<1, 32, 0, st>>>(at<int>(ws, 0), at<char>(ws, H.ws0), H.ws_stride, H.chunks);
     SDTW_CUDA(cudaGetLastError());
@@ -914,6 +967,23 @@ void sdtw_debug_set_wait(double seconds, int skip_publish)
 {
     g_wait_ns = (seconds > 0.0) ? (unsigned long long)(seconds * 1e9) : kDefaultWaitNs;
     g_skip_publish = skip_publish ? 1 : 0;
+}
+
+sdtw_status sdtw_debug_exp2_neg(const float* x, float* out, int n, void* stream)
+{
+    if (n < 0 || (n > 0 && (!x || !out))) return SDTW_ERR_ARG;
+    if (n == 0) return SDTW_OK;
+    exp2_neg_kernel<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, out, n);
+    SDTW_CUDA(cudaGetLastError());
+    return SDTW_OK;
+}
+
+void sdtw_debug_set_options(int warps_fwd, int warps_bwd, int dist_simt, int fused_simt)
+{
+    g_dbg.warps_fwd = warps_fwd > 0 ? warps_fwd : 0;
+    g_dbg.warps_bwd = warps_bwd > 0 ? warps_bwd : 0;
+    g_dbg.dist_simt = dist_simt ? 1 : 0;
+    g_dbg.fused_simt = fused_simt ? 1 : 0;
 }
 
 }  // extern "C"

@@ -98,7 +98,7 @@ __device__ __forceinline__ float exp2_neg(float x) {
 }
 
 // Math variants of the DP kernels: ACC selects the unbiased exp2_neg above and
-// log2f, otherwise the MUFU approximations.
+// log2f (the double-float path), otherwise the MUFU approximations.
 template <bool ACC> __device__ __forceinline__ float dp_exp2(float x) { return ACC ? exp2_neg(x) : ex2(x); }
 template <bool ACC> __device__ __forceinline__ float dp_log2(float x) { return ACC ? log2f(x) : lg2(x); }
 

@@ -44,8 +44,8 @@ constexpr uint32_t kYHalf = kColTile * 128;    // one K-block of 64 y rows, hi o
 constexpr int kStg = 63 * 32;                  // per-warp skew staging (floats)
 
 // grid (Lpad/32, P, 2): z = 0 writes the x image, z = 1 the y image. block 256.
-// Rows past the sequence end are zero (image and norm). KB <= 2: every thread
-// issues all of its loads (at most 8) before the first shared store.
+// Rows past the sequence end are zero (image and norm). Each thread loads its
+// values in batches of 8, all issued before their shared stores.
 __global__ void __launch_bounds__(256) simg_kernel(Problems pr, int N, int M, int D, int KB, float* __restrict__ ximg,
                                                    float* __restrict__ yimg, float* __restrict__ xnorm,
                                                    float* __restrict__ ynorm)
@@ -60,19 +60,21 @@ __global__ void __launch_bounds__(256) simg_kernel(Problems pr, int N, int M, in
     float* img = isy ? yimg : ximg;
     float* nrm = isy ? ynorm : xnorm;
     const int D32 = 32 * KB, ld = D32 + 1;
-    const int n = 32 * D32 / 256;  // values per thread: 4 or 8
-    float v[8];
+    const int n = 32 * D32 / 256;  // values per thread: 4 per K-block
+    for (int u0 = 0; u0 < n; u0 += 8) {
+        float v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int idx = threadIdx.x + 256 * u;
-        const int r = idx / D32, k = idx - r * D32;
-        v[u] = (u < n && r0 + r < L && k < D) ? src[(size_t)(r0 + r) * D + k] : 0.f;
-    }
+        for (int u = 0; u < 8; ++u) {
+            const int idx = threadIdx.x + 256 * (u0 + u);
+            const int r = idx / D32, k = idx - r * D32;
+            v[u] = (u0 + u < n && r0 + r < L && k < D) ? src[(size_t)(r0 + r) * D + k] : 0.f;
+        }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int idx = threadIdx.x + 256 * u;
-        const int r = idx / D32, k = idx - r * D32;
-        if (u < n) t[r * ld + k] = v[u];
+        for (int u = 0; u < 8; ++u) {
+            const int idx = threadIdx.x + 256 * (u0 + u);
+            const int r = idx / D32, k = idx - r * D32;
+            if (u0 + u < n) t[r * ld + k] = v[u];
+        }
     }
     __syncthreads();
     {
@@ -112,6 +114,54 @@ __global__ void __launch_bounds__(256) simg_kernel(Problems pr, int N, int M, in
         float* row = img + simg_offset(p, KB, kb, 0, Lpad, r0 + r) + 4 * (c8 ^ (r & 7));
         *reinterpret_cast<float4*>(row) = hi;
         *reinterpret_cast<float4*>(row + part) = lo;
+    }
+}
+
+// Epilogue warps 0-7 of the cost kernels: warp w reads TMEM lane quarter w mod 4
+// (rows r0 + 32(w mod 4) + lane) and the 32-column half w / 4 of each 64-column
+// tile (x_hi . y_hi + x_lo . y_hi in columns [0, 64), x_hi . y_lo in [64, 128) of
+// the tile's slot), releases the slot, forms C = |x|^2 + |y|^2 - 2 x.y clamped at 0
+// and writes the skewed layout through a per-warp staging tile (128-byte rows).
+__device__ __forceinline__ void cost_epilogue(int N, int M, int p, int r0, int nC, uint32_t tmem,
+                                              uint64_t* s_tfull, uint64_t* s_tfree, const float* __restrict__ xnorm,
+                                              const float* __restrict__ ynorm, float* __restrict__ Dsk, float* stg,
+                                              bool& ok, int* status)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Npad = (N + kTile - 1) / kTile * kTile, Mpad = (M + kTile - 1) / kTile * kTile;
+    const int NB = (N + 31) / 32;
+    const int q = warp & 3, half = warp >> 2;
+    const int rb = (r0 >> 5) + q;
+    const int row = r0 + 32 * q + lane;
+    const float nx = xnorm[(size_t)p * Npad + row];
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+    float* out = (rb < NB) ? Dsk + skew_index(N, M, p, rb, 0, lane) : nullptr;
+    for (int c = 0; c < nC; ++c) {
+        const int t = c & 1;
+        wait_ok(ok, smem_u32(&s_tfull[t]), (uint32_t)((c >> 1) & 1), status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        fence_after_sync();
+        float a[32], b[32];
+        tmem_ld32(trow + (uint32_t)(t * 2 * kColTile + 32 * half), a);
+        tmem_ld32(trow + (uint32_t)(t * 2 * kColTile + kColTile + 32 * half), b);
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s_tfree[t]));
+        const int cb = c * kColTile + 32 * half;  // first column of this warp's chunk
+        if (out == nullptr || cb >= M) continue;  // warp-uniform
+        const float nyv = ynorm[(size_t)p * Mpad + cb + lane];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float ny = __shfl_sync(0xffffffffu, nyv, j);
+            stg[(j + lane) * 32 + lane] = fmaxf(nx + ny - 2.f * (a[j] + b[j]), 0.f);
+        }
+        __syncwarp();
+        // skewed slot cb + tt holds column (tt - lane) of this chunk for this lane's row
+        for (int tt = 0; tt < 63; ++tt) {
+            const int j = tt - lane;
+            if (j >= 0 && j < 32 && cb + j < M && row < N) out[(long long)(cb + tt) * 32] = stg[tt * 32 + lane];
+        }
+        __syncwarp();
     }
 }
 
@@ -223,40 +273,119 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else {
-        // warp w: TMEM lane quarter w mod 4 (rows r0 + 32(w mod 4) + lane), 32-column half w / 4 of each tile
-        const int q = warp & 3, half = warp >> 2;
-        const int rb = (r0 >> 5) + q;
-        const int row = r0 + 32 * q + lane;
-        const float nx = xnorm[(size_t)p * Npad + row];
-        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
-        float* out = (rb < NB) ? Dsk + skew_index(N, M, p, rb, 0, lane) : nullptr;
-        for (int c = 0; c < nC; ++c) {
-            const int t = c & 1;
-            wait_ok(ok, smem_u32(&s_tfull[t]), (uint32_t)((c >> 1) & 1), status);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            fence_after_sync();
-            float a[32], b[32];
-            tmem_ld32(trow + (uint32_t)(t * 2 * kColTile + 32 * half), a);
-            tmem_ld32(trow + (uint32_t)(t * 2 * kColTile + kColTile + 32 * half), b);
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s_tfree[t]));
-            const int cb = c * kColTile + 32 * half;  // first column of this warp's chunk
-            if (out == nullptr || cb >= M) continue;  // warp-uniform
-            const float nyv = ynorm[(size_t)p * Mpad + cb + lane];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float ny = __shfl_sync(0xffffffffu, nyv, j);
-                stg[(j + lane) * 32 + lane] = fmaxf(nx + ny - 2.f * (a[j] + b[j]), 0.f);
-            }
-            __syncwarp();
-            // skewed slot cb + tt holds column (tt - lane) of this chunk for this lane's row
-            for (int tt = 0; tt < 63; ++tt) {
-                const int j = tt - lane;
-                if (j >= 0 && j < 32 && cb + j < M && row < N) out[(long long)(cb + tt) * 32] = stg[tt * 32 + lane];
-            }
-            __syncwarp();
+        cost_epilogue(N, M, p, r0, nC, tmem, s_tfull, s_tfree, xnorm, ynorm, Dsk, stg, ok, status);
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after_sync();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+
+// Wide features (more than two K-blocks): the same CTA shape and epilogue, but the
+// 128 x rows do not stay in shared memory. Every K-block of a tile comes as one
+// stage of a kStages-deep ring: the tile's x rows (hi, lo) and y rows (hi, lo) of
+// that K-block, one expect-tx mbarrier per stage. The x rows are read again for
+// every 64-column tile (from L2: 4 bytes per cell and K-block).
+//   s_full[s]  stage s landed         s_empty[s] the MMAs reading stage s are done
+//   s_tfull[t] / s_tfree[t] as above
+constexpr int kStages = 3;
+constexpr uint32_t kStageBytes = 2 * kBlockBytes + 2 * kYHalf;   // A hi, A lo, B hi, B lo
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    dist_tc_stream_kernel(int N, int M, int KB, const float* __restrict__ ximg, const float* __restrict__ yimg,
+                          const float* __restrict__ xnorm, const float* __restrict__ ynorm, float* __restrict__ Dsk,
+                          int* status)
+{
+    extern __shared__ unsigned char smem_dyn[];
+    __shared__ uint64_t s_done, s_full[kStages], s_empty[kStages], s_tfull[2], s_tfree[2];
+    __shared__ uint32_t s_tmem;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int p = blockIdx.y, r0 = blockIdx.x * kTile;
+    const int Npad = (N + kTile - 1) / kTile * kTile, Mpad = (M + kTile - 1) / kTile * kTile;
+    const int nC = (M + kColTile - 1) / kColTile;
+
+    // shared memory (1 KiB aligned): kStages x [A hi | A lo | B hi (64 rows) | B lo], staging
+    unsigned char* base = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+    float* stg = reinterpret_cast<float*>(base + kStages * kStageBytes) + warp * kStg;
+
+    if (tid == 0) {
+        mbar_init(smem_u32(&s_done), 1);
+        for (int e = 0; e < kStages; ++e) {
+            mbar_init(smem_u32(&s_full[e]), 1);
+            mbar_init(smem_u32(&s_empty[e]), 1);
         }
+        for (int e = 0; e < 2; ++e) {
+            mbar_init(smem_u32(&s_tfull[e]), 1);
+            mbar_init(smem_u32(&s_tfree[e]), kTcWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tmem_alloc(&s_tmem, 256);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = s_tmem;
+    bool ok = true;
+
+    if (warp == kTcWarps) {
+        if (lane == 0) {
+            const int G = nC * KB;   // stages in all: K-block kb of tile c is stage c * KB + kb
+            int g_last[kStages];
+            for (int e = 0; e < kStages; ++e) g_last[e] = -1;
+            auto issue = [&](int g) {
+                const int c = g / KB, kb = g - c * KB, e = g % kStages;
+                unsigned char* st = base + e * kStageBytes;
+                const uint32_t bar = smem_u32(&s_full[e]);
+                mbar_expect_tx(bar, kStageBytes);
+                bulk_g2s(smem_u32(st), ximg + simg_offset(p, KB, kb, 0, Npad, r0), kBlockBytes, bar);
+                bulk_g2s(smem_u32(st + kBlockBytes), ximg + simg_offset(p, KB, kb, 1, Npad, r0), kBlockBytes, bar);
+                bulk_g2s(smem_u32(st + 2 * kBlockBytes), yimg + simg_offset(p, KB, kb, 0, Mpad, c * kColTile), kYHalf,
+                         bar);
+                bulk_g2s(smem_u32(st + 2 * kBlockBytes + kYHalf), yimg + simg_offset(p, KB, kb, 1, Mpad, c * kColTile),
+                         kYHalf, bar);
+                g_last[e] = g;
+            };
+            for (int g = 0; g < kStages && g < G; ++g) issue(g);
+            const uint32_t id2 = idesc_tf32(kTile, 2 * kColTile), id1 = idesc_tf32(kTile, kColTile);
+            for (int g = 0; g < G && ok; ++g) {
+                const int c = g / KB, kb = g - c * KB, e = g % kStages, t = c & 1;
+                if (kb == 0 && c >= 2) wait_ok(ok, smem_u32(&s_tfree[t]), (uint32_t)(((c - 2) >> 1) & 1), status);
+                wait_ok(ok, smem_u32(&s_full[e]), (uint32_t)((g / kStages) & 1), status);
+                if (!ok) break;
+                fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)(t * 2 * kColTile);
+                const uint32_t ah = smem_u32(base + e * kStageBytes), al = ah + kBlockBytes, bh = ah + 2 * kBlockBytes;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
+                    mma_tf32(d, sdesc(ah + ko), sdesc(bh + ko), id2, (kb > 0 || ks > 0) ? 1u : 0u);
+                    mma_tf32(d, sdesc(al + ko), sdesc(bh + ko), id1, 1u);
+                }
+                mma_commit(smem_u32(&s_empty[e]));
+                if (kb == KB - 1) mma_commit(smem_u32(&s_tfull[t]));
+                // the stage of g - 1 takes stage g - 1 + kStages once MMA(g - 1) has read it
+                const int gn = g - 1 + kStages;
+                if (g >= 1 && gn < G) {
+                    wait_ok(ok, smem_u32(&s_empty[(g - 1) % kStages]), (uint32_t)(((g - 1) / kStages) & 1), status);
+                    if (!ok) break;
+                    issue(gn);
+                }
+            }
+            // no MMA may still be running, and no copy still writing shared memory, at exit
+            mma_commit(smem_u32(&s_done));
+            bool fin = true;
+            wait_ok(fin, smem_u32(&s_done), 0u, status);
+            for (int e = 0; e < kStages; ++e)
+                if (g_last[e] >= 0) wait_ok(fin, smem_u32(&s_full[e]), (uint32_t)((g_last[e] / kStages) & 1), status);
+        }
+        __syncwarp();
+    } else {
+        cost_epilogue(N, M, p, r0, nC, tmem, s_tfull, s_tfree, xnorm, ynorm, Dsk, stg, ok, status);
     }
 
     fence_before_sync();
@@ -288,6 +417,8 @@ cudaError_t launch_simg(const Problems& pr, int P, int N, int M, int D, float* x
     const int KB = (D + 31) / 32;
     const int Lmax = ((N > M ? N : M) + kTile - 1) / kTile * kTile;
     const size_t smem = sizeof(float) * 32 * (32 * KB + 1);
+    cudaError_t e = cudaFuncSetAttribute(simg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     simg_kernel<<<dim3(Lmax / 32, P, 2), 256, smem, st>>>(pr, N, M, D, KB, ximg, yimg, xnorm, ynorm);
     return cudaGetLastError();
 }
@@ -296,10 +427,17 @@ cudaError_t launch_dist_tc(int P, int N, int M, int D, const float* ximg, const 
                            const float* ynorm, float* Dsk, int* status, cudaStream_t st)
 {
     const int KB = (D + 31) / 32;
-    if (KB < 1 || KB > 2) return cudaErrorInvalidValue;
-    const size_t smem = 1024 + 2 * (size_t)KB * kBlockBytes + 2 * (size_t)KB * 2 * kYHalf +
-                        (size_t)kTcWarps * kStg * sizeof(float);
+    if (KB < 1 || KB > kMaxTcKBlocks) return cudaErrorInvalidValue;
     dim3 grid((N + kTile - 1) / kTile, P);
+    const size_t stg = (size_t)kTcWarps * kStg * sizeof(float);
+    if (KB > 2) {
+        const size_t smem = 1024 + (size_t)kStages * kStageBytes + stg;
+        cudaError_t e = cudaFuncSetAttribute(dist_tc_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        dist_tc_stream_kernel<<<grid, kTcThreads, smem, st>>>(N, M, KB, ximg, yimg, xnorm, ynorm, Dsk, status);
+        return cudaGetLastError();
+    }
+    const size_t smem = 1024 + 2 * (size_t)KB * kBlockBytes + 2 * (size_t)KB * 2 * kYHalf + stg;
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

@@ -33,7 +33,6 @@ struct WaveParams {
     int* status;      // device status word
     unsigned long long wait_ns;
     int skip_publish; // test hook: strip 0 withholds its forward ready counter
-    int accurate;     // 1: unbiased exp2/log2 in the recursions; 0: MUFU approximations
     int ext;          // 1: extended-precision forward state (wavefront_x.cu)
     const int* lens_n; // per-problem lengths of x and y (device, P each), or null: every
     const int* lens_m; // problem spans N x M. A problem aligns its leading N_b x M_b block.
@@ -54,6 +53,12 @@ __host__ __device__ inline long long band_index(const WaveParams& q, int p, int 
     const int nb = q.vh_nb > 0 ? q.vh_nb : q.NB;
     return ((long long)p * nb + (rb - q.vh_rb0)) * T * 32 + lane;
 }
+
+// Device-wait settings of sdtw_debug_set_wait (api.cu): the time limit of every
+// bounded wait, and the one-shot request that the next forward's first strip
+// withhold its ready flags (read and cleared by the call that launches it).
+unsigned long long debug_wait_ns();
+int debug_take_skip_publish();
 
 size_t wave_smem_fixed(int W, bool backward);
 size_t wave_smem_fused_per_warp(int D);
@@ -103,6 +108,9 @@ size_t egemm_bimg_bytes(int P, int K, int D);
 // Tensor-core cost tensor (dist_tc.cu), D <= 64: operand images of x and y
 // (simg_bytes each), their squared row norms (snorm_bytes each), then the
 // skewed cost tensor. status receives kStatusTimeout if a bounded wait expires.
+// Widest features the tensor-core cost kernels take (K-blocks of 32 features);
+// beyond it the difference-form kernels compute the costs.
+constexpr int kMaxTcKBlocks = 8;
 size_t simg_bytes(int P, int L, int D);
 // Operand image layout (floats): per problem, per K-block of 32 features, hi then
 // lo part, Lpad = roundup(L, 128) rows of 32 tf32 values (128 bytes, 16-byte

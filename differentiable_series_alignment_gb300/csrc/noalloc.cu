@@ -16,7 +16,12 @@
 // All calls share the array and it keeps the last call's contents: the control
 // words that must start at zero are cleared at the start of every call (an
 // asynchronous memset on the caller's stream), and calls that overlap on the
-// GPU (different streams, or several host threads) race on it.
+// GPU (different streams, or several host threads) race on it. The cached
+// address belongs to the device's current context: after cudaDeviceReset the
+// module is loaded again and the array may move, so the cache is not valid
+// across a reset. A device-side wait that runs out of time leaves NaN in every
+// loss of the call (there is no workspace whose status word the caller could
+// read).
 #include <cstdint>
 #include <mutex>
 
@@ -38,6 +43,13 @@ void* g_scratch_addr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
 
 size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// loss[b] = NaN for every b when the status word reports a timed-out wait.
+__global__ void poison_on_status_kernel(const int* status, float* loss, int B)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B && *status != 0) loss[b] = __int_as_float(0x7fc00000);
+}
 
 // Forward-only carve of the scratch: status, control words, loss partials, last
 // row, strip boundary rows, the (vl,hu) pairs and, unfused, the cost tensor.
@@ -90,7 +102,7 @@ extern "C" sdtw_status sdtw_forward_noalloc(const float* x, const float* y, int 
     if (!(gamma > 0.f) || !(gamma < 3.0e38f)) return SDTW_ERR_GAMMA;
     if (mode != SDTW_UNFUSED && mode != SDTW_FUSED) return SDTW_ERR_ARG;
     if (!x || !y || !loss) return SDTW_ERR_ARG;
-    if (B > 65535 || D > 400) return SDTW_ERR_TOO_LARGE;
+    if (B > 65535 || N > (1 << 24) || M > (1 << 24) || D > 400) return SDTW_ERR_TOO_LARGE;
     const bool fused = (mode == SDTW_FUSED);
     if (fused && wave_smem_fixed(1, false) + wave_smem_fused_per_warp(D) > 220 * 1024) return SDTW_ERR_TOO_LARGE;
     if ((long long)N * M > (1ll << 40)) return SDTW_ERR_TOO_LARGE;
@@ -144,9 +156,8 @@ extern "C" sdtw_status sdtw_forward_noalloc(const float* x, const float* y, int 
     q.rowbuf = reinterpret_cast<float*>(ws + c.rowbuf);
     q.loss = loss;
     q.status = reinterpret_cast<int*>(ws + c.status);
-    q.wait_ns = 2000000000ull;
-    q.skip_publish = 0;
-    q.accurate = 0;
+    q.wait_ns = debug_wait_ns();
+    q.skip_publish = debug_take_skip_publish();
 
     // The status word, the ticket, the counters and the strip boundary slots start at zero.
     if (cudaMemsetAsync(ws + c.status, 0, sizeof(int), st) != cudaSuccess) return SDTW_ERR_CUDA;
@@ -156,5 +167,8 @@ extern "C" sdtw_status sdtw_forward_noalloc(const float* x, const float* y, int 
     if (!fused && launch_dist_skewed(pr, B, N, M, D, reinterpret_cast<float*>(ws + c.dsk), st) != cudaSuccess)
         return SDTW_ERR_CUDA;
     if (launch_forward(q, fused, st) != cudaSuccess) return SDTW_ERR_CUDA;
+    // a wait that ran out of time makes every loss of the call NaN
+    poison_on_status_kernel<<<(B + 255) / 256, 256, 0, st>>>(q.status, loss, B);
+    if (cudaGetLastError() != cudaSuccess) return SDTW_ERR_CUDA;
     return SDTW_OK;
 }

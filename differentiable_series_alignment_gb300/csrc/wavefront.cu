@@ -26,7 +26,6 @@
 #include "common.cuh"
 #include "kernels.h"
 
-#include <cstdlib>
 #include <type_traits>
 
 namespace sdtw {
@@ -82,7 +81,7 @@ __device__ __forceinline__ void stage_y_tile(float* tile, const float* yb, int c
 // ---------------------------------------------------------------------------
 // DX (fused only): 32 or 64 keeps the warp's x rows in registers, padded to DX
 // components (D <= DX); 0 reads them from shared memory (D > 64).
-template <bool FUSED, bool ACC, int DX>
+template <bool FUSED, int DX>
 __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(const WaveParams q)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -273,7 +272,7 @@ __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(co
                 // t = d + softmin(0, vl, hu) = d + lo - log2(1 + 2^(lo-mid) + 2^(lo-hi))
                 float lo, mid, hi;
                 sort3(0.f, vl, hu, lo, mid, hi);
-                const float lz = dp_log2<ACC>((1.f + dp_exp2<ACC>(lo - mid)) + dp_exp2<ACC>(lo - hi));
+                const float lz = lg2((1.f + ex2(lo - mid)) + ex2(lo - hi));
                 const float tt = (d + lo) - lz;
                 // first column / first row: a single predecessor (R borders are +inf)
                 const bool col0 = (j == 0);
@@ -332,12 +331,13 @@ __global__ void __launch_bounds__(FUSED ? 256 : kMaxWarps * 32, 1) fwd_kernel(co
 // Backward (log space)
 // ---------------------------------------------------------------------------
 // EXT: the extended forward stored the three transition log2-probabilities of
-// each cell (float4: diag, left, up); otherwise the (vl, hu) pair from which
-// they are recomputed.
+// each cell (float4: diag, left, up), and the log-sum-exp of the messages uses
+// the unbiased exp2_neg / log2f; otherwise the (vl, hu) pair from which they are
+// recomputed, and the MUFU ex2 / lg2.
 // MAXT: the block size the kernel is compiled for. Strips of at most 8 warps take
 // the 256-thread build, whose register budget holds the prefetched state of a
 // whole group without spilling.
-template <bool ACC, bool EXT, int MAXT>
+template <bool EXT, int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) bwd_kernel(const WaveParams q)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(MAXT, 1) bwd_kernel(const WaveParams q)
             rd_hold = rd;
             float lo, mid, hi;
             sort3(a1, a2, a3, lo, mid, hi);
-            float lE = hi + dp_log2<ACC>((1.f + dp_exp2<ACC>(mid - hi)) + dp_exp2<ACC>(lo - hi));
+            float lE = hi + dp_log2<EXT>((1.f + dp_exp2<EXT>(mid - hi)) + dp_exp2<EXT>(lo - hi));
             lE = (last_lane && j == Mb - 1) ? 0.f : lE;
             VT cur;
             if (EXT) {  // single buffer (register budget): refill slot u right after use
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(MAXT, 1) bwd_kernel(const WaveParams q)
                 const float2 st = reinterpret_cast<const float2&>(cur);
                 float wlo, wmid, whi;
                 sort3(0.f, st.x, st.y, wlo, wmid, whi);
-                const float Lz = dp_log2<ACC>((1.f + dp_exp2<ACC>(wlo - wmid)) + dp_exp2<ACC>(wlo - whi)) - wlo;
+                const float Lz = lg2((1.f + ex2(wlo - wmid)) + ex2(wlo - whi)) - wlo;
                 wl = -st.x - Lz; wu = -st.y - Lz; wd = -Lz;
             }
             ml = lE + wl;
@@ -531,8 +531,7 @@ size_t wave_smem_floor()
         if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
             per_sm <= 0)
             per_sm = 228 * 1024;
-        const char* env = getenv("SDTW_PACK_CTAS");
-        floor_bytes = (env && *env == '1') ? 1 : (size_t)per_sm / 2 + 1024;
+        floor_bytes = (size_t)per_sm / 2 + 1024;
     }
     return floor_bytes;
 }
@@ -553,13 +552,9 @@ cudaError_t launch_forward(WaveParams q, bool fused, cudaStream_t st)
     };
     if (fused) {
         const int dx = (q.D <= 32) ? 32 : (q.D <= 64 ? 64 : 0);
-        if (q.accurate)
-            return dx == 32 ? go(fwd_kernel<true, true, 32>) : dx == 64 ? go(fwd_kernel<true, true, 64>)
-                                                                   : go(fwd_kernel<true, true, 0>);
-        return dx == 32 ? go(fwd_kernel<true, false, 32>) : dx == 64 ? go(fwd_kernel<true, false, 64>)
-                                                                : go(fwd_kernel<true, false, 0>);
+        return dx == 32 ? go(fwd_kernel<true, 32>) : dx == 64 ? go(fwd_kernel<true, 64>) : go(fwd_kernel<true, 0>);
     }
-    return q.accurate ? go(fwd_kernel<false, true, 0>) : go(fwd_kernel<false, false, 0>);
+    return go(fwd_kernel<false, 0>);
 }
 
 cudaError_t launch_backward(WaveParams q, cudaStream_t st)
@@ -573,12 +568,8 @@ cudaError_t launch_backward(WaveParams q, cudaStream_t st)
         kern<<<grid, q.W * 32, smem, st>>>(q);
         return cudaGetLastError();
     };
-    if (q.W <= 8) {
-        if (q.ext) return go(bwd_kernel<true, true, 256>);
-        return q.accurate ? go(bwd_kernel<true, false, 256>) : go(bwd_kernel<false, false, 256>);
-    }
-    if (q.ext) return go(bwd_kernel<true, true, kMaxWarps * 32>);
-    return q.accurate ? go(bwd_kernel<true, false, kMaxWarps * 32>) : go(bwd_kernel<false, false, kMaxWarps * 32>);
+    if (q.W <= 8) return q.ext ? go(bwd_kernel<true, 256>) : go(bwd_kernel<false, 256>);
+    return q.ext ? go(bwd_kernel<true, kMaxWarps * 32>) : go(bwd_kernel<false, kMaxWarps * 32>);
 }
 
 }  // namespace sdtw

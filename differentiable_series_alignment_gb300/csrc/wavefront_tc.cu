@@ -41,14 +41,20 @@ constexpr int kRB = 4;                    // y tiles in shared memory
 constexpr int kTmemCols = kRT * 64;       // 512: the whole tensor memory of the SM
 constexpr uint32_t kABlock = 128 * 128;   // one K-block of the CTA's 128 x rows (bytes)
 constexpr uint32_t kBHalf = 32 * 128;     // one K-block of 32 y rows, hi or lo (bytes)
+// Wide features (more than two K-blocks): the x rows are not resident; each
+// K-block of a cost tile is one stage of a kStages-deep ring holding the CTA's x
+// rows (hi, lo) and the tile's y rows (hi, lo) of that K-block.
+constexpr int kStages = 3;
+constexpr uint32_t kStageBytes = 2 * kABlock + 2 * kBHalf;
 
 }  // namespace
 
 size_t wave_tc_smem(int D)
 {
     const int KB = (D + 31) / 32;
-    return wave_smem_fixed(kDpWarps, false) + 1024 + 2 * (size_t)KB * kABlock + (size_t)kRB * KB * 2 * kBHalf +
-           (size_t)kDpWarps * (64 + 2) * 32 * sizeof(float);
+    const size_t operands = KB > 2 ? (size_t)kStages * kStageBytes
+                                   : 2 * (size_t)KB * kABlock + (size_t)kRB * KB * 2 * kBHalf;
+    return wave_smem_fixed(kDpWarps, false) + 1024 + operands + (size_t)kDpWarps * (64 + 2) * 32 * sizeof(float);
 }
 
 namespace {
@@ -61,7 +67,9 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src)
 
 // STORE: the per-cell state for the backward is written (false in a checkpointed
 // forward, which keeps only the strips' boundary rows).
-template <bool ACC, bool STORE>
+// STREAM: the x rows' K-blocks are streamed with the y tiles through a stage ring
+// (wide features) instead of staying in shared memory.
+template <bool STORE, bool STREAM>
 __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     fwd_tc_kernel(const WaveParams q, const float* __restrict__ ximg, const float* __restrict__ yimg,
                   const float* __restrict__ xnorm, const float* __restrict__ ynorm)
@@ -75,6 +83,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     __shared__ double s_red[kMaxWarps];
     __shared__ int s_last;
     __shared__ uint64_t s_a, s_fin, s_bfull[kRB], s_bempty[kRB], s_tfull[kRT], s_tfree[kRT];
+    __shared__ uint64_t s_sfull[kStages], s_sempty[kStages];
     __shared__ uint32_t s_tmem;
 
     if (threadIdx.x == 0) s_tk = atomicAdd(q.ticket_f, 1);
@@ -96,7 +105,8 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     unsigned char* a_hi = base;
     unsigned char* a_lo = base + KB * kABlock;
     unsigned char* bring = base + 2 * KB * kABlock;               // [kRB][KB][hi 32 rows | lo 32 rows]
-    float* dts = reinterpret_cast<float*>(bring + kRB * KB * 2 * kBHalf);
+    unsigned char* stages = base;                                 // STREAM: [kStages][A hi | A lo | B hi | B lo]
+    float* dts = reinterpret_cast<float*>(STREAM ? stages + kStages * kStageBytes : bring + kRB * KB * 2 * kBHalf);
     float* nys = dts + W * 64 * 32;                                // [W][2][32] y norms of the next tiles
 
     if (threadIdx.x == 0) {
@@ -110,6 +120,10 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
             mbar_init(smem_u32(&s_tfull[t]), 1);
             mbar_init(smem_u32(&s_tfree[t]), nact);
         }
+        for (int e = 0; e < kStages; ++e) {
+            mbar_init(smem_u32(&s_sfull[e]), 1);
+            mbar_init(smem_u32(&s_sempty[e]), 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
@@ -122,7 +136,61 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     float c0 = 0.f;  // scaled d(i, 0)
     bool active = false;
 
-    if (warp == kIssuerWarp) {
+    if (warp == kIssuerWarp && STREAM) {
+        if (lane == 0) {
+            // stage g = c * KB + kb carries K-block kb of the x rows and of y tile c
+            bool ok = true;
+            const int G = nT * KB;
+            int g_last[kStages];
+            for (int e = 0; e < kStages; ++e) g_last[e] = -1;
+            auto issue = [&](int g) {
+                const int c = g / KB, kb = g - c * KB, e = g % kStages;
+                unsigned char* st = stages + e * kStageBytes;
+                const uint32_t bar = smem_u32(&s_sfull[e]);
+                mbar_expect_tx(bar, kStageBytes);
+                bulk_g2s(smem_u32(st), ximg + simg_offset(p, KB, kb, 0, Npad, rs0), kABlock, bar);
+                bulk_g2s(smem_u32(st + kABlock), ximg + simg_offset(p, KB, kb, 1, Npad, rs0), kABlock, bar);
+                bulk_g2s(smem_u32(st + 2 * kABlock), yimg + simg_offset(p, KB, kb, 0, Mpad, 32 * c), kBHalf, bar);
+                bulk_g2s(smem_u32(st + 2 * kABlock + kBHalf), yimg + simg_offset(p, KB, kb, 1, Mpad, 32 * c), kBHalf,
+                         bar);
+                g_last[e] = g;
+            };
+            for (int g = 0; g < kStages && g < G; ++g) issue(g);
+            const uint32_t id2 = idesc_tf32(128, 64), id1 = idesc_tf32(128, 32);
+            for (int g = 0; g < G && ok; ++g) {
+                const int c = g / KB, kb = g - c * KB, e = g % kStages, t = c % kRT;
+                if (kb == 0 && c >= kRT) wait_ok(ok, smem_u32(&s_tfree[t]), (uint32_t)(((c - kRT) / kRT) & 1), status);
+                wait_ok(ok, smem_u32(&s_sfull[e]), (uint32_t)((g / kStages) & 1), status);
+                if (!ok) break;
+                fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)(t * 64);
+                const uint32_t ah = smem_u32(stages + e * kStageBytes), al = ah + kABlock, bh = ah + 2 * kABlock;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
+                    mma_tf32(d, sdesc(ah + ko), sdesc(bh + ko), id2, (kb > 0 || ks > 0) ? 1u : 0u);
+                    mma_tf32(d, sdesc(al + ko), sdesc(bh + ko), id1, 1u);
+                }
+                mma_commit(smem_u32(&s_sempty[e]));
+                if (kb == KB - 1) mma_commit(smem_u32(&s_tfull[t]));
+                // the stage of g - 1 takes stage g - 1 + kStages once MMA(g - 1) has read it
+                const int gn = g - 1 + kStages;
+                if (g >= 1 && gn < G) {
+                    wait_ok(ok, smem_u32(&s_sempty[(g - 1) % kStages]), (uint32_t)(((g - 1) / kStages) & 1), status);
+                    if (!ok) break;
+                    issue(gn);
+                }
+            }
+            // every MMA has completed before tensor memory is released, and no copy is
+            // still writing shared memory when the CTA exits
+            mma_commit(smem_u32(&s_fin));
+            bool fin = true;
+            wait_ok(fin, smem_u32(&s_fin), 0u, status);
+            for (int e = 0; e < kStages; ++e)
+                if (g_last[e] >= 0) wait_ok(fin, smem_u32(&s_sfull[e]), (uint32_t)((g_last[e] / kStages) & 1), status);
+        }
+        __syncwarp();
+    } else if (warp == kIssuerWarp) {
         if (lane == 0) {
             bool ok = true;
             int y_last[kRB];
@@ -296,7 +364,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                     const float d = dt[(j & 63) * 32 + lane] * scale;
                     float lo, mid, hi;
                     sort3(0.f, vl, hu, lo, mid, hi);
-                    const float lz = dp_log2<ACC>((1.f + dp_exp2<ACC>(lo - mid)) + dp_exp2<ACC>(lo - hi));
+                    const float lz = lg2((1.f + ex2(lo - mid)) + ex2(lo - hi));
                     const float tt = (d + lo) - lz;
                     const bool col0 = (j == 0);
                     // border values picked off the dependency chain: one select follows tt
@@ -369,7 +437,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
 cudaError_t launch_forward_tc(WaveParams q, const float* ximg, const float* yimg, const float* xnorm,
                               const float* ynorm, cudaStream_t st)
 {
-    if (q.W != kDpWarps || q.D > 64) return cudaErrorInvalidValue;
+    if (q.W != kDpWarps || q.D > 32 * kMaxTcKBlocks) return cudaErrorInvalidValue;
     const int grid = q.P * q.S;
     q.smem_fixed = (int)wave_smem_fixed(kDpWarps, false);
     // more than half of the SM's shared memory: one CTA per SM, which the
@@ -385,8 +453,8 @@ cudaError_t launch_forward_tc(WaveParams q, const float* ximg, const float* yimg
         kern<<<grid, (kDpWarps + 1) * 32, smem, st>>>(q, ximg, yimg, xnorm, ynorm);
         return cudaGetLastError();
     };
-    if (q.VH == nullptr) return q.accurate ? go(fwd_tc_kernel<true, false>) : go(fwd_tc_kernel<false, false>);
-    return q.accurate ? go(fwd_tc_kernel<true, true>) : go(fwd_tc_kernel<false, true>);
+    if (q.D > 64) return q.VH == nullptr ? go(fwd_tc_kernel<false, true>) : go(fwd_tc_kernel<true, true>);
+    return q.VH == nullptr ? go(fwd_tc_kernel<false, false>) : go(fwd_tc_kernel<true, false>);
 }
 
 }  // namespace sdtw

@@ -135,6 +135,16 @@ sdtw_status sdtw_normalized(const float* x, const float* y, int B, int N, int D,
                             sdtw_mode mode, float* loss, const float* grad_loss, float* grad_x,
                             float* grad_y, void* ws, size_t ws_bytes, void* stream);
 
+/* Backward of normalized Soft-DTW, for a caller that ran sdtw_normalized without
+ * grad_loss (the forward only) and kept its workspace unchanged since, as autograd
+ * keeps saved tensors: the three backward wavefronts and the ordered gradient
+ * combination of sdtw_normalized, on the forward's state, without running the
+ * forward again. Same arguments as that call; grad_loss (B,) is required,
+ * grad_x / grad_y may be NULL individually (overwritten, not accumulated). */
+sdtw_status sdtw_normalized_backward(const float* x, const float* y, int B, int N, int D, float gamma,
+                                     sdtw_mode mode, const float* grad_loss, float* grad_x, float* grad_y,
+                                     void* ws, size_t ws_bytes, void* stream);
+
 /* Normalized Soft-DTW of sequences of different lengths, x (B,N,D) and y (B,M,D):
  * the README's "Normalization" definition, loss[b] = s(x_b,y_b) - (s(x_b,x_b) +
  * s(y_b,y_b)) / 2, applied unchanged to N != M (the README's own interface takes
@@ -149,6 +159,14 @@ sdtw_status sdtw_normalized_unequal(const float* x, const float* y, int B, int N
                                     float gamma, sdtw_mode mode, float* loss, const float* grad_loss,
                                     float* grad_x, float* grad_y, void* ws, size_t ws_bytes,
                                     void* stream);
+
+/* Backward of sdtw_normalized_unequal run without grad_loss, on its unchanged
+ * workspace: as sdtw_normalized_backward, for the three batches of their own
+ * shapes. */
+sdtw_status sdtw_normalized_unequal_backward(const float* x, const float* y, int B, int N, int M, int D,
+                                             float gamma, sdtw_mode mode, const float* grad_loss,
+                                             float* grad_x, float* grad_y, void* ws, size_t ws_bytes,
+                                             void* stream);
 
 /* One Adam step of a Soft-DTW barycenter (README, "Time Series Barycenters
  * (Averaging)"; review page, "proposed method", fifth bullet):
@@ -185,11 +203,15 @@ sdtw_status sdtw_barycenter_step_clipped(float* z, float* m, float* v, int t, co
  *  - The first call on each device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress); make that first call
  *    before any stream capture.
+ *  - The looked-up address belongs to the device's current context: it is not
+ *    valid across cudaDeviceReset (the array may move when the module loads
+ *    again).
  *  - All calls share the array and it keeps the last call's contents; the
  *    control words are cleared at the start of each call. Calls that overlap
  *    on the GPU (other streams, other host threads) race on it.
- *  - No state is left for sdtw_backward, and a device-side wait that runs out
- *    of time is not reported (the loss is then undefined). */
+ *  - No state is left for sdtw_backward. A device-side wait that runs out of
+ *    time makes every loss of the call NaN (there is no workspace status word
+ *    to read); sdtw_debug_set_wait applies to this entry too. */
 sdtw_status sdtw_forward_noalloc(const float* x, const float* y, int B, int N, int M, int D,
                                  float gamma, sdtw_mode mode, float* loss, void* stream);
 
@@ -253,6 +275,23 @@ const char* sdtw_status_string(sdtw_status s);
  * tiles run out of time and the call reports SDTW_ERR_TIMEOUT through
  * sdtw_last_device_status. No GPU fault is involved. Process-wide. */
 void sdtw_debug_set_wait(double seconds, int skip_publish);
+
+/* Testing hook. Forces choices the library otherwise makes itself, so that tests
+ * reach every kernel on small inputs: warps_fwd / warps_bwd > 0 fix the warps per
+ * wavefront CTA of the forward / backward (and with them the number of strips of
+ * a problem, whose boundaries pass through global memory); dist_simt / fused_simt
+ * non-zero select the difference-form cost kernels instead of the tensor-core
+ * ones in the unfused / fused fp32 modes (with fused_simt the checkpoint flag is
+ * SDTW_ERR_ARG). All zeros restore the library's own choices. Process-wide, read
+ * by the calls that follow; set it while no other host thread calls the library. */
+void sdtw_debug_set_options(int warps_fwd, int warps_bwd, int dist_simt, int fused_simt);
+
+/* Testing hook. out[i] = 2^x[i] (n device floats each) by the library's own
+ * exponential of the double-float path: Cody & Waite reduction x = k + f, k the
+ * nearest integer, |f| <= 1/2, then a degree-7 polynomial in f fitted to 2^f,
+ * exponent added to the bits. Its error bound, stated for x in [-125, 0]:
+ * within 2 ulp of the correctly rounded value; 0 for x < -125. */
+sdtw_status sdtw_debug_exp2_neg(const float* x, float* out, int n, void* stream);
 
 #ifdef __cplusplus
 }

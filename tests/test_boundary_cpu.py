@@ -14,7 +14,7 @@ HEADER = os.path.join(ROOT, "include", "sdtw.h")
 def _declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(sdtw_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(sdtw_[a-z0-9_]+)\s*\(", src)))
 
 
 @pytest.fixture(scope="module")
@@ -121,6 +121,16 @@ def test_auto_precision_rule():
     assert L.auto_precision(0.01, 64, 64, 4) == L.EXTENDED      # small gamma
     assert L.auto_precision(1.0, 4096, 8, 4) == L.EXTENDED      # long sequences
     assert L.auto_precision(1.0, 8, 4095, 4) == 0
+    # batch rule: fp32 for batch-mean losses over B >= 32 pairs, or D <= 4
+    assert L.auto_precision(1.0, 512, 512, 64, 32) == 0          # the headline batch
+    assert L.auto_precision(1.0, 512, 512, 64, 31) == L.EXTENDED
+    assert L.auto_precision(1.0, 64, 64, 4, 4) == 0              # the small workload
+    assert L.auto_precision(1.0, 64, 64, 5, 4) == L.EXTENDED
+    assert L.auto_precision(1.0, 1024, 1024, 8, 64) == 0         # the barycenter workload (mean over K=64)
+    assert L.auto_precision(1.0, 128, 128, 20, None) == 0        # no batch rule without B
+    assert L.auto_precision(1.0, 256, 256, 256, 32) == 0         # the width sweep's batch
+    assert L.auto_precision(1.0, 256, 256, 257, 32) == L.EXTENDED
+    assert L.auto_precision(1.0, 8192, 8192, 128, 8) == L.EXTENDED  # the long workload
 
 
 def test_given_cost_entry_points_validate_on_the_host(lib):
@@ -219,14 +229,15 @@ def test_checkpoint_workspace_and_validation(lib):
     # only the fp32 tensor-core fused path checkpoints
     assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, D, L.UNFUSED | L.CHECKPOINT) == 0
     assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, D, L.FUSED | L.EXTENDED | L.CHECKPOINT) == 0
-    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, 65, L.FUSED | L.CHECKPOINT) == 0
+    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, 256, L.FUSED | L.CHECKPOINT) > 0   # tensor-core widths
+    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, 257, L.FUSED | L.CHECKPOINT) == 0
     assert L.sdtw_workspace_bytes(L.OP_NORMALIZED, B, N, N, D, L.FUSED | L.CHECKPOINT) == 0
     assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, 2, 3, 4, 2, 8) == 0
     # host-side validation, before any CUDA call
     assert _fwd(lib, mode=L.FUSED | L.CHECKPOINT, ws_bytes=16) == 5     # accepted flag, small workspace
     assert _fwd(lib, mode=L.UNFUSED | L.CHECKPOINT) == 1
     assert _fwd(lib, mode=L.FUSED | L.EXTENDED | L.CHECKPOINT) == 1
-    assert _fwd(lib, mode=L.FUSED | L.CHECKPOINT, D=65) == 1
+    assert _fwd(lib, mode=L.FUSED | L.CHECKPOINT, D=257) == 1
     vp = ctypes.c_void_p
     assert lib.sdtw_normalized(vp(0x1000), vp(0x2000), 2, 3, 2, 1.0, L.FUSED | L.CHECKPOINT, vp(0x3000), None,
                                None, None, vp(0x100000), 1 << 40, None) == 1

@@ -4,8 +4,6 @@ Tolerances: losses rel 1e-4; gradients rel 1e-3 with abs 1e-5, the upstream
 gradient being the 1/B of a batch mean. The CUDA library must be the code that
 runs: every call goes through libsdtw.so.
 """
-import os
-
 import numpy as np
 import pytest
 
@@ -28,25 +26,24 @@ def _lib():
     return _lib
 
 
-class warps:
-    """Force the warps-per-CTA choice (and so the strip count) of the wavefront kernels."""
+class options:
+    """Force kernel choices of the library for the duration of a block (its testing
+    hook sdtw_debug_set_options): warps per wavefront CTA, which sets the strip
+    count, and the difference-form cost kernels in place of the tensor-core ones."""
 
-    def __init__(self, fwd, bwd=None):
-        self.fwd, self.bwd = fwd, (fwd if bwd is None else bwd)
+    def __init__(self, warps_fwd=0, warps_bwd=None, simt=False):
+        self.kw = dict(warps_fwd=warps_fwd, warps_bwd=warps_fwd if warps_bwd is None else warps_bwd,
+                       dist_simt=simt, fused_simt=simt)
 
     def __enter__(self):
-        self.old = {k: os.environ.get(k) for k in ("SDTW_WARPS_FWD", "SDTW_WARPS_BWD")}
-        if self.fwd:
-            os.environ["SDTW_WARPS_FWD"] = str(self.fwd)
-        if self.bwd:
-            os.environ["SDTW_WARPS_BWD"] = str(self.bwd)
+        _lib().sdtw_debug_set_options(**self.kw)
 
     def __exit__(self, *a):
-        for k, v in self.old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
+        _lib().sdtw_debug_set_options()
+
+
+def warps(fwd, bwd=None):
+    return options(warps_fwd=fwd, warps_bwd=bwd)
 
 
 def run_cuda(x, y, gamma, mode, grad_loss=None, want_grads=True):
@@ -85,12 +82,19 @@ def check_against_oracle(x, y, gamma, mode, grad_loss=None, sample=None, what=""
 
 MODES = [("unfused", 0), ("fused", 1)]
 
-# Per-problem upstream gradients for the fp32 modes: varied in sign and size, at
-# the scale of a batch-mean loss over the headline batch of 32, the setting the
-# gradient tolerance (abs 1e-5) is stated for. The extended mode is also checked
-# with O(1) weights (WEIGHTS_O1).
+# Upstream gradients. The fp32 modes are checked at each test's own batch mean:
+# per-pair weights of magnitude 1/B for the test's batch of B, alternating in
+# sign so that a mix-up of problems shows. Their state is single precision, so
+# the absolute gradient error grows with the weight; where a small batch's mean
+# is beyond what the fp32 state holds at a shape (D > 4: auto_precision keeps
+# fp32 only for batches of B >= 32), the test's batch is B = 32, the size of the
+# configs' batches. The double-float mode is checked with O(1) weights (WEIGHTS_O1).
 WEIGHTS_O1 = [0.5, -1.25, 2.0]
-WEIGHTS = [w / 32 for w in WEIGHTS_O1]
+
+
+def mean_weights(B, signed=True):
+    """Per-pair upstream weights of a batch-mean loss over B pairs (signs alternate when `signed`)."""
+    return [((-1.0) ** b if signed else 1.0) / B for b in range(B)]
 
 
 # --------------------------------------------------------------------------- small config
@@ -107,7 +111,7 @@ def test_small_config(mname, mode):
                                    (64, 65, 7), (100, 37, 16), (37, 100, 1), (129, 130, 9)])
 def test_ragged_shapes(mname, mode, N, M, D):
     x, y = synth.iid_normal_pair(3, N, M, D, 90, repeat=N * 1000 + M)
-    check_against_oracle(x, y, 0.7, mode, grad_loss=WEIGHTS, what=f"{N}x{M}x{D} {mname}")
+    check_against_oracle(x, y, 0.7, mode, grad_loss=mean_weights(3), what=f"{N}x{M}x{D} {mname}")
 
 
 # Wide features in fp32. D=127 is the widest operand the gradient contraction
@@ -169,34 +173,16 @@ def test_extended_strip_decompositions(W):
         check_against_oracle(x, y, 0.05, 3, what=f"extended W={W}")
 
 
-class env:
-    """Set environment variables for the duration of a block."""
-
-    def __init__(self, **kv):
-        self.kv = kv
-
-    def __enter__(self):
-        self.old = {k: os.environ.get(k) for k in self.kv}
-        os.environ.update({k: str(v) for k, v in self.kv.items()})
-
-    def __exit__(self, *a):
-        for k, v in self.old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
-
-
 def test_fused_equals_unfused():
     # Both cost kernels exist in both modes: the tensor-core norm form (default,
-    # D <= 64) and the difference form (SDTW_DIST_SIMT / SDTW_FUSED_SIMT). With the
+    # D <= 64) and the difference form (selected through sdtw_debug_set_options). With the
     # same cost kernel the fused forward recomputes exactly the costs the unfused
     # mode stores, so the two modes agree to rounding; across cost kernels they
     # agree to the parity tolerance.
     x, y = synth.iid_normal_pair(4, 96, 80, 12, 94)
     tc_u = run_cuda(x, y, 1.0, 0)
     tc_f = run_cuda(x, y, 1.0, 1)
-    with env(SDTW_DIST_SIMT=1, SDTW_FUSED_SIMT=1):
+    with options(simt=True):
         df_u = run_cuda(x, y, 1.0, 0)
         df_f = run_cuda(x, y, 1.0, 1)
     for what, a, b in (("tensor-core costs", tc_u, tc_f), ("difference-form costs", df_u, df_f)):
@@ -209,11 +195,34 @@ def test_fused_equals_unfused():
 
 @pytest.mark.parametrize("mname,mode", MODES)
 def test_difference_form_cost_kernels(mname, mode):
-    # the difference-form cost path (the one D > 64 takes) at a width the tensor
-    # cores would otherwise handle
-    x, y = synth.iid_normal_pair(3, 70, 91, 20, 96)
-    with env(SDTW_DIST_SIMT=1, SDTW_FUSED_SIMT=1):
-        check_against_oracle(x, y, 0.8, mode, grad_loss=WEIGHTS, what=f"difference-form {mname}")
+    # the difference-form cost path at a width the tensor cores would otherwise
+    # handle; a batch of 32 at its own mean (D = 20 > 4)
+    x, y = synth.iid_normal_pair(32, 70, 91, 20, 96)
+    with options(simt=True):
+        check_against_oracle(x, y, 0.8, mode, grad_loss=mean_weights(32), what=f"difference-form {mname}")
+
+
+# Wide features on the tensor cores: above two K-blocks (D > 64) both cost
+# kernels stream the x rows' K-blocks through a stage ring instead of keeping them
+# in shared memory. Ragged tiles: N not a multiple of 128, M not of 32 or 64, D not
+# of 32.
+@pytest.mark.parametrize("mname,mode", MODES)
+@pytest.mark.parametrize("N,M,D", [(130, 97, 96), (200, 150, 128), (129, 70, 200), (64, 33, 256)])
+def test_wide_features_tensor_core_costs(mname, mode, N, M, D):
+    x, y = synth.iid_normal_pair(32, N, M, D, 104, repeat=N * 1000 + D)
+    check_against_oracle(x, y, 1.0, mode, grad_loss=mean_weights(32), what=f"wide tc {N}x{M}x{D} {mname}")
+
+
+def test_wide_tensor_core_costs_fused_equals_unfused_and_difference_form():
+    x, y = synth.iid_normal_pair(4, 150, 140, 160, 105)
+    tc_u = run_cuda(x, y, 1.0, 0)
+    tc_f = run_cuda(x, y, 1.0, 1)
+    with options(simt=True):
+        df_u = run_cuda(x, y, 1.0, 0)
+    assert_close(tc_f["loss"], tc_u["loss"], 1e-5, 0.0, "wide fused vs unfused loss")
+    assert_close(tc_f["gx"], tc_u["gx"], 1e-4, 1e-6, "wide fused vs unfused grad_x")
+    assert_close(tc_f["gy"], tc_u["gy"], 1e-4, 1e-6, "wide fused vs unfused grad_y")
+    assert_close(tc_u["loss"], df_u["loss"], LOSS_RTOL, 0.0, "wide tensor-core vs difference-form loss")
 
 
 def test_distance_kernel_matches_definition():
@@ -302,7 +311,7 @@ def run_normalized_unequal(x, y, gamma, mode, gl):
 @pytest.mark.parametrize("N,M,D", [(100, 37, 8), (33, 130, 3), (1, 9, 2)])
 def test_unequal_normalized_matches_oracle(mname, mode, N, M, D):
     x, y = synth.iid_normal_pair(3, N, M, D, 98, repeat=N * 1000 + M)
-    gl = np.array(WEIGHTS)
+    gl = np.array(WEIGHTS_O1 if mode & 2 else mean_weights(3))
     loss, gx, gy = run_normalized_unequal(x, y, 0.8, mode, gl)
     ol, ogx, ogy = oracle.normalized_unequal(x, y, 0.8, grad_loss=gl)
     sxx = oracle.batch(x, x, 0.8)[0]
@@ -335,17 +344,27 @@ def test_unequal_normalized_through_autograd():
     ol, ogx, ogy = oracle.normalized_unequal(x, y, 1.0, grad_loss=[0.5, -1.0])
     s = np.maximum(np.abs(oracle.batch(x, x, 1.0)[0]), np.abs(oracle.batch(y, y, 1.0)[0]))
     assert np.all(np.abs(loss.detach().cpu().numpy() - ol) <= 1e-4 * np.maximum(1.0, s) + LOSS_RTOL * np.abs(ol))
-    assert_close(xt.grad.cpu().numpy(), ogx, GRAD_RTOL, 32 * GRAD_ATOL, "autograd unequal normalized grad_x")
-    assert_close(yt.grad.cpu().numpy(), ogy, GRAD_RTOL, 32 * GRAD_ATOL, "autograd unequal normalized grad_y")
+    assert_close(xt.grad.cpu().numpy(), ogx, GRAD_RTOL, GRAD_ATOL, "autograd unequal normalized grad_x")
+    assert_close(yt.grad.cpu().numpy(), ogy, GRAD_RTOL, GRAD_ATOL, "autograd unequal normalized grad_y")
 
 
 CKPT = 1 | 4   # SDTW_FUSED | SDTW_CHECKPOINT
 
 
-@pytest.mark.parametrize("N,M,D", [(64, 70, 8), (128, 33, 16), (129, 100, 5), (300, 77, 64), (512, 512, 64)])
+@pytest.mark.parametrize("N,M,D", [(64, 70, 8), (128, 33, 16), (129, 100, 5), (300, 77, 64), (200, 150, 128)])
 def test_checkpointed_fused_matches_oracle(N, M, D):
-    x, y = synth.iid_normal_pair(3, N, M, D, 101, repeat=N * 1000 + M)
-    check_against_oracle(x, y, 0.9, CKPT, grad_loss=WEIGHTS, what=f"checkpoint {N}x{M}x{D}")
+    # the checkpointed mode is fp32 only: batches of 32 at their own mean (D > 4)
+    x, y = synth.iid_normal_pair(32, N, M, D, 101, repeat=N * 1000 + M)
+    check_against_oracle(x, y, 0.9, CKPT, grad_loss=mean_weights(32), what=f"checkpoint {N}x{M}x{D}")
+
+
+@pytest.mark.parametrize("mname,mode", [("fused+checkpoint", 5)])
+def test_checkpointed_headline_config(mname, mode):
+    # the headline workload's own inputs in the checkpointed mode (its results equal
+    # the stored-state fused mode's bit for bit, see below)
+    c = synth.WORKLOADS["headline"]
+    x, y = synth.iid_normal_pair(c["B"], c["N"], c["M"], c["D"], c["seed"])
+    check_against_oracle(x, y, 1.0, mode, what=f"headline {mname}")
 
 
 @pytest.mark.parametrize("N,M", [(300, 77), (257, 130)])
@@ -376,12 +395,13 @@ def test_checkpointed_padded_batch_and_autograd():
     lxt = torch.tensor(lx, dtype=torch.int32, device="cuda")
     lyt = torch.tensor(ly, dtype=torch.int32, device="cuda")
     loss = SoftDTW(gamma=gamma, fused=True, checkpoint=True)(xt, yt, lxt, lyt)
-    w = torch.tensor(WEIGHTS, device="cuda")
+    W = mean_weights(B)
+    w = torch.tensor(W, device="cuda")
     (loss * w).sum().backward()
     loss = loss.detach().cpu().numpy()
     gx, gy = xt.grad.cpu().numpy(), yt.grad.cpu().numpy()
     for b in range(B):
-        o = oracle.single(x[b, :lx[b]], y[b, :ly[b]], gamma, g=WEIGHTS[b])
+        o = oracle.single(x[b, :lx[b]], y[b, :ly[b]], gamma, g=W[b])
         assert_close(loss[b:b + 1], [o["loss"]], LOSS_RTOL, 1e-6, f"checkpoint padded pair {b} loss")
         assert_close(gx[b, :lx[b]], o["gx"], GRAD_RTOL, GRAD_ATOL, f"checkpoint padded pair {b} grad_x")
         assert_close(gy[b, :ly[b]], o["gy"], GRAD_RTOL, GRAD_ATOL, f"checkpoint padded pair {b} grad_y")
@@ -416,8 +436,8 @@ def test_barycenter_steps_match_oracle(mname, mode):
 
 # --------------------------------------------------------------------------- padded batches
 
-@pytest.mark.parametrize("mname,mode,weights", [("unfused", 0, WEIGHTS + [0.25 / 32]),
-                                                ("fused", 1, WEIGHTS + [0.25 / 32]),
+@pytest.mark.parametrize("mname,mode,weights", [("unfused", 0, mean_weights(4)),
+                                                ("fused", 1, mean_weights(4)),
                                                 ("unfused+extended", 2, WEIGHTS_O1 + [0.25]),
                                                 ("fused+extended", 3, WEIGHTS_O1 + [0.25])])
 def test_padded_batch_matches_oracle(mname, mode, weights):
@@ -470,7 +490,7 @@ def _cost_batch(kind, B, N, M, seed):
     return (2.0 * g.standard_normal((B, N, M))).astype(np.float32)   # signed costs
 
 
-@pytest.mark.parametrize("mname,mode,weights", [("fp32", 0, WEIGHTS), ("extended", 2, WEIGHTS_O1)])
+@pytest.mark.parametrize("mname,mode,weights", [("fp32", 0, mean_weights(3)), ("extended", 2, WEIGHTS_O1)])
 @pytest.mark.parametrize("kind", ["l1", "signed"])
 @pytest.mark.parametrize("N,M", [(1, 1), (1, 9), (7, 1), (33, 31), (100, 37), (129, 130)])
 def test_given_cost_matches_oracle(mname, mode, weights, kind, N, M):
@@ -552,15 +572,19 @@ def test_barycenter_driver_schedule_clipping_and_early_stopping():
 
 # --------------------------------------------------------------------------- device status
 
-@pytest.mark.parametrize("mname,mode", MODES)
-@pytest.mark.parametrize("B,chunks", [(5, 3), (1, 4), (7, 8)])
+@pytest.mark.parametrize("mname,mode", MODES + [("unfused+extended", 2), ("fused+extended", 3)])
+@pytest.mark.parametrize("B,chunks", [(5, 3), (1, 4), (7, 8), (32, 3)])
 def test_host_batch_matches_oracle_and_device_path(mname, mode, B, chunks):
     """Host buffers in, host buffers out, the batch cut into uneven chunks on side
-    streams: the same losses and gradients as the oracle and the device-buffer path."""
+    streams: the same losses and gradients as the oracle and the device-buffer path.
+    Weights: the batch's own mean (fp32 takes the batch of 32 only, D = 8 > 4),
+    O(1) in the double-float mode."""
     L = _lib()
+    if not (mode & 2) and B < 32:
+        pytest.skip("fp32 state: batch-mean weights of a batch below 32 pairs at D > 4 need the double-float mode")
     N, M, D, gamma = 100, 77, 8, 0.8
     x, y = synth.iid_normal_pair(B, N, M, D, 77, repeat=B * 10 + chunks)
-    w = (np.arange(B) % 3 - 1.0 + 0.5) / 32           # mixed-sign batch-scale weights
+    w = np.array(mean_weights(B)) if not (mode & 2) else np.array([WEIGHTS_O1[b % 3] for b in range(B)])
     xh, yh = torch.from_numpy(x).pin_memory(), torch.from_numpy(y).pin_memory()
     gl = torch.from_numpy(w.astype(np.float32)).pin_memory()
     loss = torch.full((B,), float("nan")).pin_memory()
@@ -595,6 +619,34 @@ def test_host_batch_high_level_function_and_loss_only():
     L.sdtw_value_and_grad_host(torch.from_numpy(x), torch.from_numpy(y), None, 1.0, L.UNFUSED, lo, None, None, 2, ws)
     assert L.sdtw_last_device_status(ws) == 0
     assert_close(lo.numpy(), ol, LOSS_RTOL, 0.0, "host batch loss only")
+
+
+def test_high_level_api_picks_the_precision_the_weights_need():
+    """Through the public API the precision follows the upstream weights: at the
+    shape where the fp32 state misses abs 1e-5 for a batch of 3 (70 x 91, D = 20,
+    gamma = 0.8), SoftDTW(...).mean() over B = 3 and value_and_grad_host with O(1)
+    weights both select the double-float state and hold the tolerance."""
+    from differentiable_series_alignment_gb300 import SoftDTW, value_and_grad_host
+    L = _lib()
+    B, gamma = 3, 0.8
+    x, y = synth.iid_normal_pair(B, 70, 91, 20, 96)
+    assert L.auto_precision(gamma, 70, 91, 20, B) == L.EXTENDED
+    ol, ogx, ogy = oracle.batch(x, y, gamma, grad_loss=np.full(B, 1.0 / B))
+    for fused in (False, True):
+        xt = torch.from_numpy(x).cuda().requires_grad_(True)
+        yt = torch.from_numpy(y).cuda().requires_grad_(True)
+        loss = SoftDTW(gamma=gamma, fused=fused)(xt, yt)
+        loss.mean().backward()
+        assert_close(loss.detach().cpu().numpy(), ol, LOSS_RTOL, 0.0, f"api mean loss fused={fused}")
+        assert_close(xt.grad.cpu().numpy(), ogx, GRAD_RTOL, GRAD_ATOL, f"api mean grad_x fused={fused}")
+        assert_close(yt.grad.cpu().numpy(), ogy, GRAD_RTOL, GRAD_ATOL, f"api mean grad_y fused={fused}")
+    w = np.array(WEIGHTS_O1)
+    loss, gx, gy = value_and_grad_host(torch.from_numpy(x), torch.from_numpy(y), gamma=gamma,
+                                       grad_loss=torch.from_numpy(w.astype(np.float32)))
+    ol, ogx, ogy = oracle.batch(x, y, gamma, grad_loss=w)
+    assert_close(loss.numpy(), ol, LOSS_RTOL, 0.0, "api O(1) weights loss")
+    assert_close(gx.numpy(), ogx, GRAD_RTOL, GRAD_ATOL, "api O(1) weights grad_x")
+    assert_close(gy.numpy(), ogy, GRAD_RTOL, GRAD_ATOL, "api O(1) weights grad_y")
 
 
 def test_withheld_ready_flag_times_out_and_recovers():
