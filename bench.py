@@ -337,9 +337,11 @@ def measure_per_config(L, synth, dev, flush, stream, hbm, rates, step_ns):
     for Ls, Ds in pts:
         x, y = (torch.from_numpy(a).to(dev)
                 for a in synth.iid_normal_pair(32, Ls, Ls, Ds, c["seed"], repeat=Ls * 1000 + Ds))
-        prec = L.auto_precision(1.0, Ls, Ls, Ds, 32)
-        for m in (L.UNFUSED, L.FUSED):
-            res["sweep"].append(dict(point(x, y, 1.0, m | prec, 5 if Ls <= 512 else 3), B=32, L=Ls, D=Ds, gamma=1.0))
+        auto = L.auto_precision(1.0, Ls, Ls, Ds, 32)
+        for prec in (0, L.EXTENDED):   # both precisions; `auto` marks the one the high-level API picks
+            for m in (L.UNFUSED, L.FUSED):
+                res["sweep"].append(dict(point(x, y, 1.0, m | prec, 5 if Ls <= 512 else 3), B=32, L=Ls, D=Ds,
+                                         gamma=1.0, auto=(prec == auto)))
         del x, y
 
     c = synth.WORKLOADS["long_warped"]
@@ -475,6 +477,20 @@ def run_ours(args):
         per_mode[name] = {"fwd_ms": f_ms, "bwd_wavefront_ms": bw_ms, "fwd_bwd_ms": fb_ms,
                           "cells_per_s": CELLS / (fb_ms * 1e-3)}
         assert L.sdtw_last_device_status(b["ws"]) == 0
+
+    # the double-float state (SDTW_EXTENDED: robust to near ties at any upstream weight)
+    # at the same workload, both modes
+    for mode, name in ((L.UNFUSED | L.EXTENDED, "unfused+extended"), (L.FUSED | L.EXTENDED, "fused+extended")):
+        bx = {"ws": L.workspace(L.OP_FWD_BWD, B, N, M, D, mode, dev), "loss": torch.empty(B, device=dev),
+              "gx": torch.empty_like(x), "gy": torch.empty_like(y)}
+        xi = max(10, min(50, K))
+        f_ms = timed(lambda: L.sdtw_forward(x, y, GAMMA, mode, bx["loss"], bx["ws"]), xi)
+        fb_ms = timed(lambda: (L.sdtw_forward(x, y, GAMMA, mode, bx["loss"], bx["ws"]),
+                               L.sdtw_backward(x, y, GAMMA, mode, g, bx["gx"], bx["gy"], bx["ws"])), xi)
+        per_mode[name] = {"fwd_ms": f_ms, "fwd_bwd_ms": fb_ms, "cells_per_s": CELLS / (fb_ms * 1e-3),
+                          "workspace_MB": bx["ws"].numel() / 2**20}
+        assert L.sdtw_last_device_status(bx["ws"]) == 0
+        del bx
 
     # the checkpointed fused mode (no per-cell forward state; bands recomputed in the
     # backward): reported beside the two modes of the step, not part of it

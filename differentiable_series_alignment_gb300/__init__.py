@@ -193,7 +193,7 @@ class SoftDTW:
     the DP kernels. normalize=True gives s(x,y) - (s(x,x) + s(y,y))/2; x and y may
     differ in length. extended=None picks the double-float forward state unless
     the fp32 state is accurate enough for a batch-mean loss over these B pairs
-    (auto_precision: small gamma, long sequences, D > 256, or D > 4 with B < 32
+    (auto_precision: small gamma, long sequences, D > 64, or D > 4 with B < 32
     select it); pass extended=True when the losses are summed rather than
     averaged. True/False forces it.
     checkpoint=True (fused, fp32, D <= 64, not normalized) keeps no per-cell forward

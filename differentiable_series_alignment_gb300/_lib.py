@@ -154,27 +154,26 @@ def auto_precision(gamma: float, N: int, M: int, D: int | None = None, B: int | 
     probability inherits the rounding of state values of the size of a cost
     (about 2*D/gamma for unit-variance data), and on rows where two alignments
     nearly tie the gradient cancels, so its absolute error scales with the
-    upstream weight. Measured on the GB300 against the oracle, the worst
-    gradient entry of the fp32 path over the tested shapes (D up to 256, lengths
-    up to 512, gamma >= 0.7) stays below 0.5 of the tolerance for upstream
-    weights up to 1/32 and exceeds it from about 1/8 on at D >= 16; at D <= 4 it
-    stays below 0.1 of it even at weight 1. The double-float path is below 0.06
-    of it at weight 1 everywhere.
+    upstream weight. Measured on the GB300 against the oracle: at D <= 4 the worst
+    gradient entry stays below 0.1 of the tolerance even at weight 1; at D = 16 to
+    64 it stays below 0.5 of it for batch-mean weights 1/32 on most problems but
+    can exceed it on a near tie (one problem in 32 at 2.8x, headline shape); wider
+    features are worse. The double-float path is below 0.06 of it at weight 1
+    everywhere tested.
 
-    fp32 is therefore kept when gamma >= 0.05 and max(N, M) < 4096, and
-      - with the batch size B given (the loss is the mean over the B pairs, the
-        README's ``loss.mean()``): D <= 4, or B >= 32 with D <= 256;
-      - without it (weights unknown): D <= 64. D=None (costs given by the caller)
-        skips the width rules."""
+    fp32 is therefore kept when gamma >= 0.05, max(N, M) < 4096 and D <= 64, and,
+    with the batch size B given (the loss is the mean over the B pairs, the
+    README's ``loss.mean()``), either D <= 4 or B >= 32. D=None (costs given by the
+    caller) skips the width rules; B=None (weights unknown) the batch rule."""
     if gamma < 0.05 or max(N, M) >= 4096:
         return EXTENDED
     if D is None:
         return 0
-    if B is None:
-        return EXTENDED if D > 64 else 0
-    if D <= 4:
+    if D > 64:
+        return EXTENDED
+    if B is None or D <= 4:
         return 0
-    return 0 if (B >= 32 and D <= 256) else EXTENDED
+    return 0 if B >= 32 else EXTENDED
 
 
 def sdtw_workspace_bytes(op: int, B: int, N: int, M: int, D: int, mode) -> int:
@@ -314,8 +313,7 @@ def sdtw_normalized_unequal(x, y, gamma, mode, loss, grad_loss, grad_x, grad_y, 
     _check(load().sdtw_normalized_unequal(_f32(x, "x"), _f32(y, "y"), B, N, M, D, float(gamma), _mode(mode),
                                           _f32(loss, "loss"), _f32(grad_loss, "grad_loss"), _f32(grad_x, "grad_x"),
                                           _f32(grad_y, "grad_y"), _ptr(ws), ws.numel(), _stream(stream)),
-           "sdtw_normalized_unequal", "sdtw_normalized_backward", "sdtw_normalized_unequal_backward",
-           "sdtw_debug_set_options", "sdtw_debug_exp2_neg")
+           "sdtw_normalized_unequal")
 
 
 def sdtw_normalized_backward(x, y, gamma, mode, grad_loss, grad_x, grad_y, ws, stream=None):

@@ -37,11 +37,21 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 struct Layout {
     size_t status, ctrl_f, ctrl_f_bytes, ctrl_b, ctrl_b_bytes;
     size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, gnorm, bimg, bimg2, total;
-    size_t ximg, yimg, xnorm, ynorm;  // tensor-core cost operands (tc_cost)
+    size_t ximg, yimg, xnorm, ynorm;  // tensor-core cost operands (tc_cost, or xtc: digit images and row info)
+    size_t band_slots;                // checkpointed mode: skewed slots of one band of every problem
     bool tc_cost;
-    bool ckpt;   // checkpointed fused mode: VH / E / the [X | 1] image hold one band
+    bool xtc;    // extended fused mode with the exact tensor-core cost tiles (D <= kMaxXtcD)
+    bool ckpt;   // checkpointed fused mode: VH / E hold two bands, the [X | 1] image one
     int P, N, M, D, NB;
 };
+
+// Side streams and cached events (defined below, with their rules).
+cudaStream_t side_stream();
+enum EventSlot {
+    kEvBwdFork, kEvBwdJoin, kEvHostFork, kEvHostJoin, kEvNormFork, kEvNormJoin,
+    kEvCkptFork, kEvCkptRec0, kEvCkptRec1, kEvCkptFree0, kEvCkptFree1, kEvSlots
+};
+cudaEvent_t cached_event(EventSlot slot);
 
 // Checkpointed fused mode: bands of kBandBlocks 32-row blocks (the fused forward's
 // 128-row strips). The forward keeps only each band's outgoing boundary row; the
@@ -58,14 +68,17 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     const bool ckpt = (mode & SDTW_CHECKPOINT) != 0;
     if (op == SDTW_OP_COST && fused) return false;
     // checkpointing recomputes bands with the tensor-core fused forward (fp32, D <= 256)
-    if (ckpt && (op != SDTW_OP_FWD_BWD || !fused || ext || D > 32 * kMaxTcKBlocks)) return false;
+    if (ckpt && (op != SDTW_OP_FWD_BWD || !fused || ext || D > kTcKFeat * kMaxTcKBlocks)) return false;
     const int P = (op == SDTW_OP_NORMALIZED) ? 3 * B : B;
     if (op == SDTW_OP_NORMALIZED) M = N;
     const int NB = (N + 31) / 32;
     const int SB = (NB + kBandBlocks - 1) / kBandBlocks;   // bands (checkpointed mode)
     const size_t slots = (size_t)skew_slots(N, M) * P;
-    // per-cell state and E: every cell, or one band of every problem
-    const size_t vslots = ckpt ? (size_t)P * (NB < kBandBlocks ? NB : kBandBlocks) * skew_T(M) * 32 : slots;
+    // per-cell state and E: every cell, or two bands of every problem (the band being
+    // differentiated and the next one up, recomputed meanwhile)
+    const size_t band_slots = (size_t)P * (NB < kBandBlocks ? NB : kBandBlocks) * skew_T(M) * 32;
+    const size_t vslots = ckpt ? 2 * band_slots : slots;
+    L->band_slots = band_slots;
     const size_t edge_rows = ckpt ? (size_t)SB : (size_t)NB;   // boundary rows kept per problem
     size_t o = 0;
     L->status = o; o = align_up(o + sizeof(int));
@@ -89,11 +102,17 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     if (!ext && xy) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, ckpt ? (N < 32 * kBandBlocks ? N : 32 * kBandBlocks) : N, D));
     // operand images and norms of the tensor-core costs (fp32 modes, D <= 256): the
     // unfused cost tensor and the fused forward's cost tiles
-    L->tc_cost = !ext && D <= 32 * kMaxTcKBlocks && xy;
+    L->tc_cost = !ext && D <= kTcKFeat * kMaxTcKBlocks && xy;
+    // the extended fused forward's exact cost tiles: fixed-point digit images and row info
+    L->xtc = ext && fused && D <= kMaxXtcD && xy;
     L->ximg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, N, D));
+    if (L->xtc) o = align_up(o + oimg_bytes(P, N, D));
     L->yimg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, M, D));
+    if (L->xtc) o = align_up(o + oimg_bytes(P, M, D));
     L->xnorm = o; if (L->tc_cost) o = align_up(o + snorm_bytes(P, N));
+    if (L->xtc) o = align_up(o + oinfo_bytes(P, N));
     L->ynorm = o; if (L->tc_cost) o = align_up(o + snorm_bytes(P, M));
+    if (L->xtc) o = align_up(o + oinfo_bytes(P, M));
     L->total = o;
     L->P = P; L->N = N; L->M = M; L->D = D; L->NB = NB;
     L->ckpt = ckpt;
@@ -151,7 +170,7 @@ sdtw_status check_common(const void* x, const void* y, int B, int N, int M, int 
     if (!(gamma > 0.f) || !std::isfinite(gamma)) return SDTW_ERR_GAMMA;
     if (mode & ~(allow_ckpt ? 7 : 3)) return SDTW_ERR_ARG;
     if ((mode & SDTW_CHECKPOINT) &&
-        (!(mode & SDTW_FUSED) || (mode & SDTW_EXTENDED) || D > 32 * kMaxTcKBlocks || g_dbg.fused_simt))
+        (!(mode & SDTW_FUSED) || (mode & SDTW_EXTENDED) || D > kTcKFeat * kMaxTcKBlocks || g_dbg.fused_simt))
         return SDTW_ERR_ARG;
     if (!x || !y) return SDTW_ERR_ARG;
     if (B > 65535 / 3 || N > (1 << 24) || M > (1 << 24) || D > 400) return SDTW_ERR_TOO_LARGE;
@@ -216,7 +235,8 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
     q.lens_n = lens_n;
     q.lens_m = lens_m;
     const bool tc = L.tc_cost && !(fused ? g_dbg.fused_simt : g_dbg.dist_simt);
-    if (fused && tc) {  // the tensor-core fused forward takes 128-row strips (4 warps)
+    const bool xtc = L.xtc && !g_dbg.fused_simt;
+    if ((fused && tc) || xtc) {  // the tensor-core fused forwards take 128-row strips (4 warps)
         q.W = 4;
         q.S = (L.NB + 3) / 4;
     }
@@ -229,7 +249,14 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
         else if (!fused) SDTW_CUDA(launch_dist_skewed_x(pr, L.P, L.N, L.M, L.D, at<float2>(ws, L.dsk), st));
         q.loss = loss_out;
         q.skip_publish = debug_take_skip_publish();
-        SDTW_CUDA(launch_forward_x(q, fused, st));
+        if (xtc) {
+            SDTW_CUDA(launch_oimg(pr, L.P, L.N, L.M, L.D, at<char>(ws, L.ximg), at<char>(ws, L.yimg),
+                                  at<char>(ws, L.xnorm), at<char>(ws, L.ynorm), st));
+            SDTW_CUDA(launch_forward_xtc(q, at<char>(ws, L.ximg), at<char>(ws, L.yimg), at<char>(ws, L.xnorm),
+                                         at<char>(ws, L.ynorm), st));
+        } else {
+            SDTW_CUDA(launch_forward_x(q, fused, st));
+        }
         return SDTW_OK;
     }
     if (tc)
@@ -262,50 +289,80 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
 // forward kept above it, run the band's backward wavefront (its lower boundary
 // messages come from the band below, run just before), then the band's share of the
 // gradient contractions: its rows of grad_x, and its rows' terms of grad_y, which
-// accumulate over the bands.
+// accumulate over the bands. The state and E of two bands are kept: while band k's
+// backward and gradients run on the caller's stream, band k-1 is recomputed into
+// the other buffer on a side stream, once band k+1's gradients have released it.
+// Every recompute runs on the side stream, so no two of them overlap (they share
+// the forward's strip ticket).
 sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, float gamma, int mode,
                               const float* grad_loss, float* grad_x, float* grad_y, cudaStream_t st,
                               const int* lens_n, const int* lens_m)
 {
     const int SB = (L.NB + kBandBlocks - 1) / kBandBlocks;
     int* status = at<int>(ws, L.status);
+    cudaStream_t side = side_stream();
+    cudaEvent_t ev_fork = cached_event(kEvCkptFork), ev_rec[2] = {cached_event(kEvCkptRec0), cached_event(kEvCkptRec1)};
+    cudaEvent_t ev_free[2] = {cached_event(kEvCkptFree0), cached_event(kEvCkptFree1)};
+    if (!side || !ev_fork || !ev_rec[0] || !ev_rec[1] || !ev_free[0] || !ev_free[1]) return SDTW_ERR_CUDA;
     WaveParams qb0 = wave_params(pr, L, ws, gamma, true, false, true);
     if (SB > 1) SDTW_CUDA(cudaMemsetAsync(qb0.edge_b, 0, 2 * sizeof(Slot) * (size_t)L.P * SB * L.M, st));
     GradParams g{};
     g.pr = pr;
     g.P = L.P; g.M = L.M; g.D = L.D;
-    g.E = at<float>(ws, L.e);
     g.grad_loss = grad_loss;
     g.wmod = L.P;
     g.omod = L.P;
     g.coef = 1.f;
     float* img_rows = at<float>(ws, L.bimg);
     float* img_cols = at<float>(ws, L.bimg2);
+    float2* vh_buf[2] = {at<float2>(ws, L.vh), at<float2>(ws, L.vh) + L.band_slots};
+    float* e_buf[2] = {at<float>(ws, L.e), at<float>(ws, L.e) + L.band_slots};
     if (grad_x) {  // [Y | 1] does not depend on the band
         g.N = L.N;
         SDTW_CUDA(launch_bimg(g, img_rows, nullptr, st));
     }
-    for (int k = SB - 1; k >= 0; --k) {
+    // the side stream starts after everything before this call on the caller's stream
+    SDTW_CUDA(cudaEventRecord(ev_fork, st));
+    SDTW_CUDA(cudaStreamWaitEvent(side, ev_fork, 0));
+    // band k's forward state, recomputed from the kept boundary row above it, into buffer k % 2
+    auto recompute = [&](int k, cudaStream_t s) -> sdtw_status {
+        const int rb0 = k * kBandBlocks;
+        const int nb = L.NB - rb0 < kBandBlocks ? L.NB - rb0 : kBandBlocks;
+        WaveParams qf = wave_params(pr, L, ws, gamma, true, false, false);
+        qf.W = kBandBlocks; qf.S = 1; qf.strip0 = k; qf.S_all = SB;
+        qf.vh_rb0 = rb0; qf.vh_nb = nb; qf.no_loss = 1;
+        qf.VH = vh_buf[k & 1];
+        qf.lens_n = lens_n; qf.lens_m = lens_m;
+        SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_f), 0, L.ctrl_f_bytes, s));
+        SDTW_CUDA(launch_forward_tc(qf, at<float>(ws, L.ximg), at<float>(ws, L.yimg), at<float>(ws, L.xnorm),
+                                    at<float>(ws, L.ynorm), s));
+        return SDTW_OK;
+    };
+    sdtw_status s = recompute(SB - 1, side);
+    if (s == SDTW_OK) SDTW_CUDA(cudaEventRecord(ev_rec[(SB - 1) & 1], side));
+    for (int k = SB - 1; k >= 0 && s == SDTW_OK; --k) {
         const int rb0 = k * kBandBlocks;
         const int nb = L.NB - rb0 < kBandBlocks ? L.NB - rb0 : kBandBlocks;
         const int row0 = 32 * rb0;
         const int nrows = L.N - row0 < 32 * kBandBlocks ? L.N - row0 : 32 * kBandBlocks;
-        // 1. the band's forward state, from the kept boundary row above it
-        WaveParams qf = wave_params(pr, L, ws, gamma, true, false, false);
-        qf.W = kBandBlocks; qf.S = 1; qf.strip0 = k; qf.S_all = SB;
-        qf.vh_rb0 = rb0; qf.vh_nb = nb; qf.no_loss = 1;
-        qf.lens_n = lens_n; qf.lens_m = lens_m;
-        SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_f), 0, L.ctrl_f_bytes, st));
-        SDTW_CUDA(launch_forward_tc(qf, at<float>(ws, L.ximg), at<float>(ws, L.yimg), at<float>(ws, L.xnorm),
-                                    at<float>(ws, L.ynorm), st));
-        // 2. the band's backward wavefront
+        // 1. the next band up, into the other buffer once band k + 1 has released it
+        if (k >= 1) {
+            if (k + 1 < SB) SDTW_CUDA(cudaStreamWaitEvent(side, ev_free[(k + 1) & 1], 0));
+            if ((s = recompute(k - 1, side)) != SDTW_OK) break;
+            SDTW_CUDA(cudaEventRecord(ev_rec[(k - 1) & 1], side));
+        }
+        // 2. the band's backward wavefront, once its state is recomputed
+        SDTW_CUDA(cudaStreamWaitEvent(st, ev_rec[k & 1], 0));
         WaveParams qb = wave_params(pr, L, ws, gamma, true, false, true);
         qb.W = kBandBlocks; qb.S = 1; qb.strip0 = k; qb.S_all = SB;
         qb.vh_rb0 = rb0; qb.vh_nb = nb;
+        qb.VH = vh_buf[k & 1];
+        qb.E = e_buf[k & 1];
         qb.lens_n = lens_n; qb.lens_m = lens_m;
         SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_b), 0, L.ctrl_b_bytes, st));
         SDTW_CUDA(launch_backward(qb, st));
         // 3. the band's gradient terms: E of the band is a problem of nrows x M
+        g.E = e_buf[k & 1];
         g.pr.xs[0] = pr.xs[0] + (size_t)row0 * L.D;
         g.N = nrows;
         if (grad_x) {
@@ -321,8 +378,15 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
             g.accumulate = k < SB - 1;
             SDTW_CUDA(launch_grad_tc(g, true, img_cols, status, st));
         }
+        SDTW_CUDA(cudaEventRecord(ev_free[k & 1], st));
     }
-    return SDTW_OK;
+    // the side stream's work (the last recompute was waited for above) stays ordered
+    // before anything later on the caller's stream, also after an error
+    if (s != SDTW_OK) {
+        cudaEventRecord(ev_fork, side);
+        cudaStreamWaitEvent(st, ev_fork, 0);
+    }
+    return s;
 }
 
 sdtw_status run_backward(const Problems& pr, const Layout& L, void* ws, float gamma, int mode, cudaStream_t st,
@@ -372,7 +436,6 @@ cudaStream_t side_stream()
 // is recorded and then waited on before the same thread records it again, and
 // cudaStreamWaitEvent takes the record current at the time of the call. (The
 // host-batch entry calls sdtw_backward inside its chunks, hence separate slots.)
-enum EventSlot { kEvBwdFork, kEvBwdJoin, kEvHostFork, kEvHostJoin, kEvNormFork, kEvNormJoin, kEvSlots };
 cudaEvent_t cached_event(EventSlot slot)
 {
     thread_local cudaEvent_t ev[64][kEvSlots] = {};

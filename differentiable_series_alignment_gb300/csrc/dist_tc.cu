@@ -8,23 +8,26 @@
 // (Unfused)", where the unfused mode materialises the whole cost tensor.)
 //
 // The dot products are a batched GEMM x . y^T with K = D. Each sequence is first
-// written once as an operand image (simg_kernel): every row split into tf32
-// hi + lo parts (round to nearest), stored in the 128-byte-swizzled K-major
-// layout that tcgen05.mma reads, in K-blocks of 32 features, together with the
-// squared norm of the row (compensated fp32: exact squares, TwoSum partial
-// sums). A cost CTA (dist_tc_kernel) keeps the 128 x rows of its block in shared
-// memory and streams the y rows in tiles of 64 by bulk copy; one thread issues
-// the 3xTF32 products
-//   x_hi . [y_hi ; y_lo]  (N = 128)   and   x_lo . y_hi  (N = 64)
-// per 8-wide K step into one of two tensor-memory slots, while eight warps drain
-// the other slot: they read the accumulators back, form the cost, clamp it at 0
-// and write the skewed layout of the wavefront through a per-warp shared staging
-// tile, so every global store is a 128-byte slot row.
+// written once as an operand image (simg_kernel): every value split exactly into
+// three bf16 parts v = v0 + v1 + v2 (8 significant bits each), stored in the
+// 128-byte-swizzled K-major layout that tcgen05.mma reads, in K-blocks of 64
+// features, together with the squared norm of the row (compensated fp32: exact
+// squares, TwoSum partial sums, rounded once). The dot is the sum of all nine
+// part products, each exact in fp32,
+//   x0 . [y0 ; y1 ; y2]  +  x1 . [y0 ; y1 ; y2]  +  x2 . [y0 ; y1 ; y2],
+// three bf16 MMAs per 16-wide K step with the y parts stacked along N, all
+// accumulating in fp32 in tensor memory; the three column groups are summed in
+// the epilogue, so the dot carries only the fp32 accumulation.
 //
-// Precision: the dot carries ~2^-21 of sum_k |x_k y_k|, and the final fp32
-// combination a few ulps of C; at D <= 64 that keeps the gradient of the
-// unit-variance workloads far inside rel 1e-3 / abs 1e-5 (wider features use the
-// exact difference-form kernel in dist.cu).
+// A cost CTA (dist_tc_kernel) owns 128 x rows and walks the y columns in tiles
+// of 64; one thread issues the copies and MMAs into one of two tensor-memory
+// slots while eight warps drain the other: they read the accumulators back, form
+// the cost, clamp it at 0 and write the skewed layout of the wavefront through a
+// per-warp shared staging tile, so every global store is a 128-byte slot row.
+// The x rows (one K-block: D <= 64) stay in shared memory. Wider features take the
+// exact difference-form kernel of dist.cu: beyond one K-block the fp32
+// accumulation of the dot in tensor memory adds errors of a few ulps of the cost,
+// which the fp32 DP state's gradients do not absorb at the tolerance.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -39,41 +42,44 @@ constexpr int kTile = 128;                     // x rows per cost CTA (the MMA h
 constexpr int kColTile = 64;                   // y columns per cost tile
 constexpr int kTcWarps = 8;                    // epilogue warps; warp 8 copies and issues the MMAs
 constexpr int kTcThreads = (kTcWarps + 1) * 32;
-constexpr uint32_t kBlockBytes = kTile * 128;  // one K-block of 128 x rows (32 tf32 each)
-constexpr uint32_t kYHalf = kColTile * 128;    // one K-block of 64 y rows, hi or lo
+constexpr uint32_t kPartBytes = kTile * 128;   // one bf16 part of one K-block of 128 x rows
+constexpr uint32_t kABytes = 3 * kPartBytes;   // the three parts of one K-block of x rows
+constexpr uint32_t kYPart = kColTile * 128;    // one part of one K-block of 64 y rows
+constexpr uint32_t kBBytes = 3 * kYPart;       // [y0 ; y1 ; y2] of one K-block of a y tile
+constexpr int kSlotCols = 3 * kColTile;        // tensor-memory columns of one tile: three part groups
 constexpr int kStg = 63 * 32;                  // per-warp skew staging (floats)
 
 // grid (Lpad/32, P, 2): z = 0 writes the x image, z = 1 the y image. block 256.
 // Rows past the sequence end are zero (image and norm). Each thread loads its
 // values in batches of 8, all issued before their shared stores.
-__global__ void __launch_bounds__(256) simg_kernel(Problems pr, int N, int M, int D, int KB, float* __restrict__ ximg,
-                                                   float* __restrict__ yimg, float* __restrict__ xnorm,
-                                                   float* __restrict__ ynorm)
+__global__ void __launch_bounds__(256) simg_kernel(Problems pr, int N, int M, int D, int KB,
+                                                   unsigned char* __restrict__ ximg, unsigned char* __restrict__ yimg,
+                                                   float* __restrict__ xnorm, float* __restrict__ ynorm)
 {
-    extern __shared__ float t[];  // [32][D32 + 1]
+    extern __shared__ float t[];  // [32][D64 + 1]
     const bool isy = blockIdx.z == 1;
     const int p = blockIdx.y, r0 = blockIdx.x * 32;
     const int L = isy ? M : N;
-    const int Lpad = (L + kTile - 1) / kTile * kTile;
+    const int Lpad = simg_pad(L);
     if (r0 >= Lpad) return;
     const float* src = isy ? pr.y(p) : pr.x(p);
-    float* img = isy ? yimg : ximg;
+    unsigned char* img = isy ? yimg : ximg;
     float* nrm = isy ? ynorm : xnorm;
-    const int D32 = 32 * KB, ld = D32 + 1;
-    const int n = 32 * D32 / 256;  // values per thread: 4 per K-block
+    const int D64 = kTcKFeat * KB, ld = D64 + 1;
+    const int n = 32 * D64 / 256;  // values per thread: 8 per K-block
     for (int u0 = 0; u0 < n; u0 += 8) {
         float v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int idx = threadIdx.x + 256 * (u0 + u);
-            const int r = idx / D32, k = idx - r * D32;
-            v[u] = (u0 + u < n && r0 + r < L && k < D) ? src[(size_t)(r0 + r) * D + k] : 0.f;
+            const int r = idx / D64, k = idx - r * D64;
+            v[u] = (r0 + r < L && k < D) ? src[(size_t)(r0 + r) * D + k] : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int idx = threadIdx.x + 256 * (u0 + u);
-            const int r = idx / D32, k = idx - r * D32;
-            if (u0 + u < n) t[r * ld + k] = v[u];
+            const int r = idx / D64, k = idx - r * D64;
+            t[r * ld + k] = v[u];
         }
     }
     __syncthreads();
@@ -100,35 +106,42 @@ __global__ void __launch_bounds__(256) simg_kernel(Problems pr, int N, int M, in
         }
         if (part == 0) nrm[(size_t)p * Lpad + r0 + r] = s + c;
     }
-    // one 16-byte chunk (4 features) per thread and pass: eight threads write one
-    // 128-byte image row (its chunks permuted by the swizzle), a warp four rows
-    const size_t part = (size_t)Lpad * 32;   // floats between the hi and lo images of a K-block
-    for (int idx = threadIdx.x; idx < 32 * D32 / 4; idx += blockDim.x) {
+    // one 16-byte chunk (8 features) of all three parts per thread and pass: eight
+    // threads write one 128-byte image row per part (its chunks permuted by the
+    // swizzle), a warp four rows
+    const size_t part_bytes = (size_t)Lpad * 128;   // between the parts of a K-block
+    for (int idx = threadIdx.x; idx < 32 * D64 / 8; idx += blockDim.x) {
         const int c8 = idx & 7, r = (idx >> 3) & 31, kb = idx >> 8;
-        const float* src4 = t + r * ld + kb * 32 + 4 * c8;
-        float4 hi, lo;
-        split_tf32(src4[0], hi.x, lo.x);
-        split_tf32(src4[1], hi.y, lo.y);
-        split_tf32(src4[2], hi.z, lo.z);
-        split_tf32(src4[3], hi.w, lo.w);
-        float* row = img + simg_offset(p, KB, kb, 0, Lpad, r0 + r) + 4 * (c8 ^ (r & 7));
-        *reinterpret_cast<float4*>(row) = hi;
-        *reinterpret_cast<float4*>(row + part) = lo;
+        const float* src8 = t + r * ld + kb * kTcKFeat + 8 * c8;
+        uint16_t h0[8], h1[8], h2[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) split_bf16x3(src8[q], h0[q], h1[q], h2[q]);
+        uint4 w0, w1, w2;
+        w0.x = h0[0] | ((uint32_t)h0[1] << 16); w0.y = h0[2] | ((uint32_t)h0[3] << 16);
+        w0.z = h0[4] | ((uint32_t)h0[5] << 16); w0.w = h0[6] | ((uint32_t)h0[7] << 16);
+        w1.x = h1[0] | ((uint32_t)h1[1] << 16); w1.y = h1[2] | ((uint32_t)h1[3] << 16);
+        w1.z = h1[4] | ((uint32_t)h1[5] << 16); w1.w = h1[6] | ((uint32_t)h1[7] << 16);
+        w2.x = h2[0] | ((uint32_t)h2[1] << 16); w2.y = h2[2] | ((uint32_t)h2[3] << 16);
+        w2.z = h2[4] | ((uint32_t)h2[5] << 16); w2.w = h2[6] | ((uint32_t)h2[7] << 16);
+        unsigned char* row = img + simg_offset(p, KB, kb, 0, Lpad, r0 + r) + 16 * (c8 ^ (r & 7));
+        *reinterpret_cast<uint4*>(row) = w0;
+        *reinterpret_cast<uint4*>(row + part_bytes) = w1;
+        *reinterpret_cast<uint4*>(row + 2 * part_bytes) = w2;
     }
 }
 
 // Epilogue warps 0-7 of the cost kernels: warp w reads TMEM lane quarter w mod 4
 // (rows r0 + 32(w mod 4) + lane) and the 32-column half w / 4 of each 64-column
-// tile (x_hi . y_hi + x_lo . y_hi in columns [0, 64), x_hi . y_lo in [64, 128) of
-// the tile's slot), releases the slot, forms C = |x|^2 + |y|^2 - 2 x.y clamped at 0
-// and writes the skewed layout through a per-warp staging tile (128-byte rows).
+// tile from its three part groups, releases the slot, forms C = |x|^2 + |y|^2 -
+// 2 x.y clamped at 0 and writes the skewed layout through a per-warp staging tile
+// (128-byte rows).
 __device__ __forceinline__ void cost_epilogue(int N, int M, int p, int r0, int nC, uint32_t tmem,
                                               uint64_t* s_tfull, uint64_t* s_tfree, const float* __restrict__ xnorm,
                                               const float* __restrict__ ynorm, float* __restrict__ Dsk, float* stg,
                                               bool& ok, int* status)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int Npad = (N + kTile - 1) / kTile * kTile, Mpad = (M + kTile - 1) / kTile * kTile;
+    const int Npad = simg_pad(N), Mpad = simg_pad(M);
     const int NB = (N + 31) / 32;
     const int q = warp & 3, half = warp >> 2;
     const int rb = (r0 >> 5) + q;
@@ -141,9 +154,11 @@ __device__ __forceinline__ void cost_epilogue(int N, int M, int p, int r0, int n
         wait_ok(ok, smem_u32(&s_tfull[t]), (uint32_t)((c >> 1) & 1), status);
         if (!__all_sync(0xffffffffu, ok)) break;
         fence_after_sync();
-        float a[32], b[32];
-        tmem_ld32(trow + (uint32_t)(t * 2 * kColTile + 32 * half), a);
-        tmem_ld32(trow + (uint32_t)(t * 2 * kColTile + kColTile + 32 * half), b);
+        float a[32], b[32], e[32];
+        const uint32_t col = trow + (uint32_t)(t * kSlotCols + 32 * half);
+        tmem_ld32(col, a);
+        tmem_ld32(col + kColTile, b);
+        tmem_ld32(col + 2 * kColTile, e);
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&s_tfree[t]));
@@ -153,7 +168,7 @@ __device__ __forceinline__ void cost_epilogue(int N, int M, int p, int r0, int n
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const float ny = __shfl_sync(0xffffffffu, nyv, j);
-            stg[(j + lane) * 32 + lane] = fmaxf(nx + ny - 2.f * (a[j] + b[j]), 0.f);
+            stg[(j + lane) * 32 + lane] = fmaxf(nx + ny - 2.f * (a[j] + (b[j] + e[j])), 0.f);
         }
         __syncwarp();
         // skewed slot cb + tt holds column (tt - lane) of this chunk for this lane's row
@@ -167,14 +182,14 @@ __device__ __forceinline__ void cost_epilogue(int N, int M, int p, int r0, int n
 
 // grid (ceil(N/128), P), block 288: one CTA per 128-row block of x and problem,
 // walking the y columns in tiles of 64. Warp 8 (lane 0) copies the x rows once
-// and each y tile into a two-entry ring, and issues every tile's MMAs into one of
-// two tensor-memory slots; warps 0-7 drain a slot (epilogue) while the next
-// tile's MMAs run. Hand-offs (all bounded mbarrier waits):
+// (one K-block: D <= 64) and each y tile into a two-entry ring, and issues every
+// tile's MMAs into one of two tensor-memory slots; warps 0-7 drain a slot
+// (epilogue) while the next tile's MMAs run. Hand-offs (all bounded mbarrier
+// waits):
 //   s_bfull[e]  y tile in entry e      s_bempty[e] its MMAs are done
 //   s_tfull[t]  costs in TMEM slot t   s_tfree[t]  the 8 epilogue warps read slot t
-template <int KB>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    dist_tc_kernel(int N, int M, const float* __restrict__ ximg, const float* __restrict__ yimg,
+    dist_tc_kernel(int N, int M, const unsigned char* __restrict__ ximg, const unsigned char* __restrict__ yimg,
                    const float* __restrict__ xnorm, const float* __restrict__ ynorm, float* __restrict__ Dsk,
                    int* status)
 {
@@ -184,17 +199,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int p = blockIdx.y, r0 = blockIdx.x * kTile;
-    const int Npad = (N + kTile - 1) / kTile * kTile, Mpad = (M + kTile - 1) / kTile * kTile;
-    const int NB = (N + 31) / 32;
+    const int Npad = simg_pad(N), Mpad = simg_pad(M);
     const int nC = (M + kColTile - 1) / kColTile;
 
-    // shared memory (1 KiB aligned): A_hi[KB], A_lo[KB], 2 y entries of KB x [hi 64 rows | lo 64 rows], staging
+    // shared memory (1 KiB aligned): A [x0 | x1 | x2], 2 y entries [y0 ; y1 ; y2], staging
     unsigned char* base = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
-    unsigned char* a_hi = base;
-    unsigned char* a_lo = base + KB * kBlockBytes;
-    unsigned char* yring = base + 2 * KB * kBlockBytes;
-    auto yent = [&](int e, int kb) { return yring + (e * KB + kb) * 2 * kYHalf; };
-    float* stg = reinterpret_cast<float*>(yring + 2 * KB * 2 * kYHalf) + warp * kStg;
+    unsigned char* a_img = base;
+    unsigned char* yring = base + kABytes;
+    float* stg = reinterpret_cast<float*>(yring + 2 * kBBytes) + warp * kStg;
 
     if (tid == 0) {
         mbar_init(smem_u32(&s_a), 1);
@@ -207,7 +219,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) tmem_alloc(&s_tmem, 256);
+    if (warp == 0) tmem_alloc(&s_tmem, 512);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -216,46 +228,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == kTcWarps) {
         if (lane == 0) {
-            mbar_expect_tx(smem_u32(&s_a), 2u * KB * kBlockBytes);
-            for (int kb = 0; kb < KB; ++kb) {
-                bulk_g2s(smem_u32(a_hi + kb * kBlockBytes), ximg + simg_offset(p, KB, kb, 0, Npad, r0), kBlockBytes,
+            mbar_expect_tx(smem_u32(&s_a), kABytes);
+            for (int part = 0; part < 3; ++part)
+                bulk_g2s(smem_u32(a_img + part * kPartBytes), ximg + simg_offset(p, 1, 0, part, Npad, r0), kPartBytes,
                          smem_u32(&s_a));
-                bulk_g2s(smem_u32(a_lo + kb * kBlockBytes), ximg + simg_offset(p, KB, kb, 1, Npad, r0), kBlockBytes,
-                         smem_u32(&s_a));
-            }
             int y_last[2] = {-1, -1};
             auto issue_y = [&](int c) {
                 const int e = c & 1;
-                mbar_expect_tx(smem_u32(&s_bfull[e]), 2u * KB * kYHalf);
-                for (int kb = 0; kb < KB; ++kb) {
-                    bulk_g2s(smem_u32(yent(e, kb)), yimg + simg_offset(p, KB, kb, 0, Mpad, c * kColTile), kYHalf,
-                             smem_u32(&s_bfull[e]));
-                    bulk_g2s(smem_u32(yent(e, kb) + kYHalf), yimg + simg_offset(p, KB, kb, 1, Mpad, c * kColTile),
-                             kYHalf, smem_u32(&s_bfull[e]));
-                }
+                unsigned char* dst = yring + e * kBBytes;
+                mbar_expect_tx(smem_u32(&s_bfull[e]), kBBytes);
+                for (int part = 0; part < 3; ++part)
+                    bulk_g2s(smem_u32(dst + part * kYPart), yimg + simg_offset(p, 1, 0, part, Mpad, c * kColTile),
+                             kYPart, smem_u32(&s_bfull[e]));
                 y_last[e] = c;
             };
             for (int c = 0; c < 2 && c < nC; ++c) issue_y(c);
             wait_ok(ok, smem_u32(&s_a), 0u, status);
-            const uint32_t id2 = idesc_tf32(kTile, 2 * kColTile), id1 = idesc_tf32(kTile, kColTile);
             for (int c = 0; c < nC && ok; ++c) {
                 const int e = c & 1, t = c & 1;
                 wait_ok(ok, smem_u32(&s_bfull[e]), (uint32_t)((c >> 1) & 1), status);
                 if (c >= 2) wait_ok(ok, smem_u32(&s_tfree[t]), (uint32_t)(((c - 2) >> 1) & 1), status);
                 if (!ok) break;
                 fence_after_sync();
-                const uint32_t d = tmem + (uint32_t)(t * 2 * kColTile);
+                const uint32_t d = tmem + (uint32_t)(t * kSlotCols);
+                const uint32_t a = smem_u32(a_img), b = smem_u32(yring + e * kBBytes);
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb) {
-                    const uint32_t ah = smem_u32(a_hi + kb * kBlockBytes), al = smem_u32(a_lo + kb * kBlockBytes);
-                    const uint32_t bh = smem_u32(yent(e, kb));
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
-                        mma_tf32(d, sdesc(ah + ko), sdesc(bh + ko), id2, (kb > 0 || ks > 0) ? 1u : 0u);
-                        mma_tf32(d, sdesc(al + ko), sdesc(bh + ko), id1, 1u);
-                    }
-                }
+                for (int ks = 0; ks < 4; ++ks)  // 16 bf16 = 32 bytes along K per step
+                    mma_bf16x3(d, a, b, kTile, kColTile, kPartBytes, ks * 32, ks > 0 ? 1u : 0u);
                 mma_commit(smem_u32(&s_tfull[t]));
                 mma_commit(smem_u32(&s_bempty[e]));
                 if (c + 2 < nC) {  // entry e takes tile c + 2 once MMA(c) has read it
@@ -280,119 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     if (warp == 0) {
         fence_after_sync();
-        tmem_dealloc(tmem, 256);
-    }
-}
-
-
-// Wide features (more than two K-blocks): the same CTA shape and epilogue, but the
-// 128 x rows do not stay in shared memory. Every K-block of a tile comes as one
-// stage of a kStages-deep ring: the tile's x rows (hi, lo) and y rows (hi, lo) of
-// that K-block, one expect-tx mbarrier per stage. The x rows are read again for
-// every 64-column tile (from L2: 4 bytes per cell and K-block).
-//   s_full[s]  stage s landed         s_empty[s] the MMAs reading stage s are done
-//   s_tfull[t] / s_tfree[t] as above
-constexpr int kStages = 3;
-constexpr uint32_t kStageBytes = 2 * kBlockBytes + 2 * kYHalf;   // A hi, A lo, B hi, B lo
-
-__global__ void __launch_bounds__(kTcThreads, 1)
-    dist_tc_stream_kernel(int N, int M, int KB, const float* __restrict__ ximg, const float* __restrict__ yimg,
-                          const float* __restrict__ xnorm, const float* __restrict__ ynorm, float* __restrict__ Dsk,
-                          int* status)
-{
-    extern __shared__ unsigned char smem_dyn[];
-    __shared__ uint64_t s_done, s_full[kStages], s_empty[kStages], s_tfull[2], s_tfree[2];
-    __shared__ uint32_t s_tmem;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int p = blockIdx.y, r0 = blockIdx.x * kTile;
-    const int Npad = (N + kTile - 1) / kTile * kTile, Mpad = (M + kTile - 1) / kTile * kTile;
-    const int nC = (M + kColTile - 1) / kColTile;
-
-    // shared memory (1 KiB aligned): kStages x [A hi | A lo | B hi (64 rows) | B lo], staging
-    unsigned char* base = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
-    float* stg = reinterpret_cast<float*>(base + kStages * kStageBytes) + warp * kStg;
-
-    if (tid == 0) {
-        mbar_init(smem_u32(&s_done), 1);
-        for (int e = 0; e < kStages; ++e) {
-            mbar_init(smem_u32(&s_full[e]), 1);
-            mbar_init(smem_u32(&s_empty[e]), 1);
-        }
-        for (int e = 0; e < 2; ++e) {
-            mbar_init(smem_u32(&s_tfull[e]), 1);
-            mbar_init(smem_u32(&s_tfree[e]), kTcWarps);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 0) tmem_alloc(&s_tmem, 256);
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    const uint32_t tmem = s_tmem;
-    bool ok = true;
-
-    if (warp == kTcWarps) {
-        if (lane == 0) {
-            const int G = nC * KB;   // stages in all: K-block kb of tile c is stage c * KB + kb
-            int g_last[kStages];
-            for (int e = 0; e < kStages; ++e) g_last[e] = -1;
-            auto issue = [&](int g) {
-                const int c = g / KB, kb = g - c * KB, e = g % kStages;
-                unsigned char* st = base + e * kStageBytes;
-                const uint32_t bar = smem_u32(&s_full[e]);
-                mbar_expect_tx(bar, kStageBytes);
-                bulk_g2s(smem_u32(st), ximg + simg_offset(p, KB, kb, 0, Npad, r0), kBlockBytes, bar);
-                bulk_g2s(smem_u32(st + kBlockBytes), ximg + simg_offset(p, KB, kb, 1, Npad, r0), kBlockBytes, bar);
-                bulk_g2s(smem_u32(st + 2 * kBlockBytes), yimg + simg_offset(p, KB, kb, 0, Mpad, c * kColTile), kYHalf,
-                         bar);
-                bulk_g2s(smem_u32(st + 2 * kBlockBytes + kYHalf), yimg + simg_offset(p, KB, kb, 1, Mpad, c * kColTile),
-                         kYHalf, bar);
-                g_last[e] = g;
-            };
-            for (int g = 0; g < kStages && g < G; ++g) issue(g);
-            const uint32_t id2 = idesc_tf32(kTile, 2 * kColTile), id1 = idesc_tf32(kTile, kColTile);
-            for (int g = 0; g < G && ok; ++g) {
-                const int c = g / KB, kb = g - c * KB, e = g % kStages, t = c & 1;
-                if (kb == 0 && c >= 2) wait_ok(ok, smem_u32(&s_tfree[t]), (uint32_t)(((c - 2) >> 1) & 1), status);
-                wait_ok(ok, smem_u32(&s_full[e]), (uint32_t)((g / kStages) & 1), status);
-                if (!ok) break;
-                fence_after_sync();
-                const uint32_t d = tmem + (uint32_t)(t * 2 * kColTile);
-                const uint32_t ah = smem_u32(base + e * kStageBytes), al = ah + kBlockBytes, bh = ah + 2 * kBlockBytes;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
-                    mma_tf32(d, sdesc(ah + ko), sdesc(bh + ko), id2, (kb > 0 || ks > 0) ? 1u : 0u);
-                    mma_tf32(d, sdesc(al + ko), sdesc(bh + ko), id1, 1u);
-                }
-                mma_commit(smem_u32(&s_empty[e]));
-                if (kb == KB - 1) mma_commit(smem_u32(&s_tfull[t]));
-                // the stage of g - 1 takes stage g - 1 + kStages once MMA(g - 1) has read it
-                const int gn = g - 1 + kStages;
-                if (g >= 1 && gn < G) {
-                    wait_ok(ok, smem_u32(&s_empty[(g - 1) % kStages]), (uint32_t)(((g - 1) / kStages) & 1), status);
-                    if (!ok) break;
-                    issue(gn);
-                }
-            }
-            // no MMA may still be running, and no copy still writing shared memory, at exit
-            mma_commit(smem_u32(&s_done));
-            bool fin = true;
-            wait_ok(fin, smem_u32(&s_done), 0u, status);
-            for (int e = 0; e < kStages; ++e)
-                if (g_last[e] >= 0) wait_ok(fin, smem_u32(&s_full[e]), (uint32_t)((g_last[e] / kStages) & 1), status);
-        }
-        __syncwarp();
-    } else {
-        cost_epilogue(N, M, p, r0, nC, tmem, s_tfull, s_tfree, xnorm, ynorm, Dsk, stg, ok, status);
-    }
-
-    fence_before_sync();
-    __syncthreads();
-    if (warp == 0) {
-        fence_after_sync();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -400,51 +287,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 size_t simg_bytes(int P, int L, int D)
 {
-    const int KB = (D + 31) / 32;
-    const int Lpad = (L + kTile - 1) / kTile * kTile;
-    return (size_t)P * KB * 2 * Lpad * 128;
+    const int KB = (D + kTcKFeat - 1) / kTcKFeat;
+    return (size_t)P * KB * 3 * simg_pad(L) * 128;
 }
 
-size_t snorm_bytes(int P, int L)
-{
-    const int Lpad = (L + kTile - 1) / kTile * kTile;
-    return (size_t)P * Lpad * sizeof(float);
-}
+size_t snorm_bytes(int P, int L) { return (size_t)P * simg_pad(L) * sizeof(float); }
 
-cudaError_t launch_simg(const Problems& pr, int P, int N, int M, int D, float* ximg, float* yimg, float* xnorm,
+cudaError_t launch_simg(const Problems& pr, int P, int N, int M, int D, void* ximg, void* yimg, float* xnorm,
                         float* ynorm, cudaStream_t st)
 {
-    const int KB = (D + 31) / 32;
-    const int Lmax = ((N > M ? N : M) + kTile - 1) / kTile * kTile;
-    const size_t smem = sizeof(float) * 32 * (32 * KB + 1);
+    const int KB = (D + kTcKFeat - 1) / kTcKFeat;
+    const int Lmax = simg_pad(N > M ? N : M);
+    const size_t smem = sizeof(float) * 32 * (kTcKFeat * KB + 1);
     cudaError_t e = cudaFuncSetAttribute(simg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    simg_kernel<<<dim3(Lmax / 32, P, 2), 256, smem, st>>>(pr, N, M, D, KB, ximg, yimg, xnorm, ynorm);
+    simg_kernel<<<dim3(Lmax / 32, P, 2), 256, smem, st>>>(pr, N, M, D, KB, static_cast<unsigned char*>(ximg),
+                                                          static_cast<unsigned char*>(yimg), xnorm, ynorm);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dist_tc(int P, int N, int M, int D, const float* ximg, const float* yimg, const float* xnorm,
+cudaError_t launch_dist_tc(int P, int N, int M, int D, const void* ximg, const void* yimg, const float* xnorm,
                            const float* ynorm, float* Dsk, int* status, cudaStream_t st)
 {
-    const int KB = (D + 31) / 32;
+    const int KB = (D + kTcKFeat - 1) / kTcKFeat;
     if (KB < 1 || KB > kMaxTcKBlocks) return cudaErrorInvalidValue;
     dim3 grid((N + kTile - 1) / kTile, P);
     const size_t stg = (size_t)kTcWarps * kStg * sizeof(float);
-    if (KB > 2) {
-        const size_t smem = 1024 + (size_t)kStages * kStageBytes + stg;
-        cudaError_t e = cudaFuncSetAttribute(dist_tc_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        dist_tc_stream_kernel<<<grid, kTcThreads, smem, st>>>(N, M, KB, ximg, yimg, xnorm, ynorm, Dsk, status);
-        return cudaGetLastError();
-    }
-    const size_t smem = 1024 + 2 * (size_t)KB * kBlockBytes + 2 * (size_t)KB * 2 * kYHalf + stg;
-    auto go = [&](auto kern) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        kern<<<grid, kTcThreads, smem, st>>>(N, M, ximg, yimg, xnorm, ynorm, Dsk, status);
-        return cudaGetLastError();
-    };
-    return KB == 1 ? go(dist_tc_kernel<1>) : go(dist_tc_kernel<2>);
+    const auto* xi = static_cast<const unsigned char*>(ximg);
+    const auto* yi = static_cast<const unsigned char*>(yimg);
+    const size_t smem = 1024 + kABytes + 2 * (size_t)kBBytes + stg;
+    cudaError_t e = cudaFuncSetAttribute(dist_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dist_tc_kernel<<<grid, kTcThreads, smem, st>>>(N, M, xi, yi, xnorm, ynorm, Dsk, status);
+    return cudaGetLastError();
 }
 
 }  // namespace sdtw

@@ -22,20 +22,25 @@ constexpr int kYS = kKC + 4;
 
 // Un-skew the 32x32 tile (rows of block rb, columns c0..c0+31) into es.
 // ROW_MAJOR: es[r*32 + c]; otherwise es[c*32 + r]. Entries outside the matrix are 0.
+// Returns whether this thread stored a non-zero value: away from the alignment
+// path E underflows to exactly 0, and a tile that is all zero adds nothing.
 template <bool ROW_MAJOR>
-__device__ __forceinline__ void load_tile(const float* __restrict__ Esk, int N, int M, int p, int rb, int c0,
+__device__ __forceinline__ bool load_tile(const float* __restrict__ Esk, int N, int M, int p, int rb, int c0,
                                           float* es)
 {
     const float* base = Esk + skew_index(N, M, p, rb, 0, 0);
+    bool nz = false;
     for (int idx = threadIdx.x; idx < 63 * 32; idx += blockDim.x) {
         const int tt = idx >> 5, rr = idx & 31;
         const int c = tt - rr;
         if (c < 0 || c >= 32) continue;
         const bool ok = (c0 + c < M) && (rb * 32 + rr < N);
         const float v = ok ? base[(long long)(c0 + tt) * 32 + rr] : 0.f;
+        nz = nz || (v != 0.f);
         if (ROW_MAJOR) es[rr * 32 + c] = v;
         else es[c * 32 + rr] = v;
     }
+    return nz;
 }
 
 // grid (NB, P, ceil(D/64)), block 128.
@@ -59,7 +64,7 @@ __global__ void __launch_bounds__(128) grad_rows_kernel(const GradParams g)
 #pragma unroll
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
     for (int c0 = 0; c0 < M; c0 += 32) {
-        load_tile<false>(g.E, N, M, p, rb, c0, es);
+        if (!__syncthreads_or(load_tile<false>(g.E, N, M, p, rb, c0, es))) continue;  // an all-zero tile
         for (int idx = threadIdx.x; idx < 32 * kKC; idx += blockDim.x) {
             const int c = idx / kKC, kk = idx - c * kKC;
             ys[c * kYS + kk] = (c0 + c < M && kb + kk < D) ? yb[(size_t)(c0 + c) * D + kb + kk] : 0.f;
@@ -115,7 +120,7 @@ __global__ void __launch_bounds__(128) grad_cols_kernel(const GradParams g)
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
     const int NB = (N + 31) / 32;
     for (int rb = 0; rb < NB; ++rb) {
-        load_tile<true>(g.E, N, M, p, rb, c0, es);
+        if (!__syncthreads_or(load_tile<true>(g.E, N, M, p, rb, c0, es))) continue;  // an all-zero tile
         for (int idx = threadIdx.x; idx < 32 * kKC; idx += blockDim.x) {
             const int r = idx / kKC, kk = idx - r * kKC;
             const int i = rb * 32 + r;

@@ -105,30 +105,49 @@ cudaError_t launch_grad_tc(const GradParams& g, bool cols, const float* bimg, in
 size_t egemm_smem_bytes(int D);
 size_t egemm_bimg_bytes(int P, int K, int D);
 
-// Tensor-core cost tensor (dist_tc.cu), D <= 64: operand images of x and y
-// (simg_bytes each), their squared row norms (snorm_bytes each), then the
-// skewed cost tensor. status receives kStatusTimeout if a bounded wait expires.
-// Widest features the tensor-core cost kernels take (K-blocks of 32 features);
-// beyond it the difference-form kernels compute the costs.
-constexpr int kMaxTcKBlocks = 8;
+// Tensor-core cost tensor (dist_tc.cu), D <= kTcKFeat * kMaxTcKBlocks: operand
+// images of x and y (simg_bytes each), their squared row norms (snorm_bytes each),
+// then the skewed cost tensor. status receives kStatusTimeout if a bounded wait
+// expires. Beyond that width the difference-form kernels compute the costs.
+constexpr int kTcKFeat = 64;      // features per K-block of the bf16 operand images
+constexpr int kMaxTcKBlocks = 1;  // D <= 64: the fp32 state's parity needs exact costs beyond
 size_t simg_bytes(int P, int L, int D);
-// Operand image layout (floats): per problem, per K-block of 32 features, hi then
-// lo part, Lpad = roundup(L, 128) rows of 32 tf32 values (128 bytes, 16-byte
-// chunks swizzled by row mod 8); row norms at p * Lpad + r.
+// Operand image layout (bytes): per problem, per K-block of 64 features, the three
+// bf16 parts v = v0 + v1 + v2, each Lpad = roundup(L, 128) rows of 128 bytes (64
+// bf16; 16-byte chunks swizzled by row mod 8); row norms (fp32) at p * Lpad + r.
 __host__ __device__ inline size_t simg_offset(int p, int KB, int kb, int part, int Lpad, int r)
 {
-    return ((((size_t)p * KB + kb) * 2 + part) * (size_t)Lpad + (size_t)r) * 32;
+    return ((((size_t)p * KB + kb) * 3 + part) * (size_t)Lpad + (size_t)r) * 128;
 }
 __host__ __device__ inline int simg_pad(int L) { return (L + 127) / 128 * 128; }
 size_t snorm_bytes(int P, int L);
-cudaError_t launch_simg(const Problems& pr, int P, int N, int M, int D, float* ximg, float* yimg, float* xnorm,
+cudaError_t launch_simg(const Problems& pr, int P, int N, int M, int D, void* ximg, void* yimg, float* xnorm,
                         float* ynorm, cudaStream_t st);
-cudaError_t launch_dist_tc(int P, int N, int M, int D, const float* ximg, const float* yimg, const float* xnorm,
+cudaError_t launch_dist_tc(int P, int N, int M, int D, const void* ximg, const void* yimg, const float* xnorm,
                            const float* ynorm, float* Dsk, int* status, cudaStream_t st);
+
+// Exact fixed-point operand images for the extended fused forward (wavefront_x.cu),
+// D <= kMaxXtcD: per problem, per K-block of 64 features, NS = kXtcSlices bf16
+// digit slices, each Lpad rows of 128 bytes
+// (swizzled as the bf16 images above); per row the info (norm hi, norm lo, scale
+// exponent as int bits, 0).
+constexpr int kMaxXtcD = 128;
+constexpr int kXtcSlices = 5;
+__host__ __device__ inline size_t oimg_offset(int p, int KB, int kb, int NS, int slice, int Lpad, int r)
+{
+    return ((((size_t)p * KB + kb) * NS + slice) * (size_t)Lpad + (size_t)r) * 128;
+}
+size_t oimg_bytes(int P, int L, int D);
+size_t oinfo_bytes(int P, int L);
+cudaError_t launch_oimg(const Problems& pr, int P, int N, int M, int D, void* ximg, void* yimg, void* xinfo,
+                        void* yinfo, cudaStream_t st);
+// Extended fused forward with exact tensor-core cost tiles: q.W must be 4.
+cudaError_t launch_forward_xtc(WaveParams q, const void* ximg, const void* yimg, const void* xinfo,
+                               const void* yinfo, cudaStream_t st);
 
 // Fused forward with tensor-core cost tiles (wavefront_tc.cu): q.W must be 4
 // (128-row strips), D <= 64; the operand images and norms as for launch_dist_tc.
-cudaError_t launch_forward_tc(WaveParams q, const float* ximg, const float* yimg, const float* xnorm,
+cudaError_t launch_forward_tc(WaveParams q, const void* ximg, const void* yimg, const float* xnorm,
                               const float* ynorm, cudaStream_t st);
 size_t wave_tc_smem(int D);
 

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 
 #include "common.cuh"
 
@@ -50,6 +51,48 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b
         "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// Instruction descriptor of kind::f16 with bf16 A and B (both K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// The three MMAs of one 16-wide K step (byte offset ko along K) of the exact
+// product of split operands: a = [x0 | x1 | x2], the three parts of M rows each,
+// part_a bytes apart; b = [y0 ; y1 ; y2] stacked along N, `rows` y rows per part,
+// contiguous. Each x part multiplies all three y parts, so every one of the nine
+// part products (each exact in fp32: 8 x 8 significant bits) enters; tensor-memory
+// columns [0, rows), [rows, 2 rows) and [2 rows, 3 rows) of d receive the y0, y1
+// and y2 terms, whose sum is x . y up to the fp32 accumulation.
+__device__ __forceinline__ void mma_bf16x3(uint32_t d, uint32_t a, uint32_t b, int M, int rows, uint32_t part_a,
+                                           uint32_t ko, uint32_t acc)
+{
+    const uint32_t id = idesc_bf16(M, 3 * rows);
+    mma_bf16(d, sdesc(a + ko), sdesc(b + ko), id, acc);
+    mma_bf16(d, sdesc(a + part_a + ko), sdesc(b + ko), id, 1u);
+    mma_bf16(d, sdesc(a + 2 * part_a + ko), sdesc(b + ko), id, 1u);
+}
+
+// fp32 -> three bf16 parts with v == b0 + b1 + b2 exactly: each part takes the
+// next 8 significant bits (round to nearest), and the remainders are exact in
+// fp32 (24 = 3 x 8 bits). Packed as raw 16-bit patterns.
+__device__ __forceinline__ void split_bf16x3(float v, uint16_t& b0, uint16_t& b1, uint16_t& b2) {
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(h0);
+    const __nv_bfloat16 h1 = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(h1);
+    const __nv_bfloat16 h2 = __float2bfloat16_rn(r2);
+    b0 = __bfloat16_as_ushort(h0);
+    b1 = __bfloat16_as_ushort(h1);
+    b2 = __bfloat16_as_ushort(h2);
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
@@ -81,6 +124,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
         }
     }
     return true;
+}
+
+// tcgen05.ld of 8 columns without the wait: issue several, then tmem_wait_ld()
+// once before reading any of them.
+__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = __uint_as_float(r[q]);
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {

@@ -10,10 +10,11 @@
 //
 //   C[i,j] = |x_i|^2 + |y_j|^2 - 2 x_i . y_j,
 //
-// with the x rows of the CTA resident in shared memory and 32-row y tiles
-// streamed in by bulk copy, both as the pre-split 3xTF32 operand images of
-// dist_tc.cu (x_hi . [y_hi ; y_lo] + x_lo . y_hi). A fifth warp issues the
-// copies and MMAs into a ring of tensor-memory tiles; at the start of every
+// from the exact three-part bf16 operand images of dist_tc.cu (all nine part
+// products). The x rows of the CTA stay in
+// shared memory and 32-row y tiles stream in by bulk copy. A fifth warp issues
+// the copies and MMAs into a ring of
+// tensor-memory tiles (three 32-column groups each); at the start of every
 // 32-step period each DP warp loads its 32 rows of the next tile (tcgen05.ld),
 // releases the tile, and writes the costs into its 64-column shared ring in the
 // order its lanes read them. The DP step itself then costs one shared load.
@@ -36,24 +37,22 @@ using namespace tc;
 
 constexpr int kDpWarps = 4;               // 128 rows per CTA: the MMA tile height
 constexpr int kIssuerWarp = kDpWarps;     // warp 4: bulk copies and MMAs
-constexpr int kRT = 8;                    // cost tiles in tensor memory, 64 columns each
-constexpr int kRB = 4;                    // y tiles in shared memory
-constexpr int kTmemCols = kRT * 64;       // 512: the whole tensor memory of the SM
-constexpr uint32_t kABlock = 128 * 128;   // one K-block of the CTA's 128 x rows (bytes)
-constexpr uint32_t kBHalf = 32 * 128;     // one K-block of 32 y rows, hi or lo (bytes)
-// Wide features (more than two K-blocks): the x rows are not resident; each
-// K-block of a cost tile is one stage of a kStages-deep ring holding the CTA's x
-// rows (hi, lo) and the tile's y rows (hi, lo) of that K-block.
-constexpr int kStages = 3;
-constexpr uint32_t kStageBytes = 2 * kABlock + 2 * kBHalf;
+constexpr int kSlotCols = 96;             // tensor-memory columns of a cost tile: the y0, y1, y2 groups
+constexpr int kRT = 5;                    // cost tiles in tensor memory
+constexpr int kTmemCols = 512;            // the whole tensor memory of the SM (kRT * kSlotCols rounded up)
+constexpr int kRB = 3;                    // y tiles in shared memory
+constexpr uint32_t kAPart = 128 * 128;    // one bf16 part of one K-block of the CTA's 128 x rows (bytes)
+constexpr uint32_t kABlock = 3 * kAPart;  // the three parts [x0 | x1 | x2] of one K-block
+constexpr uint32_t kBPart = 32 * 128;     // one part of one K-block of 32 y rows
+constexpr uint32_t kBBlock = 3 * kBPart;  // [y0 ; y1 ; y2] of one K-block of a y tile
 
 }  // namespace
 
 size_t wave_tc_smem(int D)
 {
-    const int KB = (D + 31) / 32;
-    const size_t operands = KB > 2 ? (size_t)kStages * kStageBytes
-                                   : 2 * (size_t)KB * kABlock + (size_t)kRB * KB * 2 * kBHalf;
+    const int KB = (D + kTcKFeat - 1) / kTcKFeat;
+    const size_t operands = (size_t)KB * kABlock + (size_t)kRB * KB * kBBlock;
+    // per DP warp: a 64-column cost ring and two tiles' y norms
     return wave_smem_fixed(kDpWarps, false) + 1024 + operands + (size_t)kDpWarps * (64 + 2) * 32 * sizeof(float);
 }
 
@@ -67,11 +66,9 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src)
 
 // STORE: the per-cell state for the backward is written (false in a checkpointed
 // forward, which keeps only the strips' boundary rows).
-// STREAM: the x rows' K-blocks are streamed with the y tiles through a stage ring
-// (wide features) instead of staying in shared memory.
-template <bool STORE, bool STREAM>
+template <bool STORE>
 __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
-    fwd_tc_kernel(const WaveParams q, const float* __restrict__ ximg, const float* __restrict__ yimg,
+    fwd_tc_kernel(const WaveParams q, const unsigned char* __restrict__ ximg, const unsigned char* __restrict__ yimg,
                   const float* __restrict__ xnorm, const float* __restrict__ ynorm)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -83,7 +80,6 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     __shared__ double s_red[kMaxWarps];
     __shared__ int s_last;
     __shared__ uint64_t s_a, s_fin, s_bfull[kRB], s_bempty[kRB], s_tfull[kRT], s_tfree[kRT];
-    __shared__ uint64_t s_sfull[kStages], s_sempty[kStages];
     __shared__ uint32_t s_tmem;
 
     if (threadIdx.x == 0) s_tk = atomicAdd(q.ticket_f, 1);
@@ -94,7 +90,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     const int tk = s_tk;
     const int p = tk % q.P, strip = q.strip0 + tk / q.P;
     const int N = q.N, M = q.M, T = skew_T(M);
-    const int KB = (q.D + 31) / 32;
+    const int KB = (q.D + kTcKFeat - 1) / kTcKFeat;
     const int Npad = simg_pad(N), Mpad = simg_pad(M);
     const int rs0 = strip * W * 32;                              // first row of the CTA
     const int nact = min(W, max(1, (N - rs0 + 31) / 32));       // DP warps with rows
@@ -102,11 +98,9 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
 
     unsigned char* tcb = smem_raw + q.smem_fixed;
     unsigned char* base = tcb + ((1024u - (smem_u32(tcb) & 1023u)) & 1023u);
-    unsigned char* a_hi = base;
-    unsigned char* a_lo = base + KB * kABlock;
-    unsigned char* bring = base + 2 * KB * kABlock;               // [kRB][KB][hi 32 rows | lo 32 rows]
-    unsigned char* stages = base;                                 // STREAM: [kStages][A hi | A lo | B hi | B lo]
-    float* dts = reinterpret_cast<float*>(STREAM ? stages + kStages * kStageBytes : bring + kRB * KB * 2 * kBHalf);
+    unsigned char* a_img = base;                                  // [KB][x0 | x1 | x2]
+    unsigned char* bring = base + KB * kABlock;                   // [kRB][KB][y0 ; y1 ; y2]
+    float* dts = reinterpret_cast<float*>(bring + kRB * KB * kBBlock);
     float* nys = dts + W * 64 * 32;                                // [W][2][32] y norms of the next tiles
 
     if (threadIdx.x == 0) {
@@ -120,10 +114,6 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
             mbar_init(smem_u32(&s_tfull[t]), 1);
             mbar_init(smem_u32(&s_tfree[t]), nact);
         }
-        for (int e = 0; e < kStages; ++e) {
-            mbar_init(smem_u32(&s_sfull[e]), 1);
-            mbar_init(smem_u32(&s_sempty[e]), 1);
-        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
@@ -136,103 +126,41 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     float c0 = 0.f;  // scaled d(i, 0)
     bool active = false;
 
-    if (warp == kIssuerWarp && STREAM) {
-        if (lane == 0) {
-            // stage g = c * KB + kb carries K-block kb of the x rows and of y tile c
-            bool ok = true;
-            const int G = nT * KB;
-            int g_last[kStages];
-            for (int e = 0; e < kStages; ++e) g_last[e] = -1;
-            auto issue = [&](int g) {
-                const int c = g / KB, kb = g - c * KB, e = g % kStages;
-                unsigned char* st = stages + e * kStageBytes;
-                const uint32_t bar = smem_u32(&s_sfull[e]);
-                mbar_expect_tx(bar, kStageBytes);
-                bulk_g2s(smem_u32(st), ximg + simg_offset(p, KB, kb, 0, Npad, rs0), kABlock, bar);
-                bulk_g2s(smem_u32(st + kABlock), ximg + simg_offset(p, KB, kb, 1, Npad, rs0), kABlock, bar);
-                bulk_g2s(smem_u32(st + 2 * kABlock), yimg + simg_offset(p, KB, kb, 0, Mpad, 32 * c), kBHalf, bar);
-                bulk_g2s(smem_u32(st + 2 * kABlock + kBHalf), yimg + simg_offset(p, KB, kb, 1, Mpad, 32 * c), kBHalf,
-                         bar);
-                g_last[e] = g;
-            };
-            for (int g = 0; g < kStages && g < G; ++g) issue(g);
-            const uint32_t id2 = idesc_tf32(128, 64), id1 = idesc_tf32(128, 32);
-            for (int g = 0; g < G && ok; ++g) {
-                const int c = g / KB, kb = g - c * KB, e = g % kStages, t = c % kRT;
-                if (kb == 0 && c >= kRT) wait_ok(ok, smem_u32(&s_tfree[t]), (uint32_t)(((c - kRT) / kRT) & 1), status);
-                wait_ok(ok, smem_u32(&s_sfull[e]), (uint32_t)((g / kStages) & 1), status);
-                if (!ok) break;
-                fence_after_sync();
-                const uint32_t d = tmem + (uint32_t)(t * 64);
-                const uint32_t ah = smem_u32(stages + e * kStageBytes), al = ah + kABlock, bh = ah + 2 * kABlock;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
-                    mma_tf32(d, sdesc(ah + ko), sdesc(bh + ko), id2, (kb > 0 || ks > 0) ? 1u : 0u);
-                    mma_tf32(d, sdesc(al + ko), sdesc(bh + ko), id1, 1u);
-                }
-                mma_commit(smem_u32(&s_sempty[e]));
-                if (kb == KB - 1) mma_commit(smem_u32(&s_tfull[t]));
-                // the stage of g - 1 takes stage g - 1 + kStages once MMA(g - 1) has read it
-                const int gn = g - 1 + kStages;
-                if (g >= 1 && gn < G) {
-                    wait_ok(ok, smem_u32(&s_sempty[(g - 1) % kStages]), (uint32_t)(((g - 1) / kStages) & 1), status);
-                    if (!ok) break;
-                    issue(gn);
-                }
-            }
-            // every MMA has completed before tensor memory is released, and no copy is
-            // still writing shared memory when the CTA exits
-            mma_commit(smem_u32(&s_fin));
-            bool fin = true;
-            wait_ok(fin, smem_u32(&s_fin), 0u, status);
-            for (int e = 0; e < kStages; ++e)
-                if (g_last[e] >= 0) wait_ok(fin, smem_u32(&s_sfull[e]), (uint32_t)((g_last[e] / kStages) & 1), status);
-        }
-        __syncwarp();
-    } else if (warp == kIssuerWarp) {
+    if (warp == kIssuerWarp) {
         if (lane == 0) {
             bool ok = true;
             int y_last[kRB];
             for (int e = 0; e < kRB; ++e) y_last[e] = -1;
-            mbar_expect_tx(smem_u32(&s_a), 2u * KB * kABlock);
-            for (int kb = 0; kb < KB; ++kb) {
-                bulk_g2s(smem_u32(a_hi + kb * kABlock), ximg + simg_offset(p, KB, kb, 0, Npad, rs0), kABlock,
-                         smem_u32(&s_a));
-                bulk_g2s(smem_u32(a_lo + kb * kABlock), ximg + simg_offset(p, KB, kb, 1, Npad, rs0), kABlock,
-                         smem_u32(&s_a));
-            }
+            mbar_expect_tx(smem_u32(&s_a), (uint32_t)KB * kABlock);
+            for (int kb = 0; kb < KB; ++kb)
+                for (int part = 0; part < 3; ++part)
+                    bulk_g2s(smem_u32(a_img + kb * kABlock + part * kAPart),
+                             ximg + simg_offset(p, KB, kb, part, Npad, rs0), kAPart, smem_u32(&s_a));
             auto issue_y = [&](int c) {
                 const int e = c % kRB;
-                mbar_expect_tx(smem_u32(&s_bfull[e]), 2u * KB * kBHalf);
+                mbar_expect_tx(smem_u32(&s_bfull[e]), (uint32_t)KB * kBBlock);
                 for (int kb = 0; kb < KB; ++kb) {
-                    unsigned char* dst = bring + (e * KB + kb) * 2 * kBHalf;
-                    bulk_g2s(smem_u32(dst), yimg + simg_offset(p, KB, kb, 0, Mpad, 32 * c), kBHalf,
-                             smem_u32(&s_bfull[e]));
-                    bulk_g2s(smem_u32(dst + kBHalf), yimg + simg_offset(p, KB, kb, 1, Mpad, 32 * c), kBHalf,
-                             smem_u32(&s_bfull[e]));
+                    unsigned char* dst = bring + (e * KB + kb) * kBBlock;
+                    for (int part = 0; part < 3; ++part)
+                        bulk_g2s(smem_u32(dst + part * kBPart), yimg + simg_offset(p, KB, kb, part, Mpad, 32 * c),
+                                 kBPart, smem_u32(&s_bfull[e]));
                 }
                 y_last[e] = c;
             };
             for (int c = 0; c < kRB - 1 && c < nT; ++c) issue_y(c);
             wait_ok(ok, smem_u32(&s_a), 0u, status);
-            const uint32_t id2 = idesc_tf32(128, 64), id1 = idesc_tf32(128, 32);
             for (int c = 0; c < nT && ok; ++c) {
                 const int t = c % kRT, e = c % kRB;
                 if (c >= kRT) wait_ok(ok, smem_u32(&s_tfree[t]), (uint32_t)(((c - kRT) / kRT) & 1), status);
                 wait_ok(ok, smem_u32(&s_bfull[e]), (uint32_t)((c / kRB) & 1), status);
                 if (!ok) break;
                 fence_after_sync();
-                const uint32_t d = tmem + (uint32_t)(t * 64);
+                const uint32_t d = tmem + (uint32_t)(t * kSlotCols);
                 for (int kb = 0; kb < KB; ++kb) {
-                    const uint32_t ah = smem_u32(a_hi + kb * kABlock), al = smem_u32(a_lo + kb * kABlock);
-                    const uint32_t bh = smem_u32(bring + (e * KB + kb) * 2 * kBHalf);
+                    const uint32_t a = smem_u32(a_img + kb * kABlock), b = smem_u32(bring + (e * KB + kb) * kBBlock);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint32_t ko = ks * 32;  // 8 tf32 = 32 bytes along K
-                        mma_tf32(d, sdesc(ah + ko), sdesc(bh + ko), id2, (kb > 0 || ks > 0) ? 1u : 0u);
-                        mma_tf32(d, sdesc(al + ko), sdesc(bh + ko), id1, 1u);
-                    }
+                    for (int ks = 0; ks < 4; ++ks)  // 16 bf16 = 32 bytes along K per step
+                        mma_bf16x3(d, a, b, 128, 32, kAPart, ks * 32, (kb > 0 || ks > 0) ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&s_tfull[t]));
                 mma_commit(smem_u32(&s_bempty[e]));
@@ -306,9 +234,10 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                     wait_ok(tc_ok, smem_u32(&s_tfull[t]), (uint32_t)((c / kRT) & 1), status);
                     if (!__all_sync(kFull, tc_ok)) break;
                     fence_after_sync();
-                    float a[32], b[32];
-                    tmem_ld32(tq + (uint32_t)(t * 64), a);
-                    tmem_ld32(tq + (uint32_t)(t * 64 + 32), b);
+                    float a[32], b[32], e[32];
+                    tmem_ld32(tq + (uint32_t)(t * kSlotCols), a);
+                    tmem_ld32(tq + (uint32_t)(t * kSlotCols + 32), b);
+                    tmem_ld32(tq + (uint32_t)(t * kSlotCols + 64), e);
                     fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&s_tfree[t]));
@@ -322,7 +251,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const float ny = __shfl_sync(kFull, nyv, u);
-                        dt[((32 * c + u) & 63) * 32 + lane] = fmaxf(nx + ny - 2.f * (a[u] + b[u]), 0.f);
+                        dt[((32 * c + u) & 63) * 32 + lane] = fmaxf(nx + ny - 2.f * (a[u] + (b[u] + e[u])), 0.f);
                     }
                     __syncwarp();
                 }
@@ -434,10 +363,10 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
 
 }  // namespace
 
-cudaError_t launch_forward_tc(WaveParams q, const float* ximg, const float* yimg, const float* xnorm,
+cudaError_t launch_forward_tc(WaveParams q, const void* ximg, const void* yimg, const float* xnorm,
                               const float* ynorm, cudaStream_t st)
 {
-    if (q.W != kDpWarps || q.D > 32 * kMaxTcKBlocks) return cudaErrorInvalidValue;
+    if (q.W != kDpWarps || q.D > kTcKFeat * kMaxTcKBlocks) return cudaErrorInvalidValue;
     const int grid = q.P * q.S;
     q.smem_fixed = (int)wave_smem_fixed(kDpWarps, false);
     // more than half of the SM's shared memory: one CTA per SM, which the
@@ -450,11 +379,11 @@ cudaError_t launch_forward_tc(WaveParams q, const float* ximg, const float* yimg
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, (kDpWarps + 1) * 32, smem, st>>>(q, ximg, yimg, xnorm, ynorm);
+        kern<<<grid, (kDpWarps + 1) * 32, smem, st>>>(q, static_cast<const unsigned char*>(ximg),
+                                                       static_cast<const unsigned char*>(yimg), xnorm, ynorm);
         return cudaGetLastError();
     };
-    if (q.D > 64) return q.VH == nullptr ? go(fwd_tc_kernel<false, true>) : go(fwd_tc_kernel<true, true>);
-    return q.VH == nullptr ? go(fwd_tc_kernel<false, false>) : go(fwd_tc_kernel<true, false>);
+    return q.VH == nullptr ? go(fwd_tc_kernel<false>) : go(fwd_tc_kernel<true>);
 }
 
 }  // namespace sdtw

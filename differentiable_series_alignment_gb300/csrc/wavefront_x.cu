@@ -14,6 +14,7 @@
 #include "channel.cuh"
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace sdtw {
 
@@ -41,17 +42,6 @@ __device__ __forceinline__ dd sub_f(dd a, float f) {
     return fast2(s, e);
 }
 __device__ __forceinline__ float to_f(dd a) { return a.hi + a.lo; }
-__device__ __forceinline__ bool less(dd a, dd b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
-__device__ __forceinline__ dd sel(bool c, dd a, dd b) { return dd{c ? a.hi : b.hi, c ? a.lo : b.lo}; }
-__device__ __forceinline__ void sort3dd(dd a, dd b, dd c, dd& lo, dd& mid, dd& hi) {
-    const bool ab = less(a, b);
-    const dd t1 = sel(ab, a, b), t2 = sel(ab, b, a);
-    lo = sel(less(c, t1), c, t1);
-    const bool c2 = less(t2, c);
-    hi = sel(c2, c, t2);
-    const dd m2 = sel(c2, t2, c);
-    mid = sel(less(t1, m2), m2, t1);
-}
 
 // Double-float squared distance accumulator: exact differences and squares.
 struct DistDD {
@@ -75,6 +65,45 @@ __device__ __forceinline__ dd scale_dd(dd d, float k) {
     const float p = d.hi * k;
     const float pe = fmaf(d.hi, k, -p);
     return fast2(p, fmaf(d.lo, k, pe));
+}
+
+// One cell of the double-float recursion: d the scaled cost, vl = v[i,j-1] and
+// hu = h[i-1,j] the incoming differences (relative to the diagonal predecessor).
+// Gives h, v and the three transition log2-probabilities to the diag, left and up
+// predecessors (float4 x, y, z); the first column and the first row have a single
+// predecessor (R borders are +inf).
+//
+// The soft-min is factored around the predecessor with the smallest leading part:
+//   t = d + lo - log2(2^-d0 + 2^-dl + 2^-du),  dk = a_k - lo >= 0,
+// exact for any choice of lo among the three, so comparing the hi parts suffices.
+// The offsets dk only feed the fp32 log and the fp32 log-probabilities: formed as
+// (a.hi - lo.hi) + (a.lo - lo.lo), the first difference is exact whenever it is
+// small (Sterbenz), and a large one leaves a negligible term.
+__device__ __forceinline__ void xcell(dd d, dd vl, dd hu, bool col0, bool row0_lane, dd& h, dd& v, float4& lp)
+{
+    const dd zero = mk(0.f, 0.f), nbig = mk(-kBig, 0.f);
+    const dd m = (hu.hi < vl.hi) ? hu : vl;
+    const dd lo = (m.hi < 0.f) ? m : zero;
+    const float d0 = (0.f - lo.hi) - lo.lo;
+    const float dl = (vl.hi - lo.hi) + (vl.lo - lo.lo);
+    const float du = (hu.hi - lo.hi) + (hu.lo - lo.lo);
+    const float L = log2f((exp2_neg(-d0) + exp2_neg(-dl)) + exp2_neg(-du));
+    const dd tt = sub_f(add(d, lo), L);
+    h = sub(tt, vl);
+    v = sub(tt, hu);
+    float lpd = -d0 - L;
+    float lpl = -dl - L;
+    float lpu = -du - L;
+    if (col0) {        // first column: only the upper predecessor (or none at (0,0))
+        h = nbig;
+        v = row0_lane ? nbig : d;
+        lpd = -kBig; lpl = -kBig; lpu = row0_lane ? -kBig : 0.f;
+    } else if (row0_lane) {  // first row: only the left predecessor
+        h = d;
+        v = nbig;
+        lpd = -kBig; lpl = 0.f; lpu = -kBig;
+    }
+    lp = make_float4(lpd, lpl, lpu, 0.f);
 }
 
 }  // namespace
@@ -287,27 +316,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
                 } else {
                     d = scale_dd(mk(dc[u].x, dc[u].y), scale);
                 }
-                dd lo, mid, hi;
-                sort3dd(zero, vl, hu, lo, mid, hi);
-                const float e1 = to_f(sub(lo, mid)), e2 = to_f(sub(lo, hi));
-                const float L = log2f((1.f + exp2_neg(e1)) + exp2_neg(e2));
-                const dd tt = sub_f(add(d, lo), L);
-                dd h = sub(tt, vl), v = sub(tt, hu);
-                float lpd = to_f(lo) - L;
-                float lpl = to_f(sub(lo, vl)) - L;
-                float lpu = to_f(sub(lo, hu)) - L;
                 const bool col0 = (j == 0);
-                if (col0) {        // first column: only the upper predecessor (or none at (0,0))
-                    h = nbig;
-                    v = row0_lane ? nbig : d;
-                    lpd = -kBig; lpl = -kBig; lpu = row0_lane ? -kBig : 0.f;
-                } else if (row0_lane) {  // first row: only the left predecessor
-                    h = d;
-                    v = nbig;
-                    lpd = -kBig; lpl = 0.f; lpu = -kBig;
-                }
+                dd h, v;
+                float4 lp;
+                xcell(d, vl, hu, col0, row0_lane, h, v, lp);
                 c0 = col0 ? d : c0;
-                lpp[(long long)s * 32] = make_float4(lpd, lpl, lpu, 0.f);
+                lpp[(long long)s * 32] = lp;
                 const bool valid = (unsigned)j < (unsigned)M;
                 if (chan_lane && valid) {
                     Slot* dst = chan_out + 2 * (j & chan_mask);
@@ -354,6 +368,618 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
             q.loss[p] = (float)(tot * (double)q.unscale);
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// Exact cost tiles on the tensor cores for the extended fused forward (D <= 128)
+//
+// The double-float DP needs each cost to ~1e-9 of itself, beyond any fp32 split
+// product (whose fp32 accumulation rounds). The dot x_i . y_j is therefore made
+// exact in fixed point and evaluated on the tensor cores in integer arithmetic:
+// every row v of x or y is scaled by its own power of two s = 2^e > max |v_k| and
+// rounded to F = NS * b bits of fixed point, V_k = rint(v_k 2^(F-1) / s), so
+// |v_k - s V_k 2^-(F-1)| <= s 2^-F, and V_k is written as NS balanced base-2^b
+// digits,
+//   V_k = sum_l a_l 2^(b (NS-1-l)),  |a_l| <= 2^(b-1),
+// each an integer that bf16 holds exactly (oimg_kernel). Then
+//   x . y = s_x s_y sum_sigma 2^(2 - 2b - b sigma) S_sigma,
+//   S_sigma = sum_{l+m=sigma} sum_k a_l,k b_m,k,
+// and the level sums S_sigma for sigma <= NS-1 are bf16 MMAs accumulated in fp32
+// in tensor memory: every partial sum is an integer of magnitude below
+// NS D 2^(2b-2) < 2^24, so fp32 holds it exactly (checked on the GB300 up to
+// 2^23.98 against int64 sums) and the level sums are exact. The digit set:
+// NS = 5 digits of b = 8 bits (F = 40) for D <= 128 (5 * 128 * 2^14 < 2^24). The
+// MMA of x digit l multiplies the stacked y digits [b_0 ; ... ; b_(NS-1-l)] into
+// tensor-memory columns starting at level l, so product (l, m) lands in level
+// l + m: NS MMAs (N = 32 NS, ..., 32 columns) per 16-wide K step. Error bound of
+// x . y: the fixed-point rounding of both rows, D (|y|_max s_x + |x|_max s_y) 2^-F
+// <= 2 D s_x s_y 2^-F, plus the dropped levels sigma >= NS, below
+// (NS+2) D s_x s_y 2^-F: at D = 128, s <= 4 (unit-variance data) and F = 40, below
+// 2e-8 absolute, ~1e-10 of a cost. The DP warps combine the level sums, the
+// exponents and the double-float row norms into C = |x|^2 + |y|^2 - 2 x . y as a
+// double-float.
+namespace {
+
+constexpr int kXDpWarps = 4;                   // 128 rows per CTA: the MMA tile height
+constexpr int kXIssuer = kXDpWarps;            // warp 4: bulk copies and MMAs
+constexpr uint32_t kXAPart = 128 * 128;        // one digit of one K-block of 128 x rows
+constexpr uint32_t kXBPart = 32 * 128;         // one digit of one K-block of 32 y rows
+
+// The digit set: NS = 5 digits of DB = 8 bits. RT cost tiles of NS * 32 columns
+// share the 512 tensor-memory columns, and RT >= 3 is required: a DP warp may start
+// its group of 16 steps at s0 only after the warp above has finished step s0 + 46,
+// so warp 3 releases tile c - RT (at step 32 (c - RT)) only once warp 0 has reached
+// step 32 (c - RT) + 94; with RT = 3 that is step 32 c - 2, before warp 0 needs tile
+// c, while with RT = 2 warp 0 would already wait for tile c and nobody progresses.
+// Six digits (192 columns a tile) leave room for two tiles only, which is why the
+// exact tiles stop at D = 128.
+template <int NS> struct XDigits {
+    static_assert(NS == 5, "five 8-bit digits: three cost tiles fit in tensor memory");
+    static constexpr int DB = 8;                          // bits per digit
+    static constexpr int RT = 3;                          // cost tiles in tensor memory (NS * 32 columns each)
+    static constexpr int SlotCols = NS * 32;
+    static constexpr uint32_t A = NS * kXAPart;           // all digits of one K-block of the x rows
+    static constexpr uint32_t B = NS * kXBPart;           // [b_0 ; ... ; b_(NS-1)] of one K-block of a y tile
+    static constexpr uint32_t Stage = A + B;
+};
+
+// Shared memory of the operand region: one K-block keeps the x digits resident
+// with a two-entry ring of y tiles; more K-blocks stream through one stage.
+__host__ __device__ inline uint32_t xtc_region(int NS, int KB)
+{
+    const uint32_t a = NS * kXAPart, b = NS * kXBPart;
+    return KB == 1 ? a + 2 * b : a + b;
+}
+
+// bf16 bit pattern of a small integer (|v| <= 256: exact)
+__device__ __forceinline__ uint32_t bf16_int(int v)
+{
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn((float)v));
+}
+
+// grid (Lpad/32, P, 2): z = 0 writes the x image, z = 1 the y image. block 256.
+// Per row: its digits (five bf16 slices per K-block of 64 features, 128-byte
+// swizzled K-major rows), and info = (|v|^2 hi, |v|^2 lo, exponent e as int bits, 0).
+template <int NS>
+__global__ void __launch_bounds__(256) oimg_kernel(Problems pr, int N, int M, int D, int KB,
+                                                   unsigned char* __restrict__ ximg, unsigned char* __restrict__ yimg,
+                                                   float4* __restrict__ xinfo, float4* __restrict__ yinfo)
+{
+    extern __shared__ float t[];  // [32][D64 + 1]
+    __shared__ int s_exp[32];
+    const bool isy = blockIdx.z == 1;
+    const int p = blockIdx.y, r0 = blockIdx.x * 32;
+    const int L = isy ? M : N;
+    const int Lpad = simg_pad(L);
+    if (r0 >= Lpad) return;
+    const float* src = isy ? pr.y(p) : pr.x(p);
+    unsigned char* img = isy ? yimg : ximg;
+    float4* info = isy ? yinfo : xinfo;
+    const int D64 = kTcKFeat * KB, ld = D64 + 1;
+    const int n = 32 * D64 / 256;
+    for (int u0 = 0; u0 < n; u0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = threadIdx.x + 256 * (u0 + u);
+            const int r = idx / D64, k = idx - r * D64;
+            v[u] = (r0 + r < L && k < D) ? src[(size_t)(r0 + r) * D + k] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = threadIdx.x + 256 * (u0 + u);
+            const int r = idx / D64, k = idx - r * D64;
+            t[r * ld + k] = v[u];
+        }
+    }
+    __syncthreads();
+    {
+        // row norm as a double-float (exact squares, TwoSum sums) and the row's scale
+        // exponent: eight threads per row, then a TwoSum / max reduction across them
+        const int r = threadIdx.x >> 3, part = threadIdx.x & 7;
+        DistDD acc;
+        float mx = 0.f;
+        for (int k = part; k < D; k += 8) {
+            const float x = t[r * ld + k];
+            acc.add_term(x, 0.f);
+            mx = fmaxf(mx, fabsf(x));
+        }
+        float s = acc.s, c = acc.c;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const float so = __shfl_xor_sync(0xffffffffu, s, o), co = __shfl_xor_sync(0xffffffffu, c, o);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            float sn, err;
+            two_sum(s, so, sn, err);
+            s = sn;
+            c += co + err;
+        }
+        int e = 0;
+        if (mx > 0.f) frexpf(mx, &e);   // mx < 2^e
+        if (part == 0) {
+            const dd nrm = fast2(s, c);
+            info[(size_t)p * Lpad + r0 + r] = make_float4(nrm.hi, nrm.lo, __int_as_float(e), 0.f);
+            s_exp[r] = e;
+        }
+    }
+    __syncthreads();
+    // digits: one 16-byte chunk (8 features) of all NS slices per thread and pass
+    constexpr int DB = XDigits<NS>::DB, F = NS * DB, HALF = 1 << (DB - 1), MASK = (1 << DB) - 1;
+    const size_t slice_bytes = (size_t)Lpad * 128;
+    for (int idx = threadIdx.x; idx < 32 * D64 / 8; idx += blockDim.x) {
+        const int c8 = idx & 7, r = (idx >> 3) & 31, kb = idx >> 8;
+        const float* src8 = t + r * ld + kb * kTcKFeat + 8 * c8;
+        const double sc = ldexp(1.0, F - 1 - s_exp[r]);   // exact power of two
+        uint32_t w[NS][4];
+#pragma unroll
+        for (int q = 0; q < 8; q += 2) {
+            uint32_t lo[NS], hi[NS];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                long long X = __double2ll_rn((double)src8[q + h] * sc);   // |X| <= 2^(F-1)
+                uint32_t* dst = h ? hi : lo;
+#pragma unroll
+                for (int l = NS - 1; l > 0; --l) {
+                    const int d = (int)((X + HALF) & MASK) - HALF;        // balanced digit
+                    dst[l] = bf16_int(d);
+                    X = (X - d) >> DB;
+                }
+                dst[0] = bf16_int((int)X);                                 // |a_0| <= 2^(DB-1)
+            }
+#pragma unroll
+            for (int l = 0; l < NS; ++l) w[l][q / 2] = lo[l] | (hi[l] << 16);
+        }
+        unsigned char* row = img + oimg_offset(p, KB, kb, NS, 0, Lpad, r0 + r) + 16 * (c8 ^ (r & 7));
+#pragma unroll
+        for (int l = 0; l < NS; ++l)
+            *reinterpret_cast<uint4*>(row + l * slice_bytes) = make_uint4(w[l][0], w[l][1], w[l][2], w[l][3]);
+    }
+}
+
+// x . y from its exact level sums S[0..NS-1]: sum_sigma 2^(-DB sigma) S_sigma as a
+// double-float (each scaled term is exact in fp32), smallest first, times 2^k.
+// 2^k for k in the normal range [-126, 127], exactly.
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
+
+template <int NS>
+__device__ __forceinline__ dd levels_dd(const float (&S)[NS], int k)
+{
+    constexpr int DB = XDigits<NS>::DB;
+    dd a = mk(S[NS - 1] * pow2i(-DB * (NS - 1)), 0.f);
+#pragma unroll
+    for (int l = NS - 2; l >= 0; --l) a = add(a, mk(S[l] * pow2i(-DB * l), 0.f));
+    if (k >= -126 && k <= 127) {
+        const float f = pow2i(k);
+        return mk(a.hi * f, a.lo * f);
+    }
+    return mk(ldexpf(a.hi, k), ldexpf(a.lo, k));
+}
+
+// 16-byte asynchronous global -> shared copy (completion: cp.async.wait_group).
+__device__ __forceinline__ void cp_async16x(void* dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+
+// Extended fused forward with the exact tensor-core cost tiles. Same recursion,
+// channels and loss as fwdx_kernel<true>, with the CTA shape of fwd_tc_kernel: 4 DP
+// warps (128 rows, the MMA height) and an issuer warp that streams each K-block of
+// the CTA's x digits with the y tile's digits through one stage buffer and issues
+// the level MMAs into a ring of three tensor-memory tiles. At the start of every
+// 32-step period each DP warp reads its 32 rows of the next tile's five levels
+// (tcgen05.ld), releases the tile, and writes the double-float costs into its
+// 64-column shared ring (hi and lo planes). Hand-offs (mbarriers, waits bounded):
+//   s_sfull    the stage's copies landed        s_sempty  the MMAs reading it are done
+//   s_tfull[t] cost tile t in TMEM              s_tfree[t] every DP warp with rows read it
+template <int NS>
+__global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
+    fwdx_tc_kernel(const WaveParams q, const unsigned char* __restrict__ ximg, const unsigned char* __restrict__ yimg,
+                   const float4* __restrict__ xinfo, const float4* __restrict__ yinfo)
+{
+    using X = XDigits<NS>;
+    constexpr int kXRT = X::RT, kXSlotCols = X::SlotCols, kXSlices = NS;
+    constexpr uint32_t kXA = X::A, kXStage = X::Stage;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr int W = kXDpWarps;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Slot* ring = reinterpret_cast<Slot*>(smem_raw);                              // [W][kRing][2]
+    volatile int* cons = reinterpret_cast<volatile int*>(ring + 2 * W * kRing);  // [W]
+    __shared__ int s_tk;
+    __shared__ double s_red[kMaxWarps];
+    __shared__ int s_last;
+    __shared__ uint64_t s_sfull, s_sempty, s_fin, s_tfull[kXRT], s_tfree[kXRT], s_bfull[2], s_bempty[2];
+    __shared__ uint32_t s_tmem;
+
+    if (threadIdx.x == 0) s_tk = atomicAdd(q.ticket_f, 1);
+    if (threadIdx.x < W) cons[threadIdx.x] = 0;
+    for (int k = threadIdx.x; k < 2 * W * kRing; k += blockDim.x) ring[k].tag = 0u;
+    __syncthreads();
+
+    const int tk = s_tk;
+    const int p = tk % q.P, strip = tk / q.P;
+    const int N = q.N, M = q.M, T = skew_T(M);
+    const int KB = (q.D + kTcKFeat - 1) / kTcKFeat;
+    // one K-block: the x digits stay resident and y tiles come through a two-entry ring
+    const bool resident = KB == 1;
+    const int Npad = simg_pad(N), Mpad = simg_pad(M);
+    const int rs0 = strip * W * 32;
+    const int nact = min(W, max(1, (N - rs0 + 31) / 32));
+    const int nT = (M + 31) / 32;
+
+    unsigned char* tcb = smem_raw + q.smem_fixed;
+    unsigned char* stage = tcb + ((1024u - (tc::smem_u32(tcb) & 1023u)) & 1023u);   // [x digits | y digits]
+    float* dts = reinterpret_cast<float*>(stage + xtc_region(NS, KB));              // [W][hi, lo][64][32]
+    float4* yis = reinterpret_cast<float4*>(dts + W * 2 * 64 * 32);                 // [W][2][32] y info
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(tc::smem_u32(&s_sfull), 1);
+        tc::mbar_init(tc::smem_u32(&s_sempty), 1);
+        tc::mbar_init(tc::smem_u32(&s_fin), 1);
+        for (int t = 0; t < kXRT; ++t) {
+            tc::mbar_init(tc::smem_u32(&s_tfull[t]), 1);
+            tc::mbar_init(tc::smem_u32(&s_tfree[t]), nact);
+        }
+        for (int e = 0; e < 2; ++e) {
+            tc::mbar_init(tc::smem_u32(&s_bfull[e]), 1);
+            tc::mbar_init(tc::smem_u32(&s_bempty[e]), 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+    int* status = q.status;
+    const dd zero = mk(0.f, 0.f);
+
+    dd c0 = zero;  // scaled d(i, 0)
+    bool active = false;
+
+    if (warp == kXIssuer && resident) {
+        if (lane == 0) {
+            // the x digits once; y tile c into ring entry c & 1, refilled once MMA(c) has read it
+            bool ok = true;
+            int y_last[2] = {-1, -1};
+            const uint32_t abar = tc::smem_u32(&s_sfull);
+            tc::mbar_expect_tx(abar, kXA);
+            for (int l = 0; l < kXSlices; ++l)
+                tc::bulk_g2s(tc::smem_u32(stage + l * kXAPart), ximg + oimg_offset(p, 1, 0, NS, l, Npad, rs0), kXAPart,
+                             abar);
+            auto issue_y = [&](int c) {
+                const int e = c & 1;
+                const uint32_t bar = tc::smem_u32(&s_bfull[e]);
+                tc::mbar_expect_tx(bar, X::B);
+                for (int l = 0; l < kXSlices; ++l)
+                    tc::bulk_g2s(tc::smem_u32(stage + kXA + e * X::B + l * kXBPart),
+                                 yimg + oimg_offset(p, 1, 0, NS, l, Mpad, 32 * c), kXBPart, bar);
+                y_last[e] = c;
+            };
+            for (int c = 0; c < 2 && c < nT; ++c) issue_y(c);
+            tc::wait_ok(ok, abar, 0u, status);
+            for (int c = 0; c < nT && ok; ++c) {
+                const int e = c & 1, t = c % kXRT;
+                if (c >= kXRT) tc::wait_ok(ok, tc::smem_u32(&s_tfree[t]), (uint32_t)(((c - kXRT) / kXRT) & 1), status);
+                tc::wait_ok(ok, tc::smem_u32(&s_bfull[e]), (uint32_t)((c >> 1) & 1), status);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const uint32_t d0 = tmem + (uint32_t)(t * kXSlotCols);
+                const uint32_t a = tc::smem_u32(stage), b = a + kXA + e * X::B;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {   // 16 bf16 = 32 bytes along K per step
+                    const uint32_t ko = ks * 32;
+#pragma unroll
+                    for (int l = 0; l < kXSlices; ++l)
+                        tc::mma_bf16(d0 + (uint32_t)(l * 32), tc::sdesc(a + l * kXAPart + ko), tc::sdesc(b + ko),
+                                     tc::idesc_bf16(128, (kXSlices - l) * 32), (ks > 0 || l > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(tc::smem_u32(&s_bempty[e]));
+                tc::mma_commit(tc::smem_u32(&s_tfull[t]));
+                if (c + 2 < nT) {   // entry e takes tile c + 2 once MMA(c) has read it
+                    tc::wait_ok(ok, tc::smem_u32(&s_bempty[e]), (uint32_t)((c >> 1) & 1), status);
+                    if (!ok) break;
+                    issue_y(c + 2);
+                }
+            }
+            tc::mma_commit(tc::smem_u32(&s_fin));
+            bool fin = true;
+            tc::wait_ok(fin, tc::smem_u32(&s_fin), 0u, status);
+            for (int e = 0; e < 2; ++e)
+                if (y_last[e] >= 0) tc::wait_ok(fin, tc::smem_u32(&s_bfull[e]), (uint32_t)((y_last[e] >> 1) & 1), status);
+        }
+        __syncwarp();
+    } else if (warp == kXIssuer) {
+        if (lane == 0) {
+            // stage g = c * KB + kb: K-block kb of the x rows' and of y tile c's digits
+            bool ok = true;
+            const int G = nT * KB;
+            int g_last = -1;
+            for (int g = 0; g < G && ok; ++g) {
+                const int c = g / KB, kb = g - c * KB, t = c % kXRT;
+                if (kb == 0 && c >= kXRT)
+                    tc::wait_ok(ok, tc::smem_u32(&s_tfree[t]), (uint32_t)(((c - kXRT) / kXRT) & 1), status);
+                if (g >= 1) tc::wait_ok(ok, tc::smem_u32(&s_sempty), (uint32_t)((g - 1) & 1), status);
+                if (!ok) break;
+                const uint32_t bar = tc::smem_u32(&s_sfull);
+                tc::mbar_expect_tx(bar, kXStage);
+                for (int l = 0; l < kXSlices; ++l)
+                    tc::bulk_g2s(tc::smem_u32(stage + l * kXAPart), ximg + oimg_offset(p, KB, kb, NS, l, Npad, rs0),
+                                 kXAPart, bar);
+                for (int l = 0; l < kXSlices; ++l)
+                    tc::bulk_g2s(tc::smem_u32(stage + kXA + l * kXBPart),
+                                 yimg + oimg_offset(p, KB, kb, NS, l, Mpad, 32 * c), kXBPart, bar);
+                g_last = g;
+                tc::wait_ok(ok, bar, (uint32_t)(g & 1), status);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const uint32_t d0 = tmem + (uint32_t)(t * kXSlotCols);
+                const uint32_t a = tc::smem_u32(stage), b = a + kXA;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {   // 16 bf16 = 32 bytes along K per step
+                    const uint32_t ko = ks * 32;
+#pragma unroll
+                    for (int l = 0; l < kXSlices; ++l)   // digit l of x against y digits 0 .. NS-1-l: levels l .. NS-1
+                        tc::mma_bf16(d0 + (uint32_t)(l * 32), tc::sdesc(a + l * kXAPart + ko), tc::sdesc(b + ko),
+                                     tc::idesc_bf16(128, (kXSlices - l) * 32), (kb > 0 || ks > 0 || l > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(tc::smem_u32(&s_sempty));
+                if (kb == KB - 1) tc::mma_commit(tc::smem_u32(&s_tfull[t]));
+            }
+            // every MMA has completed before tensor memory is released, and no copy is
+            // still writing shared memory when the CTA exits
+            tc::mma_commit(tc::smem_u32(&s_fin));
+            bool fin = true;
+            tc::wait_ok(fin, tc::smem_u32(&s_fin), 0u, status);
+            if (g_last >= 0) tc::wait_ok(fin, tc::smem_u32(&s_sfull), (uint32_t)(g_last & 1), status);
+        }
+        __syncwarp();
+    } else {
+        const int rb = strip * W + warp, r0 = rb * 32, i = r0 + lane;
+        active = r0 < N;
+        const bool has_top = active && r0 > 0;
+        const bool top_global = has_top && warp == 0;
+        const bool has_bot = active && (r0 + 32 < N);
+        const bool bot_global = has_bot && warp == W - 1;
+        const bool row0_lane = (i == 0);
+        const int Nb = q.lens_n ? min(max(q.lens_n[p], 1), N) : N;
+        const int Mb = q.lens_m ? min(max(q.lens_m[p], 1), M) : M;
+        const bool last_lane = (i == Nb - 1);
+        const float scale = q.scale;
+        float2* rowbuf = reinterpret_cast<float2*>(q.rowbuf) + (size_t)p * M;
+        float* dh = dts + warp * 2 * 64 * 32;   // [64][32] cost hi, slot (col & 63), lane
+        float* dl = dh + 64 * 32;               // [64][32] cost lo
+        const float4 xi = xinfo[(size_t)p * Npad + i];
+        const int ex = __float_as_int(xi.z);
+        const float4* yip = yinfo + (size_t)p * Mpad;
+        float4* yiw = yis + warp * 2 * 32;
+        const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
+        if (active) {
+            cp_async16x(yiw + lane, yip + lane);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
+
+        if (active) {
+            float4* lpp = reinterpret_cast<float4*>(q.VH) + skew_index(N, M, p, rb, 0, lane);
+            Slot* ring_out = ring + 2 * warp * kRing;
+            const Slot* ring_in = ring + 2 * (warp - 1) * kRing;
+            Slot* edge_out = q.edge_f + 2 * ((size_t)p * q.S + strip) * M;
+            const Slot* edge_in = q.edge_f + 2 * ((size_t)p * q.S + strip - 1) * M;
+            const bool chan_lane = has_bot && lane == 31 && !(q.skip_publish && strip == 0 && bot_global);
+            Slot* chan_out = bot_global ? edge_out : ring_out;
+            const int chan_mask = bot_global ? 0x7fffffff : (kRing - 1);
+            Slot nxt[2];
+            nxt[0].v = nxt[1].v = 0.f;
+            nxt[0].tag = nxt[1].tag = 0u;
+            if (top_global && lane < kGroup && lane < M) {
+                nxt[0] = slot_load(edge_in + 2 * lane);
+                nxt[1] = slot_load(edge_in + 2 * lane + 1);
+            }
+
+            dd h_prev = zero, v_prev = zero;
+            bool tc_ok = true;
+            int cons_seen = 0;
+            const int nG = T / kGroup;
+            for (int g = 0; g < nG; ++g) {
+                const int s0 = g * kGroup;
+                if ((s0 & 31) == 0 && (s0 >> 5) < nT) {
+                    // period c = s0/32 reads columns of tiles c-1 and c: bring tile c in
+                    const int c = s0 >> 5, t = c % kXRT;
+                    tc::wait_ok(tc_ok, tc::smem_u32(&s_tfull[t]), (uint32_t)((c / kXRT) & 1), status);
+                    if (!__all_sync(kFull, tc_ok)) break;
+                    tc::fence_after_sync();
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                    __syncwarp();
+                    const float4 yv = yiw[(c & 1) * 32 + lane];
+                    if (c + 1 < nT) {   // its buffer was last read in period c - 1
+                        cp_async16x(yiw + ((c + 1) & 1) * 32 + lane, yip + 32 * (c + 1) + lane);
+                        asm volatile("cp.async.commit_group;" ::: "memory");
+                    }
+                    const uint32_t tt0 = tq + (uint32_t)(t * kXSlotCols);
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {   // 8 columns at a time: NS x 8 level values in registers
+                        uint32_t S[NS][8];   // all levels of 8 columns in flight, one wait
+#pragma unroll
+                        for (int l = 0; l < NS; ++l) tc::tmem_ld8_nowait(tt0 + l * 32 + 8 * q8, S[l]);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int col = 8 * q8 + u;
+                            const float nyh = __shfl_sync(kFull, yv.x, col), nyl = __shfl_sync(kFull, yv.y, col);
+                            const int ey = __shfl_sync(kFull, __float_as_int(yv.z), col);
+                            float Su[NS];
+#pragma unroll
+                            for (int l = 0; l < NS; ++l) Su[l] = __uint_as_float(S[l][u]);
+                            const dd xy = levels_dd<NS>(Su, ex + ey + 2 - 2 * X::DB);
+                            dd cst = sub(add(mk(xi.x, xi.y), mk(nyh, nyl)), mk(2.f * xy.hi, 2.f * xy.lo));
+                            if (cst.hi < 0.f) cst = zero;
+                            const int slot = ((32 * c + col) & 63) * 32 + lane;
+                            dh[slot] = cst.hi;
+                            dl[slot] = cst.lo;
+                        }
+                    }
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&s_tfree[t]));
+                    __syncwarp();
+                }
+
+                // Upper-neighbour h for lane 0: lane q holds column s0 + q as a (hi, lo) slot pair.
+                dd topv = zero;
+                bool ok = true;
+                if (has_top && s0 < M) {
+                    const int col = s0 + lane;
+                    const unsigned want = (lane < kGroup && col < M) ? (unsigned)(col + 1) : 0u;
+                    Slot cur[2];
+                    if (top_global) {
+                        cur[0] = nxt[0];
+                        cur[1] = nxt[1];
+                        ok = validate(cur, edge_in + 2 * col, want, q);
+                        const int ncol = col + kGroup;
+                        if (ok && lane < kGroup && ncol < M) {
+                            nxt[0] = slot_load(edge_in + 2 * ncol);
+                            nxt[1] = slot_load(edge_in + 2 * ncol + 1);
+                        }
+                    } else {
+                        const Slot* src = ring_in + 2 * (col & (kRing - 1));
+                        cur[0].v = cur[1].v = 0.f;
+                        cur[0].tag = cur[1].tag = 0u;
+                        if (want) { cur[0] = slot_load(src); cur[1] = slot_load(src + 1); }
+                        ok = validate(cur, src, want, q);
+                    }
+                    topv = mk(cur[0].v, cur[1].v);
+                }
+                if (ok && has_bot && !bot_global) {
+                    const int need = s0 + kGroup - 31 - kRing;
+                    if (need > cons_seen) ok = wait_smem(&cons[warp], need, q, cons_seen);
+                }
+                if (!ok) break;
+
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u) {
+                    const int s = s0 + u;
+                    const int j = s - lane;
+                    const float hs_hi = __shfl_up_sync(kFull, h_prev.hi, 1);
+                    const float hs_lo = __shfl_up_sync(kFull, h_prev.lo, 1);
+                    const float tv_hi = __shfl_sync(kFull, topv.hi, u);
+                    const float tv_lo = __shfl_sync(kFull, topv.lo, u);
+                    const dd hu = (lane == 0) ? mk(tv_hi, tv_lo) : mk(hs_hi, hs_lo);
+                    const dd vl = v_prev;
+                    const int slot = (j & 63) * 32 + lane;
+                    const dd d = scale_dd(mk(dh[slot], dl[slot]), scale);
+                    const bool col0 = (j == 0);
+                    dd h, v;
+                    float4 lp;
+                    xcell(d, vl, hu, col0, row0_lane, h, v, lp);
+                    c0 = col0 ? d : c0;
+                    lpp[(long long)s * 32] = lp;
+                    const bool valid = (unsigned)j < (unsigned)M;
+                    if (chan_lane && valid) {
+                        Slot* dst = chan_out + 2 * (j & chan_mask);
+                        slot_store(dst, h.hi, (unsigned)(j + 1));
+                        slot_store(dst + 1, h.lo, (unsigned)(j + 1));
+                    }
+                    if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = make_float2(h.hi, h.lo);
+                    h_prev = h;
+                    v_prev = v;
+                }
+                if (has_top && !top_global && lane == 0) cons[warp - 1] = min(s0 + kGroup, M);
+            }
+            asm volatile("cp.async.wait_all;" ::: "memory");  // none in flight past an early exit
+        }
+    }
+
+    // Loss: R[N,M] = sum_i d(i,0) + sum_{j>=1} h(N-1, j), scaled units, in fp64.
+    const int Nb = q.lens_n ? min(max(q.lens_n[p], 1), N) : N;
+    const int Mb = q.lens_m ? min(max(q.lens_m[p], 1), M) : M;
+    double part = (active && warp < W && rs0 + 32 * warp + lane < Nb) ? (double)c0.hi + (double)c0.lo : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
+    if (lane == 0) s_red[warp] = part;
+    __threadfence();
+    __syncthreads();
+    float2* rowbuf = reinterpret_cast<float2*>(q.rowbuf) + (size_t)p * M;
+    if (threadIdx.x == 0) {
+        double cs = 0.0;
+        for (int w = 0; w < W; ++w) cs += s_red[w];
+        q.colsum[(size_t)p * q.NB + strip] = cs;
+        __threadfence();
+        s_last = (atomicAdd(&q.done[p], 1) == q.S - 1);
+    }
+    __syncthreads();
+    if (s_last) {  // the last strip of problem p to finish assembles its loss
+        __threadfence();
+        double acc = 0.0;
+        for (int j = 1 + (int)threadIdx.x; j < Mb; j += blockDim.x) {
+            const float2 hv = __ldcg(rowbuf + j);
+            acc += (double)hv.x + (double)hv.y;
+        }
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+        if (lane == 0) s_red[warp] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double tot = 0.0;
+            for (int w = 0; w <= W; ++w) tot += s_red[w];
+            for (int k = 0; k < q.S; ++k) tot += __ldcg(&q.colsum[(size_t)p * q.NB + k]);
+            q.loss[p] = (float)(tot * (double)q.unscale);
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+size_t oimg_bytes(int P, int L, int D)
+{
+    const int KB = (D + kTcKFeat - 1) / kTcKFeat;
+    return (size_t)P * KB * kXtcSlices * simg_pad(L) * 128;
+}
+
+size_t oinfo_bytes(int P, int L) { return (size_t)P * simg_pad(L) * sizeof(float4); }
+
+cudaError_t launch_oimg(const Problems& pr, int P, int N, int M, int D, void* ximg, void* yimg, void* xinfo,
+                        void* yinfo, cudaStream_t st)
+{
+    const int KB = (D + kTcKFeat - 1) / kTcKFeat;
+    const int Lmax = simg_pad(N > M ? N : M);
+    const size_t smem = sizeof(float) * 32 * (kTcKFeat * KB + 1);
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<dim3(Lmax / 32, P, 2), 256, smem, st>>>(pr, N, M, D, KB, static_cast<unsigned char*>(ximg),
+                                                       static_cast<unsigned char*>(yimg), static_cast<float4*>(xinfo),
+                                                       static_cast<float4*>(yinfo));
+        return cudaGetLastError();
+    };
+    return go(oimg_kernel<kXtcSlices>);
+}
+
+cudaError_t launch_forward_xtc(WaveParams q, const void* ximg, const void* yimg, const void* xinfo,
+                               const void* yinfo, cudaStream_t st)
+{
+    if (q.W != kXDpWarps || q.D > kMaxXtcD) return cudaErrorInvalidValue;
+    const int grid = q.P * q.S;
+    q.smem_fixed = (int)(((size_t)kXDpWarps * kRing * 2 * sizeof(Slot) + (size_t)kXDpWarps * sizeof(int) + 15) &
+                         ~(size_t)15);
+    const int KB = (q.D + kTcKFeat - 1) / kTcKFeat;
+    auto go = [&](auto kern, int NS) -> cudaError_t {
+        const size_t need = q.smem_fixed + 1024 + xtc_region(NS, KB) + (size_t)kXDpWarps * 2 * 64 * 32 * sizeof(float) +
+                            (size_t)kXDpWarps * 2 * 32 * sizeof(float4);
+        const size_t smem = max(need, wave_smem_floor());   // one CTA per SM: the whole tensor memory
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, (kXDpWarps + 1) * 32, smem, st>>>(q, static_cast<const unsigned char*>(ximg),
+                                                       static_cast<const unsigned char*>(yimg),
+                                                       static_cast<const float4*>(xinfo),
+                                                       static_cast<const float4*>(yinfo));
+        return cudaGetLastError();
+    };
+    return go(fwdx_tc_kernel<kXtcSlices>, kXtcSlices);
 }
 
 size_t wavex_smem_fused_per_warp(int D)

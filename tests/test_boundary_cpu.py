@@ -44,9 +44,9 @@ def test_workspace_sizes(lib):
     f = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.FUSED)
     # skewed slots: 16 blocks x (512+31 rounded up to a multiple of 16) x 32 per problem
     slots = 32 * 16 * 544 * 32
-    # tensor-core cost operands in both modes: x and y images (hi + lo tf32, 2
-    # K-blocks of 32 features, rows padded to 128) and row norms
-    simg = 2 * (32 * 2 * 2 * 512 * 128) + 2 * (32 * 512 * 4)
+    # tensor-core cost operands in both modes: x and y images (three bf16 parts, one
+    # K-block of 64 features, rows padded to 128) and row norms (hi, lo)
+    simg = 2 * (32 * 1 * 3 * 512 * 128) + 2 * (32 * 512 * 4)
     assert f >= slots * (8 + 4) + simg   # (vl,hu) pairs + alignment matrix
     assert u >= f + slots * 4            # + the stored cost tensor
     assert u - f < slots * 4 + 4096
@@ -61,11 +61,13 @@ def test_workspace_sizes(lib):
         assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, *bad, L.UNFUSED) == 0
     assert L.sdtw_workspace_bytes(7, 4, 4, 4, 4, L.UNFUSED) == 0
     assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, 4, 4, 4, 4, 4) == 0
-    # extended precision: 16-byte log-probabilities instead of 8-byte pairs (+8 more
-    # unfused); its costs and gradients run on the FP32 pipe, so no operand images
+    # extended precision: 16-byte log-probabilities instead of 8-byte pairs; unfused
+    # stores the double-float cost (8 bytes); fused has the exact cost tiles' digit
+    # images (five bf16 slices) and row info instead
     fx = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.FUSED | L.EXTENDED)
     ux = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.UNFUSED | L.EXTENDED)
-    assert fx - (f - bimg - simg) >= slots * 8 and ux - fx >= slots * 8
+    oimg = 2 * (32 * 1 * 5 * 512 * 128) + 2 * (32 * 512 * 16)
+    assert fx - (f - bimg - simg) >= slots * 8 + oimg and ux - (fx - oimg) >= slots * 8
 
 
 def _fwd(lib, x=0x1000, y=0x2000, B=2, N=3, M=4, D=2, gamma=1.0, mode=0, loss=0x3000, ws=0x100000,
@@ -128,8 +130,7 @@ def test_auto_precision_rule():
     assert L.auto_precision(1.0, 64, 64, 5, 4) == L.EXTENDED
     assert L.auto_precision(1.0, 1024, 1024, 8, 64) == 0         # the barycenter workload (mean over K=64)
     assert L.auto_precision(1.0, 128, 128, 20, None) == 0        # no batch rule without B
-    assert L.auto_precision(1.0, 256, 256, 256, 32) == 0         # the width sweep's batch
-    assert L.auto_precision(1.0, 256, 256, 257, 32) == L.EXTENDED
+    assert L.auto_precision(1.0, 256, 256, 128, 32) == L.EXTENDED  # wide features: double-float state
     assert L.auto_precision(1.0, 8192, 8192, 128, 8) == L.EXTENDED  # the long workload
 
 
@@ -223,21 +224,20 @@ def test_checkpoint_workspace_and_validation(lib):
     ck = L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, D, L.FUSED | L.CHECKPOINT)
     T = 544
     band = B * 4 * T * 32                       # cells of one 128-row band of every problem
-    assert ck > band * 12                       # (v_left, h_up) pairs and E of one band
-    assert full - ck >= (B * 16 * T * 32 - band) * 12   # the other bands' state and E are gone
-    assert ck < full / 2
+    assert ck > 2 * band * 12                   # (v_left, h_up) pairs and E of two bands
+    assert full - ck >= (B * 16 * T * 32 - 2 * band) * 12   # the other bands' state and E are gone
+    assert ck < 0.6 * full
     # only the fp32 tensor-core fused path checkpoints
     assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, D, L.UNFUSED | L.CHECKPOINT) == 0
     assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, D, L.FUSED | L.EXTENDED | L.CHECKPOINT) == 0
-    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, 256, L.FUSED | L.CHECKPOINT) > 0   # tensor-core widths
-    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, 257, L.FUSED | L.CHECKPOINT) == 0
+    assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, B, N, M, 65, L.FUSED | L.CHECKPOINT) == 0   # beyond the tensor-core width
     assert L.sdtw_workspace_bytes(L.OP_NORMALIZED, B, N, N, D, L.FUSED | L.CHECKPOINT) == 0
     assert L.sdtw_workspace_bytes(L.OP_FWD_BWD, 2, 3, 4, 2, 8) == 0
     # host-side validation, before any CUDA call
     assert _fwd(lib, mode=L.FUSED | L.CHECKPOINT, ws_bytes=16) == 5     # accepted flag, small workspace
     assert _fwd(lib, mode=L.UNFUSED | L.CHECKPOINT) == 1
     assert _fwd(lib, mode=L.FUSED | L.EXTENDED | L.CHECKPOINT) == 1
-    assert _fwd(lib, mode=L.FUSED | L.CHECKPOINT, D=257) == 1
+    assert _fwd(lib, mode=L.FUSED | L.CHECKPOINT, D=65) == 1
     vp = ctypes.c_void_p
     assert lib.sdtw_normalized(vp(0x1000), vp(0x2000), 2, 3, 2, 1.0, L.FUSED | L.CHECKPOINT, vp(0x3000), None,
                                None, None, vp(0x100000), 1 << 40, None) == 1
