@@ -51,7 +51,8 @@ FALLBACK_SM_MHZ = 2070.0
 # from one ncu capture (`dram__bytes_read.sum + dram__bytes_write.sum`), with the
 # SHA-256 of the sources that build the kernel at the time of the capture; the
 # bench reports it only while those sources are unchanged (else null).
-BWD_TRAFFIC = {"sha256": None, "bytes": None}
+# profiles/bwd_kernel_headline.md: 71,443,200 read + 7,559,168 written.
+BWD_TRAFFIC = {"sha256": "1ad3698e0c995b3b44078b1c473bdbcfe53a463f3326a800f57fa3d89bbaf890", "bytes": 79002368}
 BWD_SOURCES = ("wavefront.cu", "common.cuh", "channel.cuh", "kernels.h")
 # kernels per step: unfused forward (operand images, cost tensor, wavefront) + backward
 # (wavefront, gradient operand images, two gradient contractions), fused forward
@@ -645,14 +646,16 @@ def run_ours(args):
 
 
 def run_profile(args):
-    """K untimed steps of the workload (both modes), for wrapping in ncu."""
+    """K untimed steps of the workload (unfused, then fused), for wrapping in ncu; in
+    the fp32 modes of the timed step or in the extended ones."""
     import torch
     from differentiable_series_alignment_gb300 import _lib as L, synth
     L.load()
     x_np, y_np = synth.iid_normal_pair(B, N, M, D, 1)
     x, y = torch.from_numpy(x_np).cuda(), torch.from_numpy(y_np).cuda()
     g = torch.full((B,), 1.0 / B, device="cuda")
-    for mode in (L.UNFUSED, L.FUSED):
+    prec = L.EXTENDED if args.profile_precision == "extended" else 0
+    for mode in (L.UNFUSED | prec, L.FUSED | prec):
         ws = L.workspace(L.OP_FWD_BWD, B, N, M, D, mode)
         loss, gx, gy = torch.empty(B, device="cuda"), torch.empty_like(x), torch.empty_like(y)
         for _ in range(args.profile):
@@ -670,6 +673,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--profile", type=int, default=0, help="run this many untimed steps (for ncu) and exit")
+    ap.add_argument("--profile-precision", choices=("fp32", "extended"), default="fp32",
+                    help="precision of the --profile steps")
     ap.add_argument("--no-per-config", dest="per_config", action="store_false",
                     help="skip the throughput / peak-memory / roofline figures of the other workloads")
     args = ap.parse_args()

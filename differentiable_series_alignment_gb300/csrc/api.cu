@@ -27,7 +27,7 @@ int g_skip_publish = 0;
 // library's own choices).
 struct DebugOptions {
     int warps_fwd, warps_bwd;   // warps per wavefront CTA (> 0: forced)
-    int dist_simt, fused_simt;  // difference-form cost kernels in the fp32 modes
+    int dist_simt, fused_simt;  // difference-form cost kernels (unfused / fused, both precisions)
 };
 DebugOptions g_dbg{};
 
@@ -40,7 +40,7 @@ struct Layout {
     size_t ximg, yimg, xnorm, ynorm;  // tensor-core cost operands (tc_cost, or xtc: digit images and row info)
     size_t band_slots;                // checkpointed mode: skewed slots of one band of every problem
     bool tc_cost;
-    bool xtc;    // extended fused mode with the exact tensor-core cost tiles (D <= kMaxXtcD)
+    bool xtc;    // extended mode with exact tensor-core costs (fused D <= kMaxXtcD, unfused D <= kMaxXtcUD)
     bool ckpt;   // checkpointed fused mode: VH / E hold two bands, the [X | 1] image one
     int P, N, M, D, NB;
 };
@@ -103,8 +103,9 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     // operand images and norms of the tensor-core costs (fp32 modes, D <= 256): the
     // unfused cost tensor and the fused forward's cost tiles
     L->tc_cost = !ext && D <= kTcKFeat * kMaxTcKBlocks && xy;
-    // the extended fused forward's exact cost tiles: fixed-point digit images and row info
-    L->xtc = ext && fused && D <= kMaxXtcD && xy;
+    // the extended modes' exact tensor-core costs (the fused forward's cost tiles, the
+    // unfused cost tensor): fixed-point digit images and row info
+    L->xtc = ext && xy && D <= (fused ? kMaxXtcD : kMaxXtcUD);
     L->ximg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, N, D));
     if (L->xtc) o = align_up(o + oimg_bytes(P, N, D));
     L->yimg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, M, D));
@@ -235,8 +236,8 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
     q.lens_n = lens_n;
     q.lens_m = lens_m;
     const bool tc = L.tc_cost && !(fused ? g_dbg.fused_simt : g_dbg.dist_simt);
-    const bool xtc = L.xtc && !g_dbg.fused_simt;
-    if ((fused && tc) || xtc) {  // the tensor-core fused forwards take 128-row strips (4 warps)
+    const bool xtc = L.xtc && !cost && !(fused ? g_dbg.fused_simt : g_dbg.dist_simt);
+    if (fused && (tc || xtc)) {  // the tensor-core fused forwards take 128-row strips (4 warps)
         q.W = 4;
         q.S = (L.NB + 3) / 4;
     }
@@ -245,13 +246,22 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
     if (q.S > 1)  // strip boundary slots start untagged
         SDTW_CUDA(cudaMemsetAsync(q.edge_f, 0, (ext ? 2 : 1) * sizeof(Slot) * (size_t)L.P * q.S * L.M, st));
     if (ext) {
-        if (cost) SDTW_CUDA(launch_skew_cost(cost, L.P, L.N, L.M, true, at<float>(ws, L.dsk), st));
-        else if (!fused) SDTW_CUDA(launch_dist_skewed_x(pr, L.P, L.N, L.M, L.D, at<float2>(ws, L.dsk), st));
-        q.loss = loss_out;
-        q.skip_publish = debug_take_skip_publish();
-        if (xtc) {
+        if (xtc)
             SDTW_CUDA(launch_oimg(pr, L.P, L.N, L.M, L.D, at<char>(ws, L.ximg), at<char>(ws, L.yimg),
                                   at<char>(ws, L.xnorm), at<char>(ws, L.ynorm), st));
+        if (cost) {
+            SDTW_CUDA(launch_skew_cost(cost, L.P, L.N, L.M, true, at<float>(ws, L.dsk), st));
+        } else if (!fused) {
+            if (xtc)
+                SDTW_CUDA(launch_dist_xtc(L.P, L.N, L.M, L.D, at<char>(ws, L.ximg), at<char>(ws, L.yimg),
+                                          at<char>(ws, L.xnorm), at<char>(ws, L.ynorm), at<float2>(ws, L.dsk),
+                                          at<int>(ws, L.status), st));
+            else
+                SDTW_CUDA(launch_dist_skewed_x(pr, L.P, L.N, L.M, L.D, at<float2>(ws, L.dsk), st));
+        }
+        q.loss = loss_out;
+        q.skip_publish = debug_take_skip_publish();
+        if (fused && xtc) {
             SDTW_CUDA(launch_forward_xtc(q, at<char>(ws, L.ximg), at<char>(ws, L.yimg), at<char>(ws, L.xnorm),
                                          at<char>(ws, L.ynorm), st));
         } else {

@@ -41,7 +41,6 @@ __device__ __forceinline__ dd sub_f(dd a, float f) {
     e += a.lo;
     return fast2(s, e);
 }
-__device__ __forceinline__ float to_f(dd a) { return a.hi + a.lo; }
 
 // Double-float squared distance accumulator: exact differences and squares.
 struct DistDD {
@@ -78,32 +77,29 @@ __device__ __forceinline__ dd scale_dd(dd d, float k) {
 // exact for any choice of lo among the three, so comparing the hi parts suffices.
 // The offsets dk only feed the fp32 log and the fp32 log-probabilities: formed as
 // (a.hi - lo.hi) + (a.lo - lo.lo), the first difference is exact whenever it is
-// small (Sterbenz), and a large one leaves a negligible term.
+// small (Sterbenz), and a large one leaves a negligible term. The results are
+// formed as h = (d + lo - v_left) - L and v = (d + lo - h_up) - L: the bracketed
+// double-float sums do not depend on the log, so they run beside the exp2/log2
+// chain and only one double-float step follows it. The borders are selects.
 __device__ __forceinline__ void xcell(dd d, dd vl, dd hu, bool col0, bool row0_lane, dd& h, dd& v, float4& lp)
 {
-    const dd zero = mk(0.f, 0.f), nbig = mk(-kBig, 0.f);
+    const dd nbig = mk(-kBig, 0.f);
     const dd m = (hu.hi < vl.hi) ? hu : vl;
-    const dd lo = (m.hi < 0.f) ? m : zero;
+    const dd lo = (m.hi < 0.f) ? m : mk(0.f, 0.f);
     const float d0 = (0.f - lo.hi) - lo.lo;
     const float dl = (vl.hi - lo.hi) + (vl.lo - lo.lo);
     const float du = (hu.hi - lo.hi) + (hu.lo - lo.lo);
+    const dd dlo = add(d, lo);
+    const dd ph = sub(dlo, vl), pv = sub(dlo, hu);
     const float L = log2f((exp2_neg(-d0) + exp2_neg(-dl)) + exp2_neg(-du));
-    const dd tt = sub_f(add(d, lo), L);
-    h = sub(tt, vl);
-    v = sub(tt, hu);
-    float lpd = -d0 - L;
-    float lpl = -dl - L;
-    float lpu = -du - L;
-    if (col0) {        // first column: only the upper predecessor (or none at (0,0))
-        h = nbig;
-        v = row0_lane ? nbig : d;
-        lpd = -kBig; lpl = -kBig; lpu = row0_lane ? -kBig : 0.f;
-    } else if (row0_lane) {  // first row: only the left predecessor
-        h = d;
-        v = nbig;
-        lpd = -kBig; lpl = 0.f; lpu = -kBig;
-    }
-    lp = make_float4(lpd, lpl, lpu, 0.f);
+    const dd hh = sub_f(ph, L), vv = sub_f(pv, L);
+    // first column: only the upper predecessor (none at (0,0)); first row: only the left
+    h = col0 ? nbig : (row0_lane ? d : hh);
+    v = row0_lane ? nbig : (col0 ? d : vv);
+    lp.x = (col0 || row0_lane) ? -kBig : -d0 - L;
+    lp.y = col0 ? -kBig : (row0_lane ? 0.f : -dl - L);
+    lp.z = row0_lane ? -kBig : (col0 ? 0.f : -du - L);
+    lp.w = 0.f;
 }
 
 }  // namespace
@@ -387,8 +383,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
 // and the level sums S_sigma for sigma <= NS-1 are bf16 MMAs accumulated in fp32
 // in tensor memory: every partial sum is an integer of magnitude below
 // NS D 2^(2b-2) < 2^24, so fp32 holds it exactly (checked on the GB300 up to
-// 2^23.98 against int64 sums) and the level sums are exact. The digit set:
-// NS = 5 digits of b = 8 bits (F = 40) for D <= 128 (5 * 128 * 2^14 < 2^24). The
+// 2^23.98 against int64 sums) and the level sums are exact. Two digit sets:
+// NS = 5 digits of b = 8 bits (F = 40) for D <= 128 (5 * 128 * 2^14 < 2^24), and
+// NS = 6 digits of b = 7 bits (F = 42) up to D = 400 (6 * 400 * 2^12 < 2^24). The
 // MMA of x digit l multiplies the stacked y digits [b_0 ; ... ; b_(NS-1-l)] into
 // tensor-memory columns starting at level l, so product (l, m) lands in level
 // l + m: NS MMAs (N = 32 NS, ..., 32 columns) per 16-wide K step. Error bound of
@@ -405,18 +402,12 @@ constexpr int kXIssuer = kXDpWarps;            // warp 4: bulk copies and MMAs
 constexpr uint32_t kXAPart = 128 * 128;        // one digit of one K-block of 128 x rows
 constexpr uint32_t kXBPart = 32 * 128;         // one digit of one K-block of 32 y rows
 
-// The digit set: NS = 5 digits of DB = 8 bits. RT cost tiles of NS * 32 columns
-// share the 512 tensor-memory columns, and RT >= 3 is required: a DP warp may start
-// its group of 16 steps at s0 only after the warp above has finished step s0 + 46,
-// so warp 3 releases tile c - RT (at step 32 (c - RT)) only once warp 0 has reached
-// step 32 (c - RT) + 94; with RT = 3 that is step 32 c - 2, before warp 0 needs tile
-// c, while with RT = 2 warp 0 would already wait for tile c and nobody progresses.
-// Six digits (192 columns a tile) leave room for two tiles only, which is why the
-// exact tiles stop at D = 128.
+// The digit sets: NS = 5 digits of DB = 8 bits (D <= 128) or NS = 6 digits of
+// DB = 7 bits (D <= 400). SlotCols: the tensor-memory columns of one cost tile (its
+// NS level sums for 32 y columns).
 template <int NS> struct XDigits {
-    static_assert(NS == 5, "five 8-bit digits: three cost tiles fit in tensor memory");
-    static constexpr int DB = 8;                          // bits per digit
-    static constexpr int RT = 3;                          // cost tiles in tensor memory (NS * 32 columns each)
+    static_assert(NS == 5 || NS == 6, "five 8-bit or six 7-bit digits");
+    static constexpr int DB = NS == 5 ? 8 : 7;            // bits per digit
     static constexpr int SlotCols = NS * 32;
     static constexpr uint32_t A = NS * kXAPart;           // all digits of one K-block of the x rows
     static constexpr uint32_t B = NS * kXBPart;           // [b_0 ; ... ; b_(NS-1)] of one K-block of a y tile
@@ -577,7 +568,15 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
                    const float4* __restrict__ xinfo, const float4* __restrict__ yinfo)
 {
     using X = XDigits<NS>;
-    constexpr int kXRT = X::RT, kXSlotCols = X::SlotCols, kXSlices = NS;
+    // RT cost tiles share the 512 tensor-memory columns, and RT >= 3 is required: a
+    // DP warp may start its group of 16 steps at s0 only after the warp above has
+    // finished step s0 + 46, so warp 3 releases tile c - RT (at its step 32 (c - RT))
+    // only once warp 0 has reached step 32 (c - RT) + 94. With RT = 3 that is step
+    // 32 c - 2, before warp 0 needs tile c; with RT = 2 warp 0 would already be
+    // waiting for tile c and no warp could progress. Six digits (192 columns a tile)
+    // leave room for two tiles, so this kernel takes five digits (D <= 128).
+    static_assert(NS == 5, "three tiles of five levels fill the tensor memory");
+    constexpr int kXRT = 3, kXSlotCols = X::SlotCols, kXSlices = NS;
     constexpr uint32_t kXA = X::A, kXStage = X::Stage;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     constexpr int W = kXDpWarps;
@@ -932,12 +931,221 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
     }
 }
 
+// The extended unfused cost tensor from the exact level sums. One CTA per 128 x
+// rows and problem walks the y columns in tiles of 32: warp 8 (lane 0) copies the
+// digits (x resident for one K-block, else both streamed per K-block through one
+// stage) and issues each tile's level MMAs into one of two tensor-memory slots;
+// epilogue warps 0-7 drain the other. Warp w reads TMEM lane quarter w mod 4 and
+// the 16-column half w / 4 of the tile, combines the NS level sums of each column
+// with the exponents and the double-float norms into C = |x|^2 + |y|^2 - 2 x . y
+// (clamped at 0) and writes the skewed layout through a per-warp staging tile.
+// No DP runs behind the tiles, so two slots keep the MMAs ahead of the epilogue
+// and six digits (two slots of 192 columns) fit as well. Hand-offs (bounded
+// mbarrier waits):
+//   s_a         x digits resident       s_bfull[e] / s_bempty[e]  y ring (one K-block)
+//   s_sfull     stage landed            s_sempty   its MMAs are done (K-blocks streamed)
+//   s_tfull[t]  levels in TMEM slot t   s_tfree[t] the 8 epilogue warps read slot t
+constexpr int kXdWarps = 8;
+constexpr int kXdStg = 47 * 32;   // per-warp staging: skewed rows of a 16-column chunk (float2)
+
+template <int NS>
+__global__ void __launch_bounds__((kXdWarps + 1) * 32, 1)
+    distx_tc_kernel(int N, int M, int D, const unsigned char* __restrict__ ximg, const unsigned char* __restrict__ yimg,
+                    const float4* __restrict__ xinfo, const float4* __restrict__ yinfo, float2* __restrict__ Dsk,
+                    int* status)
+{
+    using X = XDigits<NS>;
+    constexpr int kSlot = X::SlotCols;
+    constexpr uint32_t kA = X::A, kB = X::B;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ uint64_t s_a, s_sfull, s_sempty, s_fin, s_bfull[2], s_bempty[2], s_tfull[2], s_tfree[2];
+    __shared__ uint32_t s_tmem;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int p = blockIdx.y, r0 = blockIdx.x * 128;
+    const int KB = (D + kTcKFeat - 1) / kTcKFeat;
+    const bool resident = KB == 1;
+    const int Npad = simg_pad(N), Mpad = simg_pad(M);
+    const int nT = (M + 31) / 32;
+    unsigned char* stage = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    float2* stg = reinterpret_cast<float2*>(stage + xtc_region(NS, KB)) + warp * kXdStg;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(tc::smem_u32(&s_a), 1);
+        tc::mbar_init(tc::smem_u32(&s_sfull), 1);
+        tc::mbar_init(tc::smem_u32(&s_sempty), 1);
+        tc::mbar_init(tc::smem_u32(&s_fin), 1);
+        for (int e = 0; e < 2; ++e) {
+            tc::mbar_init(tc::smem_u32(&s_bfull[e]), 1);
+            tc::mbar_init(tc::smem_u32(&s_bempty[e]), 1);
+            tc::mbar_init(tc::smem_u32(&s_tfull[e]), 1);
+            tc::mbar_init(tc::smem_u32(&s_tfree[e]), kXdWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+    bool ok = true;
+
+    // the level MMAs of one 16-wide K step: x digit l against the stacked y digits
+    // [b_0 ; ... ; b_(NS-1-l)], into the level columns l .. NS-1
+    auto level_mmas = [&](uint32_t d0, uint32_t a, uint32_t b, uint32_t ko, bool acc0) {
+#pragma unroll
+        for (int l = 0; l < NS; ++l)
+            tc::mma_bf16(d0 + (uint32_t)(l * 32), tc::sdesc(a + l * kXAPart + ko), tc::sdesc(b + ko),
+                         tc::idesc_bf16(128, (NS - l) * 32), (acc0 || l > 0) ? 1u : 0u);
+    };
+
+    if (warp == kXdWarps) {
+        if (lane == 0) {
+            if (resident) {
+                int y_last[2] = {-1, -1};
+                const uint32_t abar = tc::smem_u32(&s_a);
+                tc::mbar_expect_tx(abar, kA);
+                for (int l = 0; l < NS; ++l)
+                    tc::bulk_g2s(tc::smem_u32(stage + l * kXAPart), ximg + oimg_offset(p, 1, 0, NS, l, Npad, r0),
+                                 kXAPart, abar);
+                auto issue_y = [&](int c) {
+                    const int e = c & 1;
+                    const uint32_t bar = tc::smem_u32(&s_bfull[e]);
+                    tc::mbar_expect_tx(bar, kB);
+                    for (int l = 0; l < NS; ++l)
+                        tc::bulk_g2s(tc::smem_u32(stage + kA + e * kB + l * kXBPart),
+                                     yimg + oimg_offset(p, 1, 0, NS, l, Mpad, 32 * c), kXBPart, bar);
+                    y_last[e] = c;
+                };
+                for (int c = 0; c < 2 && c < nT; ++c) issue_y(c);
+                tc::wait_ok(ok, abar, 0u, status);
+                for (int c = 0; c < nT && ok; ++c) {
+                    const int e = c & 1;
+                    if (c >= 2) tc::wait_ok(ok, tc::smem_u32(&s_tfree[e]), (uint32_t)(((c - 2) >> 1) & 1), status);
+                    tc::wait_ok(ok, tc::smem_u32(&s_bfull[e]), (uint32_t)((c >> 1) & 1), status);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const uint32_t d0 = tmem + (uint32_t)(e * kSlot);
+                    const uint32_t a = tc::smem_u32(stage), b = a + kA + e * kB;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) level_mmas(d0, a, b, ks * 32, ks > 0);
+                    tc::mma_commit(tc::smem_u32(&s_bempty[e]));
+                    tc::mma_commit(tc::smem_u32(&s_tfull[e]));
+                    if (c + 2 < nT) {   // entry e takes tile c + 2 once MMA(c) has read it
+                        tc::wait_ok(ok, tc::smem_u32(&s_bempty[e]), (uint32_t)((c >> 1) & 1), status);
+                        if (!ok) break;
+                        issue_y(c + 2);
+                    }
+                }
+                tc::mma_commit(tc::smem_u32(&s_fin));
+                bool fin = true;
+                tc::wait_ok(fin, tc::smem_u32(&s_fin), 0u, status);
+                for (int e = 0; e < 2; ++e)
+                    if (y_last[e] >= 0)
+                        tc::wait_ok(fin, tc::smem_u32(&s_bfull[e]), (uint32_t)((y_last[e] >> 1) & 1), status);
+            } else {
+                // stage g = c * KB + kb: K-block kb of the x rows' and of y tile c's digits
+                const int G = nT * KB;
+                int g_last = -1;
+                for (int g = 0; g < G && ok; ++g) {
+                    const int c = g / KB, kb = g - c * KB, t = c & 1;
+                    if (kb == 0 && c >= 2)
+                        tc::wait_ok(ok, tc::smem_u32(&s_tfree[t]), (uint32_t)(((c - 2) >> 1) & 1), status);
+                    if (g >= 1) tc::wait_ok(ok, tc::smem_u32(&s_sempty), (uint32_t)((g - 1) & 1), status);
+                    if (!ok) break;
+                    const uint32_t bar = tc::smem_u32(&s_sfull);
+                    tc::mbar_expect_tx(bar, kA + kB);
+                    for (int l = 0; l < NS; ++l)
+                        tc::bulk_g2s(tc::smem_u32(stage + l * kXAPart), ximg + oimg_offset(p, KB, kb, NS, l, Npad, r0),
+                                     kXAPart, bar);
+                    for (int l = 0; l < NS; ++l)
+                        tc::bulk_g2s(tc::smem_u32(stage + kA + l * kXBPart),
+                                     yimg + oimg_offset(p, KB, kb, NS, l, Mpad, 32 * c), kXBPart, bar);
+                    g_last = g;
+                    tc::wait_ok(ok, bar, (uint32_t)(g & 1), status);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const uint32_t d0 = tmem + (uint32_t)(t * kSlot);
+                    const uint32_t a = tc::smem_u32(stage), b = a + kA;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) level_mmas(d0, a, b, ks * 32, kb > 0 || ks > 0);
+                    tc::mma_commit(tc::smem_u32(&s_sempty));
+                    if (kb == KB - 1) tc::mma_commit(tc::smem_u32(&s_tfull[t]));
+                }
+                tc::mma_commit(tc::smem_u32(&s_fin));
+                bool fin = true;
+                tc::wait_ok(fin, tc::smem_u32(&s_fin), 0u, status);
+                if (g_last >= 0) tc::wait_ok(fin, tc::smem_u32(&s_sfull), (uint32_t)(g_last & 1), status);
+            }
+        }
+        __syncwarp();
+    } else {
+        const int qd = warp & 3, half = warp >> 2;
+        const int rb = (r0 >> 5) + qd, row = r0 + 32 * qd + lane;
+        const int NB = (N + 31) / 32;
+        const float4 xi = xinfo[(size_t)p * Npad + row];
+        const int ex = __float_as_int(xi.z);
+        const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
+        float2* out = (rb < NB) ? Dsk + skew_index(N, M, p, rb, 0, lane) : nullptr;
+        for (int c = 0; c < nT; ++c) {
+            const int t = c & 1;
+            tc::wait_ok(ok, tc::smem_u32(&s_tfull[t]), (uint32_t)((c >> 1) & 1), status);
+            if (!__all_sync(kFull, ok)) break;
+            tc::fence_after_sync();
+            const int cb = 32 * c + 16 * half;   // first column of this warp's chunk
+            const float4 yv = yinfo[(size_t)p * Mpad + cb + (lane & 15)];
+            const uint32_t tt0 = tq + (uint32_t)(t * kSlot + 16 * half);
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {   // 8 columns at a time: NS x 8 level sums in registers
+                uint32_t S[NS][8];
+#pragma unroll
+                for (int l = 0; l < NS; ++l) tc::tmem_ld8_nowait(tt0 + l * 32 + 8 * h8, S[l]);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int col = 8 * h8 + u;
+                    const float nyh = __shfl_sync(kFull, yv.x, col), nyl = __shfl_sync(kFull, yv.y, col);
+                    const int ey = __shfl_sync(kFull, __float_as_int(yv.z), col);
+                    float Su[NS];
+#pragma unroll
+                    for (int l = 0; l < NS; ++l) Su[l] = __uint_as_float(S[l][u]);
+                    const dd xy = levels_dd<NS>(Su, ex + ey + 2 - 2 * X::DB);
+                    dd cst = sub(add(mk(xi.x, xi.y), mk(nyh, nyl)), mk(2.f * xy.hi, 2.f * xy.lo));
+                    if (cst.hi < 0.f) cst = mk(0.f, 0.f);
+                    stg[(col + lane) * 32 + lane] = make_float2(cst.hi, cst.lo);
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&s_tfree[t]));
+            if (out != nullptr && cb < M) {   // warp-uniform
+                // skewed slot cb + tt holds column cb + tt - lane of this lane's row
+                for (int tt = 0; tt < 47; ++tt) {
+                    const int j = tt - lane;
+                    if (j >= 0 && j < 16 && cb + j < M && row < N) out[(long long)(cb + tt) * 32] = stg[tt * 32 + lane];
+                }
+            }
+            __syncwarp();
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
 }  // namespace
+
+// digits per value of the exact cost tiles for a feature width
+int xtc_slices(int D) { return D <= 128 ? 5 : 6; }
 
 size_t oimg_bytes(int P, int L, int D)
 {
     const int KB = (D + kTcKFeat - 1) / kTcKFeat;
-    return (size_t)P * KB * kXtcSlices * simg_pad(L) * 128;
+    return (size_t)P * KB * xtc_slices(D) * simg_pad(L) * 128;
 }
 
 size_t oinfo_bytes(int P, int L) { return (size_t)P * simg_pad(L) * sizeof(float4); }
@@ -956,7 +1164,7 @@ cudaError_t launch_oimg(const Problems& pr, int P, int N, int M, int D, void* xi
                                                        static_cast<float4*>(yinfo));
         return cudaGetLastError();
     };
-    return go(oimg_kernel<kXtcSlices>);
+    return xtc_slices(D) == 5 ? go(oimg_kernel<5>) : go(oimg_kernel<6>);
 }
 
 cudaError_t launch_forward_xtc(WaveParams q, const void* ximg, const void* yimg, const void* xinfo,
@@ -979,7 +1187,28 @@ cudaError_t launch_forward_xtc(WaveParams q, const void* ximg, const void* yimg,
                                                        static_cast<const float4*>(yinfo));
         return cudaGetLastError();
     };
-    return go(fwdx_tc_kernel<kXtcSlices>, kXtcSlices);
+    return go(fwdx_tc_kernel<5>, 5);
+}
+
+cudaError_t launch_dist_xtc(int P, int N, int M, int D, const void* ximg, const void* yimg, const void* xinfo,
+                            const void* yinfo, float2* Dsk, int* status, cudaStream_t st)
+{
+    if (D < 1 || D > kMaxXtcUD) return cudaErrorInvalidValue;
+    const int KB = (D + kTcKFeat - 1) / kTcKFeat;
+    const int NS = xtc_slices(D);
+    const size_t smem = 1024 + xtc_region(NS, KB) + (size_t)kXdWarps * kXdStg * sizeof(float2);
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    const dim3 grid((N + 127) / 128, P);
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, (kXdWarps + 1) * 32, smem, st>>>(N, M, D, static_cast<const unsigned char*>(ximg),
+                                                      static_cast<const unsigned char*>(yimg),
+                                                      static_cast<const float4*>(xinfo),
+                                                      static_cast<const float4*>(yinfo), Dsk, status);
+        return cudaGetLastError();
+    };
+    return NS == 5 ? go(distx_tc_kernel<5>) : go(distx_tc_kernel<6>);
 }
 
 size_t wavex_smem_fused_per_warp(int D)

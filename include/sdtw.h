@@ -281,8 +281,8 @@ void sdtw_debug_set_wait(double seconds, int skip_publish);
  * wavefront CTA of the forward / backward (and with them the number of strips of
  * a problem, whose boundaries pass through global memory); dist_simt / fused_simt
  * non-zero select the difference-form cost kernels instead of the tensor-core
- * ones in the unfused / fused fp32 modes (with fused_simt the checkpoint flag is
- * SDTW_ERR_ARG). All zeros restore the library's own choices. Process-wide, read
+ * ones in the unfused / fused modes, fp32 and extended (with fused_simt the
+ * checkpoint flag is SDTW_ERR_ARG). All zeros restore the library's own choices. Process-wide, read
  * by the calls that follow; set it while no other host thread calls the library. */
 void sdtw_debug_set_options(int warps_fwd, int warps_bwd, int dist_simt, int fused_simt);
 

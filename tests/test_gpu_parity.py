@@ -166,22 +166,28 @@ def test_extended_precision_shapes(mname, mode, N, M, D):
     check_against_oracle(x, y, 0.7, mode, grad_loss=WEIGHTS_O1, what=f"{N}x{M}x{D} {mname}")
 
 
-# The extended fused forward takes its double-float costs from exact tensor-core
-# tiles (five 8-bit fixed-point digits, integer level sums) up to D = 128; wider
-# rows use the difference form. The difference-form kernel (the debug option)
-# computes the same costs on the FP32 pipe. Both must hold the tolerance at O(1)
-# weights and agree closely. The shapes run the three-tile tensor-memory ring
-# round several times (M up to 333 columns) and over several 128-row strips.
-@pytest.mark.parametrize("N,M,D", [(1, 9, 3), (33, 31, 1), (100, 37, 16), (129, 130, 63), (70, 91, 64),
-                                   (130, 97, 65), (200, 150, 128), (300, 333, 128), (257, 520, 96),
-                                   (129, 70, 129)])
-def test_extended_tensor_core_costs(N, M, D):
+# The extended modes take their double-float costs from exact tensor-core level
+# sums (fixed-point digits, integer level sums): the fused forward's cost tiles up
+# to D = 128 (five 8-bit digits), the unfused cost tensor up to D = 400 (six 7-bit
+# digits above D = 128); wider fused rows use the difference form. The
+# difference-form kernels (the debug option) compute the same costs on the FP32
+# pipe. Both must hold the tolerance at O(1) weights and agree closely. The shapes
+# run the tensor-memory rings round several times (M up to 520 columns), over
+# several 128-row strips, and through one, two and several K-blocks.
+XTC_SHAPES = [(1, 9, 3), (33, 31, 1), (100, 37, 16), (129, 130, 63), (70, 91, 64), (130, 97, 65),
+              (200, 150, 128), (300, 333, 128), (257, 520, 96), (129, 70, 129)]
+XTC_WIDE = [(64, 33, 256), (300, 333, 400), (131, 77, 200)]
+
+
+@pytest.mark.parametrize("mname,mode,N,M,D", [("fused+extended", 3) + s for s in XTC_SHAPES] +
+                         [("unfused+extended", 2) + s for s in XTC_SHAPES + XTC_WIDE])
+def test_extended_tensor_core_costs(mname, mode, N, M, D):
     x, y = synth.iid_normal_pair(3, N, M, D, 106, repeat=N * 1000 + D)
-    got = check_against_oracle(x, y, 0.7, 3, grad_loss=WEIGHTS_O1, what=f"extended tc {N}x{M}x{D}")
+    got = check_against_oracle(x, y, 0.7, mode, grad_loss=WEIGHTS_O1, what=f"{mname} tc {N}x{M}x{D}")
     with options(simt=True):
-        ref = run_cuda(x, y, 0.7, 3, grad_loss=WEIGHTS_O1)
-    assert_close(got["loss"], ref["loss"], 1e-6, 0.0, f"extended tc vs difference form {N}x{M}x{D} loss")
-    assert_close(got["gx"], ref["gx"], 1e-4, 1e-7, f"extended tc vs difference form {N}x{M}x{D} grad_x")
+        ref = run_cuda(x, y, 0.7, mode, grad_loss=WEIGHTS_O1)
+    assert_close(got["loss"], ref["loss"], 1e-6, 0.0, f"{mname} tc vs difference form {N}x{M}x{D} loss")
+    assert_close(got["gx"], ref["gx"], 1e-4, 1e-7, f"{mname} tc vs difference form {N}x{M}x{D} grad_x")
 
 
 @pytest.mark.parametrize("W", [1, 3])
@@ -250,12 +256,26 @@ def test_headline_config(mname, mode):
 
 # --------------------------------------------------------------------------- sweep (sampled)
 
-@pytest.mark.parametrize("mname,mode", MODES)
-@pytest.mark.parametrize("L,D", [(128, 128), (1024, 128), (2048, 128), (256, 1), (256, 4), (256, 256)])
-def test_sweep_sampled(mname, mode, L, D):
+# Every point of the Figure 1 sweep (B=32; L at D=128, D at L=256), the whole batch,
+# in the precision the high-level API picks for it (double-float above D = 64).
+SWEEP_POINTS = [(128, 128), (256, 128), (512, 128), (1024, 128), (2048, 128),
+                (256, 1), (256, 4), (256, 16), (256, 64), (256, 256)]
+
+
+@pytest.mark.parametrize("mname,base", MODES)
+@pytest.mark.parametrize("L,D", SWEEP_POINTS)
+def test_sweep(mname, base, L, D):
+    mode = base | _lib().auto_precision(1.0, L, L, D, 32)
     x, y = synth.iid_normal_pair(32, L, L, D, 2, repeat=L * 1000 + D)
-    sample = [0, 31] if L >= 1024 else [0, 7, 31]
-    check_against_oracle(x, y, 1.0, mode, sample=sample, what=f"sweep L={L} D={D} {mname}")
+    check_against_oracle(x, y, 1.0, mode, what=f"sweep L={L} D={D} {mname} mode={mode}")
+
+
+# The fp32 modes at the sweep's wide points (difference-form costs), sampled problems.
+@pytest.mark.parametrize("mname,mode", MODES)
+@pytest.mark.parametrize("L,D", [(256, 128), (2048, 128), (256, 256)])
+def test_sweep_fp32_wide_sampled(mname, mode, L, D):
+    x, y = synth.iid_normal_pair(32, L, L, D, 2, repeat=L * 1000 + D)
+    check_against_oracle(x, y, 1.0, mode, sample=[0, 7, 31], what=f"sweep fp32 L={L} D={D} {mname}")
 
 
 # --------------------------------------------------------------------------- normalized

@@ -39,7 +39,7 @@ def _worker(rank, world, port, out):
 
 def test_time_is_the_max_over_two_gloo_ranks():
     world, port = 2, _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()   # no fork of a threaded process
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     for r in range(world):
         t, v = out[r]
