@@ -33,6 +33,24 @@ static __device__ __forceinline__ bool wait_smem(const volatile int* cnt, int ta
     return __shfl_sync(kFull, ok, 0);
 }
 
+// wait_smem for a warp whose wait is off the critical path: sleeps between tests so
+// that it leaves the issue slots of its scheduler to the DP warp there.
+static __device__ __forceinline__ bool wait_smem_sleep(const volatile int* cnt, int target, const WaveParams& q,
+                                                       int& seen, unsigned ns) {
+    bool ok = true;
+    int c = *cnt;
+    if (c < target) {
+        const unsigned long long t0 = global_ns();
+        while ((c = *cnt) < target) {
+            __nanosleep(ns);
+            if (ld_volatile_global(q.status) != 0) { ok = false; break; }
+            if (global_ns() - t0 > q.wait_ns) { atomicOr(q.status, kStatusTimeout); ok = false; break; }
+        }
+    }
+    seen = __shfl_sync(kFull, c, 0);
+    return __shfl_sync(kFull, ok, 0);
+}
+
 // Wait until every lane's slot (or pair of slots) carries its expected tag,
 // reloading the lanes that do not yet. want == 0 marks a lane with nothing to
 // check. Bounded; warp-uniform result.

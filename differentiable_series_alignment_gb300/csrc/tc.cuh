@@ -187,6 +187,27 @@ __device__ __forceinline__ void wait_ok(bool& ok, uint32_t bar, uint32_t parity,
     if (ok) ok = mbar_wait(bar, parity, status);
 }
 
+// The same bounded wait, sleeping between tests: for warps whose waits are off the
+// critical path (an issuer or a converter running ahead), which would otherwise
+// take issue slots from the DP warp on their scheduler while they poll.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int* status, unsigned ns) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_test(bar, parity)) {
+        __nanosleep(ns);
+        if (global_ns() - t0 > 2000000000ull) {
+            atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void wait_ok_sleep(bool& ok, uint32_t bar, uint32_t parity, int* status,
+                                              unsigned ns = 128) {
+    if (ok) ok = mbar_wait_sleep(bar, parity, status, ns);
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     uint32_t r[32];
     asm volatile(

@@ -148,11 +148,11 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                 y_last[e] = c;
             };
             for (int c = 0; c < kRB - 1 && c < nT; ++c) issue_y(c);
-            wait_ok(ok, smem_u32(&s_a), 0u, status);
+            wait_ok_sleep(ok, smem_u32(&s_a), 0u, status);
             for (int c = 0; c < nT && ok; ++c) {
                 const int t = c % kRT, e = c % kRB;
-                if (c >= kRT) wait_ok(ok, smem_u32(&s_tfree[t]), (uint32_t)(((c - kRT) / kRT) & 1), status);
-                wait_ok(ok, smem_u32(&s_bfull[e]), (uint32_t)((c / kRB) & 1), status);
+                if (c >= kRT) wait_ok_sleep(ok, smem_u32(&s_tfree[t]), (uint32_t)(((c - kRT) / kRT) & 1), status);
+                wait_ok_sleep(ok, smem_u32(&s_bfull[e]), (uint32_t)((c / kRB) & 1), status);
                 if (!ok) break;
                 fence_after_sync();
                 const uint32_t d = tmem + (uint32_t)(t * kSlotCols);
@@ -167,7 +167,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                 // y tile c + kRB - 1 goes to entry (c - 1) % kRB, last read by MMA(c - 1)
                 const int cy = c + kRB - 1;
                 if (cy < nT) {
-                    if (c >= 1) wait_ok(ok, smem_u32(&s_bempty[(c - 1) % kRB]), (uint32_t)(((c - 1) / kRB) & 1), status);
+                    if (c >= 1) wait_ok_sleep(ok, smem_u32(&s_bempty[(c - 1) % kRB]), (uint32_t)(((c - 1) / kRB) & 1), status);
                     if (!ok) break;
                     issue_y(cy);
                 }
@@ -176,9 +176,9 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
             // and no copy is still writing shared memory when the CTA exits
             mma_commit(smem_u32(&s_fin));
             bool fin = true;
-            wait_ok(fin, smem_u32(&s_fin), 0u, status);
+            wait_ok_sleep(fin, smem_u32(&s_fin), 0u, status);
             for (int e = 0; e < kRB; ++e)
-                if (y_last[e] >= 0) wait_ok(fin, smem_u32(&s_bfull[e]), (uint32_t)((y_last[e] / kRB) & 1), status);
+                if (y_last[e] >= 0) wait_ok_sleep(fin, smem_u32(&s_bfull[e]), (uint32_t)((y_last[e] / kRB) & 1), status);
         }
         __syncwarp();
     } else {

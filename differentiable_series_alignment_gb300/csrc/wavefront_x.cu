@@ -290,10 +290,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
             }
             if (!ok) break;
 
+            // the group's 16 costs into registers before any of its stores (the compiler
+            // keeps loads behind stores it cannot prove apart)
             float2 dc[kGroup];
-            if (!FUSED) {
 #pragma unroll
-                for (int u = 0; u < kGroup; ++u) dc[u] = dp[(long long)(s0 + u) * 32];
+            for (int u = 0; u < kGroup; ++u) {
+                if (FUSED) {
+                    const int slot = ((s0 + u - lane) & 63) * 32 + lane;
+                    dc[u] = make_float2(fdh[slot], fdl[slot]);
+                } else {
+                    dc[u] = dp[(long long)(s0 + u) * 32];
+                }
             }
 #pragma unroll
             for (int u = 0; u < kGroup; ++u) {
@@ -305,13 +312,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
                 const float tv_lo = __shfl_sync(kFull, topv.lo, u);
                 const dd hu = (lane == 0) ? mk(tv_hi, tv_lo) : mk(hs_hi, hs_lo);
                 const dd vl = v_prev;
-                dd d;
-                if (FUSED) {
-                    const int slot = (j & 63) * 32 + lane;
-                    d = scale_dd(mk(fdh[slot], fdl[slot]), scale);
-                } else {
-                    d = scale_dd(mk(dc[u].x, dc[u].y), scale);
-                }
+                const dd d = scale_dd(mk(dc[u].x, dc[u].y), scale);
                 const bool col0 = (j == 0);
                 dd h, v;
                 float4 lp;
@@ -411,7 +412,6 @@ template <int NS> struct XDigits {
     static constexpr int SlotCols = NS * 32;
     static constexpr uint32_t A = NS * kXAPart;           // all digits of one K-block of the x rows
     static constexpr uint32_t B = NS * kXBPart;           // [b_0 ; ... ; b_(NS-1)] of one K-block of a y tile
-    static constexpr uint32_t Stage = A + B;
 };
 
 // Shared memory of the operand region: one K-block keeps the x digits resident
@@ -546,38 +546,52 @@ __device__ __forceinline__ dd levels_dd(const float (&S)[NS], int k)
     return mk(ldexpf(a.hi, k), ldexpf(a.lo, k));
 }
 
-// 16-byte asynchronous global -> shared copy (completion: cp.async.wait_group).
-__device__ __forceinline__ void cp_async16x(void* dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
-}
-
 // Extended fused forward with the exact tensor-core cost tiles. Same recursion,
-// channels and loss as fwdx_kernel<true>, with the CTA shape of fwd_tc_kernel: 4 DP
-// warps (128 rows, the MMA height) and an issuer warp that streams each K-block of
-// the CTA's x digits with the y tile's digits through one stage buffer and issues
-// the level MMAs into a ring of three tensor-memory tiles. At the start of every
-// 32-step period each DP warp reads its 32 rows of the next tile's five levels
-// (tcgen05.ld), releases the tile, and writes the double-float costs into its
-// 64-column shared ring (hi and lo planes). Hand-offs (mbarriers, waits bounded):
-//   s_sfull    the stage's copies landed        s_sempty  the MMAs reading it are done
-//   s_tfull[t] cost tile t in TMEM              s_tfree[t] every DP warp with rows read it
+// channels and loss as fwdx_kernel<true>. A CTA owns 128 rows (four DP warps, the
+// MMA height) of one problem as a strip of the wavefront. Warp 4 (lane 0) copies
+// the digits (the x digits once for one K-block, else x and y streamed per K-block
+// through one stage) and issues the level MMAs of each 32-column tile into a ring
+// of three tensor-memory tiles. Warps 5-8 are converters, one per TMEM lane
+// quarter: as soon as a tile is in TMEM and the shared cost ring of the DP warp
+// with the same rows has room, converter q combines its 32 rows' level sums into
+// double-float costs in that ring (hi and lo planes) and releases the tile.
+//
+// Why converters. A DP warp starts its 16-step group at s0 only after the warp
+// above has finished step s0 + 46, so warp 3 trails warp 0 by ~94 steps. Were the
+// DP warps to read the tiles themselves, tile c - 3 would be released only when
+// warp 3 reached it, at warp 0's step 32 c - 2: warp 0 would wait on warp 3 at
+// every tile, with no slack (three tiles of five levels fill the tensor memory).
+// With converters a tile waits on DP progress only for ring room. The rings hold
+// 3, 3, 3, 4 tiles (warps 0-3): a converter can fill tile c + 1 while its DP warp
+// runs period c (which reads tiles c - 1 and c), and the tile warp 0 needs at step
+// 32 c waits on warps 1-3 having finished periods c - 5, c - 5 and c - 6 (warp 0
+// near step 32 c - 66 at the latest). The conversion also leaves the DP warps'
+// critical path.
+//
+// Hand-offs (every wait bounded):
+//   s_a                      x digits resident
+//   s_sfull / s_sempty       stage copies landed / the MMAs reading it are done
+//   s_tfull[t] / s_tfree[t]  levels of tile t in TMEM / the 4 converters read them
+//   s_conv[q]                tiles converted into ring q (converter q -> DP warp q)
+//   s_used[q]                tiles DP warp q no longer needs (DP warp q -> converter q)
+constexpr int kXConvWarps = 4;
+constexpr int kXFusedThreads = (kXDpWarps + 1 + kXConvWarps) * 32;
+constexpr int kXTileFloats = 32 * 32;                       // one plane of a 32-column ring tile
+__host__ __device__ constexpr int xring_tiles(int w) { return w < 3 ? 3 : 4; }
+__host__ __device__ constexpr int xring_first(int w) { return 3 * w; }
+constexpr int kXRingTiles = 13;                             // xring_first(3) + xring_tiles(3)
+constexpr size_t kXRingBytes = (size_t)kXRingTiles * 2 * kXTileFloats * sizeof(float);
+
 template <int NS>
-__global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
+__global__ void __launch_bounds__(kXFusedThreads, 1)
     fwdx_tc_kernel(const WaveParams q, const unsigned char* __restrict__ ximg, const unsigned char* __restrict__ yimg,
                    const float4* __restrict__ xinfo, const float4* __restrict__ yinfo)
 {
     using X = XDigits<NS>;
-    // RT cost tiles share the 512 tensor-memory columns, and RT >= 3 is required: a
-    // DP warp may start its group of 16 steps at s0 only after the warp above has
-    // finished step s0 + 46, so warp 3 releases tile c - RT (at its step 32 (c - RT))
-    // only once warp 0 has reached step 32 (c - RT) + 94. With RT = 3 that is step
-    // 32 c - 2, before warp 0 needs tile c; with RT = 2 warp 0 would already be
-    // waiting for tile c and no warp could progress. Six digits (192 columns a tile)
-    // leave room for two tiles, so this kernel takes five digits (D <= 128).
-    static_assert(NS == 5, "three tiles of five levels fill the tensor memory");
+    // three tiles of five levels (160 columns each) fill the 512 tensor-memory columns
+    static_assert(NS == 5, "five digits: three cost tiles in tensor memory");
     constexpr int kXRT = 3, kXSlotCols = X::SlotCols, kXSlices = NS;
-    constexpr uint32_t kXA = X::A, kXStage = X::Stage;
+    constexpr uint32_t kXA = X::A, kXB = X::B;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     constexpr int W = kXDpWarps;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -586,11 +600,16 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
     __shared__ int s_tk;
     __shared__ double s_red[kMaxWarps];
     __shared__ int s_last;
-    __shared__ uint64_t s_sfull, s_sempty, s_fin, s_tfull[kXRT], s_tfree[kXRT], s_bfull[2], s_bempty[2];
+    __shared__ uint64_t s_a, s_sfull, s_sempty, s_fin, s_tfull[kXRT], s_tfree[kXRT];
     __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_conv[kXDpWarps], s_used[kXDpWarps];
 
     if (threadIdx.x == 0) s_tk = atomicAdd(q.ticket_f, 1);
-    if (threadIdx.x < W) cons[threadIdx.x] = 0;
+    if (threadIdx.x < W) {
+        cons[threadIdx.x] = 0;
+        s_conv[threadIdx.x] = 0;
+        s_used[threadIdx.x] = 0;
+    }
     for (int k = threadIdx.x; k < 2 * W * kRing; k += blockDim.x) ring[k].tag = 0u;
     __syncthreads();
 
@@ -598,29 +617,23 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
     const int p = tk % q.P, strip = tk / q.P;
     const int N = q.N, M = q.M, T = skew_T(M);
     const int KB = (q.D + kTcKFeat - 1) / kTcKFeat;
-    // one K-block: the x digits stay resident and y tiles come through a two-entry ring
-    const bool resident = KB == 1;
+    const bool resident = KB == 1;   // one K-block: the x digits stay in shared memory
     const int Npad = simg_pad(N), Mpad = simg_pad(M);
     const int rs0 = strip * W * 32;
-    const int nact = min(W, max(1, (N - rs0 + 31) / 32));
     const int nT = (M + 31) / 32;
 
     unsigned char* tcb = smem_raw + q.smem_fixed;
     unsigned char* stage = tcb + ((1024u - (tc::smem_u32(tcb) & 1023u)) & 1023u);   // [x digits | y digits]
-    float* dts = reinterpret_cast<float*>(stage + xtc_region(NS, KB));              // [W][hi, lo][64][32]
-    float4* yis = reinterpret_cast<float4*>(dts + W * 2 * 64 * 32);                 // [W][2][32] y info
+    float* rings = reinterpret_cast<float*>(stage + kXA + kXB);                    // cost rings of the DP warps
 
     if (threadIdx.x == 0) {
+        tc::mbar_init(tc::smem_u32(&s_a), 1);
         tc::mbar_init(tc::smem_u32(&s_sfull), 1);
         tc::mbar_init(tc::smem_u32(&s_sempty), 1);
         tc::mbar_init(tc::smem_u32(&s_fin), 1);
         for (int t = 0; t < kXRT; ++t) {
             tc::mbar_init(tc::smem_u32(&s_tfull[t]), 1);
-            tc::mbar_init(tc::smem_u32(&s_tfree[t]), nact);
-        }
-        for (int e = 0; e < 2; ++e) {
-            tc::mbar_init(tc::smem_u32(&s_bfull[e]), 1);
-            tc::mbar_init(tc::smem_u32(&s_bempty[e]), 1);
+            tc::mbar_init(tc::smem_u32(&s_tfree[t]), kXConvWarps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -635,92 +648,54 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
     dd c0 = zero;  // scaled d(i, 0)
     bool active = false;
 
-    if (warp == kXIssuer && resident) {
+    // the level MMAs of one 16-wide K step: x digit l against the stacked y digits
+    // [b_0 ; ... ; b_(NS-1-l)], into the level columns l .. NS-1
+    auto level_mmas = [&](uint32_t d0, uint32_t a, uint32_t b, uint32_t ko, bool acc0) {
+#pragma unroll
+        for (int l = 0; l < kXSlices; ++l)
+            tc::mma_bf16(d0 + (uint32_t)(l * 32), tc::sdesc(a + l * kXAPart + ko), tc::sdesc(b + ko),
+                         tc::idesc_bf16(128, (kXSlices - l) * 32), (acc0 || l > 0) ? 1u : 0u);
+    };
+
+    if (warp == kXIssuer) {
         if (lane == 0) {
-            // the x digits once; y tile c into ring entry c & 1, refilled once MMA(c) has read it
             bool ok = true;
-            int y_last[2] = {-1, -1};
-            const uint32_t abar = tc::smem_u32(&s_sfull);
-            tc::mbar_expect_tx(abar, kXA);
-            for (int l = 0; l < kXSlices; ++l)
-                tc::bulk_g2s(tc::smem_u32(stage + l * kXAPart), ximg + oimg_offset(p, 1, 0, NS, l, Npad, rs0), kXAPart,
-                             abar);
-            auto issue_y = [&](int c) {
-                const int e = c & 1;
-                const uint32_t bar = tc::smem_u32(&s_bfull[e]);
-                tc::mbar_expect_tx(bar, X::B);
+            int issued = -1, landed = -1;   // stage fills issued / waited for
+            if (resident) {
+                const uint32_t abar = tc::smem_u32(&s_a);
+                tc::mbar_expect_tx(abar, kXA);
                 for (int l = 0; l < kXSlices; ++l)
-                    tc::bulk_g2s(tc::smem_u32(stage + kXA + e * X::B + l * kXBPart),
-                                 yimg + oimg_offset(p, 1, 0, NS, l, Mpad, 32 * c), kXBPart, bar);
-                y_last[e] = c;
-            };
-            for (int c = 0; c < 2 && c < nT; ++c) issue_y(c);
-            tc::wait_ok(ok, abar, 0u, status);
-            for (int c = 0; c < nT && ok; ++c) {
-                const int e = c & 1, t = c % kXRT;
-                if (c >= kXRT) tc::wait_ok(ok, tc::smem_u32(&s_tfree[t]), (uint32_t)(((c - kXRT) / kXRT) & 1), status);
-                tc::wait_ok(ok, tc::smem_u32(&s_bfull[e]), (uint32_t)((c >> 1) & 1), status);
-                if (!ok) break;
-                tc::fence_after_sync();
-                const uint32_t d0 = tmem + (uint32_t)(t * kXSlotCols);
-                const uint32_t a = tc::smem_u32(stage), b = a + kXA + e * X::B;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {   // 16 bf16 = 32 bytes along K per step
-                    const uint32_t ko = ks * 32;
-#pragma unroll
-                    for (int l = 0; l < kXSlices; ++l)
-                        tc::mma_bf16(d0 + (uint32_t)(l * 32), tc::sdesc(a + l * kXAPart + ko), tc::sdesc(b + ko),
-                                     tc::idesc_bf16(128, (kXSlices - l) * 32), (ks > 0 || l > 0) ? 1u : 0u);
-                }
-                tc::mma_commit(tc::smem_u32(&s_bempty[e]));
-                tc::mma_commit(tc::smem_u32(&s_tfull[t]));
-                if (c + 2 < nT) {   // entry e takes tile c + 2 once MMA(c) has read it
-                    tc::wait_ok(ok, tc::smem_u32(&s_bempty[e]), (uint32_t)((c >> 1) & 1), status);
-                    if (!ok) break;
-                    issue_y(c + 2);
-                }
+                    tc::bulk_g2s(tc::smem_u32(stage + l * kXAPart), ximg + oimg_offset(p, 1, 0, NS, l, Npad, rs0),
+                                 kXAPart, abar);
+                tc::wait_ok_sleep(ok, abar, 0u, status);
             }
-            tc::mma_commit(tc::smem_u32(&s_fin));
-            bool fin = true;
-            tc::wait_ok(fin, tc::smem_u32(&s_fin), 0u, status);
-            for (int e = 0; e < 2; ++e)
-                if (y_last[e] >= 0) tc::wait_ok(fin, tc::smem_u32(&s_bfull[e]), (uint32_t)((y_last[e] >> 1) & 1), status);
-        }
-        __syncwarp();
-    } else if (warp == kXIssuer) {
-        if (lane == 0) {
-            // stage g = c * KB + kb: K-block kb of the x rows' and of y tile c's digits
-            bool ok = true;
+            // stage fill g = c * KB + kb: y tile c's digits of K-block kb (and, streamed,
+            // the x digits of that K-block), once the MMAs of fill g - 1 have read the stage
             const int G = nT * KB;
-            int g_last = -1;
             for (int g = 0; g < G && ok; ++g) {
                 const int c = g / KB, kb = g - c * KB, t = c % kXRT;
-                if (kb == 0 && c >= kXRT)
-                    tc::wait_ok(ok, tc::smem_u32(&s_tfree[t]), (uint32_t)(((c - kXRT) / kXRT) & 1), status);
-                if (g >= 1) tc::wait_ok(ok, tc::smem_u32(&s_sempty), (uint32_t)((g - 1) & 1), status);
+                if (g >= 1) tc::wait_ok_sleep(ok, tc::smem_u32(&s_sempty), (uint32_t)((g - 1) & 1), status);
                 if (!ok) break;
                 const uint32_t bar = tc::smem_u32(&s_sfull);
-                tc::mbar_expect_tx(bar, kXStage);
-                for (int l = 0; l < kXSlices; ++l)
-                    tc::bulk_g2s(tc::smem_u32(stage + l * kXAPart), ximg + oimg_offset(p, KB, kb, NS, l, Npad, rs0),
-                                 kXAPart, bar);
+                tc::mbar_expect_tx(bar, resident ? kXB : kXA + kXB);
+                if (!resident)
+                    for (int l = 0; l < kXSlices; ++l)
+                        tc::bulk_g2s(tc::smem_u32(stage + l * kXAPart),
+                                     ximg + oimg_offset(p, KB, kb, NS, l, Npad, rs0), kXAPart, bar);
                 for (int l = 0; l < kXSlices; ++l)
                     tc::bulk_g2s(tc::smem_u32(stage + kXA + l * kXBPart),
                                  yimg + oimg_offset(p, KB, kb, NS, l, Mpad, 32 * c), kXBPart, bar);
-                g_last = g;
-                tc::wait_ok(ok, bar, (uint32_t)(g & 1), status);
+                issued = g;
+                if (kb == 0 && c >= kXRT)   // TMEM tile t free: the converters have read tile c - 3
+                    tc::wait_ok_sleep(ok, tc::smem_u32(&s_tfree[t]), (uint32_t)(((c - kXRT) / kXRT) & 1), status);
+                tc::wait_ok_sleep(ok, bar, (uint32_t)(g & 1), status);
                 if (!ok) break;
+                landed = g;
                 tc::fence_after_sync();
                 const uint32_t d0 = tmem + (uint32_t)(t * kXSlotCols);
                 const uint32_t a = tc::smem_u32(stage), b = a + kXA;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {   // 16 bf16 = 32 bytes along K per step
-                    const uint32_t ko = ks * 32;
-#pragma unroll
-                    for (int l = 0; l < kXSlices; ++l)   // digit l of x against y digits 0 .. NS-1-l: levels l .. NS-1
-                        tc::mma_bf16(d0 + (uint32_t)(l * 32), tc::sdesc(a + l * kXAPart + ko), tc::sdesc(b + ko),
-                                     tc::idesc_bf16(128, (kXSlices - l) * 32), (kb > 0 || ks > 0 || l > 0) ? 1u : 0u);
-                }
+                for (int ks = 0; ks < 4; ++ks) level_mmas(d0, a, b, ks * 32, kb > 0 || ks > 0);
                 tc::mma_commit(tc::smem_u32(&s_sempty));
                 if (kb == KB - 1) tc::mma_commit(tc::smem_u32(&s_tfull[t]));
             }
@@ -728,10 +703,65 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
             // still writing shared memory when the CTA exits
             tc::mma_commit(tc::smem_u32(&s_fin));
             bool fin = true;
-            tc::wait_ok(fin, tc::smem_u32(&s_fin), 0u, status);
-            if (g_last >= 0) tc::wait_ok(fin, tc::smem_u32(&s_sfull), (uint32_t)(g_last & 1), status);
+            tc::wait_ok_sleep(fin, tc::smem_u32(&s_fin), 0u, status);
+            if (issued > landed) tc::wait_ok_sleep(fin, tc::smem_u32(&s_sfull), (uint32_t)(issued & 1), status);
         }
         __syncwarp();
+    } else if (warp > kXIssuer) {
+        // converter of TMEM lane quarter qd, feeding DP warp qd's ring
+        const int qd = warp & 3;
+        const bool rows = rs0 + 32 * qd < N;   // DP warp qd has rows (else: read and release only)
+        const int R = xring_tiles(qd);
+        float* dh = rings + xring_first(qd) * 2 * kXTileFloats;   // [32 R][32] cost hi, slot (col mod 32 R), lane
+        float* dl = dh + R * kXTileFloats;                        // [32 R][32] cost lo
+        const float4 xi = xinfo[(size_t)p * Npad + rs0 + 32 * qd + lane];
+        const int ex = __float_as_int(xi.z);
+        const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
+        bool ok = true;
+        int used_seen = 0;
+        for (int c = 0; c < nT; ++c) {
+            const int t = c % kXRT;
+            // ring slot of tile c held tile c - R: DP warp qd must be done with it
+            if (rows && c - R + 1 > used_seen) ok = wait_smem_sleep(&s_used[qd], c - R + 1, q, used_seen, 128);
+            if (!ok) break;
+            tc::wait_ok_sleep(ok, tc::smem_u32(&s_tfull[t]), (uint32_t)((c / kXRT) & 1), status);
+            if (!__all_sync(kFull, ok)) break;
+            tc::fence_after_sync();
+            const float4 yv = yinfo[(size_t)p * Mpad + 32 * c + lane];
+            const uint32_t tt0 = tq + (uint32_t)(t * kXSlotCols);
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {   // 8 columns at a time: NS x 8 level sums in registers
+                uint32_t S[NS][8];
+#pragma unroll
+                for (int l = 0; l < NS; ++l) tc::tmem_ld8_nowait(tt0 + l * 32 + 8 * q8, S[l]);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int col = 8 * q8 + u;
+                    const float nyh = __shfl_sync(kFull, yv.x, col), nyl = __shfl_sync(kFull, yv.y, col);
+                    const int ey = __shfl_sync(kFull, __float_as_int(yv.z), col);
+                    float Su[NS];
+#pragma unroll
+                    for (int l = 0; l < NS; ++l) Su[l] = __uint_as_float(S[l][u]);
+                    const dd xy = levels_dd<NS>(Su, ex + ey + 2 - 2 * X::DB);
+                    dd cst = sub(add(mk(xi.x, xi.y), mk(nyh, nyl)), mk(2.f * xy.hi, 2.f * xy.lo));
+                    if (cst.hi < 0.f) cst = zero;
+                    if (rows) {
+                        const int slot = (32 * (c % R) + col) * 32 + lane;
+                        dh[slot] = cst.hi;
+                        dl[slot] = cst.lo;
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&s_tfree[t]));
+            if (rows) {   // the costs are visible to DP warp qd before the count
+                __threadfence_block();
+                __syncwarp();
+                if (lane == 0) s_conv[qd] = c + 1;
+            }
+        }
     } else {
         const int rb = strip * W + warp, r0 = rb * 32, i = r0 + lane;
         active = r0 < N;
@@ -745,17 +775,9 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
         const bool last_lane = (i == Nb - 1);
         const float scale = q.scale;
         float2* rowbuf = reinterpret_cast<float2*>(q.rowbuf) + (size_t)p * M;
-        float* dh = dts + warp * 2 * 64 * 32;   // [64][32] cost hi, slot (col & 63), lane
-        float* dl = dh + 64 * 32;               // [64][32] cost lo
-        const float4 xi = xinfo[(size_t)p * Npad + i];
-        const int ex = __float_as_int(xi.z);
-        const float4* yip = yinfo + (size_t)p * Mpad;
-        float4* yiw = yis + warp * 2 * 32;
-        const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
-        if (active) {
-            cp_async16x(yiw + lane, yip + lane);
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        }
+        const int rcols = 32 * xring_tiles(warp);   // ring columns: slot of column j is j mod rcols
+        const float* dh = rings + xring_first(warp) * 2 * kXTileFloats;
+        const float* dl = dh + xring_tiles(warp) * kXTileFloats;
 
         if (active) {
             float4* lpp = reinterpret_cast<float4*>(q.VH) + skew_index(N, M, p, rb, 0, lane);
@@ -775,51 +797,17 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
             }
 
             dd h_prev = zero, v_prev = zero;
-            bool tc_ok = true;
-            int cons_seen = 0;
+            int cons_seen = 0, conv_seen = 0;
             const int nG = T / kGroup;
             for (int g = 0; g < nG; ++g) {
                 const int s0 = g * kGroup;
                 if ((s0 & 31) == 0 && (s0 >> 5) < nT) {
-                    // period c = s0/32 reads columns of tiles c-1 and c: bring tile c in
-                    const int c = s0 >> 5, t = c % kXRT;
-                    tc::wait_ok(tc_ok, tc::smem_u32(&s_tfull[t]), (uint32_t)((c / kXRT) & 1), status);
-                    if (!__all_sync(kFull, tc_ok)) break;
-                    tc::fence_after_sync();
-                    asm volatile("cp.async.wait_group 0;" ::: "memory");
-                    __syncwarp();
-                    const float4 yv = yiw[(c & 1) * 32 + lane];
-                    if (c + 1 < nT) {   // its buffer was last read in period c - 1
-                        cp_async16x(yiw + ((c + 1) & 1) * 32 + lane, yip + 32 * (c + 1) + lane);
-                        asm volatile("cp.async.commit_group;" ::: "memory");
-                    }
-                    const uint32_t tt0 = tq + (uint32_t)(t * kXSlotCols);
-#pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {   // 8 columns at a time: NS x 8 level values in registers
-                        uint32_t S[NS][8];   // all levels of 8 columns in flight, one wait
-#pragma unroll
-                        for (int l = 0; l < NS; ++l) tc::tmem_ld8_nowait(tt0 + l * 32 + 8 * q8, S[l]);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int col = 8 * q8 + u;
-                            const float nyh = __shfl_sync(kFull, yv.x, col), nyl = __shfl_sync(kFull, yv.y, col);
-                            const int ey = __shfl_sync(kFull, __float_as_int(yv.z), col);
-                            float Su[NS];
-#pragma unroll
-                            for (int l = 0; l < NS; ++l) Su[l] = __uint_as_float(S[l][u]);
-                            const dd xy = levels_dd<NS>(Su, ex + ey + 2 - 2 * X::DB);
-                            dd cst = sub(add(mk(xi.x, xi.y), mk(nyh, nyl)), mk(2.f * xy.hi, 2.f * xy.lo));
-                            if (cst.hi < 0.f) cst = zero;
-                            const int slot = ((32 * c + col) & 63) * 32 + lane;
-                            dh[slot] = cst.hi;
-                            dl[slot] = cst.lo;
-                        }
-                    }
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&s_tfree[t]));
-                    __syncwarp();
+                    // period c = s0/32 reads columns of tiles c-1 and c: tiles below c - 1
+                    // are free for the converter, tile c must be in the ring
+                    const int c = s0 >> 5;
+                    if (c >= 2 && lane == 0) s_used[warp] = c - 1;
+                    if (conv_seen < c + 1 && !wait_smem(&s_conv[warp], c + 1, q, conv_seen)) break;
+                    __threadfence_block();
                 }
 
                 // Upper-neighbour h for lane 0: lane q holds column s0 + q as a (hi, lo) slot pair.
@@ -853,6 +841,15 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
                 }
                 if (!ok) break;
 
+                // the group's 16 costs into registers before any of its stores (the
+                // compiler keeps loads behind stores it cannot prove apart)
+                float2 dc[kGroup];
+                int col = (s0 - lane + rcols) % rcols;   // column s0 - lane >= -31 in the ring
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u) {
+                    dc[u] = make_float2(dh[col * 32 + lane], dl[col * 32 + lane]);
+                    col = (col + 1 == rcols) ? 0 : col + 1;
+                }
 #pragma unroll
                 for (int u = 0; u < kGroup; ++u) {
                     const int s = s0 + u;
@@ -863,8 +860,7 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
                     const float tv_lo = __shfl_sync(kFull, topv.lo, u);
                     const dd hu = (lane == 0) ? mk(tv_hi, tv_lo) : mk(hs_hi, hs_lo);
                     const dd vl = v_prev;
-                    const int slot = (j & 63) * 32 + lane;
-                    const dd d = scale_dd(mk(dh[slot], dl[slot]), scale);
+                    const dd d = scale_dd(mk(dc[u].x, dc[u].y), scale);
                     const bool col0 = (j == 0);
                     dd h, v;
                     float4 lp;
@@ -883,11 +879,11 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
                 }
                 if (has_top && !top_global && lane == 0) cons[warp - 1] = min(s0 + kGroup, M);
             }
-            asm volatile("cp.async.wait_all;" ::: "memory");  // none in flight past an early exit
         }
     }
 
     // Loss: R[N,M] = sum_i d(i,0) + sum_{j>=1} h(N-1, j), scaled units, in fp64.
+    const int nwarps = (int)(blockDim.x >> 5);
     const int Nb = q.lens_n ? min(max(q.lens_n[p], 1), N) : N;
     const int Mb = q.lens_m ? min(max(q.lens_m[p], 1), M) : M;
     double part = (active && warp < W && rs0 + 32 * warp + lane < Nb) ? (double)c0.hi + (double)c0.lo : 0.0;
@@ -917,7 +913,7 @@ __global__ void __launch_bounds__((kXDpWarps + 1) * 32, 1)
         __syncthreads();
         if (threadIdx.x == 0) {
             double tot = 0.0;
-            for (int w = 0; w <= W; ++w) tot += s_red[w];
+            for (int w = 0; w < nwarps; ++w) tot += s_red[w];
             for (int k = 0; k < q.S; ++k) tot += __ldcg(&q.colsum[(size_t)p * q.NB + k]);
             q.loss[p] = (float)(tot * (double)q.unscale);
         }
@@ -1174,20 +1170,15 @@ cudaError_t launch_forward_xtc(WaveParams q, const void* ximg, const void* yimg,
     const int grid = q.P * q.S;
     q.smem_fixed = (int)(((size_t)kXDpWarps * kRing * 2 * sizeof(Slot) + (size_t)kXDpWarps * sizeof(int) + 15) &
                          ~(size_t)15);
-    const int KB = (q.D + kTcKFeat - 1) / kTcKFeat;
-    auto go = [&](auto kern, int NS) -> cudaError_t {
-        const size_t need = q.smem_fixed + 1024 + xtc_region(NS, KB) + (size_t)kXDpWarps * 2 * 64 * 32 * sizeof(float) +
-                            (size_t)kXDpWarps * 2 * 32 * sizeof(float4);
-        const size_t smem = max(need, wave_smem_floor());   // one CTA per SM: the whole tensor memory
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        kern<<<grid, (kXDpWarps + 1) * 32, smem, st>>>(q, static_cast<const unsigned char*>(ximg),
-                                                       static_cast<const unsigned char*>(yimg),
-                                                       static_cast<const float4*>(xinfo),
-                                                       static_cast<const float4*>(yinfo));
-        return cudaGetLastError();
-    };
-    return go(fwdx_tc_kernel<5>, 5);
+    const size_t need = q.smem_fixed + 1024 + XDigits<5>::A + XDigits<5>::B + kXRingBytes;
+    const size_t smem = max(need, wave_smem_floor());   // one CTA per SM: the whole tensor memory
+    cudaError_t e = cudaFuncSetAttribute(fwdx_tc_kernel<5>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    fwdx_tc_kernel<5><<<grid, kXFusedThreads, smem, st>>>(q, static_cast<const unsigned char*>(ximg),
+                                                          static_cast<const unsigned char*>(yimg),
+                                                          static_cast<const float4*>(xinfo),
+                                                          static_cast<const float4*>(yinfo));
+    return cudaGetLastError();
 }
 
 cudaError_t launch_dist_xtc(int P, int N, int M, int D, const void* ximg, const void* yimg, const void* xinfo,
