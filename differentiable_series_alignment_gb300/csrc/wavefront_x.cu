@@ -532,6 +532,9 @@ __global__ void __launch_bounds__(256) oimg_kernel(Problems pr, int N, int M, in
 // 2^k for k in the normal range [-126, 127], exactly.
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
 
+// The scale 2^k (k = e_x + e_y + 2 - 2 DB, the row exponents of two finite rows)
+// as two in-range powers of two: exact, branch-free, for k in [-252, 254]; below,
+// the dot is under 2^-220 and flushes to 0 like any fp32 value that small.
 template <int NS>
 __device__ __forceinline__ dd levels_dd(const float (&S)[NS], int k)
 {
@@ -539,11 +542,10 @@ __device__ __forceinline__ dd levels_dd(const float (&S)[NS], int k)
     dd a = mk(S[NS - 1] * pow2i(-DB * (NS - 1)), 0.f);
 #pragma unroll
     for (int l = NS - 2; l >= 0; --l) a = add(a, mk(S[l] * pow2i(-DB * l), 0.f));
-    if (k >= -126 && k <= 127) {
-        const float f = pow2i(k);
-        return mk(a.hi * f, a.lo * f);
-    }
-    return mk(ldexpf(a.hi, k), ldexpf(a.lo, k));
+    k = min(max(k, -252), 254);
+    const int k1 = k / 2;
+    const float f1 = pow2i(k1), f2 = pow2i(k - k1);
+    return mk(a.hi * f1 * f2, a.lo * f1 * f2);
 }
 
 // Extended fused forward with the exact tensor-core cost tiles. Same recursion,
@@ -729,7 +731,7 @@ __global__ void __launch_bounds__(kXFusedThreads, 1)
             tc::fence_after_sync();
             const float4 yv = yinfo[(size_t)p * Mpad + 32 * c + lane];
             const uint32_t tt0 = tq + (uint32_t)(t * kXSlotCols);
-#pragma unroll
+#pragma unroll 1
             for (int q8 = 0; q8 < 4; ++q8) {   // 8 columns at a time: NS x 8 level sums in registers
                 uint32_t S[NS][8];
 #pragma unroll
