@@ -24,27 +24,41 @@ constexpr int kYS = kKC + 4;
 // ROW_MAJOR: es[r*32 + c]; otherwise es[c*32 + r]. Entries outside the matrix are 0.
 // Returns whether this thread stored a non-zero value: away from the alignment
 // path E underflows to exactly 0, and a tile that is all zero adds nothing.
+// The tile spans 63 skewed rows of 32 lanes; each of the kGradThreads threads
+// issues all of its loads before any store, so a tile costs one memory latency.
+constexpr int kGradThreads = 128;
 template <bool ROW_MAJOR>
 __device__ __forceinline__ bool load_tile(const float* __restrict__ Esk, int N, int M, int p, int rb, int c0,
                                           float* es)
 {
+    constexpr int kIters = (63 * 32 + kGradThreads - 1) / kGradThreads;
     const float* base = Esk + skew_index(N, M, p, rb, 0, 0);
-    bool nz = false;
-    for (int idx = threadIdx.x; idx < 63 * 32; idx += blockDim.x) {
+    float v[kIters];
+#pragma unroll
+    for (int u = 0; u < kIters; ++u) {
+        const int idx = threadIdx.x + u * kGradThreads;
         const int tt = idx >> 5, rr = idx & 31;
         const int c = tt - rr;
-        if (c < 0 || c >= 32) continue;
-        const bool ok = (c0 + c < M) && (rb * 32 + rr < N);
-        const float v = ok ? base[(long long)(c0 + tt) * 32 + rr] : 0.f;
-        nz = nz || (v != 0.f);
-        if (ROW_MAJOR) es[rr * 32 + c] = v;
-        else es[c * 32 + rr] = v;
+        const bool ok = idx < 63 * 32 && c >= 0 && c < 32 && (c0 + c < M) && (rb * 32 + rr < N);
+        v[u] = ok ? base[(long long)(c0 + tt) * 32 + rr] : 0.f;
+    }
+    bool nz = false;
+#pragma unroll
+    for (int u = 0; u < kIters; ++u) {
+        const int idx = threadIdx.x + u * kGradThreads;
+        const int tt = idx >> 5, rr = idx & 31;
+        const int c = tt - rr;
+        if (idx < 63 * 32 && c >= 0 && c < 32) {
+            nz = nz || (v[u] != 0.f);
+            if (ROW_MAJOR) es[rr * 32 + c] = v[u];
+            else es[c * 32 + rr] = v[u];
+        }
     }
     return nz;
 }
 
 // grid (NB, P, ceil(D/64)), block 128.
-__global__ void __launch_bounds__(128) grad_rows_kernel(const GradParams g)
+__global__ void __launch_bounds__(kGradThreads, 4) grad_rows_kernel(const GradParams g)
 {
     __shared__ float es[32 * 32];
     __shared__ __align__(16) float ys[32 * kYS];
@@ -65,9 +79,18 @@ __global__ void __launch_bounds__(128) grad_rows_kernel(const GradParams g)
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
     for (int c0 = 0; c0 < M; c0 += 32) {
         if (!__syncthreads_or(load_tile<false>(g.E, N, M, p, rb, c0, es))) continue;  // an all-zero tile
-        for (int idx = threadIdx.x; idx < 32 * kKC; idx += blockDim.x) {
-            const int c = idx / kKC, kk = idx - c * kKC;
-            ys[c * kYS + kk] = (c0 + c < M && kb + kk < D) ? yb[(size_t)(c0 + c) * D + kb + kk] : 0.f;
+        {   // the tile's 32 y rows, k-slice kb: all loads before the stores
+            float v[32 * kKC / kGradThreads];
+#pragma unroll
+            for (int u = 0; u < 32 * kKC / kGradThreads; ++u) {
+                const int idx = threadIdx.x + u * kGradThreads, c = idx / kKC, kk = idx - c * kKC;
+                v[u] = (c0 + c < M && kb + kk < D) ? yb[(size_t)(c0 + c) * D + kb + kk] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 32 * kKC / kGradThreads; ++u) {
+                const int idx = threadIdx.x + u * kGradThreads, c = idx / kKC, kk = idx - c * kKC;
+                ys[c * kYS + kk] = v[u];
+            }
         }
         __syncthreads();
 #pragma unroll 4
@@ -99,7 +122,7 @@ __global__ void __launch_bounds__(128) grad_rows_kernel(const GradParams g)
 }
 
 // grid (ceil(M/32), P, ceil(D/64)), block 128.
-__global__ void __launch_bounds__(128) grad_cols_kernel(const GradParams g)
+__global__ void __launch_bounds__(kGradThreads, 4) grad_cols_kernel(const GradParams g)
 {
     __shared__ float es[32 * 32];
     __shared__ __align__(16) float xs[32 * kYS];
@@ -121,10 +144,19 @@ __global__ void __launch_bounds__(128) grad_cols_kernel(const GradParams g)
     const int NB = (N + 31) / 32;
     for (int rb = 0; rb < NB; ++rb) {
         if (!__syncthreads_or(load_tile<true>(g.E, N, M, p, rb, c0, es))) continue;  // an all-zero tile
-        for (int idx = threadIdx.x; idx < 32 * kKC; idx += blockDim.x) {
-            const int r = idx / kKC, kk = idx - r * kKC;
-            const int i = rb * 32 + r;
-            xs[r * kYS + kk] = (i < N && kb + kk < D) ? xb[(size_t)i * D + kb + kk] : 0.f;
+        {   // the tile's 32 x rows, k-slice kb: all loads before the stores
+            float v[32 * kKC / kGradThreads];
+#pragma unroll
+            for (int u = 0; u < 32 * kKC / kGradThreads; ++u) {
+                const int idx = threadIdx.x + u * kGradThreads, r = idx / kKC, kk = idx - r * kKC;
+                const int i = rb * 32 + r;
+                v[u] = (i < N && kb + kk < D) ? xb[(size_t)i * D + kb + kk] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 32 * kKC / kGradThreads; ++u) {
+                const int idx = threadIdx.x + u * kGradThreads, r = idx / kKC, kk = idx - r * kKC;
+                xs[r * kYS + kk] = v[u];
+            }
         }
         __syncthreads();
 #pragma unroll 4
@@ -249,14 +281,14 @@ cudaError_t launch_adam_clipped(float* z, float* m, float* v, float* gparts, int
 cudaError_t launch_grad_rows(const GradParams& g, cudaStream_t st)
 {
     dim3 grid((g.N + 31) / 32, g.P, (g.D + kKC - 1) / kKC);
-    grad_rows_kernel<<<grid, 128, 0, st>>>(g);
+    grad_rows_kernel<<<grid, kGradThreads, 0, st>>>(g);
     return cudaGetLastError();
 }
 
 cudaError_t launch_grad_cols(const GradParams& g, cudaStream_t st)
 {
     dim3 grid((g.M + 31) / 32, g.P, (g.D + kKC - 1) / kKC);
-    grad_cols_kernel<<<grid, 128, 0, st>>>(g);
+    grad_cols_kernel<<<grid, kGradThreads, 0, st>>>(g);
     return cudaGetLastError();
 }
 
