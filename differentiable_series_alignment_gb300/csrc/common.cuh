@@ -263,6 +263,33 @@ __device__ __forceinline__ Slot slot_load(const Slot* p) {
     return s;
 }
 
+// Stage rows [row0, row0 + rows) of a row-major (., D) fp32 matrix into shared
+// memory rows of ld floats (columns [0, cols): zero past D and for rows outside
+// [0, rows_valid)), cooperatively over nthreads threads (this one is tid). Each
+// thread issues its loads in batches of 8 before the batch's stores, so a batch
+// costs one memory latency instead of eight.
+__device__ __forceinline__ void stage_rows(float* dst, int ld, const float* src, int D, int row0, int rows,
+                                           int cols, int rows_valid, int tid, int nthreads)
+{
+    const int n = rows * cols;
+    for (int e0 = tid; e0 < n; e0 += 8 * nthreads) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = e0 + u * nthreads;
+            const int r = e / cols, k = e - r * cols;
+            const int row = row0 + r;
+            v[u] = (e < n && row >= 0 && row < rows_valid && k < D) ? src[(size_t)row * D + k] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = e0 + u * nthreads;
+            const int r = e / cols, k = e - r * cols;
+            if (e < n) dst[r * ld + k] = v[u];
+        }
+    }
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -37,20 +37,14 @@ __global__ void __launch_bounds__(32 * kDistWarps) dist_skew_kernel(Problems pr,
     const int r0 = rb * 32;
     const float* xb = pr.x(p);
     const float* yb = pr.y(p);
-    for (int e = threadIdx.x; e < 32 * D32; e += blockDim.x) {
-        const int r = e / D32, k = e - r * D32;
-        xs[r * XS + k] = (r0 + r < N && k < D) ? xb[(size_t)(r0 + r) * D + k] : 0.f;
-    }
+    stage_rows(xs, XS, xb, D, r0, 32, D32, N, threadIdx.x, blockDim.x);
     const int j = c0 + lane;
     float yr[DX > 0 ? DX : 1];
     if constexpr (DX > 0) {
 #pragma unroll
         for (int k = 0; k < DX; ++k) yr[k] = (j < M && k < D) ? yb[(size_t)j * D + k] : 0.f;
     } else {
-        for (int e = lane; e < 32 * D32; e += 32) {
-            const int r = e / D32, k = e - r * D32;
-            yw[r * XS + k] = (c0 + r < M && k < D) ? yb[(size_t)(c0 + r) * D + k] : 0.f;
-        }
+        stage_rows(yw, XS, yb, D, c0, 32, D32, M, lane, 32);
     }
     __syncthreads();
     if (c0 < M) {

@@ -118,15 +118,8 @@ __global__ void __launch_bounds__(256) distx_kernel(Problems pr, int N, int M, i
     const int r0 = rb * 32, jbase = t0 - 31;
     const float* xb = pr.x(p);
     const float* yb = pr.y(p);
-    for (int e = threadIdx.x; e < 32 * D; e += blockDim.x) {
-        const int r = e / D, k = e - r * D;
-        xs[r * XS + k] = (r0 + r < N) ? xb[(size_t)(r0 + r) * D + k] : 0.f;
-    }
-    for (int e = threadIdx.x; e < 95 * D; e += blockDim.x) {
-        const int r = e / D, k = e - r * D;
-        const int j = jbase + r;
-        ys[r * XS + k] = (j >= 0 && j < M) ? yb[(size_t)j * D + k] : 0.f;
-    }
+    stage_rows(xs, XS, xb, D, r0, 32, D, N, threadIdx.x, blockDim.x);
+    stage_rows(ys, XS, yb, D, jbase, 95, D, M, threadIdx.x, blockDim.x);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tw = t0 + warp * 8;

@@ -703,3 +703,34 @@ def test_validation_errors_raise():
     with pytest.raises(L.SdtwError) as e:
         L.sdtw_forward(x, x, 1.0, 0, loss, ws[:100])
     assert e.value.code == 5
+
+
+# The library's calls can be captured into a CUDA graph (the timed step of the
+# benchmark replays one): launches, memsets and the side-stream forks and joins of a
+# forward + backward, replayed, give the eager results bit for bit.
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 5])
+def test_graph_capture_replays_the_eager_results(mode):
+    L = _lib()
+    x, y = synth.iid_normal_pair(4, 150, 130, 16, 107)
+    xt, yt = torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda()
+    ws = L.workspace(L.OP_FWD_BWD, 4, 150, 130, 16, mode)
+    g = torch.tensor(mean_weights(4), dtype=torch.float32, device="cuda")
+    loss, gx, gy = torch.empty(4, device="cuda"), torch.empty_like(xt), torch.empty_like(yt)
+
+    def fwd_bwd():
+        L.sdtw_forward(xt, yt, 0.8, mode, loss, ws)
+        L.sdtw_backward(xt, yt, 0.8, mode, g, gx, gy, ws)
+
+    fwd_bwd()
+    assert L.sdtw_last_device_status(ws) == 0
+    ref = [t.clone() for t in (loss, gx, gy)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fwd_bwd()
+    for t in (loss, gx, gy):
+        t.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert L.sdtw_last_device_status(ws) == 0
+    for a, b in zip((loss, gx, gy), ref):
+        assert torch.equal(a, b)
