@@ -39,6 +39,7 @@ struct Layout {
     size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, gnorm, bimg, bimg2, total;
     size_t ximg, yimg, xnorm, ynorm;  // tensor-core cost operands (tc_cost, or xtc: digit images and row info)
     size_t band_slots;                // checkpointed mode: skewed slots of one band of every problem
+    size_t ebnd;                      // extended mode: non-zero column range of E per 32-row block
     bool tc_cost;
     bool xtc;    // extended mode with exact tensor-core costs (fused D <= kMaxXtcD, unfused D <= kMaxXtcUD)
     bool ckpt;   // checkpointed fused mode: VH / E hold two bands, the [X | 1] image one
@@ -95,6 +96,7 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->dsk = o; if (!fused) o = align_up(o + (ext ? sizeof(float2) : sizeof(float)) * slots);
     L->gparts = o; if (op == SDTW_OP_BARYCENTER) o = align_up(o + sizeof(float) * (size_t)P * N * D);
     L->gnorm = o; if (op == SDTW_OP_BARYCENTER) o = align_up(o + sizeof(float) * (((size_t)N * D + 255) / 256));
+    L->ebnd = o; if (ext && op != SDTW_OP_COST) o = align_up(o + sizeof(int2) * (size_t)P * NB);
     // gradient operand images (one batch of B problems at a time): [Y | 1] and [X | 1]
     const bool xy = op != SDTW_OP_COST;  // the path has x and y (and input gradients)
     L->bimg = o; if (!ext && xy) o = align_up(o + egemm_bimg_bytes(op == SDTW_OP_NORMALIZED ? B : P, M, D));
@@ -571,6 +573,11 @@ sdtw_status run_grads(const Problems& all, int set, int B, const Layout& L, void
     float* img_cols = at<float>(ws, L.bimg2);
     if (!simt && images_ready) SDTW_CUDA(cudaStreamWaitEvent(st, images_ready, 0));
     else if (!simt) SDTW_CUDA(launch_bimg(g, out_x ? img_rows : nullptr, out_y ? img_cols : nullptr, st));
+    if (simt) {   // the difference-form contractions visit only the tiles where E is non-zero
+        int2* bounds = at<int2>(ws, L.ebnd) + (size_t)set * B * L.NB;
+        SDTW_CUDA(launch_ebounds(g, bounds, st));
+        g.bounds = bounds;
+    }
     if (out_x) {
         g.out = out_x;
         g.out_stride = (long long)L.N * L.D;

@@ -57,6 +57,53 @@ __device__ __forceinline__ bool load_tile(const float* __restrict__ Esk, int N, 
     return nz;
 }
 
+// Column range of the non-zero E of each 32-row block: away from the alignment path
+// E underflows to exactly 0, so the contractions below need only the tiles between
+// the first and the last non-zero column of a row block. One warp scans kBoundSeg
+// skewed rows of one block (its loads in batches of 8); atomics combine the segments.
+constexpr int kBoundSeg = 512;
+__global__ void ebounds_init_kernel(int2* b, int n)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) b[i] = make_int2(0x7fffffff, -1);
+}
+
+// grid (ceil(NB/8), P, ceil(T/kBoundSeg)), block 256.
+__global__ void __launch_bounds__(256) ebounds_kernel(const float* __restrict__ Esk, int N, int M, int2* bounds)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NB = (N + 31) / 32, T = skew_T(M);
+    const int rb = blockIdx.x * 8 + warp, p = blockIdx.y;
+    if (rb >= NB) return;
+    const int t0 = blockIdx.z * kBoundSeg, t1 = min(T, t0 + kBoundSeg);
+    const bool row_ok = rb * 32 + lane < N;
+    const float* base = Esk + skew_index(N, M, p, rb, 0, lane);
+    int lo = 0x7fffffff, hi = -1;
+    for (int t = t0; t < t1; t += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = (t + u < t1) ? base[(long long)(t + u) * 32] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = t + u - lane;
+            if (v[u] != 0.f && row_ok && j >= 0 && j < M) {
+                lo = min(lo, j);
+                hi = max(hi, j);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0 && hi >= 0) {
+        int* b = reinterpret_cast<int*>(bounds + (size_t)p * NB + rb);
+        atomicMin(b, lo);
+        atomicMax(b + 1, hi);
+    }
+}
+
 // grid (NB, P, ceil(D/64)), block 128.
 __global__ void __launch_bounds__(kGradThreads, 4) grad_rows_kernel(const GradParams g)
 {
@@ -77,7 +124,13 @@ __global__ void __launch_bounds__(kGradThreads, 4) grad_rows_kernel(const GradPa
     float acc[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-    for (int c0 = 0; c0 < M; c0 += 32) {
+    int c_first = 0, c_last = M - 1;   // the block's non-zero columns (CTA-uniform)
+    if (g.bounds) {
+        const int2 bb = g.bounds[(size_t)p * ((N + 31) / 32) + rb];
+        c_first = bb.x & ~31;
+        c_last = bb.y;
+    }
+    for (int c0 = c_first; c0 <= c_last; c0 += 32) {
         if (!__syncthreads_or(load_tile<false>(g.E, N, M, p, rb, c0, es))) continue;  // an all-zero tile
         {   // the tile's 32 y rows, k-slice kb: all loads before the stores
             float v[32 * kKC / kGradThreads];
@@ -142,7 +195,18 @@ __global__ void __launch_bounds__(kGradThreads, 4) grad_cols_kernel(const GradPa
 #pragma unroll
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
     const int NB = (N + 31) / 32;
+    __shared__ int2 s_bnd[kGradThreads];   // the bounds of the next kGradThreads row blocks
     for (int rb = 0; rb < NB; ++rb) {
+        if (g.bounds) {   // row blocks whose non-zero columns miss this column tile add nothing
+            if ((rb % kGradThreads) == 0) {
+                __syncthreads();
+                const int r = rb + (int)threadIdx.x;
+                s_bnd[threadIdx.x] = r < NB ? g.bounds[(size_t)p * NB + r] : make_int2(0x7fffffff, -1);
+                __syncthreads();
+            }
+            const int2 bb = s_bnd[rb % kGradThreads];
+            if (bb.y < c0 || bb.x > c0 + 31) continue;   // CTA-uniform
+        }
         if (!__syncthreads_or(load_tile<true>(g.E, N, M, p, rb, c0, es))) continue;  // an all-zero tile
         {   // the tile's 32 x rows, k-slice kb: all loads before the stores
             float v[32 * kKC / kGradThreads];
@@ -282,6 +346,15 @@ cudaError_t launch_grad_rows(const GradParams& g, cudaStream_t st)
 {
     dim3 grid((g.N + 31) / 32, g.P, (g.D + kKC - 1) / kKC);
     grad_rows_kernel<<<grid, kGradThreads, 0, st>>>(g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ebounds(const GradParams& g, int2* bounds, cudaStream_t st)
+{
+    const int NB = (g.N + 31) / 32, n = g.P * NB;
+    ebounds_init_kernel<<<(n + 255) / 256, 256, 0, st>>>(bounds, n);
+    dim3 grid((NB + 7) / 8, g.P, (skew_T(g.M) + kBoundSeg - 1) / kBoundSeg);
+    ebounds_kernel<<<grid, 256, 0, st>>>(g.E, g.N, g.M, bounds);
     return cudaGetLastError();
 }
 

@@ -93,8 +93,14 @@ struct GradParams {
     long long out_stride;
     int omod;
     int accumulate;
+    // per problem and 32-row block, the column range [x, y] where E may be non-zero
+    // (launch_ebounds); null: every column
+    const int2* bounds;
 };
 cudaError_t launch_grad_rows(const GradParams& g, cudaStream_t st);
+// The column ranges of GradParams::bounds for the g.P problems of g.E (difference-form
+// contractions visit only the tiles inside them).
+cudaError_t launch_ebounds(const GradParams& g, int2* bounds, cudaStream_t st);
 // The same contractions on the tensor cores (tcgen05, 3xTF32); cols selects grad_y.
 // Pre-split B operand images: [Y | 1] into img_rows (for grad_x) and [X | 1]
 // into img_cols (for grad_y), one launch; a null pointer skips that image.
