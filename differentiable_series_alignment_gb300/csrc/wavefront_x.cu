@@ -836,41 +836,47 @@ __global__ void __launch_bounds__(kXFusedThreads, 1)
                 }
                 if (!ok) break;
 
-                // the group's 16 costs into registers before any of its stores (the
-                // compiler keeps loads behind stores it cannot prove apart)
-                float2 dc[kGroup];
+                // the group in two halves of 8 steps (rolled: the unrolled step is long, and
+                // nine warps' code shares the instruction cache); each half's costs go into
+                // registers before any of its stores (the compiler keeps loads behind stores
+                // it cannot prove apart)
                 int col = (s0 - lane + rcols) % rcols;   // column s0 - lane >= -31 in the ring
+#pragma unroll 1
+                for (int h8 = 0; h8 < kGroup; h8 += 8) {
+                    float2 dc[8];
 #pragma unroll
-                for (int u = 0; u < kGroup; ++u) {
-                    dc[u] = make_float2(dh[col * 32 + lane], dl[col * 32 + lane]);
-                    col = (col + 1 == rcols) ? 0 : col + 1;
-                }
-#pragma unroll
-                for (int u = 0; u < kGroup; ++u) {
-                    const int s = s0 + u;
-                    const int j = s - lane;
-                    const float hs_hi = __shfl_up_sync(kFull, h_prev.hi, 1);
-                    const float hs_lo = __shfl_up_sync(kFull, h_prev.lo, 1);
-                    const float tv_hi = __shfl_sync(kFull, topv.hi, u);
-                    const float tv_lo = __shfl_sync(kFull, topv.lo, u);
-                    const dd hu = (lane == 0) ? mk(tv_hi, tv_lo) : mk(hs_hi, hs_lo);
-                    const dd vl = v_prev;
-                    const dd d = scale_dd(mk(dc[u].x, dc[u].y), scale);
-                    const bool col0 = (j == 0);
-                    dd h, v;
-                    float4 lp;
-                    xcell(d, vl, hu, col0, row0_lane, h, v, lp);
-                    c0 = col0 ? d : c0;
-                    lpp[(long long)s * 32] = lp;
-                    const bool valid = (unsigned)j < (unsigned)M;
-                    if (chan_lane && valid) {
-                        Slot* dst = chan_out + 2 * (j & chan_mask);
-                        slot_store(dst, h.hi, (unsigned)(j + 1));
-                        slot_store(dst + 1, h.lo, (unsigned)(j + 1));
+                    for (int uu = 0; uu < 8; ++uu) {
+                        dc[uu] = make_float2(dh[col * 32 + lane], dl[col * 32 + lane]);
+                        col = (col + 1 == rcols) ? 0 : col + 1;
                     }
-                    if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = make_float2(h.hi, h.lo);
-                    h_prev = h;
-                    v_prev = v;
+#pragma unroll
+                    for (int uu = 0; uu < 8; ++uu) {
+                        const int u = h8 + uu;
+                        const int s = s0 + u;
+                        const int j = s - lane;
+                        const float hs_hi = __shfl_up_sync(kFull, h_prev.hi, 1);
+                        const float hs_lo = __shfl_up_sync(kFull, h_prev.lo, 1);
+                        const float tv_hi = __shfl_sync(kFull, topv.hi, u);
+                        const float tv_lo = __shfl_sync(kFull, topv.lo, u);
+                        const dd hu = (lane == 0) ? mk(tv_hi, tv_lo) : mk(hs_hi, hs_lo);
+                        const dd vl = v_prev;
+                        const dd d = scale_dd(mk(dc[uu].x, dc[uu].y), scale);
+                        const bool col0 = (j == 0);
+                        dd h, v;
+                        float4 lp;
+                        xcell(d, vl, hu, col0, row0_lane, h, v, lp);
+                        c0 = col0 ? d : c0;
+                        lpp[(long long)s * 32] = lp;
+                        const bool valid = (unsigned)j < (unsigned)M;
+                        if (chan_lane && valid) {
+                            Slot* dst = chan_out + 2 * (j & chan_mask);
+                            slot_store(dst, h.hi, (unsigned)(j + 1));
+                            slot_store(dst + 1, h.lo, (unsigned)(j + 1));
+                        }
+                        if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = make_float2(h.hi, h.lo);
+                        h_prev = h;
+                        v_prev = v;
+                    }
                 }
                 if (has_top && !top_global && lane == 0) cons[warp - 1] = min(s0 + kGroup, M);
             }
