@@ -66,6 +66,16 @@ __device__ __forceinline__ dd scale_dd(dd d, float k) {
     return fast2(p, fmaf(d.lo, k, pe));
 }
 
+// The double-float forwards run a 16-step group as short chunks in a rolled loop:
+// the unrolled double-float step is long, and a fully unrolled group misses the
+// instruction cache. Measured on the fused forward (nine warps of three roles) at
+// 16 / 8 / 4 / 2 steps per chunk: 1.20 / 0.62 / 0.42 / 0.40 ms at the 32 x 512^2
+// headline shape, 52 / 21 / 14.6 / 10.6 ms at 8 x 8192^2. The unfused forward takes
+// its chunk's costs by selects among the group's registers, which grow with the
+// chunk count: 4 steps there (8192^2: 14.5 ms at 4, 15.4 at 2).
+constexpr int kXChunkFused = 2;
+constexpr int kXChunk = 4;
+
 // One cell of the double-float recursion: d the scaled cost, vl = v[i,j-1] and
 // hu = h[i-1,j] the incoming differences (relative to the diagonal predecessor).
 // Gives h, v and the three transition log2-probabilities to the diag, left and up
@@ -295,32 +305,41 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
                     dc[u] = dp[(long long)(s0 + u) * 32];
                 }
             }
+            // rolled chunks of kXChunk steps; a chunk takes its costs from dc by selects
+            // between fixed indices, so dc stays in registers
+#pragma unroll 1
+            for (int h8 = 0; h8 < kGroup; h8 += kXChunk) {
 #pragma unroll
-            for (int u = 0; u < kGroup; ++u) {
-                const int s = s0 + u;
-                const int j = s - lane;
-                const float hs_hi = __shfl_up_sync(kFull, h_prev.hi, 1);
-                const float hs_lo = __shfl_up_sync(kFull, h_prev.lo, 1);
-                const float tv_hi = __shfl_sync(kFull, topv.hi, u);
-                const float tv_lo = __shfl_sync(kFull, topv.lo, u);
-                const dd hu = (lane == 0) ? mk(tv_hi, tv_lo) : mk(hs_hi, hs_lo);
-                const dd vl = v_prev;
-                const dd d = scale_dd(mk(dc[u].x, dc[u].y), scale);
-                const bool col0 = (j == 0);
-                dd h, v;
-                float4 lp;
-                xcell(d, vl, hu, col0, row0_lane, h, v, lp);
-                c0 = col0 ? d : c0;
-                lpp[(long long)s * 32] = lp;
-                const bool valid = (unsigned)j < (unsigned)M;
-                if (chan_lane && valid) {
-                    Slot* dst = chan_out + 2 * (j & chan_mask);
-                    slot_store(dst, h.hi, (unsigned)(j + 1));
-                    slot_store(dst + 1, h.lo, (unsigned)(j + 1));
+                for (int uu = 0; uu < kXChunk; ++uu) {
+                    const int u = h8 + uu;
+                    const int s = s0 + u;
+                    const int j = s - lane;
+                    const float hs_hi = __shfl_up_sync(kFull, h_prev.hi, 1);
+                    const float hs_lo = __shfl_up_sync(kFull, h_prev.lo, 1);
+                    const float tv_hi = __shfl_sync(kFull, topv.hi, u);
+                    const float tv_lo = __shfl_sync(kFull, topv.lo, u);
+                    const dd hu = (lane == 0) ? mk(tv_hi, tv_lo) : mk(hs_hi, hs_lo);
+                    const dd vl = v_prev;
+                    float2 cu = dc[uu];
+#pragma unroll
+                    for (int q = 1; q < kGroup / kXChunk; ++q) cu = (h8 == q * kXChunk) ? dc[uu + q * kXChunk] : cu;
+                    const dd d = scale_dd(mk(cu.x, cu.y), scale);
+                    const bool col0 = (j == 0);
+                    dd h, v;
+                    float4 lp;
+                    xcell(d, vl, hu, col0, row0_lane, h, v, lp);
+                    c0 = col0 ? d : c0;
+                    lpp[(long long)s * 32] = lp;
+                    const bool valid = (unsigned)j < (unsigned)M;
+                    if (chan_lane && valid) {
+                        Slot* dst = chan_out + 2 * (j & chan_mask);
+                        slot_store(dst, h.hi, (unsigned)(j + 1));
+                        slot_store(dst + 1, h.lo, (unsigned)(j + 1));
+                    }
+                    if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = make_float2(h.hi, h.lo);
+                    h_prev = h;
+                    v_prev = v;
                 }
-                if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = make_float2(h.hi, h.lo);
-                h_prev = h;
-                v_prev = v;
             }
             if (has_top && !top_global && lane == 0) cons[warp - 1] = min(s0 + kGroup, M);
         }
@@ -836,21 +855,20 @@ __global__ void __launch_bounds__(kXFusedThreads, 1)
                 }
                 if (!ok) break;
 
-                // the group in two halves of 8 steps (rolled: the unrolled step is long, and
-                // nine warps' code shares the instruction cache); each half's costs go into
-                // registers before any of its stores (the compiler keeps loads behind stores
-                // it cannot prove apart)
+                // the group in rolled chunks of kXChunkFused steps (nine warps' code shares the
+                // instruction cache); each chunk's costs go into registers before any of its
+                // stores (the compiler keeps loads behind stores it cannot prove apart)
                 int col = (s0 - lane + rcols) % rcols;   // column s0 - lane >= -31 in the ring
 #pragma unroll 1
-                for (int h8 = 0; h8 < kGroup; h8 += 8) {
-                    float2 dc[8];
+                for (int h8 = 0; h8 < kGroup; h8 += kXChunkFused) {
+                    float2 dc[kXChunkFused];
 #pragma unroll
-                    for (int uu = 0; uu < 8; ++uu) {
+                    for (int uu = 0; uu < kXChunkFused; ++uu) {
                         dc[uu] = make_float2(dh[col * 32 + lane], dl[col * 32 + lane]);
                         col = (col + 1 == rcols) ? 0 : col + 1;
                     }
 #pragma unroll
-                    for (int uu = 0; uu < 8; ++uu) {
+                    for (int uu = 0; uu < kXChunkFused; ++uu) {
                         const int u = h8 + uu;
                         const int s = s0 + u;
                         const int j = s - lane;
