@@ -41,7 +41,7 @@ struct Layout {
     size_t band_slots;                // checkpointed mode: skewed slots of one band of every problem
     size_t ebnd;                      // extended mode: non-zero column range of E per 32-row block
     bool tc_cost;
-    bool xtc;    // extended mode with exact tensor-core costs (fused D <= kMaxXtcD, unfused D <= kMaxXtcUD)
+    bool xtc;    // extended mode with exact tensor-core costs (D <= kMaxXtcD)
     bool ckpt;   // checkpointed fused mode: VH / E hold two bands, the [X | 1] image one
     int P, N, M, D, NB;
 };
@@ -107,7 +107,7 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->tc_cost = !ext && D <= kTcKFeat * kMaxTcKBlocks && xy;
     // the extended modes' exact tensor-core costs (the fused forward's cost tiles, the
     // unfused cost tensor): fixed-point digit images and row info
-    L->xtc = ext && xy && D <= (fused ? kMaxXtcD : kMaxXtcUD);
+    L->xtc = ext && xy && D <= kMaxXtcD;
     L->ximg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, N, D));
     if (L->xtc) o = align_up(o + oimg_bytes(P, N, D));
     L->yimg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, M, D));

@@ -137,8 +137,7 @@ cudaError_t launch_dist_tc(int P, int N, int M, int D, const void* ximg, const v
 // (5 up to D = 128, 6 above), each Lpad rows of 128 bytes
 // (swizzled as the bf16 images above); per row the info (norm hi, norm lo, scale
 // exponent as int bits, 0).
-constexpr int kMaxXtcD = 128;    // the fused forward's cost tiles (five digits)
-constexpr int kMaxXtcUD = 400;   // the unfused cost tensor (six digits above D = 128)
+constexpr int kMaxXtcD = 400;    // exact tensor-core costs, both modes (six digits above D = 128)
 int xtc_slices(int D);
 __host__ __device__ inline size_t oimg_offset(int p, int KB, int kb, int NS, int slice, int Lpad, int r)
 {
@@ -148,11 +147,11 @@ size_t oimg_bytes(int P, int L, int D);
 size_t oinfo_bytes(int P, int L);
 cudaError_t launch_oimg(const Problems& pr, int P, int N, int M, int D, void* ximg, void* yimg, void* xinfo,
                         void* yinfo, cudaStream_t st);
-// Extended unfused cost tensor from the exact tensor-core level sums (D <= kMaxXtcUD):
+// Extended unfused cost tensor from the exact tensor-core level sums (D <= kMaxXtcD):
 // raw double-float costs (hi, lo) in the skewed layout.
 cudaError_t launch_dist_xtc(int P, int N, int M, int D, const void* ximg, const void* yimg, const void* xinfo,
                             const void* yinfo, float2* Dsk, int* status, cudaStream_t st);
-// Extended fused forward with exact tensor-core cost tiles: q.W must be 4.
+// Extended fused forward with exact tensor-core cost tiles (D <= kMaxXtcD): q.W must be 4.
 cudaError_t launch_forward_xtc(WaveParams q, const void* ximg, const void* yimg, const void* xinfo,
                                const void* yinfo, cudaStream_t st);
 

@@ -577,10 +577,12 @@ __device__ __forceinline__ dd levels_dd(const float (&S)[NS], int k)
 // every tile, with no slack (three tiles of five levels fill the tensor memory).
 // With converters a tile waits on DP progress only for ring room. The rings hold
 // 3, 3, 3, 4 tiles (warps 0-3): a converter can fill tile c + 1 while its DP warp
-// runs period c (which reads tiles c - 1 and c), and the tile warp 0 needs at step
-// 32 c waits on warps 1-3 having finished periods c - 5, c - 5 and c - 6 (warp 0
-// near step 32 c - 66 at the latest). The conversion also leaves the DP warps'
-// critical path.
+// runs period c (which reads tiles c - 1 and c). With three tensor-memory tiles (five
+// digits) the tile warp 0 needs at step 32 c waits on warps 1-3 having finished
+// periods c - 5, c - 5 and c - 6 (warp 0 near step 32 c - 66 at the latest); with two
+// (six digits, 192 columns each) on periods c - 4, c - 4 and c - 5 (near step
+// 32 c - 34). The conversion also leaves the DP warps' critical path. Six digits
+// stage the x digits of a K-block in two fills of three (72 KB with the y digits).
 //
 // Hand-offs (every wait bounded):
 //   s_a                      x digits resident
@@ -603,9 +605,11 @@ __global__ void __launch_bounds__(kXFusedThreads, 1)
 {
     using X = XDigits<NS>;
     // three tiles of five levels (160 columns each) fill the 512 tensor-memory columns
-    static_assert(NS == 5, "five digits: three cost tiles in tensor memory");
-    constexpr int kXRT = 3, kXSlotCols = X::SlotCols, kXSlices = NS;
-    constexpr uint32_t kXA = X::A, kXB = X::B;
+    // five digits: three tiles of 160 TMEM columns, all x digits of a K-block in one
+    // fill; six digits: two tiles of 192 columns, x digits in two fills of three
+    constexpr int kXRT = NS == 5 ? 3 : 2, kXSlotCols = X::SlotCols, kXSlices = NS;
+    constexpr int kAH = NS == 5 ? 5 : 3, kH = NS / kAH;       // x digits per fill, fills per K-block
+    constexpr uint32_t kXA = X::A, kXAH = kAH * kXAPart, kXB = X::B;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     constexpr int W = kXDpWarps;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -631,14 +635,14 @@ __global__ void __launch_bounds__(kXFusedThreads, 1)
     const int p = tk % q.P, strip = tk / q.P;
     const int N = q.N, M = q.M, T = skew_T(M);
     const int KB = (q.D + kTcKFeat - 1) / kTcKFeat;
-    const bool resident = KB == 1;   // one K-block: the x digits stay in shared memory
+    const bool resident = KB == 1 && kH == 1;   // one K-block (five digits): the x digits stay in shared memory
     const int Npad = simg_pad(N), Mpad = simg_pad(M);
     const int rs0 = strip * W * 32;
     const int nT = (M + 31) / 32;
 
     unsigned char* tcb = smem_raw + q.smem_fixed;
     unsigned char* stage = tcb + ((1024u - (tc::smem_u32(tcb) & 1023u)) & 1023u);   // [x digits | y digits]
-    float* rings = reinterpret_cast<float*>(stage + kXA + kXB);                    // cost rings of the DP warps
+    float* rings = reinterpret_cast<float*>(stage + kXAH + kXB);                   // cost rings of the DP warps
 
     if (threadIdx.x == 0) {
         tc::mbar_init(tc::smem_u32(&s_a), 1);
@@ -662,13 +666,16 @@ __global__ void __launch_bounds__(kXFusedThreads, 1)
     dd c0 = zero;  // scaled d(i, 0)
     bool active = false;
 
-    // the level MMAs of one 16-wide K step: x digit l against the stacked y digits
-    // [b_0 ; ... ; b_(NS-1-l)], into the level columns l .. NS-1
-    auto level_mmas = [&](uint32_t d0, uint32_t a, uint32_t b, uint32_t ko, bool acc0) {
+    // the level MMAs of one 16-wide K step for x digits l0 .. l0 + kAH - 1 (staged from
+    // a): digit l against the stacked y digits [b_0 ; ... ; b_(NS-1-l)], into the level
+    // columns l .. NS-1
+    auto level_mmas = [&](uint32_t d0, uint32_t a, uint32_t b, uint32_t ko, int l0, bool acc0) {
 #pragma unroll
-        for (int l = 0; l < kXSlices; ++l)
-            tc::mma_bf16(d0 + (uint32_t)(l * 32), tc::sdesc(a + l * kXAPart + ko), tc::sdesc(b + ko),
+        for (int la = 0; la < kAH; ++la) {
+            const int l = l0 + la;
+            tc::mma_bf16(d0 + (uint32_t)(l * 32), tc::sdesc(a + la * kXAPart + ko), tc::sdesc(b + ko),
                          tc::idesc_bf16(128, (kXSlices - l) * 32), (acc0 || l > 0) ? 1u : 0u);
+        }
     };
 
     if (warp == kXIssuer) {
@@ -683,35 +690,38 @@ __global__ void __launch_bounds__(kXFusedThreads, 1)
                                  kXAPart, abar);
                 tc::wait_ok_sleep(ok, abar, 0u, status);
             }
-            // stage fill g = c * KB + kb: y tile c's digits of K-block kb (and, streamed,
-            // the x digits of that K-block), once the MMAs of fill g - 1 have read the stage
-            const int G = nT * KB;
+            // stage fill g = (c * KB + kb) * kH + h: y tile c's digits of K-block kb (with
+            // h = 0) and, streamed, x digits h kAH .. h kAH + kAH - 1 of that K-block, once
+            // the MMAs of fill g - 1 have read the stage
+            const int G = nT * KB * kH;
             for (int g = 0; g < G && ok; ++g) {
-                const int c = g / KB, kb = g - c * KB, t = c % kXRT;
+                const int c = g / (KB * kH), r = g - c * KB * kH, kb = r / kH, h = r - kb * kH;
+                const int t = c % kXRT;
                 if (g >= 1) tc::wait_ok_sleep(ok, tc::smem_u32(&s_sempty), (uint32_t)((g - 1) & 1), status);
                 if (!ok) break;
                 const uint32_t bar = tc::smem_u32(&s_sfull);
-                tc::mbar_expect_tx(bar, resident ? kXB : kXA + kXB);
+                tc::mbar_expect_tx(bar, (resident ? 0u : kXAH) + (h == 0 ? kXB : 0u));
                 if (!resident)
+                    for (int la = 0; la < kAH; ++la)
+                        tc::bulk_g2s(tc::smem_u32(stage + la * kXAPart),
+                                     ximg + oimg_offset(p, KB, kb, NS, h * kAH + la, Npad, rs0), kXAPart, bar);
+                if (h == 0)
                     for (int l = 0; l < kXSlices; ++l)
-                        tc::bulk_g2s(tc::smem_u32(stage + l * kXAPart),
-                                     ximg + oimg_offset(p, KB, kb, NS, l, Npad, rs0), kXAPart, bar);
-                for (int l = 0; l < kXSlices; ++l)
-                    tc::bulk_g2s(tc::smem_u32(stage + kXA + l * kXBPart),
-                                 yimg + oimg_offset(p, KB, kb, NS, l, Mpad, 32 * c), kXBPart, bar);
+                        tc::bulk_g2s(tc::smem_u32(stage + kXAH + l * kXBPart),
+                                     yimg + oimg_offset(p, KB, kb, NS, l, Mpad, 32 * c), kXBPart, bar);
                 issued = g;
-                if (kb == 0 && c >= kXRT)   // TMEM tile t free: the converters have read tile c - 3
+                if (kb == 0 && h == 0 && c >= kXRT)   // TMEM tile t free: the converters have read tile c - kXRT
                     tc::wait_ok_sleep(ok, tc::smem_u32(&s_tfree[t]), (uint32_t)(((c - kXRT) / kXRT) & 1), status);
                 tc::wait_ok_sleep(ok, bar, (uint32_t)(g & 1), status);
                 if (!ok) break;
                 landed = g;
                 tc::fence_after_sync();
                 const uint32_t d0 = tmem + (uint32_t)(t * kXSlotCols);
-                const uint32_t a = tc::smem_u32(stage), b = a + kXA;
+                const uint32_t a = tc::smem_u32(stage), b = a + kXAH;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) level_mmas(d0, a, b, ks * 32, kb > 0 || ks > 0);
+                for (int ks = 0; ks < 4; ++ks) level_mmas(d0, a, b, ks * 32, h * kAH, kb > 0 || ks > 0);
                 tc::mma_commit(tc::smem_u32(&s_sempty));
-                if (kb == KB - 1) tc::mma_commit(tc::smem_u32(&s_tfull[t]));
+                if (kb == KB - 1 && h == kH - 1) tc::mma_commit(tc::smem_u32(&s_tfull[t]));
             }
             // every MMA has completed before tensor memory is released, and no copy is
             // still writing shared memory when the CTA exits
@@ -1189,21 +1199,25 @@ cudaError_t launch_forward_xtc(WaveParams q, const void* ximg, const void* yimg,
     const int grid = q.P * q.S;
     q.smem_fixed = (int)(((size_t)kXDpWarps * kRing * 2 * sizeof(Slot) + (size_t)kXDpWarps * sizeof(int) + 15) &
                          ~(size_t)15);
-    const size_t need = q.smem_fixed + 1024 + XDigits<5>::A + XDigits<5>::B + kXRingBytes;
-    const size_t smem = max(need, wave_smem_floor());   // one CTA per SM: the whole tensor memory
-    cudaError_t e = cudaFuncSetAttribute(fwdx_tc_kernel<5>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    fwdx_tc_kernel<5><<<grid, kXFusedThreads, smem, st>>>(q, static_cast<const unsigned char*>(ximg),
-                                                          static_cast<const unsigned char*>(yimg),
-                                                          static_cast<const float4*>(xinfo),
-                                                          static_cast<const float4*>(yinfo));
-    return cudaGetLastError();
+    auto go = [&](auto kern, size_t stage) -> cudaError_t {
+        const size_t need = q.smem_fixed + 1024 + stage + kXRingBytes;
+        const size_t smem = max(need, wave_smem_floor());   // one CTA per SM: the whole tensor memory
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kXFusedThreads, smem, st>>>(q, static_cast<const unsigned char*>(ximg),
+                                                 static_cast<const unsigned char*>(yimg),
+                                                 static_cast<const float4*>(xinfo), static_cast<const float4*>(yinfo));
+        return cudaGetLastError();
+    };
+    // the stage: all five x digits of a K-block, or three of six, and the y tile's digits
+    return xtc_slices(q.D) == 5 ? go(fwdx_tc_kernel<5>, XDigits<5>::A + XDigits<5>::B)
+                                : go(fwdx_tc_kernel<6>, 3 * kXAPart + XDigits<6>::B);
 }
 
 cudaError_t launch_dist_xtc(int P, int N, int M, int D, const void* ximg, const void* yimg, const void* xinfo,
                             const void* yinfo, float2* Dsk, int* status, cudaStream_t st)
 {
-    if (D < 1 || D > kMaxXtcUD) return cudaErrorInvalidValue;
+    if (D < 1 || D > kMaxXtcD) return cudaErrorInvalidValue;
     const int KB = (D + kTcKFeat - 1) / kTcKFeat;
     const int NS = xtc_slices(D);
     const size_t smem = 1024 + xtc_region(NS, KB) + (size_t)kXdWarps * kXdStg * sizeof(float2);

@@ -64,7 +64,7 @@ def test_workspace_sizes(lib):
     # extended precision: 16-byte log-probabilities instead of 8-byte pairs; unfused
     # also stores the double-float cost (8 bytes). Both modes carry the exact
     # tensor-core costs' digit images (five bf16 slices per K-block of 64 up to
-    # D = 128, six above) and row info: fused up to D = 128, unfused up to D = 400
+    # D = 128, six above, up to D = 400) and row info
     fx = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.FUSED | L.EXTENDED)
     ux = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 64, L.UNFUSED | L.EXTENDED)
     oimg = 2 * (32 * 1 * 5 * 512 * 128) + 2 * (32 * 512 * 16)
@@ -72,7 +72,7 @@ def test_workspace_sizes(lib):
     fx256 = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 256, L.FUSED | L.EXTENDED)
     ux256 = L.sdtw_workspace_bytes(L.OP_FWD_BWD, 32, 512, 512, 256, L.UNFUSED | L.EXTENDED)
     oimg256 = 2 * (32 * 4 * 6 * 512 * 128) + 2 * (32 * 512 * 16)
-    assert ux256 - fx256 >= slots * 8 + oimg256
+    assert ux256 - fx256 >= slots * 8 and fx256 >= slots * (16 + 4) + oimg256
 
 
 def _fwd(lib, x=0x1000, y=0x2000, B=2, N=3, M=4, D=2, gamma=1.0, mode=0, loss=0x3000, ws=0x100000,

@@ -167,19 +167,17 @@ def test_extended_precision_shapes(mname, mode, N, M, D):
 
 
 # The extended modes take their double-float costs from exact tensor-core level
-# sums (fixed-point digits, integer level sums): the fused forward's cost tiles up
-# to D = 128 (five 8-bit digits), the unfused cost tensor up to D = 400 (six 7-bit
-# digits above D = 128); wider fused rows use the difference form. The
-# difference-form kernels (the debug option) compute the same costs on the FP32
-# pipe. Both must hold the tolerance at O(1) weights and agree closely. The shapes
+# sums (fixed-point digits, integer level sums), in both modes up to D = 400: five
+# 8-bit digits up to D = 128, six 7-bit digits above. The difference-form kernels
+# (the debug option) compute the same costs on the FP32 pipe. Both must hold the tolerance at O(1) weights and agree closely. The shapes
 # run the tensor-memory rings round several times (M up to 520 columns), over
 # several 128-row strips, and through one, two and several K-blocks.
 XTC_SHAPES = [(1, 9, 3), (33, 31, 1), (100, 37, 16), (129, 130, 63), (70, 91, 64), (130, 97, 65),
               (200, 150, 128), (300, 333, 128), (257, 520, 96), (129, 70, 129)]
-XTC_WIDE = [(64, 33, 256), (300, 333, 400), (131, 77, 200)]
+XTC_WIDE = [(64, 33, 256), (300, 333, 400), (131, 77, 200), (260, 300, 256)]
 
 
-@pytest.mark.parametrize("mname,mode,N,M,D", [("fused+extended", 3) + s for s in XTC_SHAPES] +
+@pytest.mark.parametrize("mname,mode,N,M,D", [("fused+extended", 3) + s for s in XTC_SHAPES + XTC_WIDE] +
                          [("unfused+extended", 2) + s for s in XTC_SHAPES + XTC_WIDE])
 def test_extended_tensor_core_costs(mname, mode, N, M, D):
     x, y = synth.iid_normal_pair(3, N, M, D, 106, repeat=N * 1000 + D)
