@@ -41,7 +41,7 @@ struct Layout {
     size_t band_slots;                // checkpointed mode: skewed slots of one band of every problem
     size_t ebnd;                      // extended mode: non-zero column range of E per 32-row block
     bool tc_cost;
-    bool xtc;    // exact tensor-core costs (D <= kMaxXtcD): extended modes, and the fp32 unfused tensor above D = 64
+    bool xtc;    // extended modes: exact tensor-core costs (D <= kMaxXtcD)
     bool ckpt;   // checkpointed fused mode: VH / E hold two bands, the [X | 1] image one
     int P, N, M, D, NB;
 };
@@ -107,7 +107,7 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->tc_cost = !ext && D <= kTcKFeat * kMaxTcKBlocks && xy;
     // the extended modes' exact tensor-core costs (the fused forward's cost tiles, the
     // unfused cost tensor): fixed-point digit images and row info
-    L->xtc = xy && D <= kMaxXtcD && (ext || (!fused && !L->tc_cost));
+    L->xtc = ext && xy && D <= kMaxXtcD;
     L->ximg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, N, D));
     if (L->xtc) o = align_up(o + oimg_bytes(P, N, D));
     L->yimg = o; if (L->tc_cost) o = align_up(o + simg_bytes(P, M, D));
@@ -136,6 +136,7 @@ int choose_warps(int P, int NB, int D, bool fused, bool ext, bool backward, int 
     }
     if (W > NB) W = NB;
     if (W > kMaxWarps) W = kMaxWarps;
+    if (ext && backward && W > kMaxWarpsBwdExt) W = kMaxWarpsBwdExt;
     if (W < 1) W = 1;
     if (fused) {
         if (W > 8) W = 8;  // fused CTAs are at most 256 threads (register budget of the cost rows)
@@ -257,7 +258,7 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
             if (xtc)
                 SDTW_CUDA(launch_dist_xtc(L.P, L.N, L.M, L.D, at<char>(ws, L.ximg), at<char>(ws, L.yimg),
                                           at<char>(ws, L.xnorm), at<char>(ws, L.ynorm), at<float2>(ws, L.dsk),
-                                          false, at<int>(ws, L.status), st));
+                                          at<int>(ws, L.status), st));
             else
                 SDTW_CUDA(launch_dist_skewed_x(pr, L.P, L.N, L.M, L.D, at<float2>(ws, L.dsk), st));
         }
@@ -281,12 +282,6 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
             SDTW_CUDA(launch_dist_tc(L.P, L.N, L.M, L.D, at<float>(ws, L.ximg), at<float>(ws, L.yimg),
                                      at<float>(ws, L.xnorm), at<float>(ws, L.ynorm), at<float>(ws, L.dsk),
                                      at<int>(ws, L.status), st));
-        } else if (xtc) {   // D > 64: the exact costs, each rounded once to fp32
-            SDTW_CUDA(launch_oimg(pr, L.P, L.N, L.M, L.D, at<char>(ws, L.ximg), at<char>(ws, L.yimg),
-                                  at<char>(ws, L.xnorm), at<char>(ws, L.ynorm), st));
-            SDTW_CUDA(launch_dist_xtc(L.P, L.N, L.M, L.D, at<char>(ws, L.ximg), at<char>(ws, L.yimg),
-                                      at<char>(ws, L.xnorm), at<char>(ws, L.ynorm), at<float>(ws, L.dsk), true,
-                                      at<int>(ws, L.status), st));
         } else {
             SDTW_CUDA(launch_dist_skewed(pr, L.P, L.N, L.M, L.D, at<float>(ws, L.dsk), st));
         }

@@ -67,6 +67,9 @@ size_t wavex_smem_fused_per_warp(int D);
 cudaError_t launch_forward_x(WaveParams q, bool fused, cudaStream_t st);
 cudaError_t launch_dist_skewed_x(const Problems& pr, int P, int N, int M, int D, float2* Dsk, cudaStream_t st);
 cudaError_t launch_forward(WaveParams q, bool fused, cudaStream_t st);
+// The double-float backward takes at most 12 warps per CTA: its ~166 registers per
+// thread fit 384 threads (a 512-thread build, capped at 128 registers, spills).
+constexpr int kMaxWarpsBwdExt = 12;
 cudaError_t launch_backward(WaveParams q, cudaStream_t st);
 
 // Unfused cost: raw squared Euclidean distances into the skewed layout.
@@ -147,11 +150,10 @@ size_t oimg_bytes(int P, int L, int D);
 size_t oinfo_bytes(int P, int L);
 cudaError_t launch_oimg(const Problems& pr, int P, int N, int M, int D, void* ximg, void* yimg, void* xinfo,
                         void* yinfo, cudaStream_t st);
-// Unfused cost tensor from the exact tensor-core level sums (D <= kMaxXtcD), in the
-// skewed layout: raw double-float costs (hi, lo), or with f32 each cost rounded once
-// to fp32 (the fp32 modes above D = 64).
+// Extended unfused cost tensor from the exact tensor-core level sums (D <= kMaxXtcD):
+// raw double-float costs (hi, lo) in the skewed layout.
 cudaError_t launch_dist_xtc(int P, int N, int M, int D, const void* ximg, const void* yimg, const void* xinfo,
-                            const void* yinfo, void* Dsk, bool f32, int* status, cudaStream_t st);
+                            const void* yinfo, float2* Dsk, int* status, cudaStream_t st);
 // Extended fused forward with exact tensor-core cost tiles (D <= kMaxXtcD): q.W must be 4.
 cudaError_t launch_forward_xtc(WaveParams q, const void* ximg, const void* yimg, const void* xinfo,
                                const void* yinfo, cudaStream_t st);

@@ -569,7 +569,8 @@ cudaError_t launch_backward(WaveParams q, cudaStream_t st)
         return cudaGetLastError();
     };
     if (q.W <= 8) return q.ext ? go(bwd_kernel<true, 256>) : go(bwd_kernel<false, 256>);
-    return q.ext ? go(bwd_kernel<true, kMaxWarps * 32>) : go(bwd_kernel<false, kMaxWarps * 32>);
+    if (q.ext) return q.W <= kMaxWarpsBwdExt ? go(bwd_kernel<true, kMaxWarpsBwdExt * 32>) : cudaErrorInvalidValue;
+    return go(bwd_kernel<false, kMaxWarps * 32>);
 }
 
 }  // namespace sdtw

@@ -973,12 +973,10 @@ __global__ void __launch_bounds__(kXFusedThreads, 1)
 constexpr int kXdWarps = 8;
 constexpr int kXdStg = 47 * 32;   // per-warp staging: skewed rows of a 16-column chunk (float2)
 
-// F32: write each cost rounded once to fp32 (the fp32 modes' cost tensor) instead of
-// the double-float pair.
-template <int NS, bool F32>
+template <int NS>
 __global__ void __launch_bounds__((kXdWarps + 1) * 32, 1)
     distx_tc_kernel(int N, int M, int D, const unsigned char* __restrict__ ximg, const unsigned char* __restrict__ yimg,
-                    const float4* __restrict__ xinfo, const float4* __restrict__ yinfo, void* __restrict__ Dsk,
+                    const float4* __restrict__ xinfo, const float4* __restrict__ yinfo, float2* __restrict__ Dsk,
                     int* status)
 {
     using X = XDigits<NS>;
@@ -1113,9 +1111,7 @@ __global__ void __launch_bounds__((kXdWarps + 1) * 32, 1)
         const float4 xi = xinfo[(size_t)p * Npad + row];
         const int ex = __float_as_int(xi.z);
         const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
-        const long long o0 = (rb < NB) ? skew_index(N, M, p, rb, 0, lane) : -1;
-        float2* out = o0 >= 0 ? static_cast<float2*>(Dsk) + o0 : nullptr;
-        float* out1 = o0 >= 0 ? static_cast<float*>(Dsk) + o0 : nullptr;
+        float2* out = (rb < NB) ? Dsk + skew_index(N, M, p, rb, 0, lane) : nullptr;
         for (int c = 0; c < nT; ++c) {
             const int t = c & 1;
             tc::wait_ok(ok, tc::smem_u32(&s_tfull[t]), (uint32_t)((c >> 1) & 1), status);
@@ -1151,11 +1147,7 @@ __global__ void __launch_bounds__((kXdWarps + 1) * 32, 1)
                 // skewed slot cb + tt holds column cb + tt - lane of this lane's row
                 for (int tt = 0; tt < 47; ++tt) {
                     const int j = tt - lane;
-                    if (j >= 0 && j < 16 && cb + j < M && row < N) {
-                        const float2 v = stg[tt * 32 + lane];
-                        if (F32) out1[(long long)(cb + tt) * 32] = v.x + v.y;
-                        else out[(long long)(cb + tt) * 32] = v;
-                    }
+                    if (j >= 0 && j < 16 && cb + j < M && row < N) out[(long long)(cb + tt) * 32] = stg[tt * 32 + lane];
                 }
             }
             __syncwarp();
@@ -1223,7 +1215,7 @@ cudaError_t launch_forward_xtc(WaveParams q, const void* ximg, const void* yimg,
 }
 
 cudaError_t launch_dist_xtc(int P, int N, int M, int D, const void* ximg, const void* yimg, const void* xinfo,
-                            const void* yinfo, void* Dsk, bool f32, int* status, cudaStream_t st)
+                            const void* yinfo, float2* Dsk, int* status, cudaStream_t st)
 {
     if (D < 1 || D > kMaxXtcD) return cudaErrorInvalidValue;
     const int KB = (D + kTcKFeat - 1) / kTcKFeat;
@@ -1240,8 +1232,7 @@ cudaError_t launch_dist_xtc(int P, int N, int M, int D, const void* ximg, const 
                                                       static_cast<const float4*>(yinfo), Dsk, status);
         return cudaGetLastError();
     };
-    if (NS == 5) return f32 ? go(distx_tc_kernel<5, true>) : go(distx_tc_kernel<5, false>);
-    return f32 ? go(distx_tc_kernel<6, true>) : go(distx_tc_kernel<6, false>);
+    return NS == 5 ? go(distx_tc_kernel<5>) : go(distx_tc_kernel<6>);
 }
 
 size_t wavex_smem_fused_per_warp(int D)
