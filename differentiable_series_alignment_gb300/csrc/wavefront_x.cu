@@ -380,7 +380,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) fwdx_kernel(const WaveParam
 }
 
 // ---------------------------------------------------------------------------
-// Exact cost tiles on the tensor cores for the extended fused forward (D <= 128)
+// Exact cost tiles on the tensor cores for the extended modes (D <= 400): the fused
+// forward's tiles and the unfused cost tensor
 //
 // The double-float DP needs each cost to ~1e-9 of itself, beyond any fp32 split
 // product (whose fp32 accumulation rounds). The dot x_i . y_j is therefore made
@@ -604,7 +605,6 @@ __global__ void __launch_bounds__(kXFusedThreads, 1)
                    const float4* __restrict__ xinfo, const float4* __restrict__ yinfo)
 {
     using X = XDigits<NS>;
-    // three tiles of five levels (160 columns each) fill the 512 tensor-memory columns
     // five digits: three tiles of 160 TMEM columns, all x digits of a K-block in one
     // fill; six digits: two tiles of 192 columns, x digits in two fills of three
     constexpr int kXRT = NS == 5 ? 3 : 2, kXSlotCols = X::SlotCols, kXSlices = NS;

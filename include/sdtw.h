@@ -49,25 +49,30 @@ typedef enum { SDTW_UNFUSED = 0, SDTW_FUSED = 1 } sdtw_mode;
 /* Precision flag, OR-ed into the mode of every entry point except
  * sdtw_forward_noalloc. Long sequences at small gamma make the gradient react
  * to cost perturbations below fp32 resolution (at N=M=8192, gamma=0.01 even an
- * fp64 DP fed correctly rounded fp32 costs misses rel 1e-3). With this flag the
- * cost and the forward DP state are carried as double-floats (hi + lo fp32
- * pairs) and the forward stores per-cell transition log-probabilities for the
- * backward; the workspace grows from 12 to 20 bytes per cell (unfused: 16 to
- * 28). Without it the DP runs in fp32 difference form, which meets the
- * tolerances for gamma >= 0.05 and N, M <= 2048 on the tested workloads. */
+ * fp64 DP fed correctly rounded fp32 costs misses rel 1e-3), and on rows where two
+ * alignments nearly tie the fp32 state's rounding moves a gradient entry by more
+ * than abs 1e-5 at O(1) upstream weights. With this flag the cost and the forward
+ * DP state are carried as double-floats (hi + lo fp32 pairs; the costs for
+ * D <= 400 from exact fixed-point digit products on the tensor cores) and the
+ * forward stores per-cell transition log-probabilities for the backward; the
+ * workspace grows from 12 to 20 bytes per cell (unfused: 16 to 28). Without it
+ * the DP runs in fp32 difference form, which met the tolerances on the tested
+ * workloads for gamma >= 0.05, N, M < 4096 and D <= 64 at batch-mean weights of
+ * at most 1/32 (or D <= 4 at any weight), but is not guaranteed to on near ties. */
 #define SDTW_EXTENDED 2
 
 /* Checkpoint flag, OR-ed into SDTW_FUSED for sdtw_forward / sdtw_backward and
  * their padded-batch forms (fp32, D <= 64 only; otherwise SDTW_ERR_ARG). The fused
  * forward then stores no per-cell state: it keeps only the boundary row of each
  * band of 128 rows (the checkpoints, 8 bytes per band row and column). The
- * backward recomputes one band at a time from the row above it, from the last
- * band up, and runs that band's backward and gradient terms. The per-cell
- * workspace shrinks to one band of every problem (12 bytes per cell of a band);
- * the bands run one after another, so the backward's time grows with N/128
- * (measured at B=32, N=M=512, D=64: workspace 146 -> 56 MiB, backward with
- * gradients 0.18 -> 0.72 ms). SoftDTW-CUDA-Torch paper, abstract, contribution
- * (3): fused memory O(B(N+M)) rather than O(BNM). */
+ * backward walks the bands from the last up: it recomputes a band's state from
+ * the row above it (on a second stream, while the band below runs its backward and
+ * gradient terms) and runs that band's backward and gradient terms. The per-cell
+ * workspace shrinks to two bands of every problem (12 bytes per cell of a band);
+ * the bands' backward wavefronts run one after another, so the backward's time
+ * grows with N/128 (measured at B=32, N=M=512, D=64: workspace 142 -> 78 MiB,
+ * forward + backward with gradients 0.32 -> 0.68 ms). SoftDTW-CUDA-Torch paper,
+ * abstract, contribution (3): fused memory O(B(N+M)) rather than O(BNM). */
 #define SDTW_CHECKPOINT 4
 
 typedef enum {
