@@ -51,8 +51,8 @@ FALLBACK_SM_MHZ = 2070.0
 # from one ncu capture (`dram__bytes_read.sum + dram__bytes_write.sum`), with the
 # SHA-256 of the sources that build the kernel at the time of the capture; the
 # bench reports it only while those sources are unchanged (else null).
-# profiles/bwd_kernel_headline.md: 71,458,304 read + 7,719,936 written.
-BWD_TRAFFIC = {"sha256": "a46cc68788db327fda5d295ebe552b9a852fdad5eb5ff391800904873675205d", "bytes": 79178240}
+# profiles/bwd_kernel_headline.md: 71,459,328 read + 7,732,736 written.
+BWD_TRAFFIC = {"sha256": "83f0391b60d431556708031e3110126cb9d2d7cf82d3150ec1491e74b4f1c9f6", "bytes": 79192064}
 BWD_SOURCES = ("wavefront.cu", "common.cuh", "channel.cuh", "kernels.h")
 # kernels per step: unfused forward (operand images, cost tensor, wavefront) + backward
 # (wavefront, gradient operand images, two gradient contractions), fused forward
