@@ -97,17 +97,10 @@ __device__ __forceinline__ float exp2_neg(float x) {
     return (x < -125.0f) ? 0.0f : r;
 }
 
-// Math variants of the DP kernels: ACC selects the unbiased exp2_neg above and
-// log2f (the double-float path), otherwise the MUFU approximations.
-template <bool ACC> __device__ __forceinline__ float dp_exp2(float x) { return ACC ? exp2_neg(x) : ex2(x); }
-template <bool ACC> __device__ __forceinline__ float dp_log2(float x) { return ACC ? log2f(x) : lg2(x); }
-
-// log2(1 + a + b) for a, b in [0, 1]: the three-term sum of a log-sum-exp whose
-// largest term has been factored out. log2f is the accurate (unbiased) library
-// function.
-__device__ __forceinline__ float log2_1pab(float a, float b) {
-    return log2f((1.0f + a) + b);
-}
+// Math of the DP kernels: the double-float path (flag set) takes the unbiased
+// exp2_neg above and log2f, the fp32 path the MUFU approximations.
+template <bool EXT> __device__ __forceinline__ float dp_exp2(float x) { return EXT ? exp2_neg(x) : ex2(x); }
+template <bool EXT> __device__ __forceinline__ float dp_log2(float x) { return EXT ? log2f(x) : lg2(x); }
 
 // Error-free sum (Knuth's TwoSum): s + e == a + b exactly.
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
@@ -294,14 +287,6 @@ __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
-}
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_gpu(int* p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ int ld_volatile_global(const int* p) {
     return *reinterpret_cast<const volatile int*>(p);

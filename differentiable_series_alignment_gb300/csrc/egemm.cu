@@ -468,13 +468,6 @@ static Pipe egemm_plan(int D, bool cols)
     return order[6];
 }
 
-size_t egemm_smem_bytes(int D)
-{
-    const size_t a = egemm_bytes(D, false, egemm_plan(D, false));
-    const size_t b = egemm_bytes(D, true, egemm_plan(D, true));
-    return a > b ? a : b;
-}
-
 size_t egemm_bimg_bytes(int P, int K, int D)
 {
     const int n_total = ((D + 1 + 15) / 16) * 16;

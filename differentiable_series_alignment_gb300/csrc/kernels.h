@@ -111,7 +111,6 @@ cudaError_t launch_ebounds(const GradParams& g, int2* bounds, cudaStream_t st);
 cudaError_t launch_bimg(const GradParams& g, float* img_rows, float* img_cols, cudaStream_t st);
 // bimg: the image for this orientation, written by launch_bimg before.
 cudaError_t launch_grad_tc(const GradParams& g, bool cols, const float* bimg, int* status, cudaStream_t st);
-size_t egemm_smem_bytes(int D);
 size_t egemm_bimg_bytes(int P, int K, int D);
 
 // Tensor-core cost tensor (dist_tc.cu), D <= kTcKFeat * kMaxTcKBlocks: operand

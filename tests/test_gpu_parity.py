@@ -195,6 +195,16 @@ def test_extended_strip_decompositions(W):
         check_against_oracle(x, y, 0.05, 3, what=f"extended W={W}")
 
 
+# Strips of 9 to 12 warps take the double-float backward's 384-thread build (wider
+# requests are capped at 12 warps); both modes, 13 row blocks per problem.
+@pytest.mark.parametrize("mname,mode", [("unfused+extended", 2), ("fused+extended", 3)])
+@pytest.mark.parametrize("W", [10, 16])
+def test_extended_wide_backward_strips(mname, mode, W):
+    x, y = synth.iid_normal_pair(2, 410, 150, 6, 108)
+    with warps(W):
+        check_against_oracle(x, y, 0.3, mode, grad_loss=[0.5, -1.25], what=f"{mname} W={W}")
+
+
 def test_fused_equals_unfused():
     # Both cost kernels exist in both modes: the tensor-core norm form (default,
     # D <= 64) and the difference form (selected through sdtw_debug_set_options). With the
