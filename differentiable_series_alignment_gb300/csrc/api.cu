@@ -48,9 +48,11 @@ struct Layout {
 
 // Side streams and cached events (defined below, with their rules).
 cudaStream_t side_stream();
+cudaStream_t grad_stream();
 enum EventSlot {
     kEvBwdFork, kEvBwdJoin, kEvHostFork, kEvHostJoin, kEvNormFork, kEvNormJoin,
-    kEvCkptFork, kEvCkptRec0, kEvCkptRec1, kEvCkptFree0, kEvCkptFree1, kEvSlots
+    kEvCkptFork, kEvCkptRec0, kEvCkptRec1, kEvCkptFree0, kEvCkptFree1, kEvCkptBwd0, kEvCkptBwd1, kEvCkptJoin,
+    kEvSlots
 };
 cudaEvent_t cached_event(EventSlot slot);
 
@@ -288,7 +290,14 @@ sdtw_status run_forward(const Problems& pr, const Layout& L, void* ws, float gam
     }
     q.loss = loss_out;
     q.skip_publish = debug_take_skip_publish();
-    if (L.ckpt) q.VH = nullptr;  // only the strips' boundary rows are kept (edge_f)
+    if (L.ckpt) {  // the strips' boundary rows (edge_f), and the state of the last band, which the
+                   // backward takes first: into the band buffer the backward reads it from
+        const int SB = (L.NB + kBandBlocks - 1) / kBandBlocks;
+        const int rb0 = (SB - 1) * kBandBlocks;
+        q.VH = at<float2>(ws, L.vh) + (size_t)((SB - 1) & 1) * L.band_slots;
+        q.vh_rb0 = rb0;
+        q.vh_nb = L.NB - rb0 < kBandBlocks ? L.NB - rb0 : kBandBlocks;
+    }
     if (fused && tc)
         SDTW_CUDA(launch_forward_tc(q, at<float>(ws, L.ximg), at<float>(ws, L.yimg), at<float>(ws, L.xnorm),
                                     at<float>(ws, L.ynorm), st));
@@ -313,10 +322,14 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
 {
     const int SB = (L.NB + kBandBlocks - 1) / kBandBlocks;
     int* status = at<int>(ws, L.status);
-    cudaStream_t side = side_stream();
-    cudaEvent_t ev_fork = cached_event(kEvCkptFork), ev_rec[2] = {cached_event(kEvCkptRec0), cached_event(kEvCkptRec1)};
+    cudaStream_t side = side_stream(), gs = grad_stream();
+    cudaEvent_t ev_fork = cached_event(kEvCkptFork), ev_join = cached_event(kEvCkptJoin);
+    cudaEvent_t ev_rec[2] = {cached_event(kEvCkptRec0), cached_event(kEvCkptRec1)};
     cudaEvent_t ev_free[2] = {cached_event(kEvCkptFree0), cached_event(kEvCkptFree1)};
-    if (!side || !ev_fork || !ev_rec[0] || !ev_rec[1] || !ev_free[0] || !ev_free[1]) return SDTW_ERR_CUDA;
+    cudaEvent_t ev_bwd[2] = {cached_event(kEvCkptBwd0), cached_event(kEvCkptBwd1)};
+    if (!side || !gs || !ev_fork || !ev_join || !ev_rec[0] || !ev_rec[1] || !ev_free[0] || !ev_free[1] ||
+        !ev_bwd[0] || !ev_bwd[1])
+        return SDTW_ERR_CUDA;
     WaveParams qb0 = wave_params(pr, L, ws, gamma, true, false, true);
     if (SB > 1) SDTW_CUDA(cudaMemsetAsync(qb0.edge_b, 0, 2 * sizeof(Slot) * (size_t)L.P * SB * L.M, st));
     GradParams g{};
@@ -334,9 +347,13 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
         g.N = L.N;
         SDTW_CUDA(launch_bimg(g, img_rows, nullptr, st));
     }
-    // the side stream starts after everything before this call on the caller's stream
+    // The helper streams start after everything before this call on the caller's
+    // stream, which includes the forward: it left the last band's state in buffer
+    // (SB - 1) & 1, so that band needs no recompute.
     SDTW_CUDA(cudaEventRecord(ev_fork, st));
     SDTW_CUDA(cudaStreamWaitEvent(side, ev_fork, 0));
+    SDTW_CUDA(cudaStreamWaitEvent(gs, ev_fork, 0));
+    SDTW_CUDA(cudaEventRecord(ev_rec[(SB - 1) & 1], st));
     // band k's forward state, recomputed from the kept boundary row above it, into buffer k % 2
     auto recompute = [&](int k, cudaStream_t s) -> sdtw_status {
         const int rb0 = k * kBandBlocks;
@@ -351,21 +368,25 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
                                     at<float>(ws, L.ynorm), s));
         return SDTW_OK;
     };
-    sdtw_status s = recompute(SB - 1, side);
-    if (s == SDTW_OK) SDTW_CUDA(cudaEventRecord(ev_rec[(SB - 1) & 1], side));
+    // Per band, from the last up: its backward on the caller's stream, its gradient
+    // terms on the gradient stream (overlapping the next band's backward), and the
+    // next band's recompute on the side stream. Buffer k % 2 holds band k's state
+    // and E: the recompute of band k - 1 waits for band k + 1's backward (its state
+    // buffer), band k's backward for band k + 2's gradient terms (its E buffer).
+    sdtw_status s = SDTW_OK;
     for (int k = SB - 1; k >= 0 && s == SDTW_OK; --k) {
         const int rb0 = k * kBandBlocks;
         const int nb = L.NB - rb0 < kBandBlocks ? L.NB - rb0 : kBandBlocks;
         const int row0 = 32 * rb0;
         const int nrows = L.N - row0 < 32 * kBandBlocks ? L.N - row0 : 32 * kBandBlocks;
-        // 1. the next band up, into the other buffer once band k + 1 has released it
         if (k >= 1) {
-            if (k + 1 < SB) SDTW_CUDA(cudaStreamWaitEvent(side, ev_free[(k + 1) & 1], 0));
+            if (k + 1 < SB) SDTW_CUDA(cudaStreamWaitEvent(side, ev_bwd[(k + 1) & 1], 0));
             if ((s = recompute(k - 1, side)) != SDTW_OK) break;
             SDTW_CUDA(cudaEventRecord(ev_rec[(k - 1) & 1], side));
         }
-        // 2. the band's backward wavefront, once its state is recomputed
+        // the band's backward wavefront, once its state is there and its E buffer free
         SDTW_CUDA(cudaStreamWaitEvent(st, ev_rec[k & 1], 0));
+        if (k + 2 < SB) SDTW_CUDA(cudaStreamWaitEvent(st, ev_free[k & 1], 0));
         WaveParams qb = wave_params(pr, L, ws, gamma, true, false, true);
         qb.W = kBandBlocks; qb.S = 1; qb.strip0 = k; qb.S_all = SB;
         qb.vh_rb0 = rb0; qb.vh_nb = nb;
@@ -374,27 +395,32 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
         qb.lens_n = lens_n; qb.lens_m = lens_m;
         SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_b), 0, L.ctrl_b_bytes, st));
         SDTW_CUDA(launch_backward(qb, st));
-        // 3. the band's gradient terms: E of the band is a problem of nrows x M
+        SDTW_CUDA(cudaEventRecord(ev_bwd[k & 1], st));
+        // the band's gradient terms: E of the band is a problem of nrows x M. The band's
+        // [X | 1] image depends on x only: it is built before waiting for the backward.
         g.E = e_buf[k & 1];
         g.pr.xs[0] = pr.xs[0] + (size_t)row0 * L.D;
         g.N = nrows;
+        if (grad_y) SDTW_CUDA(launch_bimg(g, nullptr, img_cols, gs));
+        SDTW_CUDA(cudaStreamWaitEvent(gs, ev_bwd[k & 1], 0));
         if (grad_x) {
             g.out = grad_x + (size_t)row0 * L.D;
             g.out_stride = (long long)L.N * L.D;
             g.accumulate = 0;
-            SDTW_CUDA(launch_grad_tc(g, false, img_rows, status, st));
+            SDTW_CUDA(launch_grad_tc(g, false, img_rows, status, gs));
         }
         if (grad_y) {
-            SDTW_CUDA(launch_bimg(g, nullptr, img_cols, st));
             g.out = grad_y;
             g.out_stride = (long long)L.M * L.D;
             g.accumulate = k < SB - 1;
-            SDTW_CUDA(launch_grad_tc(g, true, img_cols, status, st));
+            SDTW_CUDA(launch_grad_tc(g, true, img_cols, status, gs));
         }
-        SDTW_CUDA(cudaEventRecord(ev_free[k & 1], st));
+        SDTW_CUDA(cudaEventRecord(ev_free[k & 1], gs));
     }
-    // the side stream's work (the last recompute was waited for above) stays ordered
-    // before anything later on the caller's stream, also after an error
+    // both helper streams' work stays ordered before anything later on the caller's
+    // stream, also after an error
+    cudaEventRecord(ev_join, gs);
+    cudaStreamWaitEvent(st, ev_join, 0);
     if (s != SDTW_OK) {
         cudaEventRecord(ev_fork, side);
         cudaStreamWaitEvent(st, ev_fork, 0);
@@ -430,19 +456,22 @@ GradParams grad_params(const Problems& all, int set, int B, const Layout& L, voi
     return g;
 }
 
-// A second stream per device for work that can overlap the caller's stream
-// (created once, non-blocking; ordered against the caller's stream by events).
-cudaStream_t side_stream()
+// Helper streams per device for work that can overlap the caller's stream (created
+// once, non-blocking; ordered against the caller's stream by events): slot 0 the
+// side stream, slot 1 the checkpointed backward's gradient stream.
+cudaStream_t helper_stream(int slot)
 {
     static std::mutex mu;
-    static cudaStream_t streams[64] = {};
+    static cudaStream_t streams[2][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
-        streams[dev] = nullptr;
-    return streams[dev];
+    cudaStream_t& s = streams[slot][dev];
+    if (!s && cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) s = nullptr;
+    return s;
 }
+cudaStream_t side_stream() { return helper_stream(0); }
+cudaStream_t grad_stream() { return helper_stream(1); }
 
 // Events that order side-stream work against the caller's stream. Each call site
 // has its own slots, created once per host thread and device and reused: a slot

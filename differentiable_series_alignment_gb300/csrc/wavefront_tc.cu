@@ -64,9 +64,11 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
-// STORE: the per-cell state for the backward is written (false in a checkpointed
-// forward, which keeps only the strips' boundary rows).
-template <bool STORE>
+// STORE: 0, no per-cell state (a checkpointed forward keeps the strips' boundary
+// rows only); 1, the state of every row; 2, the state of the row blocks
+// [q.vh_rb0, q.vh_rb0 + q.vh_nb) only (one band: the checkpointed forward keeps its
+// last band, a band's recompute its own).
+template <int STORE>
 __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     fwd_tc_kernel(const WaveParams q, const unsigned char* __restrict__ ximg, const unsigned char* __restrict__ yimg,
                   const float* __restrict__ xnorm, const float* __restrict__ ynorm)
@@ -208,7 +210,8 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
         }
 
         if (active) {
-            float2* vhp = STORE ? q.VH + band_index(q, p, rb, lane, T) : nullptr;
+            const bool store_rows = STORE == 1 || (STORE == 2 && rb >= q.vh_rb0 && rb < q.vh_rb0 + q.vh_nb);
+            float2* vhp = store_rows ? q.VH + band_index(q, p, rb, lane, T) : nullptr;
             Slot* ring_out = ring + warp * kRing;
             const Slot* ring_in = ring + (warp - 1) * kRing;
             Slot* edge_out = q.edge_f + ((size_t)p * strips_all(q) + strip) * M;
@@ -304,7 +307,10 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                     const float svl = col0 ? kBig : (row0_lane ? -kBig : vl);
                     const float shu = row0_lane ? kBig : (col0 ? -kBig : hu);
                     c0 = col0 ? d : c0;
-                    if constexpr (STORE) vhp[(long long)s * 32] = make_float2(svl, shu);
+                    if constexpr (STORE == 1) vhp[(long long)s * 32] = make_float2(svl, shu);
+                    if constexpr (STORE == 2) {
+                        if (store_rows) vhp[(long long)s * 32] = make_float2(svl, shu);
+                    }
                     const bool valid = (unsigned)j < (unsigned)M;
                     slot_store_if(chan_lane && valid, chan_out + (j & chan_mask), h, (unsigned)(j + 1));
                     if (last_lane && (unsigned)j < (unsigned)Mb) rowbuf[j] = h;
@@ -383,7 +389,8 @@ cudaError_t launch_forward_tc(WaveParams q, const void* ximg, const void* yimg, 
                                                        static_cast<const unsigned char*>(yimg), xnorm, ynorm);
         return cudaGetLastError();
     };
-    return q.VH == nullptr ? go(fwd_tc_kernel<false>) : go(fwd_tc_kernel<true>);
+    if (q.VH == nullptr) return go(fwd_tc_kernel<0>);
+    return q.vh_nb > 0 ? go(fwd_tc_kernel<2>) : go(fwd_tc_kernel<1>);
 }
 
 }  // namespace sdtw

@@ -63,15 +63,16 @@ typedef enum { SDTW_UNFUSED = 0, SDTW_FUSED = 1 } sdtw_mode;
 
 /* Checkpoint flag, OR-ed into SDTW_FUSED for sdtw_forward / sdtw_backward and
  * their padded-batch forms (fp32, D <= 64 only; otherwise SDTW_ERR_ARG). The fused
- * forward then stores no per-cell state: it keeps only the boundary row of each
- * band of 128 rows (the checkpoints, 8 bytes per band row and column). The
- * backward walks the bands from the last up: it recomputes a band's state from
- * the row above it (on a second stream, while the band below runs its backward and
- * gradient terms) and runs that band's backward and gradient terms. The per-cell
- * workspace shrinks to two bands of every problem (12 bytes per cell of a band);
- * the bands' backward wavefronts run one after another, so the backward's time
- * grows with N/128 (measured at B=32, N=M=512, D=64: workspace 142 -> 78 MiB,
- * forward + backward with gradients 0.32 -> 0.68 ms). SoftDTW-CUDA-Torch paper,
+ * forward then keeps only the boundary row of each band of 128 rows (the
+ * checkpoints, 8 bytes per band row and column) and the state of the last band.
+ * The backward walks the bands from the last up: it recomputes a band's state from
+ * the row above it (on a helper stream, while the band below runs its backward)
+ * and runs that band's backward, then its gradient terms (on a second helper
+ * stream, overlapping the next band's backward). The per-cell workspace shrinks
+ * to two bands of every problem (12 bytes per cell of a band); the bands'
+ * backward wavefronts run one after another, so the backward's time grows with
+ * N/128 (measured at B=32, N=M=512, D=64: workspace 142 -> 78 MiB, forward +
+ * backward with gradients 0.32 -> 0.48 ms). SoftDTW-CUDA-Torch paper,
  * abstract, contribution (3): fused memory O(B(N+M)) rather than O(BNM). */
 #define SDTW_CHECKPOINT 4
 
