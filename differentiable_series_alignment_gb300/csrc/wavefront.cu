@@ -393,6 +393,12 @@ __global__ void __launch_bounds__(MAXT, 1) bwd_kernel(const WaveParams q)
     }
 
     float ml = -kBig, su = -kBig, sd = -kBig, rd_hold = -kBig;
+    // E leaves in bursts of kEB steps' values kept in registers: per-step stores
+    // interleaved with the chain slow every step (a warp issues in order; measured:
+    // a whole group per burst is fastest, delaying each store by one step is not).
+    // The wider builds have fewer registers to spare; the 384-thread double-float
+    // one is fastest storing at once.
+    constexpr int kEB = MAXT <= 256 ? kGroup : (EXT ? 1 : 8);
     // Per-step state of the next kGroup steps; slot u is refilled with the
     // following group's value as soon as step u has consumed it.
     VT buf[kGroup];
@@ -404,6 +410,7 @@ __global__ void __launch_bounds__(MAXT, 1) bwd_kernel(const WaveParams q)
         const int t0 = g * kGroup;   // first reverse step of the group
         const int k0 = t0 - off;     // channel slot read by lane 31 at that step
         VT bcur[EXT ? 1 : kGroup];
+        float eg[kEB];  // E of the steps not yet stored
         if (!EXT) {  // this group's state; the next group's loads go out now
 #pragma unroll
             for (int u = 0; u < kGroup; ++u) bcur[u] = buf[u];
@@ -487,7 +494,11 @@ __global__ void __launch_bounds__(MAXT, 1) bwd_kernel(const WaveParams q)
             su = lE + wu;
             sd = lE + wd;
             // cells outside this problem's own N_b x M_b block carry no alignment
-            ep[(long long)t * 32] = (row_in && (unsigned)j < (unsigned)Mb) ? ex2(lE) : 0.f;
+            eg[u % kEB] = (row_in && (unsigned)j < (unsigned)Mb) ? ex2(lE) : 0.f;
+            if (u % kEB == kEB - 1) {
+#pragma unroll
+                for (int v = 0; v < kEB; ++v) ep[(long long)(t + kEB - 1 - v) * 32] = eg[v];
+            }
             {
                 const bool pub = chan_lane && (unsigned)j < (unsigned)M;
                 const int k = M - 1 - j;
