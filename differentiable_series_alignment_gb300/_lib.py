@@ -31,7 +31,7 @@ EXPORTS = ("sdtw_workspace_bytes", "sdtw_distance", "sdtw_forward", "sdtw_backwa
            "sdtw_forward_noalloc", "sdtw_forward_cost", "sdtw_backward_cost", "sdtw_barycenter_step_clipped",
            "sdtw_forward_varlen", "sdtw_backward_varlen", "sdtw_host_workspace_bytes", "sdtw_value_and_grad_host",
            "sdtw_normalized_unequal", "sdtw_normalized_backward", "sdtw_normalized_unequal_backward",
-           "sdtw_debug_set_options", "sdtw_debug_exp2_neg")
+           "sdtw_debug_set_options", "sdtw_debug_set_clusters", "sdtw_debug_exp2_neg")
 
 
 class SdtwError(RuntimeError):
@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH):
         lib.sdtw_normalized_unequal_backward.restype = i
         lib.sdtw_debug_set_options.argtypes = [i, i, i, i]
         lib.sdtw_debug_set_options.restype = None
+        lib.sdtw_debug_set_clusters.argtypes = [i]
+        lib.sdtw_debug_set_clusters.restype = None
         lib.sdtw_debug_exp2_neg.argtypes = [vp, vp, i, vp]
         lib.sdtw_debug_exp2_neg.restype = i
         lib.sdtw_barycenter_step.argtypes = [vp, vp, vp, i, vp, i, i, i, i, f, f, f, f, f, i, vp, vp, sz, vp]
@@ -356,6 +358,12 @@ def sdtw_debug_set_options(warps_fwd: int = 0, warps_bwd: int = 0, dist_simt: bo
     """Testing hook: force the warps per wavefront CTA and the difference-form cost
     kernels (all defaults: the library's own choices)."""
     load().sdtw_debug_set_options(int(warps_fwd), int(warps_bwd), 1 if dist_simt else 0, 1 if fused_simt else 0)
+
+
+def sdtw_debug_set_clusters(max_cluster: int = 0):
+    """Testing hook: cap the CTAs per cluster of the fused tensor-core forward
+    (0: the library's choice, 1: no clusters)."""
+    load().sdtw_debug_set_clusters(int(max_cluster))
 
 
 def sdtw_debug_exp2_neg(x, out, stream=None):

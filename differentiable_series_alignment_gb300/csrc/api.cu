@@ -23,11 +23,12 @@ constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 unsigned long long g_wait_ns = kDefaultWaitNs;
 int g_skip_publish = 0;
 
-// Kernel choices forced by sdtw_debug_set_options (testing only; zeros: the
+// Kernel choices forced by sdtw_debug_set_options and sdtw_debug_set_clusters (testing only; zeros: the
 // library's own choices).
 struct DebugOptions {
     int warps_fwd, warps_bwd;   // warps per wavefront CTA (> 0: forced)
     int dist_simt, fused_simt;  // difference-form cost kernels (unfused / fused, both precisions)
+    int max_cluster;            // CTAs per cluster of the fused tensor-core forward at most (0: up to 4)
 };
 DebugOptions g_dbg{};
 
@@ -49,9 +50,11 @@ struct Layout {
 // Side streams and cached events (defined below, with their rules).
 cudaStream_t side_stream();
 cudaStream_t grad_stream();
+cudaStream_t grad_stream_cols();
 enum EventSlot {
     kEvBwdFork, kEvBwdJoin, kEvHostFork, kEvHostJoin, kEvNormFork, kEvNormJoin,
     kEvCkptFork, kEvCkptRec0, kEvCkptRec1, kEvCkptFree0, kEvCkptFree1, kEvCkptBwd0, kEvCkptBwd1, kEvCkptJoin,
+    kEvCkptCols, kEvCkptJoinCols,
     kEvSlots
 };
 cudaEvent_t cached_event(EventSlot slot);
@@ -201,6 +204,7 @@ WaveParams wave_params(const Problems& pr, const Layout& L, void* ws, float gamm
     q.P = L.P; q.N = L.N; q.M = L.M; q.D = L.D; q.NB = L.NB;
     q.W = choose_warps(L.P, L.NB, L.D, fused && !backward, ext, backward, sm_budget());
     q.S = (L.NB + q.W - 1) / q.W;
+    q.C = g_dbg.max_cluster > 0 ? g_dbg.max_cluster : 4;  // a limit: the launchers pick the size
     q.scale = (float)(1.4426950408889634 / (double)gamma);
     q.unscale = (float)((double)gamma * 0.6931471805599453);
     q.Dsk = fused ? nullptr : at<float>(ws, L.dsk);
@@ -322,13 +326,14 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
 {
     const int SB = (L.NB + kBandBlocks - 1) / kBandBlocks;
     int* status = at<int>(ws, L.status);
-    cudaStream_t side = side_stream(), gs = grad_stream();
+    cudaStream_t side = side_stream(), gs = grad_stream(), gc = grad_stream_cols();
     cudaEvent_t ev_fork = cached_event(kEvCkptFork), ev_join = cached_event(kEvCkptJoin);
     cudaEvent_t ev_rec[2] = {cached_event(kEvCkptRec0), cached_event(kEvCkptRec1)};
     cudaEvent_t ev_free[2] = {cached_event(kEvCkptFree0), cached_event(kEvCkptFree1)};
     cudaEvent_t ev_bwd[2] = {cached_event(kEvCkptBwd0), cached_event(kEvCkptBwd1)};
-    if (!side || !gs || !ev_fork || !ev_join || !ev_rec[0] || !ev_rec[1] || !ev_free[0] || !ev_free[1] ||
-        !ev_bwd[0] || !ev_bwd[1])
+    cudaEvent_t ev_cols = cached_event(kEvCkptCols), ev_join_cols = cached_event(kEvCkptJoinCols);
+    if (!side || !gs || !gc || !ev_fork || !ev_join || !ev_rec[0] || !ev_rec[1] || !ev_free[0] || !ev_free[1] ||
+        !ev_bwd[0] || !ev_bwd[1] || !ev_cols || !ev_join_cols)
         return SDTW_ERR_CUDA;
     WaveParams qb0 = wave_params(pr, L, ws, gamma, true, false, true);
     if (SB > 1) SDTW_CUDA(cudaMemsetAsync(qb0.edge_b, 0, 2 * sizeof(Slot) * (size_t)L.P * SB * L.M, st));
@@ -353,6 +358,7 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
     SDTW_CUDA(cudaEventRecord(ev_fork, st));
     SDTW_CUDA(cudaStreamWaitEvent(side, ev_fork, 0));
     SDTW_CUDA(cudaStreamWaitEvent(gs, ev_fork, 0));
+    SDTW_CUDA(cudaStreamWaitEvent(gc, ev_fork, 0));
     SDTW_CUDA(cudaEventRecord(ev_rec[(SB - 1) & 1], st));
     // band k's forward state, recomputed from the kept boundary row above it, into buffer k % 2
     auto recompute = [&](int k, cudaStream_t s) -> sdtw_status {
@@ -396,12 +402,24 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
         SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_b), 0, L.ctrl_b_bytes, st));
         SDTW_CUDA(launch_backward(qb, st));
         SDTW_CUDA(cudaEventRecord(ev_bwd[k & 1], st));
-        // the band's gradient terms: E of the band is a problem of nrows x M. The band's
-        // [X | 1] image depends on x only: it is built before waiting for the backward.
+        // the band's gradient terms, E of the band being a problem of nrows x M: the
+        // grad_x rows on one gradient stream, the grad_y terms (accumulated over the
+        // bands, in band order) on the other. The band's [X | 1] image depends on x
+        // only: it is built before waiting for the backward. The E buffer is free
+        // once both have read it.
         g.E = e_buf[k & 1];
         g.pr.xs[0] = pr.xs[0] + (size_t)row0 * L.D;
         g.N = nrows;
-        if (grad_y) SDTW_CUDA(launch_bimg(g, nullptr, img_cols, gs));
+        if (grad_y) {
+            SDTW_CUDA(launch_bimg(g, nullptr, img_cols, gc));
+            SDTW_CUDA(cudaStreamWaitEvent(gc, ev_bwd[k & 1], 0));
+            GradParams gy = g;
+            gy.out = grad_y;
+            gy.out_stride = (long long)L.M * L.D;
+            gy.accumulate = k < SB - 1;
+            SDTW_CUDA(launch_grad_tc(gy, true, img_cols, status, gc));
+            SDTW_CUDA(cudaEventRecord(ev_cols, gc));
+        }
         SDTW_CUDA(cudaStreamWaitEvent(gs, ev_bwd[k & 1], 0));
         if (grad_x) {
             g.out = grad_x + (size_t)row0 * L.D;
@@ -409,18 +427,15 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
             g.accumulate = 0;
             SDTW_CUDA(launch_grad_tc(g, false, img_rows, status, gs));
         }
-        if (grad_y) {
-            g.out = grad_y;
-            g.out_stride = (long long)L.M * L.D;
-            g.accumulate = k < SB - 1;
-            SDTW_CUDA(launch_grad_tc(g, true, img_cols, status, gs));
-        }
+        if (grad_y) SDTW_CUDA(cudaStreamWaitEvent(gs, ev_cols, 0));
         SDTW_CUDA(cudaEventRecord(ev_free[k & 1], gs));
     }
-    // both helper streams' work stays ordered before anything later on the caller's
+    // the helper streams' work stays ordered before anything later on the caller's
     // stream, also after an error
     cudaEventRecord(ev_join, gs);
     cudaStreamWaitEvent(st, ev_join, 0);
+    cudaEventRecord(ev_join_cols, gc);
+    cudaStreamWaitEvent(st, ev_join_cols, 0);
     if (s != SDTW_OK) {
         cudaEventRecord(ev_fork, side);
         cudaStreamWaitEvent(st, ev_fork, 0);
@@ -458,11 +473,12 @@ GradParams grad_params(const Problems& all, int set, int B, const Layout& L, voi
 
 // Helper streams per device for work that can overlap the caller's stream (created
 // once, non-blocking; ordered against the caller's stream by events): slot 0 the
-// side stream, slot 1 the checkpointed backward's gradient stream.
+// side stream, slots 1 and 2 the checkpointed backward's gradient streams (grad_x
+// terms, grad_y terms).
 cudaStream_t helper_stream(int slot)
 {
     static std::mutex mu;
-    static cudaStream_t streams[2][64] = {};
+    static cudaStream_t streams[3][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
@@ -472,6 +488,7 @@ cudaStream_t helper_stream(int slot)
 }
 cudaStream_t side_stream() { return helper_stream(0); }
 cudaStream_t grad_stream() { return helper_stream(1); }
+cudaStream_t grad_stream_cols() { return helper_stream(2); }
 
 // Events that order side-stream work against the caller's stream. Each call site
 // has its own slots, created once per host thread and device and reused: a slot
@@ -1094,6 +1111,11 @@ void sdtw_debug_set_options(int warps_fwd, int warps_bwd, int dist_simt, int fus
     g_dbg.warps_bwd = warps_bwd > 0 ? warps_bwd : 0;
     g_dbg.dist_simt = dist_simt ? 1 : 0;
     g_dbg.fused_simt = fused_simt ? 1 : 0;
+}
+
+void sdtw_debug_set_clusters(int max_cluster)
+{
+    g_dbg.max_cluster = max_cluster > 0 ? (max_cluster >= 4 ? 4 : max_cluster) : 0;
 }
 
 }  // extern "C"

@@ -41,6 +41,11 @@ struct WaveParams {
     // blocks [vh_rb0, vh_rb0 + vh_nb) of every problem. Zeros: the whole problem.
     int strip0, S_all, vh_rb0, vh_nb;
     int no_loss;       // 1: a recompute of stored boundary rows; no loss is assembled
+    // Fused tensor-core forward: CTAs per thread-block cluster (1: none). A cluster
+    // takes one ticket and runs C consecutive strips of a problem, by cluster rank;
+    // the boundary row between two of them goes through the consumer CTA's shared
+    // memory. The other wavefront kernels ignore it.
+    int C;
 };
 
 // Strips per problem for the boundary-row buffers.

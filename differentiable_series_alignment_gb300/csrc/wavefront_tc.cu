@@ -29,6 +29,8 @@
 #include "kernels.h"
 #include "tc.cuh"
 
+#include <mutex>
+
 namespace sdtw {
 
 namespace {
@@ -58,6 +60,27 @@ size_t wave_tc_smem(int D)
 
 namespace {
 
+// Thread-block clusters: the strips of one problem that share a cluster hand their
+// boundary rows over through distributed shared memory. cluster_map gives the
+// generic address of the same shared variable in CTA `rank` of the cluster; the
+// slot loads and stores (generic, volatile) work on it unchanged.
+__device__ __forceinline__ unsigned cluster_rank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+template <typename T>
+__device__ __forceinline__ T* cluster_map(T* p, unsigned rank) {
+    unsigned long long a;
+    asm volatile("mapa.u64 %0, %1, %2;" : "=l"(a) : "l"(p), "r"(rank));
+    return reinterpret_cast<T*>(a);
+}
+// Every non-exited thread of the cluster arrives; the writes before the barrier
+// are visible to the reads after it in every CTA of the cluster.
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // 4-byte asynchronous global -> shared copy (completion: cp.async.wait_group).
 __device__ __forceinline__ void cp_async4(float* dst, const float* src)
 {
@@ -68,7 +91,7 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src)
 // rows only); 1, the state of every row; 2, the state of the row blocks
 // [q.vh_rb0, q.vh_rb0 + q.vh_nb) only (one band: the checkpointed forward keeps its
 // last band, a band's recompute its own).
-template <int STORE>
+template <int STORE, bool CL>
 __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     fwd_tc_kernel(const WaveParams q, const unsigned char* __restrict__ ximg, const unsigned char* __restrict__ yimg,
                   const float* __restrict__ xnorm, const float* __restrict__ ynorm)
@@ -83,14 +106,27 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
     __shared__ int s_last;
     __shared__ uint64_t s_a, s_fin, s_bfull[kRB], s_bempty[kRB], s_tfull[kRT], s_tfree[kRT];
     __shared__ uint32_t s_tmem;
+    __shared__ Slot s_xring[CL ? kRing : 1];  // boundary row from the previous CTA of the cluster
+    __shared__ int s_xcons;                   // columns of this CTA's boundary row the next CTA consumed
+    const int C = CL ? q.C : 1;
+    const unsigned crank = C > 1 ? cluster_rank() : 0u;
 
-    if (threadIdx.x == 0) s_tk = atomicAdd(q.ticket_f, 1);
+    if (threadIdx.x == 0 && crank == 0) s_tk = atomicAdd(q.ticket_f, 1);
     if (threadIdx.x < W) cons[threadIdx.x] = 0;
+    if (threadIdx.x == 0) s_xcons = 0;
     for (int k = threadIdx.x; k < W * kRing; k += blockDim.x) ring[k].tag = 0u;
+    if (CL)
+        for (int k = threadIdx.x; k < kRing; k += blockDim.x) s_xring[k].tag = 0u;
     __syncthreads();
+    if (C > 1) cluster_barrier();  // every CTA of the cluster initialised; rank 0's ticket visible
 
-    const int tk = s_tk;
-    const int p = tk % q.P, strip = q.strip0 + tk / q.P;
+    const int tk = C > 1 ? *cluster_map(reinterpret_cast<volatile int*>(&s_tk), 0u) : s_tk;
+    const int o = C > 1 ? (tk / q.P) * C + (int)crank : tk / q.P;  // strip in processing order
+    if (o >= q.S) {  // a CTA of the cluster past the last strip: no rows, and no peer writes to it
+        if (C > 1) cluster_barrier();  // the cluster's final barrier
+        return;
+    }
+    const int p = tk % q.P, strip = q.strip0 + o;
     const int N = q.N, M = q.M, T = skew_T(M);
     const int KB = (q.D + kTcKFeat - 1) / kTcKFeat;
     const int Npad = simg_pad(N), Mpad = simg_pad(M);
@@ -187,9 +223,11 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
         const int rb = strip * W + warp, r0 = rb * 32, i = r0 + lane;
         active = r0 < N;
         const bool has_top = active && r0 > 0;
-        const bool top_global = has_top && warp == 0;
+        const bool top_x = has_top && warp == 0 && crank > 0;  // from the previous CTA of the cluster
+        const bool top_global = has_top && warp == 0 && !top_x;
         const bool has_bot = active && (r0 + 32 < N);
-        const bool bot_global = has_bot && warp == W - 1;
+        const bool bot_x = has_bot && warp == W - 1 && (int)crank < C - 1;  // to the next CTA of the cluster
+        const bool bot_global = has_bot && warp == W - 1 && !bot_x;
         const bool row0_lane = (i == 0);
         // this problem's own lengths (a padded batch): it aligns rows < Nb, columns < Mb
         const int Nb = q.lens_n ? min(max(q.lens_n[p], 1), N) : N;
@@ -213,11 +251,13 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
             const bool store_rows = STORE == 1 || (STORE == 2 && rb >= q.vh_rb0 && rb < q.vh_rb0 + q.vh_nb);
             float2* vhp = store_rows ? q.VH + band_index(q, p, rb, lane, T) : nullptr;
             Slot* ring_out = ring + warp * kRing;
-            const Slot* ring_in = ring + (warp - 1) * kRing;
+            const Slot* ring_in = top_x ? s_xring : ring + (warp - 1) * kRing;
             Slot* edge_out = q.edge_f + ((size_t)p * strips_all(q) + strip) * M;
             const Slot* edge_in = q.edge_f + ((size_t)p * strips_all(q) + strip - 1) * M;
-            const bool chan_lane = has_bot && lane == 31 && !(q.skip_publish && strip == 0 && bot_global);
-            Slot* chan_out = bot_global ? edge_out : ring_out;
+            const bool chan_lane =
+                has_bot && lane == 31 && !(q.skip_publish && strip == 0 && (bot_global || bot_x));
+            Slot* chan_out = bot_global ? edge_out : (bot_x ? cluster_map(s_xring, crank + 1) : ring_out);
+            volatile int* bot_cons = bot_x ? reinterpret_cast<volatile int*>(&s_xcons) : cons + warp;
             const int chan_mask = bot_global ? 0x7fffffff : (kRing - 1);
             Slot nxt[1];
             nxt[0].v = 0.f;
@@ -281,7 +321,7 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                 }
                 if (ok && has_bot && !bot_global) {
                     const int need = s0 + kGroup - 31 - kRing;  // ring slots this group overwrites are free
-                    if (need > cons_seen) ok = wait_smem(&cons[warp], need, q, cons_seen);
+                    if (need > cons_seen) ok = wait_smem(bot_cons, need, q, cons_seen);
                 }
                 if (!ok) break;
 
@@ -318,7 +358,11 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
                     v_prev = v;
                 }
 
-                if (has_top && !top_global && lane == 0) cons[warp - 1] = min(s0 + kGroup, M);
+                if (has_top && !top_global && lane == 0) {
+                    const int used = min(s0 + kGroup, M);
+                    if (top_x) *cluster_map(reinterpret_cast<volatile int*>(&s_xcons), crank - 1) = used;
+                    else cons[warp - 1] = used;
+                }
             }
             asm volatile("cp.async.wait_all;" ::: "memory");  // none in flight past an early exit
         }
@@ -365,6 +409,56 @@ __global__ void __launch_bounds__((kDpWarps + 1) * 32, 1)
         fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
+    if (C > 1) cluster_barrier();  // no CTA leaves while a peer may still write its shared memory
+}
+
+}  // namespace
+
+namespace {
+
+// Cluster size (1, 2 or 4) for a fused forward launch of kern, q.C being the
+// caller's limit: clusters only when the strips are the whole problem (no band
+// launch) and every cluster of the launch can be resident at once (a launch of
+// several waves keeps every SM).
+int tc_cluster(const WaveParams& q, const void* kern, int threads, size_t smem)
+{
+    if (q.C < 2 || q.S < 2 || q.strip0 != 0 || (q.S_all != 0 && q.S_all != q.S)) return 1;
+    struct Entry { const void* kern; int C, threads; size_t smem; int clusters; };
+    static Entry cache[32];
+    static int used = 0;
+    static std::mutex mu;
+    for (int C = q.C >= 4 ? 4 : 2; C >= 2; C >>= 1) {
+        if (C > q.S) continue;
+        const long long grid = (long long)q.P * ((q.S + C - 1) / C) * C;
+        int clusters = -1;
+        {
+            std::lock_guard<std::mutex> lk(mu);
+            for (int k = 0; k < used; ++k)
+                if (cache[k].kern == kern && cache[k].C == C && cache[k].threads == threads && cache[k].smem == smem)
+                    clusters = cache[k].clusters;
+        }
+        if (clusters < 0) {
+            cudaLaunchConfig_t cfg{};
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = (unsigned)C;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3((unsigned)C);
+            cfg.blockDim = dim3((unsigned)threads);
+            cfg.dynamicSmemBytes = smem;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                clusters = 0;
+            }
+            std::lock_guard<std::mutex> lk(mu);
+            if (used < 32) cache[used++] = Entry{kern, C, threads, smem, clusters};
+        }
+        if ((long long)clusters * C >= grid) return C;
+    }
+    return 1;
 }
 
 }  // namespace
@@ -373,7 +467,6 @@ cudaError_t launch_forward_tc(WaveParams q, const void* ximg, const void* yimg, 
                               const float* ynorm, cudaStream_t st)
 {
     if (q.W != kDpWarps || q.D > kTcKFeat * kMaxTcKBlocks) return cudaErrorInvalidValue;
-    const int grid = q.P * q.S;
     q.smem_fixed = (int)wave_smem_fixed(kDpWarps, false);
     // more than half of the SM's shared memory: one CTA per SM, which the
     // 512-column tensor-memory allocation relies on
@@ -382,15 +475,40 @@ cudaError_t launch_forward_tc(WaveParams q, const void* ximg, const void* yimg, 
     if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess || per_sm <= 0)
         per_sm = 228 * 1024;
     const size_t smem = max(wave_tc_smem(q.D), (size_t)per_sm / 2 + 1024);
-    auto go = [&](auto kern) -> cudaError_t {
+    // A checkpointed forward (STORE 0 or 2) keeps every strip's boundary row in the
+    // global edge buffer for the band recomputes: no clusters there.
+    // kern_cl: the build with the cluster paths; kern: without them (every cluster
+    // branch compiled out), which runs when no cluster is used.
+    auto go = [&](auto kern_cl, auto kern, bool may_cluster) -> cudaError_t {
+        constexpr int threads = (kDpWarps + 1) * 32;
+        const unsigned char* xi = static_cast<const unsigned char*>(ximg);
+        const unsigned char* yi = static_cast<const unsigned char*>(yimg);
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess && may_cluster)
+            e = cudaFuncSetAttribute(kern_cl, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, (kDpWarps + 1) * 32, smem, st>>>(q, static_cast<const unsigned char*>(ximg),
-                                                       static_cast<const unsigned char*>(yimg), xnorm, ynorm);
-        return cudaGetLastError();
+        q.C = may_cluster ? tc_cluster(q, reinterpret_cast<const void*>(kern_cl), threads, smem) : 1;
+        if (q.C <= 1) {
+            kern<<<q.P * q.S, threads, smem, st>>>(q, xi, yi, xnorm, ynorm);
+            return cudaGetLastError();
+        }
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)q.C;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3((unsigned)(q.P * ((q.S + q.C - 1) / q.C) * q.C));
+        cfg.blockDim = dim3((unsigned)threads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern_cl, q, xi, yi, xnorm, ynorm);
     };
-    if (q.VH == nullptr) return go(fwd_tc_kernel<0>);
-    return q.vh_nb > 0 ? go(fwd_tc_kernel<2>) : go(fwd_tc_kernel<1>);
+    if (q.VH == nullptr) return go(fwd_tc_kernel<0, false>, fwd_tc_kernel<0, false>, false);
+    if (q.vh_nb > 0) return go(fwd_tc_kernel<2, false>, fwd_tc_kernel<2, false>, false);
+    return go(fwd_tc_kernel<1, true>, fwd_tc_kernel<1, false>, true);
 }
 
 }  // namespace sdtw

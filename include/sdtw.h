@@ -292,6 +292,15 @@ void sdtw_debug_set_wait(double seconds, int skip_publish);
  * by the calls that follow; set it while no other host thread calls the library. */
 void sdtw_debug_set_options(int warps_fwd, int warps_bwd, int dist_simt, int fused_simt);
 
+/* Testing hook. Caps the CTAs per thread-block cluster of the fused fp32 forward
+ * with tensor-core costs: consecutive strips of a problem in one cluster pass their
+ * boundary rows through each other's shared memory instead of global memory (the
+ * other wavefront kernels always use global memory between strips). 0: the
+ * library's own choice (up to 4, when every cluster of the launch can be resident
+ * at once); 1: no clusters; 2: at most 2. Process-wide, read by the calls that
+ * follow; set it while no other host thread calls the library. */
+void sdtw_debug_set_clusters(int max_cluster);
+
 /* Testing hook. out[i] = 2^x[i] (n device floats each) by the library's own
  * exponential of the double-float path: Cody & Waite reduction x = k + f, k the
  * nearest integer, |f| <= 1/2, then a degree-7 polynomial in f fitted to 2^f,

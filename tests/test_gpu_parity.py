@@ -46,6 +46,20 @@ def warps(fwd, bwd=None):
     return options(warps_fwd=fwd, warps_bwd=bwd)
 
 
+class clusters:
+    """Cap the CTAs per wavefront cluster for the duration of a block (the testing
+    hook sdtw_debug_set_clusters; 1: no clusters)."""
+
+    def __init__(self, c):
+        self.c = c
+
+    def __enter__(self):
+        _lib().sdtw_debug_set_clusters(self.c)
+
+    def __exit__(self, *a):
+        _lib().sdtw_debug_set_clusters(0)
+
+
 def run_cuda(x, y, gamma, mode, grad_loss=None, want_grads=True):
     L = _lib()
     xt = torch.from_numpy(x).cuda()
@@ -203,6 +217,33 @@ def test_extended_wide_backward_strips(mname, mode, W):
     x, y = synth.iid_normal_pair(2, 410, 150, 6, 108)
     with warps(W):
         check_against_oracle(x, y, 0.3, mode, grad_loss=[0.5, -1.25], what=f"{mname} W={W}")
+
+
+# In the fused fp32 forward with tensor-core costs, consecutive 128-row strips of a
+# problem that share a thread-block cluster pass their boundary rows through each
+# other's shared memory; the others through global memory. The arithmetic is the
+# same either way: clusters of 4, of 2 and none give identical bits, and match the
+# oracle. Strip counts 5, 3, 2 and 4 (N = 520, 300, 200, 512): the last cluster of
+# a problem can be ragged (CTAs past the last strip); N = 129 has a partial strip.
+@pytest.mark.parametrize("B,N,M,D", [(3, 300, 257, 3), (3, 520, 130, 3), (3, 129, 100, 2), (3, 200, 64, 3),
+                                     (32, 512, 512, 64)])
+def test_cluster_handoff_is_bit_identical(B, N, M, D):
+    x, y = synth.iid_normal_pair(B, N, M, D, 91, repeat=N * 1000 + M)
+    w = mean_weights(B)
+    mname, mode, W = "fused", 1, 0
+    outs = {}
+    for c in (1, 2, 4):
+        with clusters(c):
+            outs[c] = run_cuda(x, y, 0.9, mode, grad_loss=w)
+    for c in (2, 4):
+        for k in outs[1]:
+            np.testing.assert_array_equal(outs[c][k], outs[1][k], err_msg=f"{mname} clusters<={c} {k}")
+    idx = np.arange(min(B, 3))
+    ol, ogx, ogy = oracle.batch(x[idx], y[idx], 0.9, grad_loss=np.asarray(w, np.float64)[idx])
+    what = f"{N}x{M}x{D} W={W} {mname}"
+    assert_close(outs[4]["loss"][idx], ol, LOSS_RTOL, 0.0, f"{what} loss")
+    assert_close(outs[4]["gx"][idx], ogx, GRAD_RTOL, GRAD_ATOL, f"{what} grad_x")
+    assert_close(outs[4]["gy"][idx], ogy, GRAD_RTOL, GRAD_ATOL, f"{what} grad_y")
 
 
 def test_fused_equals_unfused():
