@@ -37,6 +37,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 // Workspace layout. The status word sits at offset 0 for every op.
 struct Layout {
     size_t status, ctrl_f, ctrl_f_bytes, ctrl_b, ctrl_b_bytes;
+    size_t ctrl_band, ctrl_band_stride;  // checkpointed mode: each band launch's own counters
     size_t colsum, rowsum, rowbuf, losses, edge_f, edge_b, vh, e, dsk, gparts, gnorm, bimg, bimg2, total;
     size_t ximg, yimg, xnorm, ynorm;  // tensor-core cost operands (tc_cost, or xtc: digit images and row info)
     size_t band_slots;                // checkpointed mode: skewed slots of one band of every problem
@@ -50,11 +51,11 @@ struct Layout {
 // Side streams and cached events (defined below, with their rules).
 cudaStream_t side_stream();
 cudaStream_t grad_stream();
-cudaStream_t grad_stream_cols();
+cudaStream_t chain_stream(int k);
 enum EventSlot {
     kEvBwdFork, kEvBwdJoin, kEvHostFork, kEvHostJoin, kEvNormFork, kEvNormJoin,
     kEvCkptFork, kEvCkptRec0, kEvCkptRec1, kEvCkptFree0, kEvCkptFree1, kEvCkptBwd0, kEvCkptBwd1, kEvCkptJoin,
-    kEvCkptCols, kEvCkptJoinCols,
+    kEvCkptJoinChain,
     kEvSlots
 };
 cudaEvent_t cached_event(EventSlot slot);
@@ -90,6 +91,10 @@ bool make_layout(int op, int B, int N, int M, int D, int mode, Layout* L)
     L->status = o; o = align_up(o + sizeof(int));
     L->ctrl_f = o; L->ctrl_f_bytes = sizeof(int) * (1 + (size_t)P); o = align_up(o + L->ctrl_f_bytes);
     L->ctrl_b = o; L->ctrl_b_bytes = sizeof(int); o = align_up(o + L->ctrl_b_bytes);
+    // per band: the recompute's ticket and done counters, then the band backward's
+    // ticket, all zeroed by one memset before the bands run
+    L->ctrl_band_stride = align_up(sizeof(int) * (2 + (size_t)P));
+    L->ctrl_band = o; if (ckpt) o = align_up(o + L->ctrl_band_stride * SB);
     L->colsum = o; o = align_up(o + sizeof(double) * (size_t)P * NB);
     L->rowsum = o; o = align_up(o + sizeof(double) * (size_t)P);
     L->rowbuf = o; o = align_up(o + sizeof(float2) * (size_t)P * M);
@@ -326,17 +331,22 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
 {
     const int SB = (L.NB + kBandBlocks - 1) / kBandBlocks;
     int* status = at<int>(ws, L.status);
-    cudaStream_t side = side_stream(), gs = grad_stream(), gc = grad_stream_cols();
+    // the band backwards on bs, the recomputes on side (both high priority: they are
+    // the chain), the gradient terms on gs
+    cudaStream_t bs = chain_stream(0), side = chain_stream(1), gs = grad_stream();
     cudaEvent_t ev_fork = cached_event(kEvCkptFork), ev_join = cached_event(kEvCkptJoin);
+    cudaEvent_t ev_join_chain = cached_event(kEvCkptJoinChain);
     cudaEvent_t ev_rec[2] = {cached_event(kEvCkptRec0), cached_event(kEvCkptRec1)};
     cudaEvent_t ev_free[2] = {cached_event(kEvCkptFree0), cached_event(kEvCkptFree1)};
     cudaEvent_t ev_bwd[2] = {cached_event(kEvCkptBwd0), cached_event(kEvCkptBwd1)};
-    cudaEvent_t ev_cols = cached_event(kEvCkptCols), ev_join_cols = cached_event(kEvCkptJoinCols);
-    if (!side || !gs || !gc || !ev_fork || !ev_join || !ev_rec[0] || !ev_rec[1] || !ev_free[0] || !ev_free[1] ||
-        !ev_bwd[0] || !ev_bwd[1] || !ev_cols || !ev_join_cols)
+    if (!bs || !side || !gs || !ev_join_chain || !ev_fork || !ev_join || !ev_rec[0] || !ev_rec[1] || !ev_free[0] || !ev_free[1] ||
+        !ev_bwd[0] || !ev_bwd[1])
         return SDTW_ERR_CUDA;
     WaveParams qb0 = wave_params(pr, L, ws, gamma, true, false, true);
     if (SB > 1) SDTW_CUDA(cudaMemsetAsync(qb0.edge_b, 0, 2 * sizeof(Slot) * (size_t)L.P * SB * L.M, st));
+    // every band launch's counters start at zero, off the chain of band launches
+    SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_band), 0, L.ctrl_band_stride * SB, st));
+    auto band_ctrl = [&](int k) { return reinterpret_cast<int*>(at<char>(ws, L.ctrl_band) + L.ctrl_band_stride * k); };
     GradParams g{};
     g.pr = pr;
     g.P = L.P; g.M = L.M; g.D = L.D;
@@ -356,9 +366,9 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
     // stream, which includes the forward: it left the last band's state in buffer
     // (SB - 1) & 1, so that band needs no recompute.
     SDTW_CUDA(cudaEventRecord(ev_fork, st));
+    SDTW_CUDA(cudaStreamWaitEvent(bs, ev_fork, 0));
     SDTW_CUDA(cudaStreamWaitEvent(side, ev_fork, 0));
     SDTW_CUDA(cudaStreamWaitEvent(gs, ev_fork, 0));
-    SDTW_CUDA(cudaStreamWaitEvent(gc, ev_fork, 0));
     SDTW_CUDA(cudaEventRecord(ev_rec[(SB - 1) & 1], st));
     // band k's forward state, recomputed from the kept boundary row above it, into buffer k % 2
     auto recompute = [&](int k, cudaStream_t s) -> sdtw_status {
@@ -369,14 +379,15 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
         qf.vh_rb0 = rb0; qf.vh_nb = nb; qf.no_loss = 1;
         qf.VH = vh_buf[k & 1];
         qf.lens_n = lens_n; qf.lens_m = lens_m;
-        SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_f), 0, L.ctrl_f_bytes, s));
+        qf.ticket_f = band_ctrl(k);
+        qf.done = band_ctrl(k) + 1;
         SDTW_CUDA(launch_forward_tc(qf, at<float>(ws, L.ximg), at<float>(ws, L.yimg), at<float>(ws, L.xnorm),
                                     at<float>(ws, L.ynorm), s));
         return SDTW_OK;
     };
-    // Per band, from the last up: its backward on the caller's stream, its gradient
-    // terms on the gradient stream (overlapping the next band's backward), and the
-    // next band's recompute on the side stream. Buffer k % 2 holds band k's state
+    // Per band, from the last up: its backward on bs, its gradient terms on the
+    // gradient stream (overlapping the next band's backward), and the next band's
+    // recompute on the side stream. Buffer k % 2 holds band k's state
     // and E: the recompute of band k - 1 waits for band k + 1's backward (its state
     // buffer), band k's backward for band k + 2's gradient terms (its E buffer).
     sdtw_status s = SDTW_OK;
@@ -391,35 +402,23 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
             SDTW_CUDA(cudaEventRecord(ev_rec[(k - 1) & 1], side));
         }
         // the band's backward wavefront, once its state is there and its E buffer free
-        SDTW_CUDA(cudaStreamWaitEvent(st, ev_rec[k & 1], 0));
-        if (k + 2 < SB) SDTW_CUDA(cudaStreamWaitEvent(st, ev_free[k & 1], 0));
+        SDTW_CUDA(cudaStreamWaitEvent(bs, ev_rec[k & 1], 0));
+        if (k + 2 < SB) SDTW_CUDA(cudaStreamWaitEvent(bs, ev_free[k & 1], 0));
         WaveParams qb = wave_params(pr, L, ws, gamma, true, false, true);
         qb.W = kBandBlocks; qb.S = 1; qb.strip0 = k; qb.S_all = SB;
         qb.vh_rb0 = rb0; qb.vh_nb = nb;
         qb.VH = vh_buf[k & 1];
         qb.E = e_buf[k & 1];
         qb.lens_n = lens_n; qb.lens_m = lens_m;
-        SDTW_CUDA(cudaMemsetAsync(at<char>(ws, L.ctrl_b), 0, L.ctrl_b_bytes, st));
-        SDTW_CUDA(launch_backward(qb, st));
-        SDTW_CUDA(cudaEventRecord(ev_bwd[k & 1], st));
-        // the band's gradient terms, E of the band being a problem of nrows x M: the
-        // grad_x rows on one gradient stream, the grad_y terms (accumulated over the
-        // bands, in band order) on the other. The band's [X | 1] image depends on x
-        // only: it is built before waiting for the backward. The E buffer is free
-        // once both have read it.
+        qb.ticket_b = band_ctrl(k) + 1 + L.P;
+        SDTW_CUDA(launch_backward(qb, bs));
+        SDTW_CUDA(cudaEventRecord(ev_bwd[k & 1], bs));
+        // the band's gradient terms: E of the band is a problem of nrows x M. The band's
+        // [X | 1] image depends on x only: it is built before waiting for the backward.
         g.E = e_buf[k & 1];
         g.pr.xs[0] = pr.xs[0] + (size_t)row0 * L.D;
         g.N = nrows;
-        if (grad_y) {
-            SDTW_CUDA(launch_bimg(g, nullptr, img_cols, gc));
-            SDTW_CUDA(cudaStreamWaitEvent(gc, ev_bwd[k & 1], 0));
-            GradParams gy = g;
-            gy.out = grad_y;
-            gy.out_stride = (long long)L.M * L.D;
-            gy.accumulate = k < SB - 1;
-            SDTW_CUDA(launch_grad_tc(gy, true, img_cols, status, gc));
-            SDTW_CUDA(cudaEventRecord(ev_cols, gc));
-        }
+        if (grad_y) SDTW_CUDA(launch_bimg(g, nullptr, img_cols, gs));
         SDTW_CUDA(cudaStreamWaitEvent(gs, ev_bwd[k & 1], 0));
         if (grad_x) {
             g.out = grad_x + (size_t)row0 * L.D;
@@ -427,15 +426,20 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
             g.accumulate = 0;
             SDTW_CUDA(launch_grad_tc(g, false, img_rows, status, gs));
         }
-        if (grad_y) SDTW_CUDA(cudaStreamWaitEvent(gs, ev_cols, 0));
+        if (grad_y) {
+            g.out = grad_y;
+            g.out_stride = (long long)L.M * L.D;
+            g.accumulate = k < SB - 1;
+            SDTW_CUDA(launch_grad_tc(g, true, img_cols, status, gs));
+        }
         SDTW_CUDA(cudaEventRecord(ev_free[k & 1], gs));
     }
     // the helper streams' work stays ordered before anything later on the caller's
     // stream, also after an error
     cudaEventRecord(ev_join, gs);
     cudaStreamWaitEvent(st, ev_join, 0);
-    cudaEventRecord(ev_join_cols, gc);
-    cudaStreamWaitEvent(st, ev_join_cols, 0);
+    cudaEventRecord(ev_join_chain, bs);
+    cudaStreamWaitEvent(st, ev_join_chain, 0);
     if (s != SDTW_OK) {
         cudaEventRecord(ev_fork, side);
         cudaStreamWaitEvent(st, ev_fork, 0);
@@ -473,12 +477,11 @@ GradParams grad_params(const Problems& all, int set, int B, const Layout& L, voi
 
 // Helper streams per device for work that can overlap the caller's stream (created
 // once, non-blocking; ordered against the caller's stream by events): slot 0 the
-// side stream, slots 1 and 2 the checkpointed backward's gradient streams (grad_x
-// terms, grad_y terms).
+// side stream, slot 1 the checkpointed backward's gradient stream.
 cudaStream_t helper_stream(int slot)
 {
     static std::mutex mu;
-    static cudaStream_t streams[3][64] = {};
+    static cudaStream_t streams[2][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
@@ -488,7 +491,26 @@ cudaStream_t helper_stream(int slot)
 }
 cudaStream_t side_stream() { return helper_stream(0); }
 cudaStream_t grad_stream() { return helper_stream(1); }
-cudaStream_t grad_stream_cols() { return helper_stream(2); }
+
+// High-priority helper streams per device for the checkpointed backward's chain of
+// band wavefronts (k = 0: the band backwards, 1: the band recomputes): when SMs
+// free up, the block scheduler starts their CTAs before those of the gradient
+// contractions queued beside them.
+cudaStream_t chain_stream(int k)
+{
+    static std::mutex mu;
+    static cudaStream_t streams[2][64] = {};
+    int dev = 0;
+    if (k < 0 || k > 1 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    cudaStream_t& s = streams[k][dev];
+    if (!s) {
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) greatest = 0;
+        if (cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, greatest) != cudaSuccess) s = nullptr;
+    }
+    return s;
+}
 
 // Events that order side-stream work against the caller's stream. Each call site
 // has its own slots, created once per host thread and device and reused: a slot
