@@ -72,7 +72,7 @@ typedef enum { SDTW_UNFUSED = 0, SDTW_FUSED = 1 } sdtw_mode;
  * to two bands of every problem (12 bytes per cell of a band); the bands'
  * backward wavefronts run one after another, so the backward's time grows with
  * N/128 (measured at B=32, N=M=512, D=64: workspace 142 -> 78 MiB, forward +
- * backward with gradients 0.32 -> 0.48 ms). SoftDTW-CUDA-Torch paper,
+ * backward with gradients 0.32 -> 0.47 ms). SoftDTW-CUDA-Torch paper,
  * abstract, contribution (3): fused memory O(B(N+M)) rather than O(BNM). */
 #define SDTW_CHECKPOINT 4
 
