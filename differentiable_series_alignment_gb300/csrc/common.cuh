@@ -39,13 +39,19 @@ struct Problems {
     long long xstride[3];
     long long ystride[3];
     int B;
+    // Selects rather than xs[s]: indexing the kernel-parameter arrays by a run-time
+    // value would make every thread copy them to local memory first.
     __host__ __device__ __forceinline__ const float* x(int p) const {
-        int s = p / B, b = p - s * B;
-        return xs[s] + (long long)b * xstride[s];
+        const int s = p / B, b = p - s * B;
+        const float* base = s == 0 ? xs[0] : (s == 1 ? xs[1] : xs[2]);
+        const long long st = s == 0 ? xstride[0] : (s == 1 ? xstride[1] : xstride[2]);
+        return base + (long long)b * st;
     }
     __host__ __device__ __forceinline__ const float* y(int p) const {
-        int s = p / B, b = p - s * B;
-        return ys[s] + (long long)b * ystride[s];
+        const int s = p / B, b = p - s * B;
+        const float* base = s == 0 ? ys[0] : (s == 1 ? ys[1] : ys[2]);
+        const long long st = s == 0 ? ystride[0] : (s == 1 ? ystride[1] : ystride[2]);
+        return base + (long long)b * st;
     }
 };
 

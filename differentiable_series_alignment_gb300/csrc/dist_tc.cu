@@ -52,7 +52,8 @@ constexpr int kStg = 63 * 32;                  // per-warp skew staging (floats)
 // grid (Lpad/32, P, 2): z = 0 writes the x image, z = 1 the y image. block 256.
 // Rows past the sequence end are zero (image and norm). Each thread loads its
 // values in batches of 8, all issued before their shared stores.
-__global__ void __launch_bounds__(256) simg_kernel(Problems pr, int N, int M, int D, int KB,
+// Eight CTAs of 256 threads per SM (32 registers a thread): a batch's images are one wave.
+__global__ void __launch_bounds__(256, 8) simg_kernel(Problems pr, int N, int M, int D, int KB,
                                                    unsigned char* __restrict__ ximg, unsigned char* __restrict__ yimg,
                                                    float* __restrict__ xnorm, float* __restrict__ ynorm)
 {
