@@ -75,8 +75,9 @@ __device__ __forceinline__ T* cluster_map(T* p, unsigned rank) {
     asm volatile("mapa.u64 %0, %1, %2;" : "=l"(a) : "l"(p), "r"(rank));
     return reinterpret_cast<T*>(a);
 }
-// Every non-exited thread of the cluster arrives; the writes before the barrier
-// are visible to the reads after it in every CTA of the cluster.
+// Barrier of every thread of the cluster (each calls it twice per kernel: after
+// the set-up and before leaving, on every path): the writes before it are visible
+// to the reads after it in every CTA of the cluster.
 __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
