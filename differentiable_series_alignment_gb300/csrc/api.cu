@@ -23,8 +23,8 @@ constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 unsigned long long g_wait_ns = kDefaultWaitNs;
 int g_skip_publish = 0;
 
-// Kernel choices forced by sdtw_debug_set_options and sdtw_debug_set_clusters (testing only; zeros: the
-// library's own choices).
+// Kernel choices forced by sdtw_debug_set_options and sdtw_debug_set_clusters
+// (testing only; zeros: the library's own choices).
 struct DebugOptions {
     int warps_fwd, warps_bwd;   // warps per wavefront CTA (> 0: forced)
     int dist_simt, fused_simt;  // difference-form cost kernels (unfused / fused, both precisions)
@@ -339,8 +339,8 @@ sdtw_status run_backward_ckpt(const Problems& pr, const Layout& L, void* ws, flo
     cudaEvent_t ev_rec[2] = {cached_event(kEvCkptRec0), cached_event(kEvCkptRec1)};
     cudaEvent_t ev_free[2] = {cached_event(kEvCkptFree0), cached_event(kEvCkptFree1)};
     cudaEvent_t ev_bwd[2] = {cached_event(kEvCkptBwd0), cached_event(kEvCkptBwd1)};
-    if (!bs || !side || !gs || !ev_join_chain || !ev_fork || !ev_join || !ev_rec[0] || !ev_rec[1] || !ev_free[0] || !ev_free[1] ||
-        !ev_bwd[0] || !ev_bwd[1])
+    if (!bs || !side || !gs || !ev_join_chain || !ev_fork || !ev_join || !ev_rec[0] || !ev_rec[1] || !ev_free[0] ||
+        !ev_free[1] || !ev_bwd[0] || !ev_bwd[1])
         return SDTW_ERR_CUDA;
     WaveParams qb0 = wave_params(pr, L, ws, gamma, true, false, true);
     if (SB > 1) SDTW_CUDA(cudaMemsetAsync(qb0.edge_b, 0, 2 * sizeof(Slot) * (size_t)L.P * SB * L.M, st));
