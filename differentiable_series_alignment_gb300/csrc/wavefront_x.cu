@@ -743,15 +743,19 @@ __global__ void __launch_bounds__(kXFusedThreads, 1)
         const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
         bool ok = true;
         int used_seen = 0;
+        // a tile's y row info is loaded one tile ahead (rows padded to Mpad >= 32 nT)
+        const float4* yvp = yinfo + (size_t)p * Mpad + lane;
+        float4 yv_next = yvp[0];
         for (int c = 0; c < nT; ++c) {
             const int t = c % kXRT;
+            const float4 yv = yv_next;
+            if (c + 1 < nT) yv_next = yvp[32 * (c + 1)];
             // ring slot of tile c held tile c - R: DP warp qd must be done with it
             if (rows && c - R + 1 > used_seen) ok = wait_smem_sleep(&s_used[qd], c - R + 1, q, used_seen, 128);
             if (!ok) break;
             tc::wait_ok_sleep(ok, tc::smem_u32(&s_tfull[t]), (uint32_t)((c / kXRT) & 1), status);
             if (!__all_sync(kFull, ok)) break;
             tc::fence_after_sync();
-            const float4 yv = yinfo[(size_t)p * Mpad + 32 * c + lane];
             const uint32_t tt0 = tq + (uint32_t)(t * kXSlotCols);
 #pragma unroll 1
             for (int q8 = 0; q8 < 4; ++q8) {   // 8 columns at a time: NS x 8 level sums in registers
