@@ -314,6 +314,23 @@ __global__ void __launch_bounds__(kThreadsTotal, 1)
                 mbar_arrive(smem_u32(&s_a_full[kt % ts]));
             }
         }
+        // The epilogue's first batch of loads (own rows, and the output when it
+        // accumulates) does not depend on the products: it goes out before the wait.
+        constexpr int kR = 16;  // rows per batch of epilogue loads
+        const float* own = COLS ? g.pr.y(p) : g.pr.x(p);
+        float* out = g.out + (long long)(p % g.omod) * g.out_stride;
+        float ov0[kR], pv0[kR];
+        {
+            const int c = tid & 63, r0 = tid >> 6;
+            if (c < D) {
+#pragma unroll
+                for (int k = 0; k < kR; ++k) {
+                    const size_t o = (size_t)min(m0 + r0 + 4 * k, rows - 1) * D + c;
+                    ov0[k] = own[o];
+                    pv0[k] = g.accumulate ? out[o] : 0.f;
+                }
+            }
+        }
         // every MMA has completed (and every copy has landed) once s_acc fires
         {
             bool fin = true;
@@ -343,8 +360,6 @@ __global__ void __launch_bounds__(kThreadsTotal, 1)
             ssum[r_own] = s;
         }
         const float w = g.coef * 2.f * (g.grad_loss ? g.grad_loss[p % g.wmod] : 1.f);
-        const float* own = COLS ? g.pr.y(p) : g.pr.x(p);
-        float* out = g.out + (long long)(p % g.omod) * g.out_stride;
         for (int g0 = 0; g0 < D; g0 += 64) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -367,15 +382,22 @@ __global__ void __launch_bounds__(kThreadsTotal, 1)
             // group is issued before the first store
             const int c = tid & 63, r0 = tid >> 6;
             if (ok && c < D - g0) {
-                constexpr int kR = 16;  // rows per batch of loads
                 for (int rb0 = 0; rb0 < kBM; rb0 += 4 * kR) {
                     float ov[kR], pv[kR];
+                    if (g0 == 0 && rb0 == 0) {  // loaded before the wait
 #pragma unroll
-                    for (int k = 0; k < kR; ++k) {
-                        const int row = m0 + rb0 + r0 + 4 * k;
-                        const size_t o = (size_t)min(row, rows - 1) * D + g0 + c;
-                        ov[k] = own[o];
-                        pv[k] = g.accumulate ? out[o] : 0.f;
+                        for (int k = 0; k < kR; ++k) {
+                            ov[k] = ov0[k];
+                            pv[k] = pv0[k];
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kR; ++k) {
+                            const int row = m0 + rb0 + r0 + 4 * k;
+                            const size_t o = (size_t)min(row, rows - 1) * D + g0 + c;
+                            ov[k] = own[o];
+                            pv[k] = g.accumulate ? out[o] : 0.f;
+                        }
                     }
 #pragma unroll
                     for (int k = 0; k < kR; ++k) {
